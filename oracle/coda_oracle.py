@@ -1,0 +1,328 @@
+"""Plain fp64 CPU oracle for CODA-style GEMM-epilogue chains.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports, links or calls this
+module: only the tests, ``__graft_entry__.smoke()`` and the CPU legs of ``bench.py``
+(``cpu_baseline`` and ``--impl reference``) do.  It imports nothing from the CUDA
+package either; the two sides share only the seeded input generators in ``coda_synth``.
+
+Sources, by page title and section (the pages print no formulas, only op names; every
+function below is the textbook definition of the op the pages name):
+
+* [Ecosistema] "CODA: Nuevo kernel GPU reduce costos de entrenamiento IA"
+  (ecosistemastartup.com), section "¿Qué es GEMM-epilogue y por qué importa…?":
+  GEMM is C = alpha*A*B + beta*C; the epilogue applies scaling, bias, activation,
+  residual addition, precision cast and clamp before the store.
+* [KuCoin] "CODA: new research optimizes Transformer training with GEMM-epilogue
+  programming" (kucoin.com news flash):
+  - "CODA: «El epílogo» esconde un tesoro": in GEMM -> residual -> RMSNorm -> GEMM the
+    per-row RMS scale r commutes with the second matmul, so it is applied at the end of
+    the second GEMM; the first GEMM only emits partial RMS (partial sums of squares),
+    which a very light reduce kernel combines.  The same rewrite covers SwiGLU, RoPE and
+    the backward pass.
+  - "Cinco «bloques» y un «lenguaje LEGO»": elementwise/pairwise transforms (residual
+    add, activation, RoPE), vector load (RMSNorm gain broadcast), matrix-block load/store
+    (saved activations), block reduction (local RMS), state change (online max/sum-exp).
+  - "hoja de referencia": coverage is RMSNorm, residual add, SwiGLU, RoPE, cross-entropy
+    and their gradients, LLaMA-style blocks, everything but attention and embeddings.
+
+Everything is computed in float64 with numpy; ``numpy.matmul`` is the only library
+primitive (a GEMM step).  There is no blocking, fusion or reordering beyond what each
+definition states.  Two forms are written out for the chains: the plain unfused chain
+(normalise, then GEMM; textbook chain rule for backward) and the reparameterised forms
+the kernels implement (deferred r, folded gain, fused backward combine); the tests pin
+both against each other, against closed forms and against finite differences.
+
+Readings of points the pages leave open (the plainest reading consistent with them):
+  1. RMSNorm: r_i = (mean_j h_ij^2 + eps)^(-1/2), eps inside the square root.
+  2. "Partial RMS" = partial sums of squares over column tiles (RMS is not additive).
+  3. The RMSNorm gain g sits on the next GEMM's K dimension, so the reparameterised form
+     folds it into that weight: W'[n, k] = W[n, k] * g[k].
+  4. SwiGLU: a = silu(G) * U, gate = rows [0, F) and up = rows [F, 2F) of W_gu.
+  5. RoPE pairs adjacent columns (2p, 2p+1) of each head; theta_p = base^(-2p/head_dim);
+     position = row index mod sequence length; only the first ``n_rot_cols`` columns
+     (the Q and K heads) are rotated.
+  6. FP8 is OCP e4m3 ("fn": no infinities, max 448) with round-to-nearest-even and
+     saturation to +-448; dequantised value = scale * code value.
+Every function here is pinned by a test (closed form, invariant, library special case
+or brute force); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+F64 = np.float64
+
+
+def _f64(x):
+    return np.asarray(x, dtype=F64)
+
+
+# ---------------------------------------------------------------------------------------
+# GEMM  [Ecosistema, "¿Qué es GEMM-epilogue…?"]: C = alpha*A*B + beta*C
+# ---------------------------------------------------------------------------------------
+def gemm_general(A, B, alpha=1.0, C=None, beta=0.0):
+    """C_out = alpha * (A @ B) + beta * C, the GEMM as the page writes it."""
+    out = F64(alpha) * (_f64(A) @ _f64(B))
+    if C is not None and beta != 0.0:
+        out = out + F64(beta) * _f64(C)
+    return out
+
+
+def linear(X, W):
+    """Y = X W^T for a weight stored [out, in] (nn.Linear layout): B = W^T above."""
+    return gemm_general(X, _f64(W).T)
+
+
+# ---------------------------------------------------------------------------------------
+# RMSNorm and its partial form  [KuCoin, "El epílogo esconde un tesoro"]
+# ---------------------------------------------------------------------------------------
+def rms_scale(h, eps):
+    """Per-row RMSNorm scale r_i = 1 / sqrt(mean_j h_ij^2 + eps)."""
+    h = _f64(h)
+    return 1.0 / np.sqrt(np.mean(h * h, axis=1) + F64(eps))
+
+
+def rmsnorm(h, g, eps):
+    """y_ij = r_i * h_ij * g_j (RMSNorm with gain g)."""
+    h = _f64(h)
+    return rms_scale(h, eps)[:, None] * h * _f64(g)[None, :]
+
+
+def partial_sumsq(h, bn):
+    """Per-tile partial sums of squares, layout [ceil(d/bn), M]: P[t, i] = sum_{j in tile t} h_ij^2."""
+    h = _f64(h)
+    M, d = h.shape
+    nparts = (d + bn - 1) // bn
+    P = np.zeros((nparts, M), dtype=F64)
+    for t in range(nparts):
+        blk = h[:, t * bn:(t + 1) * bn]
+        P[t] = np.sum(blk * blk, axis=1)
+    return P
+
+
+def rms_scale_from_partials(P, d, eps):
+    """The light reduce: r_i = 1 / sqrt(sum_t P[t, i] / d + eps)."""
+    return 1.0 / np.sqrt(np.sum(_f64(P), axis=0) / F64(d) + F64(eps))
+
+
+def fold_gain(W, g):
+    """W'[n, k] = W[n, k] * g[k]: the gain moved onto the next GEMM's weight (reading 3)."""
+    return _f64(W) * _f64(g)[None, :]
+
+
+# ---------------------------------------------------------------------------------------
+# SwiGLU  [KuCoin, "Cinco bloques…": activation as an elementwise transform]
+# ---------------------------------------------------------------------------------------
+def sigmoid(x):
+    x = _f64(x)
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def silu(x):
+    """silu(x) = x / (1 + e^-x)."""
+    x = _f64(x)
+    return x * sigmoid(x)
+
+
+def silu_grad(x):
+    """d silu / dx = sigma(x) * (1 + x * (1 - sigma(x)))."""
+    x = _f64(x)
+    s = sigmoid(x)
+    return s * (1.0 + x * (1.0 - s))
+
+
+def swiglu(G, U):
+    """a = silu(G) * U."""
+    return silu(G) * _f64(U)
+
+
+# ---------------------------------------------------------------------------------------
+# RoPE  [KuCoin, "Cinco bloques…": RoPE as a pairwise transform]
+# ---------------------------------------------------------------------------------------
+def rope_inv_freq(head_dim, base):
+    """theta_p = base^(-2p / head_dim), p = 0 .. head_dim/2 - 1."""
+    p = np.arange(head_dim // 2, dtype=F64)
+    return F64(base) ** (-2.0 * p / F64(head_dim))
+
+
+def rope_rotate(Z, positions, n_rot_cols, head_dim, base):
+    """Rotate each adjacent pair (2p, 2p+1) of every head in columns [0, n_rot_cols) by
+    phi = position * theta_p; columns from n_rot_cols on are returned unchanged."""
+    Z = _f64(Z)
+    out = Z.copy()
+    phi = _f64(positions)[:, None] * rope_inv_freq(head_dim, base)[None, :]
+    c, s = np.cos(phi), np.sin(phi)
+    for h0 in range(0, n_rot_cols, head_dim):
+        x0 = Z[:, h0:h0 + head_dim:2]
+        x1 = Z[:, h0 + 1:h0 + head_dim:2]
+        out[:, h0:h0 + head_dim:2] = x0 * c - x1 * s
+        out[:, h0 + 1:h0 + head_dim:2] = x0 * s + x1 * c
+    return out
+
+
+# ---------------------------------------------------------------------------------------
+# FP8 e4m3 (reading 6)  [KuCoin, "El impuesto a la pereza": FP8 raises the non-GEMM share]
+# ---------------------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def e4m3_round(x):
+    """Nearest e4m3 value, ties to even mantissa, saturating to +-448 (float64 result).
+
+    Normal numbers 2^e * (1 + m/8) with e in [-6, 8]; subnormals m * 2^-9, m in 1..7.
+    The spacing at magnitude a is 2^(e-3) with e = max(floor(log2 a), -6)."""
+    x = _f64(x)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    _, ex = np.frexp(a)                       # a = f * 2^ex, f in [0.5, 1): floor(log2 a) = ex - 1
+    e = np.maximum(ex.astype(F64) - 1.0, -6.0)
+    q = np.exp2(e - 3.0)
+    v = np.rint(a / q) * q                    # numpy rint rounds half to even
+    v = np.minimum(v, E4M3_MAX)
+    return np.copysign(v, x)
+
+
+def e4m3_decode(codes):
+    """Value of each e4m3 byte: sign | 4-bit exponent (bias 7) | 3-bit mantissa; 0x7f/0xff NaN."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sgn = np.where(c & 0x80, -1.0, 1.0)
+    E = (c >> 3) & 0xF
+    m = (c & 0x7).astype(F64)
+    val = np.where(E == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(E.astype(F64) - 7.0))
+    val = np.where((c & 0x7F) == 0x7F, np.nan, val)
+    return sgn * val
+
+
+def e4m3_encode(x):
+    """e4m3 byte for each value (after e4m3_round): inverse of e4m3_decode on finite codes."""
+    v = e4m3_round(x)
+    sign = (v < 0) | ((v == 0) & np.signbit(v))
+    a = np.abs(v)
+    _, ex = np.frexp(a)
+    e = ex.astype(np.int64) - 1
+    normal = a >= 2.0 ** -6
+    E = np.where(normal, e + 7, 0)
+    M = np.where(normal, np.rint(a / np.exp2(e.astype(F64)) * 8.0 - 8.0), np.rint(a / 2.0 ** -9))
+    code = (np.where(sign, 0x80, 0) | (E.astype(np.int64) << 3) | M.astype(np.int64)).astype(np.uint8)
+    return code
+
+
+# ---------------------------------------------------------------------------------------
+# Chains.  Plain (unfused) forms first, then the reparameterised forms the kernels use.
+# ---------------------------------------------------------------------------------------
+def tiny_chain(X, R, W1, W2, g, eps):
+    """Tiny GEMM -> residual -> RMSNorm -> GEMM, weights in [in, out] form:
+    out = rmsnorm(X W1 + R, g) W2."""
+    h = gemm_general(X, W1) + _f64(R)
+    return dict(h=h, r=rms_scale(h, eps), out=gemm_general(rmsnorm(h, g, eps), W2))
+
+
+def block_forward(O, R, W_o, g, W_gu, W_d, eps):
+    """LLaMA-style block tail, plain unfused chain (weights [out, in]):
+    h = O W_o^T + R;  y = rmsnorm(h, g);  Z = y W_gu^T = [G | U];  a = silu(G) U;
+    Y = a W_d^T + h."""
+    h = linear(O, W_o) + _f64(R)
+    r = rms_scale(h, eps)
+    y = r[:, None] * h * _f64(g)[None, :]
+    Z = linear(y, W_gu)
+    F = Z.shape[1] // 2
+    G, U = Z[:, :F], Z[:, F:]
+    a = swiglu(G, U)
+    Y = linear(a, W_d) + h
+    return dict(h=h, r=r, y=y, Z=Z, G=G, U=U, a=a, Y=Y)
+
+
+def block_forward_deferred(O, R, W_o, g, W_gu, W_d, eps, bn):
+    """The reparameterised chain [KuCoin, "El epílogo esconde un tesoro"]: GEMM1 emits
+    partial sums of squares, a light reduce turns them into r, and r is applied per row
+    after the second GEMM, whose weight carries the folded gain."""
+    h = linear(O, W_o) + _f64(R)
+    P = partial_sumsq(h, bn)
+    r = rms_scale_from_partials(P, h.shape[1], eps)
+    Z = r[:, None] * linear(h, fold_gain(W_gu, g))
+    F = Z.shape[1] // 2
+    G, U = Z[:, :F], Z[:, F:]
+    a = swiglu(G, U)
+    Y = linear(a, W_d) + h
+    return dict(h=h, P=P, r=r, Z=Z, G=G, U=U, a=a, Y=Y)
+
+
+def block_backward(fwd, O, W_o, g, W_gu, W_d, dY):
+    """Plain chain rule through the unfused ops of ``block_forward`` (RMSNorm backward in
+    its textbook form dh = r (g*dy) - (r^3/d) h sum_j g_j dy_j h_j)."""
+    h, r, y, G, U, a = (fwd[k] for k in ("h", "r", "y", "G", "U", "a"))
+    dY = _f64(dY)
+    W_d, W_gu, W_o, g = _f64(W_d), _f64(W_gu), _f64(W_o), _f64(g)
+    d = h.shape[1]
+    dW_d = dY.T @ a
+    da = dY @ W_d
+    dG = da * U * silu_grad(G)
+    dU = da * silu(G)
+    dZ = np.hstack([dG, dU])
+    dW_gu = dZ.T @ y
+    dy = dZ @ W_gu
+    dg = np.sum(dy * r[:, None] * h, axis=0)
+    proj = np.sum(g[None, :] * dy * h, axis=1)
+    dh = r[:, None] * (g[None, :] * dy) - (r ** 3 / d)[:, None] * h * proj[:, None] + dY
+    dO = dh @ W_o
+    dW_o = dh.T @ _f64(O)
+    return dict(dW_d=dW_d, da=da, dZ=dZ, dW_gu=dW_gu, dg=dg, dh=dh, dR=dh, dO=dO, dW_o=dW_o)
+
+
+def block_backward_fused(fwd, O, W_o, g, W_gu, W_d, dY):
+    """The fused backward forms the kernels compute (each GEMM + its epilogue):
+      e   = r * [dG | dU]          (SwiGLU-backward epilogue on dA = dY W_d, row scale r)
+      s_i = sum_k e_ik Z_ik        (row dot partial), c_i = r_i s_i / d (light reduce)
+      t   = e W_gu;  dh = g*t - c*h + dY;  dg_j = sum_i h_ij t_ij   (RMSNorm-bwd combine)
+      dW_gu[n, k] = g_k (e^T h)[n, k];  dW_d = dY^T a;  dO = dh W_o;  dW_o = dh^T O."""
+    h, r, Z, G, U, a = (fwd[k] for k in ("h", "r", "Z", "G", "U", "a"))
+    dY = _f64(dY)
+    W_d, W_gu, W_o, g = _f64(W_d), _f64(W_gu), _f64(W_o), _f64(g)
+    d = h.shape[1]
+    dA = dY @ W_d
+    e = r[:, None] * np.hstack([dA * U * silu_grad(G), dA * silu(G)])
+    s = np.sum(e * Z, axis=1)
+    c = r * s / d
+    t = e @ W_gu
+    dh = g[None, :] * t - c[:, None] * h + dY
+    dg = np.sum(h * t, axis=0)
+    dW_gu = g[None, :] * (e.T @ h)
+    dW_d = dY.T @ a
+    dO = dh @ W_o
+    dW_o = dh.T @ _f64(O)
+    return dict(e=e, s=s, c=c, t=t, dh=dh, dR=dh, dg=dg, dW_gu=dW_gu, dW_d=dW_d, dO=dO, dW_o=dW_o)
+
+
+def qkv_rope(h, g, W_qkv, eps, seq_len, n_rot_cols, head_dim, base):
+    """Input RMSNorm -> QKV projection -> RoPE on the Q and K columns (plain chain)."""
+    y = rmsnorm(h, g, eps)
+    Z = linear(y, W_qkv)
+    pos = np.arange(Z.shape[0]) % seq_len
+    return dict(r=rms_scale(h, eps), Z=Z, out=rope_rotate(Z, pos, n_rot_cols, head_dim, base))
+
+
+def mlp_fp8(h, Xq_val, s_x, Wq_val, s_w, Wdq_val, s_wd, s_a, eps, bn):
+    """FP8 MLP with per-tensor scales.  Operands are e4m3 code values (already decoded to
+    float64) with fp32 scales: x = s_x Xq, W = s_w Wq (the effective gate/up weight),
+    W_d = s_wd Wdq.  r comes from the bf16 activation h.
+      Z = r * (x W'^T);  a = silu(G) U;  amax = max |a|;  a_q = e4m3(a / s_a);
+      Y = (s_a a_q) W_d^T + h;  P = partial sums of squares of Y."""
+    r = rms_scale(h, eps)
+    Z = r[:, None] * linear(F64(s_x) * _f64(Xq_val), F64(s_w) * _f64(Wq_val))
+    F = Z.shape[1] // 2
+    a = swiglu(Z[:, :F], Z[:, F:])
+    aq_val = e4m3_round(a / F64(s_a))
+    Y = linear(F64(s_a) * aq_val, F64(s_wd) * _f64(Wdq_val)) + _f64(h)
+    return dict(r=r, Z=Z, a=a, amax=np.max(np.abs(a)), aq_val=aq_val, Y=Y, P=partial_sumsq(Y, bn))
+
+
+# ---------------------------------------------------------------------------------------
+# Error metric used by every parity test
+# ---------------------------------------------------------------------------------------
+def max_rel_err(got, ref):
+    """max_i |got_i - ref_i| / max(|ref_i|, rms(ref)): relative error with an RMS floor so
+    that entries near zero do not dominate."""
+    got, ref = _f64(got), _f64(ref)
+    floor = np.sqrt(np.mean(ref * ref)) if ref.size else 0.0
+    den = np.maximum(np.abs(ref), floor)
+    den = np.where(den == 0, 1.0, den)
+    return float(np.max(np.abs(got - ref) / den)) if ref.size else 0.0

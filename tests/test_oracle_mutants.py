@@ -1,0 +1,100 @@
+"""Plants plausible mistakes in the oracle (on the CPU, by monkeypatching a copy of one of
+its functions) and checks that at least one pin fails for each.  This shows the pins are
+sharp enough to catch a dropped term, a wrong sign or index, or a transposed operand."""
+import numpy as np
+import pytest
+
+import oracle as O
+import oracle.coda_oracle as OC
+import tests.test_oracle_pins as pins
+
+
+def _plant(monkeypatch, name, fn):
+    # the pins use the package namespace; internal calls use the module's
+    monkeypatch.setattr(O, name, fn)
+    monkeypatch.setattr(OC, name, fn)
+
+
+def _fails(fn, *args):
+    try:
+        fn(*args)
+    except (AssertionError, ValueError, IndexError):
+        return True
+    return False
+
+
+def test_dropped_eps_is_caught(monkeypatch):
+    _plant(monkeypatch, "rms_scale", lambda h, eps: 1.0 / np.sqrt(np.mean(np.asarray(h, float) ** 2, axis=1)))
+    assert _fails(pins.test_rms_eps_only_row) or _fails(pins.test_rms_constant_row)
+
+
+def test_transposed_weight_is_caught(monkeypatch):
+    _plant(monkeypatch, "linear", lambda X, W: np.asarray(X, float) @ np.asarray(W, float))
+    assert _fails(pins.test_linear_uses_out_in_layout)
+
+
+def test_wrong_rope_sign_is_caught(monkeypatch):
+    orig = O.rope_rotate
+
+    def bad(Z, positions, n_rot_cols, head_dim, base):
+        return orig(Z, -np.asarray(positions, float), n_rot_cols, head_dim, base)
+
+    _plant(monkeypatch, "rope_rotate", bad)
+    assert _fails(pins.test_rope_closed_form_first_pair)
+
+
+def test_rope_wrong_pairing_is_caught(monkeypatch):
+    def half_split(Z, positions, n_rot_cols, head_dim, base):   # (p, p + hd/2) pairing
+        Z = np.asarray(Z, float)
+        out = Z.copy()
+        phi = np.asarray(positions, float)[:, None] * O.rope_inv_freq(head_dim, base)[None, :]
+        c, s = np.cos(phi), np.sin(phi)
+        for h0 in range(0, n_rot_cols, head_dim):
+            x0 = Z[:, h0:h0 + head_dim // 2]
+            x1 = Z[:, h0 + head_dim // 2:h0 + head_dim]
+            out[:, h0:h0 + head_dim // 2] = x0 * c - x1 * s
+            out[:, h0 + head_dim // 2:h0 + head_dim] = x0 * s + x1 * c
+        return out
+
+    _plant(monkeypatch, "rope_rotate", half_split)
+    assert _fails(pins.test_rope_closed_form_first_pair)
+
+
+def test_dropped_residual_grad_is_caught(monkeypatch):
+    orig = O.block_backward
+
+    def bad(fwd, Oa, W_o, g, W_gu, W_d, dY):
+        out = orig(fwd, Oa, W_o, g, W_gu, W_d, dY)
+        dh = out["dh"] - np.asarray(dY, float)
+        out.update(dh=dh, dR=dh, dO=dh @ np.asarray(W_o, float), dW_o=dh.T @ np.asarray(Oa, float))
+        return out
+
+    _plant(monkeypatch, "block_backward", bad)
+    assert _fails(pins.test_backward_matches_finite_differences)
+
+
+def test_swapped_gate_up_is_caught(monkeypatch):
+    _plant(monkeypatch, "swiglu", lambda G, U: O.silu(U) * np.asarray(G, float))
+    assert _fails(pins.test_swiglu_gate_and_up_roles)
+
+
+def test_e4m3_ties_away_is_caught(monkeypatch):
+    def away(x):
+        x = np.asarray(x, float)
+        a = np.minimum(np.abs(x), 448.0)
+        _, ex = np.frexp(a)
+        q = np.exp2(np.maximum(ex - 1.0, -6.0) - 3.0)
+        return np.copysign(np.minimum(np.floor(a / q + 0.5) * q, 448.0), x)
+
+    _plant(monkeypatch, "e4m3_round", away)
+    assert _fails(pins.test_e4m3_ties_to_even_and_saturation)
+
+
+def test_partial_tile_off_by_one_is_caught(monkeypatch):
+    def bad(h, bn):
+        h = np.asarray(h, float)
+        n = (h.shape[1] + bn - 1) // bn
+        return np.stack([np.sum(h[:, t * bn:(t + 1) * bn - 1] ** 2, axis=1) for t in range(n)])
+
+    _plant(monkeypatch, "partial_sumsq", bad)
+    assert _fails(pins.test_partials_sum_to_row_sumsq, 64)
