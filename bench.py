@@ -1,0 +1,470 @@
+#!/usr/bin/env python
+"""Benchmark: the fused GEMM-epilogue chain of a LLaMA-3-1B-shaped block on one GB300.
+
+Workload (one step, all on one GPU, bf16 in / fp32 accumulate / bf16 out):
+    M = 16384 tokens, hidden H = 2048, FFN F = 8192, synthetic seeded inputs.
+    fold    W_gu' = W_gu diag(g)                      (gain moved onto the next weight)
+    G1      h = O W_o^T + R, partial sums of squares  (GEMM + residual + partial RMS epilogue)
+    reduce  r = 1 / sqrt(sum partials / H + eps)      (the light row reduce)
+    G2      a = silu(G) U, [G | U] = r (h W_gu'^T)    (deferred-r GEMM + SwiGLU epilogue)
+    G3      Y = a W_d^T + h                            (GEMM + residual epilogue)
+"CODA: new research optimizes Transformer training with GEMM-epilogue programming"
+(kucoin.com news flash), sections "El epílogo esconde un tesoro" and "Resultados del
+experimento" (LLaMA-style 16K-token batches).
+
+Prints ONE JSON line (rank 0).  `value` is tokens/s over all ranks (each rank runs its own
+16384-token replica: the forward rows are independent, so there is no collective in the
+data path).  `--impl reference` times the fp64 CPU oracle instead (the slow reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused GEMM-epilogue chain TFLOP/s & tokens/s at 16K tokens; % of roofline"
+M_TOK, HID, FFN, EPS = 16384, 2048, 8192, 1e-6
+WORKLOAD = "LLaMA-3-1B-shaped block forward: attn-out GEMM+residual+partial RMS -> row reduce -> " \
+           "deferred-r gate/up GEMM+SwiGLU -> down GEMM+residual; M=16384 tokens, H=2048, F=8192, bf16"
+FLOP = {"G1": 2 * M_TOK * HID * HID, "G2": 2 * M_TOK * 2 * FFN * HID, "G3": 2 * M_TOK * HID * FFN}
+CHAIN_FLOP = sum(FLOP.values())
+MB = 1e6
+# compulsory bytes: each operand read once, each output written once (bf16 = 2 B, fp32 = 4 B)
+BYTES = {
+    "fold": 2 * (2 * FFN * HID) * 2 + 4 * HID,
+    "G1": 2 * (M_TOK * HID * 3 + HID * HID) + 4 * M_TOK * (HID // 256),
+    "reduce": 4 * (M_TOK * (HID // 256) + M_TOK),
+    "G2": 2 * (M_TOK * HID + 2 * FFN * HID + M_TOK * FFN) + 4 * M_TOK,
+    "G3": 2 * (M_TOK * FFN + HID * FFN + 2 * M_TOK * HID),
+}
+CHAIN_BYTES = sum(BYTES.values())
+LAUNCHES_PER_STEP = 5     # fold, G1, reduce, G2, G3
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SOURCES = ["gemm_epilogue_transformer_tcgen05_gb300/csrc/coda_gemm.cuh",
+                  "gemm_epilogue_transformer_tcgen05_gb300/csrc/coda_ptx.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["coda", "reference"], default="coda")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-compare", action="store_true", help="skip the torch eager comparator and error check")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------------- helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), source="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None when the
+    summary is missing or the kernel sources changed after the counters were taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        ent = d["kernels"][kernel]
+        if ent.get("source_hash") != kernel_hash():
+            return None
+        return float(ent["bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) while the timed region runs."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_id):
+        self.dev_id = dev_id
+        self.rows = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev_id}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def mark(self, begin):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sel = [r for t, r in self.rows if self.t0 and self.t1 and self.t0 - 0.05 <= t <= self.t1 + 0.05]
+        if len(sel) < 3:
+            sel = [r for _, r in self.rows]
+        sm, smax, reasons = [], [], set()
+        for r in sel:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def nvsmi_id(torch):
+    try:
+        p = torch.cuda.get_device_properties(torch.cuda.current_device())
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0]
+        return vis if vis.isdigit() else "0"
+
+
+# ------------------------------------------------------------------- distributed
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus and world > 1:
+        print(f"warning: WORLD_SIZE={world} but --gpus={args.gpus}", file=sys.stderr)
+    return world, rank, local
+
+
+# --------------------------------------------------------------- the CPU oracle arm
+def oracle_sample_rate(target_s):
+    """Times the fp64 oracle's plain block forward on a bounded sample of token rows of
+    the same workload; tokens/s = rows / seconds (forward rows are independent)."""
+    import numpy as np
+
+    import coda_synth as S
+    import oracle as O
+    inp = S.block_inputs(M_TOK, HID, FFN, seed=0)
+    x = {k: inp[k].to(__import__("torch").float64).numpy() for k in ("O", "R", "W_o", "W_gu", "W_d", "g")}
+    rows = 64
+    t0 = time.perf_counter()
+    O.block_forward(x["O"][:rows], x["R"][:rows], x["W_o"], x["g"], x["W_gu"], x["W_d"], EPS)
+    dt = time.perf_counter() - t0
+    rows = int(min(M_TOK, max(rows, rows * target_s / max(dt, 1e-3))))
+    rows = max(64, (rows // 64) * 64)
+    t0 = time.perf_counter()
+    O.block_forward(x["O"][:rows], x["R"][:rows], x["W_o"], x["g"], x["W_gu"], x["W_d"], EPS)
+    dt = time.perf_counter() - t0
+    del np
+    return rows / dt, rows, dt
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    steps = max(1, args.steps)
+    per_step_target = max(1.0, min(args.cpu_seconds, 120.0 / (steps + args.warmup)))
+    rate, rows, dt = oracle_sample_rate(per_step_target)
+    times = []
+    import coda_synth as S
+    import oracle as O
+    import torch
+    inp = S.block_inputs(M_TOK, HID, FFN, seed=0)
+    x = {k: inp[k].to(torch.float64).numpy() for k in ("O", "R", "W_o", "W_gu", "W_d", "g")}
+    for i in range(args.warmup + steps):
+        t0 = time.perf_counter()
+        O.block_forward(x["O"][:rows], x["R"][:rows], x["W_o"], x["g"], x["W_gu"], x["W_d"], EPS)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    t = sum(times) / len(times)
+    value = rows / t
+    ms_full = M_TOK / value * 1e3
+    cores = cpu_cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms_full, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens": M_TOK, "hidden": HID, "ffn": FFN,
+                   "sample_rows_per_step": rows},
+        "tflops": CHAIN_FLOP / (ms_full * 1e-3) / 1e12,
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} of {M_TOK} token rows per step (fp64 numpy oracle, plain unfused chain)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- the GPU arm
+def run_coda(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import coda_synth as S
+    from gemm_epilogue_transformer_tcgen05_gb300 import coda as C
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    C.lib()
+    BF = torch.bfloat16
+    M, H, F = M_TOK, HID, FFN
+    inp = S.block_inputs(M, H, F, seed=rank)
+    d = {k: inp[k].to("cuda").contiguous() for k in ("O", "R", "W_o", "W_gu", "W_d", "g")}
+    Wf = torch.empty_like(d["W_gu"])
+    h = torch.empty((M, H), dtype=BF, device="cuda")
+    r = torch.empty((M,), device="cuda")
+    a = torch.empty((M, F), dtype=BF, device="cuda")
+    Y = torch.empty((M, H), dtype=BF, device="cuda")
+    P = torch.empty((H // 256, M), device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        # the chain as its five C-ABI launches (coda_block_forward issues G1, reduce, G2, G3
+        # in exactly this order); events bracket the dominant GEMM
+        C.coda_fold_gain(d["W_gu"], d["g"], Wf, stream=stream)
+        C.coda_gemm_epilogue(d["O"], d["W_o"], [C.OP_ADD_SIDE, C.OP_ROW_SUMSQ_PARTIAL], h, residual=d["R"],
+                             row_partials=P, stream=stream)
+        C.coda_rms_partial_reduce(P, M, H, EPS, r, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        C.coda_gemm_epilogue(h, Wf, [C.OP_ROW_SCALE, C.OP_SWIGLU], a, row_scale=r, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        C.coda_gemm_epilogue(a, d["W_d"], [C.OP_ADD_SIDE], Y, residual=h, stream=stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    st, site = C.coda_get_device_status(stream)
+    if st != C.OK:
+        raise RuntimeError(f"device status {st} (site {site}) during warm-up")
+
+    sampler = ClockSampler(nvsmi_id(torch)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    if sampler:
+        sampler.mark(True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    barrier()
+    if sampler:
+        sampler.mark(False)
+    ms = t_start.elapsed_time(t_end)
+    g2_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    st, site = C.coda_get_device_status(stream)
+    if st != C.OK:
+        raise RuntimeError(f"device status {st} (site {site}) in the timed region")
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if sampler:
+        time.sleep(0.15)
+        sampler.stop()
+    ms_step = ms / args.steps
+    value = world * M / (ms_step * 1e-3)
+
+    # ---- end to end through the public chain call, host buffers (pinned) both ways
+    e2e = None
+    if not args.no_e2e:
+        O_h = inp["O"].pin_memory()
+        R_h = inp["R"].pin_memory()
+        Y_h = torch.empty((M, H), dtype=BF).pin_memory()
+        ws = torch.empty((C.coda_workspace_size(C.WS_BLOCK_FWD, M, H, F) // 4,), device="cuda")
+        O_d, R_d = torch.empty_like(d["O"]), torch.empty_like(d["R"])
+
+        def e2e_step():
+            O_d.copy_(O_h, non_blocking=True)
+            R_d.copy_(R_h, non_blocking=True)
+            C.coda_fold_gain(d["W_gu"], d["g"], Wf, stream=stream)
+            C.coda_block_forward(O_d, R_d, d["W_o"], Wf, d["W_d"], EPS, h, r, a, Y, ws, stream=stream)
+            Y_h.copy_(Y, non_blocking=True)
+
+        n_e2e = max(3, min(args.steps, 50))
+        for _ in range(3):
+            e2e_step()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        ems = e0.elapsed_time(e1) / n_e2e
+        if dist is not None:
+            t = torch.tensor([ems], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * M / (ems * 1e-3), "unit": "tokens/s", "ms_per_step": ems, "steps": n_e2e,
+               "h2d_bytes_per_step": O_h.numel() * 2 + R_h.numel() * 2, "d2h_bytes_per_step": Y_h.numel() * 2}
+
+    # ---- comparator: the same chain unfused in torch eager (cuBLAS GEMMs), and errors
+    compare = None
+    if not args.no_compare and rank == 0:
+        compare = unfused_compare(torch, d, Y, r, inp, stream, args)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    pk = peaks()
+    g2_tflops = FLOP["G2"] / (g2_ms * 1e-3) / 1e12
+    traffic = recorded_traffic("G2")
+    chain_roof_ms = max(CHAIN_FLOP / (pk["bf16_sus"] * 1e12), CHAIN_BYTES / (pk["hbm"] * 1e9)) * 1e3
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens": M, "hidden": H, "ffn": F,
+                   "l2": f"inputs larger than L2: {(CHAIN_BYTES) / MB:.0f} MB compulsory traffic per step "
+                         f"vs {L2_BYTES / MB:.0f} MB L2; no flush",
+                   "parallelism": f"replicas x{world} (no data-path collective)"},
+        "tflops": CHAIN_FLOP / (ms_step * 1e-3) / 1e12,
+        "chain_roofline": {"ms": chain_roof_ms, "frac": chain_roof_ms / ms_step,
+                           "peak_tflops": pk["bf16_sus"], "peak_kind": f"bf16 sustained ({pk['source']})"},
+        "roofline": {"kernel": "G2 gate/up GEMM + deferred r + SwiGLU (gemm_epilogue_kernel, EPI_SWIGLU)",
+                     "bound": "tensor", "achieved": g2_tflops, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
+                     "frac": g2_tflops / pk["bf16_sus"], "traffic": traffic,
+                     "peak_kind": f"bf16 sustained, of {pk['source']}",
+                     "frac_of_burst": g2_tflops / pk["bf16"], "ms_per_launch": g2_ms,
+                     "algorithmic_bytes": BYTES["G2"], "flop_per_launch": FLOP["G2"]},
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "clocks": sampler.summary() if sampler else None,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if compare:
+        line["compare"] = compare
+    if not args.no_cpu_baseline:
+        rate, rows, dt = oracle_sample_rate(args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": f"{rows} of {M} token rows, {dt:.1f} s (fp64 numpy oracle, plain "
+                                          f"unfused chain; rows are independent)"}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    del np
+
+
+def unfused_compare(torch, d, Y, r, inp, stream, args):
+    """torch eager bf16 chain of the same block (separate GEMM / add / RMSNorm / SwiGLU
+    kernels, cuBLAS GEMMs): its time, and the max relative error of both chains against the
+    fp64 oracle on 256 sampled rows."""
+    import numpy as np
+
+    import oracle as O
+    F_ = torch.nn.functional
+    O_, R, W_o, W_gu, W_d, g = (d[k] for k in ("O", "R", "W_o", "W_gu", "W_d", "g"))
+    gb = g.to(torch.bfloat16)
+
+    def chain():
+        hh = F_.linear(O_, W_o) + R
+        var = hh.float().pow(2).mean(-1, keepdim=True)
+        y = (hh.float() * torch.rsqrt(var + EPS)).to(torch.bfloat16) * gb
+        z = F_.linear(y, W_gu)
+        G, U = z[:, :FFN], z[:, FFN:]
+        aa = F_.silu(G) * U
+        return F_.linear(aa, W_d) + hh
+
+    for _ in range(3):
+        Yt = chain()
+    torch.cuda.synchronize()
+    n = max(3, min(args.steps, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        Yt = chain()
+    e1.record()
+    torch.cuda.synchronize()
+    t_ms = e0.elapsed_time(e1) / n
+    rows = np.sort(np.random.default_rng(0).choice(M_TOK, size=256, replace=False))
+    x = {k: inp[k].to(torch.float64).numpy() for k in ("O", "R", "W_o", "W_gu", "W_d", "g")}
+    ref = O.block_forward(x["O"][rows], x["R"][rows], x["W_o"], x["g"], x["W_gu"], x["W_d"], EPS)
+    rows_t = torch.from_numpy(rows).cuda()
+    err_f = O.max_rel_err(Y.index_select(0, rows_t).double().cpu().numpy(), ref["Y"])
+    err_u = O.max_rel_err(Yt.index_select(0, rows_t).double().cpu().numpy(), ref["Y"])
+    return {"unfused_torch_eager_ms_per_step": t_ms, "unfused_tokens_per_s": M_TOK / (t_ms * 1e-3),
+            "max_rel_err_fused_vs_oracle": err_f, "max_rel_err_unfused_torch_vs_oracle": err_u,
+            "error_rows": 256}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_init(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    run_coda(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,317 @@
+"""ctypes binding of libcoda.so (include/coda.h): argument marshalling only.
+
+Every function here turns torch tensors (device memory owned by the caller) into the
+plain pointers, sizes and layouts of the C ABI and calls the library; every step of the
+computation runs in the library's CUDA kernels.  There is no fallback: if the library is
+not built or cannot be loaded, loading raises CodaLibraryError, and a non-zero status
+from a call raises CodaError.
+
+A 2-D tensor's layout is read from its strides: stride (ld, 1) is CODA_ROW_MAJOR with
+leading dimension ld; stride (1, ld) is CODA_COL_MAJOR (a transposed view, e.g. x.t()).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, Structure, c_char_p, c_double, c_float, c_int32, c_int64, c_size_t, c_uint32, c_void_p
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "lib", "libcoda.so")
+
+# ----------------------------------------------------------------------- constants
+OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_UNSUPPORTED_PROGRAM, ERR_LAUNCH, ERR_DEVICE_TIMEOUT, ERR_NO_DEVICE = (
+    0, -1, -2, -3, -4, -5, -6, -7, -8)
+F32, BF16, E4M3 = 0, 1, 2
+ROW_MAJOR, COL_MAJOR = 0, 1
+OP_TENSOR_SCALE, OP_ROW_SCALE, OP_COL_SCALE, OP_ADD_SIDE, OP_SWIGLU, OP_ROPE = 1, 2, 3, 4, 5, 6
+OP_SWIGLU_BWD, OP_RMSBWD_COMBINE, OP_ROW_SUMSQ_PARTIAL, OP_ROW_DOT_PARTIAL = 7, 8, 9, 10
+OP_COL_DOT_PARTIAL, OP_AMAX, OP_STORE_AUX = 11, 12, 13
+REDUCE_RSQRT_MEAN, REDUCE_SCALE_SUM = 0, 1
+WS_BLOCK_FWD, WS_BLOCK_BWD = 0, 1
+MAX_OPS = 8
+
+EXPORTED = [
+    "coda_gemm_epilogue", "coda_rms_partial_reduce", "coda_row_rms", "coda_col_reduce", "coda_fold_gain",
+    "coda_rope_table", "coda_block_forward", "coda_block_backward", "coda_qkv_rope", "coda_mlp_fp8",
+    "coda_workspace_size", "coda_get_device_status", "coda_set_watchdog_ms", "coda_inject_dropped_stage",
+    "coda_device_sm_count", "coda_status_string", "coda_version",
+]
+
+
+class CodaLibraryError(RuntimeError):
+    pass
+
+
+class CodaError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({status_string(status)})")
+
+
+# ---------------------------------------------------------------------- structures
+class CodaTensor(Structure):
+    _fields_ = [("ptr", c_void_p), ("dtype", c_int32), ("layout", c_int32), ("rows", c_int64), ("cols", c_int64),
+                ("ld", c_int64)]
+
+
+class CodaProgram(Structure):
+    _fields_ = [("n_ops", c_int32), ("ops", c_int32 * MAX_OPS)]
+
+
+class CodaSide(Structure):
+    _fields_ = [("residual", POINTER(CodaTensor)), ("row_scale", c_void_p), ("row_coef", c_void_p),
+                ("col_scale", c_void_p), ("aux_in", POINTER(CodaTensor)), ("aux_in2", POINTER(CodaTensor)),
+                ("rope_cos", c_void_p), ("rope_sin", c_void_p), ("rope_seq_len", c_int32),
+                ("rope_head_dim", c_int32), ("rope_ncols", c_int32), ("tensor_scale", c_float),
+                ("out_scale", c_float)]
+
+
+class CodaAux(Structure):
+    _fields_ = [("row_partials", c_void_p), ("row_partials_ld", c_int64), ("col_partials", c_void_p),
+                ("col_partials_ld", c_int64), ("store_aux", POINTER(CodaTensor)), ("amax", c_void_p)]
+
+
+class CodaBlockFwd(Structure):
+    _fields_ = [("M", c_int64), ("H", c_int64), ("F", c_int64), ("eps", c_float), ("O", c_void_p), ("R", c_void_p),
+                ("W_o", c_void_p), ("W_gu", c_void_p), ("W_d", c_void_p), ("h", c_void_p), ("r", c_void_p),
+                ("a", c_void_p), ("Y", c_void_p), ("Z", c_void_p), ("Y_partials", c_void_p),
+                ("workspace", c_void_p)]
+
+
+class CodaBlockBwd(Structure):
+    _fields_ = [("M", c_int64), ("H", c_int64), ("F", c_int64), ("O", c_void_p), ("W_o", c_void_p),
+                ("W_gu", c_void_p), ("W_d", c_void_p), ("g", c_void_p), ("h", c_void_p), ("r", c_void_p),
+                ("Z", c_void_p), ("a", c_void_p), ("dY", c_void_p), ("e", c_void_p), ("dh", c_void_p),
+                ("dO", c_void_p), ("dW_o", c_void_p), ("dW_gu", c_void_p), ("dW_d", c_void_p), ("dg", c_void_p),
+                ("c", c_void_p), ("workspace", c_void_p)]
+
+
+class CodaQkvRope(Structure):
+    _fields_ = [("M", c_int64), ("H", c_int64), ("N", c_int64), ("seq_len", c_int32), ("head_dim", c_int32),
+                ("rope_ncols", c_int32), ("eps", c_float), ("h", c_void_p), ("W_qkv", c_void_p),
+                ("rope_cos", c_void_p), ("rope_sin", c_void_p), ("r", c_void_p), ("out", c_void_p)]
+
+
+class CodaMlpFp8(Structure):
+    _fields_ = [("M", c_int64), ("H", c_int64), ("F", c_int64), ("eps", c_float), ("s_x", c_float),
+                ("s_w", c_float), ("s_wd", c_float), ("s_a", c_float), ("h", c_void_p), ("X_q", c_void_p),
+                ("W_q", c_void_p), ("W_dq", c_void_p), ("r", c_void_p), ("a_q", c_void_p), ("amax", c_void_p),
+                ("Y", c_void_p), ("Y_partials", c_void_p)]
+
+
+# --------------------------------------------------------------------- the library
+_lib = None
+
+
+def lib():
+    """The loaded libcoda.so (raises CodaLibraryError if it is not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise CodaLibraryError(f"libcoda.so is not built ({LIB_PATH}); run __graft_entry__.build() or "
+                               "python -m gemm_epilogue_transformer_tcgen05_gb300.build")
+    L = ctypes.CDLL(LIB_PATH)
+    P = POINTER
+    sigs = {
+        "coda_gemm_epilogue": [P(CodaTensor), P(CodaTensor), P(CodaProgram), P(CodaSide), P(CodaTensor), P(CodaAux),
+                               c_void_p],
+        "coda_rms_partial_reduce": [c_void_p, c_int64, c_int32, c_int64, c_int64, c_float, c_int32, c_void_p, c_void_p,
+                                    c_void_p],
+        "coda_row_rms": [P(CodaTensor), c_float, c_void_p, c_void_p],
+        "coda_col_reduce": [c_void_p, c_int64, c_int64, c_int64, c_void_p, c_void_p],
+        "coda_fold_gain": [P(CodaTensor), c_void_p, P(CodaTensor), c_void_p],
+        "coda_rope_table": [c_int32, c_int32, c_double, c_void_p, c_void_p, c_void_p],
+        "coda_block_forward": [P(CodaBlockFwd), c_void_p],
+        "coda_block_backward": [P(CodaBlockBwd), c_void_p],
+        "coda_qkv_rope": [P(CodaQkvRope), c_void_p],
+        "coda_mlp_fp8": [P(CodaMlpFp8), c_void_p],
+        "coda_get_device_status": [c_void_p, P(c_int32)],
+        "coda_set_watchdog_ms": [c_uint32],
+        "coda_inject_dropped_stage": [c_int32],
+        "coda_device_sm_count": [P(c_int32)],
+    }
+    for name, args in sigs.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = c_int32
+    L.coda_workspace_size.argtypes = [c_int32, c_int64, c_int64, c_int64]
+    L.coda_workspace_size.restype = c_size_t
+    L.coda_status_string.argtypes = [c_int32]
+    L.coda_status_string.restype = c_char_p
+    L.coda_version.argtypes = []
+    L.coda_version.restype = c_char_p
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return lib().coda_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return lib().coda_version().decode()
+
+
+def _check(status, where):
+    if status != OK:
+        raise CodaError(int(status), where)
+
+
+def _stream(stream):
+    if stream is None:
+        return c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return c_void_p(stream.cuda_stream)
+    return c_void_p(int(stream))
+
+
+def _ptr(t):
+    return None if t is None else c_void_p(t.data_ptr())
+
+
+_DT = {torch.float32: F32, torch.bfloat16: BF16, torch.float8_e4m3fn: E4M3, torch.uint8: E4M3}
+
+
+def desc(t: torch.Tensor) -> CodaTensor:
+    """coda_tensor of a 2-D tensor (layout from its strides)."""
+    if t.dim() != 2:
+        raise ValueError("coda tensors are 2-D")
+    if t.dtype not in _DT:
+        raise ValueError(f"unsupported dtype {t.dtype}")
+    rows, cols = t.shape
+    s0, s1 = t.stride()
+    if s1 == 1 or cols <= 1:
+        layout, ld = ROW_MAJOR, max(s0, cols, 1)
+    elif s0 == 1 or rows <= 1:
+        layout, ld = COL_MAJOR, max(s1, rows, 1)
+    else:
+        raise ValueError("tensor must be row- or column-major (one unit stride)")
+    return CodaTensor(c_void_p(t.data_ptr()), _DT[t.dtype], layout, rows, cols, ld)
+
+
+def program(*ops) -> CodaProgram:
+    if len(ops) > MAX_OPS:
+        raise ValueError("too many ops")
+    p = CodaProgram()
+    p.n_ops = len(ops)
+    for i, o in enumerate(ops):
+        p.ops[i] = int(o)
+    return p
+
+
+# ------------------------------------------------------------------------ the calls
+def coda_gemm_epilogue(A, W, ops, out, *, residual=None, row_scale=None, row_coef=None, col_scale=None,
+                       aux_in=None, aux_in2=None, rope_cos=None, rope_sin=None, rope_seq_len=0, rope_head_dim=0,
+                       rope_ncols=0, tensor_scale=1.0, out_scale=1.0, row_partials=None, col_partials=None,
+                       store_aux=None, amax=None, stream=None):
+    """out = epilogue(ops, A . W^T); see include/coda.h for the programs."""
+    keep = []
+
+    def tp(t):
+        if t is None:
+            return None
+        d = desc(t)
+        keep.append(d)
+        return ctypes.pointer(d)
+
+    side = CodaSide(tp(residual), _ptr(row_scale), _ptr(row_coef), _ptr(col_scale), tp(aux_in), tp(aux_in2),
+                    _ptr(rope_cos), _ptr(rope_sin), rope_seq_len, rope_head_dim, rope_ncols, tensor_scale, out_scale)
+    aux = CodaAux(_ptr(row_partials), row_partials.stride(0) if row_partials is not None else 0,
+                  _ptr(col_partials), col_partials.stride(0) if col_partials is not None else 0,
+                  tp(store_aux), _ptr(amax))
+    a, w, o = desc(A), desc(W), desc(out)
+    prog = program(*ops)
+    st = lib().coda_gemm_epilogue(ctypes.byref(a), ctypes.byref(w), ctypes.byref(prog), ctypes.byref(side),
+                                  ctypes.byref(o), ctypes.byref(aux), _stream(stream))
+    _check(st, "coda_gemm_epilogue")
+
+
+def coda_rms_partial_reduce(partials, M, d, eps, out, mode=REDUCE_RSQRT_MEAN, rowscale=None, stream=None):
+    nparts, ld = partials.shape[0], partials.stride(0)
+    st = lib().coda_rms_partial_reduce(_ptr(partials), ld, nparts, M, d, eps, mode, _ptr(rowscale), _ptr(out),
+                                       _stream(stream))
+    _check(st, "coda_rms_partial_reduce")
+
+
+def coda_row_rms(X, eps, r_out, stream=None):
+    x = desc(X)
+    _check(lib().coda_row_rms(ctypes.byref(x), eps, _ptr(r_out), _stream(stream)), "coda_row_rms")
+
+
+def coda_col_reduce(parts, out, stream=None):
+    nblocks, N = parts.shape
+    st = lib().coda_col_reduce(_ptr(parts), nblocks, N, parts.stride(0), _ptr(out), _stream(stream))
+    _check(st, "coda_col_reduce")
+
+
+def coda_fold_gain(W, g, W_out, stream=None):
+    w, wo = desc(W), desc(W_out)
+    _check(lib().coda_fold_gain(ctypes.byref(w), _ptr(g), ctypes.byref(wo), _stream(stream)), "coda_fold_gain")
+
+
+def coda_rope_table(seq_len, head_dim, base, cos_out, sin_out, stream=None):
+    st = lib().coda_rope_table(seq_len, head_dim, base, _ptr(cos_out), _ptr(sin_out), _stream(stream))
+    _check(st, "coda_rope_table")
+
+
+def coda_workspace_size(which, M, H, F):
+    return int(lib().coda_workspace_size(which, M, H, F))
+
+
+def coda_block_forward(O, R, W_o, W_gu_folded, W_d, eps, h, r, a, Y, workspace, Z=None, Y_partials=None,
+                       stream=None):
+    M, H = O.shape
+    F = W_d.shape[1]
+    io = CodaBlockFwd(M, H, F, eps, _ptr(O), _ptr(R), _ptr(W_o), _ptr(W_gu_folded), _ptr(W_d), _ptr(h), _ptr(r),
+                      _ptr(a), _ptr(Y), _ptr(Z), _ptr(Y_partials), _ptr(workspace))
+    _check(lib().coda_block_forward(ctypes.byref(io), _stream(stream)), "coda_block_forward")
+
+
+def coda_block_backward(O, W_o, W_gu, W_d, g, h, r, Z, a, dY, e, dh, dO, dW_o, dW_gu, dW_d, dg, c, workspace,
+                        stream=None):
+    M, H = O.shape
+    F = W_d.shape[1]
+    io = CodaBlockBwd(M, H, F, _ptr(O), _ptr(W_o), _ptr(W_gu), _ptr(W_d), _ptr(g), _ptr(h), _ptr(r), _ptr(Z),
+                      _ptr(a), _ptr(dY), _ptr(e), _ptr(dh), _ptr(dO), _ptr(dW_o), _ptr(dW_gu), _ptr(dW_d), _ptr(dg),
+                      _ptr(c), _ptr(workspace))
+    _check(lib().coda_block_backward(ctypes.byref(io), _stream(stream)), "coda_block_backward")
+
+
+def coda_qkv_rope(h, W_qkv, eps, seq_len, head_dim, rope_ncols, rope_cos, rope_sin, r, out, stream=None):
+    M, H = h.shape
+    N = W_qkv.shape[0]
+    io = CodaQkvRope(M, H, N, seq_len, head_dim, rope_ncols, eps, _ptr(h), _ptr(W_qkv), _ptr(rope_cos),
+                     _ptr(rope_sin), _ptr(r), _ptr(out))
+    _check(lib().coda_qkv_rope(ctypes.byref(io), _stream(stream)), "coda_qkv_rope")
+
+
+def coda_mlp_fp8(h, X_q, W_q, W_dq, s_x, s_w, s_wd, s_a, eps, r, a_q, amax, Y, Y_partials, stream=None):
+    M, H = h.shape
+    F = W_dq.shape[1]
+    io = CodaMlpFp8(M, H, F, eps, s_x, s_w, s_wd, s_a, _ptr(h), _ptr(X_q), _ptr(W_q), _ptr(W_dq), _ptr(r),
+                    _ptr(a_q), _ptr(amax), _ptr(Y), _ptr(Y_partials))
+    _check(lib().coda_mlp_fp8(ctypes.byref(io), _stream(stream)), "coda_mlp_fp8")
+
+
+def coda_get_device_status(stream=None):
+    """(status, site): synchronises the stream and reads + clears the device status word."""
+    site = c_int32(0)
+    st = lib().coda_get_device_status(_stream(stream), ctypes.byref(site))
+    return int(st), int(site.value)
+
+
+def coda_set_watchdog_ms(ms):
+    _check(lib().coda_set_watchdog_ms(int(ms)), "coda_set_watchdog_ms")
+
+
+def coda_inject_dropped_stage(enable=True):
+    _check(lib().coda_inject_dropped_stage(1 if enable else 0), "coda_inject_dropped_stage")
+
+
+def coda_device_sm_count():
+    n = c_int32(0)
+    _check(lib().coda_device_sm_count(ctypes.byref(n)), "coda_device_sm_count")
+    return int(n.value)

@@ -1,0 +1,723 @@
+// C ABI of the GEMM-epilogue library: argument checks, epilogue-program matching, TMA
+// descriptor encoding, launches, and the block chains built from those launches.
+// The operations follow "CODA: new research optimizes Transformer training with
+// GEMM-epilogue programming" (kucoin.com news flash), sections "El epílogo esconde un
+// tesoro" (deferred r, partial RMS, backward) and "Cinco bloques y un lenguaje LEGO"
+// (primitive kinds); see include/coda.h for each call's contract.
+#include <cudaTypedefs.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/coda.h"
+#include "coda_internal.h"
+
+using namespace coda;
+
+namespace {
+
+// Device status word read by coda_get_device_status.  One per device (module global);
+// its address is looked up once per device and passed to every kernel.
+__device__ int g_device_status;
+
+struct DevState {
+  bool init;
+  bool ok;
+  int sms;
+  int* status;
+};
+constexpr int kMaxDevices = 64;
+DevState g_dev[kMaxDevices];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+uint32_t g_watchdog_ms = 0;
+int g_inject_once = 0;
+
+int ensure_device(DevState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return CODA_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState& d = g_dev[dev];
+  if (!d.init) {
+    d.init = true;
+    d.ok = false;
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return CODA_ERR_NO_DEVICE;
+    }
+    if (major != 10 || minor != 3) return CODA_ERR_NO_DEVICE;
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        cudaGetLastError();
+        return CODA_ERR_NO_DEVICE;
+      }
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess || addr == nullptr) {
+      cudaGetLastError();
+      return CODA_ERR_NO_DEVICE;
+    }
+    d.status = static_cast<int*>(addr);
+    d.sms = sms;
+    if (g_watchdog_ms == 0) {
+      const char* env = std::getenv("CODA_WATCHDOG_MS");
+      long v = env ? std::strtol(env, nullptr, 10) : 0;
+      g_watchdog_ms = v > 0 ? (uint32_t)v : 2000u;
+    }
+    d.ok = true;
+  }
+  if (!d.ok) return CODA_ERR_NO_DEVICE;
+  *out = &d;
+  return CODA_OK;
+}
+
+int esize(int dt) { return dt == CODA_F32 ? 4 : dt == CODA_BF16 ? 2 : dt == CODA_E4M3 ? 1 : 0; }
+int to_dt(int dt) { return dt == CODA_F32 ? DT_F32 : dt == CODA_BF16 ? DT_BF16 : DT_E4M3; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+const int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+// Checks a tensor's pointer, dtype, alignment and leading dimension.
+// An empty tensor (rows or cols = 0) may have a NULL pointer.
+int check_tensor(const coda_tensor* t, bool allow_col) {
+  if (!t) return CODA_ERR_NULL;
+  if (esize(t->dtype) == 0) return CODA_ERR_DTYPE;
+  if (t->layout != CODA_ROW_MAJOR && !(allow_col && t->layout == CODA_COL_MAJOR)) return CODA_ERR_SHAPE;
+  if (t->rows < 0 || t->cols < 0 || t->rows > kMaxDim || t->cols > kMaxDim) return CODA_ERR_SHAPE;
+  if (t->rows == 0 || t->cols == 0) return CODA_OK;
+  if (!t->ptr) return CODA_ERR_NULL;
+  const int64_t inner = t->layout == CODA_ROW_MAJOR ? t->cols : t->rows;
+  if (t->ld < inner || t->ld < 1) return CODA_ERR_SHAPE;
+  if (!aligned16(t->ptr) || (t->ld * esize(t->dtype)) % 16 != 0) return CODA_ERR_ALIGN;
+  return CODA_OK;
+}
+
+// 2-D tiled tensor map over storage [outer][ld] with `inner` valid elements per row.
+int encode_2d(CUtensorMap* m, int dtype, const void* ptr, int64_t inner, int64_t outer, int64_t ld, uint32_t box_in,
+              uint32_t box_out) {
+  CUtensorMapDataType t = dtype == CODA_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                          : dtype == CODA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const uint32_t row_bytes = box_in * (uint32_t)esize(dtype);
+  CUtensorMapSwizzle sw = row_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                          : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                          : row_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                            : CU_TENSOR_MAP_SWIZZLE_NONE;
+  cuuint64_t dims[2] = {(cuuint64_t)(inner > 0 ? inner : 1), (cuuint64_t)(outer > 0 ? outer : 1)};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * esize(dtype))};
+  cuuint32_t box[2] = {box_in, box_out};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, t, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CODA_OK : CODA_ERR_LAUNCH;
+}
+
+// ------------------------------------------------------------- program matching
+struct Item {
+  int op;
+  bool optional;
+};
+struct ProgramTemplate {
+  int epi;
+  int n;
+  Item items[6];
+};
+const ProgramTemplate kPrograms[] = {
+    {EPI_STORE, 2, {{CODA_OP_TENSOR_SCALE, true}, {CODA_OP_COL_SCALE, true}}},
+    {EPI_RESID, 3, {{CODA_OP_TENSOR_SCALE, true}, {CODA_OP_ADD_SIDE, false}, {CODA_OP_ROW_SUMSQ_PARTIAL, true}}},
+    {EPI_ROWSCALE, 2, {{CODA_OP_TENSOR_SCALE, true}, {CODA_OP_ROW_SCALE, false}}},
+    {EPI_SWIGLU,
+     5,
+     {{CODA_OP_TENSOR_SCALE, true},
+      {CODA_OP_ROW_SCALE, true},
+      {CODA_OP_STORE_AUX, true},
+      {CODA_OP_SWIGLU, false},
+      {CODA_OP_AMAX, true}}},
+    {EPI_ROPE, 3, {{CODA_OP_TENSOR_SCALE, true}, {CODA_OP_ROW_SCALE, true}, {CODA_OP_ROPE, false}}},
+    {EPI_SWIGLU_BWD,
+     3,
+     {{CODA_OP_SWIGLU_BWD, false}, {CODA_OP_ROW_SCALE, true}, {CODA_OP_ROW_DOT_PARTIAL, false}}},
+    {EPI_RMSBWD, 2, {{CODA_OP_RMSBWD_COMBINE, false}, {CODA_OP_COL_DOT_PARTIAL, false}}},
+};
+
+// Returns the compiled program index and the set of ops present (bit op), or -1.
+int match_program(const coda_epilogue_program* prog, uint32_t* present) {
+  const int n = prog ? prog->n_ops : 0;
+  if (n < 0 || n > CODA_MAX_OPS) return -1;
+  for (const ProgramTemplate& t : kPrograms) {
+    int pos = 0;
+    uint32_t seen = 0;
+    bool ok = true;
+    for (int i = 0; i < t.n && ok; ++i) {
+      if (pos < n && prog->ops[pos] == t.items[i].op) {
+        seen |= 1u << t.items[i].op;
+        ++pos;
+      } else if (!t.items[i].optional) {
+        ok = false;
+      }
+    }
+    if (ok && pos == n) {
+      *present = seen;
+      return t.epi;
+    }
+  }
+  return -1;
+}
+
+}  // namespace
+
+namespace coda {
+const VariantEntry* find_variant(const VariantKey& k) {
+  const VariantEntry* tables[3] = {g_variants_fwd, g_variants_bwd, g_variants_lowp};
+  const int counts[3] = {g_num_variants_fwd, g_num_variants_bwd, g_num_variants_lowp};
+  for (int t = 0; t < 3; ++t)
+    for (int i = 0; i < counts[t]; ++i) {
+      const VariantKey& v = tables[t][i].key;
+      if (v.kind == k.kind && v.epi == k.epi && v.a_mn == k.a_mn && v.b_mn == k.b_mn && v.out_dt == k.out_dt &&
+          v.side_dt == k.side_dt && v.aux == k.aux)
+        return &tables[t][i];
+    }
+  return nullptr;
+}
+}  // namespace coda
+
+// =====================================================================================
+extern "C" {
+
+const char* coda_version(void) { return "coda-gb300 sm_103a 1"; }
+
+const char* coda_status_string(int s) {
+  switch (s) {
+    case CODA_OK: return "ok";
+    case CODA_ERR_NULL: return "a required pointer is NULL";
+    case CODA_ERR_SHAPE: return "inconsistent or unsupported sizes";
+    case CODA_ERR_ALIGN: return "base address or leading dimension not 16-byte aligned";
+    case CODA_ERR_DTYPE: return "unsupported dtype combination";
+    case CODA_ERR_UNSUPPORTED_PROGRAM: return "epilogue program has no compiled variant";
+    case CODA_ERR_LAUNCH: return "CUDA launch or TMA descriptor encoding failed";
+    case CODA_ERR_DEVICE_TIMEOUT: return "a kernel wait ran out of time";
+    case CODA_ERR_NO_DEVICE: return "no sm_103 device current (or driver entry point missing)";
+    default: return "unknown status";
+  }
+}
+
+int coda_set_watchdog_ms(uint32_t ms) {
+  if (ms == 0) return CODA_ERR_SHAPE;
+  g_watchdog_ms = ms;
+  return CODA_OK;
+}
+
+int coda_inject_dropped_stage(int32_t enable) {
+  g_inject_once = enable ? 1 : 0;
+  return CODA_OK;
+}
+
+int coda_device_sm_count(int32_t* sms) {
+  if (!sms) return CODA_ERR_NULL;
+  DevState* d;
+  int st = ensure_device(&d);
+  if (st != CODA_OK) return st;
+  *sms = d->sms;
+  return CODA_OK;
+}
+
+int coda_get_device_status(void* stream, int32_t* site) {
+  if (!site) return CODA_ERR_NULL;
+  DevState* d;
+  int st = ensure_device(&d);
+  if (st != CODA_OK) return st;
+  *site = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return CODA_ERR_LAUNCH;
+  }
+  int v = 0;
+  if (cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return CODA_ERR_LAUNCH;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return CODA_ERR_LAUNCH;
+    *site = v;
+    return CODA_ERR_DEVICE_TIMEOUT;
+  }
+  return CODA_OK;
+}
+
+int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_epilogue_program* prog,
+                       const coda_side_inputs* side, const coda_tensor* out, const coda_aux_outputs* aux,
+                       void* stream) {
+  int st;
+  if ((st = check_tensor(A, true)) != CODA_OK) return st;
+  if ((st = check_tensor(W, true)) != CODA_OK) return st;
+  if ((st = check_tensor(out, false)) != CODA_OK) return st;
+  uint32_t present = 0;
+  const int epi = match_program(prog, &present);
+  if (epi < 0) return CODA_ERR_UNSUPPORTED_PROGRAM;
+  auto has = [&](int op) { return (present >> op) & 1u; };
+
+  // operand kind
+  if (A->dtype != W->dtype) return CODA_ERR_DTYPE;
+  const int kind = A->dtype == CODA_BF16 ? KIND_BF16 : A->dtype == CODA_F32 ? KIND_TF32 : KIND_E4M3;
+  const bool a_mn = A->layout == CODA_COL_MAJOR, b_mn = W->layout == CODA_COL_MAJOR;
+
+  const int64_t M = A->rows, K = A->cols;
+  if (W->cols != K) return CODA_ERR_SHAPE;
+  int64_t N;
+  if (epi == EPI_SWIGLU) {
+    N = out->cols;
+    if (W->rows != 2 * N || N % 128 != 0) return CODA_ERR_SHAPE;
+  } else if (epi == EPI_SWIGLU_BWD) {
+    N = W->rows;
+    if (out->cols != 2 * N) return CODA_ERR_SHAPE;
+  } else {
+    N = W->rows;
+    if (out->cols != N) return CODA_ERR_SHAPE;
+  }
+  if (out->rows != M) return CODA_ERR_SHAPE;
+  if (N % 32 != 0) return CODA_ERR_SHAPE;
+  if (M == 0 || N == 0) return CODA_OK;
+  if (K < 1) return CODA_ERR_SHAPE;
+
+  // side inputs and aux outputs the program needs
+  const coda_side_inputs zero_side{};
+  const coda_aux_outputs zero_aux{};
+  const coda_side_inputs& sd = side ? *side : zero_side;
+  const coda_aux_outputs& ax = aux ? *aux : zero_aux;
+  int side_dt = kind == KIND_TF32 ? DT_F32 : DT_BF16;
+  if (epi == EPI_RESID) {
+    if ((st = check_tensor(sd.residual, false)) != CODA_OK) return st;
+    if (sd.residual->rows != M || sd.residual->cols != N) return CODA_ERR_SHAPE;
+    side_dt = to_dt(sd.residual->dtype);
+  }
+  if (epi == EPI_SWIGLU_BWD) {
+    if ((st = check_tensor(sd.aux_in, false)) != CODA_OK) return st;
+    if (sd.aux_in->rows != M || sd.aux_in->cols != 2 * N) return CODA_ERR_SHAPE;
+    side_dt = to_dt(sd.aux_in->dtype);
+  }
+  if (epi == EPI_RMSBWD) {
+    if ((st = check_tensor(sd.aux_in, false)) != CODA_OK) return st;
+    if ((st = check_tensor(sd.aux_in2, false)) != CODA_OK) return st;
+    if (sd.aux_in->rows != M || sd.aux_in->cols != N || sd.aux_in2->rows != M || sd.aux_in2->cols != N)
+      return CODA_ERR_SHAPE;
+    if (sd.aux_in->dtype != sd.aux_in2->dtype) return CODA_ERR_DTYPE;
+    side_dt = to_dt(sd.aux_in->dtype);
+    if (!sd.col_scale || !sd.row_coef) return CODA_ERR_NULL;
+    if (!aligned16(sd.col_scale)) return CODA_ERR_ALIGN;
+  }
+  if (has(CODA_OP_ROW_SCALE) && !sd.row_scale) return CODA_ERR_NULL;
+  if (has(CODA_OP_COL_SCALE)) {
+    if (!sd.col_scale) return CODA_ERR_NULL;
+    if (!aligned16(sd.col_scale)) return CODA_ERR_ALIGN;
+  }
+  const bool want_aux = has(CODA_OP_STORE_AUX);
+  if (want_aux) {
+    if ((st = check_tensor(ax.store_aux, false)) != CODA_OK) return st;
+    if (ax.store_aux->rows != M || ax.store_aux->cols != 2 * N || ax.store_aux->dtype != CODA_BF16)
+      return CODA_ERR_SHAPE;
+  }
+  if (has(CODA_OP_AMAX) && !ax.amax) return CODA_ERR_NULL;
+  const int bn_out = epi == EPI_SWIGLU ? 128 : 256;
+  const int64_t m_tiles = (M + BM - 1) / BM, n_tiles = (N + bn_out - 1) / bn_out;
+  if (has(CODA_OP_ROW_SUMSQ_PARTIAL) || has(CODA_OP_ROW_DOT_PARTIAL)) {
+    if (!ax.row_partials) return CODA_ERR_NULL;
+    if (ax.row_partials_ld < M) return CODA_ERR_SHAPE;
+  }
+  if (has(CODA_OP_COL_DOT_PARTIAL)) {
+    if (!ax.col_partials) return CODA_ERR_NULL;
+    if (ax.col_partials_ld < N) return CODA_ERR_SHAPE;
+  }
+  if (has(CODA_OP_ROPE)) {
+    const int hd = sd.rope_head_dim;
+    if (!(hd == 32 || hd == 64 || hd == 128 || hd == 256)) return CODA_ERR_SHAPE;
+    if (sd.rope_ncols < 0 || sd.rope_ncols % hd != 0 || sd.rope_ncols > N || sd.rope_seq_len < 1)
+      return CODA_ERR_SHAPE;
+    if (!sd.rope_cos || !sd.rope_sin) return CODA_ERR_NULL;
+    if (!aligned16(sd.rope_cos) || !aligned16(sd.rope_sin)) return CODA_ERR_ALIGN;
+  }
+  if (out->dtype == CODA_E4M3 && epi != EPI_SWIGLU) return CODA_ERR_DTYPE;
+
+  const VariantKey key{kind, epi, a_mn ? 1 : 0, b_mn ? 1 : 0, to_dt(out->dtype), side_dt, want_aux ? 1 : 0};
+  const VariantEntry* var = find_variant(key);
+  if (!var) return CODA_ERR_DTYPE;
+
+  DevState* d;
+  if ((st = ensure_device(&d)) != CODA_OK) return st;
+
+  GemmLaunch L;
+  std::memset(&L, 0, sizeof(L));
+  const int op_bytes = esize(A->dtype);
+  const uint32_t bk = (uint32_t)(128 / op_bytes);
+  // A: K-major box {bk, 128}; MN-major (stored [K][M]) box {64, bk}
+  if (a_mn)
+    st = encode_2d(&L.tmA, A->dtype, A->ptr, M, K, A->ld, 64, bk);
+  else
+    st = encode_2d(&L.tmA, A->dtype, A->ptr, K, M, A->ld, bk, 128);
+  if (st != CODA_OK) return st;
+  if (b_mn)
+    st = encode_2d(&L.tmB, W->dtype, W->ptr, W->rows, K, W->ld, 64, bk);
+  else
+    st = encode_2d(&L.tmB, W->dtype, W->ptr, K, W->rows, W->ld, bk, 128);
+  if (st != CODA_OK) return st;
+  if ((st = encode_2d(&L.tmOut, out->dtype, out->ptr, out->cols, M, out->ld, 32, 32)) != CODA_OK) return st;
+  if (epi == EPI_RESID) {
+    const coda_tensor* r = sd.residual;
+    if ((st = encode_2d(&L.tmSide0, r->dtype, r->ptr, r->cols, M, r->ld, 32, 32)) != CODA_OK) return st;
+  } else if (epi == EPI_SWIGLU_BWD || epi == EPI_RMSBWD) {
+    const coda_tensor* r = sd.aux_in;
+    if ((st = encode_2d(&L.tmSide0, r->dtype, r->ptr, r->cols, M, r->ld, 32, 32)) != CODA_OK) return st;
+    if (epi == EPI_RMSBWD) {
+      const coda_tensor* r2 = sd.aux_in2;
+      if ((st = encode_2d(&L.tmSide1, r2->dtype, r2->ptr, r2->cols, M, r2->ld, 32, 32)) != CODA_OK) return st;
+    }
+  }
+  if (want_aux) {
+    const coda_tensor* z = ax.store_aux;
+    if ((st = encode_2d(&L.tmAux, z->dtype, z->ptr, z->cols, M, z->ld, 32, 32)) != CODA_OK) return st;
+  }
+
+  GemmParams& p = L.p;
+  p.M = (int)M;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.m_tiles = (int)m_tiles;
+  p.n_tiles = (int)n_tiles;
+  p.flags = (has(CODA_OP_ROW_SUMSQ_PARTIAL) ? F_PARTIAL : 0) | (has(CODA_OP_AMAX) ? F_AMAX : 0) |
+            (has(CODA_OP_COL_SCALE) ? F_COLSCALE : 0) | (has(CODA_OP_ROW_SCALE) ? F_ROWSCALE : 0);
+  if (g_inject_once) {
+    p.flags |= F_INJECT_SKIP;
+    g_inject_once = 0;
+  }
+  p.up_offset = (int)N;
+  p.tensor_scale = has(CODA_OP_TENSOR_SCALE) ? sd.tensor_scale : 1.0f;
+  p.out_scale = (out->dtype == CODA_E4M3) ? sd.out_scale : 1.0f;
+  p.row_scale = sd.row_scale;
+  p.row_coef = sd.row_coef;
+  p.col_scale = sd.col_scale;
+  p.rope_cos = sd.rope_cos;
+  p.rope_sin = sd.rope_sin;
+  p.rope_seq_len = sd.rope_seq_len > 0 ? sd.rope_seq_len : 1;
+  p.rope_head_dim = sd.rope_head_dim;
+  p.rope_ncols = has(CODA_OP_ROPE) ? sd.rope_ncols : 0;
+  p.row_part = ax.row_partials;
+  p.row_part_ld = ax.row_partials_ld;
+  p.col_part = ax.col_partials;
+  p.col_part_ld = ax.col_partials_ld;
+  p.amax = reinterpret_cast<unsigned int*>(ax.amax);
+  p.status = d->status;
+  p.timeout_ns = (unsigned long long)g_watchdog_ms * 1000000ull;
+  const int64_t tiles = m_tiles * n_tiles;
+  L.grid = (int)(tiles < d->sms ? tiles : d->sms);
+  const cudaError_t e = var->fn(L, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
+}
+
+int coda_rms_partial_reduce(const float* partials, int64_t ld, int32_t nparts, int64_t M, int64_t d, float eps,
+                            int32_t mode, const float* rowscale, float* out, void* stream) {
+  if (!partials || !out) return CODA_ERR_NULL;
+  if (mode != CODA_REDUCE_RSQRT_MEAN && mode != CODA_REDUCE_SCALE_SUM) return CODA_ERR_SHAPE;
+  if (mode == CODA_REDUCE_SCALE_SUM && !rowscale) return CODA_ERR_NULL;
+  if (M < 0 || d < 1 || nparts < 1 || ld < M) return CODA_ERR_SHAPE;
+  if (M == 0) return CODA_OK;
+  DevState* dv;
+  int st = ensure_device(&dv);
+  if (st != CODA_OK) return st;
+  cudaError_t e = launch_partial_reduce(partials, ld, nparts, M, 1.0f / (float)d, eps, mode, rowscale, out,
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
+}
+
+int coda_row_rms(const coda_tensor* X, float eps, float* r_out, void* stream) {
+  int st;
+  if ((st = check_tensor(X, false)) != CODA_OK) return st;
+  if (!r_out) return CODA_ERR_NULL;
+  if (X->dtype != CODA_BF16) return CODA_ERR_DTYPE;
+  if (X->cols < 1 || X->cols % 8 != 0) return CODA_ERR_SHAPE;
+  if (X->rows == 0) return CODA_OK;
+  DevState* dv;
+  if ((st = ensure_device(&dv)) != CODA_OK) return st;
+  cudaError_t e = launch_row_rms(X->ptr, X->rows, X->cols, X->ld, eps, r_out, static_cast<cudaStream_t>(stream),
+                                 dv->sms);
+  return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
+}
+
+int coda_col_reduce(const float* parts, int64_t nblocks, int64_t N, int64_t ld, float* out, void* stream) {
+  if (!parts || !out) return CODA_ERR_NULL;
+  if (nblocks < 0 || N < 0 || ld < N) return CODA_ERR_SHAPE;
+  if (N == 0) return CODA_OK;
+  DevState* dv;
+  int st = ensure_device(&dv);
+  if (st != CODA_OK) return st;
+  cudaError_t e = launch_col_reduce(parts, nblocks, N, ld, out, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
+}
+
+int coda_fold_gain(const coda_tensor* W, const float* g, const coda_tensor* W_out, void* stream) {
+  int st;
+  if ((st = check_tensor(W, false)) != CODA_OK) return st;
+  if ((st = check_tensor(W_out, false)) != CODA_OK) return st;
+  if (!g) return CODA_ERR_NULL;
+  if (!aligned16(g)) return CODA_ERR_ALIGN;
+  if (W->dtype != W_out->dtype || (W->dtype != CODA_BF16 && W->dtype != CODA_F32)) return CODA_ERR_DTYPE;
+  const bool f32 = W->dtype == CODA_F32;
+  if (W->rows != W_out->rows || W->cols != W_out->cols || W->cols % (f32 ? 4 : 8) != 0) return CODA_ERR_SHAPE;
+  if (W->rows == 0 || W->cols == 0) return CODA_OK;
+  DevState* dv;
+  if ((st = ensure_device(&dv)) != CODA_OK) return st;
+  cudaError_t e = launch_fold_gain(W->ptr, W->rows, W->cols, W->ld, g, W_out->ptr, W_out->ld, f32,
+                                   static_cast<cudaStream_t>(stream), dv->sms);
+  return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
+}
+
+int coda_rope_table(int32_t seq_len, int32_t head_dim, double base, float* cos_out, float* sin_out, void* stream) {
+  if (!cos_out || !sin_out) return CODA_ERR_NULL;
+  if (seq_len < 1 || head_dim < 2 || head_dim % 2 != 0 || !(base > 0.0)) return CODA_ERR_SHAPE;
+  DevState* dv;
+  int st = ensure_device(&dv);
+  if (st != CODA_OK) return st;
+  cudaError_t e = launch_rope_table(seq_len, head_dim, base, cos_out, sin_out, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
+}
+
+size_t coda_workspace_size(int32_t which, int64_t M, int64_t H, int64_t F) {
+  if (M < 0 || H < 0 || F < 0) return 0;
+  if (which == CODA_WS_BLOCK_FWD) return (size_t)((H + 255) / 256) * (size_t)M * sizeof(float);
+  if (which == CODA_WS_BLOCK_BWD)
+    return ((size_t)((F + 255) / 256) * (size_t)M + (size_t)(4 * ((M + 127) / 128)) * (size_t)H) * sizeof(float);
+  return 0;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------- chains
+namespace {
+coda_tensor mk(const void* p, int dt, int64_t rows, int64_t cols, int64_t ld, int layout = CODA_ROW_MAJOR) {
+  coda_tensor t;
+  t.ptr = const_cast<void*>(p);
+  t.dtype = dt;
+  t.layout = layout;
+  t.rows = rows;
+  t.cols = cols;
+  t.ld = ld;
+  return t;
+}
+coda_epilogue_program prog_of(std::initializer_list<int> ops) {
+  coda_epilogue_program p{};
+  for (int o : ops) p.ops[p.n_ops++] = o;
+  return p;
+}
+}  // namespace
+
+extern "C" {
+
+int coda_block_forward(const coda_block_fwd* io, void* stream) {
+  if (!io) return CODA_ERR_NULL;
+  const int64_t M = io->M, H = io->H, F = io->F;
+  if (M < 0 || H < 32 || F < 128 || H % 32 != 0 || F % 128 != 0) return CODA_ERR_SHAPE;
+  if (!io->O || !io->R || !io->W_o || !io->W_gu || !io->W_d || !io->h || !io->r || !io->a || !io->Y ||
+      !io->workspace)
+    return CODA_ERR_NULL;
+  if (M == 0) return CODA_OK;
+  int st;
+  const int64_t nparts = (H + 255) / 256;
+  // G1: h = O W_o^T + R, partial sums of squares of h
+  {
+    coda_tensor A = mk(io->O, CODA_BF16, M, H, H), W = mk(io->W_o, CODA_BF16, H, H, H);
+    coda_tensor R = mk(io->R, CODA_BF16, M, H, H), out = mk(io->h, CODA_BF16, M, H, H);
+    coda_epilogue_program pg = prog_of({CODA_OP_ADD_SIDE, CODA_OP_ROW_SUMSQ_PARTIAL});
+    coda_side_inputs sd{};
+    sd.residual = &R;
+    coda_aux_outputs ax{};
+    ax.row_partials = io->workspace;
+    ax.row_partials_ld = M;
+    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, &ax, stream)) != CODA_OK) return st;
+  }
+  // r = 1 / sqrt(sum of partials / H + eps)
+  if ((st = coda_rms_partial_reduce(io->workspace, M, (int32_t)nparts, M, H, io->eps, CODA_REDUCE_RSQRT_MEAN, nullptr,
+                                    io->r, stream)) != CODA_OK)
+    return st;
+  // G2: [G | U] = r (h W_gu'^T);  a = silu(G) U  [+ saved Z]
+  {
+    coda_tensor A = mk(io->h, CODA_BF16, M, H, H), W = mk(io->W_gu, CODA_BF16, 2 * F, H, H);
+    coda_tensor out = mk(io->a, CODA_BF16, M, F, F);
+    coda_tensor Z = mk(io->Z, CODA_BF16, M, 2 * F, 2 * F);
+    coda_epilogue_program pg = io->Z ? prog_of({CODA_OP_ROW_SCALE, CODA_OP_STORE_AUX, CODA_OP_SWIGLU})
+                                     : prog_of({CODA_OP_ROW_SCALE, CODA_OP_SWIGLU});
+    coda_side_inputs sd{};
+    sd.row_scale = io->r;
+    coda_aux_outputs ax{};
+    ax.store_aux = io->Z ? &Z : nullptr;
+    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, &ax, stream)) != CODA_OK) return st;
+  }
+  // G3: Y = a W_d^T + h  [+ partial sums of squares of Y for the next layer]
+  {
+    coda_tensor A = mk(io->a, CODA_BF16, M, F, F), W = mk(io->W_d, CODA_BF16, H, F, F);
+    coda_tensor R = mk(io->h, CODA_BF16, M, H, H), out = mk(io->Y, CODA_BF16, M, H, H);
+    coda_epilogue_program pg = io->Y_partials ? prog_of({CODA_OP_ADD_SIDE, CODA_OP_ROW_SUMSQ_PARTIAL})
+                                              : prog_of({CODA_OP_ADD_SIDE});
+    coda_side_inputs sd{};
+    sd.residual = &R;
+    coda_aux_outputs ax{};
+    ax.row_partials = io->Y_partials;
+    ax.row_partials_ld = M;
+    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, &ax, stream)) != CODA_OK) return st;
+  }
+  return CODA_OK;
+}
+
+int coda_block_backward(const coda_block_bwd* io, void* stream) {
+  if (!io) return CODA_ERR_NULL;
+  const int64_t M = io->M, H = io->H, F = io->F;
+  if (M < 0 || H < 32 || F < 128 || H % 32 != 0 || F % 128 != 0) return CODA_ERR_SHAPE;
+  if (!io->O || !io->W_o || !io->W_gu || !io->W_d || !io->g || !io->h || !io->r || !io->Z || !io->a || !io->dY ||
+      !io->e || !io->dh || !io->dO || !io->dW_o || !io->dW_gu || !io->dW_d || !io->dg || !io->c || !io->workspace)
+    return CODA_ERR_NULL;
+  if (M == 0) return CODA_OK;
+  int st;
+  float* S = io->workspace;                          // [F/256, M] row partials of e . Z
+  float* Dg = io->workspace + ((F + 255) / 256) * M; // [4 ceil(M/128), H] column partials of h t
+  const int64_t nS = (F + 255) / 256;
+  const int64_t nDg = 4 * ((M + 127) / 128);
+  // b1: e = r [dA U silu'(G) | dA silu(G)],  dA = dY W_d;  row partials of e . Z
+  {
+    coda_tensor A = mk(io->dY, CODA_BF16, M, H, H);
+    coda_tensor W = mk(io->W_d, CODA_BF16, F, H, F, CODA_COL_MAJOR);  // logical W_d^T
+    coda_tensor Z = mk(io->Z, CODA_BF16, M, 2 * F, 2 * F), out = mk(io->e, CODA_BF16, M, 2 * F, 2 * F);
+    coda_epilogue_program pg = prog_of({CODA_OP_SWIGLU_BWD, CODA_OP_ROW_SCALE, CODA_OP_ROW_DOT_PARTIAL});
+    coda_side_inputs sd{};
+    sd.aux_in = &Z;
+    sd.row_scale = io->r;
+    coda_aux_outputs ax{};
+    ax.row_partials = S;
+    ax.row_partials_ld = M;
+    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, &ax, stream)) != CODA_OK) return st;
+  }
+  // b2: dW_d = dY^T a
+  {
+    coda_tensor A = mk(io->dY, CODA_BF16, H, M, H, CODA_COL_MAJOR), W = mk(io->a, CODA_BF16, F, M, F, CODA_COL_MAJOR);
+    coda_tensor out = mk(io->dW_d, CODA_F32, H, F, F);
+    coda_epilogue_program pg = prog_of({});
+    if ((st = coda_gemm_epilogue(&A, &W, &pg, nullptr, &out, nullptr, stream)) != CODA_OK) return st;
+  }
+  // b3: c = r * sum(S) / H
+  if ((st = coda_rms_partial_reduce(S, M, (int32_t)nS, M, H, 0.f, CODA_REDUCE_SCALE_SUM, io->r, io->c, stream)) !=
+      CODA_OK)
+    return st;
+  // b4: t = e W_gu;  dh = g t - c h + dY;  column partials of h t
+  {
+    coda_tensor A = mk(io->e, CODA_BF16, M, 2 * F, 2 * F);
+    coda_tensor W = mk(io->W_gu, CODA_BF16, H, 2 * F, H, CODA_COL_MAJOR);  // logical W_gu^T
+    coda_tensor h = mk(io->h, CODA_BF16, M, H, H), dY = mk(io->dY, CODA_BF16, M, H, H);
+    coda_tensor out = mk(io->dh, CODA_BF16, M, H, H);
+    coda_epilogue_program pg = prog_of({CODA_OP_RMSBWD_COMBINE, CODA_OP_COL_DOT_PARTIAL});
+    coda_side_inputs sd{};
+    sd.aux_in = &h;
+    sd.aux_in2 = &dY;
+    sd.col_scale = io->g;
+    sd.row_coef = io->c;
+    coda_aux_outputs ax{};
+    ax.col_partials = Dg;
+    ax.col_partials_ld = H;
+    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, &ax, stream)) != CODA_OK) return st;
+  }
+  // b5: dg = column sums of the partials
+  if ((st = coda_col_reduce(Dg, nDg, H, H, io->dg, stream)) != CODA_OK) return st;
+  // b6: dW_gu[n, k] = g_k (e^T h)[n, k]
+  {
+    coda_tensor A = mk(io->e, CODA_BF16, 2 * F, M, 2 * F, CODA_COL_MAJOR);
+    coda_tensor W = mk(io->h, CODA_BF16, H, M, H, CODA_COL_MAJOR);
+    coda_tensor out = mk(io->dW_gu, CODA_F32, 2 * F, H, H);
+    coda_epilogue_program pg = prog_of({CODA_OP_COL_SCALE});
+    coda_side_inputs sd{};
+    sd.col_scale = io->g;
+    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, nullptr, stream)) != CODA_OK) return st;
+  }
+  // b7: dO = dh W_o
+  {
+    coda_tensor A = mk(io->dh, CODA_BF16, M, H, H);
+    coda_tensor W = mk(io->W_o, CODA_BF16, H, H, H, CODA_COL_MAJOR);  // logical W_o^T
+    coda_tensor out = mk(io->dO, CODA_BF16, M, H, H);
+    coda_epilogue_program pg = prog_of({});
+    if ((st = coda_gemm_epilogue(&A, &W, &pg, nullptr, &out, nullptr, stream)) != CODA_OK) return st;
+  }
+  // b8: dW_o = dh^T O
+  {
+    coda_tensor A = mk(io->dh, CODA_BF16, H, M, H, CODA_COL_MAJOR), W = mk(io->O, CODA_BF16, H, M, H, CODA_COL_MAJOR);
+    coda_tensor out = mk(io->dW_o, CODA_F32, H, H, H);
+    coda_epilogue_program pg = prog_of({});
+    if ((st = coda_gemm_epilogue(&A, &W, &pg, nullptr, &out, nullptr, stream)) != CODA_OK) return st;
+  }
+  return CODA_OK;
+}
+
+int coda_qkv_rope(const coda_qkv_rope_io* io, void* stream) {
+  if (!io) return CODA_ERR_NULL;
+  if (!io->h || !io->W_qkv || !io->rope_cos || !io->rope_sin || !io->r || !io->out) return CODA_ERR_NULL;
+  const int64_t M = io->M, H = io->H, N = io->N;
+  if (M < 0 || H < 8 || N < 32) return CODA_ERR_SHAPE;
+  if (M == 0) return CODA_OK;
+  int st;
+  coda_tensor h = mk(io->h, CODA_BF16, M, H, H);
+  if ((st = coda_row_rms(&h, io->eps, io->r, stream)) != CODA_OK) return st;
+  coda_tensor W = mk(io->W_qkv, CODA_BF16, N, H, H), out = mk(io->out, CODA_BF16, M, N, N);
+  coda_epilogue_program pg = prog_of({CODA_OP_ROW_SCALE, CODA_OP_ROPE});
+  coda_side_inputs sd{};
+  sd.row_scale = io->r;
+  sd.rope_cos = io->rope_cos;
+  sd.rope_sin = io->rope_sin;
+  sd.rope_seq_len = io->seq_len;
+  sd.rope_head_dim = io->head_dim;
+  sd.rope_ncols = io->rope_ncols;
+  return coda_gemm_epilogue(&h, &W, &pg, &sd, &out, nullptr, stream);
+}
+
+int coda_mlp_fp8(const coda_mlp_fp8_io* io, void* stream) {
+  if (!io) return CODA_ERR_NULL;
+  if (!io->h || !io->X_q || !io->W_q || !io->W_dq || !io->r || !io->a_q || !io->amax || !io->Y || !io->Y_partials)
+    return CODA_ERR_NULL;
+  const int64_t M = io->M, H = io->H, F = io->F;
+  if (M < 0 || H < 32 || F < 128 || H % 32 != 0 || F % 128 != 0) return CODA_ERR_SHAPE;
+  if (!(io->s_a > 0.f)) return CODA_ERR_SHAPE;
+  if (M == 0) return CODA_OK;
+  int st;
+  coda_tensor h = mk(io->h, CODA_BF16, M, H, H);
+  if ((st = coda_row_rms(&h, io->eps, io->r, stream)) != CODA_OK) return st;
+  if (cudaMemsetAsync(io->amax, 0, sizeof(float), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return CODA_ERR_LAUNCH;
+  {
+    coda_tensor A = mk(io->X_q, CODA_E4M3, M, H, H), W = mk(io->W_q, CODA_E4M3, 2 * F, H, H);
+    coda_tensor out = mk(io->a_q, CODA_E4M3, M, F, F);
+    coda_epilogue_program pg = prog_of({CODA_OP_TENSOR_SCALE, CODA_OP_ROW_SCALE, CODA_OP_SWIGLU, CODA_OP_AMAX});
+    coda_side_inputs sd{};
+    sd.tensor_scale = io->s_x * io->s_w;
+    sd.row_scale = io->r;
+    sd.out_scale = 1.0f / io->s_a;
+    coda_aux_outputs ax{};
+    ax.amax = io->amax;
+    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, &ax, stream)) != CODA_OK) return st;
+  }
+  {
+    coda_tensor A = mk(io->a_q, CODA_E4M3, M, F, F), W = mk(io->W_dq, CODA_E4M3, H, F, F);
+    coda_tensor out = mk(io->Y, CODA_BF16, M, H, H);
+    coda_epilogue_program pg = prog_of({CODA_OP_TENSOR_SCALE, CODA_OP_ADD_SIDE, CODA_OP_ROW_SUMSQ_PARTIAL});
+    coda_side_inputs sd{};
+    sd.tensor_scale = io->s_a * io->s_wd;
+    sd.residual = &h;
+    coda_aux_outputs ax{};
+    ax.row_partials = io->Y_partials;
+    ax.row_partials_ld = M;
+    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, &ax, stream)) != CODA_OK) return st;
+  }
+  return CODA_OK;
+}
+
+}  // extern "C"

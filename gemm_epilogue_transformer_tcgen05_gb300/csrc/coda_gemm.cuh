@@ -1,0 +1,733 @@
+// Persistent tcgen05 GEMM with a programmable epilogue (sm_103a).
+//
+// What it computes (one launch):  out = epilogue(acc),  acc[M, N] = A[M, K] . B[N, K]^T
+// with fp32 accumulation in TMEM.  This is the "fixed GEMM mainloop + composable
+// epilogue" split the CODA pages describe: the mainloop is written once; the epilogue
+// runs while the output tile is still on chip, before its single store to HBM
+// ("CODA: new research optimizes Transformer training with GEMM-epilogue programming",
+// kucoin.com news flash, sections "El epílogo esconde un tesoro" and "Cinco bloques y un
+// lenguaje LEGO").  The pages picture the tile in registers; on this GPU it lives in
+// tensor memory (TMEM) and is read back in 32-column chunks by the epilogue warps.
+//
+// Structure (one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer: A and B k-blocks into a STAGES-deep shared-memory ring
+//   warp 1      TMEM allocation + single-thread tcgen05.mma issue (128 x 256 x 32 bytes
+//               of K per instruction) into one of two TMEM accumulators (2 x 256 cols)
+//   warps 2..5  epilogue: tcgen05.ld (thread = output row), the epilogue program, row /
+//               column partial reductions, cast, swizzled staging in shared memory and
+//               TMA stores; side inputs (residual, saved activations) arrive by TMA.
+// The two TMEM accumulators let tile t+1's mainloop run under tile t's epilogue.
+//
+// Every wait is bounded (global timer).  On expiry the waiting thread records a site
+// code in a device status word, raises a CTA-wide abort flag, every role leaves its loop,
+// copies in flight are drained with a short bounded wait, TMEM is freed and the kernel
+// returns; the host reads the status word.  Nothing traps.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "coda_ptx.cuh"
+
+namespace coda {
+
+// ----------------------------------------------------------------------- constants
+constexpr int BM = 128;                               // tile rows = TMEM lanes
+constexpr int UMMA_N = 256;                           // MMA N = B tile rows
+constexpr int BK_BYTES = 128;                         // K bytes per stage (one 128B swizzle row)
+constexpr int KSTEPS = 4;                             // MMAs per stage, 32 bytes of K each
+constexpr int A_STAGE_BYTES = BM * BK_BYTES;          // 16 KB
+constexpr int B_STAGE_BYTES = UMMA_N * BK_BYTES;      // 32 KB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int TMEM_COLS = 2 * UMMA_N;                 // two fp32 accumulators
+constexpr int NUM_EPI_WARPS = 4;
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
+constexpr int MAX_SMEM = 232448;                      // 227 KB opt-in per CTA
+
+enum : int { DT_F32 = 0, DT_BF16 = 1, DT_E4M3 = 2 };
+__host__ __device__ constexpr int dt_bytes(int dt) { return dt == DT_F32 ? 4 : dt == DT_BF16 ? 2 : 1; }
+
+enum : int { KIND_BF16 = 0, KIND_TF32 = 1, KIND_E4M3 = 2 };
+
+// Compiled epilogue programs (the host maps an op list onto one of these).
+enum : int {
+  EPI_STORE = 0,       // out = ts * acc [* g_col]
+  EPI_RESID = 1,       // out = ts * acc + R            [+ row partial sum of squares of out]
+  EPI_ROWSCALE = 2,    // out = ts * r_row * acc
+  EPI_SWIGLU = 3,      // Z = ts * r_row * acc (gate | up halves); out = silu(Zg) * Zu * os
+                       //   [+ saved Z, + amax |silu(Zg) * Zu|]
+  EPI_ROPE = 4,        // out = rope(ts * r_row * acc) on the first rope_ncols columns
+  EPI_SWIGLU_BWD = 5,  // e = r_row * [dA * Zu * silu'(Zg) | dA * silu(Zg)]; row partial sum e . Z
+  EPI_RMSBWD = 6,      // out = g_col * acc - c_row * h + dY; column partial sum h * acc
+};
+
+enum : int {
+  F_PARTIAL = 1,    // write row partials (EPI_RESID)
+  F_AMAX = 4,       // accumulate amax (EPI_SWIGLU)
+  F_COLSCALE = 8,   // multiply by col_scale (EPI_STORE)
+  F_ROWSCALE = 16,  // multiply by row_scale (EPI_SWIGLU / EPI_ROPE / EPI_ROWSCALE / EPI_SWIGLU_BWD)
+  F_INJECT_SKIP = 1 << 30,  // test hook: the producer drops its first k-block
+};
+
+// Device status word: 0 = fine; otherwise the site of the first wait that timed out.
+enum : int {
+  SITE_PRODUCER_EMPTY = 1,
+  SITE_MMA_TMEM_EMPTY = 2,
+  SITE_MMA_FULL = 3,
+  SITE_EPI_TMEM_FULL = 4,
+  SITE_EPI_SIDE = 5,
+};
+
+struct GemmParams {
+  int M, N, K;          // out [M, N]; EPI_SWIGLU: N = F and B holds 2F rows (gate, then up)
+  int m_tiles, n_tiles;
+  int flags;
+  int up_offset;        // EPI_SWIGLU: first up row of B / first U column of saved Z;
+                        // EPI_SWIGLU_BWD: first U column of Z and of e
+  float tensor_scale;   // ts above (fp8 dequantisation), 1 otherwise
+  float out_scale;      // os above (1 / s_a before an e4m3 cast), 1 otherwise
+  const float* row_scale;
+  const float* row_coef;
+  const float* col_scale;
+  const float* rope_cos;  // [rope_seq_len, rope_head_dim / 2]
+  const float* rope_sin;
+  int rope_seq_len, rope_head_dim, rope_ncols;
+  float* row_part;        // [n_tiles, row_part_ld]
+  long long row_part_ld;
+  float* col_part;        // [4 * m_tiles, col_part_ld]
+  long long col_part_ld;
+  unsigned int* amax;     // fp32 bits, atomic max (non-negative values order as integers)
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+template <int KIND_, int EPI_, bool A_MN_, bool B_MN_, int OUT_DT_, int SIDE_DT_, bool AUX_>
+struct GemmCfg {
+  static constexpr int KIND = KIND_, EPI = EPI_, OUT_DT = OUT_DT_, SIDE_DT = SIDE_DT_;
+  static constexpr bool A_MN = A_MN_, B_MN = B_MN_, AUX = AUX_;
+  static constexpr int OP_BYTES = KIND == KIND_TF32 ? 4 : KIND == KIND_BF16 ? 2 : 1;
+  static constexpr int BK = BK_BYTES / OP_BYTES;   // K elements per stage
+  static constexpr bool DUAL = EPI == EPI_SWIGLU;
+  static constexpr int BN_OUT = DUAL ? 128 : 256;  // output columns per tile
+  static constexpr int NCHUNK = BN_OUT / 32;
+  static constexpr int NS = EPI == EPI_RESID ? 1 : (EPI == EPI_SWIGLU_BWD || EPI == EPI_RMSBWD) ? 2 : 0;
+  static constexpr int NO = EPI == EPI_SWIGLU_BWD ? 2 : 1;
+  static constexpr int OSLOT = 32 * 32 * dt_bytes(OUT_DT);  // one 32 x 32 staging block
+  static constexpr int SSLOT = 32 * 32 * dt_bytes(SIDE_DT);
+  static constexpr int XSLOT = 32 * 32 * 2;                 // saved Z (bf16)
+  static constexpr int OUTSET = NO * OSLOT + (AUX ? 2 * XSLOT : 0);
+  static constexpr int EPI_WARP_BYTES = 2 * NS * SSLOT + 2 * OUTSET;
+  static constexpr int EPI_BYTES = NUM_EPI_WARPS * EPI_WARP_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int STAGES_FIT = (MAX_SMEM - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 4 ? 4 : STAGES_FIT;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+  static_assert(STAGES >= 2, "shared memory budget");
+  static_assert(!(A_MN || B_MN) || KIND == KIND_BF16, "MN-major operands are bf16 only");
+  static_assert(!AUX || EPI == EPI_SWIGLU, "saved Z only with SwiGLU");
+  // instruction descriptor: D f32, A/B format, operand majors, N >> 3, M >> 4
+  static constexpr uint32_t FMT = KIND == KIND_BF16 ? 1u : KIND == KIND_TF32 ? 2u : 0u;
+  static constexpr uint32_t IDESC = (1u << 4) | (FMT << 7) | (FMT << 10) | ((A_MN ? 1u : 0u) << 15) |
+                                    ((B_MN ? 1u : 0u) << 16) | ((uint32_t)(UMMA_N >> 3) << 17) |
+                                    ((uint32_t)(BM >> 4) << 24);
+};
+
+// Shared-memory matrix descriptor, 128B swizzle, version 1 (sm_100 family).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+struct Watch {
+  volatile int* abort;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+// Bounded wait on an mbarrier phase.  False = gave up (timeout here, or abort elsewhere).
+__device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, const Watch& w, int site) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*w.abort) return false;
+    if (ptx::globaltimer() - t0 > w.timeout_ns) {
+      *w.abort = 1;
+      __threadfence_block();
+      if (w.status) atomicCAS(w.status, 0, site);
+      return false;
+    }
+  }
+}
+// Short bounded wait used only while draining after an abort (never raises anything).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer() - t0 > 20000000ull) return;
+  }
+}
+
+// ------------------------------------------------------- swizzled 32 x 32 staging blocks
+// A staging block holds 32 rows of 32 elements; row bytes RB = 32 * elem size; 16-byte
+// chunk j of row i sits at chunk j ^ ((i * RB / 128) & (RB / 16 - 1)), which is the TMA
+// 32/64/128-byte swizzle for that row width.  Thread i touches row i only; the XOR spreads
+// 8 consecutive rows over all 32 banks.
+template <int DT>
+__device__ __forceinline__ uint32_t swz(uint32_t slot, int row, int j) {
+  constexpr int RB = 32 * dt_bytes(DT);
+  constexpr int MASK = RB / 16 - 1;
+  return slot + row * RB + ((j ^ ((row * RB >> 7) & MASK)) << 4);
+}
+
+template <int DT>
+__device__ __forceinline__ void slot_read(uint32_t slot, int row, float (&x)[32]) {
+  if constexpr (DT == DT_BF16) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 u = ptx::ld_shared_v4(swz<DT>(slot, row, j));
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        x[8 * j + 2 * k] = __uint_as_float(w[k] << 16);
+        x[8 * j + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+      }
+    }
+  } else if constexpr (DT == DT_F32) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint4 u = ptx::ld_shared_v4(swz<DT>(slot, row, j));
+      x[4 * j] = __uint_as_float(u.x);
+      x[4 * j + 1] = __uint_as_float(u.y);
+      x[4 * j + 2] = __uint_as_float(u.z);
+      x[4 * j + 3] = __uint_as_float(u.w);
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+__device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+template <int DT>
+__device__ __forceinline__ void slot_write(uint32_t slot, int row, const float (&x)[32]) {
+  if constexpr (DT == DT_BF16) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      ptx::st_shared_v4(swz<DT>(slot, row, j), pack_bf16(x[8 * j], x[8 * j + 1]), pack_bf16(x[8 * j + 2], x[8 * j + 3]),
+                        pack_bf16(x[8 * j + 4], x[8 * j + 5]), pack_bf16(x[8 * j + 6], x[8 * j + 7]));
+  } else if constexpr (DT == DT_F32) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      ptx::st_shared_v4(swz<DT>(slot, row, j), __float_as_uint(x[4 * j]), __float_as_uint(x[4 * j + 1]),
+                        __float_as_uint(x[4 * j + 2]), __float_as_uint(x[4 * j + 3]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int e = 16 * j + 4 * k;
+        w[k] = (uint32_t)ptx::cvt_e4m3x2(x[e], x[e + 1]) | ((uint32_t)ptx::cvt_e4m3x2(x[e + 2], x[e + 3]) << 16);
+      }
+      ptx::st_shared_v4(swz<DT>(slot, row, j), w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+// Value as it will be stored (used where a partial must match the stored tensor).
+template <int DT>
+__device__ __forceinline__ float as_stored(float x) {
+  if constexpr (DT == DT_BF16) return round_bf16(x);
+  else return x;
+}
+
+// Lane l returns sum over the 32 lanes of x[l] (x is consumed).  31 shuffles.
+__device__ __forceinline__ float warp_transpose_sum(float (&x)[32], int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = upper ? x[i] : x[i + off];
+      const float keep = upper ? x[i + off] : x[i];
+      x[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return x[0];
+}
+
+__device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+
+// =====================================================================================
+template <class C>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmSide0,
+                         const __grid_constant__ CUtensorMap tmSide1, const __grid_constant__ CUtensorMap tmAux,
+                         const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  const uint32_t sm_stage = base;
+  const uint32_t sm_epi = base + C::STAGES * STAGE_BYTES;
+  const uint32_t sm_bar = sm_epi + C::EPI_BYTES;
+  const int NBAR = 2 * C::STAGES + 13;
+  uint8_t* misc = smem_raw + (sm_bar - raw) + 8 * NBAR;
+  volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+
+#define FULL_BAR(s) (sm_bar + 8u * (s))
+#define EMPTY_BAR(s) (sm_bar + 8u * (C::STAGES + (s)))
+#define TFULL_BAR(a) (sm_bar + 8u * (2 * C::STAGES + (a)))
+#define TEMPTY_BAR(a) (sm_bar + 8u * (2 * C::STAGES + 2 + (a)))
+#define SIDE_BAR(w, s) (sm_bar + 8u * (2 * C::STAGES + 4 + 2 * (w) + (s)))
+#define DONE_BAR (sm_bar + 8u * (2 * C::STAGES + 12))
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      ptx::mbar_init(FULL_BAR(s), 1);
+      ptx::mbar_init(EMPTY_BAR(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(TFULL_BAR(a), 1);
+      ptx::mbar_init(TEMPTY_BAR(a), NUM_EPI_WARPS);
+    }
+    for (int w = 0; w < NUM_EPI_WARPS; ++w)
+      for (int s = 0; s < 2; ++s) ptx::mbar_init(SIDE_BAR(w, s), 1);
+    ptx::mbar_init(DONE_BAR, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(const_cast<uint32_t*>(tmem_holder)), TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const Watch watch{abort_flag, p.status, p.timeout_ns};
+  const int total_tiles = p.m_tiles * p.n_tiles;
+  const int num_kb = (p.K + C::BK - 1) / C::BK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_any = 0, issued_par = 0;
+      bool skip = (p.flags & F_INJECT_SKIP) != 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const int mb = tile / p.n_tiles, nb = tile % p.n_tiles;
+        const int m0 = mb * BM;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!bwait(EMPTY_BAR(stage), phase ^ 1u, watch, SITE_PRODUCER_EMPTY)) {
+            ok = false;
+            break;
+          }
+          if (skip) {
+            skip = false;  // test hook: this k-block never arrives
+          } else {
+            const uint32_t fb = FULL_BAR(stage);
+            const uint32_t sa = sm_stage + stage * STAGE_BYTES;
+            const uint32_t sb = sa + A_STAGE_BYTES;
+            const int k0 = kb * C::BK;
+            ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            if constexpr (C::A_MN) {
+              ptx::tma_load_2d(sa, &tmA, m0, k0, fb);
+              ptx::tma_load_2d(sa + 8192, &tmA, m0 + 64, k0, fb);
+            } else {
+              ptx::tma_load_2d(sa, &tmA, k0, m0, fb);
+            }
+            if constexpr (C::B_MN) {
+              const int n0 = nb * UMMA_N;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) ptx::tma_load_2d(sb + 8192 * j, &tmB, n0 + 64 * j, k0, fb);
+            } else {
+              const int r0 = C::DUAL ? nb * 128 : nb * UMMA_N;
+              const int r1 = C::DUAL ? p.up_offset + nb * 128 : r0 + 128;
+              ptx::tma_load_2d(sb, &tmB, k0, r0, fb);
+              ptx::tma_load_2d(sb + 16384, &tmB, k0, r1, fb);
+            }
+            issued_any |= 1u << stage;
+            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // let loads already in flight land before the CTA exits
+        for (int s = 0; s < C::STAGES; ++s)
+          if (issued_any & (1u << s)) drain_wait(FULL_BAR(s), (issued_par >> s) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int t = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++t) {
+        const int acc = t & 1;
+        const uint32_t aph = (t >> 1) & 1;
+        if (!bwait(TEMPTY_BAR(acc), aph ^ 1u, watch, SITE_MMA_TMEM_EMPTY)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * UMMA_N;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!bwait(FULL_BAR(stage), phase, watch, SITE_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = sm_stage + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_STAGE_BYTES;
+#pragma unroll
+          for (int k = 0; k < KSTEPS; ++k) {
+            const uint64_t ad = C::A_MN ? smem_desc(sa + k * 2048, 8192, 1024) : smem_desc(sa + k * 32, 16, 1024);
+            const uint64_t bd = C::B_MN ? smem_desc(sb + k * 2048, 8192, 1024) : smem_desc(sb + k * 32, 16, 1024);
+            ptx::umma<C::KIND>(d_tmem, ad, bd, C::IDESC, (kb | k) != 0 ? 1u : 0u);
+          }
+          ptx::umma_commit(EMPTY_BAR(stage));  // frees the stage once these MMAs are done
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::umma_commit(TFULL_BAR(acc));  // accumulator complete
+      }
+      if (!ok) {  // wait for MMAs already issued before TMEM is released
+        ptx::umma_commit(DONE_BAR);
+        drain_wait(DONE_BAR, 0);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue warps
+    const int ew = warp - 2;  // staging ownership
+    const int q = warp & 3;   // TMEM lane quadrant this warp may read
+    const uint32_t side_base = sm_epi + ew * C::EPI_WARP_BYTES;
+    const uint32_t out_base = side_base + 2 * C::NS * C::SSLOT;
+    uint32_t side_par = 0, side_pending = 0;
+    float amax_local = 0.f;
+    bool ok = true;
+    int t = 0;
+    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++t) {
+      const int mb = tile / p.n_tiles, nb = tile % p.n_tiles;
+      const int m0 = mb * BM;
+      const int n0 = nb * C::BN_OUT;
+      const int r0 = m0 + 32 * q;   // first row of this warp's 32-row slab
+      const int row = r0 + lane;
+      const bool row_ok = row < p.M;
+      const int acc = t & 1;
+      const uint32_t aph = (t >> 1) & 1;
+
+      // A chunk is live if some of its rows and columns are in range; side loads of dead
+      // chunks are neither issued nor waited for.
+      const bool slab_ok = r0 < p.M;
+      auto live = [&](int c) { return slab_ok && (n0 + 32 * c < p.N); };
+      auto issue_side = [&](int c) {
+        if constexpr (C::NS > 0) {
+          const int slot = c & 1;
+          const uint32_t sbar = SIDE_BAR(ew, slot);
+          const uint32_t dst = side_base + slot * C::NS * C::SSLOT;
+          ptx::mbar_arrive_expect_tx(sbar, C::NS * C::SSLOT);
+          if constexpr (C::EPI == EPI_RESID) {
+            ptx::tma_load_2d(dst, &tmSide0, n0 + 32 * c, r0, sbar);
+          } else if constexpr (C::EPI == EPI_SWIGLU_BWD) {
+            ptx::tma_load_2d(dst, &tmSide0, n0 + 32 * c, r0, sbar);
+            ptx::tma_load_2d(dst + C::SSLOT, &tmSide0, p.up_offset + n0 + 32 * c, r0, sbar);
+          } else {
+            ptx::tma_load_2d(dst, &tmSide0, n0 + 32 * c, r0, sbar);
+            ptx::tma_load_2d(dst + C::SSLOT, &tmSide1, n0 + 32 * c, r0, sbar);
+          }
+        }
+      };
+      if constexpr (C::NS > 0) {
+        if (live(0)) {
+          if (lane == 0) issue_side(0);
+          side_pending |= 1u;
+        }
+        if (C::NCHUNK > 1 && live(1)) {
+          if (lane == 0) issue_side(1);
+          side_pending |= 2u;
+        }
+      }
+
+      float rs = 1.f, rc = 0.f;
+      if ((p.flags & F_ROWSCALE) && row_ok) rs = __ldg(p.row_scale + row);
+      if constexpr (C::EPI == EPI_RMSBWD) {
+        if (row_ok) rc = __ldg(p.row_coef + row);
+      }
+      const float ts = p.tensor_scale;
+
+      ok = bwait(TFULL_BAR(acc), aph, watch, SITE_EPI_TMEM_FULL);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t tacc = tmem_base + ((uint32_t)(32 * q) << 16) + acc * UMMA_N;
+      float rowacc = 0.f;
+
+#pragma unroll 1
+      for (int c = 0; c < C::NCHUNK; ++c) {
+        float x[32];
+        float xu[C::DUAL ? 32 : 1];
+        {
+          uint32_t v[32];
+          ptx::tmem_ld32(tacc + 32 * c, v);
+          if constexpr (C::DUAL) {
+            uint32_t u[32];
+            ptx::tmem_ld32(tacc + 128 + 32 * c, u);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) xu[j] = __uint_as_float(u[j]);
+          } else {
+            ptx::tmem_ld_wait();
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
+        }
+        if (c == C::NCHUNK - 1) {  // accumulator fully read: hand it back to the MMA warp
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(TEMPTY_BAR(acc));
+        }
+
+        // side inputs of this chunk
+        float s0[C::NS > 0 ? 32 : 1];
+        float s1[C::NS > 1 ? 32 : 1];
+        if constexpr (C::NS > 0) {
+          const int slot = c & 1;
+          if (live(c)) {
+            bool sok = bwait(SIDE_BAR(ew, slot), (side_par >> slot) & 1u, watch, SITE_EPI_SIDE);
+            sok = __all_sync(0xffffffffu, sok);
+            if (!sok) {
+              ok = false;
+              break;
+            }
+            side_par ^= 1u << slot;
+            side_pending &= ~(1u << slot);
+            const uint32_t src = side_base + slot * C::NS * C::SSLOT;
+            slot_read<C::SIDE_DT>(src, lane, s0);
+            if constexpr (C::NS > 1) slot_read<C::SIDE_DT>(src + C::SSLOT, lane, s1);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              s0[j] = 0.f;
+              if constexpr (C::NS > 1) s1[j] = 0.f;
+            }
+          }
+          __syncwarp();
+          if (c + 2 < C::NCHUNK && live(c + 2)) {
+            if (lane == 0) issue_side(c + 2);
+            side_pending |= 1u << slot;
+          }
+        }
+
+        const int col0 = n0 + 32 * c;
+        float o1[C::NO > 1 ? 32 : 1];
+        float zg[C::AUX ? 32 : 1], zu[C::AUX ? 32 : 1];
+
+        // ---------------------------------------------------------------- the program
+        if constexpr (C::EPI == EPI_STORE) {
+          if (p.flags & F_COLSCALE) {
+            const float4* g4 = reinterpret_cast<const float4*>(p.col_scale + col0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float4 g = __ldg(g4 + j);
+              x[4 * j] *= ts * g.x;
+              x[4 * j + 1] *= ts * g.y;
+              x[4 * j + 2] *= ts * g.z;
+              x[4 * j + 3] *= ts * g.w;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] *= ts;
+          }
+        } else if constexpr (C::EPI == EPI_RESID) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            x[j] = fmaf(x[j], ts, s0[j]);
+            const float st = as_stored<C::OUT_DT>(x[j]);
+            rowacc = fmaf(st, st, rowacc);
+          }
+        } else if constexpr (C::EPI == EPI_ROWSCALE) {
+          const float sc = ts * rs;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[j] *= sc;
+        } else if constexpr (C::EPI == EPI_SWIGLU) {
+          const float sc = ts * rs;
+          const float os = p.out_scale;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float G = x[j] * sc, U = xu[j] * sc;
+            if constexpr (C::AUX) {
+              zg[j] = G;
+              zu[j] = U;
+            }
+            const float a = silu_f(G) * U;
+            amax_local = fmaxf(amax_local, fabsf(a));
+            x[j] = a * os;
+          }
+        } else if constexpr (C::EPI == EPI_ROPE) {
+          const float sc = ts * rs;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[j] *= sc;
+          if (col0 < p.rope_ncols) {
+            const int pos = row % p.rope_seq_len;
+            const int half = p.rope_head_dim >> 1;
+            const int pb = (col0 % p.rope_head_dim) >> 1;
+            const float4* c4 = reinterpret_cast<const float4*>(p.rope_cos + (size_t)pos * half + pb);
+            const float4* s4 = reinterpret_cast<const float4*>(p.rope_sin + (size_t)pos * half + pb);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float4 cv = __ldg(c4 + j), sv = __ldg(s4 + j);
+              const float cs[4] = {cv.x, cv.y, cv.z, cv.w};
+              const float sn[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int e = 8 * j + 2 * k;
+                const float a0 = x[e], a1 = x[e + 1];
+                x[e] = a0 * cs[k] - a1 * sn[k];
+                x[e + 1] = a0 * sn[k] + a1 * cs[k];
+              }
+            }
+          }
+        } else if constexpr (C::EPI == EPI_SWIGLU_BWD) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float dA = x[j], G = s0[j], U = s1[j];
+            const float sg = sigmoid_f(G);
+            const float eg = as_stored<C::OUT_DT>(rs * dA * U * sg * (1.f + G * (1.f - sg)));
+            const float eu = as_stored<C::OUT_DT>(rs * dA * G * sg);
+            rowacc = fmaf(eg, G, fmaf(eu, U, rowacc));
+            x[j] = eg;
+            o1[j] = eu;
+          }
+        } else if constexpr (C::EPI == EPI_RMSBWD) {
+          float ht[32];
+          const float4* g4 = reinterpret_cast<const float4*>(p.col_scale + col0);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 g = __ldg(g4 + j);
+            const float gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int e = 4 * j + k;
+              ht[e] = s0[e] * x[e];
+              x[e] = gv[k] * x[e] - rc * s0[e] + s1[e];
+            }
+          }
+          const float colsum = warp_transpose_sum(ht, lane);
+          if (col0 + lane < p.N) p.col_part[(size_t)(4 * mb + q) * p.col_part_ld + col0 + lane] = colsum;
+        }
+
+        // ---------------------------------------------------------------- stage + store
+        const bool store = col0 < p.N && r0 < p.M;
+        const uint32_t oslot = out_base + (c & 1) * C::OUTSET;
+        if (lane == 0) ptx::bulk_wait_read<1>();  // the group that last used this set is done reading
+        __syncwarp();
+        slot_write<C::OUT_DT>(oslot, lane, x);
+        if constexpr (C::NO > 1) slot_write<C::OUT_DT>(oslot + C::OSLOT, lane, o1);
+        if constexpr (C::AUX) {
+          slot_write<DT_BF16>(oslot + C::NO * C::OSLOT, lane, zg);
+          slot_write<DT_BF16>(oslot + C::NO * C::OSLOT + C::XSLOT, lane, zu);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (store) {
+            ptx::tma_store_2d(&tmOut, col0, r0, oslot);
+            if constexpr (C::EPI == EPI_SWIGLU_BWD) ptx::tma_store_2d(&tmOut, p.up_offset + col0, r0, oslot + C::OSLOT);
+            if constexpr (C::AUX) {
+              ptx::tma_store_2d(&tmAux, col0, r0, oslot + C::NO * C::OSLOT);
+              ptx::tma_store_2d(&tmAux, p.up_offset + col0, r0, oslot + C::NO * C::OSLOT + C::XSLOT);
+            }
+          }
+          ptx::bulk_commit();
+        }
+      }
+      if (!ok) break;
+      if constexpr (C::EPI == EPI_RESID || C::EPI == EPI_SWIGLU_BWD) {
+        if ((C::EPI == EPI_SWIGLU_BWD || (p.flags & F_PARTIAL)) && row_ok)
+          p.row_part[(size_t)nb * p.row_part_ld + row] = rowacc;
+      }
+    }
+    if constexpr (C::EPI == EPI_SWIGLU) {
+      if (p.flags & F_AMAX) {
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+          amax_local = fmaxf(amax_local, __shfl_xor_sync(0xffffffffu, amax_local, off));
+        if (lane == 0 && amax_local > 0.f) atomicMax(p.amax, __float_as_uint(amax_local));
+      }
+    }
+    if (lane == 0) {
+      ptx::bulk_wait<0>();  // every TMA store of this warp has completed
+      if (!ok) {
+        for (int s = 0; s < 2; ++s)
+          if (side_pending & (1u << s)) drain_wait(SIDE_BAR(ew, s), (side_par >> s) & 1u);
+      }
+    }
+    __syncwarp();
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+#undef FULL_BAR
+#undef EMPTY_BAR
+#undef TFULL_BAR
+#undef TEMPTY_BAR
+#undef SIDE_BAR
+#undef DONE_BAR
+}
+
+// ------------------------------------------------------------------ host launcher
+struct GemmLaunch {
+  CUtensorMap tmA, tmB, tmOut, tmSide0, tmSide1, tmAux;
+  GemmParams p;
+  int grid;
+};
+
+using GemmLaunchFn = cudaError_t (*)(const GemmLaunch&, cudaStream_t);
+
+template <class C>
+cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t s) {
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_epilogue_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = 1;
+  }
+  gemm_epilogue_kernel<C><<<L.grid, NUM_THREADS, C::SMEM_BYTES, s>>>(L.tmA, L.tmB, L.tmOut, L.tmSide0, L.tmSide1,
+                                                                      L.tmAux, L.p);
+  return cudaGetLastError();
+}
+
+}  // namespace coda

@@ -1,0 +1,50 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "coda_gemm.cuh"
+
+namespace coda {
+
+// One compiled GEMM-epilogue variant.
+struct VariantKey {
+  int kind, epi, a_mn, b_mn, out_dt, side_dt, aux;
+};
+struct VariantEntry {
+  VariantKey key;
+  GemmLaunchFn fn;
+  int smem_bytes;
+  int stages;
+};
+
+// Tables defined by the instantiation units.
+extern const VariantEntry g_variants_fwd[];
+extern const int g_num_variants_fwd;
+extern const VariantEntry g_variants_bwd[];
+extern const int g_num_variants_bwd;
+extern const VariantEntry g_variants_lowp[];
+extern const int g_num_variants_lowp;
+
+const VariantEntry* find_variant(const VariantKey& k);
+
+// Small bandwidth-bound kernels (coda_small.cu).  Arguments are validated by the caller.
+cudaError_t launch_partial_reduce(const float* partials, int64_t ld, int nparts, int64_t M, float inv_d, float eps,
+                                  int mode, const float* rowscale, float* out, cudaStream_t s);
+cudaError_t launch_row_rms(const void* X, int64_t M, int64_t d, int64_t ld, float eps, float* r, cudaStream_t s,
+                           int sms);
+cudaError_t launch_col_reduce(const float* parts, int64_t nblocks, int64_t N, int64_t ld, float* out,
+                              cudaStream_t s);
+cudaError_t launch_fold_gain(const void* W, int64_t N, int64_t K, int64_t ld_in, const float* g, void* W_out,
+                             int64_t ld_out, bool f32, cudaStream_t s, int sms);
+cudaError_t launch_rope_table(int seq_len, int head_dim, double base, float* cos_out, float* sin_out,
+                              cudaStream_t s);
+
+}  // namespace coda
+
+#define CODA_VARIANT(KIND, EPI, AMN, BMN, OUT, SIDE, AUX)                                                   \
+  {{KIND, EPI, AMN, BMN, OUT, SIDE, AUX},                                                                 \
+   &launch_gemm<GemmCfg<KIND, EPI, AMN, BMN, OUT, SIDE, AUX>>,                                            \
+   GemmCfg<KIND, EPI, AMN, BMN, OUT, SIDE, AUX>::SMEM_BYTES,                                              \
+   GemmCfg<KIND, EPI, AMN, BMN, OUT, SIDE, AUX>::STAGES}

@@ -1,0 +1,197 @@
+// Bandwidth- and latency-bound helper kernels of the GEMM-epilogue chains:
+//   * the light row reduce that turns per-tile partial sums into the RMS scale r (or the
+//     backward coefficient c) — "CODA: new research optimizes Transformer training with
+//     GEMM-epilogue programming" (kucoin.com news flash), section "El epílogo esconde un
+//     tesoro": partial RMS from the first GEMM, combined by a very light reduce kernel;
+//   * a full-row RMS scale (one pass over an activation) for chains that start from a
+//     stored activation;
+//   * the column reduce of per-block column partials (RMSNorm gain gradient);
+//   * the gain fold W' = W diag(g) (weight preparation for the deferred-r GEMM);
+//   * the RoPE cos/sin table.
+#include <cuda_bf16.h>
+
+#include "coda_internal.h"
+
+namespace coda {
+
+// ---------------------------------------------------------------- partial reduce
+// One thread per row; parts summed in index order (deterministic).  Reads are coalesced
+// because the partials are stored [nparts, M].
+__global__ void partial_reduce_kernel(const float* __restrict__ P, int64_t ld, int nparts, int64_t M, float inv_d,
+                                      float eps, int mode, const float* __restrict__ rowscale,
+                                      float* __restrict__ out) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= M) return;
+  float s = 0.f;
+  for (int t = 0; t < nparts; ++t) s += __ldg(P + (int64_t)t * ld + i);
+  if (mode == 0)
+    out[i] = rsqrtf(fmaf(s, inv_d, eps));
+  else
+    out[i] = __ldg(rowscale + i) * (s * inv_d);
+}
+
+cudaError_t launch_partial_reduce(const float* partials, int64_t ld, int nparts, int64_t M, float inv_d, float eps,
+                                  int mode, const float* rowscale, float* out, cudaStream_t s) {
+  const int threads = 256;
+  const int64_t blocks = (M + threads - 1) / threads;
+  partial_reduce_kernel<<<(unsigned)blocks, threads, 0, s>>>(partials, ld, nparts, M, inv_d, eps, mode, rowscale,
+                                                              out);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- full-row RMS
+// One warp per row, 16-byte loads (8 bf16 per lane), four loads in flight per lane.
+__global__ void row_rms_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, int64_t d, int64_t ld, float eps,
+                               float* __restrict__ r) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= M) return;
+  const uint4* src = reinterpret_cast<const uint4*>(X + row * ld);
+  const int64_t nvec = d >> 3;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  int64_t v = lane;
+  for (; v + 96 < nvec; v += 128) {
+    uint4 u[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) u[k] = __ldcs(src + v + 32 * k);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t w[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
+        acc[k] = fmaf(lo, lo, fmaf(hi, hi, acc[k]));
+      }
+    }
+  }
+  for (; v < nvec; v += 32) {
+    const uint4 u = __ldcs(src + v);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
+      acc[0] = fmaf(lo, lo, fmaf(hi, hi, acc[0]));
+    }
+  }
+  float s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (lane == 0) r[row] = rsqrtf(fmaf(s, 1.0f / (float)d, eps));
+}
+
+cudaError_t launch_row_rms(const void* X, int64_t M, int64_t d, int64_t ld, float eps, float* r, cudaStream_t s,
+                           int sms) {
+  (void)sms;
+  const int rows_per_block = 8;
+  const int64_t blocks = (M + rows_per_block - 1) / rows_per_block;
+  row_rms_kernel<<<(unsigned)blocks, 32 * rows_per_block, 0, s>>>(static_cast<const __nv_bfloat16*>(X), M, d, ld,
+                                                                   eps, r);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- column reduce
+// Block = 32 columns x 8 row-groups; each thread sums a strided subset of the blocks in a
+// fixed order, then the 8 group sums are added in order (deterministic).
+__global__ void col_reduce_kernel(const float* __restrict__ parts, int64_t nblocks, int64_t N, int64_t ld,
+                                  float* __restrict__ out) {
+  __shared__ float red[8][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int64_t j = (int64_t)blockIdx.x * 32 + tx;
+  float s = 0.f;
+  if (j < N)
+    for (int64_t b = ty; b < nblocks; b += 8) s += __ldg(parts + b * ld + j);
+  red[ty][tx] = s;
+  __syncthreads();
+  if (ty == 0 && j < N) {
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t += red[k][tx];
+    out[j] = t;
+  }
+}
+
+cudaError_t launch_col_reduce(const float* parts, int64_t nblocks, int64_t N, int64_t ld, float* out,
+                              cudaStream_t s) {
+  const int64_t blocks = (N + 31) / 32;
+  col_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(parts, nblocks, N, ld, out);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- gain fold
+// W'[n, k] = bf16(W[n, k] * g[k]); 8 elements (16 bytes) per thread per step, grid-stride.
+__global__ void fold_gain_kernel(const __nv_bfloat16* __restrict__ W, int64_t N, int64_t K, int64_t ld_in,
+                                 const float* __restrict__ g, __nv_bfloat16* __restrict__ Wo, int64_t ld_out) {
+  const int64_t kv = K >> 3;
+  const int64_t total = N * kv;
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = v / kv, k = (v - n * kv) << 3;
+    const uint4 u = __ldcs(reinterpret_cast<const uint4*>(W + n * ld_in + k));
+    const float4 g0 = __ldg(reinterpret_cast<const float4*>(g + k));
+    const float4 g1 = __ldg(reinterpret_cast<const float4*>(g + k + 4));
+    const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = __uint_as_float(w[e] << 16) * gv[2 * e];
+      const float hi = __uint_as_float(w[e] & 0xFFFF0000u) * gv[2 * e + 1];
+      __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+      o[e] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    __stcs(reinterpret_cast<uint4*>(Wo + n * ld_out + k), make_uint4(o[0], o[1], o[2], o[3]));
+  }
+}
+
+// fp32 weights: 4 elements (16 bytes) per thread per step.
+__global__ void fold_gain_f32_kernel(const float* __restrict__ W, int64_t N, int64_t K, int64_t ld_in,
+                                     const float* __restrict__ g, float* __restrict__ Wo, int64_t ld_out) {
+  const int64_t kv = K >> 2;
+  const int64_t total = N * kv;
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = v / kv, k = (v - n * kv) << 2;
+    const float4 w = __ldcs(reinterpret_cast<const float4*>(W + n * ld_in + k));
+    const float4 gv = __ldg(reinterpret_cast<const float4*>(g + k));
+    __stcs(reinterpret_cast<float4*>(Wo + n * ld_out + k), make_float4(w.x * gv.x, w.y * gv.y, w.z * gv.z, w.w * gv.w));
+  }
+}
+
+cudaError_t launch_fold_gain(const void* W, int64_t N, int64_t K, int64_t ld_in, const float* g, void* W_out,
+                             int64_t ld_out, bool f32, cudaStream_t s, int sms) {
+  const int threads = 256;
+  const int64_t need = (N * (K >> (f32 ? 2 : 3)) + threads - 1) / threads;
+  const int64_t cap = (int64_t)sms * 8;
+  const int64_t blocks = need < cap ? need : cap;
+  if (blocks <= 0) return cudaSuccess;
+  if (f32)
+    fold_gain_f32_kernel<<<(unsigned)blocks, threads, 0, s>>>(static_cast<const float*>(W), N, K, ld_in, g,
+                                                               static_cast<float*>(W_out), ld_out);
+  else
+    fold_gain_kernel<<<(unsigned)blocks, threads, 0, s>>>(static_cast<const __nv_bfloat16*>(W), N, K, ld_in, g,
+                                                           static_cast<__nv_bfloat16*>(W_out), ld_out);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- RoPE table
+__global__ void rope_table_kernel(int seq_len, int half, double base, int head_dim, float* __restrict__ c,
+                                  float* __restrict__ s) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (int64_t)seq_len * half) return;
+  const int pos = (int)(idx / half), p = (int)(idx % half);
+  const double inv_freq = pow(base, -2.0 * (double)p / (double)head_dim);
+  double sn, cs;
+  sincos((double)pos * inv_freq, &sn, &cs);
+  c[idx] = (float)cs;
+  s[idx] = (float)sn;
+}
+
+cudaError_t launch_rope_table(int seq_len, int head_dim, double base, float* cos_out, float* sin_out,
+                              cudaStream_t s) {
+  const int half = head_dim / 2;
+  const int64_t n = (int64_t)seq_len * half;
+  const int threads = 256;
+  rope_table_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(seq_len, half, base, head_dim,
+                                                                                 cos_out, sin_out);
+  return cudaGetLastError();
+}
+
+}  // namespace coda

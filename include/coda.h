@@ -1,0 +1,299 @@
+/*
+ * coda.h — C ABI of the GB300 (sm_103a) GEMM-epilogue library (libcoda.so).
+ *
+ * What the library computes.  A GEMM whose output tile stays on chip while a short
+ * "epilogue program" runs on it before the single store to HBM; and the Transformer
+ * block chains built from such GEMMs, chiefly the reparameterised
+ * GEMM -> residual -> RMSNorm -> GEMM chain, in which the first GEMM emits per-row
+ * partial sums of squares, a light reduce turns them into the RMS scale r, and the second
+ * GEMM applies r per row because a per-row scalar commutes with the matmul.
+ *
+ * Sources (page title, section):
+ *   [KuCoin]     "CODA: new research optimizes Transformer training with GEMM-epilogue
+ *                programming" (kucoin.com news flash):
+ *                "CODA: «El epílogo» esconde un tesoro" (mainloop / epilogue split, the
+ *                deferred-r rewrite, partial RMS + light reduce, backward inherits the
+ *                structure), "Cinco «bloques» y un «lenguaje LEGO»" (the five epilogue
+ *                primitive kinds), "hoja de referencia" (coverage: RMSNorm, residual,
+ *                SwiGLU, RoPE, cross-entropy and their gradients; single GPU).
+ *   [Ecosistema] "CODA: Nuevo kernel GPU reduce costos de entrenamiento IA"
+ *                (ecosistemastartup.com), "¿Qué es GEMM-epilogue…?" (C = alpha*A*B + beta*C;
+ *                epilogue = scaling, bias, activation, residual add, precision cast).
+ *
+ * Conventions for every call.
+ *   - Memory: the caller owns every buffer.  Tensor pointers are DEVICE pointers on the
+ *     current CUDA device.  The library allocates no device memory in any call.
+ *   - Streams: every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream) and does not synchronise, except
+ *     coda_get_device_status, whose name says it reads the device.
+ *   - Errors: every call returns an int status (CODA_OK = 0 or a negative CODA_ERR_*).
+ *     Arguments are checked on the host before anything is launched; a rejected call has
+ *     launched nothing.  A wait inside a kernel that runs out of time (see
+ *     coda_set_watchdog_ms) ends that kernel early with wrong output and sets the device
+ *     status word, read by coda_get_device_status.
+ *   - Layout: a coda_tensor is a logical [rows, cols] matrix.  CODA_ROW_MAJOR stores
+ *     element (i, j) at ptr[i*ld + j]; CODA_COL_MAJOR at ptr[j*ld + i].  `ptr` must be
+ *     16-byte aligned and ld * element size a multiple of 16 bytes (CODA_ERR_ALIGN).
+ *   - Precision: bf16 and e4m3 operands, fp32 accumulation in tensor memory, one rounding
+ *     at the store; fp32 operands run on the tensor cores as tf32.
+ *   - Hardware: sm_103a (GB300) only.  Calls on any other device return CODA_ERR_NO_DEVICE.
+ */
+#ifndef CODA_H_
+#define CODA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CODA_API __attribute__((visibility("default")))
+#else
+#define CODA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ status codes */
+enum coda_status {
+  CODA_OK = 0,
+  CODA_ERR_NULL = -1,                /* a required pointer is NULL */
+  CODA_ERR_SHAPE = -2,               /* inconsistent or unsupported sizes */
+  CODA_ERR_ALIGN = -3,               /* base or leading dimension not 16-byte aligned */
+  CODA_ERR_DTYPE = -4,               /* unsupported dtype combination */
+  CODA_ERR_UNSUPPORTED_PROGRAM = -5, /* op list with no compiled epilogue */
+  CODA_ERR_LAUNCH = -6,              /* CUDA launch / descriptor encoding failed */
+  CODA_ERR_DEVICE_TIMEOUT = -7,      /* a kernel wait ran out of time (device status) */
+  CODA_ERR_NO_DEVICE = -8            /* no sm_103 device current, or driver entry missing */
+};
+
+enum coda_dtype { CODA_F32 = 0, CODA_BF16 = 1, CODA_E4M3 = 2 };
+enum coda_layout { CODA_ROW_MAJOR = 0, CODA_COL_MAJOR = 1 };
+
+typedef struct coda_tensor {
+  void* ptr;      /* device pointer, 16-byte aligned */
+  int32_t dtype;  /* enum coda_dtype */
+  int32_t layout; /* enum coda_layout */
+  int64_t rows;   /* logical rows */
+  int64_t cols;   /* logical columns */
+  int64_t ld;     /* leading dimension in elements (stride of the outer storage index) */
+} coda_tensor;
+
+/* ------------------------------------------------------------- epilogue programs
+ * An epilogue program is an ordered list of ops applied to the fp32 accumulator tile
+ * acc = A . W^T before the store.  Op kinds follow the five primitive kinds of
+ * [KuCoin, "Cinco bloques y un lenguaje LEGO"]: elementwise / pairwise transforms,
+ * vector loads (row or column vectors), matrix-block loads / stores (side inputs, saved
+ * activations), block reductions (partials), state (running amax).  The list must match
+ * one of the compiled programs below, else CODA_ERR_UNSUPPORTED_PROGRAM:
+ *
+ *   {}                                        out = acc
+ *   {COL_SCALE}                               out = acc * g[j]
+ *   {TENSOR_SCALE}                            out = s * acc
+ *   {ADD_SIDE [, ROW_SUMSQ_PARTIAL]}          out = acc + R; partials of out^2
+ *   {TENSOR_SCALE, ADD_SIDE [, ROW_SUMSQ_PARTIAL]}
+ *   {ROW_SCALE}                               out = r[i] * acc
+ *   {[TENSOR_SCALE,] ROW_SCALE, [STORE_AUX,] SWIGLU [, AMAX]}
+ *        W holds 2N rows (gate rows [0, N), up rows [N, 2N)); Z = s * r[i] * acc over
+ *        2N columns; out = silu(Z_gate) * Z_up (times out_scale); STORE_AUX saves Z.
+ *   {ROW_SCALE, ROPE}                         out = rope(r[i] * acc)
+ *   {SWIGLU_BWD, ROW_SCALE, ROW_DOT_PARTIAL}  acc = dA; with Z = [G | U] from aux_in:
+ *        out[:, j] = r dA U silu'(G),  out[:, N + j] = r dA silu(G)   (out is [M, 2N]);
+ *        row partials of sum_j out . Z
+ *   {RMSBWD_COMBINE, COL_DOT_PARTIAL}         acc = t; h = aux_in, dY = aux_in2:
+ *        out = g[j] t - c[i] h + dY; column partials of h * t
+ */
+enum coda_op {
+  CODA_OP_TENSOR_SCALE = 1,      /* acc *= side.tensor_scale */
+  CODA_OP_ROW_SCALE = 2,         /* acc[i, :] *= side.row_scale[i] */
+  CODA_OP_COL_SCALE = 3,         /* acc[:, j] *= side.col_scale[j] */
+  CODA_OP_ADD_SIDE = 4,          /* acc += side.residual[i, j] */
+  CODA_OP_SWIGLU = 5,            /* gate/up halves -> silu(gate) * up */
+  CODA_OP_ROPE = 6,              /* rotate adjacent pairs of the first rope_ncols columns */
+  CODA_OP_SWIGLU_BWD = 7,        /* SwiGLU backward (see above) */
+  CODA_OP_RMSBWD_COMBINE = 8,    /* RMSNorm backward combine (see above) */
+  CODA_OP_ROW_SUMSQ_PARTIAL = 9, /* aux.row_partials[t, i] = sum over tile t of out^2 */
+  CODA_OP_ROW_DOT_PARTIAL = 10,  /* aux.row_partials[t, i] = sum over tile t of out . Z */
+  CODA_OP_COL_DOT_PARTIAL = 11,  /* aux.col_partials[b, j] = sum over 32-row block b of h * t */
+  CODA_OP_AMAX = 12,             /* atomic max of |silu(gate) * up| into *aux.amax */
+  CODA_OP_STORE_AUX = 13         /* save the pre-activation Z to aux.store_aux */
+};
+
+#define CODA_MAX_OPS 8
+typedef struct coda_epilogue_program {
+  int32_t n_ops;
+  int32_t ops[CODA_MAX_OPS];
+} coda_epilogue_program;
+
+typedef struct coda_side_inputs {
+  const coda_tensor* residual;  /* ADD_SIDE: [M, N], ROW_MAJOR, dtype of out (bf16/f32) */
+  const float* row_scale;       /* ROW_SCALE: r [M] */
+  const float* row_coef;        /* RMSBWD_COMBINE: c [M] */
+  const float* col_scale;       /* COL_SCALE, RMSBWD_COMBINE: g [N], 16-byte aligned */
+  const coda_tensor* aux_in;    /* SWIGLU_BWD: Z [M, 2N] bf16; RMSBWD_COMBINE: h [M, N] bf16 */
+  const coda_tensor* aux_in2;   /* RMSBWD_COMBINE: dY [M, N] bf16 */
+  const float* rope_cos;        /* ROPE: [rope_seq_len, rope_head_dim / 2] fp32 */
+  const float* rope_sin;        /* ROPE: same shape */
+  int32_t rope_seq_len;         /* ROPE: position of row i is i mod rope_seq_len */
+  int32_t rope_head_dim;        /* ROPE: 32, 64, 128 or 256 */
+  int32_t rope_ncols;           /* ROPE: columns [0, rope_ncols) rotated; multiple of head_dim */
+  float tensor_scale;           /* TENSOR_SCALE: s (e.g. s_x * s_w for fp8) */
+  float out_scale;              /* e4m3 output of SWIGLU: multiply by this (1 / s_a) before the cast */
+} coda_side_inputs;
+
+typedef struct coda_aux_outputs {
+  float* row_partials;          /* [ceil(N / 256), row_partials_ld] (SWIGLU_BWD: tiles of dA) */
+  int64_t row_partials_ld;      /* >= M */
+  float* col_partials;          /* [4 * ceil(M / 128), col_partials_ld] */
+  int64_t col_partials_ld;      /* >= N */
+  const coda_tensor* store_aux; /* STORE_AUX: Z [M, 2N] bf16 */
+  float* amax;                  /* AMAX: one float; the caller zeroes it before the call */
+} coda_aux_outputs;
+
+/* out = epilogue(prog, A . W^T).
+ *   A    logical [M, K]: ROW_MAJOR (K contiguous) or COL_MAJOR (M contiguous).
+ *   W    logical [N, K] (nn.Linear [out, in] layout when ROW_MAJOR); [2N, K] for SWIGLU.
+ *   out  logical [M, N] ROW_MAJOR ([M, 2N] for SWIGLU_BWD).
+ * Operand dtypes: bf16 x bf16, e4m3 x e4m3 (ROW_MAJOR only), f32 x f32 (tf32, ROW_MAJOR
+ * only).  N must be a multiple of 32 (of 128 for SWIGLU), K >= 1.  M = 0 or N = 0 is a
+ * no-op.  `side` and `aux` may be NULL when the program needs none of their fields. */
+CODA_API int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_epilogue_program* prog,
+                       const coda_side_inputs* side, const coda_tensor* out, const coda_aux_outputs* aux,
+                       void* stream);
+
+/* The light row reduce [KuCoin, "El epílogo esconde un tesoro"].
+ *   partials: fp32 [nparts, ld] (part t of row i at partials[t*ld + i]), summed in t order.
+ *   mode CODA_REDUCE_RSQRT_MEAN: out[i] = 1 / sqrt(sum_t P[t, i] / d + eps)   (r)
+ *   mode CODA_REDUCE_SCALE_SUM:  out[i] = rowscale[i] * sum_t P[t, i] / d     (c = r s / d) */
+enum coda_reduce_mode { CODA_REDUCE_RSQRT_MEAN = 0, CODA_REDUCE_SCALE_SUM = 1 };
+CODA_API int coda_rms_partial_reduce(const float* partials, int64_t ld, int32_t nparts, int64_t M, int64_t d, float eps,
+                            int32_t mode, const float* rowscale, float* out, void* stream);
+
+/* Full-row RMS scale: r[i] = 1 / sqrt(mean_j X[i, j]^2 + eps) for X bf16 [M, d] ROW_MAJOR. */
+CODA_API int coda_row_rms(const coda_tensor* X, float eps, float* r_out, void* stream);
+
+/* Column reduce: out[j] = sum_b parts[b*ld + j] over b in [0, nblocks) (fixed order). */
+CODA_API int coda_col_reduce(const float* parts, int64_t nblocks, int64_t N, int64_t ld, float* out, void* stream);
+
+/* Gain fold W'[n, k] = W[n, k] * g[k] (bf16 -> bf16 or fp32 -> fp32, ROW_MAJOR [N, K]); the RMSNorm
+ * gain moved onto the weight of the GEMM that follows the norm.  W_out may alias W. */
+CODA_API int coda_fold_gain(const coda_tensor* W, const float* g, const coda_tensor* W_out, void* stream);
+
+/* RoPE table: cos/sin[pos, p] = cos/sin(pos * base^(-2p / head_dim)), fp32
+ * [seq_len, head_dim / 2], angles evaluated in fp64 on the device. */
+CODA_API int coda_rope_table(int32_t seq_len, int32_t head_dim, double base, float* cos_out, float* sin_out, void* stream);
+
+/* ------------------------------------------------------------ block chains
+ * LLaMA-style block tail, hidden H, FFN width F, M tokens, bf16, weights [out, in]:
+ *   h = O W_o^T + R;  r = rms(h);  [G | U] = r (h W_gu'^T);  a = silu(G) U;  Y = a W_d^T + h
+ * W_gu' is the gate/up weight with the RMSNorm gain folded in (coda_fold_gain). */
+typedef struct coda_block_fwd {
+  int64_t M, H, F;
+  float eps;
+  const void* O;        /* [M, H] bf16 */
+  const void* R;        /* [M, H] bf16 residual stream input */
+  const void* W_o;      /* [H, H] bf16 */
+  const void* W_gu;     /* [2F, H] bf16, gain folded, gate rows first */
+  const void* W_d;      /* [H, F] bf16 */
+  void* h;              /* out [M, H] bf16 */
+  float* r;             /* out [M] fp32 */
+  void* a;              /* out [M, F] bf16 */
+  void* Y;              /* out [M, H] bf16 */
+  void* Z;              /* optional out [M, 2F] bf16: saved [G | U] (training); NULL = not saved */
+  float* Y_partials;    /* optional out [H/256, M] fp32: partial sums of squares of Y; NULL = none */
+  float* workspace;     /* [H/256, M] fp32 scratch for the partials of h */
+} coda_block_fwd;
+CODA_API int coda_block_forward(const coda_block_fwd* io, void* stream);
+
+/* Backward of coda_block_forward (plain-chain gradients in fused form):
+ *   e = r [dA U silu'(G) | dA silu(G)] with dA = dY W_d;  s_i = sum e . Z;  c = r s / H
+ *   t = e W_gu;  dh = g t - c h + dY (= dR);  dg = sum_rows h t;  dO = dh W_o
+ *   dW_d = dY^T a;  dW_gu[n, k] = g_k (e^T h)[n, k];  dW_o = dh^T O
+ * W_gu here is the UNFOLDED gate/up weight (the model parameter itself, not the folded copy
+ * the forward reads) and g the RMSNorm gain; dW_gu is the gradient of
+ * that unfolded weight.  Weight gradients and dg are fp32; activation gradients bf16. */
+typedef struct coda_block_bwd {
+  int64_t M, H, F;
+  const void* O;       /* [M, H] bf16 */
+  const void* W_o;     /* [H, H] bf16 */
+  const void* W_gu;    /* [2F, H] bf16, unfolded */
+  const void* W_d;     /* [H, F] bf16 */
+  const float* g;      /* [H] RMSNorm gain */
+  const void* h;       /* saved by the forward: [M, H] bf16 */
+  const float* r;      /* [M] */
+  const void* Z;       /* [M, 2F] bf16 ([G | U], post-r) */
+  const void* a;       /* [M, F] bf16 */
+  const void* dY;      /* [M, H] bf16 */
+  void* e;             /* out [M, 2F] bf16 */
+  void* dh;            /* out [M, H] bf16 (also dR) */
+  void* dO;            /* out [M, H] bf16 */
+  float* dW_o;         /* out [H, H] */
+  float* dW_gu;        /* out [2F, H] */
+  float* dW_d;         /* out [H, F] */
+  float* dg;           /* out [H] */
+  float* c;            /* out [M] */
+  float* workspace;    /* coda_workspace_size(CODA_WS_BLOCK_BWD, ...) bytes */
+} coda_block_bwd;
+CODA_API int coda_block_backward(const coda_block_bwd* io, void* stream);
+
+/* QKV projection with the deferred input-RMSNorm scale and RoPE on Q and K:
+ *   QKV = rope(r (h W_qkv'^T)), pos = row mod seq_len, r = rms(h) computed here. */
+typedef struct coda_qkv_rope_io {
+  int64_t M, H, N;           /* N = (n_q + 2 n_kv) * head_dim */
+  int32_t seq_len, head_dim, rope_ncols;   /* rope_ncols = (n_q + n_kv) * head_dim */
+  float eps;
+  const void* h;             /* [M, H] bf16 */
+  const void* W_qkv;         /* [N, H] bf16, gain folded */
+  const float* rope_cos; const float* rope_sin;   /* coda_rope_table */
+  float* r;                  /* out [M] */
+  void* out;                 /* out [M, N] bf16 */
+} coda_qkv_rope_io;
+CODA_API int coda_qkv_rope(const coda_qkv_rope_io* io, void* stream);
+
+/* FP8 (e4m3, per-tensor fp32 scales) MLP with deferred r:
+ *   Z = r s_x s_w (X_q W_q^T);  a = silu(Z_gate) Z_up;  a_q = e4m3(a / s_a);  amax = max|a|
+ *   Y = s_a s_wd (a_q W_dq^T) + h;  Y_partials = partial sums of squares of Y. */
+typedef struct coda_mlp_fp8_io {
+  int64_t M, H, F;
+  float eps, s_x, s_w, s_wd, s_a;
+  const void* h;             /* [M, H] bf16: residual input, and source of r */
+  const void* X_q;           /* [M, H] e4m3 */
+  const void* W_q;           /* [2F, H] e4m3 */
+  const void* W_dq;          /* [H, F] e4m3 */
+  float* r;                  /* out [M] */
+  void* a_q;                 /* out [M, F] e4m3 */
+  float* amax;               /* out: 1 float (zeroed by this call on the stream) */
+  void* Y;                   /* out [M, H] bf16 */
+  float* Y_partials;         /* out [H/256, M] fp32 */
+} coda_mlp_fp8_io;
+CODA_API int coda_mlp_fp8(const coda_mlp_fp8_io* io, void* stream);
+
+/* Bytes of fp32 scratch a chain needs (caller allocates). */
+enum coda_workspace_kind { CODA_WS_BLOCK_FWD = 0, CODA_WS_BLOCK_BWD = 1 };
+CODA_API size_t coda_workspace_size(int32_t which, int64_t M, int64_t H, int64_t F);
+
+/* ------------------------------------------------------------------ device status
+ * Synchronises `stream`, then reads and clears the current device's status word.
+ * *site receives 0 or the site code of the first kernel wait that ran out of time
+ * (1 producer / empty stage, 2 MMA / free accumulator, 3 MMA / full stage,
+ * 4 epilogue / accumulator, 5 epilogue / side input).  Returns CODA_OK,
+ * CODA_ERR_DEVICE_TIMEOUT, or CODA_ERR_LAUNCH if the stream itself reports an error. */
+CODA_API int coda_get_device_status(void* stream, int32_t* site);
+
+/* Per-wait time limit of every kernel wait (default 2000 ms, or CODA_WATCHDOG_MS). */
+CODA_API int coda_set_watchdog_ms(uint32_t ms);
+
+/* Test hook for the watchdog: when set, the next coda_gemm_epilogue call makes its
+ * producer drop one k-block, so the MMA wait runs out of time and the kernel returns
+ * through the abort path.  Cleared after one call. */
+CODA_API int coda_inject_dropped_stage(int32_t enable);
+
+/* Number of SMs of the current device and the library's build tag. */
+CODA_API int coda_device_sm_count(int32_t* sms);
+CODA_API const char* coda_status_string(int status);
+CODA_API const char* coda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CODA_H_ */

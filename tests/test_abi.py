@@ -1,0 +1,123 @@
+"""The C ABI without a GPU: the library loads, exports every function include/coda.h
+declares, and rejects bad arguments on the host before touching a device.  No compute call
+runs here; a well-formed call on a machine without an sm_103 device returns
+CODA_ERR_NO_DEVICE (there is no CPU fallback)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gemm_epilogue_transformer_tcgen05_gb300 import coda as C
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "coda.h")) as f:
+        txt = f.read()
+    return sorted(set(re.findall(r"CODA_API\s+[\w\s\*]+?\b(coda_\w+)\s*\(", txt)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(C.LIB_PATH):
+        from gemm_epilogue_transformer_tcgen05_gb300 import build
+        build.build()
+    return C.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert len(names) >= 17
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(C.EXPORTED)
+
+
+def test_status_strings_and_version(L):
+    assert C.version().startswith("coda-gb300")
+    for s in range(-8, 1):
+        assert C.status_string(s) != "unknown status"
+    assert C.status_string(-99) == "unknown status"
+
+
+def test_workspace_sizes(L):
+    assert C.coda_workspace_size(C.WS_BLOCK_FWD, 16384, 2048, 8192) == 8 * 16384 * 4
+    assert C.coda_workspace_size(C.WS_BLOCK_BWD, 16384, 2048, 8192) == (32 * 16384 + 512 * 2048) * 4
+    assert C.coda_workspace_size(7, 1, 1, 1) == 0
+
+
+def _t(ptr, dtype, rows, cols, ld, layout=C.ROW_MAJOR):
+    return C.CodaTensor(ctypes.c_void_p(ptr), dtype, layout, rows, cols, ld)
+
+
+def _call(A, W, ops, out, side=None, aux=None):
+    p = C.program(*ops)
+    return C.lib().coda_gemm_epilogue(ctypes.byref(A) if A else None, ctypes.byref(W) if W else None,
+                                      ctypes.byref(p), ctypes.byref(side) if side else None,
+                                      ctypes.byref(out) if out else None, ctypes.byref(aux) if aux else None, None)
+
+
+FAKE = 0x10000   # never dereferenced: every check below fails before any device access
+
+
+def test_host_validation_codes(L):
+    A = _t(FAKE, C.BF16, 256, 512, 512)
+    W = _t(FAKE, C.BF16, 256, 512, 512)
+    out = _t(FAKE, C.BF16, 256, 256, 256)
+    assert _call(None, W, [], out) == C.ERR_NULL
+    assert _call(A, W, [C.OP_ROW_SUMSQ_PARTIAL, C.OP_ADD_SIDE], out) == C.ERR_UNSUPPORTED_PROGRAM
+    assert _call(A, W, [C.OP_SWIGLU, C.OP_ROW_SCALE], out) == C.ERR_UNSUPPORTED_PROGRAM
+    assert _call(A, _t(FAKE, C.BF16, 256, 256, 512), [], out) == C.ERR_SHAPE         # K mismatch
+    assert _call(A, W, [], _t(FAKE, C.BF16, 256, 128, 256)) == C.ERR_SHAPE          # N mismatch
+    assert _call(_t(FAKE + 8, C.BF16, 256, 512, 512), W, [], out) == C.ERR_ALIGN    # base
+    assert _call(_t(FAKE, C.BF16, 256, 500, 500), _t(FAKE, C.BF16, 256, 500, 500), [], out) == C.ERR_ALIGN
+    assert _call(A, _t(FAKE, C.F32, 256, 512, 512), [], out) == C.ERR_DTYPE          # mixed operands
+    assert _call(A, W, [C.OP_ROW_SCALE], out) == C.ERR_NULL                          # r missing
+    assert _call(A, W, [C.OP_ADD_SIDE], out) == C.ERR_NULL                           # residual missing
+    swo = _t(FAKE, C.BF16, 256, 200, 200)                                            # SWIGLU N % 128
+    assert _call(A, _t(FAKE, C.BF16, 400, 512, 512), [C.OP_SWIGLU], swo) == C.ERR_SHAPE
+    empty = _t(0, C.BF16, 0, 512, 512)
+    assert _call(empty, W, [], _t(0, C.BF16, 0, 256, 256)) == C.OK                   # M = 0: no-op
+
+
+def test_well_formed_call_without_device_is_refused(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    A = _t(FAKE, C.BF16, 256, 512, 512)
+    W = _t(FAKE, C.BF16, 256, 512, 512)
+    out = _t(FAKE, C.BF16, 256, 256, 256)
+    assert _call(A, W, [], out) == C.ERR_NO_DEVICE
+    n = ctypes.c_int32(0)
+    assert L.coda_device_sm_count(ctypes.byref(n)) == C.ERR_NO_DEVICE
+
+
+def test_other_entry_points_validate(L):
+    assert L.coda_rms_partial_reduce(None, 1, 1, 1, 1, 1e-6, 0, None, None, None) == C.ERR_NULL
+    assert L.coda_rms_partial_reduce(ctypes.c_void_p(FAKE), 4, 1, 8, 1, 1e-6, 0, None, ctypes.c_void_p(FAKE),
+                                     None) == C.ERR_SHAPE                              # ld < M
+    assert L.coda_rms_partial_reduce(ctypes.c_void_p(FAKE), 8, 1, 8, 1, 1e-6, 1, None, ctypes.c_void_p(FAKE),
+                                     None) == C.ERR_NULL                               # SCALE_SUM needs r
+    assert L.coda_col_reduce(None, 1, 1, 1, None, None) == C.ERR_NULL
+    assert L.coda_rope_table(0, 64, 1e4, ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), None) == C.ERR_SHAPE
+    W = _t(FAKE, C.BF16, 16, 12, 12)
+    assert L.coda_fold_gain(ctypes.byref(W), ctypes.c_void_p(FAKE), ctypes.byref(W), None) == C.ERR_ALIGN
+    assert L.coda_block_forward(None, None) == C.ERR_NULL
+    assert L.coda_block_backward(None, None) == C.ERR_NULL
+    assert L.coda_qkv_rope(None, None) == C.ERR_NULL
+    assert L.coda_mlp_fp8(None, None) == C.ERR_NULL
+    assert L.coda_set_watchdog_ms(0) == C.ERR_SHAPE
+    assert L.coda_get_device_status(None, None) == C.ERR_NULL
+
+
+def test_binding_reads_layout_from_strides():
+    import torch
+    x = torch.empty((64, 32), dtype=torch.bfloat16)
+    d = C.desc(x)
+    assert (d.layout, d.rows, d.cols, d.ld) == (C.ROW_MAJOR, 64, 32, 32)
+    d = C.desc(x.t())
+    assert (d.layout, d.rows, d.cols, d.ld) == (C.COL_MAJOR, 32, 64, 32)
+    with pytest.raises(ValueError):
+        C.desc(torch.empty((4, 4, 4)))

@@ -1,0 +1,275 @@
+"""GPU parity of the chains (tiny fp32 chain, LLaMA-shaped block forward / backward, QKV +
+RoPE, fp8 MLP) against the fp64 oracle, through the C ABI.
+
+Reduced sizes compare every output element; the full 16384-token sizes (the launch
+configuration the bench times) compare sampled token rows (rows 0-255 plus 256 random
+rows: forward rows are independent, so the oracle computes exactly those rows) and, for
+weight gradients, sampled columns over all rows."""
+import numpy as np
+import pytest
+import torch
+
+import coda_synth as S
+import oracle as O
+from tests import storage_sim as SIM
+from tests.gpu_helpers import (TOL_BF16, TOL_FP8, assert_close, assert_e4m3_codes, assert_product_close, dev, f64,
+                               fresh_status)
+
+pytestmark = pytest.mark.gpu
+BF = torch.bfloat16
+
+
+@pytest.fixture(scope="module")
+def C():
+    from gemm_epilogue_transformer_tcgen05_gb300 import coda
+    coda.lib()
+    coda.coda_set_watchdog_ms(2000)
+    return coda
+
+
+def sample_rows(M, seed=0):
+    rng = np.random.default_rng(seed)
+    extra = rng.choice(np.arange(256, M), size=min(256, max(M - 256, 0)), replace=False)
+    return np.sort(np.concatenate([np.arange(min(256, M)), extra]))
+
+
+# --------------------------------------------------------------------- tiny fp32 chain
+def test_tiny_fp32_chain(C):
+    t = S.tiny_chain_inputs()
+    X, R, W1, W2, g = (t[k] for k in ("X", "R", "W1", "W2", "g"))
+    M, d = X.shape
+    n2 = W2.shape[1]
+    W1t, W2t = dev(W1.t().contiguous()), dev(W2.t().contiguous())   # [out, in] weights
+    h = torch.empty((M, d), dtype=torch.float32, device="cuda")
+    P = torch.empty((1, M), dtype=torch.float32, device="cuda")
+    C.coda_gemm_epilogue(dev(X), W1t, [C.OP_ADD_SIDE, C.OP_ROW_SUMSQ_PARTIAL], h, residual=dev(R), row_partials=P)
+    r = torch.empty((M,), dtype=torch.float32, device="cuda")
+    C.coda_rms_partial_reduce(P, M, d, t["eps"], r)
+    W2f = torch.empty_like(W2t)
+    C.coda_fold_gain(W2t, dev(g), W2f)
+    out = torch.empty((M, n2), dtype=torch.float32, device="cuda")
+    C.coda_gemm_epilogue(h, W2f, [C.OP_ROW_SCALE], out, row_scale=r)
+    torch.cuda.synchronize()
+    fresh_status()
+    ref = O.tiny_chain(f64(X), f64(R), f64(W1), f64(W2), f64(g), t["eps"])
+    assert_close(f64(h), ref["h"], TOL_BF16, "h")
+    assert_close(f64(r), ref["r"], TOL_BF16, "r")
+    assert_close(f64(out), ref["out"], TOL_BF16, "out")
+
+
+# --------------------------------------------------------------------- block forward
+def _run_block_forward(C, inp, train=True):
+    O_, R, W_o, W_gu, W_d, g = (dev(inp[k]) for k in ("O", "R", "W_o", "W_gu", "W_d", "g"))
+    M, H = O_.shape
+    F = W_d.shape[1]
+    Wf = torch.empty_like(W_gu)
+    C.coda_fold_gain(W_gu, g, Wf)
+    out = dict(h=torch.empty((M, H), dtype=BF, device="cuda"), r=torch.empty((M,), device="cuda"),
+               a=torch.empty((M, F), dtype=BF, device="cuda"), Y=torch.empty((M, H), dtype=BF, device="cuda"),
+               Z=torch.empty((M, 2 * F), dtype=BF, device="cuda") if train else None,
+               Yp=torch.empty(((H + 255) // 256, M), device="cuda"))
+    ws = torch.empty((C.coda_workspace_size(C.WS_BLOCK_FWD, M, H, F) // 4,), device="cuda")
+    C.coda_block_forward(O_, R, W_o, Wf, W_d, inp["eps"], out["h"], out["r"], out["a"], out["Y"], ws, Z=out["Z"],
+                         Y_partials=out["Yp"])
+    torch.cuda.synchronize()
+    fresh_status()
+    return out, Wf
+
+
+def _oracle_forward_rows(inp, rows):
+    x = {k: f64(inp[k]) for k in ("O", "R", "W_o", "W_gu", "W_d", "g")}
+    return O.block_forward(x["O"][rows], x["R"][rows], x["W_o"], x["g"], x["W_gu"], x["W_d"], inp["eps"])
+
+
+def _sim_forward_rows(inp, rows):
+    x = {k: f64(inp[k]) for k in ("O", "R", "W_o", "W_gu", "W_d", "g")}
+    return SIM.block_forward(x["O"][rows], x["R"][rows], x["W_o"], x["g"], x["W_gu"], x["W_d"], inp["eps"])
+
+
+@pytest.mark.parametrize("M,H,F", [(640, 512, 1024), (300, 256, 384)])
+def test_block_forward_small(C, M, H, F):
+    inp = S.block_inputs(M, H, F, seed=0)
+    out, _ = _run_block_forward(C, inp)
+    ref = _oracle_forward_rows(inp, np.arange(M))
+    sim = _sim_forward_rows(inp, np.arange(M))
+    for k in ("h", "r", "Y"):
+        assert_close(f64(out[k]), ref[k], TOL_BF16, k)
+    assert_product_close(f64(out["a"]), ref["a"], sim["a"], "a")
+    assert_close(f64(out["Z"]), ref["Z"], TOL_BF16, "Z")
+    assert_close(f64(out["Yp"]), O.partial_sumsq(ref["Y"], 256), TOL_BF16, "Y partials")
+
+
+@pytest.mark.slow
+def test_block_forward_full_size_sampled_rows(C):
+    M, H, F = 16384, 2048, 8192
+    inp = S.block_inputs(M, H, F, seed=0)
+    out, _ = _run_block_forward(C, inp, train=False)
+    rows = sample_rows(M)
+    ref = _oracle_forward_rows(inp, rows)
+    sim = _sim_forward_rows(inp, rows)
+    for k in ("h", "r", "Y"):
+        assert_close(f64(out[k])[rows], ref[k], TOL_BF16, k)
+    assert_product_close(f64(out["a"])[rows], ref["a"], sim["a"], "a")
+
+
+# --------------------------------------------------------------------- block backward
+def _run_block_backward(C, inp, fwd_out):
+    O_, W_o, W_gu, W_d, g, dY = (dev(inp[k]) for k in ("O", "W_o", "W_gu", "W_d", "g", "dY"))
+    M, H = O_.shape
+    F = W_d.shape[1]
+    o = dict(e=torch.empty((M, 2 * F), dtype=BF, device="cuda"), dh=torch.empty((M, H), dtype=BF, device="cuda"),
+             dO=torch.empty((M, H), dtype=BF, device="cuda"), dW_o=torch.empty((H, H), device="cuda"),
+             dW_gu=torch.empty((2 * F, H), device="cuda"), dW_d=torch.empty((H, F), device="cuda"),
+             dg=torch.empty((H,), device="cuda"), c=torch.empty((M,), device="cuda"))
+    ws = torch.empty((C.coda_workspace_size(C.WS_BLOCK_BWD, M, H, F) // 4,), device="cuda")
+    C.coda_block_backward(O_, W_o, W_gu, W_d, g, fwd_out["h"], fwd_out["r"], fwd_out["Z"], fwd_out["a"], dY,
+                          o["e"], o["dh"], o["dO"], o["dW_o"], o["dW_gu"], o["dW_d"], o["dg"], o["c"], ws)
+    torch.cuda.synchronize()
+    fresh_status()
+    return o
+
+
+@pytest.mark.parametrize("M,H,F", [(640, 512, 1024), (300, 256, 384)])
+def test_block_backward_small(C, M, H, F):
+    inp = S.block_inputs(M, H, F, seed=0, with_grad=True)
+    fwd, _ = _run_block_forward(C, inp)
+    got = _run_block_backward(C, inp, fwd)
+    x = {k: f64(inp[k]) for k in ("O", "R", "W_o", "W_gu", "W_d", "g", "dY")}
+    ref_f = O.block_forward(x["O"], x["R"], x["W_o"], x["g"], x["W_gu"], x["W_d"], inp["eps"])
+    ref = O.block_backward(ref_f, x["O"], x["W_o"], x["g"], x["W_gu"], x["W_d"], x["dY"])
+    fused = O.block_backward_fused(ref_f, x["O"], x["W_o"], x["g"], x["W_gu"], x["W_d"], x["dY"])
+    sf = SIM.block_forward(x["O"], x["R"], x["W_o"], x["g"], x["W_gu"], x["W_d"], inp["eps"])
+    sb = SIM.block_backward(sf, x["O"], x["W_o"], x["g"], x["W_gu"], x["W_d"], x["dY"])
+    assert_product_close(f64(got["e"]), fused["e"], sb["e"], "e")
+    assert_close(f64(got["c"]), fused["c"], TOL_BF16, "c")
+    for k in ("dh", "dO", "dW_o", "dg"):
+        assert_close(f64(got[k]), ref[k], TOL_BF16, k)
+    for k in ("dW_gu", "dW_d"):
+        assert_product_close(f64(got[k]), ref[k], sb[k], k)
+
+
+@pytest.mark.slow
+def test_block_backward_full_size_sampled(C):
+    M, H, F = 16384, 2048, 8192
+    inp = S.block_inputs(M, H, F, seed=0, with_grad=True)
+    fwd, _ = _run_block_forward(C, inp)
+    got = _run_block_backward(C, inp, fwd)
+    x = {k: f64(inp[k]) for k in ("O", "R", "W_o", "W_gu", "W_d", "g", "dY")}
+    eps = inp["eps"]
+    # row-local outputs on sampled rows
+    rows = sample_rows(M, seed=1)
+    rf = O.block_forward(x["O"][rows], x["R"][rows], x["W_o"], x["g"], x["W_gu"], x["W_d"], eps)
+    rb = O.block_backward_fused(rf, x["O"][rows], x["W_o"], x["g"], x["W_gu"], x["W_d"], x["dY"][rows])
+    sf = SIM.block_forward(x["O"][rows], x["R"][rows], x["W_o"], x["g"], x["W_gu"], x["W_d"], eps)
+    sb = SIM.block_backward(sf, x["O"][rows], x["W_o"], x["g"], x["W_gu"], x["W_d"], x["dY"][rows])
+    for k in ("dh", "dO", "c"):
+        assert_close(f64(got[k])[rows], rb[k], TOL_BF16, k)
+    assert_product_close(f64(got["e"])[rows], rb["e"], sb["e"], "e")
+    # weight gradients on sampled columns, summed over all rows (oracle, and the bf16-storage
+    # model of the same columns)
+    cols = np.sort(np.random.default_rng(2).choice(F, size=64, replace=False))
+    dA = x["dY"] @ x["W_d"][:, cols]
+    h = O.linear(x["O"], x["W_o"]) + x["R"]
+    r = O.rms_scale(h, eps)
+    Wf = O.fold_gain(x["W_gu"], x["g"])
+    G, U = r[:, None] * (h @ Wf[cols].T), r[:, None] * (h @ Wf[F + cols].T)
+    ref_dWd = x["dY"].T @ O.swiglu(G, U)
+    ref_dWgu = x["g"][None, :] * ((r[:, None] * dA * U * O.silu_grad(G)).T @ h)
+    hs = SIM.bf(h)
+    rs = SIM.f32(1.0 / np.sqrt(np.mean(hs * hs, axis=1) + eps))
+    Wfs = SIM.bf(Wf)
+    Gs, Us = SIM.bf(rs[:, None] * (hs @ Wfs[cols].T)), SIM.bf(rs[:, None] * (hs @ Wfs[F + cols].T))
+    sim_dWd = x["dY"].T @ SIM.bf(O.swiglu(Gs, Us))
+    sim_dWgu = x["g"][None, :] * (SIM.bf(rs[:, None] * dA * Us * O.silu_grad(Gs)).T @ hs)
+    assert_product_close(f64(got["dW_d"])[:, cols], ref_dWd, sim_dWd, "dW_d[:, cols]")
+    assert_product_close(f64(got["dW_gu"])[cols], ref_dWgu, sim_dWgu, "dW_gu[cols]")
+
+
+# --------------------------------------------------------------------- QKV + RoPE
+def _run_qkv(C, inp, seq, hd, n_rot):
+    h, W, g = dev(inp["h"]), dev(inp["W_qkv"]), dev(inp["g"])
+    M, H = h.shape
+    N = W.shape[0]
+    Wf = torch.empty_like(W)
+    C.coda_fold_gain(W, g, Wf)
+    cos = torch.empty((seq, hd // 2), device="cuda")
+    sin = torch.empty_like(cos)
+    C.coda_rope_table(seq, hd, 500000.0, cos, sin)
+    r = torch.empty((M,), device="cuda")
+    out = torch.empty((M, N), dtype=BF, device="cuda")
+    C.coda_qkv_rope(h, Wf, inp["eps"], seq, hd, n_rot, cos, sin, r, out)
+    torch.cuda.synchronize()
+    fresh_status()
+    return out, r
+
+
+def test_qkv_rope_small(C):
+    M, H, seq, hd = 512, 256, 128, 64
+    inp = S.qkv_inputs(M, H, (4 + 2 * 2) * hd, seed=0)
+    out, r = _run_qkv(C, inp, seq, hd, (4 + 2) * hd)
+    ref = O.qkv_rope(f64(inp["h"]), f64(inp["g"]), f64(inp["W_qkv"]), inp["eps"], seq, (4 + 2) * hd, hd, 500000.0)
+    assert_close(f64(r), ref["r"], TOL_BF16, "r")
+    assert_close(f64(out), ref["out"], TOL_BF16, "qkv")
+
+
+@pytest.mark.slow
+def test_qkv_rope_full_size_sampled_rows(C):
+    M, H, seq, hd = 16384, 2048, 1024, 64
+    inp = S.qkv_inputs(M, H, 3072, seed=0)
+    out, r = _run_qkv(C, inp, seq, hd, 2560)
+    rows = sample_rows(M, seed=3)
+    hq = f64(inp["h"])[rows]
+    y = O.rmsnorm(hq, f64(inp["g"]), inp["eps"]) @ f64(inp["W_qkv"]).T
+    ref = O.rope_rotate(y, rows % seq, 2560, hd, 500000.0)
+    assert_close(f64(out)[rows], ref, TOL_BF16, "qkv rows")
+
+
+# --------------------------------------------------------------------- FP8 MLP
+def _run_fp8(C, inp, s_a):
+    h, Xq, Wq, Wdq = dev(inp["h"]), dev(inp["Xq"]), dev(inp["Wq"]), dev(inp["Wdq"])
+    M, H = h.shape
+    F = Wdq.shape[1]
+    r = torch.empty((M,), device="cuda")
+    aq = torch.empty((M, F), dtype=torch.uint8, device="cuda")
+    amax = torch.empty((1,), device="cuda")
+    Y = torch.empty((M, H), dtype=BF, device="cuda")
+    P = torch.empty(((H + 255) // 256, M), device="cuda")
+    C.coda_mlp_fp8(h, Xq, Wq, Wdq, inp["s_x"], inp["s_w"], inp["s_wd"], s_a, inp["eps"], r, aq, amax, Y, P)
+    torch.cuda.synchronize()
+    fresh_status()
+    return r, aq, amax, Y, P
+
+
+def _fp8_oracle(inp, rows, s_a):
+    return O.mlp_fp8(f64(inp["h"])[rows], f64(inp["Xq"])[rows], inp["s_x"], f64(inp["Wq"]), inp["s_w"],
+                     f64(inp["Wdq"]), inp["s_wd"], s_a, inp["eps"], 256)
+
+
+def _fp8_checks(inp, rows, r, aq, Y, P, s_a, ref):
+    assert_close(f64(r)[rows], ref["r"], TOL_BF16, "r")
+    assert_e4m3_codes(aq.cpu().numpy()[rows], ref["a"] / s_a, "a_q codes")
+    assert_close(f64(Y)[rows], ref["Y"], TOL_FP8, "Y")
+    assert_close(f64(P)[:, rows], ref["P"], TOL_FP8, "Y partials")
+
+
+def test_fp8_mlp_small(C):
+    M, H, F = 512, 512, 768
+    inp = S.fp8_mlp_inputs(M, H, F, seed=0)
+    rows = np.arange(M)
+    s_a = float(_fp8_oracle(inp, rows, 1.0)["amax"]) / 448.0   # delayed scaling from a prior pass
+    r, aq, amax, Y, P = _run_fp8(C, inp, s_a)
+    ref = _fp8_oracle(inp, rows, s_a)
+    _fp8_checks(inp, rows, r, aq, Y, P, s_a, ref)
+    np.testing.assert_allclose(float(amax.item()), ref["amax"], rtol=2e-2)
+
+
+@pytest.mark.slow
+def test_fp8_mlp_full_size_sampled_rows(C):
+    M, H, F = 16384, 4096, 14336
+    inp = S.fp8_mlp_inputs(M, H, F, seed=0)
+    rows = sample_rows(M, seed=4)
+    s_a = 4.0 * float(_fp8_oracle(inp, rows[:64], 1.0)["amax"]) / 448.0
+    r, aq, amax, Y, P = _run_fp8(C, inp, s_a)
+    ref = _fp8_oracle(inp, rows, s_a)
+    _fp8_checks(inp, rows, r, aq, Y, P, s_a, ref)
+    assert float(amax.item()) >= ref["amax"] * (1 - 2e-2)
