@@ -36,8 +36,9 @@ EXPORTED = [
     "coda_gemm_epilogue", "coda_rms_partial_reduce", "coda_row_rms", "coda_col_reduce", "coda_fold_gain",
     "coda_rope_table", "coda_block_forward", "coda_block_backward", "coda_qkv_rope", "coda_mlp_fp8",
     "coda_workspace_size", "coda_get_device_status", "coda_set_watchdog_ms", "coda_inject_dropped_stage",
-    "coda_device_sm_count", "coda_status_string", "coda_version",
+    "coda_device_sm_count", "coda_status_string", "coda_version", "coda_block_forward_noalloc",
 ]
+NOALLOC_MAX_PARTIALS = 1 << 20
 
 
 class CodaLibraryError(RuntimeError):
@@ -125,6 +126,7 @@ def lib():
         "coda_fold_gain": [P(CodaTensor), c_void_p, P(CodaTensor), c_void_p],
         "coda_rope_table": [c_int32, c_int32, c_double, c_void_p, c_void_p, c_void_p],
         "coda_block_forward": [P(CodaBlockFwd), c_void_p],
+        "coda_block_forward_noalloc": [P(CodaBlockFwd), c_void_p],
         "coda_block_backward": [P(CodaBlockBwd), c_void_p],
         "coda_qkv_rope": [P(CodaQkvRope), c_void_p],
         "coda_mlp_fp8": [P(CodaMlpFp8), c_void_p],
@@ -268,6 +270,18 @@ def coda_block_forward(O, R, W_o, W_gu_folded, W_d, eps, h, r, a, Y, workspace, 
     io = CodaBlockFwd(M, H, F, eps, _ptr(O), _ptr(R), _ptr(W_o), _ptr(W_gu_folded), _ptr(W_d), _ptr(h), _ptr(r),
                       _ptr(a), _ptr(Y), _ptr(Z), _ptr(Y_partials), _ptr(workspace))
     _check(lib().coda_block_forward(ctypes.byref(io), _stream(stream)), "coda_block_forward")
+
+
+def coda_block_forward_noalloc(O, R, W_o, W_gu_folded, W_d, eps, h, r, a, Y, Z=None, Y_partials=None,
+                               stream=None):
+    """The block forward for callers that cannot allocate device memory: no workspace is
+    passed; the chain's partial sums live in the library's static device array (see
+    include/coda.h for the size limit and the sharing rules)."""
+    M, H = O.shape
+    F = W_d.shape[1]
+    io = CodaBlockFwd(M, H, F, eps, _ptr(O), _ptr(R), _ptr(W_o), _ptr(W_gu_folded), _ptr(W_d), _ptr(h), _ptr(r),
+                      _ptr(a), _ptr(Y), _ptr(Z), _ptr(Y_partials), None)
+    _check(lib().coda_block_forward_noalloc(ctypes.byref(io), _stream(stream)), "coda_block_forward_noalloc")
 
 
 def coda_block_backward(O, W_o, W_gu, W_d, g, h, r, Z, a, dY, e, dh, dO, dW_o, dW_gu, dW_d, dg, c, workspace,
