@@ -53,7 +53,7 @@ LAUNCHES_PER_STEP = 5     # fold, G1, reduce, G2, G3
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = ["gemm_epilogue_transformer_tcgen05_gb300/csrc/coda_gemm.cuh",
                   "gemm_epilogue_transformer_tcgen05_gb300/csrc/coda_ptx.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_G2_block_forward.md")
 
 
 def parse():
@@ -65,6 +65,7 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-compare", action="store_true", help="skip the torch eager comparator and error check")
+    p.add_argument("--no-others", action="store_true", help="skip the backward / QKV / fp8 chain measurements")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     return p.parse_args()
 
@@ -89,16 +90,16 @@ def kernel_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None when the
-    summary is missing or the kernel sources changed after the counters were taken."""
+def recorded_traffic():
+    """DRAM bytes (read + write) per launch of G2 from the committed ncu summary, or None when
+    the summary is missing or the kernel sources changed after the counters were taken (the
+    summary records the hash of the kernel sources it was measured with)."""
     try:
         with open(TRAFFIC_FILE) as f:
-            d = json.load(f)
-        ent = d["kernels"][kernel]
-        if ent.get("source_hash") != kernel_hash():
-            return None
-        return float(ent["bytes_per_launch"])
+            txt = f.read()
+        h = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", txt).group(1)
+        b = float(re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt).group(1))
+        return b if h == kernel_hash() else None
     except Exception:
         return None
 
@@ -333,30 +334,53 @@ def run_coda(args, world, rank, local):
     ms_step = ms / args.steps
     value = world * M / (ms_step * 1e-3)
 
-    # ---- end to end through the public chain call, host buffers (pinned) both ways
+    # ---- end to end through the public chain call, host buffers (pinned) both ways.
+    # Each step copies its inputs O, R from pinned host memory and its result Y back; the
+    # copies of neighbouring steps run on two copy streams under the compute of this step
+    # (two device slots for O, R, Y), the way a stream of batches would be served.
     e2e = None
     if not args.no_e2e:
         O_h = inp["O"].pin_memory()
         R_h = inp["R"].pin_memory()
-        Y_h = torch.empty((M, H), dtype=BF).pin_memory()
+        Y_h = [torch.empty((M, H), dtype=BF).pin_memory() for _ in range(2)]
         ws = torch.empty((C.coda_workspace_size(C.WS_BLOCK_FWD, M, H, F) // 4,), device="cuda")
-        O_d, R_d = torch.empty_like(d["O"]), torch.empty_like(d["R"])
+        O_d = [torch.empty_like(d["O"]) for _ in range(2)]
+        R_d = [torch.empty_like(d["R"]) for _ in range(2)]
+        Y_d = [torch.empty_like(Y) for _ in range(2)]
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+        for e_ in ev_done + ev_out:
+            e_.record(stream)
 
-        def e2e_step():
-            O_d.copy_(O_h, non_blocking=True)
-            R_d.copy_(R_h, non_blocking=True)
+        def e2e_step(i):
+            k = i % 2
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_done[k])            # the step that used this slot has finished
+                O_d[k].copy_(O_h, non_blocking=True)
+                R_d[k].copy_(R_h, non_blocking=True)
+                ev_in[k].record(s_in)
+            stream.wait_event(ev_in[k])
+            stream.wait_event(ev_out[k])              # Y_d[k] of step i-2 has been read back
             C.coda_fold_gain(d["W_gu"], d["g"], Wf, stream=stream)
-            C.coda_block_forward(O_d, R_d, d["W_o"], Wf, d["W_d"], EPS, h, r, a, Y, ws, stream=stream)
-            Y_h.copy_(Y, non_blocking=True)
+            C.coda_block_forward(O_d[k], R_d[k], d["W_o"], Wf, d["W_d"], EPS, h, r, a, Y_d[k], ws, stream=stream)
+            ev_done[k].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[k])
+                Y_h[k].copy_(Y_d[k], non_blocking=True)
+                ev_out[k].record(s_out)
 
-        n_e2e = max(3, min(args.steps, 50))
-        for _ in range(3):
-            e2e_step()
+        n_e2e = max(4, min(args.steps, 100))
+        for i in range(4):
+            e2e_step(i)
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
+        for i in range(n_e2e):
+            e2e_step(i)
+        s_out.synchronize()
+        stream.wait_stream(s_out)
         e1.record(stream)
         barrier()
         ems = e0.elapsed_time(e1) / n_e2e
@@ -365,7 +389,13 @@ def run_coda(args, world, rank, local):
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             ems = float(t.item())
         e2e = {"value": world * M / (ems * 1e-3), "unit": "tokens/s", "ms_per_step": ems, "steps": n_e2e,
-               "h2d_bytes_per_step": O_h.numel() * 2 + R_h.numel() * 2, "d2h_bytes_per_step": Y_h.numel() * 2}
+               "h2d_bytes_per_step": O_h.numel() * 2 + R_h.numel() * 2, "d2h_bytes_per_step": Y_h[0].numel() * 2,
+               "pipelined": "copies of neighbouring steps overlap this step's compute (2 slots, 2 copy streams)"}
+
+    # ---- the other chains of the hot path, device-timed the same way (fewer steps)
+    others = None
+    if not args.no_others and rank == 0:
+        others = other_workloads(torch, C, S, args, stream)
 
     # ---- comparator: the same chain unfused in torch eager (cuBLAS GEMMs), and errors
     compare = None
@@ -378,7 +408,7 @@ def run_coda(args, world, rank, local):
         return
     pk = peaks()
     g2_tflops = FLOP["G2"] / (g2_ms * 1e-3) / 1e12
-    traffic = recorded_traffic("G2")
+    traffic = recorded_traffic()
     chain_roof_ms = max(CHAIN_FLOP / (pk["bf16_sus"] * 1e12), CHAIN_BYTES / (pk["hbm"] * 1e9)) * 1e3
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -402,6 +432,8 @@ def run_coda(args, world, rank, local):
     }
     if e2e:
         line["e2e"] = e2e
+    if others:
+        line["other_workloads"] = others
     if compare:
         line["compare"] = compare
     if not args.no_cpu_baseline:
@@ -413,6 +445,114 @@ def run_coda(args, world, rank, local):
     if dist is not None:
         dist.destroy_process_group()
     del np
+
+
+def _time(torch, fn, stream, steps, warmup=3):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def other_workloads(torch, C, S, args, stream):
+    """Device time of the other chains at their full sizes (16384 tokens): the block backward
+    (C2), QKV + RoPE (C3) and the fp8 MLP (C4), with TFLOP/s and the fraction of their
+    rooflines (bf16 sustained; fp8 = 2 x the bf16 measured peak, the nominal ratio)."""
+    BF = torch.bfloat16
+    pk = peaks()
+    steps = max(5, min(args.steps, 50))
+    out = {}
+    # C2: block backward (after a training-mode forward that saves Z)
+    M, H, F = M_TOK, HID, FFN
+    inp = S.block_inputs(M, H, F, seed=0, with_grad=True)
+    d = {k: inp[k].to("cuda").contiguous() for k in ("O", "R", "W_o", "W_gu", "W_d", "g", "dY")}
+    Wf = torch.empty_like(d["W_gu"])
+    C.coda_fold_gain(d["W_gu"], d["g"], Wf, stream=stream)
+    h = torch.empty((M, H), dtype=BF, device="cuda")
+    r = torch.empty((M,), device="cuda")
+    a = torch.empty((M, F), dtype=BF, device="cuda")
+    Y = torch.empty((M, H), dtype=BF, device="cuda")
+    Z = torch.empty((M, 2 * F), dtype=BF, device="cuda")
+    wsf = torch.empty((C.coda_workspace_size(C.WS_BLOCK_FWD, M, H, F) // 4,), device="cuda")
+    C.coda_block_forward(d["O"], d["R"], d["W_o"], Wf, d["W_d"], EPS, h, r, a, Y, wsf, Z=Z, stream=stream)
+    e = torch.empty((M, 2 * F), dtype=BF, device="cuda")
+    dh = torch.empty((M, H), dtype=BF, device="cuda")
+    dO = torch.empty((M, H), dtype=BF, device="cuda")
+    dW_o = torch.empty((H, H), device="cuda")
+    dW_gu = torch.empty((2 * F, H), device="cuda")
+    dW_d = torch.empty((H, F), device="cuda")
+    dg = torch.empty((H,), device="cuda")
+    c = torch.empty((M,), device="cuda")
+    wsb = torch.empty((C.coda_workspace_size(C.WS_BLOCK_BWD, M, H, F) // 4,), device="cuda")
+    bwd = lambda: C.coda_block_backward(d["O"], d["W_o"], d["W_gu"], d["W_d"], d["g"], h, r, Z, a, d["dY"], e, dh,
+                                        dO, dW_o, dW_gu, dW_d, dg, c, wsb, stream=stream)
+    ms = _time(torch, bwd, stream, steps)
+    flop = 2 * (2 * M * F * H + 2 * M * 2 * F * H + 2 * M * H * H)
+    byt = 2 * (M * H * 3 + H * F + 2 * M * F * 2) + 4 * H * F + 2 * (2 * M * F + 2 * F * H + 3 * M * H) + \
+        4 * 2 * F * H + 2 * (M * H * 3 + H * H) + 4 * H * H
+    roof = max(flop / (pk["bf16_sus"] * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
+    out["block_backward_C2"] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "roofline_ms": roof,
+                                "roofline_frac": roof / ms, "tokens_per_s": M / (ms * 1e-3), "launches": 8}
+    fwd_train = lambda: C.coda_block_forward(d["O"], d["R"], d["W_o"], Wf, d["W_d"], EPS, h, r, a, Y, wsf, Z=Z,
+                                             stream=stream)
+    ms_f = _time(torch, fwd_train, stream, steps)
+    out["block_forward_train_mode"] = {"ms": ms_f, "tokens_per_s": M / (ms_f * 1e-3),
+                                       "note": "G1, reduce, G2 saving Z = [G|U], G3 (gain already folded)"}
+    del d, Wf, h, r, a, Y, Z, e, dh, dO, dW_o, dW_gu, dW_d, dg, c, wsb, wsf
+    torch.cuda.empty_cache()
+    # C3: QKV projection + deferred r + RoPE (r from a full-row pass over h)
+    N, hd, seq = 3072, 64, 1024
+    qi = S.qkv_inputs(M, H, N, seed=0)
+    hq, Wq_, gq = (qi[k].to("cuda").contiguous() for k in ("h", "W_qkv", "g"))
+    Wqf = torch.empty_like(Wq_)
+    C.coda_fold_gain(Wq_, gq, Wqf, stream=stream)
+    cos = torch.empty((seq, hd // 2), device="cuda")
+    sin = torch.empty_like(cos)
+    C.coda_rope_table(seq, hd, 500000.0, cos, sin, stream=stream)
+    rq = torch.empty((M,), device="cuda")
+    oq = torch.empty((M, N), dtype=BF, device="cuda")
+    ms = _time(torch, lambda: C.coda_qkv_rope(hq, Wqf, EPS, seq, hd, 2560, cos, sin, rq, oq, stream=stream), stream,
+               steps)
+    flop = 2 * M * N * H
+    byt = 2 * (M * H * 2 + N * H + M * N) + 4 * M
+    roof = max(flop / (pk["bf16_sus"] * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
+    out["qkv_rope_C3"] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "roofline_ms": roof,
+                          "roofline_frac": roof / ms, "tokens_per_s": M / (ms * 1e-3), "launches": 2,
+                          "note": "row RMS of h (one pass) + QKV GEMM with r and RoPE epilogue"}
+    del hq, Wq_, gq, Wqf, oq
+    torch.cuda.empty_cache()
+    # C4: fp8 MLP
+    H8, F8 = 4096, 14336
+    fi = S.fp8_mlp_inputs(M, H8, F8, seed=0)
+    h8, X8, W8, Wd8 = (fi[k].to("cuda").contiguous() for k in ("h", "Xq", "Wq", "Wdq"))
+    r8 = torch.empty((M,), device="cuda")
+    aq = torch.empty((M, F8), dtype=torch.uint8, device="cuda")
+    am = torch.empty((1,), device="cuda")
+    Y8 = torch.empty((M, H8), dtype=BF, device="cuda")
+    P8 = torch.empty((H8 // 256, M), device="cuda")
+    s_a = 1.0
+    run8 = lambda: C.coda_mlp_fp8(h8, X8, W8, Wd8, fi["s_x"], fi["s_w"], fi["s_wd"], s_a, EPS, r8, aq, am, Y8, P8,
+                                  stream=stream)
+    run8()
+    torch.cuda.synchronize()
+    s_a = float(am.item()) / 448.0                     # delayed scaling from the previous pass
+    ms = _time(torch, run8, stream, steps)
+    flop = 2 * M * 2 * F8 * H8 + 2 * M * H8 * F8
+    byt = (M * H8 + 2 * F8 * H8 + M * F8) + (M * F8 + H8 * F8) + 2 * (M * H8 * 3) + 4 * M * (H8 // 256 + 1)
+    peak8 = 2 * pk["bf16_sus"]
+    roof = max(flop / (peak8 * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
+    out["mlp_fp8_C4"] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "roofline_ms": roof,
+                         "roofline_frac": roof / ms, "tokens_per_s": M / (ms * 1e-3), "launches": 3,
+                         "peak_note": "fp8 peak taken as 2x the measured bf16 sustained peak (nominal ratio)"}
+    del h8, X8, W8, Wd8, aq, Y8, P8
+    torch.cuda.empty_cache()
+    return out
 
 
 def unfused_compare(torch, d, Y, r, inp, stream, args):

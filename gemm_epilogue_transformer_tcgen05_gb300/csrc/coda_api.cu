@@ -391,6 +391,14 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
   p.K = (int)K;
   p.m_tiles = (int)m_tiles;
   p.n_tiles = (int)n_tiles;
+  {
+    // N-tiles per rasterisation group: as many as keep the group's slice of B (all of K)
+    // within about 32 MB of L2.
+    const int64_t b_tile_bytes = (int64_t)UMMA_N * K * esize(W->dtype);
+    int64_t gn = ((int64_t)32 << 20) / (b_tile_bytes > 0 ? b_tile_bytes : 1);
+    gn = gn < 1 ? 1 : (gn > n_tiles ? n_tiles : gn);
+    p.group_n = (int)gn;
+  }
   p.flags = (has(CODA_OP_ROW_SUMSQ_PARTIAL) ? F_PARTIAL : 0) | (has(CODA_OP_AMAX) ? F_AMAX : 0) |
             (has(CODA_OP_COL_SCALE) ? F_COLSCALE : 0) | (has(CODA_OP_ROW_SCALE) ? F_ROWSCALE : 0);
   if (g_inject_once) {

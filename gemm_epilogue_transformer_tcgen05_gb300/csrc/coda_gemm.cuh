@@ -82,6 +82,7 @@ enum : int {
 struct GemmParams {
   int M, N, K;          // out [M, N]; EPI_SWIGLU: N = F and B holds 2F rows (gate, then up)
   int m_tiles, n_tiles;
+  int group_n;          // tile order: groups of group_n N-tiles, M-major inside a group
   int flags;
   int up_offset;        // EPI_SWIGLU: first up row of B / first U column of saved Z;
                         // EPI_SWIGLU_BWD: first U column of Z and of e
@@ -137,6 +138,20 @@ struct GemmCfg {
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Tile order.  Tiles come in groups of group_n consecutive N-tiles; inside a group the
+// N-tile index runs fastest, then the M-tile.  The CTAs working at the same time then share
+// a few A row-blocks and one group's slice of B, which stays resident in L2 while the group
+// sweeps all M-tiles.
+__device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& mb, int& nb) {
+  const int per_group = p.m_tiles * p.group_n;
+  const int g = tile / per_group;
+  const int n_first = g * p.group_n;
+  const int gsize = min(p.group_n, p.n_tiles - n_first);
+  const int t = tile - g * per_group;
+  mb = t / gsize;
+  nb = n_first + (t - mb * gsize);
 }
 
 struct Watch {
@@ -330,8 +345,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t issued_any = 0, issued_par = 0;
       bool skip = (p.flags & F_INJECT_SKIP) != 0;
       bool ok = true;
+      const uint64_t keep = ptx::make_policy_evict_last();   // B: reused by every M-tile of a group
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-        const int mb = tile / p.n_tiles, nb = tile % p.n_tiles;
+        int mb, nb;
+        tile_coords(tile, p, mb, nb);
         const int m0 = mb * BM;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!bwait(EMPTY_BAR(stage), phase ^ 1u, watch, SITE_PRODUCER_EMPTY)) {
@@ -355,12 +372,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if constexpr (C::B_MN) {
               const int n0 = nb * UMMA_N;
 #pragma unroll
-              for (int j = 0; j < 4; ++j) ptx::tma_load_2d(sb + 8192 * j, &tmB, n0 + 64 * j, k0, fb);
+              for (int j = 0; j < 4; ++j) ptx::tma_load_2d_hint(sb + 8192 * j, &tmB, n0 + 64 * j, k0, fb, keep);
             } else {
               const int r0 = C::DUAL ? nb * 128 : nb * UMMA_N;
               const int r1 = C::DUAL ? p.up_offset + nb * 128 : r0 + 128;
-              ptx::tma_load_2d(sb, &tmB, k0, r0, fb);
-              ptx::tma_load_2d(sb + 16384, &tmB, k0, r1, fb);
+              ptx::tma_load_2d_hint(sb, &tmB, k0, r0, fb, keep);
+              ptx::tma_load_2d_hint(sb + 16384, &tmB, k0, r1, fb, keep);
             }
             issued_any |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -430,10 +447,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t out_base = side_base + 2 * C::NS * C::SSLOT;
     uint32_t side_par = 0, side_pending = 0;
     float amax_local = 0.f;
+    const uint64_t stream_pol = ptx::make_policy_evict_first();  // outputs and side inputs: touched once
     bool ok = true;
     int t = 0;
     for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++t) {
-      const int mb = tile / p.n_tiles, nb = tile % p.n_tiles;
+      int mb, nb;
+      tile_coords(tile, p, mb, nb);
       const int m0 = mb * BM;
       const int n0 = nb * C::BN_OUT;
       const int r0 = m0 + 32 * q;   // first row of this warp's 32-row slab
@@ -453,13 +472,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t dst = side_base + slot * C::NS * C::SSLOT;
           ptx::mbar_arrive_expect_tx(sbar, C::NS * C::SSLOT);
           if constexpr (C::EPI == EPI_RESID) {
-            ptx::tma_load_2d(dst, &tmSide0, n0 + 32 * c, r0, sbar);
+            ptx::tma_load_2d_hint(dst, &tmSide0, n0 + 32 * c, r0, sbar, stream_pol);
           } else if constexpr (C::EPI == EPI_SWIGLU_BWD) {
-            ptx::tma_load_2d(dst, &tmSide0, n0 + 32 * c, r0, sbar);
-            ptx::tma_load_2d(dst + C::SSLOT, &tmSide0, p.up_offset + n0 + 32 * c, r0, sbar);
+            ptx::tma_load_2d_hint(dst, &tmSide0, n0 + 32 * c, r0, sbar, stream_pol);
+            ptx::tma_load_2d_hint(dst + C::SSLOT, &tmSide0, p.up_offset + n0 + 32 * c, r0, sbar, stream_pol);
           } else {
-            ptx::tma_load_2d(dst, &tmSide0, n0 + 32 * c, r0, sbar);
-            ptx::tma_load_2d(dst + C::SSLOT, &tmSide1, n0 + 32 * c, r0, sbar);
+            ptx::tma_load_2d_hint(dst, &tmSide0, n0 + 32 * c, r0, sbar, stream_pol);
+            ptx::tma_load_2d_hint(dst + C::SSLOT, &tmSide1, n0 + 32 * c, r0, sbar, stream_pol);
           }
         }
       };
@@ -657,11 +676,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         if (lane == 0) {
           if (store) {
-            ptx::tma_store_2d(&tmOut, col0, r0, oslot);
-            if constexpr (C::EPI == EPI_SWIGLU_BWD) ptx::tma_store_2d(&tmOut, p.up_offset + col0, r0, oslot + C::OSLOT);
+            ptx::tma_store_2d_hint(&tmOut, col0, r0, oslot, stream_pol);
+            if constexpr (C::EPI == EPI_SWIGLU_BWD)
+              ptx::tma_store_2d_hint(&tmOut, p.up_offset + col0, r0, oslot + C::OSLOT, stream_pol);
             if constexpr (C::AUX) {
-              ptx::tma_store_2d(&tmAux, col0, r0, oslot + C::NO * C::OSLOT);
-              ptx::tma_store_2d(&tmAux, p.up_offset + col0, r0, oslot + C::NO * C::OSLOT + C::XSLOT);
+              ptx::tma_store_2d_hint(&tmAux, col0, r0, oslot + C::NO * C::OSLOT, stream_pol);
+              ptx::tma_store_2d_hint(&tmAux, p.up_offset + col0, r0, oslot + C::NO * C::OSLOT + C::XSLOT, stream_pol);
             }
           }
           ptx::bulk_commit();

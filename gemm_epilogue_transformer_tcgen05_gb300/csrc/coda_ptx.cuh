@@ -59,6 +59,34 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
+// Same load with an L2 cache-eviction policy (see make_policy_*).
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* m, int32_t c0, int32_t c1,
+                                                 uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+      : "memory");
+}
+// L2 policies: keep a reused operand (evict_last), stream a once-touched tensor (evict_first).
+__device__ __forceinline__ uint64_t make_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t make_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// 2-D tiled store with an L2 cache-eviction policy.
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* m, int32_t c0, int32_t c1, uint32_t src,
+                                                  uint64_t policy) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::
+                   "l"(reinterpret_cast<uint64_t>(m)),
+               "r"(c0), "r"(c1), "r"(src), "l"(policy)
+               : "memory");
+}
 // 2-D tiled store shared -> global (bulk-group completion); out-of-range parts are clipped.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, int32_t c0, int32_t c1, uint32_t src) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
