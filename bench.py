@@ -3,10 +3,10 @@
 
 Workload (one step, all on one GPU, bf16 in / fp32 accumulate / bf16 out):
     M = 16384 tokens, hidden H = 2048, FFN F = 8192, synthetic seeded inputs.
-    fold    W_gu' = W_gu diag(g)                      (gain moved onto the next weight)
-    G1      h = O W_o^T + R, partial sums of squares  (GEMM + residual + partial RMS epilogue)
+    G1      h = O W_o^T + R, partial sums of squares of h, u = h * g
+            (GEMM + residual + partial RMS + RMSNorm-gain broadcast epilogue)
     reduce  r = 1 / sqrt(sum partials / H + eps)      (the light row reduce)
-    G2      a = silu(G) U, [G | U] = r (h W_gu'^T)    (deferred-r GEMM + SwiGLU epilogue)
+    G2      a = silu(G) U, [G | U] = r (u W_gu^T)     (deferred-r GEMM + SwiGLU epilogue)
     G3      Y = a W_d^T + h                            (GEMM + residual epilogue)
 "CODA: new research optimizes Transformer training with GEMM-epilogue programming"
 (kucoin.com news flash), sections "El epílogo esconde un tesoro" and "Resultados del
@@ -35,21 +35,20 @@ if ROOT not in sys.path:
 
 METRIC = "fused GEMM-epilogue chain TFLOP/s & tokens/s at 16K tokens; % of roofline"
 M_TOK, HID, FFN, EPS = 16384, 2048, 8192, 1e-6
-WORKLOAD = "LLaMA-3-1B-shaped block forward: attn-out GEMM+residual+partial RMS -> row reduce -> " \
-           "deferred-r gate/up GEMM+SwiGLU -> down GEMM+residual; M=16384 tokens, H=2048, F=8192, bf16"
+WORKLOAD = "LLaMA-3-1B-shaped block forward: attn-out GEMM+residual+partial RMS+gain broadcast -> row reduce " \
+           "-> deferred-r gate/up GEMM+SwiGLU -> down GEMM+residual; M=16384 tokens, H=2048, F=8192, bf16"
 FLOP = {"G1": 2 * M_TOK * HID * HID, "G2": 2 * M_TOK * 2 * FFN * HID, "G3": 2 * M_TOK * HID * FFN}
 CHAIN_FLOP = sum(FLOP.values())
 MB = 1e6
 # compulsory bytes: each operand read once, each output written once (bf16 = 2 B, fp32 = 4 B)
 BYTES = {
-    "fold": 2 * (2 * FFN * HID) * 2 + 4 * HID,
-    "G1": 2 * (M_TOK * HID * 3 + HID * HID) + 4 * M_TOK * (HID // 256),
+    "G1": 2 * (M_TOK * HID * 4 + HID * HID) + 4 * M_TOK * (HID // 256) + 4 * HID,
     "reduce": 4 * (M_TOK * (HID // 256) + M_TOK),
     "G2": 2 * (M_TOK * HID + 2 * FFN * HID + M_TOK * FFN) + 4 * M_TOK,
     "G3": 2 * (M_TOK * FFN + HID * FFN + 2 * M_TOK * HID),
 }
 CHAIN_BYTES = sum(BYTES.values())
-LAUNCHES_PER_STEP = 5     # fold, G1, reduce, G2, G3
+LAUNCHES_PER_STEP = 4     # G1, reduce, G2, G3
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = ["gemm_epilogue_transformer_tcgen05_gb300/csrc/coda_gemm.cuh",
                   "gemm_epilogue_transformer_tcgen05_gb300/csrc/coda_ptx.cuh"]
@@ -270,8 +269,8 @@ def run_coda(args, world, rank, local):
     M, H, F = M_TOK, HID, FFN
     inp = S.block_inputs(M, H, F, seed=rank)
     d = {k: inp[k].to("cuda").contiguous() for k in ("O", "R", "W_o", "W_gu", "W_d", "g")}
-    Wf = torch.empty_like(d["W_gu"])
     h = torch.empty((M, H), dtype=BF, device="cuda")
+    u = torch.empty((M, H), dtype=BF, device="cuda")
     r = torch.empty((M,), device="cuda")
     a = torch.empty((M, F), dtype=BF, device="cuda")
     Y = torch.empty((M, H), dtype=BF, device="cuda")
@@ -279,15 +278,14 @@ def run_coda(args, world, rank, local):
     stream = torch.cuda.current_stream()
 
     def step(ev=None):
-        # the chain as its five C-ABI launches (coda_block_forward issues G1, reduce, G2, G3
-        # in exactly this order); events bracket the dominant GEMM
-        C.coda_fold_gain(d["W_gu"], d["g"], Wf, stream=stream)
-        C.coda_gemm_epilogue(d["O"], d["W_o"], [C.OP_ADD_SIDE, C.OP_ROW_SUMSQ_PARTIAL], h, residual=d["R"],
-                             row_partials=P, stream=stream)
+        # the chain as its four C-ABI launches (coda_block_forward with the gain broadcast
+        # issues exactly these, in this order); events bracket the dominant GEMM
+        C.coda_gemm_epilogue(d["O"], d["W_o"], [C.OP_ADD_SIDE, C.OP_ROW_SUMSQ_PARTIAL, C.OP_STORE_COL_SCALED], h,
+                             residual=d["R"], row_partials=P, col_scale=d["g"], store_aux=u, stream=stream)
         C.coda_rms_partial_reduce(P, M, H, EPS, r, stream=stream)
         if ev is not None:
             ev[0].record(stream)
-        C.coda_gemm_epilogue(h, Wf, [C.OP_ROW_SCALE, C.OP_SWIGLU], a, row_scale=r, stream=stream)
+        C.coda_gemm_epilogue(u, d["W_gu"], [C.OP_ROW_SCALE, C.OP_SWIGLU], a, row_scale=r, stream=stream)
         if ev is not None:
             ev[1].record(stream)
         C.coda_gemm_epilogue(a, d["W_d"], [C.OP_ADD_SIDE], Y, residual=h, stream=stream)
@@ -363,8 +361,8 @@ def run_coda(args, world, rank, local):
                 ev_in[k].record(s_in)
             stream.wait_event(ev_in[k])
             stream.wait_event(ev_out[k])              # Y_d[k] of step i-2 has been read back
-            C.coda_fold_gain(d["W_gu"], d["g"], Wf, stream=stream)
-            C.coda_block_forward(O_d[k], R_d[k], d["W_o"], Wf, d["W_d"], EPS, h, r, a, Y_d[k], ws, stream=stream)
+            C.coda_block_forward(O_d[k], R_d[k], d["W_o"], d["W_gu"], d["W_d"], EPS, h, r, a, Y_d[k], ws, g=d["g"],
+                                 u=u, stream=stream)
             ev_done[k].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_done[k])
@@ -472,15 +470,15 @@ def other_workloads(torch, C, S, args, stream):
     M, H, F = M_TOK, HID, FFN
     inp = S.block_inputs(M, H, F, seed=0, with_grad=True)
     d = {k: inp[k].to("cuda").contiguous() for k in ("O", "R", "W_o", "W_gu", "W_d", "g", "dY")}
-    Wf = torch.empty_like(d["W_gu"])
-    C.coda_fold_gain(d["W_gu"], d["g"], Wf, stream=stream)
     h = torch.empty((M, H), dtype=BF, device="cuda")
+    u = torch.empty((M, H), dtype=BF, device="cuda")
     r = torch.empty((M,), device="cuda")
     a = torch.empty((M, F), dtype=BF, device="cuda")
     Y = torch.empty((M, H), dtype=BF, device="cuda")
     Z = torch.empty((M, 2 * F), dtype=BF, device="cuda")
     wsf = torch.empty((C.coda_workspace_size(C.WS_BLOCK_FWD, M, H, F) // 4,), device="cuda")
-    C.coda_block_forward(d["O"], d["R"], d["W_o"], Wf, d["W_d"], EPS, h, r, a, Y, wsf, Z=Z, stream=stream)
+    C.coda_block_forward(d["O"], d["R"], d["W_o"], d["W_gu"], d["W_d"], EPS, h, r, a, Y, wsf, Z=Z, g=d["g"], u=u,
+                         stream=stream)
     e = torch.empty((M, 2 * F), dtype=BF, device="cuda")
     dh = torch.empty((M, H), dtype=BF, device="cuda")
     dO = torch.empty((M, H), dtype=BF, device="cuda")
@@ -499,32 +497,36 @@ def other_workloads(torch, C, S, args, stream):
     roof = max(flop / (pk["bf16_sus"] * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
     out["block_backward_C2"] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "roofline_ms": roof,
                                 "roofline_frac": roof / ms, "tokens_per_s": M / (ms * 1e-3), "launches": 8}
-    fwd_train = lambda: C.coda_block_forward(d["O"], d["R"], d["W_o"], Wf, d["W_d"], EPS, h, r, a, Y, wsf, Z=Z,
-                                             stream=stream)
+    fwd_train = lambda: C.coda_block_forward(d["O"], d["R"], d["W_o"], d["W_gu"], d["W_d"], EPS, h, r, a, Y, wsf,
+                                             Z=Z, g=d["g"], u=u, stream=stream)
     ms_f = _time(torch, fwd_train, stream, steps)
     out["block_forward_train_mode"] = {"ms": ms_f, "tokens_per_s": M / (ms_f * 1e-3),
-                                       "note": "G1, reduce, G2 saving Z = [G|U], G3 (gain already folded)"}
-    del d, Wf, h, r, a, Y, Z, e, dh, dO, dW_o, dW_gu, dW_d, dg, c, wsb, wsf
+                                       "note": "G1 (+ u = h g), reduce, G2 saving Z = [G|U], G3"}
+    del d, h, u, r, a, Y, Z, e, dh, dO, dW_o, dW_gu, dW_d, dg, c, wsb, wsf
     torch.cuda.empty_cache()
     # C3: QKV projection + deferred r + RoPE (r from a full-row pass over h)
     N, hd, seq = 3072, 64, 1024
     qi = S.qkv_inputs(M, H, N, seed=0)
     hq, Wq_, gq = (qi[k].to("cuda").contiguous() for k in ("h", "W_qkv", "g"))
     Wqf = torch.empty_like(Wq_)
-    C.coda_fold_gain(Wq_, gq, Wqf, stream=stream)
     cos = torch.empty((seq, hd // 2), device="cuda")
     sin = torch.empty_like(cos)
     C.coda_rope_table(seq, hd, 500000.0, cos, sin, stream=stream)
     rq = torch.empty((M,), device="cuda")
     oq = torch.empty((M, N), dtype=BF, device="cuda")
-    ms = _time(torch, lambda: C.coda_qkv_rope(hq, Wqf, EPS, seq, hd, 2560, cos, sin, rq, oq, stream=stream), stream,
-               steps)
+
+    def qkv():
+        C.coda_fold_gain(Wq_, gq, Wqf, stream=stream)    # gain onto W_qkv, every step
+        C.coda_qkv_rope(hq, Wqf, EPS, seq, hd, 2560, cos, sin, rq, oq, stream=stream)
+
+    ms = _time(torch, qkv, stream, steps)
     flop = 2 * M * N * H
-    byt = 2 * (M * H * 2 + N * H + M * N) + 4 * M
+    byt = 2 * (M * H * 2 + N * H * 3 + M * N) + 4 * M
     roof = max(flop / (pk["bf16_sus"] * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
     out["qkv_rope_C3"] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "roofline_ms": roof,
-                          "roofline_frac": roof / ms, "tokens_per_s": M / (ms * 1e-3), "launches": 2,
-                          "note": "row RMS of h (one pass) + QKV GEMM with r and RoPE epilogue"}
+                          "roofline_frac": roof / ms, "tokens_per_s": M / (ms * 1e-3), "launches": 3,
+                          "note": "gain fold onto W_qkv + row RMS of h (one pass) + QKV GEMM with r and RoPE "
+                                  "epilogue"}
     del hq, Wq_, gq, Wqf, oq
     torch.cuda.empty_cache()
     # C4: fp8 MLP

@@ -27,7 +27,7 @@ F32, BF16, E4M3 = 0, 1, 2
 ROW_MAJOR, COL_MAJOR = 0, 1
 OP_TENSOR_SCALE, OP_ROW_SCALE, OP_COL_SCALE, OP_ADD_SIDE, OP_SWIGLU, OP_ROPE = 1, 2, 3, 4, 5, 6
 OP_SWIGLU_BWD, OP_RMSBWD_COMBINE, OP_ROW_SUMSQ_PARTIAL, OP_ROW_DOT_PARTIAL = 7, 8, 9, 10
-OP_COL_DOT_PARTIAL, OP_AMAX, OP_STORE_AUX = 11, 12, 13
+OP_COL_DOT_PARTIAL, OP_AMAX, OP_STORE_AUX, OP_STORE_COL_SCALED = 11, 12, 13, 14
 REDUCE_RSQRT_MEAN, REDUCE_SCALE_SUM = 0, 1
 WS_BLOCK_FWD, WS_BLOCK_BWD = 0, 1
 MAX_OPS = 8
@@ -76,9 +76,9 @@ class CodaAux(Structure):
 
 class CodaBlockFwd(Structure):
     _fields_ = [("M", c_int64), ("H", c_int64), ("F", c_int64), ("eps", c_float), ("O", c_void_p), ("R", c_void_p),
-                ("W_o", c_void_p), ("W_gu", c_void_p), ("W_d", c_void_p), ("h", c_void_p), ("r", c_void_p),
-                ("a", c_void_p), ("Y", c_void_p), ("Z", c_void_p), ("Y_partials", c_void_p),
-                ("workspace", c_void_p)]
+                ("W_o", c_void_p), ("W_gu", c_void_p), ("W_d", c_void_p), ("g", c_void_p), ("u", c_void_p),
+                ("h", c_void_p), ("r", c_void_p), ("a", c_void_p), ("Y", c_void_p), ("Z", c_void_p),
+                ("Y_partials", c_void_p), ("workspace", c_void_p)]
 
 
 class CodaBlockBwd(Structure):
@@ -263,24 +263,26 @@ def coda_workspace_size(which, M, H, F):
     return int(lib().coda_workspace_size(which, M, H, F))
 
 
-def coda_block_forward(O, R, W_o, W_gu_folded, W_d, eps, h, r, a, Y, workspace, Z=None, Y_partials=None,
+def coda_block_forward(O, R, W_o, W_gu, W_d, eps, h, r, a, Y, workspace, Z=None, Y_partials=None, g=None, u=None,
                        stream=None):
+    """Block forward.  With g (and the u buffer) the gain is broadcast in G1's epilogue and
+    W_gu is the unfolded weight; without g, W_gu must already carry the folded gain."""
     M, H = O.shape
     F = W_d.shape[1]
-    io = CodaBlockFwd(M, H, F, eps, _ptr(O), _ptr(R), _ptr(W_o), _ptr(W_gu_folded), _ptr(W_d), _ptr(h), _ptr(r),
-                      _ptr(a), _ptr(Y), _ptr(Z), _ptr(Y_partials), _ptr(workspace))
+    io = CodaBlockFwd(M, H, F, eps, _ptr(O), _ptr(R), _ptr(W_o), _ptr(W_gu), _ptr(W_d), _ptr(g), _ptr(u), _ptr(h),
+                      _ptr(r), _ptr(a), _ptr(Y), _ptr(Z), _ptr(Y_partials), _ptr(workspace))
     _check(lib().coda_block_forward(ctypes.byref(io), _stream(stream)), "coda_block_forward")
 
 
-def coda_block_forward_noalloc(O, R, W_o, W_gu_folded, W_d, eps, h, r, a, Y, Z=None, Y_partials=None,
+def coda_block_forward_noalloc(O, R, W_o, W_gu, W_d, eps, h, r, a, Y, Z=None, Y_partials=None, g=None, u=None,
                                stream=None):
     """The block forward for callers that cannot allocate device memory: no workspace is
     passed; the chain's partial sums live in the library's static device array (see
     include/coda.h for the size limit and the sharing rules)."""
     M, H = O.shape
     F = W_d.shape[1]
-    io = CodaBlockFwd(M, H, F, eps, _ptr(O), _ptr(R), _ptr(W_o), _ptr(W_gu_folded), _ptr(W_d), _ptr(h), _ptr(r),
-                      _ptr(a), _ptr(Y), _ptr(Z), _ptr(Y_partials), None)
+    io = CodaBlockFwd(M, H, F, eps, _ptr(O), _ptr(R), _ptr(W_o), _ptr(W_gu), _ptr(W_d), _ptr(g), _ptr(u), _ptr(h),
+                      _ptr(r), _ptr(a), _ptr(Y), _ptr(Z), _ptr(Y_partials), None)
     _check(lib().coda_block_forward_noalloc(ctypes.byref(io), _stream(stream)), "coda_block_forward_noalloc")
 
 

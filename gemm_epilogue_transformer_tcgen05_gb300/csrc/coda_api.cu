@@ -135,7 +135,12 @@ struct ProgramTemplate {
 };
 const ProgramTemplate kPrograms[] = {
     {EPI_STORE, 2, {{CODA_OP_TENSOR_SCALE, true}, {CODA_OP_COL_SCALE, true}}},
-    {EPI_RESID, 3, {{CODA_OP_TENSOR_SCALE, true}, {CODA_OP_ADD_SIDE, false}, {CODA_OP_ROW_SUMSQ_PARTIAL, true}}},
+    {EPI_RESID,
+     4,
+     {{CODA_OP_TENSOR_SCALE, true},
+      {CODA_OP_ADD_SIDE, false},
+      {CODA_OP_ROW_SUMSQ_PARTIAL, true},
+      {CODA_OP_STORE_COL_SCALED, true}}},
     {EPI_ROWSCALE, 2, {{CODA_OP_TENSOR_SCALE, true}, {CODA_OP_ROW_SCALE, false}}},
     {EPI_SWIGLU,
      5,
@@ -315,26 +320,27 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
     if (!aligned16(sd.col_scale)) return CODA_ERR_ALIGN;
   }
   if (has(CODA_OP_ROW_SCALE) && !sd.row_scale) return CODA_ERR_NULL;
-  if (has(CODA_OP_COL_SCALE)) {
+  if (has(CODA_OP_COL_SCALE) || has(CODA_OP_STORE_COL_SCALED)) {
     if (!sd.col_scale) return CODA_ERR_NULL;
     if (!aligned16(sd.col_scale)) return CODA_ERR_ALIGN;
   }
-  const bool want_aux = has(CODA_OP_STORE_AUX);
+  const bool want_aux = has(CODA_OP_STORE_AUX) || has(CODA_OP_STORE_COL_SCALED);
   if (want_aux) {
     if ((st = check_tensor(ax.store_aux, false)) != CODA_OK) return st;
-    if (ax.store_aux->rows != M || ax.store_aux->cols != 2 * N || ax.store_aux->dtype != CODA_BF16)
+    const int64_t aux_cols = epi == EPI_SWIGLU ? 2 * N : N;
+    if (ax.store_aux->rows != M || ax.store_aux->cols != aux_cols || ax.store_aux->dtype != CODA_BF16)
       return CODA_ERR_SHAPE;
   }
   if (has(CODA_OP_AMAX) && !ax.amax) return CODA_ERR_NULL;
   const int bn_out = epi == EPI_SWIGLU ? 128 : 256;
-  const int64_t m_tiles = (M + BM - 1) / BM, n_tiles = (N + bn_out - 1) / bn_out;
+  const int64_t n_tiles = (N + bn_out - 1) / bn_out;
   if (has(CODA_OP_ROW_SUMSQ_PARTIAL) || has(CODA_OP_ROW_DOT_PARTIAL)) {
     if (!ax.row_partials) return CODA_ERR_NULL;
     if (ax.row_partials_ld < M) return CODA_ERR_SHAPE;
   }
   if (has(CODA_OP_COL_DOT_PARTIAL)) {
     if (!ax.col_partials) return CODA_ERR_NULL;
-    if (ax.col_partials_ld < N) return CODA_ERR_SHAPE;
+    if (ax.col_partials_ld < N) return CODA_ERR_SHAPE;   // rows: one per 32-row slab, ceil(M / 32)
   }
   if (has(CODA_OP_ROPE)) {
     const int hd = sd.rope_head_dim;
@@ -349,6 +355,8 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
   const VariantKey key{kind, epi, a_mn ? 1 : 0, b_mn ? 1 : 0, to_dt(out->dtype), side_dt, want_aux ? 1 : 0};
   const VariantEntry* var = find_variant(key);
   if (!var) return CODA_ERR_DTYPE;
+  const int64_t tile_rows = (int64_t)BM * var->cg;
+  const int64_t m_tiles = (M + tile_rows - 1) / tile_rows;
 
   DevState* d;
   if ((st = ensure_device(&d)) != CODA_OK) return st;
@@ -423,8 +431,7 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
   p.amax = reinterpret_cast<unsigned int*>(ax.amax);
   p.status = d->status;
   p.timeout_ns = (unsigned long long)g_watchdog_ms * 1000000ull;
-  const int64_t tiles = m_tiles * n_tiles;
-  L.grid = (int)(tiles < d->sms ? tiles : d->sms);
+  L.sms = d->sms;
   const cudaError_t e = var->fn(L, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
 }
@@ -500,7 +507,7 @@ size_t coda_workspace_size(int32_t which, int64_t M, int64_t H, int64_t F) {
   if (M < 0 || H < 0 || F < 0) return 0;
   if (which == CODA_WS_BLOCK_FWD) return (size_t)((H + 255) / 256) * (size_t)M * sizeof(float);
   if (which == CODA_WS_BLOCK_BWD)
-    return ((size_t)((F + 255) / 256) * (size_t)M + (size_t)(4 * ((M + 127) / 128)) * (size_t)H) * sizeof(float);
+    return ((size_t)((F + 255) / 256) * (size_t)M + (size_t)((M + 31) / 32) * (size_t)H) * sizeof(float);
   return 0;
 }
 
@@ -534,28 +541,36 @@ int coda_block_forward(const coda_block_fwd* io, void* stream) {
   if (!io->O || !io->R || !io->W_o || !io->W_gu || !io->W_d || !io->h || !io->r || !io->a || !io->Y ||
       !io->workspace)
     return CODA_ERR_NULL;
+  const bool broadcast_gain = io->g != nullptr;
+  if (broadcast_gain && !io->u) return CODA_ERR_NULL;
   if (M == 0) return CODA_OK;
   int st;
   const int64_t nparts = (H + 255) / 256;
-  // G1: h = O W_o^T + R, partial sums of squares of h
+  // G1: h = O W_o^T + R, partial sums of squares of h [, u = h * g]
   {
     coda_tensor A = mk(io->O, CODA_BF16, M, H, H), W = mk(io->W_o, CODA_BF16, H, H, H);
     coda_tensor R = mk(io->R, CODA_BF16, M, H, H), out = mk(io->h, CODA_BF16, M, H, H);
-    coda_epilogue_program pg = prog_of({CODA_OP_ADD_SIDE, CODA_OP_ROW_SUMSQ_PARTIAL});
+    coda_tensor U = mk(io->u, CODA_BF16, M, H, H);
+    coda_epilogue_program pg =
+        broadcast_gain ? prog_of({CODA_OP_ADD_SIDE, CODA_OP_ROW_SUMSQ_PARTIAL, CODA_OP_STORE_COL_SCALED})
+                       : prog_of({CODA_OP_ADD_SIDE, CODA_OP_ROW_SUMSQ_PARTIAL});
     coda_side_inputs sd{};
     sd.residual = &R;
+    sd.col_scale = io->g;
     coda_aux_outputs ax{};
     ax.row_partials = io->workspace;
     ax.row_partials_ld = M;
+    ax.store_aux = broadcast_gain ? &U : nullptr;
     if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, &ax, stream)) != CODA_OK) return st;
   }
   // r = 1 / sqrt(sum of partials / H + eps)
   if ((st = coda_rms_partial_reduce(io->workspace, M, (int32_t)nparts, M, H, io->eps, CODA_REDUCE_RSQRT_MEAN, nullptr,
                                     io->r, stream)) != CODA_OK)
     return st;
-  // G2: [G | U] = r (h W_gu'^T);  a = silu(G) U  [+ saved Z]
+  // G2: [G | U] = r (u W_gu^T) (or r (h W_gu'^T));  a = silu(G) U  [+ saved Z]
   {
-    coda_tensor A = mk(io->h, CODA_BF16, M, H, H), W = mk(io->W_gu, CODA_BF16, 2 * F, H, H);
+    coda_tensor A = mk(broadcast_gain ? io->u : io->h, CODA_BF16, M, H, H);
+    coda_tensor W = mk(io->W_gu, CODA_BF16, 2 * F, H, H);
     coda_tensor out = mk(io->a, CODA_BF16, M, F, F);
     coda_tensor Z = mk(io->Z, CODA_BF16, M, 2 * F, 2 * F);
     coda_epilogue_program pg = io->Z ? prog_of({CODA_OP_ROW_SCALE, CODA_OP_STORE_AUX, CODA_OP_SWIGLU})
@@ -592,9 +607,9 @@ int coda_block_backward(const coda_block_bwd* io, void* stream) {
   if (M == 0) return CODA_OK;
   int st;
   float* S = io->workspace;                          // [F/256, M] row partials of e . Z
-  float* Dg = io->workspace + ((F + 255) / 256) * M; // [4 ceil(M/128), H] column partials of h t
+  float* Dg = io->workspace + ((F + 255) / 256) * M; // [ceil(M/32), H] column partials of h t
   const int64_t nS = (F + 255) / 256;
-  const int64_t nDg = 4 * ((M + 127) / 128);
+  const int64_t nDg = (M + 31) / 32;
   // b1: e = r [dA U silu'(G) | dA silu(G)],  dA = dY W_d;  row partials of e . Z
   {
     coda_tensor A = mk(io->dY, CODA_BF16, M, H, H);

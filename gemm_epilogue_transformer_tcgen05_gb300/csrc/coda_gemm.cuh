@@ -37,9 +37,7 @@ constexpr int BM = 128;                               // tile rows = TMEM lanes
 constexpr int UMMA_N = 256;                           // MMA N = B tile rows
 constexpr int BK_BYTES = 128;                         // K bytes per stage (one 128B swizzle row)
 constexpr int KSTEPS = 4;                             // MMAs per stage, 32 bytes of K each
-constexpr int A_STAGE_BYTES = BM * BK_BYTES;          // 16 KB
-constexpr int B_STAGE_BYTES = UMMA_N * BK_BYTES;      // 32 KB
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int A_STAGE_BYTES = BM * BK_BYTES;          // 16 KB: this CTA's 128 rows of A
 constexpr int TMEM_COLS = 2 * UMMA_N;                 // two fp32 accumulators
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
@@ -54,6 +52,7 @@ enum : int { KIND_BF16 = 0, KIND_TF32 = 1, KIND_E4M3 = 2 };
 enum : int {
   EPI_STORE = 0,       // out = ts * acc [* g_col]
   EPI_RESID = 1,       // out = ts * acc + R            [+ row partial sum of squares of out]
+                       //   [+ aux = out * g_col: the RMSNorm gain broadcast along the tile]
   EPI_ROWSCALE = 2,    // out = ts * r_row * acc
   EPI_SWIGLU = 3,      // Z = ts * r_row * acc (gate | up halves); out = silu(Zg) * Zu * os
                        //   [+ saved Z, + amax |silu(Zg) * Zu|]
@@ -103,10 +102,17 @@ struct GemmParams {
   unsigned long long timeout_ns;
 };
 
-template <int KIND_, int EPI_, bool A_MN_, bool B_MN_, int OUT_DT_, int SIDE_DT_, bool AUX_>
+// CG = CTAs per MMA: 1, or 2 for a CTA pair (cluster of two) issuing cta_group::2 MMAs of
+// 256 x 256: each CTA holds 128 rows of A and 128 rows (N) of B per stage and receives its
+// 128 accumulator rows in its own TMEM.
+template <int KIND_, int EPI_, bool A_MN_, bool B_MN_, int OUT_DT_, int SIDE_DT_, bool AUX_, int CG_ = 2>
 struct GemmCfg {
-  static constexpr int KIND = KIND_, EPI = EPI_, OUT_DT = OUT_DT_, SIDE_DT = SIDE_DT_;
+  static constexpr int KIND = KIND_, EPI = EPI_, OUT_DT = OUT_DT_, SIDE_DT = SIDE_DT_, CG = CG_;
   static constexpr bool A_MN = A_MN_, B_MN = B_MN_, AUX = AUX_;
+  static constexpr int B_ROWS = UMMA_N / CG;                   // B rows (N) held by this CTA
+  static constexpr int B_STAGE_BYTES = B_ROWS * BK_BYTES;
+  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+  static constexpr int PAIR_ROWS = BM * CG;                    // output rows per tile
   static constexpr int OP_BYTES = KIND == KIND_TF32 ? 4 : KIND == KIND_BF16 ? 2 : 1;
   static constexpr int BK = BK_BYTES / OP_BYTES;   // K elements per stage
   static constexpr bool DUAL = EPI == EPI_SWIGLU;
@@ -116,22 +122,24 @@ struct GemmCfg {
   static constexpr int NO = EPI == EPI_SWIGLU_BWD ? 2 : 1;
   static constexpr int OSLOT = 32 * 32 * dt_bytes(OUT_DT);  // one 32 x 32 staging block
   static constexpr int SSLOT = 32 * 32 * dt_bytes(SIDE_DT);
-  static constexpr int XSLOT = 32 * 32 * 2;                 // saved Z (bf16)
-  static constexpr int OUTSET = NO * OSLOT + (AUX ? 2 * XSLOT : 0);
+  static constexpr int XSLOT = 32 * 32 * 2;                 // aux output block (bf16)
+  static constexpr int NX = AUX ? (EPI == EPI_SWIGLU ? 2 : 1) : 0;   // SwiGLU: G and U; residual: h * g
+  static constexpr int OUTSET = NO * OSLOT + NX * XSLOT;
   static constexpr int EPI_WARP_BYTES = 2 * NS * SSLOT + 2 * OUTSET;
   static constexpr int EPI_BYTES = NUM_EPI_WARPS * EPI_WARP_BYTES;
   static constexpr int BAR_BYTES = 256;
   static constexpr int STAGES_FIT = (MAX_SMEM - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT > 4 ? 4 : STAGES_FIT;
+  static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(STAGES >= 2, "shared memory budget");
   static_assert(!(A_MN || B_MN) || KIND == KIND_BF16, "MN-major operands are bf16 only");
-  static_assert(!AUX || EPI == EPI_SWIGLU, "saved Z only with SwiGLU");
+  static_assert(!AUX || EPI == EPI_SWIGLU || EPI == EPI_RESID, "aux output: SwiGLU or residual programs");
+  static_assert(CG == 1 || CG == 2, "CTA group");
   // instruction descriptor: D f32, A/B format, operand majors, N >> 3, M >> 4
   static constexpr uint32_t FMT = KIND == KIND_BF16 ? 1u : KIND == KIND_TF32 ? 2u : 0u;
   static constexpr uint32_t IDESC = (1u << 4) | (FMT << 7) | (FMT << 10) | ((A_MN ? 1u : 0u) << 15) |
                                     ((B_MN ? 1u : 0u) << 16) | ((uint32_t)(UMMA_N >> 3) << 17) |
-                                    ((uint32_t)(BM >> 4) << 24);
+                                    ((uint32_t)(PAIR_ROWS >> 4) << 24);
 };
 
 // Shared-memory matrix descriptor, 128B swizzle, version 1 (sm_100 family).
@@ -288,7 +296,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   const uint32_t sm_stage = base;
-  const uint32_t sm_epi = base + C::STAGES * STAGE_BYTES;
+  const uint32_t sm_epi = base + C::STAGES * C::STAGE_BYTES;
   const uint32_t sm_bar = sm_epi + C::EPI_BYTES;
   const int NBAR = 2 * C::STAGES + 13;
   uint8_t* misc = smem_raw + (sm_bar - raw) + 8 * NBAR;
@@ -304,6 +312,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = C::CG == 2 ? ptx::cluster_ctarank() : 0u;   // position in the CTA pair
+  const bool leader = rank == 0;
+  const int cluster_id = blockIdx.x / C::CG, n_clusters = gridDim.x / C::CG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -312,7 +323,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(TFULL_BAR(a), 1);
-      ptx::mbar_init(TEMPTY_BAR(a), NUM_EPI_WARPS);
+      ptx::mbar_init(TEMPTY_BAR(a), NUM_EPI_WARPS * C::CG);   // both CTAs' epilogue warps
     }
     for (int w = 0; w < NUM_EPI_WARPS; ++w)
       for (int s = 0; s < 2; ++s) ptx::mbar_init(SIDE_BAR(w, s), 1);
@@ -325,11 +336,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::prefetch_tmap(&tmB);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(const_cast<uint32_t*>(tmem_holder)), TMEM_COLS);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc<C::CG>(ptx::smem_u32(const_cast<uint32_t*>(tmem_holder)), TMEM_COLS);
+    ptx::tmem_relinquish<C::CG>();
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (C::CG == 2)
+    ptx::cluster_sync();   // the peer's barriers are initialised before any remote arrive
+  else
+    __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
@@ -346,10 +360,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool skip = (p.flags & F_INJECT_SKIP) != 0;
       bool ok = true;
       const uint64_t keep = ptx::make_policy_evict_last();   // B: reused by every M-tile of a group
-      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      const uint64_t normal = ptx::make_policy_evict_normal();
+      for (int tile = cluster_id; ok && tile < total_tiles; tile += n_clusters) {
         int mb, nb;
         tile_coords(tile, p, mb, nb);
-        const int m0 = mb * BM;
+        const int m0 = mb * C::PAIR_ROWS + (int)rank * BM;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!bwait(EMPTY_BAR(stage), phase ^ 1u, watch, SITE_PRODUCER_EMPTY)) {
             ok = false;
@@ -359,25 +374,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             skip = false;  // test hook: this k-block never arrives
           } else {
             const uint32_t fb = FULL_BAR(stage);
-            const uint32_t sa = sm_stage + stage * STAGE_BYTES;
+            const uint32_t sa = sm_stage + stage * C::STAGE_BYTES;
             const uint32_t sb = sa + A_STAGE_BYTES;
             const int k0 = kb * C::BK;
-            ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            // the leader's full barrier counts the bytes of both CTAs of a pair
+            if (leader) ptx::mbar_arrive_expect_tx(fb, C::CG * C::STAGE_BYTES);
+            auto load = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1, uint64_t pol) {
+              if constexpr (C::CG == 2)
+                ptx::tma_load_2d_pair(dst, m, c0, c1, ptx::mapa(fb, 0), pol);
+              else
+                ptx::tma_load_2d_hint(dst, m, c0, c1, fb, pol);
+            };
             if constexpr (C::A_MN) {
-              ptx::tma_load_2d(sa, &tmA, m0, k0, fb);
-              ptx::tma_load_2d(sa + 8192, &tmA, m0 + 64, k0, fb);
+              load(sa, &tmA, m0, k0, normal);
+              load(sa + 8192, &tmA, m0 + 64, k0, normal);
             } else {
-              ptx::tma_load_2d(sa, &tmA, k0, m0, fb);
+              load(sa, &tmA, k0, m0, normal);
             }
+            // B: this CTA's B_ROWS rows of the tile's 256 (SwiGLU: gate rows, then up rows)
             if constexpr (C::B_MN) {
-              const int n0 = nb * UMMA_N;
+              const int n0 = nb * UMMA_N + (int)rank * C::B_ROWS;
 #pragma unroll
-              for (int j = 0; j < 4; ++j) ptx::tma_load_2d_hint(sb + 8192 * j, &tmB, n0 + 64 * j, k0, fb, keep);
+              for (int j = 0; j < C::B_ROWS / 64; ++j) load(sb + 8192 * j, &tmB, n0 + 64 * j, k0, keep);
             } else {
-              const int r0 = C::DUAL ? nb * 128 : nb * UMMA_N;
-              const int r1 = C::DUAL ? p.up_offset + nb * 128 : r0 + 128;
-              ptx::tma_load_2d_hint(sb, &tmB, k0, r0, fb, keep);
-              ptx::tma_load_2d_hint(sb + 16384, &tmB, k0, r1, fb, keep);
+#pragma unroll
+              for (int h = 0; h < C::B_ROWS / 128; ++h) {
+                const int half = (int)rank * (C::B_ROWS / 128) + h;   // 0 or 1 of the tile's two halves
+                const int row = C::DUAL ? (half == 0 ? nb * 128 : p.up_offset + nb * 128) : nb * UMMA_N + half * 128;
+                load(sb + 16384 * h, &tmB, k0, row, keep);
+              }
             }
             issued_any |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -388,7 +413,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
-      if (!ok) {  // let loads already in flight land before the CTA exits
+      if (!ok && C::CG == 1) {  // let loads already in flight land before the CTA exits
         for (int s = 0; s < C::STAGES; ++s)
           if (issued_any & (1u << s)) drain_wait(FULL_BAR(s), (issued_par >> s) & 1u);
       }
@@ -396,12 +421,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {   // the pair's MMAs are issued by its leader CTA
       int stage = 0;
       uint32_t phase = 0;
       int t = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++t) {
+      for (int tile = cluster_id; ok && tile < total_tiles; tile += n_clusters, ++t) {
         const int acc = t & 1;
         const uint32_t aph = (t >> 1) & 1;
         if (!bwait(TEMPTY_BAR(acc), aph ^ 1u, watch, SITE_MMA_TMEM_EMPTY)) {
@@ -416,27 +441,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sa = sm_stage + stage * STAGE_BYTES;
+          const uint32_t sa = sm_stage + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + A_STAGE_BYTES;
 #pragma unroll
           for (int k = 0; k < KSTEPS; ++k) {
             const uint64_t ad = C::A_MN ? smem_desc(sa + k * 2048, 8192, 1024) : smem_desc(sa + k * 32, 16, 1024);
             const uint64_t bd = C::B_MN ? smem_desc(sb + k * 2048, 8192, 1024) : smem_desc(sb + k * 32, 16, 1024);
-            ptx::umma<C::KIND>(d_tmem, ad, bd, C::IDESC, (kb | k) != 0 ? 1u : 0u);
+            ptx::umma<C::KIND, C::CG>(d_tmem, ad, bd, C::IDESC, (kb | k) != 0 ? 1u : 0u);
           }
-          ptx::umma_commit(EMPTY_BAR(stage));  // frees the stage once these MMAs are done
+          ptx::umma_commit<C::CG>(EMPTY_BAR(stage));  // frees the stage (in both CTAs) once done
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        ptx::umma_commit(TFULL_BAR(acc));  // accumulator complete
+        ptx::umma_commit<C::CG>(TFULL_BAR(acc));  // accumulator complete (both CTAs)
       }
-      if (!ok) {  // wait for MMAs already issued before TMEM is released
-        ptx::umma_commit(DONE_BAR);
-        drain_wait(DONE_BAR, 0);
-      }
+      // every MMA (and the arrivals its commits make) is complete before TMEM is released
+      ptx::umma_commit<C::CG>(DONE_BAR, 1);
+      drain_wait(DONE_BAR, 0);
     }
     __syncwarp();
   } else {
@@ -450,10 +474,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint64_t stream_pol = ptx::make_policy_evict_first();  // outputs and side inputs: touched once
     bool ok = true;
     int t = 0;
-    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++t) {
+    for (int tile = cluster_id; ok && tile < total_tiles; tile += n_clusters, ++t) {
       int mb, nb;
       tile_coords(tile, p, mb, nb);
-      const int m0 = mb * BM;
+      const int m0 = mb * C::PAIR_ROWS + (int)rank * BM;
       const int n0 = nb * C::BN_OUT;
       const int r0 = m0 + 32 * q;   // first row of this warp's 32-row slab
       const int row = r0 + lane;
@@ -526,10 +550,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
         }
-        if (c == C::NCHUNK - 1) {  // accumulator fully read: hand it back to the MMA warp
+        if (c == C::NCHUNK - 1) {  // accumulator fully read: hand it back to the (leader's) MMA warp
           ptx::tc_fence_before();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(TEMPTY_BAR(acc));
+          if (lane == 0) {
+            if constexpr (C::CG == 2)
+              ptx::mbar_arrive_cluster(ptx::mapa(TEMPTY_BAR(acc), 0));
+            else
+              ptx::mbar_arrive(TEMPTY_BAR(acc));
+          }
         }
 
         // side inputs of this chunk
@@ -565,7 +594,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
         const int col0 = n0 + 32 * c;
         float o1[C::NO > 1 ? 32 : 1];
-        float zg[C::AUX ? 32 : 1], zu[C::AUX ? 32 : 1];
+        float zg[C::AUX ? 32 : 1], zu[C::NX > 1 ? 32 : 1];
 
         // ---------------------------------------------------------------- the program
         if constexpr (C::EPI == EPI_STORE) {
@@ -589,6 +618,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             x[j] = fmaf(x[j], ts, s0[j]);
             const float st = as_stored<C::OUT_DT>(x[j]);
             rowacc = fmaf(st, st, rowacc);
+          }
+          if constexpr (C::AUX) {   // u = h * g, the column vector broadcast along the tile
+            const float4* g4 = reinterpret_cast<const float4*>(p.col_scale + col0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float4 g = __ldg(g4 + j);
+              zg[4 * j] = x[4 * j] * g.x;
+              zg[4 * j + 1] = x[4 * j + 1] * g.y;
+              zg[4 * j + 2] = x[4 * j + 2] * g.z;
+              zg[4 * j + 3] = x[4 * j + 3] * g.w;
+            }
           }
         } else if constexpr (C::EPI == EPI_ROWSCALE) {
           const float sc = ts * rs;
@@ -658,7 +698,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           const float colsum = warp_transpose_sum(ht, lane);
-          if (col0 + lane < p.N) p.col_part[(size_t)(4 * mb + q) * p.col_part_ld + col0 + lane] = colsum;
+          if (slab_ok && col0 + lane < p.N) p.col_part[(size_t)(r0 >> 5) * p.col_part_ld + col0 + lane] = colsum;
         }
 
         // ---------------------------------------------------------------- stage + store
@@ -668,10 +708,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         slot_write<C::OUT_DT>(oslot, lane, x);
         if constexpr (C::NO > 1) slot_write<C::OUT_DT>(oslot + C::OSLOT, lane, o1);
-        if constexpr (C::AUX) {
-          slot_write<DT_BF16>(oslot + C::NO * C::OSLOT, lane, zg);
-          slot_write<DT_BF16>(oslot + C::NO * C::OSLOT + C::XSLOT, lane, zu);
-        }
+        if constexpr (C::NX > 0) slot_write<DT_BF16>(oslot + C::NO * C::OSLOT, lane, zg);
+        if constexpr (C::NX > 1) slot_write<DT_BF16>(oslot + C::NO * C::OSLOT + C::XSLOT, lane, zu);
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -679,10 +717,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::tma_store_2d_hint(&tmOut, col0, r0, oslot, stream_pol);
             if constexpr (C::EPI == EPI_SWIGLU_BWD)
               ptx::tma_store_2d_hint(&tmOut, p.up_offset + col0, r0, oslot + C::OSLOT, stream_pol);
-            if constexpr (C::AUX) {
-              ptx::tma_store_2d_hint(&tmAux, col0, r0, oslot + C::NO * C::OSLOT, stream_pol);
+            if constexpr (C::NX > 0) ptx::tma_store_2d_hint(&tmAux, col0, r0, oslot + C::NO * C::OSLOT, stream_pol);
+            if constexpr (C::NX > 1)
               ptx::tma_store_2d_hint(&tmAux, p.up_offset + col0, r0, oslot + C::NO * C::OSLOT + C::XSLOT, stream_pol);
-            }
           }
           ptx::bulk_commit();
         }
@@ -711,11 +748,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   }
 
+  if (C::CG == 2 && *abort_flag) {
+    // aborted: a pair's loads complete on the leader's barriers, which the peer cannot poll,
+    // so give copies still in flight a fixed 200 us to land before the pair exits
+    const uint64_t t0 = ptx::globaltimer();
+    while (ptx::globaltimer() - t0 < 200000ull) {
+    }
+  }
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (C::CG == 2)
+    ptx::cluster_sync();   // no remote arrive or load still targets this CTA's memory
+  else
+    __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    ptx::tmem_dealloc<C::CG>(tmem_base, TMEM_COLS);
   }
 #undef FULL_BAR
 #undef EMPTY_BAR
@@ -729,10 +776,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 struct GemmLaunch {
   CUtensorMap tmA, tmB, tmOut, tmSide0, tmSide1, tmAux;
   GemmParams p;
-  int grid;
+  int sms;
 };
 
 using GemmLaunchFn = cudaError_t (*)(const GemmLaunch&, cudaStream_t);
+
+// Number of CTA groups (pairs for CG = 2) that can be resident at once, per device.
+template <class C>
+int resident_groups(int sms) {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = sms / C::CG;
+  if constexpr (C::CG == 2) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_epilogue_kernel<C>, &cfg) == cudaSuccess && clusters > 0)
+      n = clusters < n ? clusters : n;
+    cudaGetLastError();
+  }
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
 
 template <class C>
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t s) {
@@ -745,9 +821,30 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_done[dev] = 1;
   }
-  gemm_epilogue_kernel<C><<<L.grid, NUM_THREADS, C::SMEM_BYTES, s>>>(L.tmA, L.tmB, L.tmOut, L.tmSide0, L.tmSide1,
-                                                                      L.tmAux, L.p);
-  return cudaGetLastError();
+  // persistent grid: one CTA group per resident slot, at most one per tile
+  const int64_t tiles = (int64_t)L.p.m_tiles * L.p.n_tiles;
+  const int groups = (int)(tiles < resident_groups<C>(L.sms) ? tiles : resident_groups<C>(L.sms));
+  if (groups <= 0) return cudaSuccess;
+  if constexpr (C::CG == 1) {
+    gemm_epilogue_kernel<C><<<groups, NUM_THREADS, C::SMEM_BYTES, s>>>(L.tmA, L.tmB, L.tmOut, L.tmSide0, L.tmSide1,
+                                                                        L.tmAux, L.p);
+    return cudaGetLastError();
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * groups, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_epilogue_kernel<C>, L.tmA, L.tmB, L.tmOut, L.tmSide0, L.tmSide1, L.tmAux,
+                              L.p);
+  }
 }
 
 }  // namespace coda

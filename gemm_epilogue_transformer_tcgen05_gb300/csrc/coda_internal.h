@@ -17,6 +17,7 @@ struct VariantEntry {
   GemmLaunchFn fn;
   int smem_bytes;
   int stages;
+  int cg;          // CTAs per MMA group (2 = CTA pair)
 };
 
 // Tables defined by the instantiation units.
@@ -47,4 +48,4 @@ cudaError_t launch_rope_table(int seq_len, int head_dim, double base, float* cos
   {{KIND, EPI, AMN, BMN, OUT, SIDE, AUX},                                                                 \
    &launch_gemm<GemmCfg<KIND, EPI, AMN, BMN, OUT, SIDE, AUX>>,                                            \
    GemmCfg<KIND, EPI, AMN, BMN, OUT, SIDE, AUX>::SMEM_BYTES,                                              \
-   GemmCfg<KIND, EPI, AMN, BMN, OUT, SIDE, AUX>::STAGES}
+   GemmCfg<KIND, EPI, AMN, BMN, OUT, SIDE, AUX>::STAGES, GemmCfg<KIND, EPI, AMN, BMN, OUT, SIDE, AUX>::CG}

@@ -6,6 +6,7 @@ const VariantEntry g_variants_fwd[] = {
     CODA_VARIANT(KIND_BF16, EPI_STORE, false, false, DT_BF16, DT_BF16, false),
     CODA_VARIANT(KIND_BF16, EPI_STORE, false, false, DT_F32, DT_BF16, false),
     CODA_VARIANT(KIND_BF16, EPI_RESID, false, false, DT_BF16, DT_BF16, false),
+    CODA_VARIANT(KIND_BF16, EPI_RESID, false, false, DT_BF16, DT_BF16, true),
     CODA_VARIANT(KIND_BF16, EPI_ROWSCALE, false, false, DT_BF16, DT_BF16, false),
     CODA_VARIANT(KIND_BF16, EPI_SWIGLU, false, false, DT_BF16, DT_BF16, false),
     CODA_VARIANT(KIND_BF16, EPI_SWIGLU, false, false, DT_BF16, DT_BF16, true),

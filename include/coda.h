@@ -90,8 +90,9 @@ typedef struct coda_tensor {
  *   {}                                        out = acc
  *   {COL_SCALE}                               out = acc * g[j]
  *   {TENSOR_SCALE}                            out = s * acc
- *   {ADD_SIDE [, ROW_SUMSQ_PARTIAL]}          out = acc + R; partials of out^2
- *   {TENSOR_SCALE, ADD_SIDE [, ROW_SUMSQ_PARTIAL]}
+ *   {[TENSOR_SCALE,] ADD_SIDE [, ROW_SUMSQ_PARTIAL] [, STORE_COL_SCALED]}
+ *        out = s * acc + R; partials of out^2; STORE_COL_SCALED also stores
+ *        out * g[j] (the RMSNorm gain broadcast along the tile) to aux.store_aux
  *   {ROW_SCALE}                               out = r[i] * acc
  *   {[TENSOR_SCALE,] ROW_SCALE, [STORE_AUX,] SWIGLU [, AMAX]}
  *        W holds 2N rows (gate rows [0, N), up rows [N, 2N)); Z = s * r[i] * acc over
@@ -116,7 +117,8 @@ enum coda_op {
   CODA_OP_ROW_DOT_PARTIAL = 10,  /* aux.row_partials[t, i] = sum over tile t of out . Z */
   CODA_OP_COL_DOT_PARTIAL = 11,  /* aux.col_partials[b, j] = sum over 32-row block b of h * t */
   CODA_OP_AMAX = 12,             /* atomic max of |silu(gate) * up| into *aux.amax */
-  CODA_OP_STORE_AUX = 13         /* save the pre-activation Z to aux.store_aux */
+  CODA_OP_STORE_AUX = 13,        /* save the pre-activation Z to aux.store_aux */
+  CODA_OP_STORE_COL_SCALED = 14  /* also store out[i, j] * side.col_scale[j] to aux.store_aux [M, N] bf16 */
 };
 
 #define CODA_MAX_OPS 8
@@ -144,9 +146,9 @@ typedef struct coda_side_inputs {
 typedef struct coda_aux_outputs {
   float* row_partials;          /* [ceil(N / 256), row_partials_ld] (SWIGLU_BWD: tiles of dA) */
   int64_t row_partials_ld;      /* >= M */
-  float* col_partials;          /* [4 * ceil(M / 128), col_partials_ld] */
+  float* col_partials;          /* [ceil(M / 32), col_partials_ld]: one row per 32-row slab */
   int64_t col_partials_ld;      /* >= N */
-  const coda_tensor* store_aux; /* STORE_AUX: Z [M, 2N] bf16 */
+  const coda_tensor* store_aux; /* STORE_AUX: Z [M, 2N] bf16; STORE_COL_SCALED: [M, N] bf16 */
   float* amax;                  /* AMAX: one float; the caller zeroes it before the call */
 } coda_aux_outputs;
 
@@ -185,16 +187,24 @@ CODA_API int coda_rope_table(int32_t seq_len, int32_t head_dim, double base, flo
 
 /* ------------------------------------------------------------ block chains
  * LLaMA-style block tail, hidden H, FFN width F, M tokens, bf16, weights [out, in]:
- *   h = O W_o^T + R;  r = rms(h);  [G | U] = r (h W_gu'^T);  a = silu(G) U;  Y = a W_d^T + h
- * W_gu' is the gate/up weight with the RMSNorm gain folded in (coda_fold_gain). */
+ *   h = O W_o^T + R;  r = rms(h);  [G | U] = r ((h * g) W_gu^T);  a = silu(G) U;  Y = a W_d^T + h
+ * (the RMSNorm y = r h g followed by the gate/up GEMM, with r deferred past the GEMM).
+ * Two ways to apply the gain g:
+ *   - g != NULL (gain broadcast): G1's epilogue also stores u = h * g, the gain broadcast
+ *     along each tile as a column vector, and the gate/up GEMM reads u with the
+ *     unfolded W_gu.  Needs the u buffer.  No weight preparation.
+ *   - g == NULL: W_gu is taken as already folded, W_gu'[n, k] = W_gu[n, k] g[k]
+ *     (coda_fold_gain), and the gate/up GEMM reads h. */
 typedef struct coda_block_fwd {
   int64_t M, H, F;
   float eps;
   const void* O;        /* [M, H] bf16 */
   const void* R;        /* [M, H] bf16 residual stream input */
   const void* W_o;      /* [H, H] bf16 */
-  const void* W_gu;     /* [2F, H] bf16, gain folded, gate rows first */
+  const void* W_gu;     /* [2F, H] bf16, gate rows first (unfolded if g is set, else folded) */
   const void* W_d;      /* [H, F] bf16 */
+  const float* g;       /* optional [H] RMSNorm gain, 16-byte aligned (see above) */
+  void* u;              /* [M, H] bf16 out when g is set: h * g, the gate/up GEMM's input */
   void* h;              /* out [M, H] bf16 */
   float* r;             /* out [M] fp32 */
   void* a;              /* out [M, F] bf16 */

@@ -26,11 +26,17 @@ def f32(x):
     return np.asarray(x, dtype=np.float32).astype(np.float64)
 
 
-def block_forward(Oa, R, W_o, g, W_gu, W_d, eps):
+def block_forward(Oa, R, W_o, g, W_gu, W_d, eps, gain="broadcast"):
+    """gain = "broadcast": G1 stores u = bf16(h g) and the gate/up GEMM reads u with the
+    unfolded weight; gain = "fold": the gate/up GEMM reads h with W' = bf16(W g)."""
     h = bf(O.linear(Oa, W_o) + R)
     r = f32(1.0 / np.sqrt(np.mean(h * h, axis=1) + eps))
-    Wf = bf(O.fold_gain(W_gu, g))
-    Zf = r[:, None] * O.linear(h, Wf)
+    if gain == "broadcast":
+        Wf = W_gu
+        Zf = r[:, None] * O.linear(bf(h * g[None, :]), W_gu)
+    else:
+        Wf = bf(O.fold_gain(W_gu, g))
+        Zf = r[:, None] * O.linear(h, Wf)
     F = Zf.shape[1] // 2
     a = bf(O.swiglu(Zf[:, :F], Zf[:, F:]))
     Y = bf(O.linear(a, W_d) + h)

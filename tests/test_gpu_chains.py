@@ -58,22 +58,29 @@ def test_tiny_fp32_chain(C):
 
 
 # --------------------------------------------------------------------- block forward
-def _run_block_forward(C, inp, train=True):
+def _run_block_forward(C, inp, train=True, gain="broadcast"):
+    """gain = "broadcast": G1's epilogue stores u = h g and G2 reads it with the unfolded
+    W_gu; gain = "fold": W_gu' = W_gu diag(g) first (coda_fold_gain) and G2 reads h."""
     O_, R, W_o, W_gu, W_d, g = (dev(inp[k]) for k in ("O", "R", "W_o", "W_gu", "W_d", "g"))
     M, H = O_.shape
     F = W_d.shape[1]
-    Wf = torch.empty_like(W_gu)
-    C.coda_fold_gain(W_gu, g, Wf)
     out = dict(h=torch.empty((M, H), dtype=BF, device="cuda"), r=torch.empty((M,), device="cuda"),
                a=torch.empty((M, F), dtype=BF, device="cuda"), Y=torch.empty((M, H), dtype=BF, device="cuda"),
                Z=torch.empty((M, 2 * F), dtype=BF, device="cuda") if train else None,
                Yp=torch.empty(((H + 255) // 256, M), device="cuda"))
     ws = torch.empty((C.coda_workspace_size(C.WS_BLOCK_FWD, M, H, F) // 4,), device="cuda")
-    C.coda_block_forward(O_, R, W_o, Wf, W_d, inp["eps"], out["h"], out["r"], out["a"], out["Y"], ws, Z=out["Z"],
-                         Y_partials=out["Yp"])
+    if gain == "fold":
+        Wf = torch.empty_like(W_gu)
+        C.coda_fold_gain(W_gu, g, Wf)
+        C.coda_block_forward(O_, R, W_o, Wf, W_d, inp["eps"], out["h"], out["r"], out["a"], out["Y"], ws,
+                             Z=out["Z"], Y_partials=out["Yp"])
+    else:
+        out["u"] = torch.empty((M, H), dtype=BF, device="cuda")
+        C.coda_block_forward(O_, R, W_o, W_gu, W_d, inp["eps"], out["h"], out["r"], out["a"], out["Y"], ws,
+                             Z=out["Z"], Y_partials=out["Yp"], g=g, u=out["u"])
     torch.cuda.synchronize()
     fresh_status()
-    return out, Wf
+    return out, None
 
 
 def _oracle_forward_rows(inp, rows):
@@ -81,22 +88,25 @@ def _oracle_forward_rows(inp, rows):
     return O.block_forward(x["O"][rows], x["R"][rows], x["W_o"], x["g"], x["W_gu"], x["W_d"], inp["eps"])
 
 
-def _sim_forward_rows(inp, rows):
+def _sim_forward_rows(inp, rows, gain="broadcast"):
     x = {k: f64(inp[k]) for k in ("O", "R", "W_o", "W_gu", "W_d", "g")}
-    return SIM.block_forward(x["O"][rows], x["R"][rows], x["W_o"], x["g"], x["W_gu"], x["W_d"], inp["eps"])
+    return SIM.block_forward(x["O"][rows], x["R"][rows], x["W_o"], x["g"], x["W_gu"], x["W_d"], inp["eps"], gain)
 
 
+@pytest.mark.parametrize("gain", ["broadcast", "fold"])
 @pytest.mark.parametrize("M,H,F", [(640, 512, 1024), (300, 256, 384)])
-def test_block_forward_small(C, M, H, F):
+def test_block_forward_small(C, M, H, F, gain):
     inp = S.block_inputs(M, H, F, seed=0)
-    out, _ = _run_block_forward(C, inp)
+    out, _ = _run_block_forward(C, inp, gain=gain)
     ref = _oracle_forward_rows(inp, np.arange(M))
-    sim = _sim_forward_rows(inp, np.arange(M))
+    sim = _sim_forward_rows(inp, np.arange(M), gain)
     for k in ("h", "r", "Y"):
         assert_close(f64(out[k]), ref[k], TOL_BF16, k)
     assert_product_close(f64(out["a"]), ref["a"], sim["a"], "a")
     assert_close(f64(out["Z"]), ref["Z"], TOL_BF16, "Z")
     assert_close(f64(out["Yp"]), O.partial_sumsq(ref["Y"], 256), TOL_BF16, "Y partials")
+    if gain == "broadcast":
+        assert_close(f64(out["u"]), ref["h"] * f64(inp["g"])[None, :], TOL_BF16, "u = h g")
 
 
 @pytest.mark.slow

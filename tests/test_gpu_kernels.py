@@ -185,7 +185,7 @@ def test_rmsnorm_backward_epilogue(C):
     g = seeded((H,), 32, std=0.1, mean=1.0)
     c = seeded((M,), 33, std=0.1)
     out = torch.empty((M, H), dtype=BF, device="cuda")
-    nblk = 4 * ((M + 127) // 128)
+    nblk = (M + 31) // 32
     Dg = torch.empty((nblk, H), dtype=torch.float32, device="cuda")
     C.coda_gemm_epilogue(dev(E), dev(Wgu).t(), [C.OP_RMSBWD_COMBINE, C.OP_COL_DOT_PARTIAL], out, aux_in=dev(h),
                          aux_in2=dev(dY), col_scale=dev(g), row_coef=dev(c), col_partials=Dg)

@@ -78,7 +78,8 @@ def test_no_alloc_refuses_oversized_problems(C):
     fake = ctypes.c_void_p(0x10000)
 
     def io(M, H, F, ws=None):
-        return C.CodaBlockFwd(M, H, F, 1e-6, fake, fake, fake, fake, fake, fake, fake, fake, fake, None, None, ws)
+        return C.CodaBlockFwd(M=M, H=H, F=F, eps=1e-6, O=fake, R=fake, W_o=fake, W_gu=fake, W_d=fake, h=fake, r=fake,
+                              a=fake, Y=fake, workspace=ws)
 
     L = C.lib()
     too_many_rows = C.NOALLOC_MAX_PARTIALS // ((2048 + 255) // 256) + 1
