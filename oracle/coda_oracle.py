@@ -43,6 +43,8 @@ Readings of points the pages leave open (the plainest reading consistent with th
      (the Q and K heads) are rotated.
   6. FP8 is OCP e4m3 ("fn": no infinities, max 448) with round-to-nearest-even and
      saturation to +-448; dequantised value = scale * code value.
+  7. Cross-entropy: mean over rows of logsumexp(logits) - logit[target], the final RMSNorm
+     before the LM head as in the block chain; every target is a valid class index.
 Every function here is pinned by a test (closed form, invariant, library special case
 or brute force); none is "parity unpinned".
 """
@@ -313,6 +315,97 @@ def mlp_fp8(h, Xq_val, s_x, Wq_val, s_w, Wdq_val, s_wd, s_a, eps, bn):
     aq_val = e4m3_round(a / F64(s_a))
     Y = linear(F64(s_a) * aq_val, F64(s_wd) * _f64(Wdq_val)) + _f64(h)
     return dict(r=r, Z=Z, a=a, amax=np.max(np.abs(a)), aq_val=aq_val, Y=Y, P=partial_sumsq(Y, bn))
+
+
+# ---------------------------------------------------------------------------------------
+# Cross-entropy after the final RMSNorm and the LM-head GEMM
+# [KuCoin, "Cinco bloques…": block log-sum-exp, and max / sum-exp statistics for online
+# normalisation; "hoja de referencia": cross-entropy and its gradient are covered]
+# ---------------------------------------------------------------------------------------
+def logsumexp(z):
+    """Row-wise log(sum_j exp(z_ij)), shifted by the row maximum (exact in real arithmetic)."""
+    z = _f64(z)
+    m = np.max(z, axis=1)
+    return m + np.log(np.sum(np.exp(z - m[:, None]), axis=1))
+
+
+def cross_entropy(logits, targets):
+    """Per-row loss_i = logsumexp(logits_i) - logits_i[target_i], and their mean."""
+    z = _f64(logits)
+    t = np.asarray(targets, dtype=np.int64)
+    lse = logsumexp(z)
+    loss = lse - z[np.arange(z.shape[0]), t]
+    return dict(lse=lse, loss=loss, mean=float(np.mean(loss)))
+
+
+def lm_head_xent_forward(h, g, W_v, targets, eps):
+    """Final RMSNorm, LM head and mean cross-entropy (plain chain):
+    y = rmsnorm(h, g);  logits = y W_v^T;  loss = mean_i (lse_i - logits_i[t_i])."""
+    r = rms_scale(h, eps)
+    y = r[:, None] * _f64(h) * _f64(g)[None, :]
+    logits = linear(y, W_v)
+    ce = cross_entropy(logits, targets)
+    return dict(r=r, y=y, logits=logits, **ce)
+
+
+def lm_head_xent_backward(fwd, h, g, W_v, targets, dloss=1.0):
+    """Plain chain rule of lm_head_xent_forward for an upstream gradient dloss of the mean:
+    dlogits = dloss (softmax(logits) - onehot(t)) / M;  dW_v = dlogits^T y;  dy = dlogits W_v;
+    RMSNorm backward (textbook form) -> dh, dg."""
+    logits, r, y = fwd["logits"], fwd["r"], fwd["y"]
+    h, g, W_v = _f64(h), _f64(g), _f64(W_v)
+    M, d = h.shape
+    p = np.exp(logits - fwd["lse"][:, None])
+    onehot = np.zeros_like(p)
+    onehot[np.arange(M), np.asarray(targets, dtype=np.int64)] = 1.0
+    dlogits = F64(dloss) * (p - onehot) / F64(M)
+    dW_v = dlogits.T @ y
+    dy = dlogits @ W_v
+    dg = np.sum(dy * r[:, None] * h, axis=0)
+    proj = np.sum(g[None, :] * dy * h, axis=1)
+    dh = r[:, None] * (g[None, :] * dy) - (r ** 3 / d)[:, None] * h * proj[:, None]
+    return dict(dlogits=dlogits, dW_v=dW_v, dh=dh, dg=dg)
+
+
+def lm_head_xent_backward_fused(fwd, h, g, W_v, targets, dloss=1.0):
+    """The fused forms the kernels compute:
+      e = r * dloss (exp(z - lse) - onehot) / M   with z = logits (softmax-gradient epilogue)
+      s_i = sum_v e_iv z_iv,  c = r s / d;  t = e W_v;  dh = g t - c h;  dg = sum_i h t
+      dW_v = e^T u with u = h g."""
+    logits, r = fwd["logits"], fwd["r"]
+    h, g, W_v = _f64(h), _f64(g), _f64(W_v)
+    M, d = h.shape
+    onehot = np.zeros_like(logits)
+    onehot[np.arange(M), np.asarray(targets, dtype=np.int64)] = 1.0
+    e = r[:, None] * F64(dloss) * (np.exp(logits - fwd["lse"][:, None]) - onehot) / F64(M)
+    s = np.sum(e * logits, axis=1)
+    c = r * s / d
+    t = e @ W_v
+    dh = g[None, :] * t - c[:, None] * h
+    return dict(e=e, c=c, dh=dh, dg=np.sum(h * t, axis=0), dW_v=e.T @ (h * g[None, :]))
+
+
+def xent_partials(z, bn):
+    """Per-tile online-normalisation state of each row: for tile t of bn columns,
+    m[t, i] = max_j z_ij and s[t, i] = sum_j exp(z_ij - m[t, i]) (layout [ntiles, M])."""
+    z = _f64(z)
+    M, V = z.shape
+    n = (V + bn - 1) // bn
+    m = np.zeros((n, M))
+    s = np.zeros((n, M))
+    for t in range(n):
+        blk = z[:, t * bn:(t + 1) * bn]
+        m[t] = np.max(blk, axis=1)
+        s[t] = np.sum(np.exp(blk - m[t][:, None]), axis=1)
+    return m, s
+
+
+def xent_combine(m, s):
+    """The light reduce of the partial states: lse = M + log(sum_t s_t exp(m_t - M)),
+    M = max_t m_t."""
+    m, s = _f64(m), _f64(s)
+    top = np.max(m, axis=0)
+    return top + np.log(np.sum(s * np.exp(m - top[None, :]), axis=0))
 
 
 # ---------------------------------------------------------------------------------------

@@ -30,6 +30,11 @@ def tiny_block():
     out = {k: fwd[k] for k in ("h", "r", "a", "Y")}
     out.update({k: bwd[k] for k in ("dh", "dO", "dW_o", "dg", "dW_gu", "dW_d")})
     out["qkv_rope"] = q["out"]
+    tgt = np.array([1, 7, 3])
+    ce = O.lm_head_xent_forward(inp["O"], inp["g"], inp["W_gu"], tgt, eps)
+    ceb = O.lm_head_xent_backward(ce, inp["O"], inp["g"], inp["W_gu"], tgt)
+    out["xent_loss"] = ce["loss"]
+    out["xent_dh"] = ceb["dh"]
     return dict(eps=eps, inputs={k: v.tolist() for k, v in inp.items()},
                 outputs={k: np.asarray(v).tolist() for k, v in out.items()})
 

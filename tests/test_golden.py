@@ -22,5 +22,9 @@ def test_tiny_block_fixture():
     got = {k: fwd[k] for k in ("h", "r", "a", "Y")}
     got.update({k: bwd[k] for k in ("dh", "dO", "dW_o", "dg", "dW_gu", "dW_d")})
     got["qkv_rope"] = q["out"]
+    tgt = np.array([1, 7, 3])
+    ce = O.lm_head_xent_forward(i["O"], i["g"], i["W_gu"], tgt, eps)
+    got["xent_loss"] = ce["loss"]
+    got["xent_dh"] = O.lm_head_xent_backward(ce, i["O"], i["g"], i["W_gu"], tgt)["dh"]
     for k, v in fx["outputs"].items():
         np.testing.assert_allclose(got[k], np.array(v), rtol=1e-12, atol=1e-14, err_msg=k)

@@ -98,3 +98,30 @@ def test_partial_tile_off_by_one_is_caught(monkeypatch):
 
     _plant(monkeypatch, "partial_sumsq", bad)
     assert _fails(pins.test_partials_sum_to_row_sumsq, 64)
+
+
+def test_xent_target_off_by_one_is_caught(monkeypatch):
+    orig = O.cross_entropy
+
+    def bad(logits, targets):
+        return orig(logits, (np.asarray(targets) + 1) % np.asarray(logits).shape[1])
+
+    _plant(monkeypatch, "cross_entropy", bad)
+    assert _fails(pins.test_cross_entropy_closed_forms)
+
+
+def test_xent_missing_mean_scale_is_caught(monkeypatch):
+    orig = O.lm_head_xent_backward
+
+    def bad(fwd, h, g, W_v, targets, dloss=1.0):
+        out = orig(fwd, h, g, W_v, targets, dloss)
+        M = np.asarray(h).shape[0]
+        return {k: v * M for k, v in out.items()}
+
+    _plant(monkeypatch, "lm_head_xent_backward", bad)
+    assert _fails(pins.test_lm_head_xent_backward_matches_finite_differences)
+
+
+def test_xent_combine_without_rescale_is_caught(monkeypatch):
+    _plant(monkeypatch, "xent_combine", lambda m, s: np.max(m, axis=0) + np.log(np.sum(s, axis=0)))
+    assert _fails(pins.test_xent_partials_combine_to_logsumexp)

@@ -332,3 +332,68 @@ def test_max_rel_err_floor():
     got = ref + np.array([0.01, 0.0, 0.0, 0.01])
     # the floor rms(ref) ~ 0.707 keeps the near-zero entries from dominating
     assert abs(O.max_rel_err(got, ref) - 0.01 / math.sqrt(0.5)) < 1e-9
+
+
+# ---------------------------------------------------------------------- cross-entropy
+def test_logsumexp_matches_scipy_and_closed_forms():
+    from scipy.special import logsumexp as lse_lib
+    z = RNG.normal(size=(7, 50)) * 10
+    np.testing.assert_allclose(O.logsumexp(z), lse_lib(z, axis=1), rtol=1e-14)
+    V = 128
+    np.testing.assert_allclose(O.logsumexp(np.zeros((2, V))), math.log(V), rtol=1e-15)
+    big = np.array([[1000.0, 1000.0]])       # shift makes it finite: 1000 + log 2
+    np.testing.assert_allclose(O.logsumexp(big), 1000.0 + math.log(2.0), rtol=1e-15)
+
+
+def test_cross_entropy_closed_forms():
+    V = 64
+    ce = O.cross_entropy(np.zeros((3, V)), [0, 5, 63])
+    np.testing.assert_allclose(ce["loss"], math.log(V), rtol=1e-15)   # uniform logits
+    z = np.full((1, 4), -50.0)
+    z[0, 2] = 50.0
+    assert O.cross_entropy(z, [2])["loss"][0] < 1e-40                 # confident and right
+    np.testing.assert_allclose(O.cross_entropy(z, [0])["loss"][0], 100.0, rtol=1e-12)
+
+
+def test_xent_partials_combine_to_logsumexp():
+    z = RNG.normal(size=(9, 700)) * 5
+    for bn in (32, 256, 700, 100):
+        m, s = O.xent_partials(z, bn)
+        np.testing.assert_allclose(O.xent_combine(m, s), O.logsumexp(z), rtol=1e-13)
+
+
+def _lm_head_case(M=5, d=8, V=11, seed=4):
+    rng = np.random.default_rng(seed)
+    return (rng.normal(size=(M, d)), 1 + 0.1 * rng.normal(size=d), rng.normal(size=(V, d)) / 2,
+            rng.integers(0, V, size=M))
+
+
+def test_lm_head_xent_backward_matches_finite_differences():
+    h, g, W, t = _lm_head_case()
+    eps = 1e-6
+    f = O.lm_head_xent_forward(h, g, W, t, eps)
+    b = O.lm_head_xent_backward(f, h, g, W, t, dloss=1.7)
+
+    def loss(hh, gg, WW):
+        return 1.7 * O.lm_head_xent_forward(hh, gg, WW, t, eps)["mean"]
+
+    for name, arr, an in (("h", h, b["dh"]), ("g", g, b["dg"]), ("W", W, b["dW_v"])):
+        num = np.zeros_like(arr)
+        for ix in np.ndindex(arr.shape):
+            p, m = arr.copy(), arr.copy()
+            p[ix] += 1e-6
+            m[ix] -= 1e-6
+            args_p = {"h": (p, g, W), "g": (h, p, W), "W": (h, g, p)}[name]
+            args_m = {"h": (m, g, W), "g": (h, m, W), "W": (h, g, m)}[name]
+            num[ix] = (loss(*args_p) - loss(*args_m)) / 2e-6
+        assert np.max(np.abs(num - an)) / np.max(np.abs(num)) <= 1e-6, name
+
+
+def test_lm_head_fused_backward_equals_chain_rule_and_rows_sum_to_zero():
+    h, g, W, t = _lm_head_case(M=12, d=16, V=40, seed=9)
+    f = O.lm_head_xent_forward(h, g, W, t, 1e-6)
+    plain = O.lm_head_xent_backward(f, h, g, W, t, dloss=0.5)
+    fused = O.lm_head_xent_backward_fused(f, h, g, W, t, dloss=0.5)
+    for k in ("dh", "dg", "dW_v"):
+        assert np.max(np.abs(fused[k] - plain[k])) <= 1e-12 * np.max(np.abs(plain[k])), k
+    np.testing.assert_allclose(np.sum(plain["dlogits"], axis=1), 0.0, atol=1e-15)   # softmax - onehot
