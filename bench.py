@@ -554,6 +554,34 @@ def other_workloads(torch, C, S, args, stream):
                          "peak_note": "fp8 peak taken as 2x the measured bf16 sustained peak (nominal ratio)"}
     del h8, X8, W8, Wd8, aq, Y8, P8
     torch.cuda.empty_cache()
+    # N1: final RMSNorm + LM head + cross-entropy (vocabulary 128256), forward and backward
+    V = 128256
+    li = S.lm_head_inputs(M, H, V, seed=0)
+    hl, gl, Wv, tg = (li[k].to("cuda").contiguous() for k in ("h", "g", "W_v", "targets"))
+    ul = torch.empty((M, H), dtype=BF, device="cuda")
+    rl, lse, loss, mean = (torch.empty((n,), device="cuda") for n in (M, M, M, 1))
+    wsx = torch.empty((C.coda_workspace_size(C.WS_XENT_FWD, M, H, V) // 4,), device="cuda")
+    fx = lambda: C.coda_lm_head_xent_forward(hl, gl, Wv, tg, EPS, ul, rl, lse, loss, mean, wsx, stream=stream)
+    steps_x = max(3, min(args.steps, 20))
+    ms_f = _time(torch, fx, stream, steps_x)
+    el = torch.empty((M, V), dtype=BF, device="cuda")
+    dhl = torch.empty((M, H), dtype=BF, device="cuda")
+    dWv = torch.empty((V, H), device="cuda")
+    dgl, cl = torch.empty((H,), device="cuda"), torch.empty((M,), device="cuda")
+    wsb = torch.empty((C.coda_workspace_size(C.WS_XENT_BWD, M, H, V) // 4,), device="cuda")
+    bx = lambda: C.coda_lm_head_xent_backward(hl, gl, Wv, tg, ul, rl, lse, 1.0, el, dhl, dWv, dgl, cl, wsb,
+                                              stream=stream)
+    ms_b = _time(torch, bx, stream, steps_x)
+    flop = 2 * M * V * H
+    byt_f = 2 * (M * H * 2 + V * H) + 4 * M * (2 * ((V + 255) // 256) + 5)
+    byt_b = 2 * (V * H * 3 + M * V * 3 + M * H * 3) + 4 * V * H
+    for name, ms, fl, by, nl in (("lm_head_xent_forward_N1", ms_f, flop, byt_f, 3),
+                                 ("lm_head_xent_backward_N1", ms_b, 3 * flop, byt_b, 5)):
+        roof = max(fl / (pk["bf16_sus"] * 1e12), by / (pk["hbm"] * 1e9)) * 1e3
+        out[name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "roofline_ms": roof, "roofline_frac": roof / ms,
+                     "tokens_per_s": M / (ms * 1e-3), "launches": nl, "vocab": V}
+    del hl, gl, Wv, tg, ul, el, dhl, dWv, wsb, wsx
+    torch.cuda.empty_cache()
     return out
 
 

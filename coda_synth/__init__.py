@@ -12,6 +12,8 @@ listed; N(mu, sigma) uses sigma as the standard deviation):
   block (1B-shaped): O, R [M, H] ~ N(0,1); W_o [H, H], W_gu [2F, H], W_d [H, F] ~ N(0, w_std);
                      g ~ 1 + N(0, 0.1); dY [M, H] ~ N(0,1)
   qkv:               h [M, H] ~ N(0,1); W_qkv [n_qkv, H] ~ N(0, w_std); g ~ 1 + N(0, 0.1)
+  lm head:           h [M, H] ~ N(0,1); g ~ 1 + N(0, 0.1); W_v [V, H] ~ N(0, w_std);
+                     targets ~ uniform integers in [0, V) (V = 128256 for LLaMA-3)
   fp8 mlp:           h [M, H] ~ N(0,1); W_gu [2F, H], W_d [H, F] ~ N(0, w_std);
                      e4m3 operands with per-tensor scales amax/448.  The fp8 gate/up
                      weight is taken as the effective weight (any RMSNorm gain already
@@ -87,3 +89,14 @@ def fp8_mlp_inputs(M, H, F, seed=0, w_std=0.015):
     Wq, s_w = _to_e4m3(W_gu)
     Wdq, s_wd = _to_e4m3(W_d)
     return dict(h=h, Xq=Xq, s_x=s_x, Wq=Wq, s_w=s_w, Wdq=Wdq, s_wd=s_wd, eps=1e-6)
+
+
+def lm_head_inputs(M, H, V, seed=0, w_std=0.02, dtype=torch.bfloat16):
+    gen = torch.Generator().manual_seed(seed)
+    return dict(
+        h=_normal(gen, (M, H)).to(dtype),
+        g=_normal(gen, (H,), std=0.1, mean=1.0),
+        W_v=_normal(gen, (V, H), std=w_std).to(dtype),
+        targets=torch.randint(0, V, (M,), generator=gen, dtype=torch.int32),
+        eps=1e-6,
+    )

@@ -27,16 +27,17 @@ F32, BF16, E4M3 = 0, 1, 2
 ROW_MAJOR, COL_MAJOR = 0, 1
 OP_TENSOR_SCALE, OP_ROW_SCALE, OP_COL_SCALE, OP_ADD_SIDE, OP_SWIGLU, OP_ROPE = 1, 2, 3, 4, 5, 6
 OP_SWIGLU_BWD, OP_RMSBWD_COMBINE, OP_ROW_SUMSQ_PARTIAL, OP_ROW_DOT_PARTIAL = 7, 8, 9, 10
-OP_COL_DOT_PARTIAL, OP_AMAX, OP_STORE_AUX, OP_STORE_COL_SCALED = 11, 12, 13, 14
+OP_COL_DOT_PARTIAL, OP_AMAX, OP_STORE_AUX, OP_STORE_COL_SCALED, OP_XENT_PARTIAL, OP_XENT_BWD = 11, 12, 13, 14, 15, 16
 REDUCE_RSQRT_MEAN, REDUCE_SCALE_SUM = 0, 1
-WS_BLOCK_FWD, WS_BLOCK_BWD = 0, 1
+WS_BLOCK_FWD, WS_BLOCK_BWD, WS_XENT_FWD, WS_XENT_BWD = 0, 1, 2, 3
 MAX_OPS = 8
 
 EXPORTED = [
     "coda_gemm_epilogue", "coda_rms_partial_reduce", "coda_row_rms", "coda_col_reduce", "coda_fold_gain",
     "coda_rope_table", "coda_block_forward", "coda_block_backward", "coda_qkv_rope", "coda_mlp_fp8",
     "coda_workspace_size", "coda_get_device_status", "coda_set_watchdog_ms", "coda_inject_dropped_stage",
-    "coda_device_sm_count", "coda_status_string", "coda_version", "coda_block_forward_noalloc",
+    "coda_device_sm_count", "coda_status_string", "coda_version", "coda_block_forward_noalloc", "coda_rms_gain",
+    "coda_xent_combine", "coda_lm_head_xent_forward", "coda_lm_head_xent_backward",
 ]
 NOALLOC_MAX_PARTIALS = 1 << 20
 
@@ -66,12 +67,13 @@ class CodaSide(Structure):
                 ("col_scale", c_void_p), ("aux_in", POINTER(CodaTensor)), ("aux_in2", POINTER(CodaTensor)),
                 ("rope_cos", c_void_p), ("rope_sin", c_void_p), ("rope_seq_len", c_int32),
                 ("rope_head_dim", c_int32), ("rope_ncols", c_int32), ("tensor_scale", c_float),
-                ("out_scale", c_float)]
+                ("out_scale", c_float), ("row_index", c_void_p)]
 
 
 class CodaAux(Structure):
     _fields_ = [("row_partials", c_void_p), ("row_partials_ld", c_int64), ("col_partials", c_void_p),
-                ("col_partials_ld", c_int64), ("store_aux", POINTER(CodaTensor)), ("amax", c_void_p)]
+                ("col_partials_ld", c_int64), ("store_aux", POINTER(CodaTensor)), ("amax", c_void_p),
+                ("row_partials2", c_void_p), ("row_values", c_void_p)]
 
 
 class CodaBlockFwd(Structure):
@@ -100,6 +102,19 @@ class CodaMlpFp8(Structure):
                 ("s_w", c_float), ("s_wd", c_float), ("s_a", c_float), ("h", c_void_p), ("X_q", c_void_p),
                 ("W_q", c_void_p), ("W_dq", c_void_p), ("r", c_void_p), ("a_q", c_void_p), ("amax", c_void_p),
                 ("Y", c_void_p), ("Y_partials", c_void_p)]
+
+
+class CodaXentFwd(Structure):
+    _fields_ = [("M", c_int64), ("H", c_int64), ("V", c_int64), ("eps", c_float), ("h", c_void_p), ("g", c_void_p),
+                ("W_v", c_void_p), ("targets", c_void_p), ("u", c_void_p), ("r", c_void_p), ("lse", c_void_p),
+                ("loss", c_void_p), ("loss_mean", c_void_p), ("workspace", c_void_p)]
+
+
+class CodaXentBwd(Structure):
+    _fields_ = [("M", c_int64), ("H", c_int64), ("V", c_int64), ("dloss", c_float), ("h", c_void_p),
+                ("g", c_void_p), ("W_v", c_void_p), ("targets", c_void_p), ("u", c_void_p), ("r", c_void_p),
+                ("lse", c_void_p), ("e", c_void_p), ("dh", c_void_p), ("dW_v", c_void_p), ("dg", c_void_p),
+                ("c", c_void_p), ("workspace", c_void_p)]
 
 
 # --------------------------------------------------------------------- the library
@@ -134,6 +149,11 @@ def lib():
         "coda_set_watchdog_ms": [c_uint32],
         "coda_inject_dropped_stage": [c_int32],
         "coda_device_sm_count": [P(c_int32)],
+        "coda_rms_gain": [P(CodaTensor), c_void_p, c_float, c_void_p, P(CodaTensor), c_void_p],
+        "coda_xent_combine": [c_void_p, c_void_p, c_int64, c_int32, c_int64, c_void_p, c_void_p, c_int64, c_void_p,
+                              c_void_p, c_void_p, c_void_p],
+        "coda_lm_head_xent_forward": [P(CodaXentFwd), c_void_p],
+        "coda_lm_head_xent_backward": [P(CodaXentBwd), c_void_p],
     }
     for name, args in sigs.items():
         fn = getattr(L, name)
@@ -208,8 +228,10 @@ def program(*ops) -> CodaProgram:
 def coda_gemm_epilogue(A, W, ops, out, *, residual=None, row_scale=None, row_coef=None, col_scale=None,
                        aux_in=None, aux_in2=None, rope_cos=None, rope_sin=None, rope_seq_len=0, rope_head_dim=0,
                        rope_ncols=0, tensor_scale=1.0, out_scale=1.0, row_partials=None, col_partials=None,
-                       store_aux=None, amax=None, stream=None):
-    """out = epilogue(ops, A . W^T); see include/coda.h for the programs."""
+                       store_aux=None, amax=None, row_index=None, row_partials2=None, row_values=None,
+                       out_shape=None, stream=None):
+    """out = epilogue(ops, A . W^T); see include/coda.h for the programs.  For XENT_PARTIAL
+    (no output tile) pass out=None and out_shape=(M, V)."""
     keep = []
 
     def tp(t):
@@ -220,11 +242,16 @@ def coda_gemm_epilogue(A, W, ops, out, *, residual=None, row_scale=None, row_coe
         return ctypes.pointer(d)
 
     side = CodaSide(tp(residual), _ptr(row_scale), _ptr(row_coef), _ptr(col_scale), tp(aux_in), tp(aux_in2),
-                    _ptr(rope_cos), _ptr(rope_sin), rope_seq_len, rope_head_dim, rope_ncols, tensor_scale, out_scale)
+                    _ptr(rope_cos), _ptr(rope_sin), rope_seq_len, rope_head_dim, rope_ncols, tensor_scale, out_scale,
+                    _ptr(row_index))
     aux = CodaAux(_ptr(row_partials), row_partials.stride(0) if row_partials is not None else 0,
                   _ptr(col_partials), col_partials.stride(0) if col_partials is not None else 0,
-                  tp(store_aux), _ptr(amax))
-    a, w, o = desc(A), desc(W), desc(out)
+                  tp(store_aux), _ptr(amax), _ptr(row_partials2), _ptr(row_values))
+    a, w = desc(A), desc(W)
+    if out is None:
+        o = CodaTensor(None, BF16, ROW_MAJOR, out_shape[0], out_shape[1], max(out_shape[1], 1))
+    else:
+        o = desc(out)
     prog = program(*ops)
     st = lib().coda_gemm_epilogue(ctypes.byref(a), ctypes.byref(w), ctypes.byref(prog), ctypes.byref(side),
                                   ctypes.byref(o), ctypes.byref(aux), _stream(stream))
@@ -257,6 +284,35 @@ def coda_fold_gain(W, g, W_out, stream=None):
 def coda_rope_table(seq_len, head_dim, base, cos_out, sin_out, stream=None):
     st = lib().coda_rope_table(seq_len, head_dim, base, _ptr(cos_out), _ptr(sin_out), _stream(stream))
     _check(st, "coda_rope_table")
+
+
+def coda_rms_gain(X, g, eps, r_out, u_out, stream=None):
+    x, u = desc(X), desc(u_out)
+    _check(lib().coda_rms_gain(ctypes.byref(x), _ptr(g), eps, _ptr(r_out), ctypes.byref(u), _stream(stream)),
+           "coda_rms_gain")
+
+
+def coda_xent_combine(Pm, Ps, target_logit, targets, V, lse, loss, mean=None, stream=None):
+    nparts, M = Pm.shape[0], lse.shape[0]
+    st = lib().coda_xent_combine(_ptr(Pm), _ptr(Ps), Pm.stride(0), nparts, M, _ptr(target_logit), _ptr(targets), V,
+                                 _ptr(lse), _ptr(loss), _ptr(mean), _stream(stream))
+    _check(st, "coda_xent_combine")
+
+
+def coda_lm_head_xent_forward(h, g, W_v, targets, eps, u, r, lse, loss, loss_mean, workspace, stream=None):
+    M, H = h.shape
+    V = W_v.shape[0]
+    io = CodaXentFwd(M, H, V, eps, _ptr(h), _ptr(g), _ptr(W_v), _ptr(targets), _ptr(u), _ptr(r), _ptr(lse),
+                     _ptr(loss), _ptr(loss_mean), _ptr(workspace))
+    _check(lib().coda_lm_head_xent_forward(ctypes.byref(io), _stream(stream)), "coda_lm_head_xent_forward")
+
+
+def coda_lm_head_xent_backward(h, g, W_v, targets, u, r, lse, dloss, e, dh, dW_v, dg, c, workspace, stream=None):
+    M, H = h.shape
+    V = W_v.shape[0]
+    io = CodaXentBwd(M, H, V, dloss, _ptr(h), _ptr(g), _ptr(W_v), _ptr(targets), _ptr(u), _ptr(r), _ptr(lse),
+                     _ptr(e), _ptr(dh), _ptr(dW_v), _ptr(dg), _ptr(c), _ptr(workspace))
+    _check(lib().coda_lm_head_xent_backward(ctypes.byref(io), _stream(stream)), "coda_lm_head_xent_backward")
 
 
 def coda_workspace_size(which, M, H, F):

@@ -154,6 +154,13 @@ const ProgramTemplate kPrograms[] = {
      3,
      {{CODA_OP_SWIGLU_BWD, false}, {CODA_OP_ROW_SCALE, true}, {CODA_OP_ROW_DOT_PARTIAL, false}}},
     {EPI_RMSBWD, 2, {{CODA_OP_RMSBWD_COMBINE, false}, {CODA_OP_COL_DOT_PARTIAL, false}}},
+    {EPI_XENT, 3, {{CODA_OP_TENSOR_SCALE, true}, {CODA_OP_ROW_SCALE, true}, {CODA_OP_XENT_PARTIAL, false}}},
+    {EPI_XENT_BWD,
+     4,
+     {{CODA_OP_TENSOR_SCALE, true},
+      {CODA_OP_ROW_SCALE, true},
+      {CODA_OP_XENT_BWD, false},
+      {CODA_OP_ROW_DOT_PARTIAL, false}}},
 };
 
 // Returns the compiled program index and the set of ops present (bit op), or -1.
@@ -264,10 +271,15 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
   int st;
   if ((st = check_tensor(A, true)) != CODA_OK) return st;
   if ((st = check_tensor(W, true)) != CODA_OK) return st;
-  if ((st = check_tensor(out, false)) != CODA_OK) return st;
   uint32_t present = 0;
   const int epi = match_program(prog, &present);
   if (epi < 0) return CODA_ERR_UNSUPPORTED_PROGRAM;
+  if (epi == EPI_XENT) {   // the logits are never stored: out only gives their shape
+    if (!out) return CODA_ERR_NULL;
+    if (out->rows < 0 || out->cols < 0 || out->rows > kMaxDim || out->cols > kMaxDim) return CODA_ERR_SHAPE;
+  } else if ((st = check_tensor(out, false)) != CODA_OK) {
+    return st;
+  }
   auto has = [&](int op) { return (present >> op) & 1u; };
 
   // operand kind
@@ -311,10 +323,12 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
   }
   if (epi == EPI_RMSBWD) {
     if ((st = check_tensor(sd.aux_in, false)) != CODA_OK) return st;
-    if ((st = check_tensor(sd.aux_in2, false)) != CODA_OK) return st;
-    if (sd.aux_in->rows != M || sd.aux_in->cols != N || sd.aux_in2->rows != M || sd.aux_in2->cols != N)
-      return CODA_ERR_SHAPE;
-    if (sd.aux_in->dtype != sd.aux_in2->dtype) return CODA_ERR_DTYPE;
+    if (sd.aux_in2 && (st = check_tensor(sd.aux_in2, false)) != CODA_OK) return st;
+    if (sd.aux_in->rows != M || sd.aux_in->cols != N) return CODA_ERR_SHAPE;
+    if (sd.aux_in2) {
+      if (sd.aux_in2->rows != M || sd.aux_in2->cols != N) return CODA_ERR_SHAPE;
+      if (sd.aux_in->dtype != sd.aux_in2->dtype) return CODA_ERR_DTYPE;
+    }
     side_dt = to_dt(sd.aux_in->dtype);
     if (!sd.col_scale || !sd.row_coef) return CODA_ERR_NULL;
     if (!aligned16(sd.col_scale)) return CODA_ERR_ALIGN;
@@ -332,6 +346,12 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
       return CODA_ERR_SHAPE;
   }
   if (has(CODA_OP_AMAX) && !ax.amax) return CODA_ERR_NULL;
+  if (epi == EPI_XENT || epi == EPI_XENT_BWD) {
+    if (!sd.row_index) return CODA_ERR_NULL;
+    if (epi == EPI_XENT && (!ax.row_partials || !ax.row_partials2 || !ax.row_values)) return CODA_ERR_NULL;
+    if (epi == EPI_XENT && ax.row_partials_ld < M) return CODA_ERR_SHAPE;
+    if (epi == EPI_XENT_BWD && !sd.row_coef) return CODA_ERR_NULL;
+  }
   const int bn_out = epi == EPI_SWIGLU ? 128 : 256;
   const int64_t n_tiles = (N + bn_out - 1) / bn_out;
   if (has(CODA_OP_ROW_SUMSQ_PARTIAL) || has(CODA_OP_ROW_DOT_PARTIAL)) {
@@ -376,14 +396,15 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
   else
     st = encode_2d(&L.tmB, W->dtype, W->ptr, K, W->rows, W->ld, bk, 128);
   if (st != CODA_OK) return st;
-  if ((st = encode_2d(&L.tmOut, out->dtype, out->ptr, out->cols, M, out->ld, 32, 32)) != CODA_OK) return st;
+  if (epi != EPI_XENT && (st = encode_2d(&L.tmOut, out->dtype, out->ptr, out->cols, M, out->ld, 32, 32)) != CODA_OK)
+    return st;
   if (epi == EPI_RESID) {
     const coda_tensor* r = sd.residual;
     if ((st = encode_2d(&L.tmSide0, r->dtype, r->ptr, r->cols, M, r->ld, 32, 32)) != CODA_OK) return st;
   } else if (epi == EPI_SWIGLU_BWD || epi == EPI_RMSBWD) {
     const coda_tensor* r = sd.aux_in;
     if ((st = encode_2d(&L.tmSide0, r->dtype, r->ptr, r->cols, M, r->ld, 32, 32)) != CODA_OK) return st;
-    if (epi == EPI_RMSBWD) {
+    if (epi == EPI_RMSBWD && sd.aux_in2) {
       const coda_tensor* r2 = sd.aux_in2;
       if ((st = encode_2d(&L.tmSide1, r2->dtype, r2->ptr, r2->cols, M, r2->ld, 32, 32)) != CODA_OK) return st;
     }
@@ -408,14 +429,15 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
     p.group_n = (int)gn;
   }
   p.flags = (has(CODA_OP_ROW_SUMSQ_PARTIAL) ? F_PARTIAL : 0) | (has(CODA_OP_AMAX) ? F_AMAX : 0) |
-            (has(CODA_OP_COL_SCALE) ? F_COLSCALE : 0) | (has(CODA_OP_ROW_SCALE) ? F_ROWSCALE : 0);
+            (has(CODA_OP_COL_SCALE) ? F_COLSCALE : 0) | (has(CODA_OP_ROW_SCALE) ? F_ROWSCALE : 0) |
+            (epi == EPI_RMSBWD && !sd.aux_in2 ? F_NO_SIDE1 : 0);
   if (g_inject_once) {
     p.flags |= F_INJECT_SKIP;
     g_inject_once = 0;
   }
   p.up_offset = (int)N;
   p.tensor_scale = has(CODA_OP_TENSOR_SCALE) ? sd.tensor_scale : 1.0f;
-  p.out_scale = (out->dtype == CODA_E4M3) ? sd.out_scale : 1.0f;
+  p.out_scale = (out->dtype == CODA_E4M3 || epi == EPI_XENT_BWD) ? sd.out_scale : 1.0f;
   p.row_scale = sd.row_scale;
   p.row_coef = sd.row_coef;
   p.col_scale = sd.col_scale;
@@ -428,6 +450,9 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
   p.row_part_ld = ax.row_partials_ld;
   p.col_part = ax.col_partials;
   p.col_part_ld = ax.col_partials_ld;
+  p.row_part2 = ax.row_partials2;
+  p.row_out = ax.row_values;
+  p.row_index = sd.row_index;
   p.amax = reinterpret_cast<unsigned int*>(ax.amax);
   p.status = d->status;
   p.timeout_ns = (unsigned long long)g_watchdog_ms * 1000000ull;
@@ -503,11 +528,43 @@ int coda_rope_table(int32_t seq_len, int32_t head_dim, double base, float* cos_o
   return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
 }
 
+int coda_rms_gain(const coda_tensor* X, const float* g, float eps, float* r_out, const coda_tensor* u_out,
+                  void* stream) {
+  int st;
+  if ((st = check_tensor(X, false)) != CODA_OK) return st;
+  if ((st = check_tensor(u_out, false)) != CODA_OK) return st;
+  if (!r_out || !g) return CODA_ERR_NULL;
+  if (!aligned16(g)) return CODA_ERR_ALIGN;
+  if (X->dtype != CODA_BF16 || u_out->dtype != CODA_BF16) return CODA_ERR_DTYPE;
+  if (X->cols < 1 || X->cols % 8 != 0 || u_out->rows != X->rows || u_out->cols != X->cols) return CODA_ERR_SHAPE;
+  if (X->rows == 0) return CODA_OK;
+  DevState* dv;
+  if ((st = ensure_device(&dv)) != CODA_OK) return st;
+  cudaError_t e = launch_rms_gain(X->ptr, X->rows, X->cols, X->ld, g, eps, r_out, u_out->ptr, u_out->ld,
+                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
+}
+
+int coda_xent_combine(const float* Pm, const float* Ps, int64_t ld, int32_t nparts, int64_t M,
+                      const float* target_logit, const int32_t* targets, int64_t V, float* lse, float* loss,
+                      float* mean, void* stream) {
+  if (!Pm || !Ps || !target_logit || !targets || !lse || !loss) return CODA_ERR_NULL;
+  if (M < 0 || nparts < 1 || ld < M || V < 1) return CODA_ERR_SHAPE;
+  if (M == 0) return CODA_OK;
+  DevState* dv;
+  int st = ensure_device(&dv);
+  if (st != CODA_OK) return st;
+  cudaError_t e = launch_xent_reduce(Pm, Ps, ld, nparts, M, target_logit, targets, V, lse, loss, mean,
+                                     static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
+}
+
 size_t coda_workspace_size(int32_t which, int64_t M, int64_t H, int64_t F) {
   if (M < 0 || H < 0 || F < 0) return 0;
   if (which == CODA_WS_BLOCK_FWD) return (size_t)((H + 255) / 256) * (size_t)M * sizeof(float);
-  if (which == CODA_WS_BLOCK_BWD)
+  if (which == CODA_WS_BLOCK_BWD || which == CODA_WS_XENT_BWD)
     return ((size_t)((F + 255) / 256) * (size_t)M + (size_t)((M + 31) / 32) * (size_t)H) * sizeof(float);
+  if (which == CODA_WS_XENT_FWD) return (size_t)(2 * ((F + 255) / 256) + 1) * (size_t)M * sizeof(float);
   return 0;
 }
 
@@ -676,6 +733,93 @@ int coda_block_backward(const coda_block_bwd* io, void* stream) {
   {
     coda_tensor A = mk(io->dh, CODA_BF16, H, M, H, CODA_COL_MAJOR), W = mk(io->O, CODA_BF16, H, M, H, CODA_COL_MAJOR);
     coda_tensor out = mk(io->dW_o, CODA_F32, H, H, H);
+    coda_epilogue_program pg = prog_of({});
+    if ((st = coda_gemm_epilogue(&A, &W, &pg, nullptr, &out, nullptr, stream)) != CODA_OK) return st;
+  }
+  return CODA_OK;
+}
+
+int coda_lm_head_xent_forward(const coda_lm_head_xent_io* io, void* stream) {
+  if (!io) return CODA_ERR_NULL;
+  if (!io->h || !io->g || !io->W_v || !io->targets || !io->u || !io->r || !io->lse || !io->loss || !io->loss_mean ||
+      !io->workspace)
+    return CODA_ERR_NULL;
+  const int64_t M = io->M, H = io->H, V = io->V;
+  if (M < 0 || H < 8 || H % 8 != 0 || V < 32 || V % 32 != 0) return CODA_ERR_SHAPE;
+  if (M == 0) return CODA_OK;
+  int st;
+  const int64_t np = (V + 255) / 256;
+  float* Pm = io->workspace;
+  float* Ps = io->workspace + np * M;
+  float* T = io->workspace + 2 * np * M;
+  coda_tensor h = mk(io->h, CODA_BF16, M, H, H), u = mk(io->u, CODA_BF16, M, H, H);
+  if ((st = coda_rms_gain(&h, io->g, io->eps, io->r, &u, stream)) != CODA_OK) return st;
+  {
+    coda_tensor W = mk(io->W_v, CODA_BF16, V, H, H), z = mk(nullptr, CODA_BF16, M, V, V);
+    coda_epilogue_program pg = prog_of({CODA_OP_ROW_SCALE, CODA_OP_XENT_PARTIAL});
+    coda_side_inputs sd{};
+    sd.row_scale = io->r;
+    sd.row_index = io->targets;
+    coda_aux_outputs ax{};
+    ax.row_partials = Pm;
+    ax.row_partials2 = Ps;
+    ax.row_partials_ld = M;
+    ax.row_values = T;
+    if ((st = coda_gemm_epilogue(&u, &W, &pg, &sd, &z, &ax, stream)) != CODA_OK) return st;
+  }
+  return coda_xent_combine(Pm, Ps, M, (int32_t)np, M, T, io->targets, V, io->lse, io->loss, io->loss_mean, stream);
+}
+
+int coda_lm_head_xent_backward(const coda_lm_head_xent_bwd_io* io, void* stream) {
+  if (!io) return CODA_ERR_NULL;
+  if (!io->h || !io->g || !io->W_v || !io->targets || !io->u || !io->r || !io->lse || !io->e || !io->dh ||
+      !io->dW_v || !io->dg || !io->c || !io->workspace)
+    return CODA_ERR_NULL;
+  const int64_t M = io->M, H = io->H, V = io->V;
+  if (M < 0 || H < 32 || H % 32 != 0 || V < 32 || V % 32 != 0) return CODA_ERR_SHAPE;
+  if (M == 0) return CODA_OK;
+  int st;
+  const int64_t np = (V + 255) / 256;
+  float* S = io->workspace;              // [np, M] row partials of e . z
+  float* Dg = io->workspace + np * M;    // [ceil(M/32), H] column partials of h t
+  coda_tensor u = mk(io->u, CODA_BF16, M, H, H), e = mk(io->e, CODA_BF16, M, V, V);
+  // e = r dloss (softmax - onehot) / M, logits recomputed; row partials of e . z
+  {
+    coda_tensor W = mk(io->W_v, CODA_BF16, V, H, H);
+    coda_epilogue_program pg = prog_of({CODA_OP_ROW_SCALE, CODA_OP_XENT_BWD, CODA_OP_ROW_DOT_PARTIAL});
+    coda_side_inputs sd{};
+    sd.row_scale = io->r;
+    sd.row_coef = io->lse;
+    sd.row_index = io->targets;
+    sd.out_scale = io->dloss / (float)M;
+    coda_aux_outputs ax{};
+    ax.row_partials = S;
+    ax.row_partials_ld = M;
+    if ((st = coda_gemm_epilogue(&u, &W, &pg, &sd, &e, &ax, stream)) != CODA_OK) return st;
+  }
+  // c = r s / H
+  if ((st = coda_rms_partial_reduce(S, M, (int32_t)np, M, H, 0.f, CODA_REDUCE_SCALE_SUM, io->r, io->c, stream)) !=
+      CODA_OK)
+    return st;
+  // t = e W_v;  dh = g t - c h;  column partials of h t
+  {
+    coda_tensor W = mk(io->W_v, CODA_BF16, H, V, H, CODA_COL_MAJOR);   // logical W_v^T
+    coda_tensor h = mk(io->h, CODA_BF16, M, H, H), out = mk(io->dh, CODA_BF16, M, H, H);
+    coda_epilogue_program pg = prog_of({CODA_OP_RMSBWD_COMBINE, CODA_OP_COL_DOT_PARTIAL});
+    coda_side_inputs sd{};
+    sd.aux_in = &h;
+    sd.col_scale = io->g;
+    sd.row_coef = io->c;
+    coda_aux_outputs ax{};
+    ax.col_partials = Dg;
+    ax.col_partials_ld = H;
+    if ((st = coda_gemm_epilogue(&e, &W, &pg, &sd, &out, &ax, stream)) != CODA_OK) return st;
+  }
+  if ((st = coda_col_reduce(Dg, (M + 31) / 32, H, H, io->dg, stream)) != CODA_OK) return st;
+  // dW_v = e^T u
+  {
+    coda_tensor A = mk(io->e, CODA_BF16, V, M, V, CODA_COL_MAJOR), W = mk(io->u, CODA_BF16, H, M, H, CODA_COL_MAJOR);
+    coda_tensor out = mk(io->dW_v, CODA_F32, V, H, H);
     coda_epilogue_program pg = prog_of({});
     if ((st = coda_gemm_epilogue(&A, &W, &pg, nullptr, &out, nullptr, stream)) != CODA_OK) return st;
   }

@@ -58,7 +58,11 @@ enum : int {
                        //   [+ saved Z, + amax |silu(Zg) * Zu|]
   EPI_ROPE = 4,        // out = rope(ts * r_row * acc) on the first rope_ncols columns
   EPI_SWIGLU_BWD = 5,  // e = r_row * [dA * Zu * silu'(Zg) | dA * silu(Zg)]; row partial sum e . Z
-  EPI_RMSBWD = 6,      // out = g_col * acc - c_row * h + dY; column partial sum h * acc
+  EPI_RMSBWD = 6,      // out = g_col * acc - c_row * h [+ dY]; column partial sum h * acc
+  EPI_XENT = 7,        // z = ts * r_row * acc (logits, never stored): per tile and row the online
+                       //   state (max_j z, sum_j exp(z - max)) and the target's logit
+  EPI_XENT_BWD = 8,    // z as above; e = r_row * os * (exp(z - lse_row) - [j == target_row]);
+                       //   row partial sum e . z
 };
 
 enum : int {
@@ -66,6 +70,7 @@ enum : int {
   F_AMAX = 4,       // accumulate amax (EPI_SWIGLU)
   F_COLSCALE = 8,   // multiply by col_scale (EPI_STORE)
   F_ROWSCALE = 16,  // multiply by row_scale (EPI_SWIGLU / EPI_ROPE / EPI_ROWSCALE / EPI_SWIGLU_BWD)
+  F_NO_SIDE1 = 32,  // EPI_RMSBWD without the dY side input
   F_INJECT_SKIP = 1 << 30,  // test hook: the producer drops its first k-block
 };
 
@@ -95,6 +100,9 @@ struct GemmParams {
   int rope_seq_len, rope_head_dim, rope_ncols;
   float* row_part;        // [n_tiles, row_part_ld]
   long long row_part_ld;
+  float* row_part2;       // EPI_XENT: sum-exp partials, same layout as row_part (the maxima)
+  float* row_out;         // EPI_XENT: [M] logit of each row's target
+  const int* row_index;   // EPI_XENT / EPI_XENT_BWD: [M] target class of each row
   float* col_part;        // [4 * m_tiles, col_part_ld]
   long long col_part_ld;
   unsigned int* amax;     // fp32 bits, atomic max (non-negative values order as integers)
@@ -119,7 +127,7 @@ struct GemmCfg {
   static constexpr int BN_OUT = DUAL ? 128 : 256;  // output columns per tile
   static constexpr int NCHUNK = BN_OUT / 32;
   static constexpr int NS = EPI == EPI_RESID ? 1 : (EPI == EPI_SWIGLU_BWD || EPI == EPI_RMSBWD) ? 2 : 0;
-  static constexpr int NO = EPI == EPI_SWIGLU_BWD ? 2 : 1;
+  static constexpr int NO = EPI == EPI_SWIGLU_BWD ? 2 : EPI == EPI_XENT ? 0 : 1;   // XENT stores no tile
   static constexpr int OSLOT = 32 * 32 * dt_bytes(OUT_DT);  // one 32 x 32 staging block
   static constexpr int SSLOT = 32 * 32 * dt_bytes(SIDE_DT);
   static constexpr int XSLOT = 32 * 32 * 2;                 // aux output block (bf16)
@@ -494,7 +502,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int slot = c & 1;
           const uint32_t sbar = SIDE_BAR(ew, slot);
           const uint32_t dst = side_base + slot * C::NS * C::SSLOT;
-          ptx::mbar_arrive_expect_tx(sbar, C::NS * C::SSLOT);
+          const bool side1 = C::NS > 1 && !(p.flags & F_NO_SIDE1);
+          ptx::mbar_arrive_expect_tx(sbar, (side1 ? C::NS : 1) * C::SSLOT);
           if constexpr (C::EPI == EPI_RESID) {
             ptx::tma_load_2d_hint(dst, &tmSide0, n0 + 32 * c, r0, sbar, stream_pol);
           } else if constexpr (C::EPI == EPI_SWIGLU_BWD) {
@@ -502,7 +511,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::tma_load_2d_hint(dst + C::SSLOT, &tmSide0, p.up_offset + n0 + 32 * c, r0, sbar, stream_pol);
           } else {
             ptx::tma_load_2d_hint(dst, &tmSide0, n0 + 32 * c, r0, sbar, stream_pol);
-            ptx::tma_load_2d_hint(dst + C::SSLOT, &tmSide1, n0 + 32 * c, r0, sbar, stream_pol);
+            if (side1) ptx::tma_load_2d_hint(dst + C::SSLOT, &tmSide1, n0 + 32 * c, r0, sbar, stream_pol);
           }
         }
       };
@@ -519,9 +528,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
       float rs = 1.f, rc = 0.f;
       if ((p.flags & F_ROWSCALE) && row_ok) rs = __ldg(p.row_scale + row);
-      if constexpr (C::EPI == EPI_RMSBWD) {
-        if (row_ok) rc = __ldg(p.row_coef + row);
+      if constexpr (C::EPI == EPI_RMSBWD || C::EPI == EPI_XENT_BWD) {
+        if (row_ok) rc = __ldg(p.row_coef + row);   // c (RMSNorm backward) or lse (cross-entropy)
       }
+      int target = -1;
+      if constexpr (C::EPI == EPI_XENT || C::EPI == EPI_XENT_BWD) {
+        if (row_ok) target = __ldg(p.row_index + row);
+      }
+      float xmax = -INFINITY, xsum = 0.f, xtgt = 0.f;   // online softmax state of this row's tile
       const float ts = p.tensor_scale;
 
       ok = bwait(TFULL_BAR(acc), aph, watch, SITE_EPI_TMEM_FULL);
@@ -577,7 +591,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             side_pending &= ~(1u << slot);
             const uint32_t src = side_base + slot * C::NS * C::SSLOT;
             slot_read<C::SIDE_DT>(src, lane, s0);
-            if constexpr (C::NS > 1) slot_read<C::SIDE_DT>(src + C::SSLOT, lane, s1);
+            if constexpr (C::NS > 1) {
+              if (p.flags & F_NO_SIDE1) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) s1[j] = 0.f;
+              } else {
+                slot_read<C::SIDE_DT>(src + C::SSLOT, lane, s1);
+              }
+            }
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
@@ -683,6 +704,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             x[j] = eg;
             o1[j] = eu;
           }
+        } else if constexpr (C::EPI == EPI_XENT) {
+          // P4 / P5: block log-sum-exp with the running (max, sum-exp) state of the row
+          const float sc = ts * rs;
+          float cm = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            x[j] = (col0 + j < p.N) ? x[j] * sc : -INFINITY;
+            cm = fmaxf(cm, x[j]);
+          }
+          if (cm > xmax) {
+            xsum *= __expf(xmax - cm);
+            xmax = cm;
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            xsum += __expf(x[j] - xmax);
+            if (col0 + j == target) xtgt = x[j];
+          }
+        } else if constexpr (C::EPI == EPI_XENT_BWD) {
+          const float sc = ts * rs;
+          const float gs = rs * p.out_scale;   // r * dloss / M
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const bool in = col0 + j < p.N;
+            const float z = x[j] * sc;
+            const float pj = in ? __expf(z - rc) : 0.f;
+            const float e = as_stored<C::OUT_DT>(gs * (pj - (col0 + j == target ? 1.f : 0.f)));
+            rowacc = in ? fmaf(e, z, rowacc) : rowacc;
+            x[j] = e;
+          }
         } else if constexpr (C::EPI == EPI_RMSBWD) {
           float ht[32];
           const float4* g4 = reinterpret_cast<const float4*>(p.col_scale + col0);
@@ -702,6 +753,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
 
         // ---------------------------------------------------------------- stage + store
+        if constexpr (C::NO == 0) continue;
         const bool store = col0 < p.N && r0 < p.M;
         const uint32_t oslot = out_base + (c & 1) * C::OUTSET;
         if (lane == 0) ptx::bulk_wait_read<1>();  // the group that last used this set is done reading
@@ -725,9 +777,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       if (!ok) break;
-      if constexpr (C::EPI == EPI_RESID || C::EPI == EPI_SWIGLU_BWD) {
-        if ((C::EPI == EPI_SWIGLU_BWD || (p.flags & F_PARTIAL)) && row_ok)
+      if constexpr (C::EPI == EPI_RESID || C::EPI == EPI_SWIGLU_BWD || C::EPI == EPI_XENT_BWD) {
+        if ((C::EPI != EPI_RESID || (p.flags & F_PARTIAL)) && row_ok)
           p.row_part[(size_t)nb * p.row_part_ld + row] = rowacc;
+      }
+      if constexpr (C::EPI == EPI_XENT) {
+        if (row_ok) {
+          p.row_part[(size_t)nb * p.row_part_ld + row] = xmax;
+          p.row_part2[(size_t)nb * p.row_part_ld + row] = xsum;
+          if (target >= n0 && target < n0 + C::BN_OUT) p.row_out[row] = xtgt;
+        }
       }
     }
     if constexpr (C::EPI == EPI_SWIGLU) {

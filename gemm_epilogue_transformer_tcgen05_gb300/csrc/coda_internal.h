@@ -41,6 +41,10 @@ cudaError_t launch_fold_gain(const void* W, int64_t N, int64_t K, int64_t ld_in,
                              int64_t ld_out, bool f32, cudaStream_t s, int sms);
 cudaError_t launch_rope_table(int seq_len, int head_dim, double base, float* cos_out, float* sin_out,
                               cudaStream_t s);
+cudaError_t launch_rms_gain(const void* X, int64_t M, int64_t d, int64_t ld, const float* g, float eps, float* r,
+                            void* U, int64_t ldu, cudaStream_t s);
+cudaError_t launch_xent_reduce(const float* Pm, const float* Ps, int64_t ld, int nparts, int64_t M, const float* T,
+                               const int* targets, int64_t V, float* lse, float* loss, float* mean, cudaStream_t s);
 
 }  // namespace coda
 

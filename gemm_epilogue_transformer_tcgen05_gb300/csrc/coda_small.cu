@@ -89,6 +89,90 @@ cudaError_t launch_row_rms(const void* X, int64_t M, int64_t d, int64_t ld, floa
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- RMS + gain broadcast
+// One warp per row: r = 1 / sqrt(mean x^2 + eps) and u = x * g (bf16), one pass over X.
+__global__ void rms_gain_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, int64_t d, int64_t ld,
+                                const float* __restrict__ g, float eps, float* __restrict__ r,
+                                __nv_bfloat16* __restrict__ U, int64_t ldu) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= M) return;
+  const uint4* src = reinterpret_cast<const uint4*>(X + row * ld);
+  uint4* dst = reinterpret_cast<uint4*>(U + row * ldu);
+  const int64_t nvec = d >> 3;
+  float acc = 0.f;
+  for (int64_t v = lane; v < nvec; v += 32) {
+    const uint4 u = __ldcs(src + v);
+    const float4 g0 = __ldg(reinterpret_cast<const float4*>(g + 8 * v));
+    const float4 g1 = __ldg(reinterpret_cast<const float4*>(g + 8 * v + 4));
+    const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
+      acc = fmaf(lo, lo, fmaf(hi, hi, acc));
+      __nv_bfloat162 b = __floats2bfloat162_rn(lo * gv[2 * e], hi * gv[2 * e + 1]);
+      o[e] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) r[row] = rsqrtf(fmaf(acc, 1.0f / (float)d, eps));
+}
+
+cudaError_t launch_rms_gain(const void* X, int64_t M, int64_t d, int64_t ld, const float* g, float eps, float* r,
+                            void* U, int64_t ldu, cudaStream_t s) {
+  const int rows_per_block = 8;
+  const int64_t blocks = (M + rows_per_block - 1) / rows_per_block;
+  rms_gain_kernel<<<(unsigned)blocks, 32 * rows_per_block, 0, s>>>(static_cast<const __nv_bfloat16*>(X), M, d, ld,
+                                                                    g, eps, r, static_cast<__nv_bfloat16*>(U), ldu);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- cross-entropy combine
+// The light reduce of the per-tile online-softmax states: per row, lse = m + log(sum_t s_t
+// exp(m_t - m)) with m = max_t m_t, in tile order; loss = lse - logit[target] (NaN for a
+// target outside [0, V)).
+__global__ void xent_reduce_kernel(const float* __restrict__ Pm, const float* __restrict__ Ps, int64_t ld, int nparts,
+                                   int64_t M, const float* __restrict__ T, const int* __restrict__ targets, int64_t V,
+                                   float* __restrict__ lse, float* __restrict__ loss) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= M) return;
+  float m = -INFINITY;
+  for (int t = 0; t < nparts; ++t) m = fmaxf(m, __ldg(Pm + (int64_t)t * ld + i));
+  float s = 0.f;
+  for (int t = 0; t < nparts; ++t) s += __ldg(Ps + (int64_t)t * ld + i) * __expf(__ldg(Pm + (int64_t)t * ld + i) - m);
+  const float l = m + __logf(s);
+  lse[i] = l;
+  const int tg = __ldg(targets + i);
+  loss[i] = (tg >= 0 && tg < V) ? l - __ldg(T + i) : __int_as_float(0x7fc00000);
+}
+
+// Mean of n floats by one block: strided partial sums in fixed order, then a fixed tree.
+__global__ void mean_kernel(const float* __restrict__ x, int64_t n, float* __restrict__ out) {
+  __shared__ float red[1024];
+  float s = 0.f;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) s += x[i];
+  red[threadIdx.x] = s;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if ((int)threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) out[0] = red[0] / (float)n;
+}
+
+cudaError_t launch_xent_reduce(const float* Pm, const float* Ps, int64_t ld, int nparts, int64_t M, const float* T,
+                               const int* targets, int64_t V, float* lse, float* loss, float* mean, cudaStream_t s) {
+  const int threads = 256;
+  xent_reduce_kernel<<<(unsigned)((M + threads - 1) / threads), threads, 0, s>>>(Pm, Ps, ld, nparts, M, T, targets, V,
+                                                                                 lse, loss);
+  if (mean) mean_kernel<<<1, 1024, 0, s>>>(loss, M, mean);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- column reduce
 // Block = 32 columns x 8 row-groups; each thread sums a strided subset of the blocks in a
 // fixed order, then the 8 group sums are added in order (deterministic).

@@ -101,8 +101,15 @@ typedef struct coda_tensor {
  *   {SWIGLU_BWD, ROW_SCALE, ROW_DOT_PARTIAL}  acc = dA; with Z = [G | U] from aux_in:
  *        out[:, j] = r dA U silu'(G),  out[:, N + j] = r dA silu(G)   (out is [M, 2N]);
  *        row partials of sum_j out . Z
- *   {RMSBWD_COMBINE, COL_DOT_PARTIAL}         acc = t; h = aux_in, dY = aux_in2:
- *        out = g[j] t - c[i] h + dY; column partials of h * t
+ *   {RMSBWD_COMBINE, COL_DOT_PARTIAL}         acc = t; h = aux_in, dY = aux_in2 (optional):
+ *        out = g[j] t - c[i] h [+ dY]; column partials of h * t
+ *   {[TENSOR_SCALE,] [ROW_SCALE,] XENT_PARTIAL}    z = s * r[i] * acc are logits (never stored;
+ *        out only gives the shape [M, V], its ptr may be NULL); per 256-column tile t and row i:
+ *        aux.row_partials[t, i] = max_j z_ij, aux.row_partials2[t, i] = sum_j exp(z_ij - max),
+ *        and aux.row_values[i] = z[i, side.row_index[i]] (the target's logit)
+ *   {[TENSOR_SCALE,] [ROW_SCALE,] XENT_BWD, ROW_DOT_PARTIAL}   z as above, lse = side.row_coef:
+ *        out = r[i] * out_scale * (exp(z - lse_i) - [j == side.row_index[i]]); row partials of
+ *        sum_j out * z
  */
 enum coda_op {
   CODA_OP_TENSOR_SCALE = 1,      /* acc *= side.tensor_scale */
@@ -118,7 +125,9 @@ enum coda_op {
   CODA_OP_COL_DOT_PARTIAL = 11,  /* aux.col_partials[b, j] = sum over 32-row block b of h * t */
   CODA_OP_AMAX = 12,             /* atomic max of |silu(gate) * up| into *aux.amax */
   CODA_OP_STORE_AUX = 13,        /* save the pre-activation Z to aux.store_aux */
-  CODA_OP_STORE_COL_SCALED = 14  /* also store out[i, j] * side.col_scale[j] to aux.store_aux [M, N] bf16 */
+  CODA_OP_STORE_COL_SCALED = 14, /* also store out[i, j] * side.col_scale[j] to aux.store_aux [M, N] bf16 */
+  CODA_OP_XENT_PARTIAL = 15,     /* online (max, sum-exp) state and target logit per row and tile */
+  CODA_OP_XENT_BWD = 16          /* softmax-minus-onehot gradient of the cross-entropy */
 };
 
 #define CODA_MAX_OPS 8
@@ -140,7 +149,8 @@ typedef struct coda_side_inputs {
   int32_t rope_head_dim;        /* ROPE: 32, 64, 128 or 256 */
   int32_t rope_ncols;           /* ROPE: columns [0, rope_ncols) rotated; multiple of head_dim */
   float tensor_scale;           /* TENSOR_SCALE: s (e.g. s_x * s_w for fp8) */
-  float out_scale;              /* e4m3 output of SWIGLU: multiply by this (1 / s_a) before the cast */
+  float out_scale;              /* e4m3 output of SWIGLU: 1 / s_a before the cast; XENT_BWD: dloss / M */
+  const int32_t* row_index;     /* XENT_PARTIAL, XENT_BWD: [M] target class of each row, in [0, N) */
 } coda_side_inputs;
 
 typedef struct coda_aux_outputs {
@@ -150,6 +160,8 @@ typedef struct coda_aux_outputs {
   int64_t col_partials_ld;      /* >= N */
   const coda_tensor* store_aux; /* STORE_AUX: Z [M, 2N] bf16; STORE_COL_SCALED: [M, N] bf16 */
   float* amax;                  /* AMAX: one float; the caller zeroes it before the call */
+  float* row_partials2;         /* XENT_PARTIAL: sum-exp partials, same layout as row_partials */
+  float* row_values;            /* XENT_PARTIAL: [M] logit of each row's target */
 } coda_aux_outputs;
 
 /* out = epilogue(prog, A . W^T).
@@ -173,6 +185,21 @@ CODA_API int coda_rms_partial_reduce(const float* partials, int64_t ld, int32_t 
 
 /* Full-row RMS scale: r[i] = 1 / sqrt(mean_j X[i, j]^2 + eps) for X bf16 [M, d] ROW_MAJOR. */
 CODA_API int coda_row_rms(const coda_tensor* X, float eps, float* r_out, void* stream);
+
+/* RMS scale and gain broadcast in one pass over X (bf16 [M, d] ROW_MAJOR):
+ *   r[i] = 1 / sqrt(mean_j X[i, j]^2 + eps),  u[i, j] = X[i, j] * g[j] (bf16 [M, d]).
+ * The RMSNorm of a stored activation, split as the deferred-r chains use it. */
+CODA_API int coda_rms_gain(const coda_tensor* X, const float* g, float eps, float* r_out, const coda_tensor* u_out,
+                           void* stream);
+
+/* The light reduce of the cross-entropy partials [KuCoin, "Cinco bloques…": block
+ * log-sum-exp and the max / sum-exp state]: per row, in tile order,
+ *   lse[i] = m + log(sum_t Ps[t, i] exp(Pm[t, i] - m)),  m = max_t Pm[t, i];
+ *   loss[i] = lse[i] - target_logit[i]  (NaN when targets[i] is outside [0, V));
+ *   *mean = sum_i loss[i] / M (fixed-order reduction; mean may be NULL). */
+CODA_API int coda_xent_combine(const float* Pm, const float* Ps, int64_t ld, int32_t nparts, int64_t M,
+                               const float* target_logit, const int32_t* targets, int64_t V, float* lse, float* loss,
+                               float* mean, void* stream);
 
 /* Column reduce: out[j] = sum_b parts[b*ld + j] over b in [0, nblocks) (fixed order). */
 CODA_API int coda_col_reduce(const float* parts, int64_t nblocks, int64_t N, int64_t ld, float* out, void* stream);
@@ -303,8 +330,55 @@ typedef struct coda_mlp_fp8_io {
 } coda_mlp_fp8_io;
 CODA_API int coda_mlp_fp8(const coda_mlp_fp8_io* io, void* stream);
 
-/* Bytes of fp32 scratch a chain needs (caller allocates). */
-enum coda_workspace_kind { CODA_WS_BLOCK_FWD = 0, CODA_WS_BLOCK_BWD = 1 };
+/* ------------------------------------------------------------ LM head + cross-entropy
+ * Final RMSNorm, LM head and mean cross-entropy, with the logits never stored
+ * [KuCoin, "El epílogo esconde un tesoro" (cross-entropy rewritten as an epilogue),
+ * "Cinco bloques…" (block log-sum-exp, max / sum-exp state), "hoja de referencia"]:
+ *   u = h * g, r = rms(h)                        (coda_rms_gain)
+ *   z = r (u W_v^T): per tile online (max, sum-exp) and the target logit   (XENT GEMM)
+ *   lse, loss_i = lse_i - z[i, target_i], mean  (coda_xent_combine) */
+typedef struct coda_lm_head_xent_io {
+  int64_t M, H, V;
+  float eps;
+  const void* h;            /* [M, H] bf16 final hidden state */
+  const float* g;           /* [H] final RMSNorm gain, 16-byte aligned */
+  const void* W_v;          /* [V, H] bf16 LM-head weight */
+  const int32_t* targets;   /* [M] target classes in [0, V) */
+  void* u;                  /* out [M, H] bf16 = h * g */
+  float* r;                 /* out [M] */
+  float* lse;               /* out [M] */
+  float* loss;              /* out [M] per-row loss */
+  float* loss_mean;         /* out [1] */
+  float* workspace;         /* coda_workspace_size(CODA_WS_XENT_FWD, M, H, V) bytes */
+} coda_lm_head_xent_io;
+CODA_API int coda_lm_head_xent_forward(const coda_lm_head_xent_io* io, void* stream);
+
+/* Backward for an upstream gradient dloss of the mean loss (fused forms):
+ *   e = r dloss (exp(z - lse) - onehot(target)) / M   (logits recomputed in the epilogue)
+ *   s_i = sum_v e_iv z_iv, c = r s / H;  t = e W_v;  dh = g t - c h;  dg = sum_rows h t
+ *   dW_v = e^T u */
+typedef struct coda_lm_head_xent_bwd_io {
+  int64_t M, H, V;
+  float dloss;
+  const void* h;            /* [M, H] bf16 */
+  const float* g;           /* [H] */
+  const void* W_v;          /* [V, H] bf16 */
+  const int32_t* targets;   /* [M] */
+  const void* u;            /* saved by the forward: [M, H] bf16 */
+  const float* r;           /* saved: [M] */
+  const float* lse;         /* saved: [M] */
+  void* e;                  /* out [M, V] bf16 */
+  void* dh;                 /* out [M, H] bf16 */
+  float* dW_v;              /* out [V, H] fp32 */
+  float* dg;                /* out [H] */
+  float* c;                 /* out [M] */
+  float* workspace;         /* coda_workspace_size(CODA_WS_XENT_BWD, M, H, V) bytes */
+} coda_lm_head_xent_bwd_io;
+CODA_API int coda_lm_head_xent_backward(const coda_lm_head_xent_bwd_io* io, void* stream);
+
+/* Bytes of fp32 scratch a chain needs (caller allocates).  The third size is F for the
+ * block chains and V for the cross-entropy chains. */
+enum coda_workspace_kind { CODA_WS_BLOCK_FWD = 0, CODA_WS_BLOCK_BWD = 1, CODA_WS_XENT_FWD = 2, CODA_WS_XENT_BWD = 3 };
 CODA_API size_t coda_workspace_size(int32_t which, int64_t M, int64_t H, int64_t F);
 
 /* ------------------------------------------------------------------ device status
