@@ -554,6 +554,26 @@ def other_workloads(torch, C, S, args, stream):
                          "peak_note": "fp8 peak taken as 2x the measured bf16 sustained peak (nominal ratio)"}
     del h8, X8, W8, Wd8, aq, Y8, P8
     torch.cuda.empty_cache()
+    # N3: the block forward at the 7B and 70B LLaMA-3 hidden sizes, beside torch eager
+    for name, Hs, Fs in (("block_forward_7B_H4096_F14336", 4096, 14336), ("block_forward_70B_H8192_F28672", 8192,
+                                                                           28672)):
+        bi = S.block_inputs(M, Hs, Fs, seed=0, device="cuda")
+        hs, us, Ys = (torch.empty((M, Hs), dtype=BF, device="cuda") for _ in range(3))
+        rs_ = torch.empty((M,), device="cuda")
+        as_ = torch.empty((M, Fs), dtype=BF, device="cuda")
+        wss = torch.empty((C.coda_workspace_size(C.WS_BLOCK_FWD, M, Hs, Fs) // 4,), device="cuda")
+        run = lambda: C.coda_block_forward(bi["O"], bi["R"], bi["W_o"], bi["W_gu"], bi["W_d"], EPS, hs, rs_, as_, Ys,
+                                           wss, g=bi["g"], u=us, stream=stream)
+        ms = _time(torch, run, stream, max(3, min(args.steps, 20)))
+        flop = 2 * M * Hs * Hs + 2 * M * 2 * Fs * Hs + 2 * M * Hs * Fs
+        byt = 2 * (M * Hs * 4 + Hs * Hs) + 2 * (M * Hs + 2 * Fs * Hs + M * Fs) + 2 * (M * Fs + Hs * Fs + 2 * M * Hs)
+        roof = max(flop / (pk["bf16_sus"] * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
+        t_ms = _time(torch, lambda: unfused_chain(torch, bi, Fs), stream, max(3, min(args.steps, 10)))
+        out[name] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "roofline_ms": roof, "roofline_frac": roof / ms,
+                     "tokens_per_s": M / (ms * 1e-3), "launches": 4, "unfused_torch_eager_ms": t_ms,
+                     "speedup_vs_unfused": t_ms / ms}
+        del bi, hs, us, Ys, as_, wss
+        torch.cuda.empty_cache()
     # N1: final RMSNorm + LM head + cross-entropy (vocabulary 128256), forward and backward
     V = 128256
     li = S.lm_head_inputs(M, H, V, seed=0)
@@ -585,6 +605,18 @@ def other_workloads(torch, C, S, args, stream):
     return out
 
 
+def unfused_chain(torch, d, F):
+    """The same block forward as separate torch eager ops (cuBLAS GEMMs, then residual add,
+    RMSNorm, SwiGLU, residual add as their own kernels): the comparator the pages measure
+    against."""
+    F_ = torch.nn.functional
+    hh = F_.linear(d["O"], d["W_o"]) + d["R"]
+    var = hh.float().pow(2).mean(-1, keepdim=True)
+    y = (hh.float() * torch.rsqrt(var + EPS)).to(torch.bfloat16) * d["g"].to(torch.bfloat16)
+    z = F_.linear(y, d["W_gu"])
+    return F_.linear(F_.silu(z[:, :F]) * z[:, F:], d["W_d"]) + hh
+
+
 def unfused_compare(torch, d, Y, r, inp, stream, args):
     """torch eager bf16 chain of the same block (separate GEMM / add / RMSNorm / SwiGLU
     kernels, cuBLAS GEMMs): its time, and the max relative error of both chains against the
@@ -592,18 +624,9 @@ def unfused_compare(torch, d, Y, r, inp, stream, args):
     import numpy as np
 
     import oracle as O
-    F_ = torch.nn.functional
-    O_, R, W_o, W_gu, W_d, g = (d[k] for k in ("O", "R", "W_o", "W_gu", "W_d", "g"))
-    gb = g.to(torch.bfloat16)
 
     def chain():
-        hh = F_.linear(O_, W_o) + R
-        var = hh.float().pow(2).mean(-1, keepdim=True)
-        y = (hh.float() * torch.rsqrt(var + EPS)).to(torch.bfloat16) * gb
-        z = F_.linear(y, W_gu)
-        G, U = z[:, :FFN], z[:, FFN:]
-        aa = F_.silu(G) * U
-        return F_.linear(aa, W_d) + hh
+        return unfused_chain(torch, d, FFN)
 
     for _ in range(3):
         Yt = chain()

@@ -27,7 +27,7 @@ E4M3_MAX = 448.0
 
 
 def _normal(gen, shape, std=1.0, mean=0.0):
-    t = torch.empty(shape, dtype=torch.float32)
+    t = torch.empty(shape, dtype=torch.float32, device=gen.device)
     t.normal_(mean=0.0, std=1.0, generator=gen)
     if std != 1.0:
         t.mul_(std)
@@ -46,8 +46,10 @@ def tiny_chain_inputs(M=128, d=256, n2=512, seed=0):
     return dict(X=X, R=R, W1=W1, W2=W2, g=g, eps=1e-6)
 
 
-def block_inputs(M, H, F, seed=0, w_std=0.02, with_grad=False, dtype=torch.bfloat16):
-    gen = torch.Generator().manual_seed(seed)
+def block_inputs(M, H, F, seed=0, w_std=0.02, with_grad=False, dtype=torch.bfloat16, device="cpu"):
+    """device="cuda" draws on the GPU's generator (same recipe, different stream of numbers):
+    used where only timing needs the tensors."""
+    gen = torch.Generator(device=device).manual_seed(seed)
     out = dict(
         O=_normal(gen, (M, H)).to(dtype),
         R=_normal(gen, (M, H)).to(dtype),

@@ -302,6 +302,39 @@ def qkv_rope(h, g, W_qkv, eps, seq_len, n_rot_cols, head_dim, base):
     return dict(r=rms_scale(h, eps), Z=Z, out=rope_rotate(Z, pos, n_rot_cols, head_dim, base))
 
 
+def qkv_rope_backward(h, g, W_qkv, dout, eps, seq_len, n_rot_cols, head_dim, base):
+    """Plain chain rule through qkv_rope (RMSNorm -> QKV GEMM -> RoPE) for an upstream
+    gradient dout of its output: dZ = RoPE^T dout (rotation by -phi); dW = dZ^T y;
+    dy = dZ W; RMSNorm backward in its textbook form -> dh, dg."""
+    h, g, W = _f64(h), _f64(g), _f64(W_qkv)
+    M, d = h.shape
+    r = rms_scale(h, eps)
+    y = r[:, None] * h * g[None, :]
+    pos = np.arange(M) % seq_len
+    dZ = rope_rotate(dout, -pos, n_rot_cols, head_dim, base)
+    dy = dZ @ W
+    dg = np.sum(dy * r[:, None] * h, axis=0)
+    proj = np.sum(g[None, :] * dy * h, axis=1)
+    dh = r[:, None] * (g[None, :] * dy) - (r ** 3 / d)[:, None] * h * proj[:, None]
+    return dict(dZ=dZ, dW=dZ.T @ y, dh=dh, dg=dg)
+
+
+def qkv_rope_backward_fused(h, g, W_qkv, dout, out, eps, seq_len, n_rot_cols, head_dim, base):
+    """The fused forms: e = r RoPE^T(dout) (row-wise pass); s_i = sum_n e_in Z_in, which equals
+    r_i sum_n dout_in out_in because the rotation keeps inner products; c = r s / d;
+    t = e W;  dh = g t - c h;  dg = sum_rows h t;  dW[n, k] = g_k (e^T h)[n, k]."""
+    h, g, W = _f64(h), _f64(g), _f64(W_qkv)
+    M, d = h.shape
+    r = rms_scale(h, eps)
+    pos = np.arange(M) % seq_len
+    e = r[:, None] * rope_rotate(dout, -pos, n_rot_cols, head_dim, base)
+    s = r * np.sum(_f64(dout) * _f64(out), axis=1)
+    c = r * s / d
+    t = e @ W
+    return dict(e=e, c=c, dh=g[None, :] * t - c[:, None] * h, dg=np.sum(h * t, axis=0),
+                dW=g[None, :] * (e.T @ h))
+
+
 def mlp_fp8(h, Xq_val, s_x, Wq_val, s_w, Wdq_val, s_wd, s_a, eps, bn):
     """FP8 MLP with per-tensor scales.  Operands are e4m3 code values (already decoded to
     float64) with fp32 scales: x = s_x Xq, W = s_w Wq (the effective gate/up weight),

@@ -96,6 +96,16 @@ def _sim_forward_rows(inp, rows, gain="broadcast"):
 @pytest.mark.parametrize("gain", ["broadcast", "fold"])
 @pytest.mark.parametrize("M,H,F", [(640, 512, 1024), (300, 256, 384)])
 def test_block_forward_small(C, M, H, F, gain):
+    _check_block_forward(C, M, H, F, gain)
+
+
+# hidden sizes of the 7B and 70B LLaMA-3 shapes (the pages' 1B / 7B / 70B sweep), fewer tokens
+@pytest.mark.parametrize("M,H,F", [(256, 4096, 14336), (128, 8192, 28672)])
+def test_block_forward_7b_70b_hidden_sizes(C, M, H, F):
+    _check_block_forward(C, M, H, F, "broadcast")
+
+
+def _check_block_forward(C, M, H, F, gain):
     inp = S.block_inputs(M, H, F, seed=0)
     out, _ = _run_block_forward(C, inp, gain=gain)
     ref = _oracle_forward_rows(inp, np.arange(M))

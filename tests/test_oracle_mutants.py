@@ -125,3 +125,17 @@ def test_xent_missing_mean_scale_is_caught(monkeypatch):
 def test_xent_combine_without_rescale_is_caught(monkeypatch):
     _plant(monkeypatch, "xent_combine", lambda m, s: np.max(m, axis=0) + np.log(np.sum(s, axis=0)))
     assert _fails(pins.test_xent_partials_combine_to_logsumexp)
+
+
+def test_rope_backward_with_forward_rotation_is_caught(monkeypatch):
+    orig = O.qkv_rope_backward
+
+    def bad(h, g, W_qkv, dout, eps, seq_len, n_rot_cols, head_dim, base):
+        # rotate the gradient by +phi instead of -phi: the transpose of the rotation is missed
+        M = np.asarray(h).shape[0]
+        pos = np.arange(M) % seq_len
+        d2 = O.rope_rotate(O.rope_rotate(dout, pos, n_rot_cols, head_dim, base), pos, n_rot_cols, head_dim, base)
+        return orig(h, g, W_qkv, d2, eps, seq_len, n_rot_cols, head_dim, base)
+
+    _plant(monkeypatch, "qkv_rope_backward", bad)
+    assert _fails(pins.test_qkv_rope_backward_matches_finite_differences)

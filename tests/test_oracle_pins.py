@@ -397,3 +397,47 @@ def test_lm_head_fused_backward_equals_chain_rule_and_rows_sum_to_zero():
     for k in ("dh", "dg", "dW_v"):
         assert np.max(np.abs(fused[k] - plain[k])) <= 1e-12 * np.max(np.abs(plain[k])), k
     np.testing.assert_allclose(np.sum(plain["dlogits"], axis=1), 0.0, atol=1e-15)   # softmax - onehot
+
+
+# ------------------------------------------------------------------- QKV / RoPE backward
+def test_rope_inverse_rotation():
+    Z, hd, nh = _rope_setup()
+    pos = np.arange(Z.shape[0]) * 11 + 2
+    back = O.rope_rotate(O.rope_rotate(Z, pos, hd * nh, hd, 500000.0), -pos, hd * nh, hd, 500000.0)
+    np.testing.assert_allclose(back, Z, rtol=1e-13, atol=1e-14)
+
+
+def _qkv_case(M=6, d=8, N=24, seed=12):
+    rng = np.random.default_rng(seed)
+    return (rng.normal(size=(M, d)), 1 + 0.1 * rng.normal(size=d), rng.normal(size=(N, d)) / 2,
+            rng.normal(size=(M, N)))
+
+
+def test_qkv_rope_backward_matches_finite_differences():
+    h, g, W, dout = _qkv_case()
+    kw = dict(seq_len=4, n_rot_cols=16, head_dim=8, base=10000.0)
+    b = O.qkv_rope_backward(h, g, W, dout, 1e-6, **kw)
+
+    def loss(hh, gg, WW):
+        return float(np.sum(O.qkv_rope(hh, gg, WW, 1e-6, **kw)["out"] * dout))
+
+    for name, arr, an in (("h", h, b["dh"]), ("g", g, b["dg"]), ("W", W, b["dW"])):
+        num = np.zeros_like(arr)
+        for ix in np.ndindex(arr.shape):
+            p, m = arr.copy(), arr.copy()
+            p[ix] += 1e-6
+            m[ix] -= 1e-6
+            ap = {"h": (p, g, W), "g": (h, p, W), "W": (h, g, p)}[name]
+            am = {"h": (m, g, W), "g": (h, m, W), "W": (h, g, m)}[name]
+            num[ix] = (loss(*ap) - loss(*am)) / 2e-6
+        assert np.max(np.abs(num - an)) / np.max(np.abs(num)) <= 1e-6, name
+
+
+def test_qkv_rope_fused_backward_equals_chain_rule():
+    h, g, W, dout = _qkv_case(M=10, d=16, N=48, seed=13)
+    kw = dict(seq_len=4, n_rot_cols=32, head_dim=16, base=500000.0)
+    out = O.qkv_rope(h, g, W, 1e-6, **kw)["out"]
+    plain = O.qkv_rope_backward(h, g, W, dout, 1e-6, **kw)
+    fused = O.qkv_rope_backward_fused(h, g, W, dout, out, 1e-6, **kw)
+    for k, pk in (("dh", "dh"), ("dg", "dg"), ("dW", "dW")):
+        assert np.max(np.abs(fused[k] - plain[pk])) <= 1e-11 * np.max(np.abs(plain[pk])), k
