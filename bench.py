@@ -527,7 +527,24 @@ def other_workloads(torch, C, S, args, stream):
                           "roofline_frac": roof / ms, "tokens_per_s": M / (ms * 1e-3), "launches": 3,
                           "note": "gain fold onto W_qkv + row RMS of h (one pass) + QKV GEMM with r and RoPE "
                                   "epilogue"}
-    del hq, Wq_, gq, Wqf, oq
+    # N2: its backward (RoPE transposed + attention-input RMSNorm backward + dW)
+    dq = torch.randn((M, N), generator=torch.Generator(device="cuda").manual_seed(7), device="cuda").to(BF)
+    eq = torch.empty((M, N), dtype=BF, device="cuda")
+    dhq = torch.empty((M, H), dtype=BF, device="cuda")
+    dWq = torch.empty((N, H), device="cuda")
+    dgq, cq = torch.empty((H,), device="cuda"), torch.empty((M,), device="cuda")
+    wsq = torch.empty((((M + 31) // 32) * H,), device="cuda")
+    qb = lambda: C.coda_qkv_rope_backward(hq, gq, Wq_, rq, oq, dq, seq, hd, 2560, cos, sin, eq, dhq, dWq, dgq, cq,
+                                          wsq, stream=stream)
+    ms = _time(torch, qb, stream, steps)
+    flop = 2 * (2 * M * N * H)
+    byt = 2 * (M * N * 3 + M * N * 2 + N * H * 2 + M * H * 3) + 4 * N * H
+    roof = max(flop / (pk["bf16_sus"] * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
+    out["qkv_rope_backward_N2"] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "roofline_ms": roof,
+                                   "roofline_frac": roof / ms, "tokens_per_s": M / (ms * 1e-3), "launches": 4,
+                                   "note": "RoPE backward + row scale pass, dh GEMM + RMSNorm-bwd epilogue, dg "
+                                           "column reduce, dW GEMM"}
+    del hq, Wq_, gq, Wqf, oq, dq, eq, dhq, dWq, wsq
     torch.cuda.empty_cache()
     # C4: fp8 MLP
     H8, F8 = 4096, 14336

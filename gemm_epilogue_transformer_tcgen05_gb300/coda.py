@@ -37,7 +37,8 @@ EXPORTED = [
     "coda_rope_table", "coda_block_forward", "coda_block_backward", "coda_qkv_rope", "coda_mlp_fp8",
     "coda_workspace_size", "coda_get_device_status", "coda_set_watchdog_ms", "coda_inject_dropped_stage",
     "coda_device_sm_count", "coda_status_string", "coda_version", "coda_block_forward_noalloc", "coda_rms_gain",
-    "coda_xent_combine", "coda_lm_head_xent_forward", "coda_lm_head_xent_backward",
+    "coda_xent_combine", "coda_lm_head_xent_forward", "coda_lm_head_xent_backward", "coda_rope_backward",
+    "coda_qkv_rope_backward",
 ]
 NOALLOC_MAX_PARTIALS = 1 << 20
 
@@ -117,6 +118,14 @@ class CodaXentBwd(Structure):
                 ("c", c_void_p), ("workspace", c_void_p)]
 
 
+class CodaQkvRopeBwd(Structure):
+    _fields_ = [("M", c_int64), ("H", c_int64), ("N", c_int64), ("seq_len", c_int32), ("head_dim", c_int32),
+                ("rope_ncols", c_int32), ("h", c_void_p), ("g", c_void_p), ("W_qkv", c_void_p), ("r", c_void_p),
+                ("out", c_void_p), ("dout", c_void_p), ("dres", c_void_p), ("rope_cos", c_void_p),
+                ("rope_sin", c_void_p), ("e", c_void_p), ("dh", c_void_p), ("dW_qkv", c_void_p), ("dg", c_void_p),
+                ("c", c_void_p), ("workspace", c_void_p)]
+
+
 # --------------------------------------------------------------------- the library
 _lib = None
 
@@ -154,6 +163,9 @@ def lib():
                               c_void_p, c_void_p, c_void_p],
         "coda_lm_head_xent_forward": [P(CodaXentFwd), c_void_p],
         "coda_lm_head_xent_backward": [P(CodaXentBwd), c_void_p],
+        "coda_rope_backward": [P(CodaTensor), P(CodaTensor), c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32,
+                               c_int64, P(CodaTensor), c_void_p, c_void_p],
+        "coda_qkv_rope_backward": [P(CodaQkvRopeBwd), c_void_p],
     }
     for name, args in sigs.items():
         fn = getattr(L, name)
@@ -313,6 +325,24 @@ def coda_lm_head_xent_backward(h, g, W_v, targets, u, r, lse, dloss, e, dh, dW_v
     io = CodaXentBwd(M, H, V, dloss, _ptr(h), _ptr(g), _ptr(W_v), _ptr(targets), _ptr(u), _ptr(r), _ptr(lse),
                      _ptr(e), _ptr(dh), _ptr(dW_v), _ptr(dg), _ptr(c), _ptr(workspace))
     _check(lib().coda_lm_head_xent_backward(ctypes.byref(io), _stream(stream)), "coda_lm_head_xent_backward")
+
+
+def coda_rope_backward(dout, out, r, rope_cos, rope_sin, seq_len, head_dim, rope_ncols, H, e_out, c_out,
+                       stream=None):
+    d, o, e = desc(dout), desc(out), desc(e_out)
+    st = lib().coda_rope_backward(ctypes.byref(d), ctypes.byref(o), _ptr(r), _ptr(rope_cos), _ptr(rope_sin), seq_len,
+                                  head_dim, rope_ncols, H, ctypes.byref(e), _ptr(c_out), _stream(stream))
+    _check(st, "coda_rope_backward")
+
+
+def coda_qkv_rope_backward(h, g, W_qkv, r, out, dout, seq_len, head_dim, rope_ncols, rope_cos, rope_sin, e, dh,
+                           dW_qkv, dg, c, workspace, dres=None, stream=None):
+    M, H = h.shape
+    N = W_qkv.shape[0]
+    io = CodaQkvRopeBwd(M, H, N, seq_len, head_dim, rope_ncols, _ptr(h), _ptr(g), _ptr(W_qkv), _ptr(r), _ptr(out),
+                        _ptr(dout), _ptr(dres), _ptr(rope_cos), _ptr(rope_sin), _ptr(e), _ptr(dh), _ptr(dW_qkv),
+                        _ptr(dg), _ptr(c), _ptr(workspace))
+    _check(lib().coda_qkv_rope_backward(ctypes.byref(io), _stream(stream)), "coda_qkv_rope_backward")
 
 
 def coda_workspace_size(which, M, H, F):

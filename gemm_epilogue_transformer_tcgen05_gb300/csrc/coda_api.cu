@@ -826,6 +826,70 @@ int coda_lm_head_xent_backward(const coda_lm_head_xent_bwd_io* io, void* stream)
   return CODA_OK;
 }
 
+int coda_rope_backward(const coda_tensor* dout, const coda_tensor* out, const float* r, const float* rope_cos,
+                       const float* rope_sin, int32_t seq_len, int32_t head_dim, int32_t rope_ncols, int64_t H,
+                       const coda_tensor* e_out, float* c_out, void* stream) {
+  int st;
+  if ((st = check_tensor(dout, false)) != CODA_OK) return st;
+  if ((st = check_tensor(out, false)) != CODA_OK) return st;
+  if ((st = check_tensor(e_out, false)) != CODA_OK) return st;
+  if (!r || !rope_cos || !rope_sin || !c_out) return CODA_ERR_NULL;
+  if (dout->dtype != CODA_BF16 || out->dtype != CODA_BF16 || e_out->dtype != CODA_BF16) return CODA_ERR_DTYPE;
+  const int64_t M = dout->rows, N = dout->cols;
+  if (out->rows != M || out->cols != N || e_out->rows != M || e_out->cols != N || out->ld != dout->ld) return CODA_ERR_SHAPE;
+  if (N % 8 != 0 || head_dim < 8 || head_dim % 8 != 0 || rope_ncols < 0 || rope_ncols % head_dim != 0 ||
+      rope_ncols > N || seq_len < 1 || H < 1)
+    return CODA_ERR_SHAPE;
+  if (M == 0) return CODA_OK;
+  DevState* dv;
+  if ((st = ensure_device(&dv)) != CODA_OK) return st;
+  cudaError_t e = launch_rope_bwd(dout->ptr, out->ptr, M, N, dout->ld, r, rope_cos, rope_sin, seq_len, head_dim,
+                                  rope_ncols, H, e_out->ptr, e_out->ld, c_out, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
+}
+
+int coda_qkv_rope_backward(const coda_qkv_rope_bwd_io* io, void* stream) {
+  if (!io) return CODA_ERR_NULL;
+  if (!io->h || !io->g || !io->W_qkv || !io->r || !io->out || !io->dout || !io->rope_cos || !io->rope_sin ||
+      !io->e || !io->dh || !io->dW_qkv || !io->dg || !io->c || !io->workspace)
+    return CODA_ERR_NULL;
+  const int64_t M = io->M, H = io->H, N = io->N;
+  if (M < 0 || H < 32 || H % 32 != 0 || N < 32 || N % 32 != 0) return CODA_ERR_SHAPE;
+  if (M == 0) return CODA_OK;
+  int st;
+  coda_tensor dout = mk(io->dout, CODA_BF16, M, N, N), out = mk(io->out, CODA_BF16, M, N, N);
+  coda_tensor e = mk(io->e, CODA_BF16, M, N, N);
+  if ((st = coda_rope_backward(&dout, &out, io->r, io->rope_cos, io->rope_sin, io->seq_len, io->head_dim,
+                               io->rope_ncols, H, &e, io->c, stream)) != CODA_OK)
+    return st;
+  float* Dg = io->workspace;
+  {
+    coda_tensor W = mk(io->W_qkv, CODA_BF16, H, N, H, CODA_COL_MAJOR);   // logical W_qkv^T
+    coda_tensor h = mk(io->h, CODA_BF16, M, H, H), dres = mk(io->dres, CODA_BF16, M, H, H);
+    coda_tensor dh = mk(io->dh, CODA_BF16, M, H, H);
+    coda_epilogue_program pg = prog_of({CODA_OP_RMSBWD_COMBINE, CODA_OP_COL_DOT_PARTIAL});
+    coda_side_inputs sd{};
+    sd.aux_in = &h;
+    sd.aux_in2 = io->dres ? &dres : nullptr;
+    sd.col_scale = io->g;
+    sd.row_coef = io->c;
+    coda_aux_outputs ax{};
+    ax.col_partials = Dg;
+    ax.col_partials_ld = H;
+    if ((st = coda_gemm_epilogue(&e, &W, &pg, &sd, &dh, &ax, stream)) != CODA_OK) return st;
+  }
+  if ((st = coda_col_reduce(Dg, (M + 31) / 32, H, H, io->dg, stream)) != CODA_OK) return st;
+  {
+    coda_tensor A = mk(io->e, CODA_BF16, N, M, N, CODA_COL_MAJOR), W = mk(io->h, CODA_BF16, H, M, H, CODA_COL_MAJOR);
+    coda_tensor dW = mk(io->dW_qkv, CODA_F32, N, H, H);
+    coda_epilogue_program pg = prog_of({CODA_OP_COL_SCALE});
+    coda_side_inputs sd{};
+    sd.col_scale = io->g;
+    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &dW, nullptr, stream)) != CODA_OK) return st;
+  }
+  return CODA_OK;
+}
+
 int coda_qkv_rope(const coda_qkv_rope_io* io, void* stream) {
   if (!io) return CODA_ERR_NULL;
   if (!io->h || !io->W_qkv || !io->rope_cos || !io->rope_sin || !io->r || !io->out) return CODA_ERR_NULL;

@@ -43,6 +43,9 @@ cudaError_t launch_rope_table(int seq_len, int head_dim, double base, float* cos
                               cudaStream_t s);
 cudaError_t launch_rms_gain(const void* X, int64_t M, int64_t d, int64_t ld, const float* g, float eps, float* r,
                             void* U, int64_t ldu, cudaStream_t s);
+cudaError_t launch_rope_bwd(const void* dout, const void* out, int64_t M, int64_t N, int64_t ld, const float* r,
+                            const float* cs, const float* sn, int seq_len, int head_dim, int rope_ncols, int64_t H,
+                            void* e, int64_t lde, float* c, cudaStream_t s);
 cudaError_t launch_xent_reduce(const float* Pm, const float* Ps, int64_t ld, int nparts, int64_t M, const float* T,
                                const int* targets, int64_t V, float* lse, float* loss, float* mean, cudaStream_t s);
 

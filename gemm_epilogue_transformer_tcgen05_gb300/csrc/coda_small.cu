@@ -131,6 +131,62 @@ cudaError_t launch_rms_gain(const void* X, int64_t M, int64_t d, int64_t ld, con
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- RoPE backward
+// One warp per row: e = r * R(-phi) dout (the transpose of the forward rotation on the
+// first rope_ncols columns, plain copy after), and c = r * s / H with
+// s = r * sum_n dout_n out_n (= sum_n e_n Z_n, the rotation keeps inner products).
+__global__ void rope_bwd_kernel(const __nv_bfloat16* __restrict__ dout, const __nv_bfloat16* __restrict__ out,
+                                int64_t M, int64_t N, int64_t ld, const float* __restrict__ r,
+                                const float* __restrict__ cs, const float* __restrict__ sn, int seq_len, int head_dim,
+                                int rope_ncols, float inv_h, __nv_bfloat16* __restrict__ e, int64_t lde,
+                                float* __restrict__ c) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= M) return;
+  const float rr = __ldg(r + row);
+  const int pos = (int)(row % seq_len);
+  const int half = head_dim >> 1;
+  const uint4* dsrc = reinterpret_cast<const uint4*>(dout + row * ld);
+  const uint4* osrc = reinterpret_cast<const uint4*>(out + row * ld);
+  uint4* edst = reinterpret_cast<uint4*>(e + row * lde);
+  float acc = 0.f;
+  for (int64_t v = lane; v < (N >> 3); v += 32) {
+    const uint4 du = __ldcs(dsrc + v), ou = __ldcs(osrc + v);
+    const uint32_t dw[4] = {du.x, du.y, du.z, du.w}, ow[4] = {ou.x, ou.y, ou.z, ou.w};
+    const int col = (int)(v << 3);
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float x0 = __uint_as_float(dw[k] << 16), x1 = __uint_as_float(dw[k] & 0xFFFF0000u);
+      acc = fmaf(x0, __uint_as_float(ow[k] << 16), fmaf(x1, __uint_as_float(ow[k] & 0xFFFF0000u), acc));
+      if (col < rope_ncols) {
+        const int p = ((col % head_dim) >> 1) + k;
+        const float cv = __ldg(cs + (int64_t)pos * half + p), sv = __ldg(sn + (int64_t)pos * half + p);
+        const float y0 = x0 * cv + x1 * sv, y1 = x1 * cv - x0 * sv;
+        x0 = y0;
+        x1 = y1;
+      }
+      __nv_bfloat162 b = __floats2bfloat162_rn(rr * x0, rr * x1);
+      o[k] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    edst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) c[row] = rr * rr * acc * inv_h;
+}
+
+cudaError_t launch_rope_bwd(const void* dout, const void* out, int64_t M, int64_t N, int64_t ld, const float* r,
+                            const float* cs, const float* sn, int seq_len, int head_dim, int rope_ncols, int64_t H,
+                            void* e, int64_t lde, float* c, cudaStream_t s) {
+  const int rows_per_block = 8;
+  const int64_t blocks = (M + rows_per_block - 1) / rows_per_block;
+  rope_bwd_kernel<<<(unsigned)blocks, 32 * rows_per_block, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(out), M, N, ld, r, cs, sn, seq_len,
+      head_dim, rope_ncols, 1.0f / (float)H, static_cast<__nv_bfloat16*>(e), lde, c);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- cross-entropy combine
 // The light reduce of the per-tile online-softmax states: per row, lse = m + log(sum_t s_t
 // exp(m_t - m)) with m = max_t m_t, in tile order; loss = lse - logit[target] (NaN for a

@@ -312,6 +312,38 @@ typedef struct coda_qkv_rope_io {
 } coda_qkv_rope_io;
 CODA_API int coda_qkv_rope(const coda_qkv_rope_io* io, void* stream);
 
+/* Backward of coda_qkv_rope for an upstream gradient dout of its output (the attention
+ * backward's dQ, dK, dV), in fused form:
+ *   e = r R(-phi) dout   (rotation transposed on the first rope_ncols columns; coda_rope_backward)
+ *   c = r s / H with s = r sum_n dout_n out_n (= sum_n e_n Z_n: rotations keep inner products)
+ *   t = e W_qkv;  dh = g t - c h [+ dres];  dg = sum_rows h t;  dW_qkv[n, k] = g_k (e^T h)[n, k]
+ * W_qkv is the unfolded weight and g the attention-input RMSNorm gain. */
+typedef struct coda_qkv_rope_bwd_io {
+  int64_t M, H, N;
+  int32_t seq_len, head_dim, rope_ncols;
+  const void* h;             /* [M, H] bf16 */
+  const float* g;            /* [H] */
+  const void* W_qkv;         /* [N, H] bf16, unfolded */
+  const float* r;            /* [M] from the forward */
+  const void* out;           /* [M, N] bf16 forward output */
+  const void* dout;          /* [M, N] bf16 */
+  const void* dres;          /* optional [M, H] bf16 gradient arriving on the residual stream */
+  const float* rope_cos; const float* rope_sin;
+  void* e;                   /* out [M, N] bf16 */
+  void* dh;                  /* out [M, H] bf16 */
+  float* dW_qkv;             /* out [N, H] fp32 */
+  float* dg;                 /* out [H] */
+  float* c;                  /* out [M] */
+  float* workspace;          /* ceil(M / 32) * H floats */
+} coda_qkv_rope_bwd_io;
+CODA_API int coda_qkv_rope_backward(const coda_qkv_rope_bwd_io* io, void* stream);
+
+/* The row-wise RoPE-backward pass on its own: e = r R(-phi) dout (bf16 [M, N]) and
+ * c[i] = r_i^2 sum_n dout_in out_in / H. */
+CODA_API int coda_rope_backward(const coda_tensor* dout, const coda_tensor* out, const float* r, const float* rope_cos,
+                                const float* rope_sin, int32_t seq_len, int32_t head_dim, int32_t rope_ncols,
+                                int64_t H, const coda_tensor* e_out, float* c_out, void* stream);
+
 /* FP8 (e4m3, per-tensor fp32 scales) MLP with deferred r:
  *   Z = r s_x s_w (X_q W_q^T);  a = silu(Z_gate) Z_up;  a_q = e4m3(a / s_a);  amax = max|a|
  *   Y = s_a s_wd (a_q W_dq^T) + h;  Y_partials = partial sums of squares of Y. */
