@@ -428,6 +428,37 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
     gn = gn < 1 ? 1 : (gn > n_tiles ? n_tiles : gn);
     p.group_n = (int)gn;
   }
+  // Split-K for the linear fp32-output program when the tiles alone leave the last wave of
+  // CTA groups mostly idle: the slices reduce-add into a zeroed output (fp32 adds in any
+  // order: not bitwise reproducible from run to run).
+  {
+    const int64_t tiles = m_tiles * n_tiles;
+    const int64_t groups = d->sms / var->cg;
+    const int64_t num_kb = (K + (128 / op_bytes) - 1) / (128 / op_bytes);
+    int best = 1;
+    double best_score = 0.0;
+    if (epi == EPI_STORE && out->dtype == CODA_F32) {
+      for (int sk = 1; sk <= 8; ++sk) {
+        if (sk > 1 && num_kb / sk < 32) break;
+        const int64_t work = tiles * sk;
+        const double eff = (double)work / (double)(((work + groups - 1) / groups) * groups);
+        const double score = eff - 0.01 * (sk - 1);
+        if (score > best_score + 1e-9) {
+          best_score = score;
+          best = sk;
+        }
+      }
+    }
+    p.k_splits = best;
+    p.kb_per_split = (int)((num_kb + best - 1) / best);
+    if (best > 1) {
+      const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+      const size_t row_bytes = (size_t)N * 4;
+      const cudaError_t me = out->ld == N ? cudaMemsetAsync(out->ptr, 0, row_bytes * (size_t)M, cs)
+                                          : cudaMemset2DAsync(out->ptr, (size_t)out->ld * 4, 0, row_bytes, (size_t)M, cs);
+      if (me != cudaSuccess) return CODA_ERR_LAUNCH;
+    }
+  }
   p.flags = (has(CODA_OP_ROW_SUMSQ_PARTIAL) ? F_PARTIAL : 0) | (has(CODA_OP_AMAX) ? F_AMAX : 0) |
             (has(CODA_OP_COL_SCALE) ? F_COLSCALE : 0) | (has(CODA_OP_ROW_SCALE) ? F_ROWSCALE : 0) |
             (epi == EPI_RMSBWD && !sd.aux_in2 ? F_NO_SIDE1 : 0);

@@ -87,6 +87,8 @@ struct GemmParams {
   int M, N, K;          // out [M, N]; EPI_SWIGLU: N = F and B holds 2F rows (gate, then up)
   int m_tiles, n_tiles;
   int group_n;          // tile order: groups of group_n N-tiles, M-major inside a group
+  int k_splits;         // split-K: each tile's K range in k_splits slices, reduce-added into out
+  int kb_per_split;     // k-blocks per slice (the last slice may be shorter)
   int flags;
   int up_offset;        // EPI_SWIGLU: first up row of B / first U column of saved Z;
                         // EPI_SWIGLU_BWD: first U column of Z and of e
@@ -168,6 +170,17 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& 
   const int t = tile - g * per_group;
   mb = t / gsize;
   nb = n_first + (t - mb * gsize);
+}
+
+// Work item w -> (tile coordinates, K slice).  The K slice is the slowest index, so the CTAs
+// working at the same time share one slice of K.
+__device__ __forceinline__ void work_coords(int w, const GemmParams& p, int& mb, int& nb, int& kb0, int& kb1,
+                                            int num_kb) {
+  const int tiles = p.m_tiles * p.n_tiles;
+  const int ks = w / tiles;
+  tile_coords(w - ks * tiles, p, mb, nb);
+  kb0 = ks * p.kb_per_split;
+  kb1 = min(num_kb, kb0 + p.kb_per_split);
 }
 
 struct Watch {
@@ -356,7 +369,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *tmem_holder;
 
   const Watch watch{abort_flag, p.status, p.timeout_ns};
-  const int total_tiles = p.m_tiles * p.n_tiles;
+  const int total_tiles = p.m_tiles * p.n_tiles * p.k_splits;   // work items
   const int num_kb = (p.K + C::BK - 1) / C::BK;
 
   if (warp == 0) {
@@ -370,10 +383,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint64_t keep = ptx::make_policy_evict_last();   // B: reused by every M-tile of a group
       const uint64_t normal = ptx::make_policy_evict_normal();
       for (int tile = cluster_id; ok && tile < total_tiles; tile += n_clusters) {
-        int mb, nb;
-        tile_coords(tile, p, mb, nb);
+        int mb, nb, kb0, kb1;
+        work_coords(tile, p, mb, nb, kb0, kb1, num_kb);
         const int m0 = mb * C::PAIR_ROWS + (int)rank * BM;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!bwait(EMPTY_BAR(stage), phase ^ 1u, watch, SITE_PRODUCER_EMPTY)) {
             ok = false;
             break;
@@ -443,7 +456,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * UMMA_N;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        int mb_, nb_, kb0, kb1;
+        work_coords(tile, p, mb_, nb_, kb0, kb1, num_kb);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!bwait(FULL_BAR(stage), phase, watch, SITE_MMA_FULL)) {
             ok = false;
             break;
@@ -455,7 +470,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int k = 0; k < KSTEPS; ++k) {
             const uint64_t ad = C::A_MN ? smem_desc(sa + k * 2048, 8192, 1024) : smem_desc(sa + k * 32, 16, 1024);
             const uint64_t bd = C::B_MN ? smem_desc(sb + k * 2048, 8192, 1024) : smem_desc(sb + k * 32, 16, 1024);
-            ptx::umma<C::KIND, C::CG>(d_tmem, ad, bd, C::IDESC, (kb | k) != 0 ? 1u : 0u);
+            ptx::umma<C::KIND, C::CG>(d_tmem, ad, bd, C::IDESC, (kb != kb0 || k != 0) ? 1u : 0u);
           }
           ptx::umma_commit<C::CG>(EMPTY_BAR(stage));  // frees the stage (in both CTAs) once done
           if (++stage == C::STAGES) {
@@ -483,8 +498,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     int t = 0;
     for (int tile = cluster_id; ok && tile < total_tiles; tile += n_clusters, ++t) {
-      int mb, nb;
-      tile_coords(tile, p, mb, nb);
+      int mb, nb, kb0_, kb1_;
+      work_coords(tile, p, mb, nb, kb0_, kb1_, num_kb);
       const int m0 = mb * C::PAIR_ROWS + (int)rank * BM;
       const int n0 = nb * C::BN_OUT;
       const int r0 = m0 + 32 * q;   // first row of this warp's 32-row slab
@@ -766,7 +781,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         if (lane == 0) {
           if (store) {
-            ptx::tma_store_2d_hint(&tmOut, col0, r0, oslot, stream_pol);
+            if (C::EPI == EPI_STORE && C::OUT_DT == DT_F32 && p.k_splits > 1)
+              ptx::tma_reduce_add_2d_hint(&tmOut, col0, r0, oslot, stream_pol);   // split-K partial
+            else
+              ptx::tma_store_2d_hint(&tmOut, col0, r0, oslot, stream_pol);
             if constexpr (C::EPI == EPI_SWIGLU_BWD)
               ptx::tma_store_2d_hint(&tmOut, p.up_offset + col0, r0, oslot + C::OSLOT, stream_pol);
             if constexpr (C::NX > 0) ptx::tma_store_2d_hint(&tmAux, col0, r0, oslot + C::NO * C::OSLOT, stream_pol);
@@ -880,8 +898,8 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_done[dev] = 1;
   }
-  // persistent grid: one CTA group per resident slot, at most one per tile
-  const int64_t tiles = (int64_t)L.p.m_tiles * L.p.n_tiles;
+  // persistent grid: one CTA group per resident slot, at most one per work item
+  const int64_t tiles = (int64_t)L.p.m_tiles * L.p.n_tiles * L.p.k_splits;
   const int groups = (int)(tiles < resident_groups<C>(L.sms) ? tiles : resident_groups<C>(L.sms));
   if (groups <= 0) return cudaSuccess;
   if constexpr (C::CG == 1) {

@@ -92,6 +92,15 @@ __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* m, int32_t 
                "r"(c0), "r"(c1), "r"(src), "l"(policy)
                : "memory");
 }
+// 2-D tiled reduce-add shared -> global (fp32 add into the destination; bulk-group completion).
+__device__ __forceinline__ void tma_reduce_add_2d_hint(const CUtensorMap* m, int32_t c0, int32_t c1, uint32_t src,
+                                                       uint64_t policy) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::
+          "l"(reinterpret_cast<uint64_t>(m)),
+      "r"(c0), "r"(c1), "r"(src), "l"(policy)
+      : "memory");
+}
 // 2-D tiled store shared -> global (bulk-group completion); out-of-range parts are clipped.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, int32_t c0, int32_t c1, uint32_t src) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(

@@ -313,3 +313,20 @@ def test_rejections_launch_nothing(C):
         C.coda_gemm_epilogue(bad, W[:, :60], [], out)
     assert ei.value.status == C.ERR_ALIGN
     fresh_status()
+
+
+@pytest.mark.parametrize("M,N,K,colscale", [(256, 512, 16384, False), (384, 256, 9000, True)])
+def test_split_k_reduce_add(C, M, N, K, colscale):
+    # few output tiles and a long K: the library splits K and reduce-adds the fp32 partials
+    X = seeded((K, M), 80, dtype=BF)
+    Y = seeded((K, N), 81, std=0.1, dtype=BF)
+    g = seeded((N,), 82, std=0.1, mean=1.0)
+    out = torch.full((M, N), 123.0, device="cuda")       # must be overwritten, not added to
+    ops = [C.OP_COL_SCALE] if colscale else []
+    C.coda_gemm_epilogue(dev(X).t(), dev(Y).t(), ops, out, col_scale=dev(g) if colscale else None)
+    torch.cuda.synchronize()
+    fresh_status()
+    ref = f64(X).T @ f64(Y)
+    if colscale:
+        ref = ref * f64(g)[None, :]
+    assert_close(f64(out), ref, 1e-5, "split-K X^T Y")
