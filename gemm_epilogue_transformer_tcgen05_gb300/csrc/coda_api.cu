@@ -437,12 +437,15 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
     const int64_t num_kb = (K + (128 / op_bytes) - 1) / (128 / op_bytes);
     int best = 1;
     double best_score = 0.0;
-    if (epi == EPI_STORE && out->dtype == CODA_F32) {
+    // split only when a single pass leaves more than a quarter of the groups idle: the memset
+    // and the reduce-adds cost more than the idle groups otherwise
+    const double eff1 = (double)tiles / (double)(((tiles + groups - 1) / groups) * groups);
+    if (epi == EPI_STORE && out->dtype == CODA_F32 && eff1 < 0.75) {
       for (int sk = 1; sk <= 8; ++sk) {
         if (sk > 1 && num_kb / sk < 32) break;
         const int64_t work = tiles * sk;
         const double eff = (double)work / (double)(((work + groups - 1) / groups) * groups);
-        const double score = eff - 0.01 * (sk - 1);
+        const double score = eff - 0.02 * (sk - 1);
         if (score > best_score + 1e-9) {
           best_score = score;
           best = sk;
