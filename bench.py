@@ -184,6 +184,20 @@ def nvsmi_id(torch):
 
 
 # ------------------------------------------------------------------- distributed
+def max_over_ranks(ms, dist, device="cuda"):
+    """The slowest rank's time (every rank gets it); `dist` None means a single rank."""
+    if dist is None:
+        return float(ms)
+    import torch
+    t = torch.tensor([float(ms)], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tokens_per_s(world, tokens_per_rank, ms):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / (ms * 1e-3)
+
 def dist_init(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -322,15 +336,12 @@ def run_coda(args, world, rank, local):
     st, site = C.coda_get_device_status(stream)
     if st != C.OK:
         raise RuntimeError(f"device status {st} (site {site}) in the timed region")
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist)
     if sampler:
         time.sleep(0.15)
         sampler.stop()
     ms_step = ms / args.steps
-    value = world * M / (ms_step * 1e-3)
+    value = aggregate_tokens_per_s(world, M, ms_step)
 
     # ---- end to end through the public chain call, host buffers (pinned) both ways.
     # Each step copies its inputs O, R from pinned host memory and its result Y back; the
@@ -381,14 +392,42 @@ def run_coda(args, world, rank, local):
         stream.wait_stream(s_out)
         e1.record(stream)
         barrier()
-        ems = e0.elapsed_time(e1) / n_e2e
-        if dist is not None:
-            t = torch.tensor([ems], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * M / (ems * 1e-3), "unit": "tokens/s", "ms_per_step": ems, "steps": n_e2e,
+        ems = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dist)
+        e2e = {"value": aggregate_tokens_per_s(world, M, ems), "unit": "tokens/s", "ms_per_step": ems, "steps": n_e2e,
                "h2d_bytes_per_step": O_h.numel() * 2 + R_h.numel() * 2, "d2h_bytes_per_step": Y_h[0].numel() * 2,
                "pipelined": "copies of neighbouring steps overlap this step's compute (2 slots, 2 copy streams)"}
+
+    # ---- the same chain captured once in a CUDA graph and replayed (host launch work gone)
+    graph_ms = None
+    if rank == 0:
+        gs = torch.cuda.Stream()
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            step_on = lambda: (C.coda_gemm_epilogue(d["O"], d["W_o"], [C.OP_ADD_SIDE, C.OP_ROW_SUMSQ_PARTIAL,
+                                                                        C.OP_STORE_COL_SCALED], h, residual=d["R"],
+                                                    row_partials=P, col_scale=d["g"], store_aux=u, stream=gs),
+                               C.coda_rms_partial_reduce(P, M, H, EPS, r, stream=gs),
+                               C.coda_gemm_epilogue(u, d["W_gu"], [C.OP_ROW_SCALE, C.OP_SWIGLU], a, row_scale=r,
+                                                    stream=gs),
+                               C.coda_gemm_epilogue(a, d["W_d"], [C.OP_ADD_SIDE], Y, residual=h, stream=gs))
+            step_on()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gs):
+            for _ in range(10):
+                step_on()
+        n_rep = max(3, min(args.steps // 10, 50))
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(gs)
+        for _ in range(n_rep):
+            graph.replay()
+        g1.record(gs)
+        torch.cuda.synchronize()
+        graph_ms = g0.elapsed_time(g1) / (10 * n_rep)
+        del graph
 
     # ---- the other chains of the hot path, device-timed the same way (fewer steps)
     others = None
@@ -430,6 +469,9 @@ def run_coda(args, world, rank, local):
     }
     if e2e:
         line["e2e"] = e2e
+    if graph_ms:
+        line["cuda_graph"] = {"ms_per_step": graph_ms, "tokens_per_s": M / (graph_ms * 1e-3),
+                              "note": "10 steps captured once in a CUDA graph, replayed"}
     if others:
         line["other_workloads"] = others
     if compare:
