@@ -417,14 +417,15 @@ def run_coda(args, world, rank, local):
             for _ in range(10):
                 step_on()
         n_rep = max(3, min(args.steps // 10, 50))
-        for _ in range(2):
-            graph.replay()
-        torch.cuda.synchronize()
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record(gs)
-        for _ in range(n_rep):
-            graph.replay()
-        g1.record(gs)
+        with torch.cuda.stream(gs):           # replay() launches on the current stream
+            for _ in range(2):
+                graph.replay()
+            torch.cuda.synchronize()
+            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g0.record(gs)
+            for _ in range(n_rep):
+                graph.replay()
+            g1.record(gs)
         torch.cuda.synchronize()
         graph_ms = g0.elapsed_time(g1) / (10 * n_rep)
         del graph
