@@ -262,7 +262,7 @@ def _run_fp8(C, inp, s_a):
 
 def _fp8_oracle(inp, rows, s_a):
     return O.mlp_fp8(f64(inp["h"])[rows], f64(inp["Xq"])[rows], inp["s_x"], f64(inp["Wq"]), inp["s_w"],
-                     f64(inp["Wdq"]), inp["s_wd"], s_a, inp["eps"], 256)
+                     f64(inp["Wdq"]), inp["s_wd"], s_a, inp["eps"], 128)
 
 
 def _fp8_checks(inp, rows, r, aq, Y, P, s_a, ref):
