@@ -595,11 +595,10 @@ int coda_xent_combine(const float* Pm, const float* Ps, int64_t ld, int32_t npar
 
 size_t coda_workspace_size(int32_t which, int64_t M, int64_t H, int64_t F) {
   if (M < 0 || H < 0 || F < 0) return 0;
-  // row partials: one per half tile (128 columns), 2 * ceil(n / 256) per row
-  if (which == CODA_WS_BLOCK_FWD) return (size_t)(2 * ((H + 255) / 256)) * (size_t)M * sizeof(float);
+  if (which == CODA_WS_BLOCK_FWD) return (size_t)((H + 255) / 256) * (size_t)M * sizeof(float);
   if (which == CODA_WS_BLOCK_BWD || which == CODA_WS_XENT_BWD)
-    return ((size_t)(2 * ((F + 255) / 256)) * (size_t)M + (size_t)((M + 31) / 32) * (size_t)H) * sizeof(float);
-  if (which == CODA_WS_XENT_FWD) return (size_t)(4 * ((F + 255) / 256) + 1) * (size_t)M * sizeof(float);
+    return ((size_t)((F + 255) / 256) * (size_t)M + (size_t)((M + 31) / 32) * (size_t)H) * sizeof(float);
+  if (which == CODA_WS_XENT_FWD) return (size_t)(2 * ((F + 255) / 256) + 1) * (size_t)M * sizeof(float);
   return 0;
 }
 
@@ -637,7 +636,7 @@ int coda_block_forward(const coda_block_fwd* io, void* stream) {
   if (broadcast_gain && !io->u) return CODA_ERR_NULL;
   if (M == 0) return CODA_OK;
   int st;
-  const int64_t nparts = 2 * ((H + 255) / 256);   // one partial per half tile
+  const int64_t nparts = (H + 255) / 256;
   // G1: h = O W_o^T + R, partial sums of squares of h [, u = h * g]
   {
     coda_tensor A = mk(io->O, CODA_BF16, M, H, H), W = mk(io->W_o, CODA_BF16, H, H, H);
@@ -699,8 +698,8 @@ int coda_block_backward(const coda_block_bwd* io, void* stream) {
   if (M == 0) return CODA_OK;
   int st;
   float* S = io->workspace;                          // [F/256, M] row partials of e . Z
-  const int64_t nS = 2 * ((F + 255) / 256);          // one partial per half tile of dA
-  float* Dg = io->workspace + nS * M;                // [ceil(M/32), H] column partials of h t
+  float* Dg = io->workspace + ((F + 255) / 256) * M; // [ceil(M/32), H] column partials of h t
+  const int64_t nS = (F + 255) / 256;
   const int64_t nDg = (M + 31) / 32;
   // b1: e = r [dA U silu'(G) | dA silu(G)],  dA = dY W_d;  row partials of e . Z
   {
@@ -783,7 +782,7 @@ int coda_lm_head_xent_forward(const coda_lm_head_xent_io* io, void* stream) {
   if (M < 0 || H < 8 || H % 8 != 0 || V < 32 || V % 32 != 0) return CODA_ERR_SHAPE;
   if (M == 0) return CODA_OK;
   int st;
-  const int64_t np = 2 * ((V + 255) / 256);   // one partial per half tile
+  const int64_t np = (V + 255) / 256;
   float* Pm = io->workspace;
   float* Ps = io->workspace + np * M;
   float* T = io->workspace + 2 * np * M;
@@ -814,7 +813,7 @@ int coda_lm_head_xent_backward(const coda_lm_head_xent_bwd_io* io, void* stream)
   if (M < 0 || H < 32 || H % 32 != 0 || V < 32 || V % 32 != 0) return CODA_ERR_SHAPE;
   if (M == 0) return CODA_OK;
   int st;
-  const int64_t np = 2 * ((V + 255) / 256);   // one partial per half tile
+  const int64_t np = (V + 255) / 256;
   float* S = io->workspace;              // [np, M] row partials of e . z
   float* Dg = io->workspace + np * M;    // [ceil(M/32), H] column partials of h t
   coda_tensor u = mk(io->u, CODA_BF16, M, H, H), e = mk(io->e, CODA_BF16, M, V, V);

@@ -13,11 +13,9 @@
 //   warp 0      TMA producer: A and B k-blocks into a STAGES-deep shared-memory ring
 //   warp 1      TMEM allocation + single-thread tcgen05.mma issue (128 x 256 x 32 bytes
 //               of K per instruction) into one of two TMEM accumulators (2 x 256 cols)
-//   warps 2..9  epilogue: tcgen05.ld (thread = output row), the epilogue program, row /
+//   warps 2..5  epilogue: tcgen05.ld (thread = output row), the epilogue program, row /
 //               column partial reductions, cast, swizzled staging in shared memory and
-//               TMA stores; side inputs (residual, saved activations) arrive by TMA.  Two
-//               warps share each TMEM lane quadrant (32 rows), one per half of the columns,
-//               so each SM sub-partition runs two epilogue warps.
+//               TMA stores; side inputs (residual, saved activations) arrive by TMA.
 // The two TMEM accumulators let tile t+1's mainloop run under tile t's epilogue.
 //
 // Every wait is bounded (global timer).  On expiry the waiting thread records a site
@@ -41,7 +39,7 @@ constexpr int BK_BYTES = 128;                         // K bytes per stage (one 
 constexpr int KSTEPS = 4;                             // MMAs per stage, 32 bytes of K each
 constexpr int A_STAGE_BYTES = BM * BK_BYTES;          // 16 KB: this CTA's 128 rows of A
 constexpr int TMEM_COLS = 2 * UMMA_N;                 // two fp32 accumulators
-constexpr int NUM_EPI_WARPS = 8;   // two per TMEM lane quadrant, each taking half of a tile's columns
+constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int MAX_SMEM = 232448;                      // 227 KB opt-in per CTA
 
@@ -102,7 +100,7 @@ struct GemmParams {
   const float* rope_cos;  // [rope_seq_len, rope_head_dim / 2]
   const float* rope_sin;
   int rope_seq_len, rope_head_dim, rope_ncols;
-  float* row_part;        // [2 * n_tiles, row_part_ld]: one partial per half tile
+  float* row_part;        // [n_tiles, row_part_ld]
   long long row_part_ld;
   float* row_part2;       // EPI_XENT: sum-exp partials, same layout as row_part (the maxima)
   float* row_out;         // EPI_XENT: [M] logit of each row's target
@@ -137,11 +135,9 @@ struct GemmCfg {
   static constexpr int XSLOT = 32 * 32 * 2;                 // aux output block (bf16)
   static constexpr int NX = AUX ? (EPI == EPI_SWIGLU ? 2 : 1) : 0;   // SwiGLU: G and U; residual: h * g
   static constexpr int OUTSET = NO * OSLOT + NX * XSLOT;
-  static constexpr int HALF_CHUNKS = NCHUNK / 2;   // chunks per epilogue warp
-  // side inputs double-buffered (prefetched two chunks ahead), output staging single
-  static constexpr int EPI_WARP_BYTES = 2 * NS * SSLOT + OUTSET;
+  static constexpr int EPI_WARP_BYTES = 2 * NS * SSLOT + 2 * OUTSET;
   static constexpr int EPI_BYTES = NUM_EPI_WARPS * EPI_WARP_BYTES;
-  static constexpr int BAR_BYTES = 512;
+  static constexpr int BAR_BYTES = 256;
   static constexpr int STAGES_FIT = (MAX_SMEM - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
@@ -323,7 +319,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t sm_stage = base;
   const uint32_t sm_epi = base + C::STAGES * C::STAGE_BYTES;
   const uint32_t sm_bar = sm_epi + C::EPI_BYTES;
-  const int NBAR = 2 * C::STAGES + 5 + 2 * NUM_EPI_WARPS;
+  const int NBAR = 2 * C::STAGES + 13;
   uint8_t* misc = smem_raw + (sm_bar - raw) + 8 * NBAR;
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
@@ -333,7 +329,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #define TFULL_BAR(a) (sm_bar + 8u * (2 * C::STAGES + (a)))
 #define TEMPTY_BAR(a) (sm_bar + 8u * (2 * C::STAGES + 2 + (a)))
 #define SIDE_BAR(w, s) (sm_bar + 8u * (2 * C::STAGES + 4 + 2 * (w) + (s)))
-#define DONE_BAR (sm_bar + 8u * (2 * C::STAGES + 4 + 2 * NUM_EPI_WARPS))
+#define DONE_BAR (sm_bar + 8u * (2 * C::STAGES + 12))
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -494,10 +490,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------ epilogue warps
     const int ew = warp - 2;  // staging ownership
     const int q = warp & 3;   // TMEM lane quadrant this warp may read
-    const int half = ew >> 2; // which half of the tile's columns this warp handles
-    const int c_begin = half * C::HALF_CHUNKS, c_end = c_begin + C::HALF_CHUNKS;
     const uint32_t side_base = sm_epi + ew * C::EPI_WARP_BYTES;
-    const uint32_t oslot = side_base + 2 * C::NS * C::SSLOT;   // single output staging set
+    const uint32_t out_base = side_base + 2 * C::NS * C::SSLOT;
     uint32_t side_par = 0, side_pending = 0;
     float amax_local = 0.f;
     const uint64_t stream_pol = ptx::make_policy_evict_first();  // outputs and side inputs: touched once
@@ -520,7 +514,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       auto live = [&](int c) { return slab_ok && (n0 + 32 * c < p.N); };
       auto issue_side = [&](int c) {
         if constexpr (C::NS > 0) {
-          const int slot = (c - c_begin) & 1;
+          const int slot = c & 1;
           const uint32_t sbar = SIDE_BAR(ew, slot);
           const uint32_t dst = side_base + slot * C::NS * C::SSLOT;
           const bool side1 = C::NS > 1 && !(p.flags & F_NO_SIDE1);
@@ -537,12 +531,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       };
       if constexpr (C::NS > 0) {
-        if (live(c_begin)) {
-          if (lane == 0) issue_side(c_begin);
+        if (live(0)) {
+          if (lane == 0) issue_side(0);
           side_pending |= 1u;
         }
-        if (C::HALF_CHUNKS > 1 && live(c_begin + 1)) {
-          if (lane == 0) issue_side(c_begin + 1);
+        if (C::NCHUNK > 1 && live(1)) {
+          if (lane == 0) issue_side(1);
           side_pending |= 2u;
         }
       }
@@ -567,7 +561,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float rowacc = 0.f;
 
 #pragma unroll 1
-      for (int c = c_begin; c < c_end; ++c) {
+      for (int c = 0; c < C::NCHUNK; ++c) {
         float x[32];
         float xu[C::DUAL ? 32 : 1];
         {
@@ -585,7 +579,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
         }
-        if (c == c_end - 1) {  // this warp's part of the accumulator is read: release it
+        if (c == C::NCHUNK - 1) {  // accumulator fully read: hand it back to the (leader's) MMA warp
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) {
@@ -600,7 +594,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float s0[C::NS > 0 ? 32 : 1];
         float s1[C::NS > 1 ? 32 : 1];
         if constexpr (C::NS > 0) {
-          const int slot = (c - c_begin) & 1;
+          const int slot = c & 1;
           if (live(c)) {
             bool sok = bwait(SIDE_BAR(ew, slot), (side_par >> slot) & 1u, watch, SITE_EPI_SIDE);
             sok = __all_sync(0xffffffffu, sok);
@@ -628,7 +622,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           __syncwarp();
-          if (c + 2 < c_end && live(c + 2)) {
+          if (c + 2 < C::NCHUNK && live(c + 2)) {
             if (lane == 0) issue_side(c + 2);
             side_pending |= 1u << slot;
           }
@@ -776,7 +770,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ---------------------------------------------------------------- stage + store
         if constexpr (C::NO == 0) continue;
         const bool store = col0 < p.N && r0 < p.M;
-        if (lane == 0) ptx::bulk_wait_read<0>();  // the previous chunk's stores have read the staging
+        const uint32_t oslot = out_base + (c & 1) * C::OUTSET;
+        if (lane == 0) ptx::bulk_wait_read<1>();  // the group that last used this set is done reading
         __syncwarp();
         slot_write<C::OUT_DT>(oslot, lane, x);
         if constexpr (C::NO > 1) slot_write<C::OUT_DT>(oslot + C::OSLOT, lane, o1);
@@ -802,13 +797,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       if constexpr (C::EPI == EPI_RESID || C::EPI == EPI_SWIGLU_BWD || C::EPI == EPI_XENT_BWD) {
         if ((C::EPI != EPI_RESID || (p.flags & F_PARTIAL)) && row_ok)
-          p.row_part[(size_t)(2 * nb + half) * p.row_part_ld + row] = rowacc;   // one partial per half tile
+          p.row_part[(size_t)nb * p.row_part_ld + row] = rowacc;
       }
       if constexpr (C::EPI == EPI_XENT) {
         if (row_ok) {
-          p.row_part[(size_t)(2 * nb + half) * p.row_part_ld + row] = xmax;
-          p.row_part2[(size_t)(2 * nb + half) * p.row_part_ld + row] = xsum;
-          if (target >= n0 + 32 * c_begin && target < n0 + 32 * c_end) p.row_out[row] = xtgt;
+          p.row_part[(size_t)nb * p.row_part_ld + row] = xmax;
+          p.row_part2[(size_t)nb * p.row_part_ld + row] = xsum;
+          if (target >= n0 && target < n0 + C::BN_OUT) p.row_out[row] = xtgt;
         }
       }
     }

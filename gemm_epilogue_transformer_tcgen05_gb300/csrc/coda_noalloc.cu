@@ -46,7 +46,7 @@ extern "C" int coda_block_forward_noalloc(const coda_block_fwd* io, void* stream
   if (!io) return CODA_ERR_NULL;
   if (io->workspace != nullptr) return CODA_ERR_SHAPE;  // the scratch is internal here
   if (io->M < 0 || io->H < 1) return CODA_ERR_SHAPE;
-  const int64_t nparts = 2 * ((io->H + 255) / 256);   // one partial per half tile
+  const int64_t nparts = (io->H + 255) / 256;
   if (io->M > 0 && nparts > (int64_t)CODA_NOALLOC_MAX_PARTIALS / io->M) return CODA_ERR_SHAPE;
   float* scratch = nullptr;
   const int st = scratch_on_current_device(&scratch);

@@ -154,8 +154,7 @@ typedef struct coda_side_inputs {
 } coda_side_inputs;
 
 typedef struct coda_aux_outputs {
-  float* row_partials;          /* [2 * ceil(N / 256), row_partials_ld]: one partial per half
-                                   tile (columns [128 p, 128 p + 128)); SWIGLU_BWD: of dA */
+  float* row_partials;          /* [ceil(N / 256), row_partials_ld] (SWIGLU_BWD: tiles of dA) */
   int64_t row_partials_ld;      /* >= M */
   float* col_partials;          /* [ceil(M / 32), col_partials_ld]: one row per 32-row slab */
   int64_t col_partials_ld;      /* >= N */
@@ -238,8 +237,8 @@ typedef struct coda_block_fwd {
   void* a;              /* out [M, F] bf16 */
   void* Y;              /* out [M, H] bf16 */
   void* Z;              /* optional out [M, 2F] bf16: saved [G | U] (training); NULL = not saved */
-  float* Y_partials;    /* optional out [2 H/256, M] fp32: partial sums of squares of Y; NULL = none */
-  float* workspace;     /* [2 H/256, M] fp32 scratch for the partials of h */
+  float* Y_partials;    /* optional out [H/256, M] fp32: partial sums of squares of Y; NULL = none */
+  float* workspace;     /* [H/256, M] fp32 scratch for the partials of h */
 } coda_block_fwd;
 CODA_API int coda_block_forward(const coda_block_fwd* io, void* stream);
 
@@ -255,7 +254,7 @@ CODA_API int coda_block_forward(const coda_block_fwd* io, void* stream);
  *   - The partial sums of squares that G1 writes and the row reduce reads live instead in
  *     a static device array of CODA_NOALLOC_MAX_PARTIALS floats (4 MiB), which every device
  *     that loads the library holds until the process exits.
- *   - Limit: 2 * ceil(H / 256) * M <= CODA_NOALLOC_MAX_PARTIALS (M <= 65536 tokens at
+ *   - Limit: ceil(H / 256) * M <= CODA_NOALLOC_MAX_PARTIALS (M <= 131072 tokens at
  *     H = 2048).  Larger problems, or a non-NULL workspace, return CODA_ERR_SHAPE and
  *     launch nothing.
  *   - Set-up: the first call on each device looks up the array's device address (with
@@ -359,7 +358,7 @@ typedef struct coda_mlp_fp8_io {
   void* a_q;                 /* out [M, F] e4m3 */
   float* amax;               /* out: 1 float (zeroed by this call on the stream) */
   void* Y;                   /* out [M, H] bf16 */
-  float* Y_partials;         /* out [2 H/256, M] fp32 */
+  float* Y_partials;         /* out [H/256, M] fp32 */
 } coda_mlp_fp8_io;
 CODA_API int coda_mlp_fp8(const coda_mlp_fp8_io* io, void* stream);
 

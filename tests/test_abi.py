@@ -43,11 +43,9 @@ def test_status_strings_and_version(L):
 
 
 def test_workspace_sizes(L):
-    # row partials: one per half tile (128 columns) -> 2 * ceil(n / 256) per row
-    assert C.coda_workspace_size(C.WS_BLOCK_FWD, 16384, 2048, 8192) == 16 * 16384 * 4
-    assert C.coda_workspace_size(C.WS_BLOCK_BWD, 16384, 2048, 8192) == (64 * 16384 + 512 * 2048) * 4
-    assert C.coda_workspace_size(C.WS_BLOCK_BWD, 300, 256, 384) == (4 * 300 + 10 * 256) * 4
-    assert C.coda_workspace_size(C.WS_XENT_FWD, 100, 256, 1000) == (4 * 4 + 1) * 100 * 4
+    assert C.coda_workspace_size(C.WS_BLOCK_FWD, 16384, 2048, 8192) == 8 * 16384 * 4
+    assert C.coda_workspace_size(C.WS_BLOCK_BWD, 16384, 2048, 8192) == (32 * 16384 + 512 * 2048) * 4
+    assert C.coda_workspace_size(C.WS_BLOCK_BWD, 300, 256, 384) == (2 * 300 + 10 * 256) * 4
     assert C.coda_workspace_size(7, 1, 1, 1) == 0
 
 

@@ -52,7 +52,7 @@ def test_residual_and_partial_sumsq(C):
     W = seeded((N, K), 6, std=0.05, dtype=BF)
     R = seeded((M, N), 7, dtype=BF)
     out = torch.empty((M, N), dtype=BF, device="cuda")
-    P = torch.full((4, M + 4), -1.0, dtype=torch.float32, device="cuda")   # 2 tiles x 2 halves
+    P = torch.full((2, M + 4), -1.0, dtype=torch.float32, device="cuda")
     C.coda_gemm_epilogue(dev(A), dev(W), [C.OP_ADD_SIDE, C.OP_ROW_SUMSQ_PARTIAL], out, residual=dev(R),
                          row_partials=P)
     torch.cuda.synchronize()
@@ -60,7 +60,7 @@ def test_residual_and_partial_sumsq(C):
     h = O.linear(f64(A), f64(W)) + f64(R)
     assert_close(f64(out), h, TOL_BF16, "A W^T + R")
     Pg = f64(P)
-    assert_close(Pg[:, :M], O.partial_sumsq(h, 128), TOL_BF16, "partial sums of squares")
+    assert_close(Pg[:, :M], O.partial_sumsq(h, 256), TOL_BF16, "partial sums of squares")
     assert np.all(Pg[:, M:] == -1.0), "wrote past M in the partials"
 
 
@@ -162,7 +162,7 @@ def test_swiglu_backward_epilogue(C):
     Z = seeded((M, 2 * F), 26, dtype=BF)
     r = seeded((M,), 27, std=0.2, mean=1.0)
     e = torch.empty((M, 2 * F), dtype=BF, device="cuda")
-    S = torch.empty((2 * (F // 256), M), dtype=torch.float32, device="cuda")
+    S = torch.empty((F // 256, M), dtype=torch.float32, device="cuda")
     C.coda_gemm_epilogue(dev(dY), dev(Wd).t(), [C.OP_SWIGLU_BWD, C.OP_ROW_SCALE, C.OP_ROW_DOT_PARTIAL], e,
                          aux_in=dev(Z), row_scale=dev(r), row_partials=S)
     torch.cuda.synchronize()
@@ -171,8 +171,8 @@ def test_swiglu_backward_epilogue(C):
     G, U = f64(Z)[:, :F], f64(Z)[:, F:]
     ref = f64(r)[:, None] * np.hstack([dA * U * O.silu_grad(G), dA * O.silu(G)])
     assert_close(f64(e), ref, TOL_BF16, "e")
-    s_ref = np.stack([np.sum((ref * f64(Z))[:, np.r_[t * 128:(t + 1) * 128, F + t * 128:F + (t + 1) * 128]], axis=1)
-                      for t in range(F // 128)])
+    s_ref = np.stack([np.sum((ref * f64(Z))[:, np.r_[t * 256:(t + 1) * 256, F + t * 256:F + (t + 1) * 256]], axis=1)
+                      for t in range(F // 256)])
     assert_close(f64(S), s_ref, TOL_BF16, "row partials of e . Z")
 
 
@@ -205,7 +205,7 @@ def test_tf32_residual_and_rowscale(C):
     W = seeded((N, K), 35, std=1 / 16)
     R = seeded((M, N), 36)
     out = torch.empty((M, N), dtype=torch.float32, device="cuda")
-    P = torch.empty((2, M), dtype=torch.float32, device="cuda")
+    P = torch.empty((1, M), dtype=torch.float32, device="cuda")
     C.coda_gemm_epilogue(dev(A), dev(W), [C.OP_ADD_SIDE, C.OP_ROW_SUMSQ_PARTIAL], out, residual=dev(R),
                          row_partials=P)
     torch.cuda.synchronize()
@@ -252,14 +252,14 @@ def test_fp8_swiglu_requant_and_residual(C):
     Wdq = _e4m3(wd, swd)
     h = seeded((M, H), 42, dtype=BF)
     Y = torch.empty((M, H), dtype=BF, device="cuda")
-    P = torch.empty((2, M), dtype=torch.float32, device="cuda")
+    P = torch.empty((1, M), dtype=torch.float32, device="cuda")
     C.coda_gemm_epilogue(aq.view(torch.float8_e4m3fn), dev(Wdq), [C.OP_TENSOR_SCALE, C.OP_ADD_SIDE,
                          C.OP_ROW_SUMSQ_PARTIAL], Y, tensor_scale=sa * swd, residual=dev(h), row_partials=P)
     torch.cuda.synchronize()
     fresh_status()
     Yref = got @ (swd * f64(Wdq)).T + f64(h)
     assert_close(f64(Y), Yref, TOL_BF16, "fp8 down + residual")
-    assert_close(f64(P), O.partial_sumsq(Yref, 128), TOL_BF16, "fp8 partials")
+    assert_close(f64(P), O.partial_sumsq(Yref, 256), TOL_BF16, "fp8 partials")
 
 
 def test_partial_reduce_and_row_rms(C):

@@ -41,7 +41,7 @@ def _prepare(C, M, H, F, seed):
 def _outs(M, H, F):
     return dict(h=torch.empty((M, H), dtype=BF, device="cuda"), r=torch.empty((M,), device="cuda"),
                 a=torch.empty((M, F), dtype=BF, device="cuda"), Y=torch.empty((M, H), dtype=BF, device="cuda"),
-                Yp=torch.empty((2 * ((H + 255) // 256), M), device="cuda"))
+                Yp=torch.empty(((H + 255) // 256, M), device="cuda"))
 
 
 def _with_workspace(C, d, eps, M, H, F):
@@ -82,7 +82,7 @@ def test_no_alloc_refuses_oversized_problems(C):
                               a=fake, Y=fake, workspace=ws)
 
     L = C.lib()
-    too_many_rows = C.NOALLOC_MAX_PARTIALS // (2 * ((2048 + 255) // 256)) + 1
+    too_many_rows = C.NOALLOC_MAX_PARTIALS // ((2048 + 255) // 256) + 1
     assert L.coda_block_forward_noalloc(ctypes.byref(io(too_many_rows, 2048, 8192)), None) == C.ERR_SHAPE
     assert L.coda_block_forward_noalloc(ctypes.byref(io(256, 2048, 8192, fake)), None) == C.ERR_SHAPE
     assert L.coda_block_forward_noalloc(None, None) == C.ERR_NULL
