@@ -22,8 +22,15 @@ __global__ void partial_reduce_kernel(const float* __restrict__ P, int64_t ld, i
                                       float* __restrict__ out) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= M) return;
-  float s = 0.f;
-  for (int t = 0; t < nparts; ++t) s += __ldg(P + (int64_t)t * ld + i);
+  // four independent running sums keep four loads in flight; combined in a fixed order
+  float s4[4] = {0.f, 0.f, 0.f, 0.f};
+  int t = 0;
+  for (; t + 4 <= nparts; t += 4) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) s4[k] += __ldg(P + (int64_t)(t + k) * ld + i);
+  }
+  for (; t < nparts; ++t) s4[0] += __ldg(P + (int64_t)t * ld + i);
+  const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
   if (mode == 0)
     out[i] = rsqrtf(fmaf(s, inv_d, eps));
   else
@@ -230,22 +237,29 @@ cudaError_t launch_xent_reduce(const float* Pm, const float* Ps, int64_t ld, int
 }
 
 // ---------------------------------------------------------------- column reduce
-// Block = 32 columns x 8 row-groups; each thread sums a strided subset of the blocks in a
-// fixed order, then the 8 group sums are added in order (deterministic).
+// Block = 32 columns x 32 row-groups; each thread sums a strided subset of the blocks in a
+// fixed order (two loads in flight), then the 32 group sums are added in order
+// (deterministic).
 __global__ void col_reduce_kernel(const float* __restrict__ parts, int64_t nblocks, int64_t N, int64_t ld,
                                   float* __restrict__ out) {
-  __shared__ float red[8][33];
+  __shared__ float red[32][33];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int64_t j = (int64_t)blockIdx.x * 32 + tx;
-  float s = 0.f;
-  if (j < N)
-    for (int64_t b = ty; b < nblocks; b += 8) s += __ldg(parts + b * ld + j);
-  red[ty][tx] = s;
+  float s0 = 0.f, s1 = 0.f;
+  if (j < N) {
+    int64_t b = ty;
+    for (; b + 32 < nblocks; b += 64) {
+      s0 += __ldg(parts + b * ld + j);
+      s1 += __ldg(parts + (b + 32) * ld + j);
+    }
+    if (b < nblocks) s0 += __ldg(parts + b * ld + j);
+  }
+  red[ty][tx] = s0 + s1;
   __syncthreads();
   if (ty == 0 && j < N) {
     float t = 0.f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) t += red[k][tx];
+    for (int k = 0; k < 32; ++k) t += red[k][tx];
     out[j] = t;
   }
 }
@@ -253,7 +267,7 @@ __global__ void col_reduce_kernel(const float* __restrict__ parts, int64_t nbloc
 cudaError_t launch_col_reduce(const float* parts, int64_t nblocks, int64_t N, int64_t ld, float* out,
                               cudaStream_t s) {
   const int64_t blocks = (N + 31) / 32;
-  col_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(parts, nblocks, N, ld, out);
+  col_reduce_kernel<<<(unsigned)blocks, 1024, 0, s>>>(parts, nblocks, N, ld, out);
   return cudaGetLastError();
 }
 
