@@ -135,13 +135,17 @@ struct GemmCfg {
   static constexpr int XSLOT = 32 * 32 * 2;                 // aux output block (bf16)
   static constexpr int NX = AUX ? (EPI == EPI_SWIGLU ? 2 : 1) : 0;   // SwiGLU: G and U; residual: h * g
   static constexpr int OUTSET = NO * OSLOT + NX * XSLOT;
-  static constexpr int EPI_WARP_BYTES = 2 * NS * SSLOT + 2 * OUTSET;
+  // side inputs are prefetched NSS chunks ahead (one staging set per chunk in flight); the
+  // SwiGLU backward, with two side inputs and two outputs per chunk, goes deeper
+  static constexpr int NSS = EPI == EPI_SWIGLU_BWD ? 4 : 2;
+  static constexpr int EPI_WARP_BYTES = NSS * NS * SSLOT + 2 * OUTSET;
   static constexpr int EPI_BYTES = NUM_EPI_WARPS * EPI_WARP_BYTES;
-  static constexpr int BAR_BYTES = 256;
+  static constexpr int BAR_BYTES = 320;
   static constexpr int STAGES_FIT = (MAX_SMEM - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(STAGES >= 2, "shared memory budget");
+  static_assert(8 * (2 * STAGES + 5 + NSS * NUM_EPI_WARPS) + 8 <= BAR_BYTES, "barrier area");
   static_assert(!(A_MN || B_MN) || KIND == KIND_BF16, "MN-major operands are bf16 only");
   static_assert(!AUX || EPI == EPI_SWIGLU || EPI == EPI_RESID, "aux output: SwiGLU or residual programs");
   static_assert(CG == 1 || CG == 2, "CTA group");
@@ -319,7 +323,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t sm_stage = base;
   const uint32_t sm_epi = base + C::STAGES * C::STAGE_BYTES;
   const uint32_t sm_bar = sm_epi + C::EPI_BYTES;
-  const int NBAR = 2 * C::STAGES + 13;
+  const int NBAR = 2 * C::STAGES + 5 + C::NSS * NUM_EPI_WARPS;
   uint8_t* misc = smem_raw + (sm_bar - raw) + 8 * NBAR;
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
@@ -328,8 +332,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #define EMPTY_BAR(s) (sm_bar + 8u * (C::STAGES + (s)))
 #define TFULL_BAR(a) (sm_bar + 8u * (2 * C::STAGES + (a)))
 #define TEMPTY_BAR(a) (sm_bar + 8u * (2 * C::STAGES + 2 + (a)))
-#define SIDE_BAR(w, s) (sm_bar + 8u * (2 * C::STAGES + 4 + 2 * (w) + (s)))
-#define DONE_BAR (sm_bar + 8u * (2 * C::STAGES + 12))
+#define SIDE_BAR(w, s) (sm_bar + 8u * (2 * C::STAGES + 4 + C::NSS * (w) + (s)))
+#define DONE_BAR (sm_bar + 8u * (2 * C::STAGES + 4 + C::NSS * NUM_EPI_WARPS))
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -347,7 +351,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::mbar_init(TEMPTY_BAR(a), NUM_EPI_WARPS * C::CG);   // both CTAs' epilogue warps
     }
     for (int w = 0; w < NUM_EPI_WARPS; ++w)
-      for (int s = 0; s < 2; ++s) ptx::mbar_init(SIDE_BAR(w, s), 1);
+      for (int s = 0; s < C::NSS; ++s) ptx::mbar_init(SIDE_BAR(w, s), 1);
     ptx::mbar_init(DONE_BAR, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -491,7 +495,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int ew = warp - 2;  // staging ownership
     const int q = warp & 3;   // TMEM lane quadrant this warp may read
     const uint32_t side_base = sm_epi + ew * C::EPI_WARP_BYTES;
-    const uint32_t out_base = side_base + 2 * C::NS * C::SSLOT;
+    const uint32_t out_base = side_base + C::NSS * C::NS * C::SSLOT;
     uint32_t side_par = 0, side_pending = 0;
     float amax_local = 0.f;
     const uint64_t stream_pol = ptx::make_policy_evict_first();  // outputs and side inputs: touched once
@@ -514,7 +518,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       auto live = [&](int c) { return slab_ok && (n0 + 32 * c < p.N); };
       auto issue_side = [&](int c) {
         if constexpr (C::NS > 0) {
-          const int slot = c & 1;
+          const int slot = c % C::NSS;
           const uint32_t sbar = SIDE_BAR(ew, slot);
           const uint32_t dst = side_base + slot * C::NS * C::SSLOT;
           const bool side1 = C::NS > 1 && !(p.flags & F_NO_SIDE1);
@@ -531,13 +535,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       };
       if constexpr (C::NS > 0) {
-        if (live(0)) {
-          if (lane == 0) issue_side(0);
-          side_pending |= 1u;
-        }
-        if (C::NCHUNK > 1 && live(1)) {
-          if (lane == 0) issue_side(1);
-          side_pending |= 2u;
+#pragma unroll
+        for (int c = 0; c < C::NSS; ++c) {
+          if (c < C::NCHUNK && live(c)) {
+            if (lane == 0) issue_side(c);
+            side_pending |= 1u << c;
+          }
         }
       }
 
@@ -594,7 +597,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float s0[C::NS > 0 ? 32 : 1];
         float s1[C::NS > 1 ? 32 : 1];
         if constexpr (C::NS > 0) {
-          const int slot = c & 1;
+          const int slot = c % C::NSS;
           if (live(c)) {
             bool sok = bwait(SIDE_BAR(ew, slot), (side_par >> slot) & 1u, watch, SITE_EPI_SIDE);
             sok = __all_sync(0xffffffffu, sok);
@@ -622,8 +625,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           __syncwarp();
-          if (c + 2 < C::NCHUNK && live(c + 2)) {
-            if (lane == 0) issue_side(c + 2);
+          if (c + C::NSS < C::NCHUNK && live(c + C::NSS)) {
+            if (lane == 0) issue_side(c + C::NSS);
             side_pending |= 1u << slot;
           }
         }
@@ -818,7 +821,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       ptx::bulk_wait<0>();  // every TMA store of this warp has completed
       if (!ok) {
-        for (int s = 0; s < 2; ++s)
+        for (int s = 0; s < C::NSS; ++s)
           if (side_pending & (1u << s)) drain_wait(SIDE_BAR(ew, s), (side_par >> s) & 1u);
       }
     }
