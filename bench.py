@@ -66,6 +66,13 @@ def parse():
     p.add_argument("--no-compare", action="store_true", help="skip the torch eager comparator and error check")
     p.add_argument("--no-others", action="store_true", help="skip the backward / QKV / fp8 chain measurements")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    p.add_argument("--no-layers", action="store_true", help="skip the full decoder-layer measurements")
+    p.add_argument("--traffic-pass", action="store_true",
+                   help="run only the fused chain twice, then the torch eager chain twice (a short program "
+                        "for a per-kernel DRAM-bytes capture); prints one JSON line naming the launches")
+    p.add_argument("--tokens", type=int, default=M_TOK, help="token count of --traffic-pass")
+    p.add_argument("--compile-compare", action="store_true",
+                   help="also time torch.compile of the unfused comparators (compiles on first use)")
     return p.parse_args()
 
 
@@ -266,6 +273,38 @@ def run_reference(args, world, rank):
 
 
 # ------------------------------------------------------------------- the GPU arm
+def traffic_pass(args):
+    """The fused block forward (coda_block_forward: G1, reduce, G2, G3) twice, then the same
+    block as torch eager ops twice, with nothing else on the device: under a per-kernel
+    counter capture the second pass of each is the warm, steady-state one."""
+    import torch
+
+    import coda_synth as S
+    from gemm_epilogue_transformer_tcgen05_gb300 import coda as C
+
+    C.lib()
+    BF = torch.bfloat16
+    M, H, F = args.tokens, HID, FFN
+    d = S.block_inputs(M, H, F, seed=0, device="cuda")
+    h, u, Y = (torch.empty((M, H), dtype=BF, device="cuda") for _ in range(3))
+    r = torch.empty((M,), device="cuda")
+    a = torch.empty((M, F), dtype=BF, device="cuda")
+    ws = torch.empty((C.coda_workspace_size(C.WS_BLOCK_FWD, M, H, F) // 4,), device="cuda")
+    for _ in range(2):
+        C.coda_block_forward(d["O"], d["R"], d["W_o"], d["W_gu"], d["W_d"], EPS, h, r, a, Y, ws, g=d["g"], u=u)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        Yt = unfused_chain(torch, d, F)
+    torch.cuda.synchronize()
+    st, site = C.coda_get_device_status()
+    if st != C.OK:
+        raise RuntimeError(f"device status {st} (site {site})")
+    print(json.dumps({"traffic_pass": {"tokens": M, "hidden": H, "ffn": F,
+                                       "order": "fused chain x2 (G1, reduce, G2, G3), then torch eager chain x2",
+                                       "normwise_diff": float((Y.float() - Yt.float()).abs().max()
+                                                              / Yt.float().abs().max())}}), flush=True)
+
+
 def run_coda(args, world, rank, local):
     import numpy as np
     import torch
@@ -430,10 +469,16 @@ def run_coda(args, world, rank, local):
         graph_ms = g0.elapsed_time(g1) / (10 * n_rep)
         del graph
 
+    # ---- the same chain with L2 cold before every step (the timed line above is warm:
+    # back to back, as in training)
+    cold_ms = cold_l2(torch, step, stream, max(5, min(args.steps, 50))) if rank == 0 else None
+
     # ---- the other chains of the hot path, device-timed the same way (fewer steps)
     others = None
     if not args.no_others and rank == 0:
         others = other_workloads(torch, C, S, args, stream)
+        if not args.no_layers:
+            others.update(layer_workloads(torch, C, S, args, stream))
 
     # ---- comparator: the same chain unfused in torch eager (cuBLAS GEMMs), and errors
     compare = None
@@ -470,6 +515,10 @@ def run_coda(args, world, rank, local):
     }
     if e2e:
         line["e2e"] = e2e
+    if cold_ms:
+        line["cold_l2"] = {"ms_per_step": cold_ms, "tokens_per_s": M / (cold_ms * 1e-3),
+                           "chain_roofline_frac": chain_roof_ms / cold_ms,
+                           "note": "1 GiB scratch write before every step, outside the timed events; median"}
     if graph_ms:
         line["cuda_graph"] = {"ms_per_step": graph_ms, "tokens_per_s": M / (graph_ms * 1e-3),
                               "note": "10 steps captured once in a CUDA graph, replayed"}
@@ -501,6 +550,60 @@ def _time(torch, fn, stream, steps, warmup=3):
     return e0.elapsed_time(e1) / steps
 
 
+def cold_l2(torch, fn, stream, n, warmup=3):
+    """Median device time of fn with L2 cold: a 1 GiB scratch write (eight times L2) runs
+    before every repetition, outside the events that time fn."""
+    scratch = torch.empty((1 << 30,), dtype=torch.uint8, device="cuda")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(warmup + n):
+        scratch.zero_()
+        if i >= warmup:
+            evs[i - warmup][0].record(stream)
+        fn()
+        if i >= warmup:
+            evs[i - warmup][1].record(stream)
+    torch.cuda.synchronize()
+    del scratch
+    return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+
+
+def fp8_peak(torch, seconds=2.0):
+    """Dense e4m3 GEMM throughput of the vendor library (torch._scaled_mm, per-tensor scales,
+    bf16 out) at 8192^3, measured the way the bf16 peaks were: the best of 10 single launches
+    (burst) and back to back for a few seconds (sustained).  A roofline denominator only."""
+    n = 8192
+    gen = torch.Generator(device="cuda").manual_seed(3)
+    a = torch.randn((n, n), device="cuda", generator=gen).to(torch.float8_e4m3fn)
+    b = torch.randn((n, n), device="cuda", generator=gen).to(torch.float8_e4m3fn)
+    one = torch.ones((), device="cuda")
+
+    def f():
+        return torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+
+    for _ in range(5):
+        f()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = float("inf")
+    for _ in range(10):
+        e0.record()
+        f()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    flop = 2.0 * n ** 3
+    reps = max(10, int(seconds * 1e3 / best))
+    e0.record()
+    for _ in range(reps):
+        f()
+    e1.record()
+    torch.cuda.synchronize()
+    sus = flop * reps / (e0.elapsed_time(e1) * 1e-3) / 1e12
+    return {"burst_tflops": flop / (best * 1e-3) / 1e12, "sustained_tflops": sus, "reps_sustained": reps,
+            "how": "torch._scaled_mm e4m3 x e4m3 -> bf16, 8192^3, per-tensor scales: best of 10 (burst); "
+                   f"{reps} back to back (sustained)"}
+
+
 def other_workloads(torch, C, S, args, stream):
     """Device time of the other chains at their full sizes (16384 tokens): the block backward
     (C2), QKV + RoPE (C3) and the fp8 MLP (C4), with TFLOP/s and the fraction of their
@@ -509,6 +612,21 @@ def other_workloads(torch, C, S, args, stream):
     pk = peaks()
     steps = max(5, min(args.steps, 50))
     out = {}
+    # measured e4m3 peak (library GEMM), the denominator of the fp8 chain below
+    try:
+        out["fp8_peak"] = fp8_peak(torch)
+    except Exception as ex:                       # a torch without e4m3 GEMMs: keep the nominal ratio
+        out["fp8_peak"] = {"error": f"{type(ex).__name__}: {ex}"[:200]}
+    # the light row reduce in its full-row form, where bandwidth can be seen: r of a
+    # [16384, 8192] bf16 tensor (268 MB read), back to back
+    Xr = torch.randn((M_TOK, 8192), device="cuda", generator=torch.Generator(device="cuda").manual_seed(5)).to(BF)
+    rr = torch.empty((M_TOK,), device="cuda")
+    ms = _time(torch, lambda: C.coda_row_rms(Xr, EPS, rr, stream=stream), stream, 50)
+    byt = 2 * M_TOK * 8192 + 4 * M_TOK
+    out["row_rms_full_row_M16384_N8192"] = {"ms": ms, "gbs": byt / (ms * 1e-3) / 1e9, "bytes": byt,
+                                             "frac_of_hbm": byt / (ms * 1e-3) / 1e9 / pk["hbm"],
+                                             "peak_kind": f"HBM copy, {pk['source']}"}
+    del Xr, rr
     # C2: block backward (after a training-mode forward that saves Z)
     M, H, F = M_TOK, HID, FFN
     inp = S.block_inputs(M, H, F, seed=0, with_grad=True)
@@ -607,11 +725,17 @@ def other_workloads(torch, C, S, args, stream):
     ms = _time(torch, run8, stream, steps)
     flop = 2 * M * 2 * F8 * H8 + 2 * M * H8 * F8
     byt = (M * H8 + 2 * F8 * H8 + M * F8) + (M * F8 + H8 * F8) + 2 * (M * H8 * 3) + 4 * M * (H8 // 256 + 1)
-    peak8 = 2 * pk["bf16_sus"]
+    if "sustained_tflops" in out["fp8_peak"]:
+        peak8 = out["fp8_peak"]["sustained_tflops"]
+        note = "fp8 peak: e4m3 library GEMM measured above, sustained"
+    else:
+        peak8 = 2 * pk["bf16_sus"]
+        note = "fp8 peak taken as 2x the measured bf16 sustained peak (nominal ratio)"
     roof = max(flop / (peak8 * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
     out["mlp_fp8_C4"] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "roofline_ms": roof,
                          "roofline_frac": roof / ms, "tokens_per_s": M / (ms * 1e-3), "launches": 3,
-                         "peak_note": "fp8 peak taken as 2x the measured bf16 sustained peak (nominal ratio)"}
+                         "peak_tflops": peak8, "peak_note": note,
+                         "frac_of_2x_bf16": flop / (ms * 1e-3) / 1e12 / (2 * pk["bf16_sus"])}
     del h8, X8, W8, Wd8, aq, Y8, P8
     torch.cuda.empty_cache()
     # N3: the block forward at the 7B and 70B LLaMA-3 hidden sizes, beside torch eager
@@ -632,6 +756,9 @@ def other_workloads(torch, C, S, args, stream):
         out[name] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "roofline_ms": roof, "roofline_frac": roof / ms,
                      "tokens_per_s": M / (ms * 1e-3), "launches": 4, "unfused_torch_eager_ms": t_ms,
                      "speedup_vs_unfused": t_ms / ms}
+        if args.compile_compare:
+            out[name].update(compiled_time(torch, lambda: unfused_chain(torch, bi, Fs), stream,
+                                           max(3, min(args.steps, 10)), ms))
         del bi, hs, us, Ys, as_, wss
         torch.cuda.empty_cache()
     # N1: final RMSNorm + LM head + cross-entropy (vocabulary 128256), forward and backward
@@ -662,6 +789,96 @@ def other_workloads(torch, C, S, args, stream):
                      "tokens_per_s": M / (ms * 1e-3), "launches": nl, "vocab": V}
     del hl, gl, Wv, tg, ul, el, dhl, dWv, wsb, wsx
     torch.cuda.empty_cache()
+    return out
+
+
+def compiled_time(torch, fn, stream, steps, ms_coda):
+    """Device time of torch.compile(fn) (compiled on its first calls, outside the timing)."""
+    try:
+        cf = torch.compile(fn)
+        t = _time(torch, cf, stream, steps, warmup=3)
+        return {"torch_compile_ms": t, "speedup_vs_torch_compile": t / ms_coda}
+    except Exception as ex:
+        return {"torch_compile_error": f"{type(ex).__name__}: {ex}"[:200]}
+
+
+LAYERS = (("layer_1B_H2048_F8192", 2048, 8192, 32, 8, 64),
+          ("layer_7B_H4096_F14336", 4096, 14336, 32, 8, 128),
+          ("layer_70B_H8192_F28672", 8192, 28672, 64, 8, 128))
+
+
+def layer_workloads(torch, C, S, args, stream):
+    """A whole LLaMA-style decoder layer forward at 16384 tokens (16 sequences of 1024):
+    attention-input RMSNorm + QKV + RoPE, causal attention with grouped KV heads, output
+    projection + residual, MLP RMSNorm + gate/up + SwiGLU + down + residual.  Attention is
+    the library's (torch scaled_dot_product_attention) on both sides; everything else is
+    either the fused chain (coda_fold_gain + coda_qkv_rope, then coda_block_forward) or
+    torch eager ops with cuBLAS GEMMs.  Device time per layer, both sides, and attention
+    alone."""
+    BF = torch.bfloat16
+    Fn = torch.nn.functional
+    M, seq = M_TOK, 1024
+    B = M // seq
+    steps = max(3, min(args.steps, 10))
+    out = {}
+    for name, H, F, nq, nkv, hd in LAYERS:
+        li = S.layer_inputs(M, H, F, nq, nkv, hd, seed=0, device="cuda")
+        x, g1, Wqkv, W_o, g2, W_gu, W_d = (li[k] for k in ("x", "g_attn", "W_qkv", "W_o", "g_mlp", "W_gu", "W_d"))
+        nqk = (nq + nkv) * hd
+        cos = torch.empty((seq, hd // 2), device="cuda")
+        sin = torch.empty_like(cos)
+        C.coda_rope_table(seq, hd, 500000.0, cos, sin, stream=stream)
+        Wqf = torch.empty_like(Wqkv)
+        r1 = torch.empty((M,), device="cuda")
+        qkv = torch.empty((M, Wqkv.shape[0]), dtype=BF, device="cuda")
+        h, u, Y = (torch.empty((M, H), dtype=BF, device="cuda") for _ in range(3))
+        r2 = torch.empty((M,), device="cuda")
+        a = torch.empty((M, F), dtype=BF, device="cuda")
+        ws = torch.empty((C.coda_workspace_size(C.WS_BLOCK_FWD, M, H, F) // 4,), device="cuda")
+
+        def attention(t):
+            q = t[:, :nq * hd].view(B, seq, nq, hd).transpose(1, 2)
+            k = t[:, nq * hd:nqk].view(B, seq, nkv, hd).transpose(1, 2)
+            v = t[:, nqk:].view(B, seq, nkv, hd).transpose(1, 2)
+            o = Fn.scaled_dot_product_attention(q, k, v, is_causal=True, enable_gqa=True)
+            return o.transpose(1, 2).reshape(M, nq * hd)
+
+        def ours():
+            C.coda_fold_gain(Wqkv, g1, Wqf, stream=stream)
+            C.coda_qkv_rope(x, Wqf, EPS, seq, hd, nqk, cos, sin, r1, qkv, stream=stream)
+            o = attention(qkv)
+            C.coda_block_forward(o, x, W_o, W_gu, W_d, EPS, h, r2, a, Y, ws, g=g2, u=u, stream=stream)
+            return Y
+
+        def rope_t(t, nh):
+            tf = t.float().view(B, seq, nh, hd // 2, 2)
+            c, s_ = cos.view(1, seq, 1, hd // 2), sin.view(1, seq, 1, hd // 2)
+            x0, x1 = tf[..., 0], tf[..., 1]
+            return torch.stack((x0 * c - x1 * s_, x0 * s_ + x1 * c), -1).view(M, nh * hd).to(BF)
+
+        def torch_layer():
+            xf = x.float()
+            xn = (xf * torch.rsqrt(xf.pow(2).mean(-1, keepdim=True) + EPS)).to(BF) * g1.to(BF)
+            t = Fn.linear(xn, Wqkv)
+            t = torch.cat((rope_t(t[:, :nq * hd], nq), rope_t(t[:, nq * hd:nqk], nkv), t[:, nqk:]), 1)
+            o = attention(t)
+            return unfused_chain(torch, {"O": o, "R": x, "W_o": W_o, "g": g2, "W_gu": W_gu, "W_d": W_d}, F)
+
+        ms = _time(torch, ours, stream, steps)
+        t_ms = _time(torch, torch_layer, stream, steps)
+        att_ms = _time(torch, lambda: attention(qkv), stream, steps)
+        Yc = ours().float()
+        Yt = torch_layer().float()
+        torch.cuda.synchronize()
+        diff = float((Yc - Yt).abs().max() / Yt.abs().max())
+        out[name] = {"ms": ms, "torch_eager_ms": t_ms, "speedup_vs_torch_eager": t_ms / ms,
+                     "attention_ms": att_ms, "non_attention_speedup": (t_ms - att_ms) / (ms - att_ms),
+                     "tokens_per_s": M / (ms * 1e-3), "normwise_diff_vs_torch_eager": diff,
+                     "heads": f"{nq} query / {nkv} key-value heads of {hd}"}
+        if args.compile_compare:
+            out[name].update(compiled_time(torch, torch_layer, stream, steps, ms))
+        del li, x, g1, Wqkv, W_o, g2, W_gu, W_d, Wqf, qkv, h, u, Y, a, ws, Yc, Yt
+        torch.cuda.empty_cache()
     return out
 
 
@@ -715,6 +932,10 @@ def main():
     world, rank, local = dist_init(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
+        return
+    if args.traffic_pass:
+        if rank == 0:
+            traffic_pass(args)
         return
     run_coda(args, world, rank, local)
 

@@ -74,6 +74,23 @@ def qkv_inputs(M, H, n_qkv, seed=0, w_std=0.02, dtype=torch.bfloat16):
     )
 
 
+def layer_inputs(M, H, F, n_q, n_kv, head_dim, seed=0, w_std=0.02, dtype=torch.bfloat16, device="cpu"):
+    """One LLaMA-style decoder layer: input x, attention-input gain g_attn and W_qkv (Q heads,
+    then K heads, then V heads), attention-output W_o, MLP gain g_mlp, W_gu (gate rows, then
+    up rows) and W_d."""
+    gen = torch.Generator(device=device).manual_seed(seed)
+    return dict(
+        x=_normal(gen, (M, H)).to(dtype),
+        g_attn=_normal(gen, (H,), std=0.1, mean=1.0),
+        W_qkv=_normal(gen, ((n_q + 2 * n_kv) * head_dim, H), std=w_std).to(dtype),
+        W_o=_normal(gen, (H, n_q * head_dim), std=w_std).to(dtype),
+        g_mlp=_normal(gen, (H,), std=0.1, mean=1.0),
+        W_gu=_normal(gen, (2 * F, H), std=w_std).to(dtype),
+        W_d=_normal(gen, (H, F), std=w_std).to(dtype),
+        eps=1e-6,
+    )
+
+
 def _to_e4m3(x):
     """Per-tensor e4m3 operand: scale = amax/448, codes = torch's float8_e4m3fn cast of x/scale."""
     amax = float(x.abs().max())
