@@ -422,9 +422,15 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
   p.n_tiles = (int)n_tiles;
   {
     // N-tiles per rasterisation group: as many as keep the group's slice of B (all of K)
-    // within about 32 MB of L2.
+    // within about 32 MB of L2.  When K is so long that fewer than ~sqrt(CTA groups) tiles
+    // fit, no slice stays resident anyway; the groups working at the same time then read the
+    // least from DRAM with a near-square footprint (as many N-tiles as M-tiles), since each
+    // distinct A row-block and B column-block they touch is fetched once per wave.
     const int64_t b_tile_bytes = (int64_t)UMMA_N * K * esize(W->dtype);
     int64_t gn = ((int64_t)32 << 20) / (b_tile_bytes > 0 ? b_tile_bytes : 1);
+    int64_t square = 1;
+    while ((square + 1) * (square + 1) <= d->sms / var->cg) ++square;
+    if (gn < square) gn = square;
     gn = gn < 1 ? 1 : (gn > n_tiles ? n_tiles : gn);
     p.group_n = (int)gn;
   }
