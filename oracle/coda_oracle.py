@@ -45,6 +45,11 @@ Readings of points the pages leave open (the plainest reading consistent with th
      saturation to +-448; dequantised value = scale * code value.
   7. Cross-entropy: mean over rows of logsumexp(logits) - logit[target], the final RMSNorm
      before the LM head as in the block chain; every target is a valid class index.
+  8. FP8 backward of the MLP: every backward GEMM takes e4m3 operands with per-tensor
+     scales like the forward's.  The output gradient dY and the SwiGLU-backward output e
+     are quantised with scales the caller supplies (delayed scaling, as for s_a); the GEMMs
+     and the row sum behind c see the dequantised values; the residual gradient (+ dY) and
+     the RMSNorm-backward combine use dY and h as stored (bf16).
 Every function here is pinned by a test (closed form, invariant, library special case
 or brute force); none is "parity unpinned".
 """
@@ -348,6 +353,39 @@ def mlp_fp8(h, Xq_val, s_x, Wq_val, s_w, Wdq_val, s_wd, s_a, eps, bn):
     aq_val = e4m3_round(a / F64(s_a))
     Y = linear(F64(s_a) * aq_val, F64(s_wd) * _f64(Wdq_val)) + _f64(h)
     return dict(r=r, Z=Z, a=a, amax=np.max(np.abs(a)), aq_val=aq_val, Y=Y, P=partial_sumsq(Y, bn))
+
+
+def mlp_fp8_backward(h, Xq_val, s_x, Wq_val, s_w, Wdq_val, s_wd, Z, aq_val, s_a, r, dY, s_dy, s_e,
+                     quant=e4m3_round):
+    """Backward of mlp_fp8 with e4m3 GEMM operands (reading 8).  Saved from the forward: Z =
+    [G | U] (post-r, pre-activation), a_q and r.  W = s_w Wq, W_d = s_wd Wdq, x = s_x Xq.
+      dY_q = quant(dY / s_dy);  dA = (s_dy dY_q) W_d
+      e = r [dA U silu'(G) | dA silu(G)];  e_q = quant(e / s_e);  e_hat = s_e e_q
+      c_i = r_i sum_k e_hat_ik Z_ik / H          (RMSNorm backward, scale-invariant part)
+      t = e_hat W;  dh = t - c h + dY
+      dW_d = (s_dy dY_q)^T (s_a a_q);  dW = e_hat^T x
+    ``quant`` is the quantiser (identity gives the exact-arithmetic chain rule)."""
+    h, Z, r, dY = _f64(h), _f64(Z), _f64(r), _f64(dY)
+    x = F64(s_x) * _f64(Xq_val)
+    W = F64(s_w) * _f64(Wq_val)
+    W_d = F64(s_wd) * _f64(Wdq_val)
+    a = F64(s_a) * _f64(aq_val)
+    H = h.shape[1]
+    F = Z.shape[1] // 2
+    dYq_val = quant(dY / F64(s_dy))
+    dYd = F64(s_dy) * dYq_val
+    dA = dYd @ W_d
+    G, U = Z[:, :F], Z[:, F:]
+    e = r[:, None] * np.hstack([dA * U * silu_grad(G), dA * silu(G)])
+    eq_val = quant(e / F64(s_e))
+    e_hat = F64(s_e) * eq_val
+    s = np.sum(e_hat * Z, axis=1)
+    c = r * s / H
+    t = e_hat @ W
+    dh = t - c[:, None] * h + dY
+    return dict(dYq_val=dYq_val, amax_dy=float(np.max(np.abs(dY))), dA=dA, e=e, eq_val=eq_val,
+                amax_e=float(np.max(np.abs(e))), e_hat=e_hat, s=s, c=c, t=t, dh=dh, dW_d=dYd.T @ a,
+                dW=e_hat.T @ x)
 
 
 # ---------------------------------------------------------------------------------------

@@ -139,3 +139,52 @@ def test_rope_backward_with_forward_rotation_is_caught(monkeypatch):
 
     _plant(monkeypatch, "qkv_rope_backward", bad)
     assert _fails(pins.test_qkv_rope_backward_matches_finite_differences)
+
+
+def _plant_fp8_bwd(monkeypatch, edit):
+    orig = O.mlp_fp8_backward
+
+    def bad(*a, **k):
+        return edit(orig(*a, **k), *a, **k)
+
+    _plant(monkeypatch, "mlp_fp8_backward", bad)
+
+
+def test_fp8_backward_dropped_norm_term_is_caught(monkeypatch):
+    def edit(out, *a, **k):
+        out["dh"] = out["dh"] + out["c"][:, None] * np.asarray(k.get("h", a[0] if a else None), float)
+        return out
+
+    _plant_fp8_bwd(monkeypatch, edit)
+    assert _fails(pins.test_mlp_fp8_backward_identity_quantiser_matches_finite_differences)
+
+
+def test_fp8_backward_missing_e_scale_is_caught(monkeypatch):
+    def edit(out, *a, **k):
+        s_e = k["s_e"] if "s_e" in k else a[13]
+        out["t"] = out["t"] / s_e
+        out["dW"] = out["dW"] / s_e
+        return out
+
+    _plant_fp8_bwd(monkeypatch, edit)
+    assert _fails(pins.test_mlp_fp8_backward_power_of_two_rescaling_is_exact)
+
+
+def test_fp8_backward_weight_gradient_from_h_is_caught(monkeypatch):
+    def edit(out, *a, **k):
+        h = np.asarray(k["h"] if "h" in k else a[0], float)
+        out["dW"] = out["e_hat"].T @ h
+        return out
+
+    _plant_fp8_bwd(monkeypatch, edit)
+    assert _fails(pins.test_mlp_fp8_backward_zero_operands_give_closed_forms)
+
+
+def test_fp8_backward_unquantised_e_is_caught(monkeypatch):
+    def edit(out, *a, **k):
+        s_e = k["s_e"] if "s_e" in k else a[13]
+        out["eq_val"] = out["e"] / s_e
+        return out
+
+    _plant_fp8_bwd(monkeypatch, edit)
+    assert _fails(pins.test_mlp_fp8_backward_quantises_like_the_library_cast)

@@ -327,6 +327,83 @@ def test_mlp_fp8_unit_scales_reduce_to_block_pieces():
     assert res["amax"] == np.max(np.abs(a))
 
 
+# ------------------------------------------------------------------ fp8 MLP backward
+def _mlp_loss(h, W, W_d, dY, eps):
+    """The gain-free MLP forward in exact arithmetic, written out here independently of the
+    oracle (x = h, no quantisation), and its loss sum(Y * dY)."""
+    r = 1.0 / np.sqrt(np.mean(h * h, axis=1) + eps)
+    Z = r[:, None] * (h @ W.T)
+    F = Z.shape[1] // 2
+    G, U = Z[:, :F], Z[:, F:]
+    a = G / (1.0 + np.exp(-G)) * U
+    return float(np.sum((a @ W_d.T + h) * dY)), Z, a, r
+
+
+def test_mlp_fp8_backward_identity_quantiser_matches_finite_differences():
+    eps = 1e-6
+    rng = np.random.default_rng(11)
+    h, W, W_d = rng.normal(size=(3, 8)), 0.5 * rng.normal(size=(8, 8)), 0.5 * rng.normal(size=(8, 4))
+    dY = rng.normal(size=(3, 8))
+    _, Z, a, r = _mlp_loss(h, W, W_d, dY, eps)
+    got = O.mlp_fp8_backward(h, h, 1.0, W, 1.0, W_d, 1.0, Z, a, 1.0, r, dY, 1.0, 1.0,
+                             quant=lambda v: np.asarray(v, float))
+    args = {"h": h, "W": W, "W_d": W_d}
+    for name, key in (("h", "dh"), ("W", "dW"), ("W_d", "dW_d")):
+        fd = np.zeros_like(args[name])
+        for ix in np.ndindex(fd.shape):
+            p = {k: v.copy() for k, v in args.items()}
+            m = {k: v.copy() for k, v in args.items()}
+            p[name][ix] += 1e-6
+            m[name][ix] -= 1e-6
+            fd[ix] = (_mlp_loss(p["h"], p["W"], p["W_d"], dY, eps)[0] -
+                      _mlp_loss(m["h"], m["W"], m["W_d"], dY, eps)[0]) / 2e-6
+        err = np.max(np.abs(got[key] - fd)) / np.max(np.abs(fd))
+        assert err <= 1e-6, (key, err)
+
+
+def _fp8_bwd_case(seed=12, M=8, H=16, F=8):
+    rng = np.random.default_rng(seed)
+    return dict(h=rng.normal(size=(M, H)), Xq_val=O.e4m3_round(rng.normal(size=(M, H)) * 40), s_x=2.0 ** -5,
+                Wq_val=O.e4m3_round(rng.normal(size=(2 * F, H)) * 40), s_w=2.0 ** -7,
+                Wdq_val=O.e4m3_round(rng.normal(size=(H, F)) * 40), s_wd=2.0 ** -6,
+                Z=rng.normal(size=(M, 2 * F)), aq_val=O.e4m3_round(rng.normal(size=(M, F)) * 40), s_a=2.0 ** -4,
+                r=0.5 + rng.random(M), dY=rng.normal(size=(M, H)), s_dy=0.011, s_e=0.0023)
+
+
+def test_mlp_fp8_backward_power_of_two_rescaling_is_exact():
+    # doubling dY with s_dy and s_e keeps every e4m3 code and doubles every gradient exactly
+    b = _fp8_bwd_case()
+    base = O.mlp_fp8_backward(**b)
+    d = dict(b, dY=2 * b["dY"], s_dy=2 * b["s_dy"], s_e=2 * b["s_e"])
+    dbl = O.mlp_fp8_backward(**d)
+    np.testing.assert_array_equal(dbl["dYq_val"], base["dYq_val"])
+    np.testing.assert_array_equal(dbl["eq_val"], base["eq_val"])
+    for k in ("dA", "e", "c", "t", "dh", "dW_d", "dW"):
+        np.testing.assert_array_equal(dbl[k], 2 * base[k], err_msg=k)
+
+
+def test_mlp_fp8_backward_quantises_like_the_library_cast():
+    b = _fp8_bwd_case(seed=13)
+    b["s_dy"] = float(np.max(np.abs(b["dY"]))) / 400.0
+    e = O.mlp_fp8_backward(**b)["e"]
+    b["s_e"] = float(np.max(np.abs(e))) / 400.0
+    res = O.mlp_fp8_backward(**b)
+    cast = lambda v: torch.from_numpy(np.ascontiguousarray(v)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(res["dYq_val"], cast(b["dY"] / b["s_dy"]))
+    np.testing.assert_array_equal(res["eq_val"], cast(res["e"] / b["s_e"]))
+
+
+def test_mlp_fp8_backward_zero_operands_give_closed_forms():
+    b = _fp8_bwd_case(seed=14)
+    res = O.mlp_fp8_backward(**dict(b, Xq_val=np.zeros_like(b["Xq_val"])))
+    assert np.all(res["dW"] == 0)                       # weight gradient of a zero input
+    res = O.mlp_fp8_backward(**dict(b, aq_val=np.zeros_like(b["aq_val"])))
+    assert np.all(res["dW_d"] == 0)
+    res = O.mlp_fp8_backward(**dict(b, Wdq_val=np.zeros_like(b["Wdq_val"])))
+    assert np.all(res["e"] == 0) and np.all(res["dW"] == 0) and np.all(res["c"] == 0)
+    np.testing.assert_array_equal(res["dh"], b["dY"])   # only the residual path is left
+
+
 def test_max_rel_err_floor():
     ref = np.array([0.0, 1.0, -1.0, 1e-9])
     got = ref + np.array([0.01, 0.0, 0.0, 0.01])
