@@ -99,7 +99,7 @@ def _to_e4m3(x):
     return q, scale
 
 
-def fp8_mlp_inputs(M, H, F, seed=0, w_std=0.015):
+def fp8_mlp_inputs(M, H, F, seed=0, w_std=0.015, with_grad=False):
     gen = torch.Generator().manual_seed(seed)
     h = _normal(gen, (M, H)).to(torch.bfloat16)
     W_gu = _normal(gen, (2 * F, H), std=w_std)
@@ -107,7 +107,10 @@ def fp8_mlp_inputs(M, H, F, seed=0, w_std=0.015):
     Xq, s_x = _to_e4m3(h.float())
     Wq, s_w = _to_e4m3(W_gu)
     Wdq, s_wd = _to_e4m3(W_d)
-    return dict(h=h, Xq=Xq, s_x=s_x, Wq=Wq, s_w=s_w, Wdq=Wdq, s_wd=s_wd, eps=1e-6)
+    out = dict(h=h, Xq=Xq, s_x=s_x, Wq=Wq, s_w=s_w, Wdq=Wdq, s_wd=s_wd, eps=1e-6)
+    if with_grad:
+        out["dY"] = _normal(gen, (M, H)).to(torch.bfloat16)
+    return out
 
 
 def lm_head_inputs(M, H, V, seed=0, w_std=0.02, dtype=torch.bfloat16):

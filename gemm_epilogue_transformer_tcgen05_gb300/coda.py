@@ -29,7 +29,7 @@ OP_TENSOR_SCALE, OP_ROW_SCALE, OP_COL_SCALE, OP_ADD_SIDE, OP_SWIGLU, OP_ROPE = 1
 OP_SWIGLU_BWD, OP_RMSBWD_COMBINE, OP_ROW_SUMSQ_PARTIAL, OP_ROW_DOT_PARTIAL = 7, 8, 9, 10
 OP_COL_DOT_PARTIAL, OP_AMAX, OP_STORE_AUX, OP_STORE_COL_SCALED, OP_XENT_PARTIAL, OP_XENT_BWD = 11, 12, 13, 14, 15, 16
 REDUCE_RSQRT_MEAN, REDUCE_SCALE_SUM = 0, 1
-WS_BLOCK_FWD, WS_BLOCK_BWD, WS_XENT_FWD, WS_XENT_BWD = 0, 1, 2, 3
+WS_BLOCK_FWD, WS_BLOCK_BWD, WS_XENT_FWD, WS_XENT_BWD, WS_MLP_FP8_BWD = 0, 1, 2, 3, 4
 MAX_OPS = 8
 
 EXPORTED = [
@@ -38,7 +38,7 @@ EXPORTED = [
     "coda_workspace_size", "coda_get_device_status", "coda_set_watchdog_ms", "coda_inject_dropped_stage",
     "coda_device_sm_count", "coda_status_string", "coda_version", "coda_block_forward_noalloc", "coda_rms_gain",
     "coda_xent_combine", "coda_lm_head_xent_forward", "coda_lm_head_xent_backward", "coda_rope_backward",
-    "coda_qkv_rope_backward",
+    "coda_qkv_rope_backward", "coda_mlp_fp8_backward", "coda_quantize_e4m3",
 ]
 NOALLOC_MAX_PARTIALS = 1 << 20
 
@@ -102,7 +102,16 @@ class CodaMlpFp8(Structure):
     _fields_ = [("M", c_int64), ("H", c_int64), ("F", c_int64), ("eps", c_float), ("s_x", c_float),
                 ("s_w", c_float), ("s_wd", c_float), ("s_a", c_float), ("h", c_void_p), ("X_q", c_void_p),
                 ("W_q", c_void_p), ("W_dq", c_void_p), ("r", c_void_p), ("a_q", c_void_p), ("amax", c_void_p),
-                ("Y", c_void_p), ("Y_partials", c_void_p)]
+                ("Y", c_void_p), ("Y_partials", c_void_p), ("Z", c_void_p)]
+
+
+class CodaMlpFp8Bwd(Structure):
+    _fields_ = [("M", c_int64), ("H", c_int64), ("F", c_int64), ("s_x", c_float), ("s_w", c_float),
+                ("s_wd", c_float), ("s_a", c_float), ("s_dy", c_float), ("s_e", c_float), ("h", c_void_p),
+                ("X_q", c_void_p), ("W_q", c_void_p), ("W_dq", c_void_p), ("Z", c_void_p), ("a_q", c_void_p),
+                ("r", c_void_p), ("dY", c_void_p), ("dY_q", c_void_p), ("amax_dy", c_void_p), ("e_q", c_void_p),
+                ("amax_e", c_void_p), ("c", c_void_p), ("dh", c_void_p), ("dW_d", c_void_p), ("dW", c_void_p),
+                ("workspace", c_void_p)]
 
 
 class CodaXentFwd(Structure):
@@ -154,6 +163,8 @@ def lib():
         "coda_block_backward": [P(CodaBlockBwd), c_void_p],
         "coda_qkv_rope": [P(CodaQkvRope), c_void_p],
         "coda_mlp_fp8": [P(CodaMlpFp8), c_void_p],
+        "coda_mlp_fp8_backward": [P(CodaMlpFp8Bwd), c_void_p],
+        "coda_quantize_e4m3": [P(CodaTensor), c_float, P(CodaTensor), c_void_p, c_void_p],
         "coda_get_device_status": [c_void_p, P(c_int32)],
         "coda_set_watchdog_ms": [c_uint32],
         "coda_inject_dropped_stage": [c_int32],
@@ -390,12 +401,28 @@ def coda_qkv_rope(h, W_qkv, eps, seq_len, head_dim, rope_ncols, rope_cos, rope_s
     _check(lib().coda_qkv_rope(ctypes.byref(io), _stream(stream)), "coda_qkv_rope")
 
 
-def coda_mlp_fp8(h, X_q, W_q, W_dq, s_x, s_w, s_wd, s_a, eps, r, a_q, amax, Y, Y_partials, stream=None):
+def coda_mlp_fp8(h, X_q, W_q, W_dq, s_x, s_w, s_wd, s_a, eps, r, a_q, amax, Y, Y_partials, Z=None, stream=None):
     M, H = h.shape
     F = W_dq.shape[1]
     io = CodaMlpFp8(M, H, F, eps, s_x, s_w, s_wd, s_a, _ptr(h), _ptr(X_q), _ptr(W_q), _ptr(W_dq), _ptr(r),
-                    _ptr(a_q), _ptr(amax), _ptr(Y), _ptr(Y_partials))
+                    _ptr(a_q), _ptr(amax), _ptr(Y), _ptr(Y_partials), _ptr(Z))
     _check(lib().coda_mlp_fp8(ctypes.byref(io), _stream(stream)), "coda_mlp_fp8")
+
+
+def coda_mlp_fp8_backward(h, X_q, W_q, W_dq, Z, a_q, r, dY, s_x, s_w, s_wd, s_a, s_dy, s_e, dY_q, amax_dy, e_q,
+                          amax_e, c, dh, dW_d, dW, workspace, stream=None):
+    M, H = h.shape
+    F = W_dq.shape[1]
+    io = CodaMlpFp8Bwd(M, H, F, s_x, s_w, s_wd, s_a, s_dy, s_e, _ptr(h), _ptr(X_q), _ptr(W_q), _ptr(W_dq), _ptr(Z),
+                       _ptr(a_q), _ptr(r), _ptr(dY), _ptr(dY_q), _ptr(amax_dy), _ptr(e_q), _ptr(amax_e), _ptr(c),
+                       _ptr(dh), _ptr(dW_d), _ptr(dW), _ptr(workspace))
+    _check(lib().coda_mlp_fp8_backward(ctypes.byref(io), _stream(stream)), "coda_mlp_fp8_backward")
+
+
+def coda_quantize_e4m3(X, scale, Q, amax=None, stream=None):
+    x, q = desc(X), desc(Q)
+    _check(lib().coda_quantize_e4m3(ctypes.byref(x), scale, ctypes.byref(q), _ptr(amax), _stream(stream)),
+           "coda_quantize_e4m3")
 
 
 def coda_get_device_status(stream=None):

@@ -151,9 +151,15 @@ const ProgramTemplate kPrograms[] = {
       {CODA_OP_AMAX, true}}},
     {EPI_ROPE, 3, {{CODA_OP_TENSOR_SCALE, true}, {CODA_OP_ROW_SCALE, true}, {CODA_OP_ROPE, false}}},
     {EPI_SWIGLU_BWD,
+     5,
+     {{CODA_OP_TENSOR_SCALE, true},
+      {CODA_OP_SWIGLU_BWD, false},
+      {CODA_OP_ROW_SCALE, true},
+      {CODA_OP_ROW_DOT_PARTIAL, false},
+      {CODA_OP_AMAX, true}}},
+    {EPI_RMSBWD,
      3,
-     {{CODA_OP_SWIGLU_BWD, false}, {CODA_OP_ROW_SCALE, true}, {CODA_OP_ROW_DOT_PARTIAL, false}}},
-    {EPI_RMSBWD, 2, {{CODA_OP_RMSBWD_COMBINE, false}, {CODA_OP_COL_DOT_PARTIAL, false}}},
+     {{CODA_OP_TENSOR_SCALE, true}, {CODA_OP_RMSBWD_COMBINE, false}, {CODA_OP_COL_DOT_PARTIAL, true}}},
     {EPI_XENT, 3, {{CODA_OP_TENSOR_SCALE, true}, {CODA_OP_ROW_SCALE, true}, {CODA_OP_XENT_PARTIAL, false}}},
     {EPI_XENT_BWD,
      4,
@@ -191,9 +197,9 @@ int match_program(const coda_epilogue_program* prog, uint32_t* present) {
 
 namespace coda {
 const VariantEntry* find_variant(const VariantKey& k) {
-  const VariantEntry* tables[3] = {g_variants_fwd, g_variants_bwd, g_variants_lowp};
-  const int counts[3] = {g_num_variants_fwd, g_num_variants_bwd, g_num_variants_lowp};
-  for (int t = 0; t < 3; ++t)
+  const VariantEntry* tables[4] = {g_variants_fwd, g_variants_bwd, g_variants_lowp, g_variants_fp8};
+  const int counts[4] = {g_num_variants_fwd, g_num_variants_bwd, g_num_variants_lowp, g_num_variants_fp8};
+  for (int t = 0; t < 4; ++t)
     for (int i = 0; i < counts[t]; ++i) {
       const VariantKey& v = tables[t][i].key;
       if (v.kind == k.kind && v.epi == k.epi && v.a_mn == k.a_mn && v.b_mn == k.b_mn && v.out_dt == k.out_dt &&
@@ -330,8 +336,9 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
       if (sd.aux_in->dtype != sd.aux_in2->dtype) return CODA_ERR_DTYPE;
     }
     side_dt = to_dt(sd.aux_in->dtype);
-    if (!sd.col_scale || !sd.row_coef) return CODA_ERR_NULL;
-    if (!aligned16(sd.col_scale)) return CODA_ERR_ALIGN;
+    if (!sd.row_coef) return CODA_ERR_NULL;
+    if (sd.col_scale && !aligned16(sd.col_scale)) return CODA_ERR_ALIGN;
+    if (has(CODA_OP_COL_DOT_PARTIAL) && !sd.col_scale) return CODA_ERR_NULL;   // dg needs the gain
   }
   if (has(CODA_OP_ROW_SCALE) && !sd.row_scale) return CODA_ERR_NULL;
   if (has(CODA_OP_COL_SCALE) || has(CODA_OP_STORE_COL_SCALED)) {
@@ -370,7 +377,9 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
     if (!sd.rope_cos || !sd.rope_sin) return CODA_ERR_NULL;
     if (!aligned16(sd.rope_cos) || !aligned16(sd.rope_sin)) return CODA_ERR_ALIGN;
   }
-  if (out->dtype == CODA_E4M3 && epi != EPI_SWIGLU) return CODA_ERR_DTYPE;
+  if (out->dtype == CODA_E4M3 && epi != EPI_SWIGLU && epi != EPI_SWIGLU_BWD) return CODA_ERR_DTYPE;
+  if (epi == EPI_SWIGLU_BWD && has(CODA_OP_AMAX) && out->dtype != CODA_E4M3) return CODA_ERR_UNSUPPORTED_PROGRAM;
+  if (out->dtype == CODA_E4M3 && !(sd.out_scale > 0.f)) return CODA_ERR_SHAPE;   // 1 / scale of the codes
 
   const VariantKey key{kind, epi, a_mn ? 1 : 0, b_mn ? 1 : 0, to_dt(out->dtype), side_dt, want_aux ? 1 : 0};
   const VariantEntry* var = find_variant(key);
@@ -385,14 +394,15 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
   std::memset(&L, 0, sizeof(L));
   const int op_bytes = esize(A->dtype);
   const uint32_t bk = (uint32_t)(128 / op_bytes);
-  // A: K-major box {bk, 128}; MN-major (stored [K][M]) box {64, bk}
+  // A: K-major box {bk, 128}; MN-major (stored [K][M]) box {128 bytes of M, bk}
+  const uint32_t mn_atom = (uint32_t)(128 / op_bytes);
   if (a_mn)
-    st = encode_2d(&L.tmA, A->dtype, A->ptr, M, K, A->ld, 64, bk);
+    st = encode_2d(&L.tmA, A->dtype, A->ptr, M, K, A->ld, mn_atom, bk);
   else
     st = encode_2d(&L.tmA, A->dtype, A->ptr, K, M, A->ld, bk, 128);
   if (st != CODA_OK) return st;
   if (b_mn)
-    st = encode_2d(&L.tmB, W->dtype, W->ptr, W->rows, K, W->ld, 64, bk);
+    st = encode_2d(&L.tmB, W->dtype, W->ptr, W->rows, K, W->ld, mn_atom, bk);
   else
     st = encode_2d(&L.tmB, W->dtype, W->ptr, K, W->rows, W->ld, bk, 128);
   if (st != CODA_OK) return st;
@@ -469,7 +479,8 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
     }
   }
   p.flags = (has(CODA_OP_ROW_SUMSQ_PARTIAL) ? F_PARTIAL : 0) | (has(CODA_OP_AMAX) ? F_AMAX : 0) |
-            (has(CODA_OP_COL_SCALE) ? F_COLSCALE : 0) | (has(CODA_OP_ROW_SCALE) ? F_ROWSCALE : 0) |
+            (has(CODA_OP_COL_SCALE) || (epi == EPI_RMSBWD && sd.col_scale) ? F_COLSCALE : 0) |
+            (has(CODA_OP_ROW_SCALE) ? F_ROWSCALE : 0) | (has(CODA_OP_COL_DOT_PARTIAL) ? F_COLPART : 0) |
             (epi == EPI_RMSBWD && !sd.aux_in2 ? F_NO_SIDE1 : 0);
   if (g_inject_once) {
     p.flags |= F_INJECT_SKIP;
@@ -527,6 +538,21 @@ int coda_row_rms(const coda_tensor* X, float eps, float* r_out, void* stream) {
   if ((st = ensure_device(&dv)) != CODA_OK) return st;
   cudaError_t e = launch_row_rms(X->ptr, X->rows, X->cols, X->ld, eps, r_out, static_cast<cudaStream_t>(stream),
                                  dv->sms);
+  return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
+}
+
+int coda_quantize_e4m3(const coda_tensor* X, float scale, const coda_tensor* Q, float* amax, void* stream) {
+  int st;
+  if ((st = check_tensor(X, false)) != CODA_OK) return st;
+  if ((st = check_tensor(Q, false)) != CODA_OK) return st;
+  if (X->dtype != CODA_BF16 || Q->dtype != CODA_E4M3) return CODA_ERR_DTYPE;
+  if (Q->rows != X->rows || Q->cols != X->cols || X->cols % 16 != 0) return CODA_ERR_SHAPE;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return CODA_ERR_SHAPE;
+  if (X->rows == 0 || X->cols == 0) return CODA_OK;
+  DevState* dv;
+  if ((st = ensure_device(&dv)) != CODA_OK) return st;
+  cudaError_t e = launch_quantize_e4m3(X->ptr, X->rows, X->cols, X->ld, 1.0f / scale, Q->ptr, Q->ld, amax,
+                                       static_cast<cudaStream_t>(stream), dv->sms);
   return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
 }
 
@@ -605,6 +631,7 @@ size_t coda_workspace_size(int32_t which, int64_t M, int64_t H, int64_t F) {
   if (which == CODA_WS_BLOCK_BWD || which == CODA_WS_XENT_BWD)
     return ((size_t)((F + 255) / 256) * (size_t)M + (size_t)((M + 31) / 32) * (size_t)H) * sizeof(float);
   if (which == CODA_WS_XENT_FWD) return (size_t)(2 * ((F + 255) / 256) + 1) * (size_t)M * sizeof(float);
+  if (which == CODA_WS_MLP_FP8_BWD) return (size_t)((F + 255) / 256) * (size_t)M * sizeof(float);
   return 0;
 }
 
@@ -967,13 +994,17 @@ int coda_mlp_fp8(const coda_mlp_fp8_io* io, void* stream) {
   {
     coda_tensor A = mk(io->X_q, CODA_E4M3, M, H, H), W = mk(io->W_q, CODA_E4M3, 2 * F, H, H);
     coda_tensor out = mk(io->a_q, CODA_E4M3, M, F, F);
-    coda_epilogue_program pg = prog_of({CODA_OP_TENSOR_SCALE, CODA_OP_ROW_SCALE, CODA_OP_SWIGLU, CODA_OP_AMAX});
+    coda_tensor Z = mk(io->Z, CODA_BF16, M, 2 * F, 2 * F);
+    coda_epilogue_program pg =
+        io->Z ? prog_of({CODA_OP_TENSOR_SCALE, CODA_OP_ROW_SCALE, CODA_OP_STORE_AUX, CODA_OP_SWIGLU, CODA_OP_AMAX})
+              : prog_of({CODA_OP_TENSOR_SCALE, CODA_OP_ROW_SCALE, CODA_OP_SWIGLU, CODA_OP_AMAX});
     coda_side_inputs sd{};
     sd.tensor_scale = io->s_x * io->s_w;
     sd.row_scale = io->r;
     sd.out_scale = 1.0f / io->s_a;
     coda_aux_outputs ax{};
     ax.amax = io->amax;
+    if (io->Z) ax.store_aux = &Z;
     if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, &ax, stream)) != CODA_OK) return st;
   }
   {
@@ -987,6 +1018,90 @@ int coda_mlp_fp8(const coda_mlp_fp8_io* io, void* stream) {
     ax.row_partials = io->Y_partials;
     ax.row_partials_ld = M;
     if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, &ax, stream)) != CODA_OK) return st;
+  }
+  return CODA_OK;
+}
+
+int coda_mlp_fp8_backward(const coda_mlp_fp8_bwd_io* io, void* stream) {
+  if (!io) return CODA_ERR_NULL;
+  const int64_t M = io->M, H = io->H, F = io->F;
+  if (M < 0 || H < 32 || F < 128 || H % 32 != 0 || F % 128 != 0) return CODA_ERR_SHAPE;
+  if (!(io->s_x > 0.f) || !(io->s_w > 0.f) || !(io->s_wd > 0.f) || !(io->s_a > 0.f) || !(io->s_dy > 0.f) ||
+      !(io->s_e > 0.f))
+    return CODA_ERR_SHAPE;
+  if (!io->W_q || !io->W_dq || !io->amax_dy || !io->amax_e || !io->dW_d || !io->dW) return CODA_ERR_NULL;
+  if (M > 0 && (!io->h || !io->X_q || !io->Z || !io->a_q || !io->r || !io->dY || !io->dY_q || !io->e_q || !io->c ||
+                !io->dh || !io->workspace))
+    return CODA_ERR_NULL;
+  if (M > 0 && !aligned16(io->workspace)) return CODA_ERR_ALIGN;
+  int st;
+  DevState* dv;
+  if ((st = ensure_device(&dv)) != CODA_OK) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(io->amax_dy, 0, sizeof(float), cs) != cudaSuccess ||
+      cudaMemsetAsync(io->amax_e, 0, sizeof(float), cs) != cudaSuccess)
+    return CODA_ERR_LAUNCH;
+  if (M == 0) {   // sums over an empty batch: zero weight gradients
+    if (cudaMemsetAsync(io->dW_d, 0, (size_t)H * F * sizeof(float), cs) != cudaSuccess ||
+        cudaMemsetAsync(io->dW, 0, (size_t)2 * F * H * sizeof(float), cs) != cudaSuccess)
+      return CODA_ERR_LAUNCH;
+    return CODA_OK;
+  }
+  coda_tensor dY = mk(io->dY, CODA_BF16, M, H, H), dYq = mk(io->dY_q, CODA_E4M3, M, H, H);
+  if ((st = coda_quantize_e4m3(&dY, io->s_dy, &dYq, io->amax_dy, stream)) != CODA_OK) return st;
+  float* spart = io->workspace;   // [ceil(F / 256), M] row partials of sum e . Z
+  {
+    // dA = s_dy s_wd (dY_q W_dq); SwiGLU backward with r; e stored as e4m3, row partials
+    coda_tensor W = mk(io->W_dq, CODA_E4M3, F, H, F, CODA_COL_MAJOR);   // logical W_d^T
+    coda_tensor Z = mk(io->Z, CODA_BF16, M, 2 * F, 2 * F), e = mk(io->e_q, CODA_E4M3, M, 2 * F, 2 * F);
+    coda_epilogue_program pg = prog_of({CODA_OP_TENSOR_SCALE, CODA_OP_SWIGLU_BWD, CODA_OP_ROW_SCALE,
+                                        CODA_OP_ROW_DOT_PARTIAL, CODA_OP_AMAX});
+    coda_side_inputs sd{};
+    sd.tensor_scale = io->s_dy * io->s_wd;
+    sd.row_scale = io->r;
+    sd.aux_in = &Z;
+    sd.out_scale = 1.0f / io->s_e;
+    coda_aux_outputs ax{};
+    ax.row_partials = spart;
+    ax.row_partials_ld = M;
+    ax.amax = io->amax_e;
+    if ((st = coda_gemm_epilogue(&dYq, &W, &pg, &sd, &e, &ax, stream)) != CODA_OK) return st;
+  }
+  if ((st = coda_rms_partial_reduce(spart, M, (int32_t)((F + 255) / 256), M, H, 0.f, CODA_REDUCE_SCALE_SUM, io->r,
+                                    io->c, stream)) != CODA_OK)
+    return st;
+  {
+    // dW_d = s_dy s_a (dY_q^T a_q)
+    coda_tensor A = mk(io->dY_q, CODA_E4M3, H, M, H, CODA_COL_MAJOR);
+    coda_tensor W = mk(io->a_q, CODA_E4M3, F, M, F, CODA_COL_MAJOR);
+    coda_tensor out = mk(io->dW_d, CODA_F32, H, F, F);
+    coda_epilogue_program pg = prog_of({CODA_OP_TENSOR_SCALE});
+    coda_side_inputs sd{};
+    sd.tensor_scale = io->s_dy * io->s_a;
+    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, nullptr, stream)) != CODA_OK) return st;
+  }
+  {
+    // dh = s_e s_w (e_q W_q) - c h + dY
+    coda_tensor A = mk(io->e_q, CODA_E4M3, M, 2 * F, 2 * F);
+    coda_tensor W = mk(io->W_q, CODA_E4M3, H, 2 * F, H, CODA_COL_MAJOR);   // logical W^T
+    coda_tensor h = mk(io->h, CODA_BF16, M, H, H), out = mk(io->dh, CODA_BF16, M, H, H);
+    coda_epilogue_program pg = prog_of({CODA_OP_TENSOR_SCALE, CODA_OP_RMSBWD_COMBINE});
+    coda_side_inputs sd{};
+    sd.tensor_scale = io->s_e * io->s_w;
+    sd.row_coef = io->c;
+    sd.aux_in = &h;
+    sd.aux_in2 = &dY;
+    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, nullptr, stream)) != CODA_OK) return st;
+  }
+  {
+    // dW = s_e s_x (e_q^T X_q)
+    coda_tensor A = mk(io->e_q, CODA_E4M3, 2 * F, M, 2 * F, CODA_COL_MAJOR);
+    coda_tensor W = mk(io->X_q, CODA_E4M3, H, M, H, CODA_COL_MAJOR);
+    coda_tensor out = mk(io->dW, CODA_F32, 2 * F, H, H);
+    coda_epilogue_program pg = prog_of({CODA_OP_TENSOR_SCALE});
+    coda_side_inputs sd{};
+    sd.tensor_scale = io->s_e * io->s_x;
+    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, nullptr, stream)) != CODA_OK) return st;
   }
   return CODA_OK;
 }

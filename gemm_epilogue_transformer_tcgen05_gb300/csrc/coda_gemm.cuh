@@ -57,8 +57,10 @@ enum : int {
   EPI_SWIGLU = 3,      // Z = ts * r_row * acc (gate | up halves); out = silu(Zg) * Zu * os
                        //   [+ saved Z, + amax |silu(Zg) * Zu|]
   EPI_ROPE = 4,        // out = rope(ts * r_row * acc) on the first rope_ncols columns
-  EPI_SWIGLU_BWD = 5,  // e = r_row * [dA * Zu * silu'(Zg) | dA * silu(Zg)]; row partial sum e . Z
-  EPI_RMSBWD = 6,      // out = g_col * acc - c_row * h [+ dY]; column partial sum h * acc
+  EPI_SWIGLU_BWD = 5,  // dA = ts * acc; e = r_row * [dA * Zu * silu'(Zg) | dA * silu(Zg)]; row partial
+                       //   sum e . Z; e4m3 out: codes of e * os, partial of the dequantised e, amax |e|
+  EPI_RMSBWD = 6,      // t = ts * acc; out = g_col * t - c_row * h [+ dY] (g = 1 without F_COLSCALE);
+                       //   column partial sum h * t (F_COLPART)
   EPI_XENT = 7,        // z = ts * r_row * acc (logits, never stored): per tile and row the online
                        //   state (max_j z, sum_j exp(z - max)) and the target's logit
   EPI_XENT_BWD = 8,    // z as above; e = r_row * os * (exp(z - lse_row) - [j == target_row]);
@@ -71,6 +73,7 @@ enum : int {
   F_COLSCALE = 8,   // multiply by col_scale (EPI_STORE)
   F_ROWSCALE = 16,  // multiply by row_scale (EPI_SWIGLU / EPI_ROPE / EPI_ROWSCALE / EPI_SWIGLU_BWD)
   F_NO_SIDE1 = 32,  // EPI_RMSBWD without the dY side input
+  F_COLPART = 64,   // write column partials (EPI_RMSBWD)
   F_INJECT_SKIP = 1 << 30,  // test hook: the producer drops its first k-block
 };
 
@@ -146,7 +149,12 @@ struct GemmCfg {
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(STAGES >= 2, "shared memory budget");
   static_assert(8 * (2 * STAGES + 5 + NSS * NUM_EPI_WARPS) + 8 <= BAR_BYTES, "barrier area");
-  static_assert(!(A_MN || B_MN) || KIND == KIND_BF16, "MN-major operands are bf16 only");
+  static_assert(!(A_MN || B_MN) || KIND != KIND_TF32, "MN-major operands are bf16 or e4m3");
+  // MN-major operands: a 128-byte swizzle row holds MN_ATOM elements of M (or N); one atom is
+  // BK rows of K; a 128-row tile is BM / MN_ATOM atoms; one MMA consumes UMMA_K rows of K
+  static constexpr int MN_ATOM = 128 / OP_BYTES;
+  static constexpr int MN_ATOM_BYTES = BK * 128;
+  static constexpr int UMMA_K = 32 / OP_BYTES;
   static_assert(!AUX || EPI == EPI_SWIGLU || EPI == EPI_RESID, "aux output: SwiGLU or residual programs");
   static_assert(CG == 1 || CG == 2, "CTA group");
   // instruction descriptor: D f32, A/B format, operand majors, N >> 3, M >> 4
@@ -411,8 +419,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ptx::tma_load_2d_hint(dst, m, c0, c1, fb, pol);
             };
             if constexpr (C::A_MN) {
-              load(sa, &tmA, m0, k0, normal);
-              load(sa + 8192, &tmA, m0 + 64, k0, normal);
+#pragma unroll
+              for (int j = 0; j < BM / C::MN_ATOM; ++j)
+                load(sa + C::MN_ATOM_BYTES * j, &tmA, m0 + C::MN_ATOM * j, k0, normal);
             } else {
               load(sa, &tmA, k0, m0, normal);
             }
@@ -420,7 +429,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if constexpr (C::B_MN) {
               const int n0 = nb * UMMA_N + (int)rank * C::B_ROWS;
 #pragma unroll
-              for (int j = 0; j < C::B_ROWS / 64; ++j) load(sb + 8192 * j, &tmB, n0 + 64 * j, k0, keep);
+              for (int j = 0; j < C::B_ROWS / C::MN_ATOM; ++j)
+                load(sb + C::MN_ATOM_BYTES * j, &tmB, n0 + C::MN_ATOM * j, k0, keep);
             } else {
 #pragma unroll
               for (int h = 0; h < C::B_ROWS / 128; ++h) {
@@ -472,8 +482,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sb = sa + A_STAGE_BYTES;
 #pragma unroll
           for (int k = 0; k < KSTEPS; ++k) {
-            const uint64_t ad = C::A_MN ? smem_desc(sa + k * 2048, 8192, 1024) : smem_desc(sa + k * 32, 16, 1024);
-            const uint64_t bd = C::B_MN ? smem_desc(sb + k * 2048, 8192, 1024) : smem_desc(sb + k * 32, 16, 1024);
+            const uint64_t ad = C::A_MN ? smem_desc(sa + k * C::UMMA_K * 128, C::MN_ATOM_BYTES, 1024)
+                                        : smem_desc(sa + k * 32, 16, 1024);
+            const uint64_t bd = C::B_MN ? smem_desc(sb + k * C::UMMA_K * 128, C::MN_ATOM_BYTES, 1024)
+                                        : smem_desc(sb + k * 32, 16, 1024);
             ptx::umma<C::KIND, C::CG>(d_tmem, ad, bd, C::IDESC, (kb != kb0 || k != 0) ? 1u : 0u);
           }
           ptx::umma_commit<C::CG>(EMPTY_BAR(stage));  // frees the stage (in both CTAs) once done
@@ -712,12 +724,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
         } else if constexpr (C::EPI == EPI_SWIGLU_BWD) {
+          const float sc = ts * rs;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float dA = x[j], G = s0[j], U = s1[j];
             const float sg = sigmoid_f(G);
-            const float eg = as_stored<C::OUT_DT>(rs * dA * U * sg * (1.f + G * (1.f - sg)));
-            const float eu = as_stored<C::OUT_DT>(rs * dA * G * sg);
+            float eg = sc * dA * U * sg * (1.f + G * (1.f - sg));
+            float eu = sc * dA * G * sg;
+            if constexpr (C::OUT_DT == DT_E4M3) {
+              // stored: the e4m3 codes of e * os; the partial sums the dequantised e (the
+              // sum is scaled back once per row below)
+              amax_local = fmaxf(amax_local, fmaxf(fabsf(eg), fabsf(eu)));
+              ptx::e4m3x2_to_f32(ptx::cvt_e4m3x2(eg * p.out_scale, eu * p.out_scale), eg, eu);
+            } else {
+              eg = as_stored<C::OUT_DT>(eg);
+              eu = as_stored<C::OUT_DT>(eu);
+            }
             rowacc = fmaf(eg, G, fmaf(eu, U, rowacc));
             x[j] = eg;
             o1[j] = eu;
@@ -754,20 +776,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         } else if constexpr (C::EPI == EPI_RMSBWD) {
           float ht[32];
-          const float4* g4 = reinterpret_cast<const float4*>(p.col_scale + col0);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 g = __ldg(g4 + j);
-            const float gv[4] = {g.x, g.y, g.z, g.w};
+          for (int j = 0; j < 32; ++j) {
+            x[j] *= ts;                 // t
+            ht[j] = s0[j] * x[j];       // h * t
+          }
+          if (p.flags & F_COLSCALE) {
+            const float4* g4 = reinterpret_cast<const float4*>(p.col_scale + col0);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int e = 4 * j + k;
-              ht[e] = s0[e] * x[e];
-              x[e] = gv[k] * x[e] - rc * s0[e] + s1[e];
+            for (int j = 0; j < 8; ++j) {
+              const float4 g = __ldg(g4 + j);
+              const float gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) x[4 * j + k] *= gv[k];
             }
           }
-          const float colsum = warp_transpose_sum(ht, lane);
-          if (slab_ok && col0 + lane < p.N) p.col_part[(size_t)(r0 >> 5) * p.col_part_ld + col0 + lane] = colsum;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[j] = x[j] - rc * s0[j] + s1[j];
+          if (p.flags & F_COLPART) {
+            const float colsum = warp_transpose_sum(ht, lane);
+            if (slab_ok && col0 + lane < p.N) p.col_part[(size_t)(r0 >> 5) * p.col_part_ld + col0 + lane] = colsum;
+          }
         }
 
         // ---------------------------------------------------------------- stage + store
@@ -798,6 +827,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       if (!ok) break;
+      if constexpr (C::EPI == EPI_SWIGLU_BWD && C::OUT_DT == DT_E4M3) rowacc *= 1.f / p.out_scale;
       if constexpr (C::EPI == EPI_RESID || C::EPI == EPI_SWIGLU_BWD || C::EPI == EPI_XENT_BWD) {
         if ((C::EPI != EPI_RESID || (p.flags & F_PARTIAL)) && row_ok)
           p.row_part[(size_t)nb * p.row_part_ld + row] = rowacc;
@@ -810,7 +840,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     }
-    if constexpr (C::EPI == EPI_SWIGLU) {
+    if constexpr (C::EPI == EPI_SWIGLU || (C::EPI == EPI_SWIGLU_BWD && C::OUT_DT == DT_E4M3)) {
       if (p.flags & F_AMAX) {
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1)

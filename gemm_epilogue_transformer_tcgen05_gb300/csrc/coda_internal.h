@@ -27,6 +27,8 @@ extern const VariantEntry g_variants_bwd[];
 extern const int g_num_variants_bwd;
 extern const VariantEntry g_variants_lowp[];
 extern const int g_num_variants_lowp;
+extern const VariantEntry g_variants_fp8[];
+extern const int g_num_variants_fp8;
 
 const VariantEntry* find_variant(const VariantKey& k);
 
@@ -46,6 +48,8 @@ cudaError_t launch_rms_gain(const void* X, int64_t M, int64_t d, int64_t ld, con
 cudaError_t launch_rope_bwd(const void* dout, const void* out, int64_t M, int64_t N, int64_t ld, const float* r,
                             const float* cs, const float* sn, int seq_len, int head_dim, int rope_ncols, int64_t H,
                             void* e, int64_t lde, float* c, cudaStream_t s);
+cudaError_t launch_quantize_e4m3(const void* X, int64_t M, int64_t N, int64_t ldx, float inv_scale, void* Q,
+                                 int64_t ldq, float* amax, cudaStream_t s, int sms);
 cudaError_t launch_xent_reduce(const float* Pm, const float* Ps, int64_t ld, int nparts, int64_t M, const float* T,
                                const int* targets, int64_t V, float* lse, float* loss, float* mean, cudaStream_t s);
 

@@ -263,5 +263,18 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Packed e4m3x2 -> the two fp32 values (exact: every e4m3 value is an f16 value); the low
+// byte gives `lo`.
+__device__ __forceinline__ void e4m3x2_to_f32(uint16_t v, float& lo, float& hi) {
+  asm volatile(
+      "{\n\t.reg .b16 l, h;\n\t.reg .b32 t;\n\t"
+      "cvt.rn.f16x2.e4m3x2 t, %2;\n\t"
+      "mov.b32 {l, h}, t;\n\t"
+      "cvt.f32.f16 %0, l;\n\t"
+      "cvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "h"(v));
+}
+
 }  // namespace ptx
 }  // namespace coda

@@ -338,6 +338,51 @@ __global__ void rope_table_kernel(int seq_len, int half, double base, int head_d
   s[idx] = (float)sn;
 }
 
+// ---------------------------------------------------------------- e4m3 quantisation
+// Q[i, j] = e4m3(X[i, j] * inv_scale) (nearest even, saturating); 16 elements (32 bytes in,
+// 16 bytes out) per thread per step, grid-stride; optional running max of |X|.
+__global__ void quantize_e4m3_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, int64_t N, int64_t ldx,
+                                     float inv_scale, uint8_t* __restrict__ Q, int64_t ldq,
+                                     unsigned int* __restrict__ amax) {
+  const int64_t nv = N >> 4;
+  const int64_t total = M * nv;
+  float m = 0.f;
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = v / nv, j = (v - i * nv) << 4;
+    const uint4* src = reinterpret_cast<const uint4*>(X + i * ldx + j);
+    const uint4 u0 = __ldcs(src), u1 = __ldcs(src + 1);
+    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float a0 = __uint_as_float(w[2 * e] << 16), a1 = __uint_as_float(w[2 * e] & 0xFFFF0000u);
+      const float a2 = __uint_as_float(w[2 * e + 1] << 16), a3 = __uint_as_float(w[2 * e + 1] & 0xFFFF0000u);
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3))));
+      o[e] = (uint32_t)ptx::cvt_e4m3x2(a0 * inv_scale, a1 * inv_scale) |
+             ((uint32_t)ptx::cvt_e4m3x2(a2 * inv_scale, a3 * inv_scale) << 16);
+    }
+    __stcs(reinterpret_cast<uint4*>(Q + i * ldq + j), make_uint4(o[0], o[1], o[2], o[3]));
+  }
+  if (amax) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((threadIdx.x & 31) == 0 && m > 0.f) atomicMax(amax, __float_as_uint(m));   // |x| orders as its bits
+  }
+}
+
+cudaError_t launch_quantize_e4m3(const void* X, int64_t M, int64_t N, int64_t ldx, float inv_scale, void* Q,
+                                 int64_t ldq, float* amax, cudaStream_t s, int sms) {
+  const int threads = 256;
+  const int64_t total = M * (N >> 4);
+  int64_t blocks = (total + threads - 1) / threads;
+  if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+  if (blocks < 1) blocks = 1;
+  quantize_e4m3_kernel<<<(unsigned)blocks, threads, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(X), M, N, ldx,
+                                                            inv_scale, reinterpret_cast<uint8_t*>(Q), ldq,
+                                                            reinterpret_cast<unsigned int*>(amax));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_rope_table(int seq_len, int head_dim, double base, float* cos_out, float* sin_out,
                               cudaStream_t s) {
   const int half = head_dim / 2;

@@ -98,11 +98,15 @@ typedef struct coda_tensor {
  *        W holds 2N rows (gate rows [0, N), up rows [N, 2N)); Z = s * r[i] * acc over
  *        2N columns; out = silu(Z_gate) * Z_up (times out_scale); STORE_AUX saves Z.
  *   {ROW_SCALE, ROPE}                         out = rope(r[i] * acc)
- *   {SWIGLU_BWD, ROW_SCALE, ROW_DOT_PARTIAL}  acc = dA; with Z = [G | U] from aux_in:
+ *   {SWIGLU_BWD, ROW_SCALE, ROW_DOT_PARTIAL [, AMAX]}   (optionally TENSOR_SCALE first)
+ *        dA = s * acc; with Z = [G | U] from aux_in:
  *        out[:, j] = r dA U silu'(G),  out[:, N + j] = r dA silu(G)   (out is [M, 2N]);
- *        row partials of sum_j out . Z
- *   {RMSBWD_COMBINE, COL_DOT_PARTIAL}         acc = t; h = aux_in, dY = aux_in2 (optional):
- *        out = g[j] t - c[i] h [+ dY]; column partials of h * t
+ *        row partials of sum_j out . Z.  e4m3 out: the codes of out * out_scale are stored,
+ *        the partials sum the dequantised values (code / out_scale) and AMAX keeps max |out|
+ *        before quantisation.
+ *   {[TENSOR_SCALE,] RMSBWD_COMBINE [, COL_DOT_PARTIAL]}   t = s * acc; h = aux_in, dY =
+ *        aux_in2 (optional), g = side.col_scale (optional, 1 when NULL):
+ *        out = g[j] t - c[i] h [+ dY]; COL_DOT_PARTIAL (needs g): column partials of h * t
  *   {[TENSOR_SCALE,] [ROW_SCALE,] XENT_PARTIAL}    z = s * r[i] * acc are logits (never stored;
  *        out only gives the shape [M, V], its ptr may be NULL); per 256-column tile t and row i:
  *        aux.row_partials[t, i] = max_j z_ij, aux.row_partials2[t, i] = sum_j exp(z_ij - max),
@@ -123,7 +127,7 @@ enum coda_op {
   CODA_OP_ROW_SUMSQ_PARTIAL = 9, /* aux.row_partials[t, i] = sum over tile t of out^2 */
   CODA_OP_ROW_DOT_PARTIAL = 10,  /* aux.row_partials[t, i] = sum over tile t of out . Z */
   CODA_OP_COL_DOT_PARTIAL = 11,  /* aux.col_partials[b, j] = sum over 32-row block b of h * t */
-  CODA_OP_AMAX = 12,             /* atomic max of |silu(gate) * up| into *aux.amax */
+  CODA_OP_AMAX = 12,             /* atomic max of |out| before the e4m3 cast into *aux.amax */
   CODA_OP_STORE_AUX = 13,        /* save the pre-activation Z to aux.store_aux */
   CODA_OP_STORE_COL_SCALED = 14, /* also store out[i, j] * side.col_scale[j] to aux.store_aux [M, N] bf16 */
   CODA_OP_XENT_PARTIAL = 15,     /* online (max, sum-exp) state and target logit per row and tile */
@@ -149,7 +153,7 @@ typedef struct coda_side_inputs {
   int32_t rope_head_dim;        /* ROPE: 32, 64, 128 or 256 */
   int32_t rope_ncols;           /* ROPE: columns [0, rope_ncols) rotated; multiple of head_dim */
   float tensor_scale;           /* TENSOR_SCALE: s (e.g. s_x * s_w for fp8) */
-  float out_scale;              /* e4m3 output of SWIGLU: 1 / s_a before the cast; XENT_BWD: dloss / M */
+  float out_scale;              /* e4m3 outputs: 1 / scale before the cast (> 0); XENT_BWD: dloss / M */
   const int32_t* row_index;     /* XENT_PARTIAL, XENT_BWD: [M] target class of each row, in [0, N) */
 } coda_side_inputs;
 
@@ -168,8 +172,9 @@ typedef struct coda_aux_outputs {
  *   A    logical [M, K]: ROW_MAJOR (K contiguous) or COL_MAJOR (M contiguous).
  *   W    logical [N, K] (nn.Linear [out, in] layout when ROW_MAJOR); [2N, K] for SWIGLU.
  *   out  logical [M, N] ROW_MAJOR ([M, 2N] for SWIGLU_BWD).
- * Operand dtypes: bf16 x bf16, e4m3 x e4m3 (ROW_MAJOR only), f32 x f32 (tf32, ROW_MAJOR
- * only).  N must be a multiple of 32 (of 128 for SWIGLU), K >= 1.  M = 0 or N = 0 is a
+ * Operand dtypes: bf16 x bf16, e4m3 x e4m3, f32 x f32 (tf32, ROW_MAJOR only); which
+ * layouts each program has compiled is listed in the variant tables (others return
+ * CODA_ERR_UNSUPPORTED_PROGRAM or CODA_ERR_DTYPE).  N must be a multiple of 32 (of 128 for SWIGLU), K >= 1.  M = 0 or N = 0 is a
  * no-op.  `side` and `aux` may be NULL when the program needs none of their fields. */
 CODA_API int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_epilogue_program* prog,
                        const coda_side_inputs* side, const coda_tensor* out, const coda_aux_outputs* aux,
@@ -359,8 +364,53 @@ typedef struct coda_mlp_fp8_io {
   float* amax;               /* out: 1 float (zeroed by this call on the stream) */
   void* Y;                   /* out [M, H] bf16 */
   float* Y_partials;         /* out [H/256, M] fp32 */
+  void* Z;                   /* optional out [M, 2F] bf16: saved [G | U] for the backward; NULL = none */
 } coda_mlp_fp8_io;
 CODA_API int coda_mlp_fp8(const coda_mlp_fp8_io* io, void* stream);
+
+/* Backward of the FP8 MLP, every GEMM on e4m3 operands with per-tensor scales like the
+ * forward's.  The output gradient dY and the SwiGLU-backward output e are quantised with
+ * the caller's scales s_dy and s_e (delayed scaling: take them from amax_dy / 448 and
+ * amax_e / 448 of an earlier step) [KuCoin, "El epílogo esconde un tesoro" (the backward
+ * inherits the epilogue structure); "El «impuesto a la pereza» para entrenar modelos
+ * grandes" (FP8 shrinks the GEMM time, so the non-GEMM traffic weighs more)]:
+ *   dY_q = e4m3(dY / s_dy);  dA = s_dy s_wd (dY_q W_dq)          (W_dq read MN-major)
+ *   e = r [dA U silu'(G) | dA silu(G)];  e_q = e4m3(e / s_e)     (in the dA GEMM's epilogue)
+ *   c = r sum_k (s_e e_q) Z / H;  dh = s_e s_w (e_q W_q) - c h + dY
+ *   dW_d = s_dy s_a (dY_q^T a_q);  dW = s_e s_x (e_q^T X_q)      (both operands MN-major)
+ * dW is the gradient of the effective gate/up weight s_w W_q (the gain, if any, folded in).
+ * Six launches: quantise dY, dA GEMM, row reduce, dW_d GEMM, dh GEMM, dW GEMM.  The e4m3
+ * quantisations divide by the scale as a multiply by its fp32 reciprocal.  All scales must
+ * be > 0 (else CODA_ERR_SHAPE).  M = 0 zeroes dW_d, dW and the two amax outputs; the
+ * M-sized pointers may then be NULL. */
+typedef struct coda_mlp_fp8_bwd_io {
+  int64_t M, H, F;
+  float s_x, s_w, s_wd, s_a, s_dy, s_e;
+  const void* h;             /* [M, H] bf16 forward input (residual, source of r) */
+  const void* X_q;           /* [M, H] e4m3 */
+  const void* W_q;           /* [2F, H] e4m3 */
+  const void* W_dq;          /* [H, F] e4m3 */
+  const void* Z;             /* [M, 2F] bf16 saved by the forward */
+  const void* a_q;           /* [M, F] e4m3 saved by the forward */
+  const float* r;            /* [M] saved by the forward */
+  const void* dY;            /* [M, H] bf16 */
+  void* dY_q;                /* out [M, H] e4m3 */
+  float* amax_dy;            /* out: max |dY| (zeroed by this call on the stream) */
+  void* e_q;                 /* out [M, 2F] e4m3 */
+  float* amax_e;             /* out: max |e| before quantisation (zeroed by this call) */
+  float* c;                  /* out [M] */
+  void* dh;                  /* out [M, H] bf16 */
+  float* dW_d;               /* out [H, F] fp32 */
+  float* dW;                 /* out [2F, H] fp32 */
+  float* workspace;          /* coda_workspace_size(CODA_WS_MLP_FP8_BWD, M, H, F) bytes */
+} coda_mlp_fp8_bwd_io;
+CODA_API int coda_mlp_fp8_backward(const coda_mlp_fp8_bwd_io* io, void* stream);
+
+/* e4m3 quantisation of a bf16 tensor X (ROW_MAJOR [M, N], N a multiple of 16) into Q
+ * (e4m3 ROW_MAJOR [M, N]): Q = e4m3(X * (1 / scale)), round to nearest even, saturating
+ * to +-448, 1 / scale taken in fp32; amax (optional) receives the atomic max of |X| (the
+ * caller zeroes it).  A bandwidth-bound pass: 3 bytes moved per element. */
+CODA_API int coda_quantize_e4m3(const coda_tensor* X, float scale, const coda_tensor* Q, float* amax, void* stream);
 
 /* ------------------------------------------------------------ LM head + cross-entropy
  * Final RMSNorm, LM head and mean cross-entropy, with the logits never stored
@@ -410,7 +460,13 @@ CODA_API int coda_lm_head_xent_backward(const coda_lm_head_xent_bwd_io* io, void
 
 /* Bytes of fp32 scratch a chain needs (caller allocates).  The third size is F for the
  * block chains and V for the cross-entropy chains. */
-enum coda_workspace_kind { CODA_WS_BLOCK_FWD = 0, CODA_WS_BLOCK_BWD = 1, CODA_WS_XENT_FWD = 2, CODA_WS_XENT_BWD = 3 };
+enum coda_workspace_kind {
+  CODA_WS_BLOCK_FWD = 0,
+  CODA_WS_BLOCK_BWD = 1,
+  CODA_WS_XENT_FWD = 2,
+  CODA_WS_XENT_BWD = 3,
+  CODA_WS_MLP_FP8_BWD = 4
+};
 CODA_API size_t coda_workspace_size(int32_t which, int64_t M, int64_t H, int64_t F);
 
 /* ------------------------------------------------------------------ device status
