@@ -736,7 +736,40 @@ def other_workloads(torch, C, S, args, stream):
                          "roofline_frac": roof / ms, "tokens_per_s": M / (ms * 1e-3), "launches": 3,
                          "peak_tflops": peak8, "peak_note": note,
                          "frac_of_2x_bf16": flop / (ms * 1e-3) / 1e12 / (2 * pk["bf16_sus"])}
-    del h8, X8, W8, Wd8, aq, Y8, P8
+    # N4: its backward on e4m3 operands, after a training-mode forward that saves Z = [G | U]
+    Z8 = torch.empty((M, 2 * F8), dtype=BF, device="cuda")
+    fwd8 = lambda: C.coda_mlp_fp8(h8, X8, W8, Wd8, fi["s_x"], fi["s_w"], fi["s_wd"], s_a, EPS, r8, aq, am, Y8, P8,
+                                  Z=Z8, stream=stream)
+    ms_fz = _time(torch, fwd8, stream, steps)
+    dY8 = torch.randn((M, H8), generator=torch.Generator(device="cuda").manual_seed(9), device="cuda").to(BF)
+    s_dy = float(dY8.abs().max()) / 448.0
+    U8 = torch.uint8
+    dYq8 = torch.empty((M, H8), dtype=U8, device="cuda")
+    eq8 = torch.empty((M, 2 * F8), dtype=U8, device="cuda")
+    am_dy, am_e = torch.empty((1,), device="cuda"), torch.empty((1,), device="cuda")
+    c8 = torch.empty((M,), device="cuda")
+    dh8 = torch.empty((M, H8), dtype=BF, device="cuda")
+    dWd8, dW8 = torch.empty((H8, F8), device="cuda"), torch.empty((2 * F8, H8), device="cuda")
+    ws8 = torch.empty((C.coda_workspace_size(C.WS_MLP_FP8_BWD, M, H8, F8) // 4,), device="cuda")
+    s_e = [1.0]
+    bwd8 = lambda: C.coda_mlp_fp8_backward(h8, X8, W8, Wd8, Z8, aq, r8, dY8, fi["s_x"], fi["s_w"], fi["s_wd"], s_a,
+                                           s_dy, s_e[0], dYq8, am_dy, eq8, am_e, c8, dh8, dWd8, dW8, ws8,
+                                           stream=stream)
+    bwd8()
+    torch.cuda.synchronize()
+    s_e[0] = float(am_e.item()) / 448.0               # delayed scaling from the previous pass
+    ms = _time(torch, bwd8, stream, steps)
+    flop = 12 * M * H8 * F8                            # dA, dW_d: 2MHF each; dh, dW: 4MHF each
+    byt = 3 * M * H8 + (M * H8 + H8 * F8 + 4 * M * F8 + 2 * M * F8) + (M * H8 + M * F8 + 4 * H8 * F8) + \
+        (2 * M * F8 + 2 * F8 * H8 + 6 * M * H8) + (2 * M * F8 + M * H8 + 8 * F8 * H8)
+    roof = max(flop / (peak8 * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
+    out["mlp_fp8_backward_N4"] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "roofline_ms": roof,
+                                  "roofline_frac": roof / ms, "tokens_per_s": M / (ms * 1e-3), "launches": 6,
+                                  "train_forward_ms": ms_fz, "peak_tflops": peak8,
+                                  "note": "quantise dY, dA GEMM + SwiGLU-bwd (e4m3 e), row reduce, dW_d, "
+                                          "dh GEMM + RMSNorm-bwd combine, dW; e4m3 operands, MN-major where "
+                                          "transposed"}
+    del h8, X8, W8, Wd8, aq, Y8, P8, Z8, dY8, dYq8, eq8, dh8, dWd8, dW8, ws8
     torch.cuda.empty_cache()
     # N3: the block forward at the 7B and 70B LLaMA-3 hidden sizes, beside torch eager
     for name, Hs, Fs in (("block_forward_7B_H4096_F14336", 4096, 14336), ("block_forward_70B_H8192_F28672", 8192,
