@@ -38,7 +38,7 @@ EXPORTED = [
     "coda_workspace_size", "coda_get_device_status", "coda_set_watchdog_ms", "coda_inject_dropped_stage",
     "coda_device_sm_count", "coda_status_string", "coda_version", "coda_block_forward_noalloc", "coda_rms_gain",
     "coda_xent_combine", "coda_lm_head_xent_forward", "coda_lm_head_xent_backward", "coda_rope_backward",
-    "coda_qkv_rope_backward", "coda_mlp_fp8_backward", "coda_quantize_e4m3",
+    "coda_qkv_rope_backward", "coda_mlp_fp8_backward", "coda_quantize_e4m3", "coda_set_launch_overlap",
 ]
 NOALLOC_MAX_PARTIALS = 1 << 20
 
@@ -167,6 +167,7 @@ def lib():
         "coda_quantize_e4m3": [P(CodaTensor), c_float, P(CodaTensor), c_void_p, c_void_p],
         "coda_get_device_status": [c_void_p, P(c_int32)],
         "coda_set_watchdog_ms": [c_uint32],
+        "coda_set_launch_overlap": [c_int32],
         "coda_inject_dropped_stage": [c_int32],
         "coda_device_sm_count": [P(c_int32)],
         "coda_rms_gain": [P(CodaTensor), c_void_p, c_float, c_void_p, P(CodaTensor), c_void_p],
@@ -430,6 +431,10 @@ def coda_get_device_status(stream=None):
     site = c_int32(0)
     st = lib().coda_get_device_status(_stream(stream), ctypes.byref(site))
     return int(st), int(site.value)
+
+
+def coda_set_launch_overlap(enable):
+    _check(lib().coda_set_launch_overlap(1 if enable else 0), "coda_set_launch_overlap")
 
 
 def coda_set_watchdog_ms(ms):

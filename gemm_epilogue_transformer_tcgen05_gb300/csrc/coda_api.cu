@@ -196,6 +196,11 @@ int match_program(const coda_epilogue_program* prog, uint32_t* present) {
 }  // namespace
 
 namespace coda {
+int g_launch_overlap = [] {
+  const char* e = std::getenv("CODA_LAUNCH_OVERLAP");
+  return (e && e[0] == '0') ? 0 : 1;
+}();
+
 const VariantEntry* find_variant(const VariantKey& k) {
   const VariantEntry* tables[4] = {g_variants_fwd, g_variants_bwd, g_variants_lowp, g_variants_fp8};
   const int counts[4] = {g_num_variants_fwd, g_num_variants_bwd, g_num_variants_lowp, g_num_variants_fp8};
@@ -228,6 +233,12 @@ const char* coda_status_string(int s) {
     case CODA_ERR_NO_DEVICE: return "no sm_103 device current (or driver entry point missing)";
     default: return "unknown status";
   }
+}
+
+int coda_set_launch_overlap(int32_t enable) {
+  if (enable != 0 && enable != 1) return CODA_ERR_SHAPE;
+  coda::g_launch_overlap = enable;
+  return CODA_OK;
 }
 
 int coda_set_watchdog_ms(uint32_t ms) {
@@ -508,6 +519,7 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
   p.status = d->status;
   p.timeout_ns = (unsigned long long)g_watchdog_ms * 1000000ull;
   L.sms = d->sms;
+  L.overlap = g_launch_overlap;
   const cudaError_t e = var->fn(L, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
 }

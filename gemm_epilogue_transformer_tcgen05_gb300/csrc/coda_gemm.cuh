@@ -343,6 +343,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #define SIDE_BAR(w, s) (sm_bar + 8u * (2 * C::STAGES + 4 + C::NSS * (w) + (s)))
 #define DONE_BAR (sm_bar + 8u * (2 * C::STAGES + 4 + C::NSS * NUM_EPI_WARPS))
 
+  ptx::griddep_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = C::CG == 2 ? ptx::cluster_ctarank() : 0u;   // position in the CTA pair
@@ -379,6 +380,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  ptx::griddep_wait();   // everything above touched only this CTA's shared memory and TMEM
 
   const Watch watch{abort_flag, p.status, p.timeout_ns};
   const int total_tiles = p.m_tiles * p.n_tiles * p.k_splits;   // work items
@@ -887,6 +889,7 @@ struct GemmLaunch {
   CUtensorMap tmA, tmB, tmOut, tmSide0, tmSide1, tmAux;
   GemmParams p;
   int sms;
+  int overlap;   // launch with a programmatic dependency on the previous kernel of the stream
 };
 
 using GemmLaunchFn = cudaError_t (*)(const GemmLaunch&, cudaStream_t);
@@ -935,26 +938,28 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   const int64_t tiles = (int64_t)L.p.m_tiles * L.p.n_tiles * L.p.k_splits;
   const int groups = (int)(tiles < resident_groups<C>(L.sms) ? tiles : resident_groups<C>(L.sms));
   if (groups <= 0) return cudaSuccess;
-  if constexpr (C::CG == 1) {
-    gemm_epilogue_kernel<C><<<groups, NUM_THREADS, C::SMEM_BYTES, s>>>(L.tmA, L.tmB, L.tmOut, L.tmSide0, L.tmSide1,
-                                                                        L.tmAux, L.p);
-    return cudaGetLastError();
-  } else {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2 * groups, 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_epilogue_kernel<C>, L.tmA, L.tmB, L.tmOut, L.tmSide0, L.tmSide1, L.tmAux,
-                              L.p);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if constexpr (C::CG == 2) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 2;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
   }
+  if (L.overlap) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.gridDim = dim3(C::CG * groups, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, gemm_epilogue_kernel<C>, L.tmA, L.tmB, L.tmOut, L.tmSide0, L.tmSide1, L.tmAux, L.p);
 }
 
 }  // namespace coda

@@ -32,6 +32,10 @@ extern const int g_num_variants_fp8;
 
 const VariantEntry* find_variant(const VariantKey& k);
 
+// 1 (default): kernels are launched with a programmatic dependency on the previous kernel of the
+// stream (their launch overlaps its tail); 0: plain stream serialisation.
+extern int g_launch_overlap;
+
 // Small bandwidth-bound kernels (coda_small.cu).  Arguments are validated by the caller.
 cudaError_t launch_partial_reduce(const float* partials, int64_t ld, int nparts, int64_t M, float inv_d, float eps,
                                   int mode, const float* rowscale, float* out, cudaStream_t s);

@@ -263,6 +263,17 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Programmatic dependent launch.  launch_dependents: once every CTA of this grid has executed
+// it (or exited), the next kernel in the stream may be scheduled, so its prologue overlaps this
+// grid's tail.  wait: blocks until the previous grid in the stream has completed and its memory
+// is visible; a no-op when this launch carries no programmatic dependency.  Every kernel of the
+// library signals at entry and waits before its first global memory access, so stream order is
+// kept exactly.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Packed e4m3x2 -> the two fp32 values (exact: every e4m3 value is an f16 value); the low
 // byte gives `lo`.
 __device__ __forceinline__ void e4m3x2_to_f32(uint16_t v, float& lo, float& hi) {

@@ -14,12 +14,31 @@
 
 namespace coda {
 
+// Launch with a programmatic dependency on the previous kernel of the stream (when enabled):
+// every kernel here signals at entry and waits (griddepcontrol.wait) before its first global
+// memory access, so only the launch latency overlaps the previous kernel's tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), unsigned grid, unsigned block, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = g_launch_overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------- partial reduce
 // One thread per row; parts summed in index order (deterministic).  Reads are coalesced
 // because the partials are stored [nparts, M].
 __global__ void partial_reduce_kernel(const float* __restrict__ P, int64_t ld, int nparts, int64_t M, float inv_d,
                                       float eps, int mode, const float* __restrict__ rowscale,
                                       float* __restrict__ out) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= M) return;
   // four independent running sums keep four loads in flight; combined in a fixed order
@@ -41,7 +60,7 @@ cudaError_t launch_partial_reduce(const float* partials, int64_t ld, int nparts,
                                   int mode, const float* rowscale, float* out, cudaStream_t s) {
   const int threads = 256;
   const int64_t blocks = (M + threads - 1) / threads;
-  partial_reduce_kernel<<<(unsigned)blocks, threads, 0, s>>>(partials, ld, nparts, M, inv_d, eps, mode, rowscale,
+  launch_k(partial_reduce_kernel, (unsigned)blocks, threads, s, partials, ld, nparts, M, inv_d, eps, mode, rowscale,
                                                               out);
   return cudaGetLastError();
 }
@@ -50,6 +69,8 @@ cudaError_t launch_partial_reduce(const float* partials, int64_t ld, int nparts,
 // One warp per row, 16-byte loads (8 bf16 per lane), four loads in flight per lane.
 __global__ void row_rms_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, int64_t d, int64_t ld, float eps,
                                float* __restrict__ r) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= M) return;
@@ -91,7 +112,7 @@ cudaError_t launch_row_rms(const void* X, int64_t M, int64_t d, int64_t ld, floa
   (void)sms;
   const int rows_per_block = 8;
   const int64_t blocks = (M + rows_per_block - 1) / rows_per_block;
-  row_rms_kernel<<<(unsigned)blocks, 32 * rows_per_block, 0, s>>>(static_cast<const __nv_bfloat16*>(X), M, d, ld,
+  launch_k(row_rms_kernel, (unsigned)blocks, 32 * rows_per_block, s, static_cast<const __nv_bfloat16*>(X), M, d, ld,
                                                                    eps, r);
   return cudaGetLastError();
 }
@@ -101,6 +122,8 @@ cudaError_t launch_row_rms(const void* X, int64_t M, int64_t d, int64_t ld, floa
 __global__ void rms_gain_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, int64_t d, int64_t ld,
                                 const float* __restrict__ g, float eps, float* __restrict__ r,
                                 __nv_bfloat16* __restrict__ U, int64_t ldu) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= M) return;
@@ -133,7 +156,7 @@ cudaError_t launch_rms_gain(const void* X, int64_t M, int64_t d, int64_t ld, con
                             void* U, int64_t ldu, cudaStream_t s) {
   const int rows_per_block = 8;
   const int64_t blocks = (M + rows_per_block - 1) / rows_per_block;
-  rms_gain_kernel<<<(unsigned)blocks, 32 * rows_per_block, 0, s>>>(static_cast<const __nv_bfloat16*>(X), M, d, ld,
+  launch_k(rms_gain_kernel, (unsigned)blocks, 32 * rows_per_block, s, static_cast<const __nv_bfloat16*>(X), M, d, ld,
                                                                     g, eps, r, static_cast<__nv_bfloat16*>(U), ldu);
   return cudaGetLastError();
 }
@@ -147,6 +170,8 @@ __global__ void rope_bwd_kernel(const __nv_bfloat16* __restrict__ dout, const __
                                 const float* __restrict__ cs, const float* __restrict__ sn, int seq_len, int head_dim,
                                 int rope_ncols, float inv_h, __nv_bfloat16* __restrict__ e, int64_t lde,
                                 float* __restrict__ c) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= M) return;
@@ -188,7 +213,7 @@ cudaError_t launch_rope_bwd(const void* dout, const void* out, int64_t M, int64_
                             void* e, int64_t lde, float* c, cudaStream_t s) {
   const int rows_per_block = 8;
   const int64_t blocks = (M + rows_per_block - 1) / rows_per_block;
-  rope_bwd_kernel<<<(unsigned)blocks, 32 * rows_per_block, 0, s>>>(
+  launch_k(rope_bwd_kernel, (unsigned)blocks, 32 * rows_per_block, s, 
       static_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(out), M, N, ld, r, cs, sn, seq_len,
       head_dim, rope_ncols, 1.0f / (float)H, static_cast<__nv_bfloat16*>(e), lde, c);
   return cudaGetLastError();
@@ -201,6 +226,8 @@ cudaError_t launch_rope_bwd(const void* dout, const void* out, int64_t M, int64_
 __global__ void xent_reduce_kernel(const float* __restrict__ Pm, const float* __restrict__ Ps, int64_t ld, int nparts,
                                    int64_t M, const float* __restrict__ T, const int* __restrict__ targets, int64_t V,
                                    float* __restrict__ lse, float* __restrict__ loss) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= M) return;
   float m = -INFINITY;
@@ -215,6 +242,8 @@ __global__ void xent_reduce_kernel(const float* __restrict__ Pm, const float* __
 
 // Mean of n floats by one block: strided partial sums in fixed order, then a fixed tree.
 __global__ void mean_kernel(const float* __restrict__ x, int64_t n, float* __restrict__ out) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   __shared__ float red[1024];
   float s = 0.f;
   for (int64_t i = threadIdx.x; i < n; i += blockDim.x) s += x[i];
@@ -230,9 +259,9 @@ __global__ void mean_kernel(const float* __restrict__ x, int64_t n, float* __res
 cudaError_t launch_xent_reduce(const float* Pm, const float* Ps, int64_t ld, int nparts, int64_t M, const float* T,
                                const int* targets, int64_t V, float* lse, float* loss, float* mean, cudaStream_t s) {
   const int threads = 256;
-  xent_reduce_kernel<<<(unsigned)((M + threads - 1) / threads), threads, 0, s>>>(Pm, Ps, ld, nparts, M, T, targets, V,
+  launch_k(xent_reduce_kernel, (unsigned)((M + threads - 1) / threads), threads, s, Pm, Ps, ld, nparts, M, T, targets, V,
                                                                                  lse, loss);
-  if (mean) mean_kernel<<<1, 1024, 0, s>>>(loss, M, mean);
+  if (mean) launch_k(mean_kernel, 1, 1024, s, loss, M, mean);
   return cudaGetLastError();
 }
 
@@ -242,6 +271,8 @@ cudaError_t launch_xent_reduce(const float* Pm, const float* Ps, int64_t ld, int
 // (deterministic).
 __global__ void col_reduce_kernel(const float* __restrict__ parts, int64_t nblocks, int64_t N, int64_t ld,
                                   float* __restrict__ out) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   __shared__ float red[32][33];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int64_t j = (int64_t)blockIdx.x * 32 + tx;
@@ -267,7 +298,7 @@ __global__ void col_reduce_kernel(const float* __restrict__ parts, int64_t nbloc
 cudaError_t launch_col_reduce(const float* parts, int64_t nblocks, int64_t N, int64_t ld, float* out,
                               cudaStream_t s) {
   const int64_t blocks = (N + 31) / 32;
-  col_reduce_kernel<<<(unsigned)blocks, 1024, 0, s>>>(parts, nblocks, N, ld, out);
+  launch_k(col_reduce_kernel, (unsigned)blocks, 1024, s, parts, nblocks, N, ld, out);
   return cudaGetLastError();
 }
 
@@ -275,6 +306,8 @@ cudaError_t launch_col_reduce(const float* parts, int64_t nblocks, int64_t N, in
 // W'[n, k] = bf16(W[n, k] * g[k]); 8 elements (16 bytes) per thread per step, grid-stride.
 __global__ void fold_gain_kernel(const __nv_bfloat16* __restrict__ W, int64_t N, int64_t K, int64_t ld_in,
                                  const float* __restrict__ g, __nv_bfloat16* __restrict__ Wo, int64_t ld_out) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   const int64_t kv = K >> 3;
   const int64_t total = N * kv;
   for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
@@ -299,6 +332,8 @@ __global__ void fold_gain_kernel(const __nv_bfloat16* __restrict__ W, int64_t N,
 // fp32 weights: 4 elements (16 bytes) per thread per step.
 __global__ void fold_gain_f32_kernel(const float* __restrict__ W, int64_t N, int64_t K, int64_t ld_in,
                                      const float* __restrict__ g, float* __restrict__ Wo, int64_t ld_out) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   const int64_t kv = K >> 2;
   const int64_t total = N * kv;
   for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
@@ -317,10 +352,10 @@ cudaError_t launch_fold_gain(const void* W, int64_t N, int64_t K, int64_t ld_in,
   const int64_t blocks = need < cap ? need : cap;
   if (blocks <= 0) return cudaSuccess;
   if (f32)
-    fold_gain_f32_kernel<<<(unsigned)blocks, threads, 0, s>>>(static_cast<const float*>(W), N, K, ld_in, g,
+    launch_k(fold_gain_f32_kernel, (unsigned)blocks, threads, s, static_cast<const float*>(W), N, K, ld_in, g,
                                                                static_cast<float*>(W_out), ld_out);
   else
-    fold_gain_kernel<<<(unsigned)blocks, threads, 0, s>>>(static_cast<const __nv_bfloat16*>(W), N, K, ld_in, g,
+    launch_k(fold_gain_kernel, (unsigned)blocks, threads, s, static_cast<const __nv_bfloat16*>(W), N, K, ld_in, g,
                                                            static_cast<__nv_bfloat16*>(W_out), ld_out);
   return cudaGetLastError();
 }
@@ -328,6 +363,8 @@ cudaError_t launch_fold_gain(const void* W, int64_t N, int64_t K, int64_t ld_in,
 // ---------------------------------------------------------------- RoPE table
 __global__ void rope_table_kernel(int seq_len, int half, double base, int head_dim, float* __restrict__ c,
                                   float* __restrict__ s) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (int64_t)seq_len * half) return;
   const int pos = (int)(idx / half), p = (int)(idx % half);
@@ -344,6 +381,8 @@ __global__ void rope_table_kernel(int seq_len, int half, double base, int head_d
 __global__ void quantize_e4m3_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, int64_t N, int64_t ldx,
                                      float inv_scale, uint8_t* __restrict__ Q, int64_t ldq,
                                      unsigned int* __restrict__ amax) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   const int64_t nv = N >> 4;
   const int64_t total = M * nv;
   float m = 0.f;
@@ -377,7 +416,7 @@ cudaError_t launch_quantize_e4m3(const void* X, int64_t M, int64_t N, int64_t ld
   int64_t blocks = (total + threads - 1) / threads;
   if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
   if (blocks < 1) blocks = 1;
-  quantize_e4m3_kernel<<<(unsigned)blocks, threads, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(X), M, N, ldx,
+  launch_k(quantize_e4m3_kernel, (unsigned)blocks, threads, s, reinterpret_cast<const __nv_bfloat16*>(X), M, N, ldx,
                                                             inv_scale, reinterpret_cast<uint8_t*>(Q), ldq,
                                                             reinterpret_cast<unsigned int*>(amax));
   return cudaGetLastError();
@@ -388,7 +427,7 @@ cudaError_t launch_rope_table(int seq_len, int head_dim, double base, float* cos
   const int half = head_dim / 2;
   const int64_t n = (int64_t)seq_len * half;
   const int threads = 256;
-  rope_table_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(seq_len, half, base, head_dim,
+  launch_k(rope_table_kernel, (unsigned)((n + threads - 1) / threads), threads, s, seq_len, half, base, head_dim,
                                                                                  cos_out, sin_out);
   return cudaGetLastError();
 }

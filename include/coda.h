@@ -480,6 +480,13 @@ CODA_API int coda_get_device_status(void* stream, int32_t* site);
 /* Per-wait time limit of every kernel wait (default 2000 ms, or CODA_WATCHDOG_MS). */
 CODA_API int coda_set_watchdog_ms(uint32_t ms);
 
+/* Launch overlap (default on; CODA_LAUNCH_OVERLAP=0 in the environment turns it off): every
+ * kernel of the library is launched with a programmatic dependency on the previous kernel of
+ * the stream, signals at entry and waits for that kernel's completion before its first global
+ * memory access, so stream order is kept while the launch itself overlaps the previous kernel's
+ * tail.  enable = 0 gives plain stream serialisation.  Other values: CODA_ERR_SHAPE. */
+CODA_API int coda_set_launch_overlap(int32_t enable);
+
 /* Test hook for the watchdog: when set, the next coda_gemm_epilogue call makes its
  * producer drop one k-block, so the MMA wait runs out of time and the kernel returns
  * through the abort path.  Cleared after one call. */
