@@ -282,9 +282,11 @@ int coda_get_device_status(void* stream, int32_t* site) {
   return CODA_OK;
 }
 
-int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_epilogue_program* prog,
-                       const coda_side_inputs* side, const coda_tensor* out, const coda_aux_outputs* aux,
-                       void* stream) {
+// ab_ready: the caller guarantees that the kernel issued just before this one on the stream
+// writes neither A nor W (the chains know this; the public entry point does not).
+static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const coda_epilogue_program* prog,
+                              const coda_side_inputs* side, const coda_tensor* out, const coda_aux_outputs* aux,
+                              void* stream, bool ab_ready) {
   int st;
   if ((st = check_tensor(A, true)) != CODA_OK) return st;
   if ((st = check_tensor(W, true)) != CODA_OK) return st;
@@ -493,6 +495,7 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
             (has(CODA_OP_COL_SCALE) || (epi == EPI_RMSBWD && sd.col_scale) ? F_COLSCALE : 0) |
             (has(CODA_OP_ROW_SCALE) ? F_ROWSCALE : 0) | (has(CODA_OP_COL_DOT_PARTIAL) ? F_COLPART : 0) |
             (epi == EPI_RMSBWD && !sd.aux_in2 ? F_NO_SIDE1 : 0);
+  if (ab_ready && g_launch_overlap) p.flags |= F_AB_READY;
   if (g_inject_once) {
     p.flags |= F_INJECT_SKIP;
     g_inject_once = 0;
@@ -522,6 +525,12 @@ int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_ep
   L.overlap = g_launch_overlap;
   const cudaError_t e = var->fn(L, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
+}
+
+int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, const coda_epilogue_program* prog,
+                       const coda_side_inputs* side, const coda_tensor* out, const coda_aux_outputs* aux,
+                       void* stream) {
+  return gemm_epilogue_impl(A, W, prog, side, out, aux, stream, false);
 }
 
 int coda_rms_partial_reduce(const float* partials, int64_t ld, int32_t nparts, int64_t M, int64_t d, float eps,
@@ -715,7 +724,7 @@ int coda_block_forward(const coda_block_fwd* io, void* stream) {
     sd.row_scale = io->r;
     coda_aux_outputs ax{};
     ax.store_aux = io->Z ? &Z : nullptr;
-    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, &ax, stream)) != CODA_OK) return st;
+    if ((st = gemm_epilogue_impl(&A, &W, &pg, &sd, &out, &ax, stream, true)) != CODA_OK) return st;
   }
   // G3: Y = a W_d^T + h  [+ partial sums of squares of Y for the next layer]
   {
@@ -765,7 +774,7 @@ int coda_block_backward(const coda_block_bwd* io, void* stream) {
     coda_tensor A = mk(io->dY, CODA_BF16, H, M, H, CODA_COL_MAJOR), W = mk(io->a, CODA_BF16, F, M, F, CODA_COL_MAJOR);
     coda_tensor out = mk(io->dW_d, CODA_F32, H, F, F);
     coda_epilogue_program pg = prog_of({});
-    if ((st = coda_gemm_epilogue(&A, &W, &pg, nullptr, &out, nullptr, stream)) != CODA_OK) return st;
+    if ((st = gemm_epilogue_impl(&A, &W, &pg, nullptr, &out, nullptr, stream, true)) != CODA_OK) return st;
   }
   // b3: c = r * sum(S) / H
   if ((st = coda_rms_partial_reduce(S, M, (int32_t)nS, M, H, 0.f, CODA_REDUCE_SCALE_SUM, io->r, io->c, stream)) !=
@@ -786,7 +795,7 @@ int coda_block_backward(const coda_block_bwd* io, void* stream) {
     coda_aux_outputs ax{};
     ax.col_partials = Dg;
     ax.col_partials_ld = H;
-    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, &ax, stream)) != CODA_OK) return st;
+    if ((st = gemm_epilogue_impl(&A, &W, &pg, &sd, &out, &ax, stream, true)) != CODA_OK) return st;
   }
   // b5: dg = column sums of the partials
   if ((st = coda_col_reduce(Dg, nDg, H, H, io->dg, stream)) != CODA_OK) return st;
@@ -798,7 +807,7 @@ int coda_block_backward(const coda_block_bwd* io, void* stream) {
     coda_epilogue_program pg = prog_of({CODA_OP_COL_SCALE});
     coda_side_inputs sd{};
     sd.col_scale = io->g;
-    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, nullptr, stream)) != CODA_OK) return st;
+    if ((st = gemm_epilogue_impl(&A, &W, &pg, &sd, &out, nullptr, stream, true)) != CODA_OK) return st;
   }
   // b7: dO = dh W_o
   {
@@ -806,14 +815,14 @@ int coda_block_backward(const coda_block_bwd* io, void* stream) {
     coda_tensor W = mk(io->W_o, CODA_BF16, H, H, H, CODA_COL_MAJOR);  // logical W_o^T
     coda_tensor out = mk(io->dO, CODA_BF16, M, H, H);
     coda_epilogue_program pg = prog_of({});
-    if ((st = coda_gemm_epilogue(&A, &W, &pg, nullptr, &out, nullptr, stream)) != CODA_OK) return st;
+    if ((st = gemm_epilogue_impl(&A, &W, &pg, nullptr, &out, nullptr, stream, true)) != CODA_OK) return st;
   }
   // b8: dW_o = dh^T O
   {
     coda_tensor A = mk(io->dh, CODA_BF16, H, M, H, CODA_COL_MAJOR), W = mk(io->O, CODA_BF16, H, M, H, CODA_COL_MAJOR);
     coda_tensor out = mk(io->dW_o, CODA_F32, H, H, H);
     coda_epilogue_program pg = prog_of({});
-    if ((st = coda_gemm_epilogue(&A, &W, &pg, nullptr, &out, nullptr, stream)) != CODA_OK) return st;
+    if ((st = gemm_epilogue_impl(&A, &W, &pg, nullptr, &out, nullptr, stream, true)) != CODA_OK) return st;
   }
   return CODA_OK;
 }
@@ -892,7 +901,7 @@ int coda_lm_head_xent_backward(const coda_lm_head_xent_bwd_io* io, void* stream)
     coda_aux_outputs ax{};
     ax.col_partials = Dg;
     ax.col_partials_ld = H;
-    if ((st = coda_gemm_epilogue(&e, &W, &pg, &sd, &out, &ax, stream)) != CODA_OK) return st;
+    if ((st = gemm_epilogue_impl(&e, &W, &pg, &sd, &out, &ax, stream, true)) != CODA_OK) return st;
   }
   if ((st = coda_col_reduce(Dg, (M + 31) / 32, H, H, io->dg, stream)) != CODA_OK) return st;
   // dW_v = e^T u
@@ -900,7 +909,7 @@ int coda_lm_head_xent_backward(const coda_lm_head_xent_bwd_io* io, void* stream)
     coda_tensor A = mk(io->e, CODA_BF16, V, M, V, CODA_COL_MAJOR), W = mk(io->u, CODA_BF16, H, M, H, CODA_COL_MAJOR);
     coda_tensor out = mk(io->dW_v, CODA_F32, V, H, H);
     coda_epilogue_program pg = prog_of({});
-    if ((st = coda_gemm_epilogue(&A, &W, &pg, nullptr, &out, nullptr, stream)) != CODA_OK) return st;
+    if ((st = gemm_epilogue_impl(&A, &W, &pg, nullptr, &out, nullptr, stream, true)) != CODA_OK) return st;
   }
   return CODA_OK;
 }
@@ -964,7 +973,7 @@ int coda_qkv_rope_backward(const coda_qkv_rope_bwd_io* io, void* stream) {
     coda_epilogue_program pg = prog_of({CODA_OP_COL_SCALE});
     coda_side_inputs sd{};
     sd.col_scale = io->g;
-    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &dW, nullptr, stream)) != CODA_OK) return st;
+    if ((st = gemm_epilogue_impl(&A, &W, &pg, &sd, &dW, nullptr, stream, true)) != CODA_OK) return st;
   }
   return CODA_OK;
 }
@@ -987,7 +996,7 @@ int coda_qkv_rope(const coda_qkv_rope_io* io, void* stream) {
   sd.rope_seq_len = io->seq_len;
   sd.rope_head_dim = io->head_dim;
   sd.rope_ncols = io->rope_ncols;
-  return coda_gemm_epilogue(&h, &W, &pg, &sd, &out, nullptr, stream);
+  return gemm_epilogue_impl(&h, &W, &pg, &sd, &out, nullptr, stream, true);
 }
 
 int coda_mlp_fp8(const coda_mlp_fp8_io* io, void* stream) {
@@ -1000,9 +1009,9 @@ int coda_mlp_fp8(const coda_mlp_fp8_io* io, void* stream) {
   if (M == 0) return CODA_OK;
   int st;
   coda_tensor h = mk(io->h, CODA_BF16, M, H, H);
-  if ((st = coda_row_rms(&h, io->eps, io->r, stream)) != CODA_OK) return st;
   if (cudaMemsetAsync(io->amax, 0, sizeof(float), static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return CODA_ERR_LAUNCH;
+  if ((st = coda_row_rms(&h, io->eps, io->r, stream)) != CODA_OK) return st;
   {
     coda_tensor A = mk(io->X_q, CODA_E4M3, M, H, H), W = mk(io->W_q, CODA_E4M3, 2 * F, H, H);
     coda_tensor out = mk(io->a_q, CODA_E4M3, M, F, F);
@@ -1017,7 +1026,7 @@ int coda_mlp_fp8(const coda_mlp_fp8_io* io, void* stream) {
     coda_aux_outputs ax{};
     ax.amax = io->amax;
     if (io->Z) ax.store_aux = &Z;
-    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, &ax, stream)) != CODA_OK) return st;
+    if ((st = gemm_epilogue_impl(&A, &W, &pg, &sd, &out, &ax, stream, true)) != CODA_OK) return st;
   }
   {
     coda_tensor A = mk(io->a_q, CODA_E4M3, M, F, F), W = mk(io->W_dq, CODA_E4M3, H, F, F);
@@ -1090,7 +1099,7 @@ int coda_mlp_fp8_backward(const coda_mlp_fp8_bwd_io* io, void* stream) {
     coda_epilogue_program pg = prog_of({CODA_OP_TENSOR_SCALE});
     coda_side_inputs sd{};
     sd.tensor_scale = io->s_dy * io->s_a;
-    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, nullptr, stream)) != CODA_OK) return st;
+    if ((st = gemm_epilogue_impl(&A, &W, &pg, &sd, &out, nullptr, stream, true)) != CODA_OK) return st;
   }
   {
     // dh = s_e s_w (e_q W_q) - c h + dY
@@ -1103,7 +1112,7 @@ int coda_mlp_fp8_backward(const coda_mlp_fp8_bwd_io* io, void* stream) {
     sd.row_coef = io->c;
     sd.aux_in = &h;
     sd.aux_in2 = &dY;
-    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, nullptr, stream)) != CODA_OK) return st;
+    if ((st = gemm_epilogue_impl(&A, &W, &pg, &sd, &out, nullptr, stream, true)) != CODA_OK) return st;
   }
   {
     // dW = s_e s_x (e_q^T X_q)
@@ -1113,7 +1122,7 @@ int coda_mlp_fp8_backward(const coda_mlp_fp8_bwd_io* io, void* stream) {
     coda_epilogue_program pg = prog_of({CODA_OP_TENSOR_SCALE});
     coda_side_inputs sd{};
     sd.tensor_scale = io->s_e * io->s_x;
-    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, nullptr, stream)) != CODA_OK) return st;
+    if ((st = gemm_epilogue_impl(&A, &W, &pg, &sd, &out, nullptr, stream, true)) != CODA_OK) return st;
   }
   return CODA_OK;
 }

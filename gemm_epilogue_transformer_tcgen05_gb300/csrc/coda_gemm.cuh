@@ -74,6 +74,7 @@ enum : int {
   F_ROWSCALE = 16,  // multiply by row_scale (EPI_SWIGLU / EPI_ROPE / EPI_ROWSCALE / EPI_SWIGLU_BWD)
   F_NO_SIDE1 = 32,  // EPI_RMSBWD without the dY side input
   F_COLPART = 64,   // write column partials (EPI_RMSBWD)
+  F_AB_READY = 128, // A and B are not written by the previous kernel of the stream
   F_INJECT_SKIP = 1 << 30,  // test hook: the producer drops its first k-block
 };
 
@@ -343,7 +344,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #define SIDE_BAR(w, s) (sm_bar + 8u * (2 * C::STAGES + 4 + C::NSS * (w) + (s)))
 #define DONE_BAR (sm_bar + 8u * (2 * C::STAGES + 4 + C::NSS * NUM_EPI_WARPS))
 
-  ptx::griddep_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = C::CG == 2 ? ptx::cluster_ctarank() : 0u;   // position in the CTA pair
@@ -380,7 +380,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  ptx::griddep_wait();   // everything above touched only this CTA's shared memory and TMEM
+  // Stream order.  Everything above touched only this CTA's shared memory and TMEM.  The
+  // epilogue waits for the previous kernel before its first global access (side inputs, row
+  // and column vectors, stores).  With F_AB_READY the caller guarantees that the previous
+  // kernel writes neither A nor B (all earlier work is complete once that kernel has started,
+  // see griddep_launch_dependents), so the producer streams them at once and the MMA warp,
+  // which touches no global memory, does not wait.
+  if (!(p.flags & F_AB_READY) || warp >= 2) {
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
+  }
 
   const Watch watch{abort_flag, p.status, p.timeout_ns};
   const int total_tiles = p.m_tiles * p.n_tiles * p.k_splits;   // work items

@@ -264,11 +264,11 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
 }
 
 // Programmatic dependent launch.  launch_dependents: once every CTA of this grid has executed
-// it (or exited), the next kernel in the stream may be scheduled, so its prologue overlaps this
+// it (or exited), the next kernel in the stream may be scheduled, so its start overlaps this
 // grid's tail.  wait: blocks until the previous grid in the stream has completed and its memory
 // is visible; a no-op when this launch carries no programmatic dependency.  Every kernel of the
-// library signals at entry and waits before its first global memory access, so stream order is
-// kept exactly.
+// library signals only after its own wait returned, so when a kernel starts, all stream work
+// before its predecessor is complete.
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

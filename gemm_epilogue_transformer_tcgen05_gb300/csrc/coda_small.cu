@@ -15,8 +15,8 @@
 namespace coda {
 
 // Launch with a programmatic dependency on the previous kernel of the stream (when enabled):
-// every kernel here signals at entry and waits (griddepcontrol.wait) before its first global
-// memory access, so only the launch latency overlaps the previous kernel's tail.
+// every kernel here first waits (griddepcontrol.wait) for that kernel's completion, then lets
+// the next kernel launch; only the launch latency overlaps the previous kernel's tail.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kernel)(KArgs...), unsigned grid, unsigned block, cudaStream_t s, Args... args) {
   cudaLaunchConfig_t cfg = {};
@@ -37,8 +37,8 @@ cudaError_t launch_k(void (*kernel)(KArgs...), unsigned grid, unsigned block, cu
 __global__ void partial_reduce_kernel(const float* __restrict__ P, int64_t ld, int nparts, int64_t M, float inv_d,
                                       float eps, int mode, const float* __restrict__ rowscale,
                                       float* __restrict__ out) {
-  ptx::griddep_launch_dependents();
   ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= M) return;
   // four independent running sums keep four loads in flight; combined in a fixed order
@@ -69,8 +69,8 @@ cudaError_t launch_partial_reduce(const float* partials, int64_t ld, int nparts,
 // One warp per row, 16-byte loads (8 bf16 per lane), four loads in flight per lane.
 __global__ void row_rms_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, int64_t d, int64_t ld, float eps,
                                float* __restrict__ r) {
-  ptx::griddep_launch_dependents();
   ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= M) return;
@@ -122,8 +122,8 @@ cudaError_t launch_row_rms(const void* X, int64_t M, int64_t d, int64_t ld, floa
 __global__ void rms_gain_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, int64_t d, int64_t ld,
                                 const float* __restrict__ g, float eps, float* __restrict__ r,
                                 __nv_bfloat16* __restrict__ U, int64_t ldu) {
-  ptx::griddep_launch_dependents();
   ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= M) return;
@@ -170,8 +170,8 @@ __global__ void rope_bwd_kernel(const __nv_bfloat16* __restrict__ dout, const __
                                 const float* __restrict__ cs, const float* __restrict__ sn, int seq_len, int head_dim,
                                 int rope_ncols, float inv_h, __nv_bfloat16* __restrict__ e, int64_t lde,
                                 float* __restrict__ c) {
-  ptx::griddep_launch_dependents();
   ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= M) return;
@@ -226,8 +226,8 @@ cudaError_t launch_rope_bwd(const void* dout, const void* out, int64_t M, int64_
 __global__ void xent_reduce_kernel(const float* __restrict__ Pm, const float* __restrict__ Ps, int64_t ld, int nparts,
                                    int64_t M, const float* __restrict__ T, const int* __restrict__ targets, int64_t V,
                                    float* __restrict__ lse, float* __restrict__ loss) {
-  ptx::griddep_launch_dependents();
   ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= M) return;
   float m = -INFINITY;
@@ -242,8 +242,8 @@ __global__ void xent_reduce_kernel(const float* __restrict__ Pm, const float* __
 
 // Mean of n floats by one block: strided partial sums in fixed order, then a fixed tree.
 __global__ void mean_kernel(const float* __restrict__ x, int64_t n, float* __restrict__ out) {
-  ptx::griddep_launch_dependents();
   ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   __shared__ float red[1024];
   float s = 0.f;
   for (int64_t i = threadIdx.x; i < n; i += blockDim.x) s += x[i];
@@ -271,8 +271,8 @@ cudaError_t launch_xent_reduce(const float* Pm, const float* Ps, int64_t ld, int
 // (deterministic).
 __global__ void col_reduce_kernel(const float* __restrict__ parts, int64_t nblocks, int64_t N, int64_t ld,
                                   float* __restrict__ out) {
-  ptx::griddep_launch_dependents();
   ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   __shared__ float red[32][33];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int64_t j = (int64_t)blockIdx.x * 32 + tx;
@@ -306,8 +306,8 @@ cudaError_t launch_col_reduce(const float* parts, int64_t nblocks, int64_t N, in
 // W'[n, k] = bf16(W[n, k] * g[k]); 8 elements (16 bytes) per thread per step, grid-stride.
 __global__ void fold_gain_kernel(const __nv_bfloat16* __restrict__ W, int64_t N, int64_t K, int64_t ld_in,
                                  const float* __restrict__ g, __nv_bfloat16* __restrict__ Wo, int64_t ld_out) {
-  ptx::griddep_launch_dependents();
   ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int64_t kv = K >> 3;
   const int64_t total = N * kv;
   for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
@@ -332,8 +332,8 @@ __global__ void fold_gain_kernel(const __nv_bfloat16* __restrict__ W, int64_t N,
 // fp32 weights: 4 elements (16 bytes) per thread per step.
 __global__ void fold_gain_f32_kernel(const float* __restrict__ W, int64_t N, int64_t K, int64_t ld_in,
                                      const float* __restrict__ g, float* __restrict__ Wo, int64_t ld_out) {
-  ptx::griddep_launch_dependents();
   ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int64_t kv = K >> 2;
   const int64_t total = N * kv;
   for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
@@ -363,8 +363,8 @@ cudaError_t launch_fold_gain(const void* W, int64_t N, int64_t K, int64_t ld_in,
 // ---------------------------------------------------------------- RoPE table
 __global__ void rope_table_kernel(int seq_len, int half, double base, int head_dim, float* __restrict__ c,
                                   float* __restrict__ s) {
-  ptx::griddep_launch_dependents();
   ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (int64_t)seq_len * half) return;
   const int pos = (int)(idx / half), p = (int)(idx % half);
@@ -381,8 +381,8 @@ __global__ void rope_table_kernel(int seq_len, int half, double base, int head_d
 __global__ void quantize_e4m3_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, int64_t N, int64_t ldx,
                                      float inv_scale, uint8_t* __restrict__ Q, int64_t ldq,
                                      unsigned int* __restrict__ amax) {
-  ptx::griddep_launch_dependents();
   ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int64_t nv = N >> 4;
   const int64_t total = M * nv;
   float m = 0.f;

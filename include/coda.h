@@ -22,7 +22,10 @@
  *
  * Conventions for every call.
  *   - Memory: the caller owns every buffer.  Tensor pointers are DEVICE pointers on the
- *     current CUDA device.  The library allocates no device memory in any call.
+ *     current CUDA device.  The library allocates no device memory in any call.  An output
+ *     must not overlap any input or other output of the same call, unless the call says so
+ *     (the chains start a GEMM before the previous kernel ends when that kernel writes none of
+ *     the GEMM's operands, which relies on it).
  *   - Streams: every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL = the legacy default stream) and does not synchronise, except
  *     coda_get_device_status, whose name says it reads the device.
