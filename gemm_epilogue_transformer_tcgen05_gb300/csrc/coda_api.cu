@@ -922,6 +922,7 @@ int coda_rope_backward(const coda_tensor* dout, const coda_tensor* out, const fl
   if ((st = check_tensor(out, false)) != CODA_OK) return st;
   if ((st = check_tensor(e_out, false)) != CODA_OK) return st;
   if (!r || !rope_cos || !rope_sin || !c_out) return CODA_ERR_NULL;
+  if (!aligned16(rope_cos) || !aligned16(rope_sin)) return CODA_ERR_ALIGN;
   if (dout->dtype != CODA_BF16 || out->dtype != CODA_BF16 || e_out->dtype != CODA_BF16) return CODA_ERR_DTYPE;
   const int64_t M = dout->rows, N = dout->cols;
   if (out->rows != M || out->cols != N || e_out->rows != M || e_out->cols != N || out->ld != dout->ld) return CODA_ERR_SHAPE;

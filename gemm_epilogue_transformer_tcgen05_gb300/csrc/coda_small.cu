@@ -182,26 +182,41 @@ __global__ void rope_bwd_kernel(const __nv_bfloat16* __restrict__ dout, const __
   const uint4* osrc = reinterpret_cast<const uint4*>(out + row * ld);
   uint4* edst = reinterpret_cast<uint4*>(e + row * lde);
   float acc = 0.f;
-  for (int64_t v = lane; v < (N >> 3); v += 32) {
-    const uint4 du = __ldcs(dsrc + v), ou = __ldcs(osrc + v);
+  // 8 columns (16 bytes of each tensor) per step: pairs p .. p+3 of one head, whose cos/sin
+  // are 4 consecutive floats of the table row
+  auto step = [&](int64_t v, const uint4 du, const uint4 ou) {
     const uint32_t dw[4] = {du.x, du.y, du.z, du.w}, ow[4] = {ou.x, ou.y, ou.z, ou.w};
     const int col = (int)(v << 3);
+    float cv[4] = {1.f, 1.f, 1.f, 1.f}, sv[4] = {0.f, 0.f, 0.f, 0.f};
+    if (col < rope_ncols) {
+      const int64_t t = (int64_t)pos * half + ((col % head_dim) >> 1);
+      const float4 c4 = __ldg(reinterpret_cast<const float4*>(cs + t));
+      const float4 s4 = __ldg(reinterpret_cast<const float4*>(sn + t));
+      cv[0] = c4.x; cv[1] = c4.y; cv[2] = c4.z; cv[3] = c4.w;
+      sv[0] = s4.x; sv[1] = s4.y; sv[2] = s4.z; sv[3] = s4.w;
+    }
     uint32_t o[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      float x0 = __uint_as_float(dw[k] << 16), x1 = __uint_as_float(dw[k] & 0xFFFF0000u);
+      const float x0 = __uint_as_float(dw[k] << 16), x1 = __uint_as_float(dw[k] & 0xFFFF0000u);
       acc = fmaf(x0, __uint_as_float(ow[k] << 16), fmaf(x1, __uint_as_float(ow[k] & 0xFFFF0000u), acc));
-      if (col < rope_ncols) {
-        const int p = ((col % head_dim) >> 1) + k;
-        const float cv = __ldg(cs + (int64_t)pos * half + p), sv = __ldg(sn + (int64_t)pos * half + p);
-        const float y0 = x0 * cv + x1 * sv, y1 = x1 * cv - x0 * sv;
-        x0 = y0;
-        x1 = y1;
-      }
-      __nv_bfloat162 b = __floats2bfloat162_rn(rr * x0, rr * x1);
+      const float y0 = x0 * cv[k] + x1 * sv[k], y1 = x1 * cv[k] - x0 * sv[k];
+      __nv_bfloat162 b = __floats2bfloat162_rn(rr * y0, rr * y1);
       o[k] = *reinterpret_cast<uint32_t*>(&b);
     }
     edst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+  };
+  const int64_t nv = N >> 3;
+  for (int64_t v = lane; v < nv; v += 64) {   // two steps' loads in flight
+    const bool two = v + 32 < nv;
+    const uint4 d0 = __ldcs(dsrc + v), o0 = __ldcs(osrc + v);
+    uint4 d1 = make_uint4(0, 0, 0, 0), o1 = d1;
+    if (two) {
+      d1 = __ldcs(dsrc + v + 32);
+      o1 = __ldcs(osrc + v + 32);
+    }
+    step(v, d0, o0);
+    if (two) step(v + 32, d1, o1);
   }
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);

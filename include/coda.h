@@ -347,7 +347,8 @@ typedef struct coda_qkv_rope_bwd_io {
 CODA_API int coda_qkv_rope_backward(const coda_qkv_rope_bwd_io* io, void* stream);
 
 /* The row-wise RoPE-backward pass on its own: e = r R(-phi) dout (bf16 [M, N]) and
- * c[i] = r_i^2 sum_n dout_in out_in / H. */
+ * c[i] = r_i^2 sum_n dout_in out_in / H.  The cos/sin tables are those of coda_rope_table,
+ * 16-byte aligned (CODA_ERR_ALIGN otherwise); head_dim a multiple of 8. */
 CODA_API int coda_rope_backward(const coda_tensor* dout, const coda_tensor* out, const float* r, const float* rope_cos,
                                 const float* rope_sin, int32_t seq_len, int32_t head_dim, int32_t rope_ncols,
                                 int64_t H, const coda_tensor* e_out, float* c_out, void* stream);
