@@ -123,6 +123,23 @@ int encode_2d(CUtensorMap* m, int dtype, const void* ptr, int64_t inner, int64_t
   return r == CUDA_SUCCESS ? CODA_OK : CODA_ERR_LAUNCH;
 }
 
+// 3-D map of a ROW_MAJOR [rows, 2 * half] tensor whose two column halves (gate, up) are copied
+// together: dims {half, rows, 2} (strides: a row, then a half), box {32, 32, 2}, i.e. the two
+// 32 x 32 blocks of the halves one after the other, each swizzled like a 2-D 32 x 32 box.
+int encode_pair(CUtensorMap* m, int dtype, const void* ptr, int64_t half, int64_t rows, int64_t ld) {
+  const int es = esize(dtype);
+  const uint32_t row_bytes = 32u * (uint32_t)es;
+  CUtensorMapSwizzle sw = row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  CUtensorMapDataType t = dtype == CODA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  cuuint64_t dims[3] = {(cuuint64_t)(half > 0 ? half : 1), (cuuint64_t)(rows > 0 ? rows : 1), 2};
+  cuuint64_t strides[2] = {(cuuint64_t)(ld * es), (cuuint64_t)(half * es)};
+  cuuint32_t box[3] = {32, 32, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, t, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CODA_OK : CODA_ERR_LAUNCH;
+}
+
 // ------------------------------------------------------------- program matching
 struct Item {
   int op;
@@ -419,11 +436,18 @@ static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const 
   else
     st = encode_2d(&L.tmB, W->dtype, W->ptr, K, W->rows, W->ld, bk, 128);
   if (st != CODA_OK) return st;
-  if (epi != EPI_XENT && (st = encode_2d(&L.tmOut, out->dtype, out->ptr, out->cols, M, out->ld, 32, 32)) != CODA_OK)
+  if (epi == EPI_SWIGLU_BWD) {
+    if ((st = encode_pair(&L.tmOut, out->dtype, out->ptr, N, M, out->ld)) != CODA_OK) return st;   // e: both halves
+  } else if (epi != EPI_XENT &&
+             (st = encode_2d(&L.tmOut, out->dtype, out->ptr, out->cols, M, out->ld, 32, 32)) != CODA_OK) {
     return st;
+  }
   if (epi == EPI_RESID) {
     const coda_tensor* r = sd.residual;
     if ((st = encode_2d(&L.tmSide0, r->dtype, r->ptr, r->cols, M, r->ld, 32, 32)) != CODA_OK) return st;
+  } else if (epi == EPI_SWIGLU_BWD) {
+    const coda_tensor* z = sd.aux_in;   // Z = [G | U]: both halves of a chunk in one copy
+    if ((st = encode_pair(&L.tmSide0, z->dtype, z->ptr, N, M, z->ld)) != CODA_OK) return st;
   } else if (epi == EPI_SWIGLU_BWD || epi == EPI_RMSBWD) {
     const coda_tensor* r = sd.aux_in;
     if ((st = encode_2d(&L.tmSide0, r->dtype, r->ptr, r->cols, M, r->ld, 32, 32)) != CODA_OK) return st;
@@ -432,7 +456,10 @@ static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const 
       if ((st = encode_2d(&L.tmSide1, r2->dtype, r2->ptr, r2->cols, M, r2->ld, 32, 32)) != CODA_OK) return st;
     }
   }
-  if (want_aux) {
+  if (want_aux && epi == EPI_SWIGLU) {
+    const coda_tensor* z = ax.store_aux;   // saved Z = [G | U]: both halves of a chunk in one copy
+    if ((st = encode_pair(&L.tmAux, z->dtype, z->ptr, N, M, z->ld)) != CODA_OK) return st;
+  } else if (want_aux) {
     const coda_tensor* z = ax.store_aux;
     if ((st = encode_2d(&L.tmAux, z->dtype, z->ptr, z->cols, M, z->ld, 32, 32)) != CODA_OK) return st;
   }

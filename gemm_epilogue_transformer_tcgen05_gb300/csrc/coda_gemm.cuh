@@ -139,6 +139,13 @@ struct GemmCfg {
   static constexpr int XSLOT = 32 * 32 * 2;                 // aux output block (bf16)
   static constexpr int NX = AUX ? (EPI == EPI_SWIGLU ? 2 : 1) : 0;   // SwiGLU: G and U; residual: h * g
   static constexpr int OUTSET = NO * OSLOT + NX * XSLOT;
+  // Gate/up halves moved as one 3-D box {32 columns, 32 rows, 2 halves}: one TMA operation
+  // instead of two for the saved Z read by the SwiGLU backward, its output e, and the Z that
+  // the SwiGLU forward saves.  In shared memory the box is the two 32 x 32 staging blocks of
+  // the halves, one after the other, each swizzled as a 2-D block.
+  static constexpr bool PAIR_SIDE = EPI == EPI_SWIGLU_BWD;
+  static constexpr bool PAIR_OUT = EPI == EPI_SWIGLU_BWD;
+  static constexpr bool PAIR_AUX = EPI == EPI_SWIGLU && AUX;
   // side inputs are prefetched NSS chunks ahead (one staging set per chunk in flight); the
   // SwiGLU backward, with two side inputs and two outputs per chunk, goes deeper
   static constexpr int NSS = EPI == EPI_SWIGLU_BWD ? 4 : 2;
@@ -548,9 +555,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ptx::mbar_arrive_expect_tx(sbar, (side1 ? C::NS : 1) * C::SSLOT);
           if constexpr (C::EPI == EPI_RESID) {
             ptx::tma_load_2d_hint(dst, &tmSide0, n0 + 32 * c, r0, sbar, stream_pol);
-          } else if constexpr (C::EPI == EPI_SWIGLU_BWD) {
-            ptx::tma_load_2d_hint(dst, &tmSide0, n0 + 32 * c, r0, sbar, stream_pol);
-            ptx::tma_load_2d_hint(dst + C::SSLOT, &tmSide0, p.up_offset + n0 + 32 * c, r0, sbar, stream_pol);
+          } else if constexpr (C::PAIR_SIDE) {
+            ptx::tma_load_3d_hint(dst, &tmSide0, n0 + 32 * c, r0, 0, sbar, stream_pol);   // G and U blocks
           } else {
             ptx::tma_load_2d_hint(dst, &tmSide0, n0 + 32 * c, r0, sbar, stream_pol);
             if (side1) ptx::tma_load_2d_hint(dst + C::SSLOT, &tmSide1, n0 + 32 * c, r0, sbar, stream_pol);
@@ -824,15 +830,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         if (lane == 0) {
           if (store) {
-            if (C::EPI == EPI_STORE && C::OUT_DT == DT_F32 && p.k_splits > 1)
-              ptx::tma_reduce_add_2d_hint(&tmOut, col0, r0, oslot, stream_pol);   // split-K partial
-            else
-              ptx::tma_store_2d_hint(&tmOut, col0, r0, oslot, stream_pol);
-            if constexpr (C::EPI == EPI_SWIGLU_BWD)
-              ptx::tma_store_2d_hint(&tmOut, p.up_offset + col0, r0, oslot + C::OSLOT, stream_pol);
-            if constexpr (C::NX > 0) ptx::tma_store_2d_hint(&tmAux, col0, r0, oslot + C::NO * C::OSLOT, stream_pol);
-            if constexpr (C::NX > 1)
-              ptx::tma_store_2d_hint(&tmAux, p.up_offset + col0, r0, oslot + C::NO * C::OSLOT + C::XSLOT, stream_pol);
+            if constexpr (C::PAIR_OUT) {
+              ptx::tma_store_3d_hint(&tmOut, col0, r0, 0, oslot, stream_pol);   // e's gate and up blocks
+            } else {
+              if (C::EPI == EPI_STORE && C::OUT_DT == DT_F32 && p.k_splits > 1)
+                ptx::tma_reduce_add_2d_hint(&tmOut, col0, r0, oslot, stream_pol);   // split-K partial
+              else
+                ptx::tma_store_2d_hint(&tmOut, col0, r0, oslot, stream_pol);
+              if constexpr (C::EPI == EPI_SWIGLU_BWD)
+                ptx::tma_store_2d_hint(&tmOut, p.up_offset + col0, r0, oslot + C::OSLOT, stream_pol);
+            }
+            if constexpr (C::PAIR_AUX) {
+              ptx::tma_store_3d_hint(&tmAux, col0, r0, 0, oslot + C::NO * C::OSLOT, stream_pol);   // Z's G and U
+            } else {
+              if constexpr (C::NX > 0)
+                ptx::tma_store_2d_hint(&tmAux, col0, r0, oslot + C::NO * C::OSLOT, stream_pol);
+              if constexpr (C::NX > 1)
+                ptx::tma_store_2d_hint(&tmAux, p.up_offset + col0, r0, oslot + C::NO * C::OSLOT + C::XSLOT,
+                                       stream_pol);
+            }
           }
           ptx::bulk_commit();
         }

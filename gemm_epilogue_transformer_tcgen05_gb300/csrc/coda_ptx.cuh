@@ -68,6 +68,15 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
       : "memory");
 }
+// 3-D tiled load (coordinates innermost first) with an L2 cache hint.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* m, int32_t c0, int32_t c1,
+                                                 int32_t c2, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+      : "memory");
+}
 // L2 policies: keep a reused operand (evict_last), stream a once-touched tensor (evict_first).
 __device__ __forceinline__ uint64_t make_policy_evict_last() {
   uint64_t p;
@@ -91,6 +100,15 @@ __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* m, int32_t 
                    "l"(reinterpret_cast<uint64_t>(m)),
                "r"(c0), "r"(c1), "r"(src), "l"(policy)
                : "memory");
+}
+// 3-D tiled store shared -> global (bulk-group completion).
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* m, int32_t c0, int32_t c1, int32_t c2,
+                                                  uint32_t src, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%1, %2, %3}], [%4], %5;" ::
+          "l"(reinterpret_cast<uint64_t>(m)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(src), "l"(policy)
+      : "memory");
 }
 // 2-D tiled reduce-add shared -> global (fp32 add into the destination; bulk-group completion).
 __device__ __forceinline__ void tma_reduce_add_2d_hint(const CUtensorMap* m, int32_t c0, int32_t c1, uint32_t src,
