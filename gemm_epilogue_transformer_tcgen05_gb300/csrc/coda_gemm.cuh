@@ -301,6 +301,17 @@ __device__ __forceinline__ void slot_write(uint32_t slot, int row, const float (
   }
 }
 
+// An e4m3 staging block from codes already packed in pairs (q[i] holds elements 2i, 2i+1).
+__device__ __forceinline__ void slot_write_codes(uint32_t slot, int row, const uint16_t (&q)[16]) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = (uint32_t)q[8 * j + 2 * k] | ((uint32_t)q[8 * j + 2 * k + 1] << 16);
+    ptx::st_shared_v4(swz<DT_E4M3>(slot, row, j), w[0], w[1], w[2], w[3]);
+  }
+}
+
 // Value as it will be stored (used where a partial must match the stored tensor).
 template <int DT>
 __device__ __forceinline__ float as_stored(float x) {
@@ -662,6 +673,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
         const int col0 = n0 + 32 * c;
         float o1[C::NO > 1 ? 32 : 1];
+        constexpr bool CODES = C::EPI == EPI_SWIGLU_BWD && C::OUT_DT == DT_E4M3;   // e quantised in place
+        uint16_t qg[CODES ? 16 : 1], qu[CODES ? 16 : 1];
         float zg[C::AUX ? 32 : 1], zu[C::NX > 1 ? 32 : 1];
 
         // ---------------------------------------------------------------- the program
@@ -742,24 +755,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         } else if constexpr (C::EPI == EPI_SWIGLU_BWD) {
           const float sc = ts * rs;
+          if constexpr (C::OUT_DT == DT_E4M3) {
+            // e is quantised once: its e4m3 codes (of e * os) go to the staging blocks as they
+            // are, and the partial sums the dequantised values (scaled back once per row below)
+            const float os = p.out_scale;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float dA = x[j], G = s0[j], U = s1[j];
-            const float sg = sigmoid_f(G);
-            float eg = sc * dA * U * sg * (1.f + G * (1.f - sg));
-            float eu = sc * dA * G * sg;
-            if constexpr (C::OUT_DT == DT_E4M3) {
-              // stored: the e4m3 codes of e * os; the partial sums the dequantised e (the
-              // sum is scaled back once per row below)
-              amax_local = fmaxf(amax_local, fmaxf(fabsf(eg), fabsf(eu)));
-              ptx::e4m3x2_to_f32(ptx::cvt_e4m3x2(eg * p.out_scale, eu * p.out_scale), eg, eu);
-            } else {
-              eg = as_stored<C::OUT_DT>(eg);
-              eu = as_stored<C::OUT_DT>(eu);
+            for (int j = 0; j < 32; j += 2) {
+              float eg[2], eu[2];
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const float G = s0[j + k], U = s1[j + k], d = sc * x[j + k];
+                const float sg = sigmoid_f(G);
+                eg[k] = d * U * sg * (1.f + G * (1.f - sg));
+                eu[k] = d * G * sg;
+                amax_local = fmaxf(amax_local, fmaxf(fabsf(eg[k]), fabsf(eu[k])));
+              }
+              qg[j >> 1] = ptx::cvt_e4m3x2(eg[0] * os, eg[1] * os);
+              qu[j >> 1] = ptx::cvt_e4m3x2(eu[0] * os, eu[1] * os);
+              float g0, g1, u0, u1;
+              ptx::e4m3x2_to_f32(qg[j >> 1], g0, g1);
+              ptx::e4m3x2_to_f32(qu[j >> 1], u0, u1);
+              rowacc = fmaf(g0, s0[j], fmaf(u0, s1[j], fmaf(g1, s0[j + 1], fmaf(u1, s1[j + 1], rowacc))));
             }
-            rowacc = fmaf(eg, G, fmaf(eu, U, rowacc));
-            x[j] = eg;
-            o1[j] = eu;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float G = s0[j], U = s1[j], d = sc * x[j];
+              const float sg = sigmoid_f(G);
+              const float eg = as_stored<C::OUT_DT>(d * U * sg * (1.f + G * (1.f - sg)));
+              const float eu = as_stored<C::OUT_DT>(d * G * sg);
+              rowacc = fmaf(eg, G, fmaf(eu, U, rowacc));
+              x[j] = eg;
+              o1[j] = eu;
+            }
           }
         } else if constexpr (C::EPI == EPI_XENT) {
           // P4 / P5: block log-sum-exp with the running (max, sum-exp) state of the row
@@ -822,8 +850,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t oslot = out_base + (c & 1) * C::OUTSET;
         if (lane == 0) ptx::bulk_wait_read<1>();  // the group that last used this set is done reading
         __syncwarp();
-        slot_write<C::OUT_DT>(oslot, lane, x);
-        if constexpr (C::NO > 1) slot_write<C::OUT_DT>(oslot + C::OSLOT, lane, o1);
+        if constexpr (CODES) {
+          slot_write_codes(oslot, lane, qg);
+          slot_write_codes(oslot + C::OSLOT, lane, qu);
+        } else {
+          slot_write<C::OUT_DT>(oslot, lane, x);
+          if constexpr (C::NO > 1) slot_write<C::OUT_DT>(oslot + C::OSLOT, lane, o1);
+        }
         if constexpr (C::NX > 0) slot_write<DT_BF16>(oslot + C::NO * C::OSLOT, lane, zg);
         if constexpr (C::NX > 1) slot_write<DT_BF16>(oslot + C::NO * C::OSLOT + C::XSLOT, lane, zu);
         ptx::fence_proxy_async_smem();
