@@ -625,6 +625,7 @@ def other_workloads(torch, C, S, args, stream):
     byt = 2 * M_TOK * 8192 + 4 * M_TOK
     out["row_rms_full_row_M16384_N8192"] = {"ms": ms, "gbs": byt / (ms * 1e-3) / 1e9, "bytes": byt,
                                              "frac_of_hbm": byt / (ms * 1e-3) / 1e9 / pk["hbm"],
+                                             "frac_of_nominal_7900": byt / (ms * 1e-3) / 1e9 / 7900.0,
                                              "peak_kind": f"HBM copy, {pk['source']}"}
     del Xr, rr
     # C2: block backward (after a training-mode forward that saves Z)
