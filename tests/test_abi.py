@@ -113,6 +113,31 @@ def test_other_entry_points_validate(L):
     assert L.coda_get_device_status(None, None) == C.ERR_NULL
 
 
+def test_fp8_backward_quantiser_and_overlap_validate(L):
+    X = _t(FAKE, C.BF16, 64, 48, 48)
+    Q = _t(FAKE, C.E4M3, 64, 48, 48)
+    assert L.coda_quantize_e4m3(None, 1.0, ctypes.byref(Q), None, None) == C.ERR_NULL
+    assert L.coda_quantize_e4m3(ctypes.byref(X), 0.0, ctypes.byref(Q), None, None) == C.ERR_SHAPE   # scale > 0
+    assert L.coda_quantize_e4m3(ctypes.byref(Q), 1.0, ctypes.byref(Q), None, None) == C.ERR_DTYPE   # bf16 in
+    assert L.coda_quantize_e4m3(ctypes.byref(X), 1.0, ctypes.byref(_t(FAKE, C.E4M3, 64, 32, 48)), None,
+                                None) == C.ERR_SHAPE
+    assert L.coda_quantize_e4m3(ctypes.byref(_t(FAKE, C.BF16, 64, 40, 40)), 1.0,
+                                ctypes.byref(_t(FAKE, C.E4M3, 64, 40, 48)), None, None) == C.ERR_SHAPE   # N % 16
+    assert L.coda_mlp_fp8_backward(None, None) == C.ERR_NULL
+    f = ctypes.c_void_p(FAKE)
+    io = C.CodaMlpFp8Bwd(M=256, H=256, F=128, s_x=1.0, s_w=1.0, s_wd=1.0, s_a=1.0, s_dy=1.0, s_e=0.0, h=f, X_q=f,
+                         W_q=f, W_dq=f, Z=f, a_q=f, r=f, dY=f, dY_q=f, amax_dy=f, e_q=f, amax_e=f, c=f, dh=f,
+                         dW_d=f, dW=f, workspace=f)
+    assert L.coda_mlp_fp8_backward(ctypes.byref(io), None) == C.ERR_SHAPE            # s_e must be > 0
+    io.s_e, io.F = 1.0, 100
+    assert L.coda_mlp_fp8_backward(ctypes.byref(io), None) == C.ERR_SHAPE            # F % 128
+    io.F, io.dW = 128, None
+    assert L.coda_mlp_fp8_backward(ctypes.byref(io), None) == C.ERR_NULL
+    assert C.coda_workspace_size(C.WS_MLP_FP8_BWD, 16384, 4096, 14336) == 56 * 16384 * 4
+    assert L.coda_set_launch_overlap(2) == C.ERR_SHAPE
+    assert L.coda_set_launch_overlap(1) == C.OK
+
+
 def test_binding_reads_layout_from_strides():
     import torch
     x = torch.empty((64, 32), dtype=torch.bfloat16)
