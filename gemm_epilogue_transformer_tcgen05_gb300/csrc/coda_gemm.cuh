@@ -9,14 +9,20 @@
 // lenguaje LEGO").  The pages picture the tile in registers; on this GPU it lives in
 // tensor memory (TMEM) and is read back in 32-column chunks by the epilogue warps.
 //
-// Structure (one CTA per SM, persistent over output tiles):
-//   warp 0      TMA producer: A and B k-blocks into a STAGES-deep shared-memory ring
-//   warp 1      TMEM allocation + single-thread tcgen05.mma issue (128 x 256 x 32 bytes
-//               of K per instruction) into one of two TMEM accumulators (2 x 256 cols)
+// Structure (CTA pairs: clusters of two CTAs on two SMs, persistent over 256 x 256 output
+// tiles; each CTA owns 128 rows of the tile):
+//   warp 0      TMA producer: this CTA's 128 rows of A and 128 rows of B per k-block into a
+//               STAGES-deep shared-memory ring (both CTAs' copies complete on the leader's
+//               barrier)
+//   warp 1      TMEM allocation; in the leader CTA, single-thread tcgen05.mma.cta_group::2
+//               issue (256 x 256 x 32 bytes of K per instruction) into one of two TMEM
+//               accumulators (2 x 256 columns in each CTA)
 //   warps 2..5  epilogue: tcgen05.ld (thread = output row), the epilogue program, row /
 //               column partial reductions, cast, swizzled staging in shared memory and
 //               TMA stores; side inputs (residual, saved activations) arrive by TMA.
-// The two TMEM accumulators let tile t+1's mainloop run under tile t's epilogue.
+// The two TMEM accumulators let tile t+1's mainloop run under tile t's epilogue.  The
+// launch carries a programmatic dependency on the previous kernel of the stream (see
+// griddep_wait in coda_ptx.cuh).
 //
 // Every wait is bounded (global timer).  On expiry the waiting thread records a site
 // code in a device status word, raises a CTA-wide abort flag, every role leaves its loop,
