@@ -155,6 +155,7 @@ struct GemmCfg {
   // side inputs are prefetched NSS chunks ahead (one staging set per chunk in flight); the
   // SwiGLU backward, with two side inputs and two outputs per chunk, goes deeper
   static constexpr int NSS = EPI == EPI_SWIGLU_BWD ? 4 : 2;
+  static_assert(NCHUNK % NSS == 0, "a chunk and the next tile's chunk NCHUNK later share a ring slot");
   static constexpr int EPI_WARP_BYTES = NSS * NS * SSLOT + 2 * OUTSET;
   static constexpr int EPI_BYTES = NUM_EPI_WARPS * EPI_WARP_BYTES;
   static constexpr int BAR_BYTES = 320;
@@ -544,6 +545,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t side_base = sm_epi + ew * C::EPI_WARP_BYTES;
     const uint32_t out_base = side_base + C::NSS * C::NS * C::SSLOT;
     uint32_t side_par = 0, side_pending = 0;
+    uint32_t prefetched = 0;   // chunks (< NSS) of the coming tile whose side inputs are in flight
     float amax_local = 0.f;
     const uint64_t stream_pol = ptx::make_policy_evict_first();  // outputs and side inputs: touched once
     bool ok = true;
@@ -563,7 +565,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // chunks are neither issued nor waited for.
       const bool slab_ok = r0 < p.M;
       auto live = [&](int c) { return slab_ok && (n0 + 32 * c < p.N); };
-      auto issue_side = [&](int c) {
+      // side inputs of chunk c of the tile at (tn0, tr0) into ring slot c % NSS
+      auto issue_side_at = [&](int c, int tn0, int tr0) {
         if constexpr (C::NS > 0) {
           const int slot = c % C::NSS;
           const uint32_t sbar = SIDE_BAR(ew, slot);
@@ -571,23 +574,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const bool side1 = C::NS > 1 && !(p.flags & F_NO_SIDE1);
           ptx::mbar_arrive_expect_tx(sbar, (side1 ? C::NS : 1) * C::SSLOT);
           if constexpr (C::EPI == EPI_RESID) {
-            ptx::tma_load_2d_hint(dst, &tmSide0, n0 + 32 * c, r0, sbar, stream_pol);
+            ptx::tma_load_2d_hint(dst, &tmSide0, tn0 + 32 * c, tr0, sbar, stream_pol);
           } else if constexpr (C::PAIR_SIDE) {
-            ptx::tma_load_3d_hint(dst, &tmSide0, n0 + 32 * c, r0, 0, sbar, stream_pol);   // G and U blocks
+            ptx::tma_load_3d_hint(dst, &tmSide0, tn0 + 32 * c, tr0, 0, sbar, stream_pol);   // G and U blocks
           } else {
-            ptx::tma_load_2d_hint(dst, &tmSide0, n0 + 32 * c, r0, sbar, stream_pol);
-            if (side1) ptx::tma_load_2d_hint(dst + C::SSLOT, &tmSide1, n0 + 32 * c, r0, sbar, stream_pol);
+            ptx::tma_load_2d_hint(dst, &tmSide0, tn0 + 32 * c, tr0, sbar, stream_pol);
+            if (side1) ptx::tma_load_2d_hint(dst + C::SSLOT, &tmSide1, tn0 + 32 * c, tr0, sbar, stream_pol);
           }
         }
       };
+      // The next tile of this CTA: its first chunks' side inputs are issued while this tile's
+      // last chunks are processed, so its epilogue does not start on a cold load.
+      const int next_tile = tile + n_clusters;
+      int nn0 = 0, nr0 = 0;
+      bool next_slab_ok = false;
+      if constexpr (C::NS > 0) {
+        if (next_tile < total_tiles) {
+          int nmb, nnb, nk0, nk1;
+          work_coords(next_tile, p, nmb, nnb, nk0, nk1, num_kb);
+          nn0 = nnb * C::BN_OUT;
+          nr0 = nmb * C::PAIR_ROWS + (int)rank * BM + 32 * q;
+          next_slab_ok = nr0 < p.M;
+        }
+      }
+      auto live_next = [&](int c) { return next_slab_ok && (nn0 + 32 * c < p.N); };
       if constexpr (C::NS > 0) {
 #pragma unroll
         for (int c = 0; c < C::NSS; ++c) {
-          if (c < C::NCHUNK && live(c)) {
-            if (lane == 0) issue_side(c);
+          if (c < C::NCHUNK && live(c) && !((prefetched >> c) & 1u)) {
+            if (lane == 0) issue_side_at(c, n0, r0);
             side_pending |= 1u << c;
           }
         }
+        prefetched = 0;
       }
 
       float rs = 1.f, rc = 0.f;
@@ -671,9 +690,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           __syncwarp();
-          if (c + C::NSS < C::NCHUNK && live(c + C::NSS)) {
-            if (lane == 0) issue_side(c + C::NSS);
+          if (c + C::NSS < C::NCHUNK) {
+            if (live(c + C::NSS)) {
+              if (lane == 0) issue_side_at(c + C::NSS, n0, r0);
+              side_pending |= 1u << slot;
+            }
+          } else if (live_next(c + C::NSS - C::NCHUNK)) {   // same slot: NCHUNK is a multiple of NSS
+            if (lane == 0) issue_side_at(c + C::NSS - C::NCHUNK, nn0, nr0);
             side_pending |= 1u << slot;
+            prefetched |= 1u << (c + C::NSS - C::NCHUNK);
           }
         }
 
