@@ -46,3 +46,43 @@ def test_dropped_stage_times_out_and_context_survives(C):
     st3, _ = C.coda_get_device_status()
     assert st3 == C.OK
     assert_close(f64(out2), O.linear(f64(A), f64(W)), TOL_BF16, "GEMM after a timed-out launch")
+
+
+@pytest.mark.parametrize("program", ["residual", "swiglu_backward"])
+def test_dropped_stage_with_side_inputs_in_flight(C, program):
+    """The same with epilogue programs whose side inputs (the residual; the saved Z) are
+    already being loaded when the wait runs out: the epilogue lets those copies land before
+    the CTA exits, and the next launch of the same program is exact."""
+    M, N, K = 1024, 1024, 256
+    A = dev(seeded((M, K), 62, dtype=BF))
+    W = dev(seeded((N, K), 63, std=0.05, dtype=BF))
+    if program == "residual":
+        R = dev(seeded((M, N), 64, dtype=BF))
+        out = torch.zeros((M, N), dtype=BF, device="cuda")
+        run = lambda o: C.coda_gemm_epilogue(A, W, [C.OP_ADD_SIDE], o, residual=R)
+        ref = lambda: O.linear(f64(A), f64(W)) + f64(R)
+    else:
+        W = dev(seeded((K, N), 63, std=0.05, dtype=BF)).t()   # read MN-major, as the backward reads W_d
+        Z = dev(seeded((M, 2 * N), 65, dtype=BF))
+        r = dev(seeded((M,), 66, std=0.1, mean=1.0))
+        S_ = torch.empty(((N + 255) // 256, M), device="cuda")
+        out = torch.zeros((M, 2 * N), dtype=BF, device="cuda")
+        run = lambda o: C.coda_gemm_epilogue(A, W, [C.OP_SWIGLU_BWD, C.OP_ROW_SCALE, C.OP_ROW_DOT_PARTIAL], o,
+                                             aux_in=Z, row_scale=r, row_partials=S_)
+
+        def ref():
+            dA, z, rr = O.linear(f64(A), f64(W)), f64(Z), f64(r)[:, None]
+            G, U = z[:, :N], z[:, N:]
+            return rr * __import__("numpy").hstack([dA * U * O.silu_grad(G), dA * O.silu(G)])
+    C.coda_set_watchdog_ms(200)
+    C.coda_inject_dropped_stage(True)
+    run(out)
+    st, site = C.coda_get_device_status()
+    assert st == C.ERR_DEVICE_TIMEOUT, st
+    assert site in (1, 2, 3, 4, 5), site
+    C.coda_set_watchdog_ms(2000)
+    out2 = torch.empty_like(out)
+    run(out2)
+    st3, _ = C.coda_get_device_status()
+    assert st3 == C.OK
+    assert_close(f64(out2), ref(), TOL_BF16, f"{program} after a timed-out launch")
