@@ -155,25 +155,51 @@ def test_colscale_mn_major(C):
     assert_close(f64(out), (f64(X).T @ f64(Y)) * f64(g)[None, :], 1e-5, "(X^T Y) g")
 
 
-def test_swiglu_backward_epilogue(C):
-    M, H, F = 300, 256, 512
+@pytest.mark.parametrize("M,F,ts", [(300, 512, None), (300, 288, 0.5)])
+def test_swiglu_backward_epilogue(C, M, F, ts):
+    """F = 288: the second 256-column tile has one live 32-column chunk, so the gate and up
+    blocks of Z and e (moved as one 3-D box) are clipped at F in both halves."""
+    H = 256
     dY = seeded((M, H), 24, dtype=BF)
     Wd = seeded((H, F), 25, std=0.05, dtype=BF)       # stored [H, F]; the GEMM reads W_d^T
     Z = seeded((M, 2 * F), 26, dtype=BF)
     r = seeded((M,), 27, std=0.2, mean=1.0)
-    e = torch.empty((M, 2 * F), dtype=BF, device="cuda")
-    S = torch.empty((F // 256, M), dtype=torch.float32, device="cuda")
-    C.coda_gemm_epilogue(dev(dY), dev(Wd).t(), [C.OP_SWIGLU_BWD, C.OP_ROW_SCALE, C.OP_ROW_DOT_PARTIAL], e,
-                         aux_in=dev(Z), row_scale=dev(r), row_partials=S)
+    e = torch.full((M, 2 * F), float("nan"), dtype=BF, device="cuda")
+    nt = (F + 255) // 256
+    S = torch.empty((nt, M), dtype=torch.float32, device="cuda")
+    ops = [C.OP_SWIGLU_BWD, C.OP_ROW_SCALE, C.OP_ROW_DOT_PARTIAL]
+    if ts is not None:
+        ops = [C.OP_TENSOR_SCALE] + ops
+    C.coda_gemm_epilogue(dev(dY), dev(Wd).t(), ops, e, aux_in=dev(Z), row_scale=dev(r), row_partials=S,
+                         tensor_scale=ts if ts is not None else 1.0)
     torch.cuda.synchronize()
     fresh_status()
-    dA = f64(dY) @ f64(Wd)
+    dA = (ts if ts is not None else 1.0) * (f64(dY) @ f64(Wd))
     G, U = f64(Z)[:, :F], f64(Z)[:, F:]
     ref = f64(r)[:, None] * np.hstack([dA * U * O.silu_grad(G), dA * O.silu(G)])
     assert_close(f64(e), ref, TOL_BF16, "e")
-    s_ref = np.stack([np.sum((ref * f64(Z))[:, np.r_[t * 256:(t + 1) * 256, F + t * 256:F + (t + 1) * 256]], axis=1)
-                      for t in range(F // 256)])
+    s_ref = np.stack([np.sum((ref * f64(Z))[:, np.r_[t * 256:min((t + 1) * 256, F), F + t * 256:F + min((t + 1) * 256,
+                                                                                                    F)]], axis=1)
+                      for t in range(nt)])
     assert_close(f64(S), s_ref, TOL_BF16, "row partials of e . Z")
+
+
+def test_rmsnorm_backward_without_gain_and_scaled(C):
+    """The combine with a tensor scale and no gain (g = 1, no column partials), the form the
+    FP8 backward uses, at a ragged width (H = 288)."""
+    M, H, K = 300, 288, 384
+    E = seeded((M, K), 34, dtype=BF)
+    W = seeded((K, H), 35, std=0.05, dtype=BF)
+    h = seeded((M, H), 36, dtype=BF)
+    dY = seeded((M, H), 37, dtype=BF)
+    c = seeded((M,), 38, std=0.1)
+    out = torch.empty((M, H), dtype=BF, device="cuda")
+    C.coda_gemm_epilogue(dev(E), dev(W).t(), [C.OP_TENSOR_SCALE, C.OP_RMSBWD_COMBINE], out, aux_in=dev(h),
+                         aux_in2=dev(dY), row_coef=dev(c), tensor_scale=0.25)
+    torch.cuda.synchronize()
+    fresh_status()
+    ref = 0.25 * (f64(E) @ f64(W)) - f64(c)[:, None] * f64(h) + f64(dY)
+    assert_close(f64(out), ref, TOL_BF16, "s t - c h + dY")
 
 
 def test_rmsnorm_backward_epilogue(C):
