@@ -6,6 +6,7 @@
 // (primitive kinds); see include/coda.h for each call's contract.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -31,8 +32,8 @@ constexpr int kMaxDevices = 64;
 DevState g_dev[kMaxDevices];
 std::mutex g_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-uint32_t g_watchdog_ms = 0;
-int g_inject_once = 0;
+std::atomic<uint32_t> g_watchdog_ms{0};
+std::atomic<int> g_inject_once{0};
 
 int ensure_device(DevState** out) {
   int dev = -1;
@@ -213,7 +214,7 @@ int match_program(const coda_epilogue_program* prog, uint32_t* present) {
 }  // namespace
 
 namespace coda {
-int g_launch_overlap = [] {
+std::atomic<int> g_launch_overlap = [] {
   const char* e = std::getenv("CODA_LAUNCH_OVERLAP");
   return (e && e[0] == '0') ? 0 : 1;
 }();
@@ -523,10 +524,7 @@ static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const 
             (has(CODA_OP_ROW_SCALE) ? F_ROWSCALE : 0) | (has(CODA_OP_COL_DOT_PARTIAL) ? F_COLPART : 0) |
             (epi == EPI_RMSBWD && !sd.aux_in2 ? F_NO_SIDE1 : 0);
   if (ab_ready && g_launch_overlap) p.flags |= F_AB_READY;
-  if (g_inject_once) {
-    p.flags |= F_INJECT_SKIP;
-    g_inject_once = 0;
-  }
+  if (g_inject_once.exchange(0)) p.flags |= F_INJECT_SKIP;
   p.up_offset = (int)N;
   p.tensor_scale = has(CODA_OP_TENSOR_SCALE) ? sd.tensor_scale : 1.0f;
   p.out_scale = (out->dtype == CODA_E4M3 || epi == EPI_XENT_BWD) ? sd.out_scale : 1.0f;

@@ -29,6 +29,8 @@
 // copies in flight are drained with a short bounded wait, TMEM is freed and the kernel
 // returns; the host reads the status word.  Nothing traps.
 #pragma once
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -986,7 +988,7 @@ using GemmLaunchFn = cudaError_t (*)(const GemmLaunch&, cudaStream_t);
 // Number of CTA groups (pairs for CG = 2) that can be resident at once, per device.
 template <class C>
 int resident_groups(int sms) {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && cached[dev] > 0) return cached[dev];
@@ -1014,7 +1016,7 @@ int resident_groups(int sms) {
 
 template <class C>
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t s) {
-  static int attr_done[64] = {0};
+  static std::atomic<int> attr_done[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {

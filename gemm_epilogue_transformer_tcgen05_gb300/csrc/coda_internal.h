@@ -1,5 +1,7 @@
 // Internal declarations shared by the library's translation units (not part of the ABI).
 #pragma once
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -34,7 +36,7 @@ const VariantEntry* find_variant(const VariantKey& k);
 
 // 1 (default): kernels are launched with a programmatic dependency on the previous kernel of the
 // stream (their launch overlaps its tail); 0: plain stream serialisation.
-extern int g_launch_overlap;
+extern std::atomic<int> g_launch_overlap;
 
 // Small bandwidth-bound kernels (coda_small.cu).  Arguments are validated by the caller.
 cudaError_t launch_partial_reduce(const float* partials, int64_t ld, int nparts, int64_t M, float inv_d, float eps,
