@@ -50,6 +50,16 @@ Readings of points the pages leave open (the plainest reading consistent with th
      are quantised with scales the caller supplies (delayed scaling, as for s_a); the GEMMs
      and the row sum behind c see the dequantised values; the residual gradient (+ dY) and
      the RMSNorm-backward combine use dY and h as stored (bf16).
+  9. FP4 operands are NVFP4, the block-scaled 4-bit format of the Blackwell tensor cores (the
+     pages name FP4 only as a faster matmul format).  Each row of an operand is cut into
+     blocks of 16 consecutive K elements.  A block carries one unsigned e4m3 scale sf, the
+     tensor carries one fp32 scale s, and an element carries an e2m1 code q (values 0, 0.5,
+     1, 1.5, 2, 3, 4, 6 and their negatives); its value is s * sf * q.  Quantising a block:
+     sf = e4m3(amax / (6 s)), then q = e2m1(x / (sf s)) (zero when sf is zero), both
+     rounded to nearest-even with saturation.  The quotients and the product sf s are taken
+     in fp32, the precision the kernels decide the codes in, so that equal fp32 inputs give
+     equal codes.  s is chosen by the caller: amax / (6 * 448) of the tensor for operands
+     known up front, and a delayed scale (as s_a above) for the SwiGLU output.
 Every function here is pinned by a test (closed form, invariant, library special case
 or brute force); none is "parity unpinned".
 """
@@ -211,6 +221,93 @@ def e4m3_encode(x):
     M = np.where(normal, np.rint(a / np.exp2(e.astype(F64)) * 8.0 - 8.0), np.rint(a / 2.0 ** -9))
     code = (np.where(sign, 0x80, 0) | (E.astype(np.int64) << 3) | M.astype(np.int64)).astype(np.uint8)
     return code
+
+
+# ---------------------------------------------------------------------------------------
+# NVFP4 (reading 9)  [KuCoin, "El impuesto a la pereza": FP8 and FP4 speed up the matmul,
+# so the tensor traffic around it weighs more]
+# ---------------------------------------------------------------------------------------
+E2M1_MAX = 6.0
+NVFP4_BLOCK = 16
+
+
+def e2m1_round(x):
+    """Nearest e2m1 value, ties to the even code, saturating to +-6 (float64 result).
+
+    e2m1 = sign | 2-bit exponent (bias 1) | 1-bit mantissa: subnormals 0 and 0.5, then
+    1, 1.5, 2, 3, 4, 6.  The spacing at magnitude a is 2^(e-1) with e = max(floor(log2 a), 0),
+    and an even multiple of the spacing is an even code."""
+    x = _f64(x)
+    a = np.minimum(np.abs(x), E2M1_MAX)
+    _, ex = np.frexp(a)
+    e = np.maximum(ex.astype(F64) - 1.0, 0.0)
+    q = np.exp2(e - 1.0)
+    v = np.minimum(np.rint(a / q) * q, E2M1_MAX)
+    return np.copysign(v, x)
+
+
+def e2m1_decode(codes):
+    """Value of each 4-bit code (low nibble of the input): sign bit 3, exponent bits 2-1, mantissa bit 0."""
+    c = np.asarray(codes).astype(np.int64) & 0xF
+    sgn = np.where(c & 0x8, -1.0, 1.0)
+    E = (c >> 1) & 0x3
+    m = (c & 0x1).astype(F64)
+    val = np.where(E == 0, 0.5 * m, (1.0 + 0.5 * m) * np.exp2(E.astype(F64) - 1.0))
+    return sgn * val
+
+
+def e2m1_encode(x):
+    """4-bit code of each value (after e2m1_round): inverse of e2m1_decode; -0 keeps its sign bit."""
+    v = e2m1_round(x)
+    sign = (v < 0) | ((v == 0) & np.signbit(v))
+    a = np.abs(v)
+    _, ex = np.frexp(a)
+    e = ex.astype(np.int64) - 1
+    normal = a >= 1.0
+    E = np.where(normal, e + 1, 0)
+    M = np.where(normal, np.rint(a / np.exp2(e.astype(F64)) * 2.0 - 2.0), np.rint(a * 2.0))
+    return (np.where(sign, 0x8, 0) | (E.astype(np.int64) << 1) | M.astype(np.int64)).astype(np.uint8)
+
+
+def nvfp4_quantize(x, s):
+    """NVFP4 quantisation of x [R, K] (K a multiple of 16) with the tensor scale s (reading 9).
+
+    Returns (q, sf): q [R, K] e2m1 values and sf [R, K / 16] e4m3 block scales (float64), so
+    that the dequantised tensor is s * sf (repeated over each block) * q.  x is taken in fp32
+    first; amax / (6 s), sf * s and x / (sf s) are fp32 operations, each rounded once."""
+    x32 = np.asarray(x, dtype=np.float32)
+    R, K = x32.shape
+    assert K % NVFP4_BLOCK == 0
+    s32 = np.float32(s)
+    xb = x32.reshape(R, K // NVFP4_BLOCK, NVFP4_BLOCK)
+    amax = np.max(np.abs(xb), axis=2)
+    u = amax / (np.float32(E2M1_MAX) * s32)                     # fp32 product, fp32 quotient
+    sf = e4m3_round(u.astype(F64))
+    d = (sf.astype(np.float32) * s32)[:, :, None]                # exact e4m3 value times s, in fp32
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y = np.where(d > 0, xb / np.where(d > 0, d, np.float32(1)), np.float32(0))
+    q = e2m1_round(y.astype(F64)).reshape(R, K)
+    return q, sf
+
+
+def nvfp4_dequantize(q, sf, s):
+    """s * sf * q with each block scale spread over its 16 elements."""
+    q, sf = _f64(q), _f64(sf)
+    return F64(s) * np.repeat(sf, NVFP4_BLOCK, axis=1) * q
+
+
+def mlp_nvfp4(h, Xq, Xsf, s_x, Wq, Wsf, s_w, Wdq, Wdsf, s_wd, s_a, eps, bn):
+    """The FP8 MLP above with NVFP4 operands (reading 9).  x, W (the effective gate/up weight)
+    and W_d are given as (codes, block scales, tensor scale); r comes from the bf16 h.
+      Z = r * (x W^T);  a = silu(G) U;  amax = max |a|;  (a_q, a_sf) = nvfp4(a, s_a);
+      Y = nvfp4_dequantize(a_q, a_sf, s_a) W_d^T + h;  P = partial sums of squares of Y."""
+    r = rms_scale(h, eps)
+    Z = r[:, None] * linear(nvfp4_dequantize(Xq, Xsf, s_x), nvfp4_dequantize(Wq, Wsf, s_w))
+    F = Z.shape[1] // 2
+    a = swiglu(Z[:, :F], Z[:, F:])
+    aq, asf = nvfp4_quantize(a, s_a)
+    Y = linear(nvfp4_dequantize(aq, asf, s_a), nvfp4_dequantize(Wdq, Wdsf, s_wd)) + _f64(h)
+    return dict(r=r, Z=Z, a=a, amax=float(np.max(np.abs(a))), aq=aq, asf=asf, Y=Y, P=partial_sumsq(Y, bn))
 
 
 # ---------------------------------------------------------------------------------------

@@ -188,3 +188,51 @@ def test_fp8_backward_unquantised_e_is_caught(monkeypatch):
 
     _plant_fp8_bwd(monkeypatch, edit)
     assert _fails(pins.test_mlp_fp8_backward_quantises_like_the_library_cast)
+
+
+# ------------------------------------------------------------------ NVFP4 (reading 9)
+import tests.test_oracle_nvfp4 as fp4pins
+
+
+def test_e2m1_ties_away_is_caught(monkeypatch):
+    def away(x):
+        x = np.asarray(x, float)
+        a = np.minimum(np.abs(x), 6.0)
+        _, ex = np.frexp(a)
+        q = np.exp2(np.maximum(ex - 1.0, 0.0) - 1.0)
+        return np.copysign(np.minimum(np.floor(a / q + 0.5) * q, 6.0), x)
+
+    _plant(monkeypatch, "e2m1_round", away)
+    assert _fails(fp4pins.test_e2m1_round_is_the_nearest_value_with_ties_to_even)
+
+
+def test_nvfp4_block_of_32_is_caught(monkeypatch):
+    monkeypatch.setattr(OC, "NVFP4_BLOCK", 32)
+    assert _fails(fp4pins.test_nvfp4_blocks_are_16_consecutive_elements_of_a_row)
+
+
+def test_nvfp4_scale_from_e4m3_range_is_caught(monkeypatch):
+    # block scale amax / 448 (the e4m3 range) instead of amax / 6 (the e2m1 range)
+    def bad(x, s):
+        x32 = np.asarray(x, dtype=np.float32)
+        R, K = x32.shape
+        xb = x32.reshape(R, K // 16, 16)
+        sf = O.e4m3_round((np.max(np.abs(xb), axis=2) / (np.float32(448) * np.float32(s))).astype(float))
+        d = (sf.astype(np.float32) * np.float32(s))[:, :, None]
+        y = np.where(d > 0, xb / np.where(d > 0, d, 1), 0)
+        return O.e2m1_round(y.astype(float)).reshape(R, K), sf
+
+    _plant(monkeypatch, "nvfp4_quantize", bad)
+    assert _fails(fp4pins.test_nvfp4_exactly_representable_blocks_round_trip)
+
+
+def test_nvfp4_scales_repeated_across_rows_is_caught(monkeypatch):
+    # block scales spread along the wrong axis (a transposed scale matrix)
+    def bad(q, sf, s):
+        q, sf = np.asarray(q, float), np.asarray(sf, float)
+        R, K = q.shape
+        flat = np.repeat(sf.T.ravel(), 16)[: R * K].reshape(R, K)
+        return float(s) * flat * q
+
+    _plant(monkeypatch, "nvfp4_dequantize", bad)
+    assert _fails(fp4pins.test_block_scaled_gemm_is_the_sum_of_per_block_products)
