@@ -21,7 +21,7 @@ OUT_DIR = os.path.join(HERE, "lib")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libcoda.so")
 SOURCES = ["coda_api.cu", "coda_small.cu", "gemm_fwd.cu", "gemm_bwd.cu", "gemm_lowp.cu", "gemm_fp8_train.cu",
-           "coda_noalloc.cu"]
+           "gemm_fp4.cu", "coda_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]

@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(HERE, "lib", "libcoda.so")
 # ----------------------------------------------------------------------- constants
 OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_UNSUPPORTED_PROGRAM, ERR_LAUNCH, ERR_DEVICE_TIMEOUT, ERR_NO_DEVICE = (
     0, -1, -2, -3, -4, -5, -6, -7, -8)
-F32, BF16, E4M3 = 0, 1, 2
+F32, BF16, E4M3, NVFP4 = 0, 1, 2, 3
 ROW_MAJOR, COL_MAJOR = 0, 1
 OP_TENSOR_SCALE, OP_ROW_SCALE, OP_COL_SCALE, OP_ADD_SIDE, OP_SWIGLU, OP_ROPE = 1, 2, 3, 4, 5, 6
 OP_SWIGLU_BWD, OP_RMSBWD_COMBINE, OP_ROW_SUMSQ_PARTIAL, OP_ROW_DOT_PARTIAL = 7, 8, 9, 10
@@ -39,6 +39,7 @@ EXPORTED = [
     "coda_device_sm_count", "coda_status_string", "coda_version", "coda_block_forward_noalloc", "coda_rms_gain",
     "coda_xent_combine", "coda_lm_head_xent_forward", "coda_lm_head_xent_backward", "coda_rope_backward",
     "coda_qkv_rope_backward", "coda_mlp_fp8_backward", "coda_quantize_e4m3", "coda_set_launch_overlap",
+    "coda_quantize_nvfp4", "coda_nvfp4_scale_bytes", "coda_mlp_nvfp4",
 ]
 NOALLOC_MAX_PARTIALS = 1 << 20
 
@@ -68,13 +69,14 @@ class CodaSide(Structure):
                 ("col_scale", c_void_p), ("aux_in", POINTER(CodaTensor)), ("aux_in2", POINTER(CodaTensor)),
                 ("rope_cos", c_void_p), ("rope_sin", c_void_p), ("rope_seq_len", c_int32),
                 ("rope_head_dim", c_int32), ("rope_ncols", c_int32), ("tensor_scale", c_float),
-                ("out_scale", c_float), ("row_index", c_void_p)]
+                ("out_scale", c_float), ("row_index", c_void_p), ("a_block_scales", c_void_p),
+                ("w_block_scales", c_void_p), ("out_fp4_scale", c_float)]
 
 
 class CodaAux(Structure):
     _fields_ = [("row_partials", c_void_p), ("row_partials_ld", c_int64), ("col_partials", c_void_p),
                 ("col_partials_ld", c_int64), ("store_aux", POINTER(CodaTensor)), ("amax", c_void_p),
-                ("row_partials2", c_void_p), ("row_values", c_void_p)]
+                ("row_partials2", c_void_p), ("row_values", c_void_p), ("out_block_scales", c_void_p)]
 
 
 class CodaBlockFwd(Structure):
@@ -103,6 +105,14 @@ class CodaMlpFp8(Structure):
                 ("s_w", c_float), ("s_wd", c_float), ("s_a", c_float), ("h", c_void_p), ("X_q", c_void_p),
                 ("W_q", c_void_p), ("W_dq", c_void_p), ("r", c_void_p), ("a_q", c_void_p), ("amax", c_void_p),
                 ("Y", c_void_p), ("Y_partials", c_void_p), ("Z", c_void_p)]
+
+
+class CodaMlpNvfp4(Structure):
+    _fields_ = [("M", c_int64), ("H", c_int64), ("F", c_int64), ("eps", c_float), ("s_x", c_float),
+                ("s_w", c_float), ("s_wd", c_float), ("s_a", c_float), ("h", c_void_p), ("X_q", c_void_p),
+                ("X_sf", c_void_p), ("W_q", c_void_p), ("W_sf", c_void_p), ("W_dq", c_void_p), ("W_dsf", c_void_p),
+                ("r", c_void_p), ("a_q", c_void_p), ("a_sf", c_void_p), ("amax", c_void_p), ("Y", c_void_p),
+                ("Y_partials", c_void_p)]
 
 
 class CodaMlpFp8Bwd(Structure):
@@ -178,6 +188,8 @@ def lib():
         "coda_rope_backward": [P(CodaTensor), P(CodaTensor), c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32,
                                c_int64, P(CodaTensor), c_void_p, c_void_p],
         "coda_qkv_rope_backward": [P(CodaQkvRopeBwd), c_void_p],
+        "coda_quantize_nvfp4": [P(CodaTensor), c_float, P(CodaTensor), c_void_p, c_int64, c_void_p, c_void_p],
+        "coda_mlp_nvfp4": [P(CodaMlpNvfp4), c_void_p],
     }
     for name, args in sigs.items():
         fn = getattr(L, name)
@@ -185,6 +197,8 @@ def lib():
         fn.restype = c_int32
     L.coda_workspace_size.argtypes = [c_int32, c_int64, c_int64, c_int64]
     L.coda_workspace_size.restype = c_size_t
+    L.coda_nvfp4_scale_bytes.argtypes = [c_int64, c_int64]
+    L.coda_nvfp4_scale_bytes.restype = c_size_t
     L.coda_status_string.argtypes = [c_int32]
     L.coda_status_string.restype = c_char_p
     L.coda_version.argtypes = []
@@ -238,6 +252,36 @@ def desc(t: torch.Tensor) -> CodaTensor:
     return CodaTensor(c_void_p(t.data_ptr()), _DT[t.dtype], layout, rows, cols, ld)
 
 
+class Nvfp4:
+    """An NVFP4 tensor [R, K]: ``codes`` (uint8 [R, K / 2], two e2m1 codes per byte, element 2j
+    in the low nibble of byte j), ``scales`` (uint8, coda_nvfp4_scale_bytes(R, K) bytes in the
+    library's block-scale layout) and the fp32 tensor scale ``s``."""
+
+    def __init__(self, codes, scales, s):
+        self.codes, self.scales, self.s = codes, scales, float(s)
+
+    @property
+    def shape(self):
+        return self.codes.shape[0], 2 * self.codes.shape[1]
+
+    @staticmethod
+    def empty(R, K, s=1.0, device="cuda"):
+        return Nvfp4(torch.empty((R, K // 2), dtype=torch.uint8, device=device),
+                     torch.zeros((coda_nvfp4_scale_bytes(R, K),), dtype=torch.uint8, device=device), s)
+
+
+def desc_nvfp4(codes) -> CodaTensor:
+    """coda_tensor of NVFP4 codes held as uint8 [R, K / 2] (row-major)."""
+    if codes.dim() != 2 or codes.dtype != torch.uint8 or (codes.shape[0] > 1 and codes.stride(1) != 1):
+        raise ValueError("NVFP4 codes are a row-major uint8 [R, K / 2] tensor")
+    R, KB = codes.shape
+    return CodaTensor(c_void_p(codes.data_ptr()), NVFP4, ROW_MAJOR, R, 2 * KB, 2 * max(codes.stride(0), KB, 1))
+
+
+def _desc_any(t):
+    return desc_nvfp4(t.codes) if isinstance(t, Nvfp4) else desc(t)
+
+
 def program(*ops) -> CodaProgram:
     if len(ops) > MAX_OPS:
         raise ValueError("too many ops")
@@ -255,7 +299,8 @@ def coda_gemm_epilogue(A, W, ops, out, *, residual=None, row_scale=None, row_coe
                        store_aux=None, amax=None, row_index=None, row_partials2=None, row_values=None,
                        out_shape=None, stream=None):
     """out = epilogue(ops, A . W^T); see include/coda.h for the programs.  For XENT_PARTIAL
-    (no output tile) pass out=None and out_shape=(M, V)."""
+    (no output tile) pass out=None and out_shape=(M, V).  A, W (and a SWIGLU out) may be
+    Nvfp4 tensors: their block scales ride along, and tensor_scale carries s_A * s_W."""
     keep = []
 
     def tp(t):
@@ -265,17 +310,18 @@ def coda_gemm_epilogue(A, W, ops, out, *, residual=None, row_scale=None, row_coe
         keep.append(d)
         return ctypes.pointer(d)
 
+    sc = lambda t: _ptr(t.scales) if isinstance(t, Nvfp4) else None
     side = CodaSide(tp(residual), _ptr(row_scale), _ptr(row_coef), _ptr(col_scale), tp(aux_in), tp(aux_in2),
                     _ptr(rope_cos), _ptr(rope_sin), rope_seq_len, rope_head_dim, rope_ncols, tensor_scale, out_scale,
-                    _ptr(row_index))
+                    _ptr(row_index), sc(A), sc(W), out.s if isinstance(out, Nvfp4) else 0.0)
     aux = CodaAux(_ptr(row_partials), row_partials.stride(0) if row_partials is not None else 0,
                   _ptr(col_partials), col_partials.stride(0) if col_partials is not None else 0,
-                  tp(store_aux), _ptr(amax), _ptr(row_partials2), _ptr(row_values))
-    a, w = desc(A), desc(W)
+                  tp(store_aux), _ptr(amax), _ptr(row_partials2), _ptr(row_values), sc(out))
+    a, w = _desc_any(A), _desc_any(W)
     if out is None:
         o = CodaTensor(None, BF16, ROW_MAJOR, out_shape[0], out_shape[1], max(out_shape[1], 1))
     else:
-        o = desc(out)
+        o = _desc_any(out)
     prog = program(*ops)
     st = lib().coda_gemm_epilogue(ctypes.byref(a), ctypes.byref(w), ctypes.byref(prog), ctypes.byref(side),
                                   ctypes.byref(o), ctypes.byref(aux), _stream(stream))
@@ -418,6 +464,28 @@ def coda_mlp_fp8_backward(h, X_q, W_q, W_dq, Z, a_q, r, dY, s_x, s_w, s_wd, s_a,
                        _ptr(a_q), _ptr(r), _ptr(dY), _ptr(dY_q), _ptr(amax_dy), _ptr(e_q), _ptr(amax_e), _ptr(c),
                        _ptr(dh), _ptr(dW_d), _ptr(dW), _ptr(workspace))
     _check(lib().coda_mlp_fp8_backward(ctypes.byref(io), _stream(stream)), "coda_mlp_fp8_backward")
+
+
+def coda_nvfp4_scale_bytes(R, K):
+    return int(lib().coda_nvfp4_scale_bytes(R, K))
+
+
+def coda_quantize_nvfp4(X, Q, pair_half=0, amax=None, stream=None):
+    """Q (an Nvfp4 of X's shape, tensor scale Q.s) = NVFP4 quantisation of the bf16 tensor X."""
+    x, q = desc(X), desc_nvfp4(Q.codes)
+    _check(lib().coda_quantize_nvfp4(ctypes.byref(x), Q.s, ctypes.byref(q), _ptr(Q.scales), pair_half, _ptr(amax),
+                                     _stream(stream)), "coda_quantize_nvfp4")
+
+
+def coda_mlp_nvfp4(h, X, W, Wd, eps, r, a, amax, Y, Y_partials, stream=None):
+    """NVFP4 MLP: X, W (gate/up, scales in pair order), Wd and the output a are Nvfp4 tensors;
+    a.s is the delayed scale s_a of the SwiGLU output."""
+    M, H = h.shape
+    F = Wd.shape[1]
+    io = CodaMlpNvfp4(M, H, F, eps, X.s, W.s, Wd.s, a.s, _ptr(h), _ptr(X.codes), _ptr(X.scales), _ptr(W.codes),
+                      _ptr(W.scales), _ptr(Wd.codes), _ptr(Wd.scales), _ptr(r), _ptr(a.codes), _ptr(a.scales),
+                      _ptr(amax), _ptr(Y), _ptr(Y_partials))
+    _check(lib().coda_mlp_nvfp4(ctypes.byref(io), _stream(stream)), "coda_mlp_nvfp4")
 
 
 def coda_quantize_e4m3(X, scale, Q, amax=None, stream=None):

@@ -84,8 +84,11 @@ int ensure_device(DevState** out) {
   return CODA_OK;
 }
 
-int esize(int dt) { return dt == CODA_F32 ? 4 : dt == CODA_BF16 ? 2 : dt == CODA_E4M3 ? 1 : 0; }
-int to_dt(int dt) { return dt == CODA_F32 ? DT_F32 : dt == CODA_BF16 ? DT_BF16 : DT_E4M3; }
+// element bytes (NVFP4: 1, the byte holding two codes; sizes in bytes are halved where used)
+int esize(int dt) { return dt == CODA_F32 ? 4 : dt == CODA_BF16 ? 2 : (dt == CODA_E4M3 || dt == CODA_NVFP4) ? 1 : 0; }
+int to_dt(int dt) { return dt == CODA_F32 ? DT_F32 : dt == CODA_BF16 ? DT_BF16 : dt == CODA_NVFP4 ? DT_E2M1 : DT_E4M3; }
+// bytes of n elements along a row
+int64_t row_bytes(int dt, int64_t n) { return dt == CODA_NVFP4 ? n / 2 : n * esize(dt); }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 const int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
@@ -100,7 +103,9 @@ int check_tensor(const coda_tensor* t, bool allow_col) {
   if (!t->ptr) return CODA_ERR_NULL;
   const int64_t inner = t->layout == CODA_ROW_MAJOR ? t->cols : t->rows;
   if (t->ld < inner || t->ld < 1) return CODA_ERR_SHAPE;
-  if (!aligned16(t->ptr) || (t->ld * esize(t->dtype)) % 16 != 0) return CODA_ERR_ALIGN;
+  if (t->dtype == CODA_NVFP4 && (t->layout != CODA_ROW_MAJOR || t->cols % 2 != 0 || t->ld % 2 != 0))
+    return CODA_ERR_SHAPE;
+  if (!aligned16(t->ptr) || row_bytes(t->dtype, t->ld) % 16 != 0) return CODA_ERR_ALIGN;
   return CODA_OK;
 }
 
@@ -138,6 +143,18 @@ int encode_pair(CUtensorMap* m, int dtype, const void* ptr, int64_t half, int64_
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, t, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CODA_OK : CODA_ERR_LAUNCH;
+}
+
+// Map over NVFP4 block-scale atoms: n_atoms rows of 512 bytes (128 uint32), box of 4 atoms.
+int encode_atoms(CUtensorMap* m, const void* ptr, int64_t n_atoms) {
+  cuuint64_t dims[2] = {128, (cuuint64_t)(n_atoms > 0 ? n_atoms : 1)};
+  cuuint64_t strides[1] = {512};
+  cuuint32_t box[2] = {128, 4};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? CODA_OK : CODA_ERR_LAUNCH;
 }
 
@@ -220,9 +237,10 @@ std::atomic<int> g_launch_overlap = [] {
 }();
 
 const VariantEntry* find_variant(const VariantKey& k) {
-  const VariantEntry* tables[4] = {g_variants_fwd, g_variants_bwd, g_variants_lowp, g_variants_fp8};
-  const int counts[4] = {g_num_variants_fwd, g_num_variants_bwd, g_num_variants_lowp, g_num_variants_fp8};
-  for (int t = 0; t < 4; ++t)
+  const VariantEntry* tables[5] = {g_variants_fwd, g_variants_bwd, g_variants_lowp, g_variants_fp8, g_variants_fp4};
+  const int counts[5] = {g_num_variants_fwd, g_num_variants_bwd, g_num_variants_lowp, g_num_variants_fp8,
+                         g_num_variants_fp4};
+  for (int t = 0; t < 5; ++t)
     for (int i = 0; i < counts[t]; ++i) {
       const VariantKey& v = tables[t][i].key;
       if (v.kind == k.kind && v.epi == k.epi && v.a_mn == k.a_mn && v.b_mn == k.b_mn && v.out_dt == k.out_dt &&
@@ -321,7 +339,11 @@ static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const 
 
   // operand kind
   if (A->dtype != W->dtype) return CODA_ERR_DTYPE;
-  const int kind = A->dtype == CODA_BF16 ? KIND_BF16 : A->dtype == CODA_F32 ? KIND_TF32 : KIND_E4M3;
+  const int kind = A->dtype == CODA_BF16   ? KIND_BF16
+                   : A->dtype == CODA_F32  ? KIND_TF32
+                   : A->dtype == CODA_NVFP4 ? KIND_NVFP4
+                                            : KIND_E4M3;
+  const bool fp4 = kind == KIND_NVFP4;
   const bool a_mn = A->layout == CODA_COL_MAJOR, b_mn = W->layout == CODA_COL_MAJOR;
 
   const int64_t M = A->rows, K = A->cols;
@@ -341,6 +363,7 @@ static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const 
   if (N % 32 != 0) return CODA_ERR_SHAPE;
   if (M == 0 || N == 0) return CODA_OK;
   if (K < 1) return CODA_ERR_SHAPE;
+  if (fp4 && K % 256 != 0) return CODA_ERR_SHAPE;
 
   // side inputs and aux outputs the program needs
   const coda_side_inputs zero_side{};
@@ -390,8 +413,6 @@ static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const 
     if (epi == EPI_XENT && ax.row_partials_ld < M) return CODA_ERR_SHAPE;
     if (epi == EPI_XENT_BWD && !sd.row_coef) return CODA_ERR_NULL;
   }
-  const int bn_out = epi == EPI_SWIGLU ? 128 : 256;
-  const int64_t n_tiles = (N + bn_out - 1) / bn_out;
   if (has(CODA_OP_ROW_SUMSQ_PARTIAL) || has(CODA_OP_ROW_DOT_PARTIAL)) {
     if (!ax.row_partials) return CODA_ERR_NULL;
     if (ax.row_partials_ld < M) return CODA_ERR_SHAPE;
@@ -409,6 +430,16 @@ static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const 
     if (!aligned16(sd.rope_cos) || !aligned16(sd.rope_sin)) return CODA_ERR_ALIGN;
   }
   if (out->dtype == CODA_E4M3 && epi != EPI_SWIGLU && epi != EPI_SWIGLU_BWD) return CODA_ERR_DTYPE;
+  if (out->dtype == CODA_NVFP4) {   // the NVFP4 SwiGLU output: codes, block scales, tensor scale
+    if (!fp4 || epi != EPI_SWIGLU) return CODA_ERR_DTYPE;
+    if (!ax.out_block_scales) return CODA_ERR_NULL;
+    if (!aligned16(ax.out_block_scales)) return CODA_ERR_ALIGN;
+    if (!(sd.out_fp4_scale > 0.f) || !(sd.out_fp4_scale < INFINITY)) return CODA_ERR_SHAPE;
+  }
+  if (fp4) {
+    if (!sd.a_block_scales || !sd.w_block_scales) return CODA_ERR_NULL;
+    if (!aligned16(sd.a_block_scales) || !aligned16(sd.w_block_scales)) return CODA_ERR_ALIGN;
+  }
   if (epi == EPI_SWIGLU_BWD && has(CODA_OP_AMAX) && out->dtype != CODA_E4M3) return CODA_ERR_UNSUPPORTED_PROGRAM;
   if (out->dtype == CODA_E4M3 && !(sd.out_scale > 0.f)) return CODA_ERR_SHAPE;   // 1 / scale of the codes
 
@@ -417,6 +448,7 @@ static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const 
   if (!var) return CODA_ERR_DTYPE;
   const int64_t tile_rows = (int64_t)BM * var->cg;
   const int64_t m_tiles = (M + tile_rows - 1) / tile_rows;
+  const int64_t n_tiles = (N + var->bn_out - 1) / var->bn_out;
 
   DevState* d;
   if ((st = ensure_device(&d)) != CODA_OK) return st;
@@ -425,19 +457,32 @@ static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const 
   std::memset(&L, 0, sizeof(L));
   const int op_bytes = esize(A->dtype);
   const uint32_t bk = (uint32_t)(128 / op_bytes);
-  // A: K-major box {bk, 128}; MN-major (stored [K][M]) box {128 bytes of M, bk}
+  // A: K-major box {bk, 128}; MN-major (stored [K][M]) box {128 bytes of M, bk}.  NVFP4
+  // operands are mapped as bytes (two codes each): box {128 bytes, rows}.
   const uint32_t mn_atom = (uint32_t)(128 / op_bytes);
-  if (a_mn)
+  if (fp4)
+    st = encode_2d(&L.tmA, CODA_E4M3, A->ptr, K / 2, M, A->ld / 2, 128, 128);
+  else if (a_mn)
     st = encode_2d(&L.tmA, A->dtype, A->ptr, M, K, A->ld, mn_atom, bk);
   else
     st = encode_2d(&L.tmA, A->dtype, A->ptr, K, M, A->ld, bk, 128);
   if (st != CODA_OK) return st;
-  if (b_mn)
+  if (fp4)
+    st = encode_2d(&L.tmB, CODA_E4M3, W->ptr, K / 2, W->rows, W->ld / 2, 128, (uint32_t)var->b_box);
+  else if (b_mn)
     st = encode_2d(&L.tmB, W->dtype, W->ptr, W->rows, K, W->ld, mn_atom, bk);
   else
-    st = encode_2d(&L.tmB, W->dtype, W->ptr, K, W->rows, W->ld, bk, 128);
+    st = encode_2d(&L.tmB, W->dtype, W->ptr, K, W->rows, W->ld, bk, (uint32_t)var->b_box);
   if (st != CODA_OK) return st;
-  if (epi == EPI_SWIGLU_BWD) {
+  if (fp4) {
+    // block scales: rows of 512-byte atoms (as 128 uint32), 4 atoms (one stage) per copy
+    const int64_t kc = K / 64;
+    if ((st = encode_atoms(&L.tmSFA, sd.a_block_scales, (M + 127) / 128 * kc)) != CODA_OK) return st;
+    if ((st = encode_atoms(&L.tmSFB, sd.w_block_scales, (W->rows + 127) / 128 * kc)) != CODA_OK) return st;
+  }
+  if (out->dtype == CODA_NVFP4) {
+    if ((st = encode_2d(&L.tmOut, CODA_E4M3, out->ptr, N / 2, M, out->ld / 2, 16, 32)) != CODA_OK) return st;
+  } else if (epi == EPI_SWIGLU_BWD) {
     if ((st = encode_pair(&L.tmOut, out->dtype, out->ptr, N, M, out->ld)) != CODA_OK) return st;   // e: both halves
   } else if (epi != EPI_XENT &&
              (st = encode_2d(&L.tmOut, out->dtype, out->ptr, out->cols, M, out->ld, 32, 32)) != CODA_OK) {
@@ -477,7 +522,7 @@ static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const 
     // fit, no slice stays resident anyway; the groups working at the same time then read the
     // least from DRAM with a near-square footprint (as many N-tiles as M-tiles), since each
     // distinct A row-block and B column-block they touch is fetched once per wave.
-    const int64_t b_tile_bytes = (int64_t)UMMA_N * K * esize(W->dtype);
+    const int64_t b_tile_bytes = (int64_t)var->un * row_bytes(W->dtype, K);
     int64_t gn = ((int64_t)32 << 20) / (b_tile_bytes > 0 ? b_tile_bytes : 1);
     int64_t square = 1;
     while ((square + 1) * (square + 1) <= d->sms / var->cg) ++square;
@@ -491,7 +536,7 @@ static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const 
   {
     const int64_t tiles = m_tiles * n_tiles;
     const int64_t groups = d->sms / var->cg;
-    const int64_t num_kb = (K + (128 / op_bytes) - 1) / (128 / op_bytes);
+    const int64_t num_kb = (K + var->bk - 1) / var->bk;
     int best = 1;
     double best_score = 0.0;
     // split only when a single pass leaves more than a quarter of the groups idle: the memset
@@ -544,6 +589,9 @@ static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const 
   p.row_out = ax.row_values;
   p.row_index = sd.row_index;
   p.amax = reinterpret_cast<unsigned int*>(ax.amax);
+  p.fp4_scale = out->dtype == CODA_NVFP4 ? sd.out_fp4_scale : 1.0f;
+  p.out_sf = reinterpret_cast<uint8_t*>(ax.out_block_scales);
+  p.out_sf_kc = N / 64;
   p.status = d->status;
   p.timeout_ns = (unsigned long long)g_watchdog_ms * 1000000ull;
   L.sms = d->sms;
@@ -599,6 +647,31 @@ int coda_quantize_e4m3(const coda_tensor* X, float scale, const coda_tensor* Q, 
   if ((st = ensure_device(&dv)) != CODA_OK) return st;
   cudaError_t e = launch_quantize_e4m3(X->ptr, X->rows, X->cols, X->ld, 1.0f / scale, Q->ptr, Q->ld, amax,
                                        static_cast<cudaStream_t>(stream), dv->sms);
+  return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
+}
+
+size_t coda_nvfp4_scale_bytes(int64_t R, int64_t K) {
+  if (R <= 0 || K <= 0) return 0;
+  return (size_t)((R + 127) / 128) * (size_t)(K / 64) * 512u;
+}
+
+int coda_quantize_nvfp4(const coda_tensor* X, float s, const coda_tensor* Q, void* block_scales, int64_t pair_half,
+                        float* amax, void* stream) {
+  int st;
+  if ((st = check_tensor(X, false)) != CODA_OK) return st;
+  if ((st = check_tensor(Q, false)) != CODA_OK) return st;
+  if (X->dtype != CODA_BF16 || Q->dtype != CODA_NVFP4) return CODA_ERR_DTYPE;
+  if (Q->rows != X->rows || Q->cols != X->cols || X->cols % 64 != 0) return CODA_ERR_SHAPE;
+  if (!(s > 0.f) || !(s < INFINITY)) return CODA_ERR_SHAPE;
+  if (pair_half < 0 || (pair_half > 0 && (pair_half % 64 != 0 || X->rows != 2 * pair_half))) return CODA_ERR_SHAPE;
+  if (X->rows == 0 || X->cols == 0) return CODA_OK;
+  if (!block_scales) return CODA_ERR_NULL;
+  if (!aligned16(block_scales)) return CODA_ERR_ALIGN;
+  DevState* dv;
+  if ((st = ensure_device(&dv)) != CODA_OK) return st;
+  cudaError_t e = launch_quantize_nvfp4(X->ptr, X->rows, X->cols, X->ld, s, Q->ptr, Q->ld / 2,
+                                        static_cast<uint8_t*>(block_scales), pair_half, amax,
+                                        static_cast<cudaStream_t>(stream), dv->sms);
   return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
 }
 
@@ -1061,6 +1134,53 @@ int coda_mlp_fp8(const coda_mlp_fp8_io* io, void* stream) {
     coda_side_inputs sd{};
     sd.tensor_scale = io->s_a * io->s_wd;
     sd.residual = &h;
+    coda_aux_outputs ax{};
+    ax.row_partials = io->Y_partials;
+    ax.row_partials_ld = M;
+    if ((st = coda_gemm_epilogue(&A, &W, &pg, &sd, &out, &ax, stream)) != CODA_OK) return st;
+  }
+  return CODA_OK;
+}
+
+int coda_mlp_nvfp4(const coda_mlp_nvfp4_io* io, void* stream) {
+  if (!io) return CODA_ERR_NULL;
+  if (!io->h || !io->X_q || !io->X_sf || !io->W_q || !io->W_sf || !io->W_dq || !io->W_dsf || !io->r || !io->a_q ||
+      !io->a_sf || !io->amax || !io->Y || !io->Y_partials)
+    return CODA_ERR_NULL;
+  const int64_t M = io->M, H = io->H, F = io->F;
+  if (M < 0 || H < 256 || F < 256 || H % 256 != 0 || F % 256 != 0) return CODA_ERR_SHAPE;
+  if (!(io->s_a > 0.f)) return CODA_ERR_SHAPE;
+  if (M == 0) return CODA_OK;
+  int st;
+  coda_tensor h = mk(io->h, CODA_BF16, M, H, H);
+  if (cudaMemsetAsync(io->amax, 0, sizeof(float), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return CODA_ERR_LAUNCH;
+  if ((st = coda_row_rms(&h, io->eps, io->r, stream)) != CODA_OK) return st;
+  {
+    coda_tensor A = mk(io->X_q, CODA_NVFP4, M, H, H), W = mk(io->W_q, CODA_NVFP4, 2 * F, H, H);
+    coda_tensor out = mk(io->a_q, CODA_NVFP4, M, F, F);
+    coda_epilogue_program pg =
+        prog_of({CODA_OP_TENSOR_SCALE, CODA_OP_ROW_SCALE, CODA_OP_SWIGLU, CODA_OP_AMAX});
+    coda_side_inputs sd{};
+    sd.tensor_scale = io->s_x * io->s_w;
+    sd.row_scale = io->r;
+    sd.a_block_scales = io->X_sf;
+    sd.w_block_scales = io->W_sf;
+    sd.out_fp4_scale = io->s_a;
+    coda_aux_outputs ax{};
+    ax.amax = io->amax;
+    ax.out_block_scales = io->a_sf;
+    if ((st = gemm_epilogue_impl(&A, &W, &pg, &sd, &out, &ax, stream, true)) != CODA_OK) return st;
+  }
+  {
+    coda_tensor A = mk(io->a_q, CODA_NVFP4, M, F, F), W = mk(io->W_dq, CODA_NVFP4, H, F, F);
+    coda_tensor out = mk(io->Y, CODA_BF16, M, H, H);
+    coda_epilogue_program pg = prog_of({CODA_OP_TENSOR_SCALE, CODA_OP_ADD_SIDE, CODA_OP_ROW_SUMSQ_PARTIAL});
+    coda_side_inputs sd{};
+    sd.tensor_scale = io->s_a * io->s_wd;
+    sd.residual = &h;
+    sd.a_block_scales = io->a_sf;
+    sd.w_block_scales = io->W_dsf;
     coda_aux_outputs ax{};
     ax.row_partials = io->Y_partials;
     ax.row_partials_ld = M;

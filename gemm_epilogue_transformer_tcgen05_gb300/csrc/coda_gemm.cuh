@@ -42,7 +42,7 @@ namespace coda {
 
 // ----------------------------------------------------------------------- constants
 constexpr int BM = 128;                               // tile rows = TMEM lanes
-constexpr int UMMA_N = 256;                           // MMA N = B tile rows
+constexpr int UMMA_N = 256;                           // MMA N = B tile rows (NVFP4: 128, see GemmCfg)
 constexpr int BK_BYTES = 128;                         // K bytes per stage (one 128B swizzle row)
 constexpr int KSTEPS = 4;                             // MMAs per stage, 32 bytes of K each
 constexpr int A_STAGE_BYTES = BM * BK_BYTES;          // 16 KB: this CTA's 128 rows of A
@@ -51,10 +51,23 @@ constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int MAX_SMEM = 232448;                      // 227 KB opt-in per CTA
 
-enum : int { DT_F32 = 0, DT_BF16 = 1, DT_E4M3 = 2 };
+enum : int { DT_F32 = 0, DT_BF16 = 1, DT_E4M3 = 2, DT_E2M1 = 3 };
 __host__ __device__ constexpr int dt_bytes(int dt) { return dt == DT_F32 ? 4 : dt == DT_BF16 ? 2 : 1; }
+// bytes of one 32 x 32 staging block (e2m1: two codes per byte)
+__host__ __device__ constexpr int slot_bytes(int dt) { return dt == DT_E2M1 ? 512 : 32 * 32 * dt_bytes(dt); }
 
-enum : int { KIND_BF16 = 0, KIND_TF32 = 1, KIND_E4M3 = 2 };
+// KIND_NVFP4: e2m1 operands packed two per byte along K, one ue4m3 scale per 16 K elements
+// (block-scaled MMA, scales staged through TMEM), fp32 tensor scales in the epilogue.
+enum : int { KIND_BF16 = 0, KIND_TF32 = 1, KIND_E4M3 = 2, KIND_NVFP4 = 3 };
+
+// NVFP4 block scales in memory: atoms of 128 rows x 4 blocks of 16 K elements (512 bytes).
+// Atom (row / 128, kb / 4) sits at ((row / 128) * kc + kb / 4) * 512, kc = K / 64 atoms per
+// 128-row block; inside an atom, row r is at byte 16 (r % 32) + 4 ((r % 128) / 32) and block
+// kb at + kb % 4.  A 32-lane TMEM copy of an atom's 32 16-byte rows, repeated into the four
+// lane quarters, puts row r's scales in lane r % 32 (+ 32 q) of column (r % 128) / 32.
+__host__ __device__ constexpr long long sf_offset(long long row, long long kb, long long kc) {
+  return ((row / 128) * kc + kb / 4) * 512 + 16 * (row % 32) + 4 * ((row % 128) / 32) + kb % 4;
+}
 
 // Compiled epilogue programs (the host maps an op list onto one of these).
 enum : int {
@@ -120,6 +133,9 @@ struct GemmParams {
   float* col_part;        // [4 * m_tiles, col_part_ld]
   long long col_part_ld;
   unsigned int* amax;     // fp32 bits, atomic max (non-negative values order as integers)
+  float fp4_scale;        // NVFP4 output: tensor scale s of the codes
+  uint8_t* out_sf;        // NVFP4 output: block scales (atom layout, kc = out_sf_kc)
+  long long out_sf_kc;
   int* status;
   unsigned long long timeout_ns;
 };
@@ -127,23 +143,33 @@ struct GemmParams {
 // CG = CTAs per MMA: 1, or 2 for a CTA pair (cluster of two) issuing cta_group::2 MMAs of
 // 256 x 256: each CTA holds 128 rows of A and 128 rows (N) of B per stage and receives its
 // 128 accumulator rows in its own TMEM.
-template <int KIND_, int EPI_, bool A_MN_, bool B_MN_, int OUT_DT_, int SIDE_DT_, bool AUX_, int CG_ = 2>
+// UN = MMA N (B rows of a tile).  256 fills TMEM with the two accumulators; NVFP4 tiles use
+// 128 so that the block scales of the pipeline stages fit in TMEM beside them.
+template <int KIND_, int EPI_, bool A_MN_, bool B_MN_, int OUT_DT_, int SIDE_DT_, bool AUX_, int CG_ = 2,
+          int UN_ = UMMA_N>
 struct GemmCfg {
-  static constexpr int KIND = KIND_, EPI = EPI_, OUT_DT = OUT_DT_, SIDE_DT = SIDE_DT_, CG = CG_;
+  static constexpr int KIND = KIND_, EPI = EPI_, OUT_DT = OUT_DT_, SIDE_DT = SIDE_DT_, CG = CG_, UN = UN_;
   static constexpr bool A_MN = A_MN_, B_MN = B_MN_, AUX = AUX_;
-  static constexpr int B_ROWS = UMMA_N / CG;                   // B rows (N) held by this CTA
+  static constexpr bool FP4 = KIND == KIND_NVFP4;
+  static constexpr int B_ROWS = UN / CG;                       // B rows (N) held by this CTA
+  static constexpr int B_BOX = B_ROWS < 128 ? B_ROWS : 128;    // rows per B copy
   static constexpr int B_STAGE_BYTES = B_ROWS * BK_BYTES;
-  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+  // NVFP4 block scales of a stage: one atom per MMA for this CTA's 128 rows of A, and one per
+  // MMA and 128 rows of the tile's N for B (each CTA of a pair holds all of them)
+  static constexpr int SF_A_BYTES = FP4 ? KSTEPS * 512 : 0;
+  static constexpr int SF_B_BYTES = FP4 ? KSTEPS * 512 * (UN / 128) : 0;
+  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES + SF_A_BYTES + SF_B_BYTES;
   static constexpr int PAIR_ROWS = BM * CG;                    // output rows per tile
   static constexpr int OP_BYTES = KIND == KIND_TF32 ? 4 : KIND == KIND_BF16 ? 2 : 1;
-  static constexpr int BK = BK_BYTES / OP_BYTES;   // K elements per stage
+  static constexpr int BK = FP4 ? 2 * BK_BYTES : BK_BYTES / OP_BYTES;   // K elements per stage
+  static constexpr int K_COORD = FP4 ? BK_BYTES : BK;   // TMA K step per stage (NVFP4 maps count bytes)
   static constexpr bool DUAL = EPI == EPI_SWIGLU;
-  static constexpr int BN_OUT = DUAL ? 128 : 256;  // output columns per tile
+  static constexpr int BN_OUT = DUAL ? UN / 2 : UN;  // output columns per tile
   static constexpr int NCHUNK = BN_OUT / 32;
   static constexpr int NS = EPI == EPI_RESID ? 1 : (EPI == EPI_SWIGLU_BWD || EPI == EPI_RMSBWD) ? 2 : 0;
   static constexpr int NO = EPI == EPI_SWIGLU_BWD ? 2 : EPI == EPI_XENT ? 0 : 1;   // XENT stores no tile
-  static constexpr int OSLOT = 32 * 32 * dt_bytes(OUT_DT);  // one 32 x 32 staging block
-  static constexpr int SSLOT = 32 * 32 * dt_bytes(SIDE_DT);
+  static constexpr int OSLOT = slot_bytes(OUT_DT);  // one 32 x 32 staging block
+  static constexpr int SSLOT = slot_bytes(SIDE_DT);
   static constexpr int XSLOT = 32 * 32 * 2;                 // aux output block (bf16)
   static constexpr int NX = AUX ? (EPI == EPI_SWIGLU ? 2 : 1) : 0;   // SwiGLU: G and U; residual: h * g
   static constexpr int OUTSET = NO * OSLOT + NX * XSLOT;
@@ -162,7 +188,15 @@ struct GemmCfg {
   static constexpr int EPI_BYTES = NUM_EPI_WARPS * EPI_WARP_BYTES;
   static constexpr int BAR_BYTES = 320;
   static constexpr int STAGES_FIT = (MAX_SMEM - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
+  static constexpr int MAX_STAGES = FP4 ? 8 : 6;
+  static constexpr int STAGES = STAGES_FIT > MAX_STAGES ? MAX_STAGES : STAGES_FIT;
+  // TMEM: two accumulators of UN columns, then (NVFP4) each stage's block scales, 4 columns
+  // per atom
+  static constexpr int SF_COLS = (SF_A_BYTES + SF_B_BYTES) / 128;
+  static_assert(2 * UN + STAGES * SF_COLS <= TMEM_COLS, "TMEM columns");
+  static_assert(UN % 128 == 0 && UN <= UMMA_N && B_ROWS % B_BOX == 0, "MMA N");
+  static_assert(!FP4 || (!A_MN && !B_MN && !AUX), "NVFP4 operands are K-major");
+  static_assert(OUT_DT != DT_E2M1 || (FP4 && EPI == EPI_SWIGLU), "e2m1 output: NVFP4 SwiGLU");
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(STAGES >= 2, "shared memory budget");
   static_assert(8 * (2 * STAGES + 5 + NSS * NUM_EPI_WARPS) + 8 <= BAR_BYTES, "barrier area");
@@ -174,10 +208,12 @@ struct GemmCfg {
   static constexpr int UMMA_K = 32 / OP_BYTES;
   static_assert(!AUX || EPI == EPI_SWIGLU || EPI == EPI_RESID, "aux output: SwiGLU or residual programs");
   static_assert(CG == 1 || CG == 2, "CTA group");
-  // instruction descriptor: D f32, A/B format, operand majors, N >> 3, M >> 4
-  static constexpr uint32_t FMT = KIND == KIND_BF16 ? 1u : KIND == KIND_TF32 ? 2u : 0u;
-  static constexpr uint32_t IDESC = (1u << 4) | (FMT << 7) | (FMT << 10) | ((A_MN ? 1u : 0u) << 15) |
-                                    ((B_MN ? 1u : 0u) << 16) | ((uint32_t)(UMMA_N >> 3) << 17) |
+  // instruction descriptor: D f32, A/B format, operand majors, N >> 3, M >> 4.  Block-scaled
+  // (NVFP4): bits 4-5 and 29-30 select the scale columns' byte (0: all four used by a 4X
+  // vector), the formats are e2m1 (1), bit 23 = 0 selects ue4m3 scales, and D is f32.
+  static constexpr uint32_t FMT = KIND == KIND_BF16 ? 1u : KIND == KIND_TF32 ? 2u : KIND == KIND_NVFP4 ? 1u : 0u;
+  static constexpr uint32_t IDESC = (FP4 ? 0u : 1u << 4) | (FMT << 7) | (FMT << 10) | ((A_MN ? 1u : 0u) << 15) |
+                                    ((B_MN ? 1u : 0u) << 16) | ((uint32_t)(UN >> 3) << 17) |
                                     ((uint32_t)(PAIR_ROWS >> 4) << 24);
 };
 
@@ -185,6 +221,11 @@ struct GemmCfg {
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// The same without swizzle: 8-row groups of 16-byte rows, SBO bytes apart (NVFP4 scale atoms).
+__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
 }
 
 // Tile order.  Tiles come in groups of group_n consecutive N-tiles; inside a group the
@@ -344,6 +385,27 @@ __device__ __forceinline__ float warp_transpose_sum(float (&x)[32], int lane) {
 }
 
 __device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+
+// NVFP4 quantisation of one block of 16 values with tensor scale s: sf = e4m3(amax / (6 s)),
+// q = e2m1(x / (sf s)) (all zero when sf is 0), each quotient and product rounded once in
+// fp32.  q[0..1] receive the 16 codes (element 2j in the low nibble of byte j); returns the
+// scale's e4m3 byte.  The quantiser kernel and the SwiGLU epilogue both decide through here.
+__device__ __forceinline__ uint32_t nvfp4_block16(const float* x, float s, uint32_t* q) {
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(x[j]));
+  const float u = __fdiv_rn(amax, __fmul_rn(6.0f, s));
+  const uint16_t code2 = ptx::cvt_e4m3x2(u, 0.0f);   // low byte: e4m3(u), saturating at 448
+  float sfv, zero;
+  ptx::e4m3x2_to_f32(code2, sfv, zero);
+  const float d = __fmul_rn(sfv, s);
+  float y[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) y[j] = d > 0.f ? __fdiv_rn(x[j], d) : 0.f;
+  q[0] = ptx::cvt_e2m1x8(y);
+  q[1] = ptx::cvt_e2m1x8(y + 8);
+  return code2 & 0xFFu;
+}
 __device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 // =====================================================================================
@@ -352,6 +414,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmSide0,
                          const __grid_constant__ CUtensorMap tmSide1, const __grid_constant__ CUtensorMap tmAux,
+                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                          const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -395,6 +458,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
+    if constexpr (C::FP4) {
+      ptx::prefetch_tmap(&tmSFA);
+      ptx::prefetch_tmap(&tmSFB);
+    }
   }
   if (warp == 1) {
     ptx::tmem_alloc<C::CG>(ptx::smem_u32(const_cast<uint32_t*>(tmem_holder)), TMEM_COLS);
@@ -447,7 +514,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t fb = FULL_BAR(stage);
             const uint32_t sa = sm_stage + stage * C::STAGE_BYTES;
             const uint32_t sb = sa + A_STAGE_BYTES;
-            const int k0 = kb * C::BK;
+            const int k0 = kb * C::K_COORD;
             // the leader's full barrier counts the bytes of both CTAs of a pair
             if (leader) ptx::mbar_arrive_expect_tx(fb, C::CG * C::STAGE_BYTES);
             auto load = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1, uint64_t pol) {
@@ -463,19 +530,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             } else {
               load(sa, &tmA, k0, m0, normal);
             }
-            // B: this CTA's B_ROWS rows of the tile's 256 (SwiGLU: gate rows, then up rows)
+            // B: this CTA's B_ROWS rows of the tile's UN (SwiGLU: UN / 2 gate rows, then up rows)
             if constexpr (C::B_MN) {
-              const int n0 = nb * UMMA_N + (int)rank * C::B_ROWS;
+              const int n0 = nb * C::UN + (int)rank * C::B_ROWS;
 #pragma unroll
               for (int j = 0; j < C::B_ROWS / C::MN_ATOM; ++j)
                 load(sb + C::MN_ATOM_BYTES * j, &tmB, n0 + C::MN_ATOM * j, k0, keep);
             } else {
+              constexpr int HALF = C::UN / 2;
 #pragma unroll
-              for (int h = 0; h < C::B_ROWS / 128; ++h) {
-                const int half = (int)rank * (C::B_ROWS / 128) + h;   // 0 or 1 of the tile's two halves
-                const int row = C::DUAL ? (half == 0 ? nb * 128 : p.up_offset + nb * 128) : nb * UMMA_N + half * 128;
-                load(sb + 16384 * h, &tmB, k0, row, keep);
+              for (int h = 0; h < C::B_ROWS / C::B_BOX; ++h) {
+                const int off = ((int)rank * (C::B_ROWS / C::B_BOX) + h) * C::B_BOX;   // row offset in the tile
+                const int row = C::DUAL ? (off < HALF ? nb * HALF + off : p.up_offset + nb * HALF + off - HALF)
+                                        : nb * C::UN + off;
+                load(sb + C::B_BOX * BK_BYTES * h, &tmB, k0, row, keep);
               }
+            }
+            if constexpr (C::FP4) {
+              // block scales: KSTEPS atoms (one per MMA) for this CTA's A rows, then for each 128
+              // rows of the tile's N; an atom row of the maps is one 512-byte atom
+              const uint32_t ssf = sb + C::B_STAGE_BYTES;
+              const int kc = p.K / 64;
+              load(ssf, &tmSFA, 0, (m0 / 128) * kc + KSTEPS * kb, normal);
+#pragma unroll
+              for (int j = 0; j < C::UN / 128; ++j)
+                load(ssf + C::SF_A_BYTES + KSTEPS * 512 * j, &tmSFB, 0, (nb * (C::UN / 128) + j) * kc + KSTEPS * kb,
+                     keep);
             }
             issued_any |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -507,7 +587,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * UMMA_N;
+        const uint32_t d_tmem = tmem_base + acc * C::UN;
         int mb_, nb_, kb0, kb1;
         work_coords(tile, p, mb_, nb_, kb0, kb1, num_kb);
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -518,13 +598,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ptx::tc_fence_after();
           const uint32_t sa = sm_stage + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + A_STAGE_BYTES;
+          if constexpr (C::FP4) {
+            // this stage's block scales into its TMEM columns (A: 4 per MMA; B: 4 per MMA and
+            // 128 rows of N), then the block-scaled MMAs; the copies and the MMAs run in issue order
+            const uint32_t ssf = sb + C::B_STAGE_BYTES;
+            const uint32_t tsa = tmem_base + 2 * C::UN + stage * C::SF_COLS;
+            const uint32_t tsb = tsa + 4 * KSTEPS;
+            constexpr int NB128 = C::UN / 128;
 #pragma unroll
-          for (int k = 0; k < KSTEPS; ++k) {
-            const uint64_t ad = C::A_MN ? smem_desc(sa + k * C::UMMA_K * 128, C::MN_ATOM_BYTES, 1024)
-                                        : smem_desc(sa + k * 32, 16, 1024);
-            const uint64_t bd = C::B_MN ? smem_desc(sb + k * C::UMMA_K * 128, C::MN_ATOM_BYTES, 1024)
-                                        : smem_desc(sb + k * 32, 16, 1024);
-            ptx::umma<C::KIND, C::CG>(d_tmem, ad, bd, C::IDESC, (kb != kb0 || k != 0) ? 1u : 0u);
+            for (int k = 0; k < KSTEPS; ++k) {
+              ptx::tmem_cp_32x128b_x4<C::CG>(tsa + 4 * k, smem_desc_plain(ssf + 512 * k, 128, 128));
+#pragma unroll
+              for (int j = 0; j < NB128; ++j)
+                ptx::tmem_cp_32x128b_x4<C::CG>(tsb + 4 * (NB128 * k + j),
+                                               smem_desc_plain(ssf + C::SF_A_BYTES + KSTEPS * 512 * j + 512 * k, 128, 128));
+            }
+#pragma unroll
+            for (int k = 0; k < KSTEPS; ++k) {
+              const uint64_t ad = smem_desc(sa + k * 32, 16, 1024);
+              const uint64_t bd = smem_desc(sb + k * 32, 16, 1024);
+              ptx::umma_nvfp4<C::CG>(d_tmem, ad, bd, C::IDESC, tsa + 4 * k, tsb + 4 * NB128 * k,
+                                     (kb != kb0 || k != 0) ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < KSTEPS; ++k) {
+              const uint64_t ad = C::A_MN ? smem_desc(sa + k * C::UMMA_K * 128, C::MN_ATOM_BYTES, 1024)
+                                          : smem_desc(sa + k * 32, 16, 1024);
+              const uint64_t bd = C::B_MN ? smem_desc(sb + k * C::UMMA_K * 128, C::MN_ATOM_BYTES, 1024)
+                                          : smem_desc(sb + k * 32, 16, 1024);
+              ptx::umma<C::KIND, C::CG>(d_tmem, ad, bd, C::IDESC, (kb != kb0 || k != 0) ? 1u : 0u);
+            }
           }
           ptx::umma_commit<C::CG>(EMPTY_BAR(stage));  // frees the stage (in both CTAs) once done
           if (++stage == C::STAGES) {
@@ -627,7 +731,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
-      const uint32_t tacc = tmem_base + ((uint32_t)(32 * q) << 16) + acc * UMMA_N;
+      const uint32_t tacc = tmem_base + ((uint32_t)(32 * q) << 16) + acc * C::UN;
       float rowacc = 0.f;
 
 #pragma unroll 1
@@ -639,7 +743,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ptx::tmem_ld32(tacc + 32 * c, v);
           if constexpr (C::DUAL) {
             uint32_t u[32];
-            ptx::tmem_ld32(tacc + 128 + 32 * c, u);
+            ptx::tmem_ld32(tacc + C::UN / 2 + 32 * c, u);
             ptx::tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; ++j) xu[j] = __uint_as_float(u[j]);
@@ -708,6 +812,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float o1[C::NO > 1 ? 32 : 1];
         constexpr bool CODES = C::EPI == EPI_SWIGLU_BWD && C::OUT_DT == DT_E4M3;   // e quantised in place
         uint16_t qg[CODES ? 16 : 1], qu[CODES ? 16 : 1];
+        constexpr bool FP4_OUT = C::OUT_DT == DT_E2M1;   // NVFP4 codes + block scales of the SwiGLU output
+        uint32_t q4[FP4_OUT ? 4 : 1];
+        uint32_t sfc = 0;
         float zg[C::AUX ? 32 : 1], zu[C::NX > 1 ? 32 : 1];
 
         // ---------------------------------------------------------------- the program
@@ -761,6 +868,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const float a = silu_f(G) * U;
             amax_local = fmaxf(amax_local, fabsf(a));
             x[j] = a * os;
+          }
+          if constexpr (FP4_OUT) {   // two blocks of 16 columns (os is 1 here)
+            sfc = nvfp4_block16(x, p.fp4_scale, q4) | (nvfp4_block16(x + 16, p.fp4_scale, q4 + 2) << 8);
+            if (row_ok && col0 < p.N)
+              *reinterpret_cast<uint16_t*>(p.out_sf + sf_offset(row, col0 / 16, p.out_sf_kc)) = (uint16_t)sfc;
           }
         } else if constexpr (C::EPI == EPI_ROPE) {
           const float sc = ts * rs;
@@ -883,7 +995,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t oslot = out_base + (c & 1) * C::OUTSET;
         if (lane == 0) ptx::bulk_wait_read<1>();  // the group that last used this set is done reading
         __syncwarp();
-        if constexpr (CODES) {
+        if constexpr (FP4_OUT) {
+          ptx::st_shared_v4(oslot + 16 * lane, q4[0], q4[1], q4[2], q4[3]);   // 32 rows of 16 bytes
+        } else if constexpr (CODES) {
           slot_write_codes(oslot, lane, qg);
           slot_write_codes(oslot + C::OSLOT, lane, qu);
         } else {
@@ -902,7 +1016,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (C::EPI == EPI_STORE && C::OUT_DT == DT_F32 && p.k_splits > 1)
                 ptx::tma_reduce_add_2d_hint(&tmOut, col0, r0, oslot, stream_pol);   // split-K partial
               else
-                ptx::tma_store_2d_hint(&tmOut, col0, r0, oslot, stream_pol);
+                ptx::tma_store_2d_hint(&tmOut, FP4_OUT ? col0 / 2 : col0, r0, oslot, stream_pol);
               if constexpr (C::EPI == EPI_SWIGLU_BWD)
                 ptx::tma_store_2d_hint(&tmOut, p.up_offset + col0, r0, oslot + C::OSLOT, stream_pol);
             }
@@ -978,6 +1092,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // ------------------------------------------------------------------ host launcher
 struct GemmLaunch {
   CUtensorMap tmA, tmB, tmOut, tmSide0, tmSide1, tmAux;
+  CUtensorMap tmSFA, tmSFB;   // NVFP4 block scales of A and B (unused otherwise)
   GemmParams p;
   int sms;
   int overlap;   // launch with a programmatic dependency on the previous kernel of the stream
@@ -1050,7 +1165,8 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, gemm_epilogue_kernel<C>, L.tmA, L.tmB, L.tmOut, L.tmSide0, L.tmSide1, L.tmAux, L.p);
+  return cudaLaunchKernelEx(&cfg, gemm_epilogue_kernel<C>, L.tmA, L.tmB, L.tmOut, L.tmSide0, L.tmSide1, L.tmAux,
+                            L.tmSFA, L.tmSFB, L.p);
 }
 
 }  // namespace coda

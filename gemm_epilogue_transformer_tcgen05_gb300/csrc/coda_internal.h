@@ -20,6 +20,10 @@ struct VariantEntry {
   int smem_bytes;
   int stages;
   int cg;          // CTAs per MMA group (2 = CTA pair)
+  int un;          // MMA N (B rows per tile)
+  int bn_out;      // output columns per tile
+  int b_box;       // B rows per TMA copy
+  int bk;          // K elements per pipeline stage
 };
 
 // Tables defined by the instantiation units.
@@ -31,6 +35,8 @@ extern const VariantEntry g_variants_lowp[];
 extern const int g_num_variants_lowp;
 extern const VariantEntry g_variants_fp8[];
 extern const int g_num_variants_fp8;
+extern const VariantEntry g_variants_fp4[];
+extern const int g_num_variants_fp4;
 
 const VariantEntry* find_variant(const VariantKey& k);
 
@@ -56,13 +62,22 @@ cudaError_t launch_rope_bwd(const void* dout, const void* out, int64_t M, int64_
                             void* e, int64_t lde, float* c, cudaStream_t s);
 cudaError_t launch_quantize_e4m3(const void* X, int64_t M, int64_t N, int64_t ldx, float inv_scale, void* Q,
                                  int64_t ldq, float* amax, cudaStream_t s, int sms);
+cudaError_t launch_quantize_nvfp4(const void* X, int64_t R, int64_t K, int64_t ldx, float s, void* Q, int64_t ldq_bytes,
+                                  uint8_t* sf, int64_t pair_half, float* amax, cudaStream_t st, int sms);
 cudaError_t launch_xent_reduce(const float* Pm, const float* Ps, int64_t ld, int nparts, int64_t M, const float* T,
                                const int* targets, int64_t V, float* lse, float* loss, float* mean, cudaStream_t s);
 
 }  // namespace coda
 
-#define CODA_VARIANT(KIND, EPI, AMN, BMN, OUT, SIDE, AUX)                                                   \
-  {{KIND, EPI, AMN, BMN, OUT, SIDE, AUX},                                                                 \
-   &launch_gemm<GemmCfg<KIND, EPI, AMN, BMN, OUT, SIDE, AUX>>,                                            \
-   GemmCfg<KIND, EPI, AMN, BMN, OUT, SIDE, AUX>::SMEM_BYTES,                                              \
-   GemmCfg<KIND, EPI, AMN, BMN, OUT, SIDE, AUX>::STAGES, GemmCfg<KIND, EPI, AMN, BMN, OUT, SIDE, AUX>::CG}
+namespace coda {
+template <class C>
+constexpr VariantEntry make_variant(VariantKey k) {
+  return {k, &launch_gemm<C>, C::SMEM_BYTES, C::STAGES, C::CG, C::UN, C::BN_OUT, C::B_BOX, C::BK};
+}
+}  // namespace coda
+#define CODA_VARIANT(KIND, EPI, AMN, BMN, OUT, SIDE, AUX) \
+  make_variant<GemmCfg<KIND, EPI, AMN, BMN, OUT, SIDE, AUX>>(VariantKey{KIND, EPI, AMN, BMN, OUT, SIDE, AUX})
+// NVFP4 variants: CTA pairs with MMA N = 128
+#define CODA_VARIANT_FP4(EPI, OUT)                                                        \
+  make_variant<GemmCfg<KIND_NVFP4, EPI, false, false, OUT, DT_BF16, false, 2, 128>>( \
+      VariantKey{KIND_NVFP4, EPI, false, false, OUT, DT_BF16, false})

@@ -7,7 +7,8 @@
 //     stored activation;
 //   * the column reduce of per-block column partials (RMSNorm gain gradient);
 //   * the gain fold W' = W diag(g) (weight preparation for the deferred-r GEMM);
-//   * the RoPE cos/sin table.
+//   * the RoPE cos/sin table;
+//   * e4m3 and NVFP4 quantisers.
 #include <cuda_bf16.h>
 
 #include "coda_internal.h"
@@ -434,6 +435,61 @@ cudaError_t launch_quantize_e4m3(const void* X, int64_t M, int64_t N, int64_t ld
   launch_k(quantize_e4m3_kernel, (unsigned)blocks, threads, s, reinterpret_cast<const __nv_bfloat16*>(X), M, N, ldx,
                                                             inv_scale, reinterpret_cast<uint8_t*>(Q), ldq,
                                                             reinterpret_cast<unsigned int*>(amax));
+  return cudaGetLastError();
+}
+
+// NVFP4 quantiser: one thread per block of 16 elements of a row (32 bytes read, 8 bytes of
+// codes and one scale byte written); rows from R up to the next multiple of 128 get zero
+// scales.  pair_half > 0 writes the scales of a SwiGLU weight in pair order (gate rows
+// 64 j.. and up rows F + 64 j.. share scale block j).
+__global__ void quantize_nvfp4_kernel(const __nv_bfloat16* __restrict__ X, int64_t R, int64_t K, int64_t ldx, float s,
+                                      uint8_t* __restrict__ Q, int64_t ldq, uint8_t* __restrict__ sf,
+                                      int64_t pair_half, unsigned int* __restrict__ amax) {
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+  const int64_t nb = K >> 4, kc = K >> 6;
+  const int64_t rpad = (R + 127) / 128 * 128;
+  const int64_t total = rpad * nb;
+  float m = 0.f;
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = v / nb, b = v - i * nb;
+    uint32_t code = 0;
+    int64_t pr = i;
+    if (i < R) {
+      const uint4* src = reinterpret_cast<const uint4*>(X + i * ldx + 16 * b);
+      const uint4 u0 = __ldcs(src), u1 = __ldcs(src + 1);
+      const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+      float x[16];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        x[2 * e] = __uint_as_float(w[e] << 16);
+        x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+        m = fmaxf(m, fmaxf(fabsf(x[2 * e]), fabsf(x[2 * e + 1])));
+      }
+      uint32_t q[2];
+      code = nvfp4_block16(x, s, q);
+      __stcs(reinterpret_cast<uint2*>(Q + i * ldq + 8 * b), make_uint2(q[0], q[1]));
+      if (pair_half > 0)
+        pr = i < pair_half ? 128 * (i / 64) + i % 64 : 128 * ((i - pair_half) / 64) + 64 + (i - pair_half) % 64;
+    }
+    sf[sf_offset(pr, b, kc)] = (uint8_t)code;
+  }
+  if (amax) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((threadIdx.x & 31) == 0 && m > 0.f) atomicMax(amax, __float_as_uint(m));
+  }
+}
+
+cudaError_t launch_quantize_nvfp4(const void* X, int64_t R, int64_t K, int64_t ldx, float s, void* Q, int64_t ldq_bytes,
+                                  uint8_t* sf, int64_t pair_half, float* amax, cudaStream_t st, int sms) {
+  const int threads = 256;
+  const int64_t total = (R + 127) / 128 * 128 * (K >> 4);
+  int64_t blocks = (total + threads - 1) / threads;
+  if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+  if (blocks < 1) blocks = 1;
+  launch_k(quantize_nvfp4_kernel, (unsigned)blocks, threads, st, reinterpret_cast<const __nv_bfloat16*>(X), R, K, ldx,
+           s, reinterpret_cast<uint8_t*>(Q), ldq_bytes, sf, pair_half, reinterpret_cast<unsigned int*>(amax));
   return cudaGetLastError();
 }
 

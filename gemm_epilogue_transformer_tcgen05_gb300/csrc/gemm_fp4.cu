@@ -1,0 +1,14 @@
+// NVFP4 variants: block-scaled e2m1 operands (CTA pairs, MMA N = 128): the plain GEMM, the
+// residual program of a down projection, and the SwiGLU program with an NVFP4 or bf16 output.
+#include "coda_internal.h"
+
+namespace coda {
+const VariantEntry g_variants_fp4[] = {
+    CODA_VARIANT_FP4(EPI_STORE, DT_F32),
+    CODA_VARIANT_FP4(EPI_STORE, DT_BF16),
+    CODA_VARIANT_FP4(EPI_RESID, DT_BF16),
+    CODA_VARIANT_FP4(EPI_SWIGLU, DT_E2M1),
+    CODA_VARIANT_FP4(EPI_SWIGLU, DT_BF16),
+};
+const int g_num_variants_fp4 = sizeof(g_variants_fp4) / sizeof(g_variants_fp4[0]);
+}  // namespace coda

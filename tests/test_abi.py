@@ -147,3 +147,49 @@ def test_binding_reads_layout_from_strides():
     assert (d.layout, d.rows, d.cols, d.ld) == (C.COL_MAJOR, 32, 64, 32)
     with pytest.raises(ValueError):
         C.desc(torch.empty((4, 4, 4)))
+
+
+def test_nvfp4_entry_points_validate(L):
+    f = ctypes.c_void_p(FAKE)
+    assert C.coda_nvfp4_scale_bytes(300, 512) == 3 * 8 * 512
+    assert C.coda_nvfp4_scale_bytes(0, 512) == 0
+    X = _t(FAKE, C.BF16, 256, 512, 512)
+    Q = _t(FAKE, C.NVFP4, 256, 512, 512)
+    q = L.coda_quantize_nvfp4
+    assert q(None, 1.0, ctypes.byref(Q), f, 0, None, None) == C.ERR_NULL
+    assert q(ctypes.byref(X), 1.0, ctypes.byref(Q), None, 0, None, None) == C.ERR_NULL        # scales missing
+    assert q(ctypes.byref(X), 0.0, ctypes.byref(Q), f, 0, None, None) == C.ERR_SHAPE         # s > 0
+    assert q(ctypes.byref(X), 1.0, ctypes.byref(X), f, 0, None, None) == C.ERR_DTYPE         # Q must be NVFP4
+    assert q(ctypes.byref(X), 1.0, ctypes.byref(Q), f, 100, None, None) == C.ERR_SHAPE       # pair_half % 64
+    assert q(ctypes.byref(X), 1.0, ctypes.byref(Q), ctypes.c_void_p(FAKE + 8), 0, None, None) == C.ERR_ALIGN
+    assert q(ctypes.byref(_t(FAKE, C.BF16, 256, 48, 48)), 1.0, ctypes.byref(_t(FAKE, C.NVFP4, 256, 48, 64)), f, 0,
+             None, None) == C.ERR_SHAPE                                                        # K % 64
+    assert q(ctypes.byref(X), 1.0, ctypes.byref(_t(FAKE, C.NVFP4, 256, 512, 520)), f, 0, None,
+             None) == C.ERR_ALIGN                                                              # ld / 2 % 16
+    # the GEMM with NVFP4 operands
+    A = _t(FAKE, C.NVFP4, 256, 512, 512)
+    W = _t(FAKE, C.NVFP4, 256, 512, 512)
+    out = _t(FAKE, C.F32, 256, 256, 256)
+    p = C.program(C.OP_TENSOR_SCALE)
+    side = C.CodaSide()
+    aux = C.CodaAux()
+    g = lambda A_, W_, o: L.coda_gemm_epilogue(ctypes.byref(A_), ctypes.byref(W_), ctypes.byref(p), ctypes.byref(side),
+                                               ctypes.byref(o), ctypes.byref(aux), None)
+    assert g(A, W, out) == C.ERR_NULL                                                         # block scales missing
+    side.a_block_scales, side.w_block_scales = FAKE, FAKE + 8
+    assert g(A, W, out) == C.ERR_ALIGN
+    side.w_block_scales = FAKE
+    assert g(_t(FAKE, C.NVFP4, 256, 320, 320), _t(FAKE, C.NVFP4, 256, 320, 320), out) == C.ERR_SHAPE   # K % 256
+    assert g(A, _t(FAKE, C.BF16, 256, 512, 512), out) == C.ERR_DTYPE                          # mixed operands
+    assert g(A, W, _t(FAKE, C.NVFP4, 256, 256, 256)) == C.ERR_DTYPE                           # fp4 out: SWIGLU only
+    assert g(_t(FAKE, C.NVFP4, 256, 512, 512, C.COL_MAJOR), W, out) == C.ERR_SHAPE            # row-major only
+    # the chain
+    assert L.coda_mlp_nvfp4(None, None) == C.ERR_NULL
+    io = C.CodaMlpNvfp4(M=256, H=512, F=512, eps=1e-6, s_x=1.0, s_w=1.0, s_wd=1.0, s_a=1.0, h=f, X_q=f, X_sf=f,
+                        W_q=f, W_sf=f, W_dq=f, W_dsf=f, r=f, a_q=f, a_sf=f, amax=f, Y=f, Y_partials=f)
+    io.F = 384
+    assert L.coda_mlp_nvfp4(ctypes.byref(io), None) == C.ERR_SHAPE                            # F % 256
+    io.F, io.s_a = 512, 0.0
+    assert L.coda_mlp_nvfp4(ctypes.byref(io), None) == C.ERR_SHAPE                            # s_a > 0
+    io.s_a, io.W_dsf = 1.0, None
+    assert L.coda_mlp_nvfp4(ctypes.byref(io), None) == C.ERR_NULL
