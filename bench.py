@@ -70,7 +70,10 @@ def parse():
     p.add_argument("--traffic-pass", action="store_true",
                    help="run only the fused chain twice, then the torch eager chain twice (a short program "
                         "for a per-kernel DRAM-bytes capture); prints one JSON line naming the launches")
-    p.add_argument("--tokens", type=int, default=M_TOK, help="token count of --traffic-pass")
+    p.add_argument("--nvfp4-pass", action="store_true",
+                   help="run only the NVFP4 MLP (H 4096, F 14336): quantise X, then the chain twice (a short "
+                        "program for a per-kernel capture)")
+    p.add_argument("--tokens", type=int, default=M_TOK, help="token count of --traffic-pass / --nvfp4-pass")
     p.add_argument("--compile-compare", action="store_true",
                    help="also time torch.compile of the unfused comparators (compiles on first use)")
     return p.parse_args()
@@ -308,6 +311,41 @@ def traffic_pass(args):
                                        "order": "fused chain x2 (G1, reduce, G2, G3), then torch eager chain x2",
                                        "normwise_diff": float((Y.float() - Yt.float()).abs().max()
                                                               / Yt.float().abs().max())}}), flush=True)
+
+
+def nvfp4_pass(args):
+    """The NVFP4 MLP at the LLaMA-3-8B width: weight and X quantisation (three quantiser
+    launches), then the chain twice (row RMS, gate/up GEMM, down GEMM each time), nothing else
+    on the device: under a per-kernel capture the second chain is the warm one."""
+    import torch
+
+    import coda_synth as S
+    from gemm_epilogue_transformer_tcgen05_gb300 import coda as C
+
+    C.lib()
+    M, H, F = args.tokens, 4096, 14336
+    ni = S.nvfp4_mlp_inputs(M, H, F, seed=0, device="cuda")
+    sc = lambda t: float(t.abs().max()) / (6 * 448)
+    X, W, Wd = C.Nvfp4.empty(M, H, sc(ni["h"])), C.Nvfp4.empty(2 * F, H, sc(ni["W_gu"])), C.Nvfp4.empty(H, F, sc(ni["W_d"]))
+    C.coda_quantize_nvfp4(ni["W_gu"], W, pair_half=F)
+    C.coda_quantize_nvfp4(ni["W_d"], Wd)
+    C.coda_quantize_nvfp4(ni["h"], X)
+    r, amax = torch.empty((M,), device="cuda"), torch.empty((1,), device="cuda")
+    a = C.Nvfp4.empty(M, F, 1.0)
+    Y = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    P = torch.empty((H // 128, M), device="cuda")
+    for i in range(2):
+        C.coda_mlp_nvfp4(ni["h"], X, W, Wd, EPS, r, a, amax, Y, P)
+        if i == 0:
+            torch.cuda.synchronize()
+            a.s = float(amax.item()) / (6 * 448)
+    torch.cuda.synchronize()
+    st, site = C.coda_get_device_status()
+    if st != C.OK:
+        raise RuntimeError(f"device status {st} (site {site})")
+    print(json.dumps({"nvfp4_pass": {"tokens": M, "hidden": H, "ffn": F,
+                                     "order": "quantise W_gu, W_d, X; chain x2 (row RMS, gate/up GEMM, down GEMM)",
+                                     "Y_rms": float(Y.float().pow(2).mean().sqrt())}}), flush=True)
 
 
 def run_coda(args, world, rank, local):
@@ -609,6 +647,51 @@ def fp8_peak(torch, seconds=2.0):
                    f"{reps} back to back (sustained)"}
 
 
+def fp4_peak(torch, fp8_sustained, seconds=2.0):
+    """Dense NVFP4 GEMM throughput of the vendor library (torch._scaled_mm on e2m1 operands
+    with e4m3 block scales, bf16 out) at 8192^3, burst and sustained as for fp8.  Where this
+    torch cannot run it, the nominal ratio (13.5 / 4.5 PFLOP/s = 3x the measured e4m3 peak)
+    stands in, and the entry says so."""
+    n = 8192
+    try:
+        gen = torch.Generator(device="cuda").manual_seed(4)
+        a = torch.randint(0, 256, (n, n // 2), dtype=torch.uint8, device="cuda", generator=gen)
+        b = torch.randint(0, 256, (n, n // 2), dtype=torch.uint8, device="cuda", generator=gen)
+        a, b = a.view(torch.float4_e2m1fn_x2), b.view(torch.float4_e2m1fn_x2)
+        sa = torch.full((n, n // 16), 0x38, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
+        sb = torch.full((n, n // 16), 0x38, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
+
+        def f():
+            return torch._scaled_mm(a, b.t(), scale_a=sa, scale_b=sb, out_dtype=torch.bfloat16)
+
+        for _ in range(5):
+            f()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        best = float("inf")
+        for _ in range(10):
+            e0.record()
+            f()
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        flop = 2.0 * n ** 3
+        reps = max(10, int(seconds * 1e3 / best))
+        e0.record()
+        for _ in range(reps):
+            f()
+        e1.record()
+        torch.cuda.synchronize()
+        sus = flop * reps / (e0.elapsed_time(e1) * 1e-3) / 1e12
+        return {"burst_tflops": flop / (best * 1e-3) / 1e12, "sustained_tflops": sus, "reps_sustained": reps,
+                "how": "torch._scaled_mm NVFP4 (e2m1, e4m3 block scales) -> bf16, 8192^3: best of 10 (burst); "
+                       f"{reps} back to back (sustained)"}
+    except Exception as ex:
+        return {"sustained_tflops_nominal_ratio": 3.0 * fp8_sustained,
+                "error": f"{type(ex).__name__}: {ex}"[:200],
+                "how": "library NVFP4 GEMM unavailable here: 3x the measured e4m3 sustained peak (nominal ratio)"}
+
+
 def other_workloads(torch, C, S, args, stream):
     """Device time of the other chains at their full sizes (16384 tokens): the block backward
     (C2), QKV + RoPE (C3) and the fp8 MLP (C4), with TFLOP/s and the fraction of their
@@ -777,6 +860,47 @@ def other_workloads(torch, C, S, args, stream):
                                           "dh GEMM + RMSNorm-bwd combine, dW; e4m3 operands, MN-major where "
                                           "transposed"}
     del h8, X8, W8, Wd8, aq, Y8, P8, Z8, dY8, dYq8, eq8, dh8, dWd8, dW8, ws8
+    torch.cuda.empty_cache()
+    # N4: the same MLP with NVFP4 operands (e2m1 codes, e4m3 block scales per 16 K elements)
+    out["fp4_peak"] = fp4_peak(torch, peak8)
+    peak4 = out["fp4_peak"].get("sustained_tflops", out["fp4_peak"].get("sustained_tflops_nominal_ratio"))
+    ni = S.nvfp4_mlp_inputs(M, H8, F8, seed=0, device="cuda")
+    h4 = ni["h"]
+    amax4 = lambda t: float(t.abs().max()) / (6 * 448)
+    X4 = C.Nvfp4.empty(M, H8, amax4(h4))
+    W4 = C.Nvfp4.empty(2 * F8, H8, amax4(ni["W_gu"]))
+    Wd4 = C.Nvfp4.empty(H8, F8, amax4(ni["W_d"]))
+    C.coda_quantize_nvfp4(ni["W_gu"], W4, pair_half=F8, stream=stream)   # weight preparation
+    C.coda_quantize_nvfp4(ni["W_d"], Wd4, stream=stream)
+    quant_x = lambda: C.coda_quantize_nvfp4(h4, X4, stream=stream)
+    quant_x()
+    del ni
+    r4 = torch.empty((M,), device="cuda")
+    am4 = torch.empty((1,), device="cuda")
+    Y4 = torch.empty((M, H8), dtype=BF, device="cuda")
+    P4 = torch.empty((H8 // 128, M), device="cuda")
+    a4 = C.Nvfp4.empty(M, F8, 1.0)
+    run4 = lambda: C.coda_mlp_nvfp4(h4, X4, W4, Wd4, EPS, r4, a4, am4, Y4, P4, stream=stream)
+    run4()
+    torch.cuda.synchronize()
+    a4.s = float(am4.item()) / (6 * 448)              # delayed scaling from the previous pass
+    ms = _time(torch, run4, stream, steps)
+    flop = 2 * M * 2 * F8 * H8 + 2 * M * H8 * F8
+    sfb = lambda R, K: (R * K) // 16                    # block-scale bytes
+    byt = (M * H8 // 2 + sfb(M, H8) + F8 * H8 + sfb(2 * F8, H8) + M * F8 // 2 + sfb(M, F8)) + \
+        (M * F8 // 2 + sfb(M, F8) + H8 * F8 // 2 + sfb(H8, F8)) + 2 * (M * H8 * 3) + 4 * M * (H8 // 128 + 1)
+    roof = max(flop / (peak4 * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
+    ms_q = _time(torch, quant_x, stream, steps)
+    byt_q = 2 * M * H8 + M * H8 // 2 + sfb(M, H8)
+    out["mlp_nvfp4_N4"] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "roofline_ms": roof,
+                           "roofline_frac": roof / ms, "tokens_per_s": M / (ms * 1e-3), "launches": 3,
+                           "peak_tflops": peak4, "vs_fp8_chain": out["mlp_fp8_C4"]["ms"] / ms,
+                           "quantize_x_ms": ms_q, "quantize_x_gbs": byt_q / (ms_q * 1e-3) / 1e9,
+                           "quantize_x_frac_of_hbm": byt_q / (ms_q * 1e-3) / 1e9 / pk["hbm"],
+                           "note": "row RMS, gate/up GEMM + r + SwiGLU + NVFP4 quantisation of a (codes, block "
+                                   "scales, amax), down GEMM + residual + partials; X quantised beforehand "
+                                   "(quantize_x_ms, the pass a previous layer's epilogue would fold in)"}
+    del h4, X4, W4, Wd4, Y4, P4, a4
     torch.cuda.empty_cache()
     # N3: the block forward at the 7B and 70B LLaMA-3 hidden sizes, beside torch eager
     for name, Hs, Fs in (("block_forward_7B_H4096_F14336", 4096, 14336), ("block_forward_70B_H8192_F28672", 8192,
@@ -973,9 +1097,9 @@ def main():
     if args.impl == "reference":
         run_reference(args, world, rank)
         return
-    if args.traffic_pass:
+    if args.traffic_pass or args.nvfp4_pass:
         if rank == 0:
-            traffic_pass(args)
+            traffic_pass(args) if args.traffic_pass else nvfp4_pass(args)
         return
     run_coda(args, world, rank, local)
 

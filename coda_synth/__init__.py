@@ -113,6 +113,17 @@ def fp8_mlp_inputs(M, H, F, seed=0, w_std=0.015, with_grad=False):
     return out
 
 
+def nvfp4_mlp_inputs(M, H, F, seed=0, w_std=0.015, device="cpu"):
+    """The FP8 MLP's tensors in bf16 (h ~ N(0, 1), weights ~ N(0, 0.015^2)) for the NVFP4 MLP:
+    each side quantises them itself (the library's quantiser on the device, the oracle's on
+    the host), with tensor scales amax / (6 * 448)."""
+    gen = torch.Generator(device=device).manual_seed(seed)
+    h = torch.randn((M, H), generator=gen, device=device).to(torch.bfloat16)
+    W_gu = (torch.randn((2 * F, H), generator=gen, device=device) * w_std).to(torch.bfloat16)
+    W_d = (torch.randn((H, F), generator=gen, device=device) * w_std).to(torch.bfloat16)
+    return dict(h=h, W_gu=W_gu, W_d=W_d, eps=1e-6)
+
+
 def lm_head_inputs(M, H, V, seed=0, w_std=0.02, dtype=torch.bfloat16):
     gen = torch.Generator().manual_seed(seed)
     return dict(
