@@ -327,13 +327,13 @@ def nvfp4_pass(args):
     ni = S.nvfp4_mlp_inputs(M, H, F, seed=0, device="cuda")
     sc = lambda t: float(t.abs().max()) / (6 * 448)
     X, W, Wd = C.Nvfp4.empty(M, H, sc(ni["h"])), C.Nvfp4.empty(2 * F, H, sc(ni["W_gu"])), C.Nvfp4.empty(H, F, sc(ni["W_d"]))
-    C.coda_quantize_nvfp4(ni["W_gu"], W, pair_half=F)
+    C.coda_quantize_nvfp4(ni["W_gu"], W)
     C.coda_quantize_nvfp4(ni["W_d"], Wd)
     C.coda_quantize_nvfp4(ni["h"], X)
     r, amax = torch.empty((M,), device="cuda"), torch.empty((1,), device="cuda")
     a = C.Nvfp4.empty(M, F, 1.0)
     Y = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
-    P = torch.empty((H // 128, M), device="cuda")
+    P = torch.empty((H // 256, M), device="cuda")
     for i in range(2):
         C.coda_mlp_nvfp4(ni["h"], X, W, Wd, EPS, r, a, amax, Y, P)
         if i == 0:
@@ -870,7 +870,7 @@ def other_workloads(torch, C, S, args, stream):
     X4 = C.Nvfp4.empty(M, H8, amax4(h4))
     W4 = C.Nvfp4.empty(2 * F8, H8, amax4(ni["W_gu"]))
     Wd4 = C.Nvfp4.empty(H8, F8, amax4(ni["W_d"]))
-    C.coda_quantize_nvfp4(ni["W_gu"], W4, pair_half=F8, stream=stream)   # weight preparation
+    C.coda_quantize_nvfp4(ni["W_gu"], W4, stream=stream)   # weight preparation
     C.coda_quantize_nvfp4(ni["W_d"], Wd4, stream=stream)
     quant_x = lambda: C.coda_quantize_nvfp4(h4, X4, stream=stream)
     quant_x()
@@ -878,7 +878,7 @@ def other_workloads(torch, C, S, args, stream):
     r4 = torch.empty((M,), device="cuda")
     am4 = torch.empty((1,), device="cuda")
     Y4 = torch.empty((M, H8), dtype=BF, device="cuda")
-    P4 = torch.empty((H8 // 128, M), device="cuda")
+    P4 = torch.empty((H8 // 256, M), device="cuda")
     a4 = C.Nvfp4.empty(M, F8, 1.0)
     run4 = lambda: C.coda_mlp_nvfp4(h4, X4, W4, Wd4, EPS, r4, a4, am4, Y4, P4, stream=stream)
     run4()
@@ -888,7 +888,7 @@ def other_workloads(torch, C, S, args, stream):
     flop = 2 * M * 2 * F8 * H8 + 2 * M * H8 * F8
     sfb = lambda R, K: (R * K) // 16                    # block-scale bytes
     byt = (M * H8 // 2 + sfb(M, H8) + F8 * H8 + sfb(2 * F8, H8) + M * F8 // 2 + sfb(M, F8)) + \
-        (M * F8 // 2 + sfb(M, F8) + H8 * F8 // 2 + sfb(H8, F8)) + 2 * (M * H8 * 3) + 4 * M * (H8 // 128 + 1)
+        (M * F8 // 2 + sfb(M, F8) + H8 * F8 // 2 + sfb(H8, F8)) + 2 * (M * H8 * 3) + 4 * M * (H8 // 256 + 1)
     roof = max(flop / (peak4 * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
     ms_q = _time(torch, quant_x, stream, steps)
     byt_q = 2 * M * H8 + M * H8 // 2 + sfb(M, H8)

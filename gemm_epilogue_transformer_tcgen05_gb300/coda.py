@@ -188,7 +188,7 @@ def lib():
         "coda_rope_backward": [P(CodaTensor), P(CodaTensor), c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32,
                                c_int64, P(CodaTensor), c_void_p, c_void_p],
         "coda_qkv_rope_backward": [P(CodaQkvRopeBwd), c_void_p],
-        "coda_quantize_nvfp4": [P(CodaTensor), c_float, P(CodaTensor), c_void_p, c_int64, c_void_p, c_void_p],
+        "coda_quantize_nvfp4": [P(CodaTensor), c_float, P(CodaTensor), c_void_p, c_void_p, c_void_p],
         "coda_mlp_nvfp4": [P(CodaMlpNvfp4), c_void_p],
     }
     for name, args in sigs.items():
@@ -470,15 +470,15 @@ def coda_nvfp4_scale_bytes(R, K):
     return int(lib().coda_nvfp4_scale_bytes(R, K))
 
 
-def coda_quantize_nvfp4(X, Q, pair_half=0, amax=None, stream=None):
+def coda_quantize_nvfp4(X, Q, amax=None, stream=None):
     """Q (an Nvfp4 of X's shape, tensor scale Q.s) = NVFP4 quantisation of the bf16 tensor X."""
     x, q = desc(X), desc_nvfp4(Q.codes)
-    _check(lib().coda_quantize_nvfp4(ctypes.byref(x), Q.s, ctypes.byref(q), _ptr(Q.scales), pair_half, _ptr(amax),
+    _check(lib().coda_quantize_nvfp4(ctypes.byref(x), Q.s, ctypes.byref(q), _ptr(Q.scales), _ptr(amax),
                                      _stream(stream)), "coda_quantize_nvfp4")
 
 
 def coda_mlp_nvfp4(h, X, W, Wd, eps, r, a, amax, Y, Y_partials, stream=None):
-    """NVFP4 MLP: X, W (gate/up, scales in pair order), Wd and the output a are Nvfp4 tensors;
+    """NVFP4 MLP: X, W (gate/up), Wd and the output a are Nvfp4 tensors;
     a.s is the delayed scale s_a of the SwiGLU output."""
     M, H = h.shape
     F = Wd.shape[1]

@@ -655,22 +655,21 @@ size_t coda_nvfp4_scale_bytes(int64_t R, int64_t K) {
   return (size_t)((R + 127) / 128) * (size_t)(K / 64) * 512u;
 }
 
-int coda_quantize_nvfp4(const coda_tensor* X, float s, const coda_tensor* Q, void* block_scales, int64_t pair_half,
-                        float* amax, void* stream) {
+int coda_quantize_nvfp4(const coda_tensor* X, float s, const coda_tensor* Q, void* block_scales, float* amax,
+                        void* stream) {
   int st;
   if ((st = check_tensor(X, false)) != CODA_OK) return st;
   if ((st = check_tensor(Q, false)) != CODA_OK) return st;
   if (X->dtype != CODA_BF16 || Q->dtype != CODA_NVFP4) return CODA_ERR_DTYPE;
   if (Q->rows != X->rows || Q->cols != X->cols || X->cols % 64 != 0) return CODA_ERR_SHAPE;
   if (!(s > 0.f) || !(s < INFINITY)) return CODA_ERR_SHAPE;
-  if (pair_half < 0 || (pair_half > 0 && (pair_half % 64 != 0 || X->rows != 2 * pair_half))) return CODA_ERR_SHAPE;
   if (X->rows == 0 || X->cols == 0) return CODA_OK;
   if (!block_scales) return CODA_ERR_NULL;
   if (!aligned16(block_scales)) return CODA_ERR_ALIGN;
   DevState* dv;
   if ((st = ensure_device(&dv)) != CODA_OK) return st;
   cudaError_t e = launch_quantize_nvfp4(X->ptr, X->rows, X->cols, X->ld, s, Q->ptr, Q->ld / 2,
-                                        static_cast<uint8_t*>(block_scales), pair_half, amax,
+                                        static_cast<uint8_t*>(block_scales), amax,
                                         static_cast<cudaStream_t>(stream), dv->sms);
   return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
 }

@@ -42,7 +42,7 @@ namespace coda {
 
 // ----------------------------------------------------------------------- constants
 constexpr int BM = 128;                               // tile rows = TMEM lanes
-constexpr int UMMA_N = 256;                           // MMA N = B tile rows (NVFP4: 128, see GemmCfg)
+constexpr int UMMA_N = 256;                           // MMA N = B tile rows
 constexpr int BK_BYTES = 128;                         // K bytes per stage (one 128B swizzle row)
 constexpr int KSTEPS = 4;                             // MMAs per stage, 32 bytes of K each
 constexpr int A_STAGE_BYTES = BM * BK_BYTES;          // 16 KB: this CTA's 128 rows of A
@@ -143,8 +143,9 @@ struct GemmParams {
 // CG = CTAs per MMA: 1, or 2 for a CTA pair (cluster of two) issuing cta_group::2 MMAs of
 // 256 x 256: each CTA holds 128 rows of A and 128 rows (N) of B per stage and receives its
 // 128 accumulator rows in its own TMEM.
-// UN = MMA N (B rows of a tile).  256 fills TMEM with the two accumulators; NVFP4 tiles use
-// 128 so that the block scales of the pipeline stages fit in TMEM beside them.
+// UN = MMA N (B rows of a tile).  256 fills TMEM with two accumulators.  NVFP4 tiles keep
+// UN = 256 with one accumulator, so that the block scales of the pipeline stages fit in TMEM
+// beside it (the epilogue of a tile then runs between that tile's MMAs and the next's).
 template <int KIND_, int EPI_, bool A_MN_, bool B_MN_, int OUT_DT_, int SIDE_DT_, bool AUX_, int CG_ = 2,
           int UN_ = UMMA_N>
 struct GemmCfg {
@@ -193,9 +194,10 @@ struct GemmCfg {
   // TMEM: two accumulators of UN columns, then (NVFP4) each stage's block scales, 4 columns
   // per atom
   static constexpr int SF_COLS = (SF_A_BYTES + SF_B_BYTES) / 128;
-  static_assert(2 * UN + STAGES * SF_COLS <= TMEM_COLS, "TMEM columns");
+  static constexpr int ACC = FP4 ? 1 : 2;   // accumulators in TMEM
+  static_assert(ACC * UN + STAGES * SF_COLS <= TMEM_COLS, "TMEM columns");
   static_assert(UN % 128 == 0 && UN <= UMMA_N && B_ROWS % B_BOX == 0, "MMA N");
-  static_assert(!FP4 || (!A_MN && !B_MN && !AUX), "NVFP4 operands are K-major");
+  static_assert(!FP4 || (!A_MN && !B_MN && !AUX && UN == 256), "NVFP4: K-major operands, MMA N 256");
   static_assert(OUT_DT != DT_E2M1 || (FP4 && EPI == EPI_SWIGLU), "e2m1 output: NVFP4 SwiGLU");
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(STAGES >= 2, "shared memory budget");
@@ -387,9 +389,10 @@ __device__ __forceinline__ float warp_transpose_sum(float (&x)[32], int lane) {
 __device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 // NVFP4 quantisation of one block of 16 values with tensor scale s: sf = e4m3(amax / (6 s)),
-// q = e2m1(x / (sf s)) (all zero when sf is 0), each quotient and product rounded once in
-// fp32.  q[0..1] receive the 16 codes (element 2j in the low nibble of byte j); returns the
-// scale's e4m3 byte.  The quantiser kernel and the SwiGLU epilogue both decide through here.
+// q = e2m1(x * (1 / (sf s))) (all zero when sf is 0), each product, quotient and reciprocal
+// rounded once in fp32.  q[0..1] receive the 16 codes (element 2j in the low nibble of byte j);
+// returns the scale's e4m3 byte.  The quantiser kernel and the SwiGLU epilogue both decide
+// through here.
 __device__ __forceinline__ uint32_t nvfp4_block16(const float* x, float s, uint32_t* q) {
   float amax = 0.f;
 #pragma unroll
@@ -399,9 +402,10 @@ __device__ __forceinline__ uint32_t nvfp4_block16(const float* x, float s, uint3
   float sfv, zero;
   ptx::e4m3x2_to_f32(code2, sfv, zero);
   const float d = __fmul_rn(sfv, s);
+  const float rd = d > 0.f ? __frcp_rn(d) : 0.f;
   float y[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) y[j] = d > 0.f ? __fdiv_rn(x[j], d) : 0.f;
+  for (int j = 0; j < 16; ++j) y[j] = __fmul_rn(x[j], rd);
   q[0] = ptx::cvt_e2m1x8(y);
   q[1] = ptx::cvt_e2m1x8(y + 8);
   return code2 & 0xFFu;
@@ -548,14 +552,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if constexpr (C::FP4) {
               // block scales: KSTEPS atoms (one per MMA) for this CTA's A rows, then for each 128
-              // rows of the tile's N; an atom row of the maps is one 512-byte atom
+              // rows of the tile's N (SwiGLU: the gate rows' block, then the up rows'); an atom
+              // row of the maps is one 512-byte atom
               const uint32_t ssf = sb + C::B_STAGE_BYTES;
               const int kc = p.K / 64;
               load(ssf, &tmSFA, 0, (m0 / 128) * kc + KSTEPS * kb, normal);
 #pragma unroll
-              for (int j = 0; j < C::UN / 128; ++j)
-                load(ssf + C::SF_A_BYTES + KSTEPS * 512 * j, &tmSFB, 0, (nb * (C::UN / 128) + j) * kc + KSTEPS * kb,
-                     keep);
+              for (int j = 0; j < C::UN / 128; ++j) {
+                const int blk = C::DUAL ? (j == 0 ? nb : p.up_offset / 128 + nb) : nb * (C::UN / 128) + j;
+                load(ssf + C::SF_A_BYTES + KSTEPS * 512 * j, &tmSFB, 0, blk * kc + KSTEPS * kb, keep);
+              }
             }
             issued_any |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -580,8 +586,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int t = 0;
       bool ok = true;
       for (int tile = cluster_id; ok && tile < total_tiles; tile += n_clusters, ++t) {
-        const int acc = t & 1;
-        const uint32_t aph = (t >> 1) & 1;
+        const int acc = t % C::ACC;
+        const uint32_t aph = (t / C::ACC) & 1;
         if (!bwait(TEMPTY_BAR(acc), aph ^ 1u, watch, SITE_MMA_TMEM_EMPTY)) {
           ok = false;
           break;
@@ -602,7 +608,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // this stage's block scales into its TMEM columns (A: 4 per MMA; B: 4 per MMA and
             // 128 rows of N), then the block-scaled MMAs; the copies and the MMAs run in issue order
             const uint32_t ssf = sb + C::B_STAGE_BYTES;
-            const uint32_t tsa = tmem_base + 2 * C::UN + stage * C::SF_COLS;
+            const uint32_t tsa = tmem_base + C::ACC * C::UN + stage * C::SF_COLS;
             const uint32_t tsb = tsa + 4 * KSTEPS;
             constexpr int NB128 = C::UN / 128;
 #pragma unroll
@@ -664,8 +670,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int r0 = m0 + 32 * q;   // first row of this warp's 32-row slab
       const int row = r0 + lane;
       const bool row_ok = row < p.M;
-      const int acc = t & 1;
-      const uint32_t aph = (t >> 1) & 1;
+      const int acc = t % C::ACC;
+      const uint32_t aph = (t / C::ACC) & 1;
 
       // A chunk is live if some of its rows and columns are in range; side loads of dead
       // chunks are neither issued nor waited for.

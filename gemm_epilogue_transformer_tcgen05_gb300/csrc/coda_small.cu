@@ -440,11 +440,10 @@ cudaError_t launch_quantize_e4m3(const void* X, int64_t M, int64_t N, int64_t ld
 
 // NVFP4 quantiser: one thread per block of 16 elements of a row (32 bytes read, 8 bytes of
 // codes and one scale byte written); rows from R up to the next multiple of 128 get zero
-// scales.  pair_half > 0 writes the scales of a SwiGLU weight in pair order (gate rows
-// 64 j.. and up rows F + 64 j.. share scale block j).
+// scales.
 __global__ void quantize_nvfp4_kernel(const __nv_bfloat16* __restrict__ X, int64_t R, int64_t K, int64_t ldx, float s,
                                       uint8_t* __restrict__ Q, int64_t ldq, uint8_t* __restrict__ sf,
-                                      int64_t pair_half, unsigned int* __restrict__ amax) {
+                                      unsigned int* __restrict__ amax) {
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
   const int64_t nb = K >> 4, kc = K >> 6;
@@ -454,7 +453,6 @@ __global__ void quantize_nvfp4_kernel(const __nv_bfloat16* __restrict__ X, int64
   for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
     const int64_t i = v / nb, b = v - i * nb;
     uint32_t code = 0;
-    int64_t pr = i;
     if (i < R) {
       const uint4* src = reinterpret_cast<const uint4*>(X + i * ldx + 16 * b);
       const uint4 u0 = __ldcs(src), u1 = __ldcs(src + 1);
@@ -469,10 +467,8 @@ __global__ void quantize_nvfp4_kernel(const __nv_bfloat16* __restrict__ X, int64
       uint32_t q[2];
       code = nvfp4_block16(x, s, q);
       __stcs(reinterpret_cast<uint2*>(Q + i * ldq + 8 * b), make_uint2(q[0], q[1]));
-      if (pair_half > 0)
-        pr = i < pair_half ? 128 * (i / 64) + i % 64 : 128 * ((i - pair_half) / 64) + 64 + (i - pair_half) % 64;
     }
-    sf[sf_offset(pr, b, kc)] = (uint8_t)code;
+    sf[sf_offset(i, b, kc)] = (uint8_t)code;
   }
   if (amax) {
 #pragma unroll
@@ -482,14 +478,14 @@ __global__ void quantize_nvfp4_kernel(const __nv_bfloat16* __restrict__ X, int64
 }
 
 cudaError_t launch_quantize_nvfp4(const void* X, int64_t R, int64_t K, int64_t ldx, float s, void* Q, int64_t ldq_bytes,
-                                  uint8_t* sf, int64_t pair_half, float* amax, cudaStream_t st, int sms) {
+                                  uint8_t* sf, float* amax, cudaStream_t st, int sms) {
   const int threads = 256;
   const int64_t total = (R + 127) / 128 * 128 * (K >> 4);
   int64_t blocks = (total + threads - 1) / threads;
   if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
   if (blocks < 1) blocks = 1;
   launch_k(quantize_nvfp4_kernel, (unsigned)blocks, threads, st, reinterpret_cast<const __nv_bfloat16*>(X), R, K, ldx,
-           s, reinterpret_cast<uint8_t*>(Q), ldq_bytes, sf, pair_half, reinterpret_cast<unsigned int*>(amax));
+           s, reinterpret_cast<uint8_t*>(Q), ldq_bytes, sf, reinterpret_cast<unsigned int*>(amax));
   return cudaGetLastError();
 }
 

@@ -1,4 +1,4 @@
-// NVFP4 variants: block-scaled e2m1 operands (CTA pairs, MMA N = 128): the plain GEMM, the
+// NVFP4 variants: block-scaled e2m1 operands (CTA pairs, MMA N = 256, one accumulator): the plain GEMM, the
 // residual program of a down projection, and the SwiGLU program with an NVFP4 or bf16 output.
 #include "coda_internal.h"
 

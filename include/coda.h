@@ -171,8 +171,7 @@ typedef struct coda_side_inputs {
 } coda_side_inputs;
 
 typedef struct coda_aux_outputs {
-  float* row_partials;          /* [ceil(N / 256), row_partials_ld], one row per 256-column tile
-                                   (128 for NVFP4 operands; SWIGLU_BWD: tiles of dA) */
+  float* row_partials;          /* [ceil(N / 256), row_partials_ld] (SWIGLU_BWD: tiles of dA) */
   int64_t row_partials_ld;      /* >= M */
   float* col_partials;          /* [ceil(M / 32), col_partials_ld]: one row per 32-row slab */
   int64_t col_partials_ld;      /* >= N */
@@ -191,8 +190,7 @@ typedef struct coda_aux_outputs {
  * (ROW_MAJOR, K a multiple of 256, block scales in side.a_block_scales / w_block_scales, the
  * product of the tensor scales as TENSOR_SCALE; programs {}, {TENSOR_SCALE}, the ADD_SIDE
  * program, and the SWIGLU program with a bf16 or NVFP4 out; an NVFP4 out takes its tensor
- * scale from side.out_fp4_scale and writes its block scales to aux.out_block_scales, and a
- * SWIGLU weight's block scales come in pair order, see coda_quantize_nvfp4); which
+ * scale from side.out_fp4_scale and writes its block scales to aux.out_block_scales); which
  * layouts each program has compiled is listed in the variant tables (others return
  * CODA_ERR_UNSUPPORTED_PROGRAM or CODA_ERR_DTYPE).  N must be a multiple of 32 (of 128 for SWIGLU), K >= 1.  M = 0 or N = 0 is a
  * no-op.  `side` and `aux` may be NULL when the program needs none of their fields. */
@@ -435,27 +433,27 @@ CODA_API int coda_quantize_e4m3(const coda_tensor* X, float scale, const coda_te
 
 /* NVFP4 quantisation of a bf16 tensor X (ROW_MAJOR [R, K], K a multiple of 64) with tensor
  * scale s > 0: for each block of 16 consecutive elements of a row,
- *   sf = e4m3(amax_block / (6 s)),  q = e2m1(x / (sf s))   (q = 0 where sf = 0),
- * each quotient and product rounded once in fp32, both conversions round-to-nearest-even and
- * saturating.  Q (CODA_NVFP4 [R, K]) receives the codes, block_scales the e4m3 scale bytes,
- * amax (optional, zeroed by the caller) the atomic max of |X|.  The SwiGLU epilogue of an
- * NVFP4 GEMM decides its output's codes the same way.
+ *   sf = e4m3(amax_block / (6 s)),  q = e2m1(x * (1 / (sf s)))   (q = 0 where sf = 0),
+ * each product, quotient and reciprocal rounded once in fp32 (the reciprocal, as the e4m3
+ * quantiser multiplies by 1 / scale), both conversions round-to-nearest-even and saturating.
+ * Q (CODA_NVFP4 [R, K]) receives the codes, block_scales the e4m3 scale bytes, amax (optional,
+ * zeroed by the caller) the atomic max of |X|.  The SwiGLU epilogue of an NVFP4 GEMM decides
+ * its output's codes the same way.
  * Block-scale layout (ceil(R / 128) * (K / 64) * 512 bytes): atoms of 128 rows x 4 blocks;
  * atom (row / 128, kb / 4) starts at byte ((row / 128) * (K / 64) + kb / 4) * 512, and inside
- * it row r, block kb sits at 16 (r % 32) + 4 ((r % 128) / 32) + kb % 4.  Rows from R up to the
- * next multiple of 128 get zero scales.  pair_half = F > 0 (R = 2F, F a multiple of 64) lays
- * out the scales of a SwiGLU weight [gate; up] in pair order: scale row 128 j + i holds gate
- * row 64 j + i and scale row 128 j + 64 + i up row F + 64 j + i (i < 64), the order in which
- * the SwiGLU program's tiles read gate and up rows.  The codes keep the row order of X. */
+ * it row r, block kb sits at 16 (r % 32) + 4 ((r % 128) / 32) + kb % 4 (the order in which a
+ * 32-lane TMEM copy, repeated into the four lane quarters, places each row's scales where the
+ * block-scaled MMA reads them: row m in lane m, column (m % 128) / 32).  Rows from R up to the
+ * next multiple of 128 get zero scales. */
 CODA_API int coda_quantize_nvfp4(const coda_tensor* X, float s, const coda_tensor* Q, void* block_scales,
-                                 int64_t pair_half, float* amax, void* stream);
+                                 float* amax, void* stream);
 
 /* Bytes of the block scales of an NVFP4 tensor [R, K]: ceil(R / 128) * (K / 64) * 512. */
 CODA_API size_t coda_nvfp4_scale_bytes(int64_t R, int64_t K);
 
 /* NVFP4 MLP with deferred r, the FP8 MLP above with every GEMM operand in NVFP4:
  *   Z = r s_x s_w (X W^T);  a = silu(Z_gate) Z_up;  (a_q, a_sf) = nvfp4(a, s_a);  amax = max|a|
- *   Y = s_a s_wd (a W_d^T) + h;  Y_partials = partial sums of squares of Y  (per 128 columns)
+ *   Y = s_a s_wd (a W_d^T) + h;  Y_partials = partial sums of squares of Y
  * X, W, W_d, a are (codes, block scales); s_a is the caller's delayed scale of a (e.g. the
  * previous step's amax / (6 * 448)).  H and F multiples of 256.  Three launches: row RMS,
  * gate/up GEMM + r + SwiGLU + NVFP4 quantisation, down GEMM + residual + partials. */
@@ -466,7 +464,7 @@ typedef struct coda_mlp_nvfp4_io {
   const void* X_q;           /* [M, H] NVFP4 codes (M x H / 2 bytes) */
   const void* X_sf;          /* block scales of X */
   const void* W_q;           /* [2F, H] NVFP4 codes, gate rows then up rows (gain folded) */
-  const void* W_sf;          /* block scales of W in pair order (pair_half = F) */
+  const void* W_sf;          /* block scales of W */
   const void* W_dq;          /* [H, F] NVFP4 codes */
   const void* W_dsf;         /* block scales of W_d */
   float* r;                  /* out [M] */
@@ -474,7 +472,7 @@ typedef struct coda_mlp_nvfp4_io {
   void* a_sf;                /* out: block scales of a (coda_nvfp4_scale_bytes(M, F)) */
   float* amax;               /* out: 1 float (zeroed by this call on the stream) */
   void* Y;                   /* out [M, H] bf16 */
-  float* Y_partials;         /* out [H/128, M] fp32 */
+  float* Y_partials;         /* out [H/256, M] fp32 */
 } coda_mlp_nvfp4_io;
 CODA_API int coda_mlp_nvfp4(const coda_mlp_nvfp4_io* io, void* stream);
 

@@ -22,19 +22,10 @@ def unpack_codes(b: np.ndarray) -> np.ndarray:
     return out
 
 
-def _scale_rows(R: int, pair_half: int) -> np.ndarray:
-    """Scale row of each tensor row (pair order for a SwiGLU weight [gate; up])."""
-    i = np.arange(R)
-    if pair_half <= 0:
-        return i
-    g = np.where(i < pair_half, i, i - pair_half)
-    return 128 * (g // 64) + np.where(i < pair_half, 0, 64) + g % 64
-
-
-def atom_offsets(R: int, K: int, pair_half: int = 0) -> np.ndarray:
+def atom_offsets(R: int, K: int) -> np.ndarray:
     """Byte offset [R, K / 16] of each row's block scales in the atom layout."""
     kc = K // 64
-    r = _scale_rows(R, pair_half)[:, None]
+    r = np.arange(R)[:, None]
     kb = np.arange(K // 16)[None, :]
     return ((r // 128) * kc + kb // 4) * 512 + 16 * (r % 32) + 4 * ((r % 128) // 32) + kb % 4
 
@@ -43,30 +34,30 @@ def scale_bytes(R: int, K: int) -> int:
     return -(-R // 128) * (K // 64) * 512
 
 
-def to_atoms(sf_codes: np.ndarray, R: int, K: int, pair_half: int = 0) -> np.ndarray:
+def to_atoms(sf_codes: np.ndarray, R: int, K: int) -> np.ndarray:
     """Atom-layout byte buffer (zeros elsewhere) from e4m3 scale bytes [R, K / 16]."""
     buf = np.zeros(scale_bytes(R, K), dtype=np.uint8)
-    buf[atom_offsets(R, K, pair_half)] = sf_codes
+    buf[atom_offsets(R, K)] = sf_codes
     return buf
 
 
-def from_atoms(buf: np.ndarray, R: int, K: int, pair_half: int = 0) -> np.ndarray:
-    return np.asarray(buf, dtype=np.uint8)[atom_offsets(R, K, pair_half)]
+def from_atoms(buf: np.ndarray, R: int, K: int) -> np.ndarray:
+    return np.asarray(buf, dtype=np.uint8)[atom_offsets(R, K)]
 
 
-def oracle_nvfp4(x: np.ndarray, s: float, pair_half: int = 0, device="cuda"):
+def oracle_nvfp4(x: np.ndarray, s: float, device="cuda"):
     """The oracle's NVFP4 quantisation of x, as device tensors the library reads
     (codes, atom-layout scales) plus the oracle's own values (q, sf)."""
     from gemm_epilogue_transformer_tcgen05_gb300 import coda as C
     q, sf = O.nvfp4_quantize(x, s)
     R, K = q.shape
     codes = torch.from_numpy(pack_codes(q)).to(device)
-    scales = torch.from_numpy(to_atoms(O.e4m3_encode(sf), R, K, pair_half)).to(device)
+    scales = torch.from_numpy(to_atoms(O.e4m3_encode(sf), R, K)).to(device)
     return C.Nvfp4(codes, scales, s), q, sf
 
 
-def nvfp4_values(t, R: int, K: int, pair_half: int = 0) -> np.ndarray:
+def nvfp4_values(t, R: int, K: int) -> np.ndarray:
     """float64 values s * sf * q of a device Nvfp4 tensor."""
     q = O.e2m1_decode(unpack_codes(t.codes.cpu().numpy()))
-    sf = O.e4m3_decode(from_atoms(t.scales.cpu().numpy(), R, K, pair_half))
+    sf = O.e4m3_decode(from_atoms(t.scales.cpu().numpy(), R, K))
     return O.nvfp4_dequantize(q, sf, t.s)

@@ -156,16 +156,15 @@ def test_nvfp4_entry_points_validate(L):
     X = _t(FAKE, C.BF16, 256, 512, 512)
     Q = _t(FAKE, C.NVFP4, 256, 512, 512)
     q = L.coda_quantize_nvfp4
-    assert q(None, 1.0, ctypes.byref(Q), f, 0, None, None) == C.ERR_NULL
-    assert q(ctypes.byref(X), 1.0, ctypes.byref(Q), None, 0, None, None) == C.ERR_NULL        # scales missing
-    assert q(ctypes.byref(X), 0.0, ctypes.byref(Q), f, 0, None, None) == C.ERR_SHAPE         # s > 0
-    assert q(ctypes.byref(X), 1.0, ctypes.byref(X), f, 0, None, None) == C.ERR_DTYPE         # Q must be NVFP4
-    assert q(ctypes.byref(X), 1.0, ctypes.byref(Q), f, 100, None, None) == C.ERR_SHAPE       # pair_half % 64
-    assert q(ctypes.byref(X), 1.0, ctypes.byref(Q), ctypes.c_void_p(FAKE + 8), 0, None, None) == C.ERR_ALIGN
-    assert q(ctypes.byref(_t(FAKE, C.BF16, 256, 48, 48)), 1.0, ctypes.byref(_t(FAKE, C.NVFP4, 256, 48, 64)), f, 0,
-             None, None) == C.ERR_SHAPE                                                        # K % 64
-    assert q(ctypes.byref(X), 1.0, ctypes.byref(_t(FAKE, C.NVFP4, 256, 512, 520)), f, 0, None,
-             None) == C.ERR_ALIGN                                                              # ld / 2 % 16
+    assert q(None, 1.0, ctypes.byref(Q), f, None, None) == C.ERR_NULL
+    assert q(ctypes.byref(X), 1.0, ctypes.byref(Q), None, None, None) == C.ERR_NULL        # scales missing
+    assert q(ctypes.byref(X), 0.0, ctypes.byref(Q), f, None, None) == C.ERR_SHAPE         # s > 0
+    assert q(ctypes.byref(X), 1.0, ctypes.byref(X), f, None, None) == C.ERR_DTYPE         # Q must be NVFP4
+    assert q(ctypes.byref(X), 1.0, ctypes.byref(Q), ctypes.c_void_p(FAKE + 8), None, None) == C.ERR_ALIGN
+    assert q(ctypes.byref(_t(FAKE, C.BF16, 256, 48, 48)), 1.0, ctypes.byref(_t(FAKE, C.NVFP4, 256, 48, 64)), f,
+             None, None) == C.ERR_SHAPE                                                     # K % 64
+    assert q(ctypes.byref(X), 1.0, ctypes.byref(_t(FAKE, C.NVFP4, 256, 512, 520)), f, None,
+             None) == C.ERR_ALIGN                                                           # ld / 2 % 16
     # the GEMM with NVFP4 operands
     A = _t(FAKE, C.NVFP4, 256, 512, 512)
     W = _t(FAKE, C.NVFP4, 256, 512, 512)

@@ -1,7 +1,7 @@
 """GPU parity of the NVFP4 path against the fp64 oracle, through the C ABI (oracle reading 9:
 e2m1 codes, e4m3 block scales per 16 K elements, fp32 tensor scales):
 
-* the quantiser, bit-exact in codes and block scales (plain and SwiGLU pair order);
+* the quantiser, bit-exact in codes and block scales;
 * the block-scaled GEMM (plain store), on operands the oracle quantised, at ragged sizes;
 * the gate/up GEMM with r, SwiGLU and a bf16 or NVFP4 output (codes checked against the
   oracle's rounding window, block scales and amax);
@@ -41,8 +41,8 @@ def _scale_of(x):
 
 
 # ------------------------------------------------------------------------- quantiser
-@pytest.mark.parametrize("R,K,pair", [(300, 512, 0), (256, 320, 0), (256, 192, 128)])
-def test_quantize_nvfp4_bit_exact(C, R, K, pair):
+@pytest.mark.parametrize("R,K", [(300, 512), (256, 320), (128, 192)])
+def test_quantize_nvfp4_bit_exact(C, R, K):
     X = _bf16((R, K), 31 + R)
     X[0, :16] = 0.0                                   # an all-zero block: scale 0, codes 0
     X[1, 5] = 1e4                                     # one large value: its block saturates nothing
@@ -51,15 +51,15 @@ def test_quantize_nvfp4_bit_exact(C, R, K, pair):
     Q = C.Nvfp4.empty(R, K, s)
     Q.scales.fill_(0xEE)                              # padding rows must be overwritten with 0
     amax = torch.zeros((1,), device="cuda")
-    C.coda_quantize_nvfp4(dev(X), Q, pair_half=pair, amax=amax)
+    C.coda_quantize_nvfp4(dev(X), Q, amax=amax)
     torch.cuda.synchronize()
     fresh_status()
     q, sf = O.nvfp4_quantize(x, s)
     np.testing.assert_array_equal(L.unpack_codes(Q.codes.cpu().numpy()), O.e2m1_encode(q))
     buf = Q.scales.cpu().numpy()
-    np.testing.assert_array_equal(L.from_atoms(buf, R, K, pair), O.e4m3_encode(sf))
+    np.testing.assert_array_equal(L.from_atoms(buf, R, K), O.e4m3_encode(sf))
     used = np.zeros(buf.size, dtype=bool)
-    used[L.atom_offsets(R, K, pair)] = True
+    used[L.atom_offsets(R, K)] = True
     assert not buf[~used].any(), "scales of padding rows are not zero"
     assert float(amax.item()) == float(np.max(np.abs(x)))
 
@@ -102,7 +102,7 @@ def _swiglu_case(M, H, F, seed):
     h = f64(_bf16((M, H), seed))
     W = f64(_bf16((2 * F, H), seed + 1, 0.015))
     X, qx, sfx = L.oracle_nvfp4(h, _scale_of(h))
-    Wq, qw, sfw = L.oracle_nvfp4(W, _scale_of(W), pair_half=F)
+    Wq, qw, sfw = L.oracle_nvfp4(W, _scale_of(W))
     r = O.rms_scale(h, 1e-6).astype(np.float32)
     Z = r.astype(np.float64)[:, None] * O.linear(O.nvfp4_dequantize(qx, sfx, X.s), O.nvfp4_dequantize(qw, sfw, Wq.s))
     a = O.swiglu(Z[:, :F], Z[:, F:])
@@ -166,14 +166,14 @@ def test_nvfp4_down_gemm_residual_partials(C):
     A, qa, sfa = L.oracle_nvfp4(a, _scale_of(a))
     B, qb, sfb = L.oracle_nvfp4(Wd, _scale_of(Wd))
     Y = torch.empty((M, H), dtype=BF, device="cuda")
-    P = torch.empty((H // 128, M), device="cuda")
+    P = torch.empty((H // 256, M), device="cuda")
     C.coda_gemm_epilogue(A, B, [C.OP_TENSOR_SCALE, C.OP_ADD_SIDE, C.OP_ROW_SUMSQ_PARTIAL], Y,
                          residual=dev(Hres), tensor_scale=A.s * B.s, row_partials=P)
     torch.cuda.synchronize()
     fresh_status()
     ref = O.linear(O.nvfp4_dequantize(qa, sfa, A.s), O.nvfp4_dequantize(qb, sfb, B.s)) + f64(Hres)
     assert_close(f64(Y), ref, TOL_BF16, "Y")
-    assert_close(f64(P), O.partial_sumsq(f64(Y), 128), 1e-4, "partials of the stored Y")
+    assert_close(f64(P), O.partial_sumsq(f64(Y), 256), 1e-4, "partials of the stored Y")
 
 
 # ------------------------------------------------------------------------ the chain
@@ -183,7 +183,7 @@ def _chain(C, M, H, F, seed):
     Wgu = f64(_bf16((2 * F, H), seed + 1, 0.015))
     Wd = f64(_bf16((H, F), seed + 2, 0.015))
     X, qx, sfx = L.oracle_nvfp4(hx, _scale_of(hx))
-    Wq, qw, sfw = L.oracle_nvfp4(Wgu, _scale_of(Wgu), pair_half=F)
+    Wq, qw, sfw = L.oracle_nvfp4(Wgu, _scale_of(Wgu))
     Wdq, qd, sfd = L.oracle_nvfp4(Wd, _scale_of(Wd))
     return h, hx, (X, qx, sfx), (Wq, qw, sfw), (Wdq, qd, sfd)
 
@@ -193,7 +193,7 @@ def _run_chain(C, h, X, Wq, Wdq, s_a, M, H, F):
     a = C.Nvfp4.empty(M, F, s_a)
     amax = torch.empty((1,), device="cuda")
     Y = torch.empty((M, H), dtype=BF, device="cuda")
-    P = torch.empty((H // 128, M), device="cuda")
+    P = torch.empty((H // 256, M), device="cuda")
     C.coda_mlp_nvfp4(dev(h), X, Wq, Wdq, 1e-6, r, a, amax, Y, P)
     torch.cuda.synchronize()
     fresh_status()
@@ -203,15 +203,15 @@ def _run_chain(C, h, X, Wq, Wdq, s_a, M, H, F):
 def test_mlp_nvfp4_chain_small(C):
     M, H, F = 300, 512, 768
     h, hx, (X, qx, sfx), (Wq, qw, sfw), (Wdq, qd, sfd) = _chain(C, M, H, F, 71)
-    pre = O.mlp_nvfp4(hx, qx, sfx, X.s, qw, sfw, Wq.s, qd, sfd, Wdq.s, 1.0, 1e-6, 128)   # amax of a
+    pre = O.mlp_nvfp4(hx, qx, sfx, X.s, qw, sfw, Wq.s, qd, sfd, Wdq.s, 1.0, 1e-6, 256)   # amax of a
     s_a = _scale_of(pre["a"])
-    ref = O.mlp_nvfp4(hx, qx, sfx, X.s, qw, sfw, Wq.s, qd, sfd, Wdq.s, s_a, 1e-6, 128)
+    ref = O.mlp_nvfp4(hx, qx, sfx, X.s, qw, sfw, Wq.s, qd, sfd, Wdq.s, s_a, 1e-6, 256)
     r, a, amax, Y, P = _run_chain(C, h, X, Wq, Wdq, s_a, M, H, F)
     assert_close(f64(r), ref["r"], 1e-5, "r")
     assert abs(float(amax.item()) - ref["amax"]) <= 1e-3 * ref["amax"]
     _check_nvfp4_output(a, ref["a"], s_a, M, F)
     assert_close(f64(Y), ref["Y"], TOL_FP8, "Y")
-    assert_close(f64(P), O.partial_sumsq(f64(Y), 128), 1e-4, "partials of the stored Y")
+    assert_close(f64(P), O.partial_sumsq(f64(Y), 256), 1e-4, "partials of the stored Y")
 
 
 def test_mlp_nvfp4_chain_llama8b_shape_sampled_rows(C):
@@ -220,11 +220,11 @@ def test_mlp_nvfp4_chain_llama8b_shape_sampled_rows(C):
     M, H, F = 16384, 4096, 14336
     h, hx, (X, qx, sfx), (Wq, qw, sfw), (Wdq, qd, sfd) = _chain(C, M, H, F, 81)
     rows = np.concatenate([np.arange(32), np.random.default_rng(5).choice(np.arange(32, M), 64, replace=False)])
-    pre = O.mlp_nvfp4(hx[rows], qx[rows], sfx[rows], X.s, qw, sfw, Wq.s, qd, sfd, Wdq.s, 1.0, 1e-6, 128)
+    pre = O.mlp_nvfp4(hx[rows], qx[rows], sfx[rows], X.s, qw, sfw, Wq.s, qd, sfd, Wdq.s, 1.0, 1e-6, 256)
     s_a = _scale_of(pre["a"]) * 2.0    # headroom for rows outside the sample
-    ref = O.mlp_nvfp4(hx[rows], qx[rows], sfx[rows], X.s, qw, sfw, Wq.s, qd, sfd, Wdq.s, s_a, 1e-6, 128)
+    ref = O.mlp_nvfp4(hx[rows], qx[rows], sfx[rows], X.s, qw, sfw, Wq.s, qd, sfd, Wdq.s, s_a, 1e-6, 256)
     r, a, amax, Y, P = _run_chain(C, h, X, Wq, Wdq, s_a, M, H, F)
     assert_close(f64(r)[rows], ref["r"], 1e-5, "r")
     assert float(amax.item()) >= ref["amax"] * (1 - 1e-3)
     assert_close(f64(Y)[rows], ref["Y"], TOL_FP8, "Y (sampled rows)")
-    assert_close(f64(P)[:, rows], O.partial_sumsq(f64(Y)[rows], 128), 1e-4, "partials (sampled rows)")
+    assert_close(f64(P)[:, rows], O.partial_sumsq(f64(Y)[rows], 256), 1e-4, "partials (sampled rows)")

@@ -1,5 +1,6 @@
 """The test-side NVFP4 layout helpers (code packing, block-scale atoms) on the CPU: packing
-round-trips, and the atom offsets are a one-to-one map into the buffer, in pair order too."""
+round-trips, the atom offsets are a one-to-one map into the buffer, and each row's scales sit
+where the MMA reads them."""
 import numpy as np
 
 import oracle as O
@@ -16,17 +17,19 @@ def test_pack_unpack_round_trip_and_nibble_order():
 
 
 def test_atom_offsets_are_one_to_one():
-    for R, K, pair in [(300, 512, 0), (256, 192, 128), (128, 64, 0)]:
-        off = L.atom_offsets(R, K, pair)
+    for R, K in [(300, 512), (256, 192), (128, 64)]:
+        off = L.atom_offsets(R, K)
         assert off.shape == (R, K // 16)
         assert len(np.unique(off)) == off.size
         assert off.max() < L.scale_bytes(R, K)
         sf = np.arange(off.size, dtype=np.uint64).reshape(off.shape).astype(np.uint8)
-        np.testing.assert_array_equal(L.from_atoms(L.to_atoms(sf, R, K, pair), R, K, pair), sf)
+        np.testing.assert_array_equal(L.from_atoms(L.to_atoms(sf, R, K), R, K), sf)
 
 
-def test_pair_order_puts_gate_and_up_rows_of_a_group_in_one_block():
-    off = L.atom_offsets(256, 64, pair_half=128)
-    # gate row 3 and up row 128 + 3 share scale block 0, at scale rows 3 and 64 + 3
-    assert off[3, 0] == 16 * 3 and off[131, 0] == 16 * 3 + 4 * 2
-    assert off[64, 0] == 512 and off[192, 0] == 512 + 4 * 2   # the next group: the next 128-row block
+def test_atom_rows_match_the_mma_reading_order():
+    # a 32-lane copy of an atom puts its 16-byte row i in lanes i, 32 + i, 64 + i, 96 + i,
+    # four bytes per column; the MMA reads row m in lane m, column (m % 128) / 32: so row m's
+    # four scales must be bytes 4 ((m % 128) / 32) of the atom's row m % 32
+    off = L.atom_offsets(256, 64)
+    for m in (0, 5, 37, 70, 127, 200):
+        assert list(off[m]) == [(m // 128) * 512 + 16 * (m % 32) + 4 * ((m % 128) // 32) + i for i in range(4)]
