@@ -791,8 +791,13 @@ def other_workloads(torch, C, S, args, stream):
     flop = 2 * (2 * M * N * H)
     byt = 2 * (M * N * 3 + M * N * 2 + N * H * 2 + M * H * 3) + 4 * N * H
     roof = max(flop / (pk["bf16_sus"] * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
+    # per kernel: the two GEMMs at the tensor peak plus the RoPE-backward pass (dout and out read,
+    # e written) at the HBM peak
+    roof_k = (flop / (pk["bf16_sus"] * 1e12) + (2 * 3 * M * N + 4 * 2 * M) / (pk["hbm"] * 1e9)) * 1e3
     out["qkv_rope_backward_N2"] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "roofline_ms": roof,
-                                   "roofline_frac": roof / ms, "tokens_per_s": M / (ms * 1e-3), "launches": 4,
+                                   "roofline_frac": roof / ms, "kernel_sum_roofline_ms": roof_k,
+                                   "kernel_sum_roofline_frac": roof_k / ms,
+                                   "tokens_per_s": M / (ms * 1e-3), "launches": 4,
                                    "note": "RoPE backward + row scale pass, dh GEMM + RMSNorm-bwd epilogue, dg "
                                            "column reduce, dW GEMM"}
     del hq, Wq_, gq, Wqf, oq, dq, eq, dhq, dWq, wsq

@@ -86,3 +86,32 @@ def test_dropped_stage_with_side_inputs_in_flight(C, program):
     st3, _ = C.coda_get_device_status()
     assert st3 == C.OK
     assert_close(f64(out2), ref(), TOL_BF16, f"{program} after a timed-out launch")
+
+
+def test_dropped_stage_in_a_block_scaled_nvfp4_gemm(C):
+    """The NVFP4 GEMM, whose MMA thread also copies each stage's block scales into TMEM: a
+    stage that never fills ends the launch through the abort path, and the next launch is
+    exact."""
+    import numpy as np
+    from tests import nvfp4_layout as L
+    M, N, K = 512, 512, 1024
+    g = torch.Generator().manual_seed(67)
+    xa = f64((torch.randn((M, K), generator=g)).to(BF))
+    xb = f64((torch.randn((N, K), generator=g) * 0.05).to(BF))
+    sc = lambda x: float(np.float32(np.max(np.abs(x)) / (6 * 448)))
+    A, qa, sfa = L.oracle_nvfp4(xa, sc(xa))
+    B, qb, sfb = L.oracle_nvfp4(xb, sc(xb))
+    out = torch.zeros((M, N), device="cuda")
+    C.coda_set_watchdog_ms(200)
+    C.coda_inject_dropped_stage(True)
+    C.coda_gemm_epilogue(A, B, [C.OP_TENSOR_SCALE], out, tensor_scale=A.s * B.s)
+    st, site = C.coda_get_device_status()
+    assert st == C.ERR_DEVICE_TIMEOUT, st
+    assert site in (1, 2, 3, 4, 5), site
+    C.coda_set_watchdog_ms(2000)
+    out2 = torch.empty((M, N), device="cuda")
+    C.coda_gemm_epilogue(A, B, [C.OP_TENSOR_SCALE], out2, tensor_scale=A.s * B.s)
+    st2, _ = C.coda_get_device_status()
+    assert st2 == C.OK
+    ref = O.linear(O.nvfp4_dequantize(qa, sfa, A.s), O.nvfp4_dequantize(qb, sfb, B.s))
+    assert_close(f64(out2), ref, 1e-3, "NVFP4 GEMM after a timed-out launch")
