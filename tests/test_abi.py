@@ -192,3 +192,5 @@ def test_nvfp4_entry_points_validate(L):
     assert L.coda_mlp_nvfp4(ctypes.byref(io), None) == C.ERR_SHAPE                            # s_a > 0
     io.s_a, io.W_dsf = 1.0, None
     assert L.coda_mlp_nvfp4(ctypes.byref(io), None) == C.ERR_NULL
+    io.W_dsf, io.M = f, 0
+    assert L.coda_mlp_nvfp4(ctypes.byref(io), None) == C.OK                                   # empty batch: no-op

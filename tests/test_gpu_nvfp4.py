@@ -84,6 +84,21 @@ def test_nvfp4_gemm_store(C, M, N, K):
         pytest.fail(f"max rel err {err:.3e}; {len(rows)} rows (first {rows[:8]}), {len(cols)} cols (first {cols[:8]})")
 
 
+def test_nvfp4_gemm_split_k(C):
+    """Few tiles and a long K: the fp32 GEMM splits K across CTA pairs and reduce-adds the
+    slices into the zeroed output (each slice's MMAs and scale copies start mid-K)."""
+    M, N, K = 256, 256, 16384
+    xa, xb = f64(_bf16((M, K), 45)), f64(_bf16((N, K), 46, 0.02))
+    A, qa, sfa = L.oracle_nvfp4(xa, _scale_of(xa))
+    B, qb, sfb = L.oracle_nvfp4(xb, _scale_of(xb))
+    out = torch.full((M, N), float("nan"), device="cuda")
+    C.coda_gemm_epilogue(A, B, [C.OP_TENSOR_SCALE], out, tensor_scale=A.s * B.s)
+    torch.cuda.synchronize()
+    fresh_status()
+    ref = O.linear(O.nvfp4_dequantize(qa, sfa, A.s), O.nvfp4_dequantize(qb, sfb, B.s))
+    assert_close(f64(out), ref, 1e-3, "split-K fp32 out")
+
+
 def test_nvfp4_gemm_bf16_out_and_k_equal_one_stage(C):
     M, N, K = 256, 256, 256
     xa, xb = f64(_bf16((M, K), 43)), f64(_bf16((N, K), 44, 0.02))
