@@ -24,7 +24,8 @@ def C():
 BF = torch.bfloat16
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 288, 200), (513, 768, 1000)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 288, 200), (513, 768, 1000),
+                                   (1, 32, 8), (7, 64, 16)])   # degenerate: one row, the narrowest N, K of one TMA row
 def test_plain_bf16(C, M, N, K):
     A = seeded((M, K), 1, dtype=BF)
     W = seeded((N, K), 2, std=0.05, dtype=BF)
