@@ -740,8 +740,58 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t tacc = tmem_base + ((uint32_t)(32 * q) << 16) + acc * C::UN;
       float rowacc = 0.f;
 
+      // NVFP4 SwiGLU with its one accumulator: the tile's SwiGLU outputs (4 chunks of 32 per
+      // thread) are formed from TMEM first and TMEM is handed back before they are quantised and
+      // stored, so that the next tile's MMAs run under that work.
+      constexpr bool EARLY = C::FP4 && C::DUAL && C::OUT_DT == DT_E2M1;
+      if constexpr (EARLY) {
+        float abuf[C::NCHUNK][32];
+        const float sc = ts * rs;
+#pragma unroll
+        for (int c = 0; c < C::NCHUNK; ++c) {
+          uint32_t v[32], u[32];
+          ptx::tmem_ld32(tacc + 32 * c, v);
+          ptx::tmem_ld32(tacc + C::UN / 2 + 32 * c, u);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float G = __uint_as_float(v[j]) * sc, U = __uint_as_float(u[j]) * sc;
+            const float a = silu_f(G) * U;
+            amax_local = fmaxf(amax_local, fabsf(a));
+            abuf[c][j] = a;
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (C::CG == 2)
+            ptx::mbar_arrive_cluster(ptx::mapa(TEMPTY_BAR(acc), 0));
+          else
+            ptx::mbar_arrive(TEMPTY_BAR(acc));
+        }
+#pragma unroll
+        for (int c = 0; c < C::NCHUNK; ++c) {
+          const int col0 = n0 + 32 * c;
+          uint32_t q4[4];
+          const uint32_t sfc =
+              nvfp4_block16(abuf[c], p.fp4_scale, q4) | (nvfp4_block16(abuf[c] + 16, p.fp4_scale, q4 + 2) << 8);
+          if (row_ok && col0 < p.N)
+            *reinterpret_cast<uint16_t*>(p.out_sf + sf_offset(row, col0 / 16, p.out_sf_kc)) = (uint16_t)sfc;
+          const uint32_t oslot = out_base + (c & 1) * C::OUTSET;
+          if (lane == 0) ptx::bulk_wait_read<1>();  // the group that last used this set is done reading
+          __syncwarp();
+          ptx::st_shared_v4(oslot + 16 * lane, q4[0], q4[1], q4[2], q4[3]);   // 32 rows of 16 bytes
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (col0 < p.N && r0 < p.M) ptx::tma_store_2d_hint(&tmOut, col0 / 2, r0, oslot, stream_pol);
+            ptx::bulk_commit();
+          }
+        }
+      }
+
 #pragma unroll 1
-      for (int c = 0; c < C::NCHUNK; ++c) {
+      for (int c = 0; c < (EARLY ? 0 : C::NCHUNK); ++c) {
         float x[32];
         float xu[C::DUAL ? 32 : 1];
         {
