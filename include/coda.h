@@ -166,7 +166,7 @@ typedef struct coda_side_inputs {
   float out_scale;              /* e4m3 outputs: 1 / scale before the cast (> 0); XENT_BWD: dloss / M */
   const int32_t* row_index;     /* XENT_PARTIAL, XENT_BWD: [M] target class of each row, in [0, N) */
   const void* a_block_scales;   /* NVFP4 A: its block scales (16-byte aligned) */
-  const void* w_block_scales;   /* NVFP4 W: its block scales (16-byte aligned; SWIGLU: pair order) */
+  const void* w_block_scales;   /* NVFP4 W: its block scales (16-byte aligned) */
   float out_fp4_scale;          /* NVFP4 out: the tensor scale s of the stored codes (> 0) */
 } coda_side_inputs;
 
