@@ -752,6 +752,20 @@ def other_workloads(torch, C, S, args, stream):
     ms_f = _time(torch, fwd_train, stream, steps)
     out["block_forward_train_mode"] = {"ms": ms_f, "tokens_per_s": M / (ms_f * 1e-3),
                                        "note": "G1 (+ u = h g), reduce, G2 saving Z = [G|U], G3"}
+    # the other way to apply the RMSNorm gain: folded into W_gu once per weight update, so that
+    # G1 stores only h and the gate/up GEMM reads h
+    Wf = torch.empty_like(d["W_gu"])
+    fold = lambda: C.coda_fold_gain(d["W_gu"], d["g"], Wf, stream=stream)
+    fold()
+    fwd_fold = lambda: C.coda_block_forward(d["O"], d["R"], d["W_o"], Wf, d["W_d"], EPS, h, r, a, Y, wsf,
+                                            stream=stream)
+    ms_ff = _time(torch, fwd_fold, stream, steps)
+    ms_fold = _time(torch, fold, stream, steps)
+    out["block_forward_folded_gain"] = {"ms": ms_ff, "tokens_per_s": M / (ms_ff * 1e-3), "fold_ms": ms_fold,
+                                        "plus_fold_ms": ms_ff + ms_fold,
+                                        "note": "C1 with W_gu' = W_gu diag(g) folded beforehand (timed on its own): "
+                                                "G1 stores h only, G2 reads h; the headline broadcasts g instead"}
+    del Wf
     del d, h, u, r, a, Y, Z, e, dh, dO, dW_o, dW_gu, dW_d, dg, c, wsb, wsf
     torch.cuda.empty_cache()
     # C3: QKV projection + deferred r + RoPE (r from a full-row pass over h)
