@@ -1080,7 +1080,7 @@ int coda_qkv_rope(const coda_qkv_rope_io* io, void* stream) {
   if (!io) return CODA_ERR_NULL;
   if (!io->h || !io->W_qkv || !io->rope_cos || !io->rope_sin || !io->r || !io->out) return CODA_ERR_NULL;
   const int64_t M = io->M, H = io->H, N = io->N;
-  if (M < 0 || H < 8 || N < 32) return CODA_ERR_SHAPE;
+  if (M < 0 || H < 8 || N < 32 || io->seq_len < 1) return CODA_ERR_SHAPE;
   if (M == 0) return CODA_OK;
   int st;
   coda_tensor h = mk(io->h, CODA_BF16, M, H, H);

@@ -232,12 +232,24 @@ def test_qkv_rope_small(C):
     assert_close(f64(out), ref["out"], TOL_BF16, "qkv")
 
 
+def test_qkv_rope_ragged_rows_every_row(C):
+    """3300 tokens (a ragged last tile of 228 rows, RoPE positions wrapping at 1024) x 3072
+    columns: every row is checked against the oracle."""
+    M, H, seq, hd = 3300, 256, 1024, 64
+    inp = S.qkv_inputs(M, H, 3072, seed=4)
+    out, r = _run_qkv(C, inp, seq, hd, 2560)
+    ref = O.qkv_rope(f64(inp["h"]), f64(inp["g"]), f64(inp["W_qkv"]), inp["eps"], seq, 2560, hd, 500000.0)
+    assert_close(f64(r), ref["r"], TOL_BF16, "r")
+    assert_close(f64(out), ref["out"], TOL_BF16, "qkv")
+    assert_close(f64(out)[3072:], ref["out"][3072:], TOL_BF16, "qkv, rows of the last tile")
+
+
 @pytest.mark.slow
 def test_qkv_rope_full_size_sampled_rows(C):
     M, H, seq, hd = 16384, 2048, 1024, 64
     inp = S.qkv_inputs(M, H, 3072, seed=0)
     out, r = _run_qkv(C, inp, seq, hd, 2560)
-    rows = sample_rows(M, seed=3)
+    rows = np.union1d(sample_rows(M, seed=3), np.arange(M - 64, M))   # and rows of the last block
     hq = f64(inp["h"])[rows]
     y = O.rmsnorm(hq, f64(inp["g"]), inp["eps"]) @ f64(inp["W_qkv"]).T
     ref = O.rope_rotate(y, rows % seq, 2560, hd, 500000.0)
