@@ -113,3 +113,36 @@ def test_fp8_and_qkv_chains_same_with_and_without_overlap(C):
             torch.testing.assert_close(o[k], ref[k], rtol=1e-5, atol=1e-6, msg=k)
         else:
             assert torch.equal(o[k], ref[k]), k
+
+
+def test_nvfp4_chain_same_with_and_without_overlap(C):
+    """The NVFP4 quantiser and MLP chain (whose GEMMs stream their operands early): the same
+    codes, scales, amax and Y with the overlap off, on, and issued back to back."""
+    M, H, F = 384, 512, 768
+    ni = S.nvfp4_mlp_inputs(M, H, F, seed=9, device="cuda")
+    sc = lambda t: float(t.abs().max()) / (6 * 448)
+    X, W, Wd = C.Nvfp4.empty(M, H, sc(ni["h"])), C.Nvfp4.empty(2 * F, H, sc(ni["W_gu"])), C.Nvfp4.empty(H, F, sc(ni["W_d"]))
+    r, amax = torch.empty((M,), device="cuda"), torch.empty((1,), device="cuda")
+    a = C.Nvfp4.empty(M, F, 0.01)
+    Y = torch.empty((M, H), dtype=BF, device="cuda")
+    P = torch.empty((H // 256, M), device="cuda")
+    outs = [X.codes, X.scales, W.codes, W.scales, Wd.codes, Wd.scales, r, a.codes, a.scales, amax, Y, P]
+
+    def run():
+        for src, dst in ((ni["W_gu"], W), (ni["W_d"], Wd), (ni["h"], X)):
+            C.coda_quantize_nvfp4(src, dst)
+        C.coda_mlp_nvfp4(ni["h"], X, W, Wd, 1e-6, r, a, amax, Y, P)
+
+    C.coda_set_launch_overlap(False)
+    run()
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in outs]
+    C.coda_set_launch_overlap(True)
+    for t in outs:
+        t.zero_()
+    for _ in range(10):
+        run()
+    torch.cuda.synchronize()
+    fresh_status()
+    for got, want in zip(outs, ref):
+        assert torch.equal(got, want)
