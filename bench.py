@@ -516,6 +516,39 @@ def run_coda(args, world, rank, local):
     # back to back, as in training)
     cold_ms = cold_l2(torch, step, stream, max(5, min(args.steps, 50))) if rank == 0 else None
 
+    # ---- per-kernel device times: a separate short run with events between the four launches
+    # (kept out of the timed region, where extra events could hold back the launch overlap)
+    per_kernel = None
+    if rank == 0:
+        n_k = max(5, min(args.steps, 100))
+        kev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_k)]
+        calls = [lambda: C.coda_gemm_epilogue(d["O"], d["W_o"], [C.OP_ADD_SIDE, C.OP_ROW_SUMSQ_PARTIAL,
+                                                                 C.OP_STORE_COL_SCALED], h, residual=d["R"],
+                                              row_partials=P, col_scale=d["g"], store_aux=u, stream=stream),
+                 lambda: C.coda_rms_partial_reduce(P, M, H, EPS, r, stream=stream),
+                 lambda: C.coda_gemm_epilogue(u, d["W_gu"], [C.OP_ROW_SCALE, C.OP_SWIGLU], a, row_scale=r,
+                                              stream=stream),
+                 lambda: C.coda_gemm_epilogue(a, d["W_d"], [C.OP_ADD_SIDE], Y, residual=h, stream=stream)]
+        for i in range(3 + n_k):
+            for j, call in enumerate(calls):
+                if i >= 3:
+                    kev[i - 3][j].record(stream)
+                call()
+            if i >= 3:
+                kev[i - 3][4].record(stream)
+        torch.cuda.synchronize()
+        pk_ = peaks()
+        per_kernel = {}
+        for j, name in enumerate(("G1", "reduce", "G2", "G3")):
+            k_ms = statistics.mean(e[j].elapsed_time(e[j + 1]) for e in kev)
+            entry = {"ms": k_ms, "algorithmic_bytes": BYTES[name]}
+            if name in FLOP:
+                entry.update(tflops=FLOP[name] / (k_ms * 1e-3) / 1e12,
+                             frac_of_sustained=FLOP[name] / (k_ms * 1e-3) / 1e12 / pk_["bf16_sus"])
+            else:
+                entry.update(gbs=BYTES[name] / (k_ms * 1e-3) / 1e9, bound="launch latency")
+            per_kernel[name] = entry
+
     # ---- the other chains of the hot path, device-timed the same way (fewer steps)
     others = None
     if not args.no_others and rank == 0:
@@ -565,6 +598,9 @@ def run_coda(args, world, rank, local):
     if graph_ms:
         line["cuda_graph"] = {"ms_per_step": graph_ms, "tokens_per_s": M / (graph_ms * 1e-3),
                               "note": "10 steps captured once in a CUDA graph, replayed"}
+    if per_kernel:
+        line["per_kernel"] = dict(per_kernel, note="events between the four launches in a separate run of the "
+                                                   "same chain; TFLOP/s against the measured sustained bf16 peak")
     if others:
         line["other_workloads"] = others
     if compare:
