@@ -284,8 +284,8 @@ def _fp8_checks(inp, rows, r, aq, Y, P, s_a, ref):
     assert_close(f64(P)[:, rows], ref["P"], TOL_FP8, "Y partials")
 
 
-def test_fp8_mlp_small(C):
-    M, H, F = 512, 512, 768
+@pytest.mark.parametrize("M,H,F", [(512, 512, 768), (300, 256, 384)])   # the second ragged in M and in tiles
+def test_fp8_mlp_small(C, M, H, F):
     inp = S.fp8_mlp_inputs(M, H, F, seed=0)
     rows = np.arange(M)
     s_a = float(_fp8_oracle(inp, rows, 1.0)["amax"]) / 448.0   # delayed scaling from a prior pass
