@@ -93,6 +93,28 @@ def _sim_forward_rows(inp, rows, gain="broadcast"):
     return SIM.block_forward(x["O"][rows], x["R"][rows], x["W_o"], x["g"], x["W_gu"], x["W_d"], inp["eps"], gain)
 
 
+def test_block_forward_zero_and_constant_rows(C):
+    """Degenerate rows of the RMSNorm: a zero row of h (O and R zero) has r = (0 + eps)^(-1/2)
+    exactly and zero outputs; rows where O W_o^T + R is zero but for one column keep r finite;
+    the other rows are unaffected."""
+    M, H, F = 300, 256, 384
+    inp = S.block_inputs(M, H, F, seed=11)
+    inp["O"][:4] = 0
+    inp["R"][:4] = 0                                          # rows 0-3: h = 0
+    inp["O"][4:6] = 0
+    inp["R"][4:6] = 0
+    inp["R"][4:6, 7] = 3.0                                   # rows 4, 5: h = 3 e_7
+    out, _ = _run_block_forward(C, inp)
+    eps = inp["eps"]
+    r = f64(out["r"])
+    np.testing.assert_allclose(r[:4], 1.0 / np.sqrt(eps), rtol=1e-6)
+    np.testing.assert_allclose(r[4:6], 1.0 / np.sqrt(9.0 / H + eps), rtol=1e-6)   # one nonzero a: |a| / sqrt(d)
+    assert not f64(out["Y"])[:4].any() and not f64(out["a"])[:4].any()
+    ref = _oracle_forward_rows(inp, np.arange(M))
+    assert_close(f64(out["Y"]), ref["Y"], TOL_BF16, "Y")
+    assert_close(r, ref["r"], TOL_BF16, "r")
+
+
 @pytest.mark.parametrize("gain", ["broadcast", "fold"])
 @pytest.mark.parametrize("M,H,F", [(640, 512, 1024), (300, 256, 384)])
 def test_block_forward_small(C, M, H, F, gain):
