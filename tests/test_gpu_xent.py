@@ -92,6 +92,27 @@ def _run_bwd(C, fwd, dv, dloss):
     return o
 
 
+def test_lm_head_xent_uniform_logits_closed_form(C):
+    """A zero LM head makes every logit 0: the loss of each row is log V, the gradient of the
+    logits is r dloss (1/V - onehot) / M, and no gradient reaches h (c = 0, t = 0)."""
+    M, H, V = 300, 256, 992
+    inp = S.lm_head_inputs(M, H, V, seed=2)
+    inp["W_v"] = torch.zeros_like(inp["W_v"])
+    fwd, dv = _run_fwd(C, inp)
+    np.testing.assert_allclose(f64(fwd["lse"]), np.log(V), rtol=1e-6)
+    np.testing.assert_allclose(f64(fwd["loss"]), np.log(V), rtol=1e-6)
+    np.testing.assert_allclose(float(fwd["mean"].item()), np.log(V), rtol=1e-6)
+    dloss = 1.0
+    bwd = _run_bwd(C, fwd, dv, dloss)
+    r = f64(fwd["r"])
+    onehot = np.zeros((M, V))
+    onehot[np.arange(M), inp["targets"].numpy()] = 1.0
+    e_ref = r[:, None] * dloss * (1.0 / V - onehot) / M
+    assert_close(f64(bwd["e"]), e_ref, TOL_BF16, "e")
+    assert not f64(bwd["dh"]).any(), "dh must be zero"
+    assert not f64(bwd["c"]).any(), "c must be zero"
+
+
 @pytest.mark.parametrize("M,H,V", [(300, 256, 992), (512, 512, 4096)])
 def test_lm_head_xent_small(C, M, H, V):
     inp = S.lm_head_inputs(M, H, V, seed=1, w_std=0.1)
