@@ -171,6 +171,20 @@ def _run_block_backward(C, inp, fwd_out):
     return o
 
 
+def test_block_backward_zero_output_gradient(C):
+    """dY = 0: every gradient of the block is exactly zero (nothing stale from the workspace,
+    the partial buffers or a previous call leaks in); the buffers start non-zero."""
+    M, H, F = 300, 256, 384
+    inp = S.block_inputs(M, H, F, seed=12, with_grad=True)
+    fwd, _ = _run_block_forward(C, inp)
+    warm = _run_block_backward(C, inp, fwd)                  # a call with a real dY first
+    assert f64(warm["dh"]).any()
+    inp["dY"] = torch.zeros_like(inp["dY"])
+    o = _run_block_backward(C, inp, fwd)
+    for k in ("e", "dh", "dO", "dW_o", "dW_gu", "dW_d", "dg", "c"):
+        assert not f64(o[k]).any(), k
+
+
 @pytest.mark.parametrize("M,H,F", [(640, 512, 1024), (300, 256, 384)])
 def test_block_backward_small(C, M, H, F):
     inp = S.block_inputs(M, H, F, seed=0, with_grad=True)
