@@ -357,3 +357,43 @@ def test_split_k_reduce_add(C, M, N, K, colscale):
     if colscale:
         ref = ref * f64(g)[None, :]
     assert_close(f64(out), ref, 1e-5, "split-K X^T Y")
+
+
+def test_padded_leading_dimensions(C):
+    """Operands, residual and output as column slices of wider buffers (ld > cols): the tensor
+    maps take their strides from ld, and nothing outside the slices is written."""
+    M, N, K = 300, 256, 200
+    A_full = seeded((M, K + 56), 80, dtype=BF)                 # ld 256 for a [300, 200] A
+    W_full = seeded((N, K + 24), 81, std=0.05, dtype=BF)        # ld 224 for a [256, 200] W
+    R_full = seeded((M, N + 64), 82, dtype=BF)
+    A, W, R = dev(A_full)[:, :K], dev(W_full)[:, :K], dev(R_full)[:, 8:8 + N]
+    out_full = torch.full((M, N + 32), 7.0, dtype=BF, device="cuda")
+    out = out_full[:, 16:16 + N]
+    C.coda_gemm_epilogue(A, W, [C.OP_ADD_SIDE], out, residual=R)
+    torch.cuda.synchronize()
+    fresh_status()
+    ref = O.linear(f64(A_full)[:, :K], f64(W_full)[:, :K]) + f64(R_full)[:, 8:8 + N]
+    assert_close(f64(out), ref, TOL_BF16, "A W^T + R through padded views")
+    got = f64(out_full)
+    assert np.all(got[:, :16] == 7.0) and np.all(got[:, 16 + N:] == 7.0), "wrote outside the output slice"
+
+
+def test_nvfp4_padded_codes(C):
+    """NVFP4 operands whose code rows are wider than K / 2 bytes (ld > cols)."""
+    from tests import nvfp4_layout as L
+    M, N, K = 256, 256, 512
+    g = torch.Generator().manual_seed(83)
+    xa = f64(torch.randn((M, K), generator=g).to(BF))
+    xb = f64((torch.randn((N, K), generator=g) * 0.05).to(BF))
+    sc = lambda x: float(np.float32(np.max(np.abs(x)) / (6 * 448)))
+    A, qa, sfa = L.oracle_nvfp4(xa, sc(xa))
+    B, qb, sfb = L.oracle_nvfp4(xb, sc(xb))
+    pad = torch.zeros((M, K // 2 + 48), dtype=torch.uint8, device="cuda")
+    pad[:, :K // 2] = A.codes
+    A.codes = pad[:, :K // 2]                                   # rows K/2 + 48 bytes apart
+    out = torch.empty((M, N), device="cuda")
+    C.coda_gemm_epilogue(A, B, [C.OP_TENSOR_SCALE], out, tensor_scale=A.s * B.s)
+    torch.cuda.synchronize()
+    fresh_status()
+    ref = O.linear(O.nvfp4_dequantize(qa, sfa, A.s), O.nvfp4_dequantize(qb, sfb, B.s))
+    assert_close(f64(out), ref, 1e-3, "NVFP4 GEMM with padded code rows")
