@@ -65,7 +65,7 @@ def test_quantize_nvfp4_bit_exact(C, R, K):
 
 
 # ------------------------------------------------------------- block-scaled GEMM
-@pytest.mark.parametrize("M,N,K", [(300, 384, 512), (1024, 1024, 2048), (128, 128, 256)])
+@pytest.mark.parametrize("M,N,K", [(300, 384, 512), (1024, 1024, 2048), (128, 128, 256), (1, 128, 256)])
 def test_nvfp4_gemm_store(C, M, N, K):
     xa = f64(_bf16((M, K), 41, 2.0))
     xb = f64(_bf16((N, K), 42, 0.05))
