@@ -106,6 +106,8 @@ enum : int {
   SITE_MMA_FULL = 3,
   SITE_EPI_TMEM_FULL = 4,
   SITE_EPI_SIDE = 5,
+  SITE_SCALES_FULL = 6,   // NVFP4 scale warp / block scales in shared memory
+  SITE_MMA_SCALES = 7,    // MMA / block scales in TMEM (both CTAs)
 };
 
 struct GemmParams {
@@ -187,7 +189,10 @@ struct GemmCfg {
   static_assert(NCHUNK % NSS == 0, "a chunk and the next tile's chunk NCHUNK later share a ring slot");
   static constexpr int EPI_WARP_BYTES = NSS * NS * SSLOT + 2 * OUTSET;
   static constexpr int EPI_BYTES = NUM_EPI_WARPS * EPI_WARP_BYTES;
-  static constexpr int BAR_BYTES = 320;
+  // NVFP4: four scale warps write the block scales into TMEM (see the kernel)
+  static constexpr int SF_WARPS = FP4 ? 4 : 0;
+  static constexpr int THREADS = NUM_THREADS + 32 * SF_WARPS;
+  static constexpr int BAR_BYTES = FP4 ? 384 : 320;
   static constexpr int STAGES_FIT = (MAX_SMEM - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
   static constexpr int MAX_STAGES = FP4 ? 8 : 6;
   static constexpr int STAGES = STAGES_FIT > MAX_STAGES ? MAX_STAGES : STAGES_FIT;
@@ -197,11 +202,14 @@ struct GemmCfg {
   static constexpr int ACC = FP4 ? 1 : 2;   // accumulators in TMEM
   static_assert(ACC * UN + STAGES * SF_COLS <= TMEM_COLS, "TMEM columns");
   static_assert(UN % 128 == 0 && UN <= UMMA_N && B_ROWS % B_BOX == 0, "MMA N");
-  static_assert(!FP4 || (!A_MN && !B_MN && !AUX && UN == 256), "NVFP4: K-major operands, MMA N 256");
+  static_assert(!FP4 || (!A_MN && !B_MN && !AUX && UN == 256 && CG == 2), "NVFP4: K-major operands, CTA pairs, MMA N 256");
   static_assert(OUT_DT != DT_E2M1 || (FP4 && EPI == EPI_SWIGLU), "e2m1 output: NVFP4 SwiGLU");
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(STAGES >= 2, "shared memory budget");
-  static_assert(8 * (2 * STAGES + 5 + NSS * NUM_EPI_WARPS) + 8 <= BAR_BYTES, "barrier area");
+  // barriers: full and empty per stage, 2 + 2 accumulator, side loads, done; NVFP4 adds per
+  // stage the scales-landed (this CTA) and scales-in-TMEM (leader) barriers
+  static constexpr int NBAR = 2 * STAGES + 5 + NSS * NUM_EPI_WARPS + (FP4 ? 2 * STAGES : 0);
+  static_assert(8 * NBAR + 8 <= BAR_BYTES, "barrier area");
   static_assert(!(A_MN || B_MN) || KIND != KIND_TF32, "MN-major operands are bf16 or e4m3");
   // MN-major operands: a 128-byte swizzle row holds MN_ATOM elements of M (or N); one atom is
   // BK rows of K; a 128-row tile is BM / MN_ATOM atoms; one MMA consumes UMMA_K rows of K
@@ -224,12 +232,6 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-// The same without swizzle: 8-row groups of 16-byte rows, SBO bytes apart (NVFP4 scale atoms).
-__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
-}
-
 // Tile order.  Tiles come in groups of group_n consecutive N-tiles; inside a group the
 // N-tile index runs fastest, then the M-tile.  The CTAs working at the same time then share
 // a few A row-blocks and one group's slice of B, which stays resident in L2 while the group
@@ -414,7 +416,7 @@ __device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.
 
 // =====================================================================================
 template <class C>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(C::THREADS, 1)
     gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmSide0,
                          const __grid_constant__ CUtensorMap tmSide1, const __grid_constant__ CUtensorMap tmAux,
@@ -426,7 +428,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t sm_stage = base;
   const uint32_t sm_epi = base + C::STAGES * C::STAGE_BYTES;
   const uint32_t sm_bar = sm_epi + C::EPI_BYTES;
-  const int NBAR = 2 * C::STAGES + 5 + C::NSS * NUM_EPI_WARPS;
+  const int NBAR = C::NBAR;
   uint8_t* misc = smem_raw + (sm_bar - raw) + 8 * NBAR;
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
@@ -437,6 +439,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #define TEMPTY_BAR(a) (sm_bar + 8u * (2 * C::STAGES + 2 + (a)))
 #define SIDE_BAR(w, s) (sm_bar + 8u * (2 * C::STAGES + 4 + C::NSS * (w) + (s)))
 #define DONE_BAR (sm_bar + 8u * (2 * C::STAGES + 4 + C::NSS * NUM_EPI_WARPS))
+#define SFULL_BAR(s) (sm_bar + 8u * (2 * C::STAGES + 5 + C::NSS * NUM_EPI_WARPS + (s)))
+#define SREADY_BAR(s) (sm_bar + 8u * (3 * C::STAGES + 5 + C::NSS * NUM_EPI_WARPS + (s)))
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -456,6 +460,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int w = 0; w < NUM_EPI_WARPS; ++w)
       for (int s = 0; s < C::NSS; ++s) ptx::mbar_init(SIDE_BAR(w, s), 1);
     ptx::mbar_init(DONE_BAR, 1);
+    if constexpr (C::FP4) {
+      for (int s = 0; s < C::STAGES; ++s) {
+        ptx::mbar_init(SFULL_BAR(s), 1);                  // this CTA's producer + scale bytes
+        ptx::mbar_init(SREADY_BAR(s), C::SF_WARPS * C::CG);   // every scale warp of the pair
+      }
+    }
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -519,8 +529,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t sa = sm_stage + stage * C::STAGE_BYTES;
             const uint32_t sb = sa + A_STAGE_BYTES;
             const int k0 = kb * C::K_COORD;
-            // the leader's full barrier counts the bytes of both CTAs of a pair
-            if (leader) ptx::mbar_arrive_expect_tx(fb, C::CG * C::STAGE_BYTES);
+            // the leader's full barrier counts the operand bytes of both CTAs of a pair
+            if (leader) ptx::mbar_arrive_expect_tx(fb, C::CG * (A_STAGE_BYTES + C::B_STAGE_BYTES));
             auto load = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1, uint64_t pol) {
               if constexpr (C::CG == 2)
                 ptx::tma_load_2d_pair(dst, m, c0, c1, ptx::mapa(fb, 0), pol);
@@ -553,14 +563,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if constexpr (C::FP4) {
               // block scales: KSTEPS atoms (one per MMA) for this CTA's A rows, then for each 128
               // rows of the tile's N (SwiGLU: the gate rows' block, then the up rows'); an atom
-              // row of the maps is one 512-byte atom
+              // row of the maps is one 512-byte atom.  They land on this CTA's own barrier,
+              // which its scale warps wait on.
               const uint32_t ssf = sb + C::B_STAGE_BYTES;
+              const uint32_t sfb_bar = SFULL_BAR(stage);
               const int kc = p.K / 64;
-              load(ssf, &tmSFA, 0, (m0 / 128) * kc + KSTEPS * kb, normal);
+              ptx::mbar_arrive_expect_tx(sfb_bar, C::SF_A_BYTES + C::SF_B_BYTES);
+              ptx::tma_load_2d_hint(ssf, &tmSFA, 0, (m0 / 128) * kc + KSTEPS * kb, sfb_bar, normal);
 #pragma unroll
               for (int j = 0; j < C::UN / 128; ++j) {
                 const int blk = C::DUAL ? (j == 0 ? nb : p.up_offset / 128 + nb) : nb * (C::UN / 128) + j;
-                load(ssf + C::SF_A_BYTES + KSTEPS * 512 * j, &tmSFB, 0, blk * kc + KSTEPS * kb, keep);
+                ptx::tma_load_2d_hint(ssf + C::SF_A_BYTES + KSTEPS * 512 * j, &tmSFB, 0, blk * kc + KSTEPS * kb,
+                                      sfb_bar, keep);
               }
             }
             issued_any |= 1u << stage;
@@ -605,20 +619,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sa = sm_stage + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + A_STAGE_BYTES;
           if constexpr (C::FP4) {
-            // this stage's block scales into its TMEM columns (A: 4 per MMA; B: 4 per MMA and
-            // 128 rows of N), then the block-scaled MMAs; the copies and the MMAs run in issue order
-            const uint32_t ssf = sb + C::B_STAGE_BYTES;
+            // the scale warps of both CTAs have written this stage's block scales into TMEM
+            // (A: 4 columns per MMA; B: 4 per MMA and 128 rows of N)
+            if (!bwait(SREADY_BAR(stage), phase, watch, SITE_MMA_SCALES)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
             const uint32_t tsa = tmem_base + C::ACC * C::UN + stage * C::SF_COLS;
             const uint32_t tsb = tsa + 4 * KSTEPS;
             constexpr int NB128 = C::UN / 128;
-#pragma unroll
-            for (int k = 0; k < KSTEPS; ++k) {
-              ptx::tmem_cp_32x128b_x4<C::CG>(tsa + 4 * k, smem_desc_plain(ssf + 512 * k, 128, 128));
-#pragma unroll
-              for (int j = 0; j < NB128; ++j)
-                ptx::tmem_cp_32x128b_x4<C::CG>(tsb + 4 * (NB128 * k + j),
-                                               smem_desc_plain(ssf + C::SF_A_BYTES + KSTEPS * 512 * j + 512 * k, 128, 128));
-            }
 #pragma unroll
             for (int k = 0; k < KSTEPS; ++k) {
               const uint64_t ad = smem_desc(sa + k * 32, 16, 1024);
@@ -650,7 +660,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       drain_wait(DONE_BAR, 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 2 + NUM_EPI_WARPS) {
     // ------------------------------------------------------------ epilogue warps
     const int ew = warp - 2;  // staging ownership
     const int q = warp & 3;   // TMEM lane quadrant this warp may read
@@ -741,24 +751,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float rowacc = 0.f;
 
       // NVFP4 SwiGLU with its one accumulator: the tile's SwiGLU outputs (4 chunks of 32 per
-      // thread) are formed from TMEM first and TMEM is handed back before they are quantised and
-      // stored, so that the next tile's MMAs run under that work.
+      // thread, read 16 columns at a time) are formed from TMEM first and TMEM is handed back
+      // before they are quantised and stored, so that the next tile's MMAs run under that work.
       constexpr bool EARLY = C::FP4 && C::DUAL && C::OUT_DT == DT_E2M1;
       if constexpr (EARLY) {
         float abuf[C::NCHUNK][32];
         const float sc = ts * rs;
 #pragma unroll
-        for (int c = 0; c < C::NCHUNK; ++c) {
-          uint32_t v[32], u[32];
-          ptx::tmem_ld32(tacc + 32 * c, v);
-          ptx::tmem_ld32(tacc + C::UN / 2 + 32 * c, u);
+        for (int c = 0; c < 2 * C::NCHUNK; ++c) {
+          uint32_t v[16], u[16];
+          ptx::tmem_ld16(tacc + 16 * c, v);
+          ptx::tmem_ld16(tacc + C::UN / 2 + 16 * c, u);
           ptx::tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
+          for (int j = 0; j < 16; ++j) {
             const float G = __uint_as_float(v[j]) * sc, U = __uint_as_float(u[j]) * sc;
             const float a = silu_f(G) * U;
             amax_local = fmaxf(amax_local, fabsf(a));
-            abuf[c][j] = a;
+            abuf[c / 2][16 * (c % 2) + j] = a;
           }
         }
         ptx::tc_fence_before();
@@ -1119,6 +1129,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     __syncwarp();
+  } else {
+    // ------------------------------------------------------------ scale warps (NVFP4)
+    // Warp w writes TMEM lane quarter w % 4 of this CTA.  The block-scaled MMA reads row m of
+    // A's scales from lane m, column base + m / 32 of each 4-column group, and every quarter
+    // reads all 256 rows of B's scales from its own lanes (row n: lane n % 32 of the quarter,
+    // column 4 (n / 128) + (n % 128) / 32 of each 8-column group).  So per stage, once its
+    // scales have landed in this CTA's shared memory, each warp stores A's scales of its 32 rows
+    // into the one column per MMA read for them, and B's scales into the 8 columns per MMA:
+    // stores from registers run beside the MMAs, where copies into TMEM would stall them.
+    if constexpr (C::FP4) {
+      const uint32_t q = (uint32_t)(warp & 3);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = cluster_id; ok && tile < total_tiles; tile += n_clusters) {
+        int mb_, nb_, kb0, kb1;
+        work_coords(tile, p, mb_, nb_, kb0, kb1, num_kb);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          ok = __all_sync(0xffffffffu, bwait(SFULL_BAR(stage), phase, watch, SITE_SCALES_FULL));
+          if (!ok) break;
+          // atom row `lane` of a scale atom holds rows lane + 32 i (i = 0..3), 4 scales each
+          const uint32_t ssf = sm_stage + stage * C::STAGE_BYTES + A_STAGE_BYTES + C::B_STAGE_BYTES + 16 * lane;
+          const uint32_t tcol = tmem_base + ((32u * q) << 16) + C::ACC * C::UN + stage * C::SF_COLS;
+#pragma unroll
+          for (int k = 0; k < KSTEPS; ++k)
+            ptx::tmem_st_x1(tcol + 4 * k + q, ptx::ld_shared_u32(ssf + 512 * k + 4 * q));
+#pragma unroll
+          for (int k = 0; k < KSTEPS; ++k)
+            ptx::tmem_st_x8(tcol + 4 * KSTEPS + 8 * k, ptx::ld_shared_v4(ssf + C::SF_A_BYTES + 512 * k),
+                            ptx::ld_shared_v4(ssf + C::SF_A_BYTES + KSTEPS * 512 + 512 * k));
+          ptx::tmem_st_wait();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(SREADY_BAR(stage), 0));
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
   }
 
   if (C::CG == 2 && *abort_flag) {
@@ -1143,6 +1195,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #undef TEMPTY_BAR
 #undef SIDE_BAR
 #undef DONE_BAR
+#undef SFULL_BAR
+#undef SREADY_BAR
 }
 
 // ------------------------------------------------------------------ host launcher
@@ -1172,7 +1226,7 @@ int resident_groups(int sms) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -1216,7 +1270,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t s) {
     ++na;
   }
   cfg.gridDim = dim3(C::CG * groups, 1, 1);
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = s;
   cfg.attrs = attr;

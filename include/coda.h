@@ -537,7 +537,8 @@ CODA_API size_t coda_workspace_size(int32_t which, int64_t M, int64_t H, int64_t
  * Synchronises `stream`, then reads and clears the current device's status word.
  * *site receives 0 or the site code of the first kernel wait that ran out of time
  * (1 producer / empty stage, 2 MMA / free accumulator, 3 MMA / full stage,
- * 4 epilogue / accumulator, 5 epilogue / side input).  Returns CODA_OK,
+ * 4 epilogue / accumulator, 5 epilogue / side input, 6 NVFP4 scale warp / block scales in
+ * shared memory, 7 MMA / NVFP4 block scales in TMEM).  Returns CODA_OK,
  * CODA_ERR_DEVICE_TIMEOUT, or CODA_ERR_LAUNCH if the stream itself reports an error. */
 CODA_API int coda_get_device_status(void* stream, int32_t* site);
 

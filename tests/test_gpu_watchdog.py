@@ -35,7 +35,7 @@ def test_dropped_stage_times_out_and_context_survives(C):
     C.coda_gemm_epilogue(A, W, [], out)
     st, site = C.coda_get_device_status()
     assert st == C.ERR_DEVICE_TIMEOUT, st
-    assert site in (1, 2, 3, 4, 5), site
+    assert site in (1, 2, 3, 4, 5, 6, 7), site
     # the status word is cleared by the read
     st2, site2 = C.coda_get_device_status()
     assert (st2, site2) == (C.OK, 0)
@@ -79,7 +79,7 @@ def test_dropped_stage_with_side_inputs_in_flight(C, program):
     run(out)
     st, site = C.coda_get_device_status()
     assert st == C.ERR_DEVICE_TIMEOUT, st
-    assert site in (1, 2, 3, 4, 5), site
+    assert site in (1, 2, 3, 4, 5, 6, 7), site
     C.coda_set_watchdog_ms(2000)
     out2 = torch.empty_like(out)
     run(out2)
@@ -107,7 +107,7 @@ def test_dropped_stage_in_a_block_scaled_nvfp4_gemm(C):
     C.coda_gemm_epilogue(A, B, [C.OP_TENSOR_SCALE], out, tensor_scale=A.s * B.s)
     st, site = C.coda_get_device_status()
     assert st == C.ERR_DEVICE_TIMEOUT, st
-    assert site in (1, 2, 3, 4, 5), site
+    assert site in (1, 2, 3, 4, 5, 6, 7), site
     C.coda_set_watchdog_ms(2000)
     out2 = torch.empty((M, N), device="cuda")
     C.coda_gemm_epilogue(A, B, [C.OP_TENSOR_SCALE], out2, tensor_scale=A.s * B.s)
