@@ -20,6 +20,9 @@
 //   warps 2..5  epilogue: tcgen05.ld (thread = output row), the epilogue program, row /
 //               column partial reductions, cast, swizzled staging in shared memory and
 //               TMA stores; side inputs (residual, saved activations) arrive by TMA.
+//   warps 6..9  NVFP4 only: block scales from shared memory into TMEM with tcgen05.st, one
+//               warp per TMEM lane quarter (NVFP4 tiles keep one accumulator; the other
+//               TMEM columns hold the scales of the ring's stages).
 // The two TMEM accumulators let tile t+1's mainloop run under tile t's epilogue.  The
 // launch carries a programmatic dependency on the previous kernel of the stream (see
 // griddep_wait in coda_ptx.cuh).
