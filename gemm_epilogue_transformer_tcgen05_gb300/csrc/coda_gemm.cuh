@@ -60,14 +60,15 @@ __host__ __device__ constexpr int dt_bytes(int dt) { return dt == DT_F32 ? 4 : d
 __host__ __device__ constexpr int slot_bytes(int dt) { return dt == DT_E2M1 ? 512 : 32 * 32 * dt_bytes(dt); }
 
 // KIND_NVFP4: e2m1 operands packed two per byte along K, one ue4m3 scale per 16 K elements
-// (block-scaled MMA, scales staged through TMEM), fp32 tensor scales in the epilogue.
+// (block-scaled MMA, scales stored into TMEM by scale warps), fp32 tensor scales in the epilogue.
 enum : int { KIND_BF16 = 0, KIND_TF32 = 1, KIND_E4M3 = 2, KIND_NVFP4 = 3 };
 
 // NVFP4 block scales in memory: atoms of 128 rows x 4 blocks of 16 K elements (512 bytes).
 // Atom (row / 128, kb / 4) sits at ((row / 128) * kc + kb / 4) * 512, kc = K / 64 atoms per
 // 128-row block; inside an atom, row r is at byte 16 (r % 32) + 4 ((r % 128) / 32) and block
-// kb at + kb % 4.  A 32-lane TMEM copy of an atom's 32 16-byte rows, repeated into the four
-// lane quarters, puts row r's scales in lane r % 32 (+ 32 q) of column (r % 128) / 32.
+// kb at + kb % 4: the 16 bytes at 16 i hold rows i + 32 q (q = 0..3), the order of the
+// 4-column groups from which the block-scaled MMA reads row r's scales (lane r, column
+// (r % 128) / 32).
 __host__ __device__ constexpr long long sf_offset(long long row, long long kb, long long kc) {
   return ((row / 128) * kc + kb / 4) * 512 + 16 * (row % 32) + 4 * ((row % 128) / 32) + kb % 4;
 }

@@ -441,10 +441,11 @@ CODA_API int coda_quantize_e4m3(const coda_tensor* X, float scale, const coda_te
  * its output's codes the same way.
  * Block-scale layout (ceil(R / 128) * (K / 64) * 512 bytes): atoms of 128 rows x 4 blocks;
  * atom (row / 128, kb / 4) starts at byte ((row / 128) * (K / 64) + kb / 4) * 512, and inside
- * it row r, block kb sits at 16 (r % 32) + 4 ((r % 128) / 32) + kb % 4 (the order in which a
- * 32-lane TMEM copy, repeated into the four lane quarters, places each row's scales where the
- * block-scaled MMA reads them: row m in lane m, column (m % 128) / 32).  Rows from R up to the
- * next multiple of 128 get zero scales. */
+ * it row r, block kb sits at 16 (r % 32) + 4 ((r % 128) / 32) + kb % 4.  So the 16 bytes at
+ * 16 i hold rows i, i + 32, i + 64, i + 96 (the order in which the block-scaled MMA reads the
+ * scales from TMEM, row m at lane m, column (m % 128) / 32 of a 4-column group): the GEMM's
+ * scale warps, one per TMEM lane quarter, fetch their rows' scales with conflict-free loads.
+ * Rows from R up to the next multiple of 128 get zero scales. */
 CODA_API int coda_quantize_nvfp4(const coda_tensor* X, float s, const coda_tensor* Q, void* block_scales,
                                  float* amax, void* stream);
 

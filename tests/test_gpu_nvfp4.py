@@ -86,7 +86,7 @@ def test_nvfp4_gemm_store(C, M, N, K):
 
 def test_nvfp4_gemm_split_k(C):
     """Few tiles and a long K: the fp32 GEMM splits K across CTA pairs and reduce-adds the
-    slices into the zeroed output (each slice's MMAs and scale copies start mid-K)."""
+    slices into the zeroed output (each slice's MMAs and scale stores start mid-K)."""
     M, N, K = 256, 256, 16384
     xa, xb = f64(_bf16((M, K), 45)), f64(_bf16((N, K), 46, 0.02))
     A, qa, sfa = L.oracle_nvfp4(xa, _scale_of(xa))
