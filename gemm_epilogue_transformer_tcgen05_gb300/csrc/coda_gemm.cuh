@@ -192,9 +192,12 @@ struct GemmCfg {
   static constexpr int NSS = EPI == EPI_SWIGLU_BWD ? 4 : 2;
   static_assert(NCHUNK % NSS == 0, "a chunk and the next tile's chunk NCHUNK later share a ring slot");
   static constexpr int EPI_WARP_BYTES = NSS * NS * SSLOT + 2 * OUTSET;
-  static constexpr int EPI_BYTES = NUM_EPI_WARPS * EPI_WARP_BYTES;
   // NVFP4: four scale warps write the block scales into TMEM (see the kernel)
   static constexpr int SF_WARPS = FP4 ? 4 : 0;
+  // NVFP4 SwiGLU with NVFP4 output: the scale warps also form half of each tile's output
+  static constexpr bool EARLY = FP4 && DUAL && OUT_DT == DT_E2M1;
+  static constexpr int OUT_WARPS = NUM_EPI_WARPS + (EARLY ? SF_WARPS : 0);   // warps storing output
+  static constexpr int EPI_BYTES = OUT_WARPS * EPI_WARP_BYTES;
   static constexpr int THREADS = NUM_THREADS + 32 * SF_WARPS;
   static constexpr int BAR_BYTES = FP4 ? 384 : 320;
   static constexpr int STAGES_FIT = (MAX_SMEM - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
@@ -459,7 +462,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(TFULL_BAR(a), 1);
-      ptx::mbar_init(TEMPTY_BAR(a), NUM_EPI_WARPS * C::CG);   // both CTAs' epilogue warps
+      ptx::mbar_init(TEMPTY_BAR(a), C::OUT_WARPS * C::CG);   // every warp of the pair that reads it
     }
     for (int w = 0; w < NUM_EPI_WARPS; ++w)
       for (int s = 0; s < C::NSS; ++s) ptx::mbar_init(SIDE_BAR(w, s), 1);
@@ -506,6 +509,53 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const Watch watch{abort_flag, p.status, p.timeout_ns};
   const int total_tiles = p.m_tiles * p.n_tiles * p.k_splits;   // work items
   const int num_kb = (p.K + C::BK - 1) / C::BK;
+
+  // NVFP4 SwiGLU output with its one accumulator: a quarter's epilogue warp and scale warp split
+  // each tile, NCHUNK / 2 chunks of 32 output columns each.  Each forms its chunks' outputs from
+  // the accumulator's gate and up halves, hands TMEM back (one arrival per warp), then quantises
+  // and stores them while the next tile's MMAs run.
+  auto early_half = [&](uint32_t tacc, int c0, int n0, int r0, float sc, uint32_t out_base, uint64_t pol,
+                        float& amax_local) {
+    constexpr int NH = C::NCHUNK / 2;
+    const int row = r0 + lane;
+    float abuf[NH][32];
+#pragma unroll
+    for (int c = 0; c < NH; ++c) {
+      uint32_t v[32], u[32];
+      ptx::tmem_ld32(tacc + 32 * (c0 + c), v);
+      ptx::tmem_ld32(tacc + C::UN / 2 + 32 * (c0 + c), u);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float G = __uint_as_float(v[j]) * sc, U = __uint_as_float(u[j]) * sc;
+        const float a = silu_f(G) * U;
+        amax_local = fmaxf(amax_local, fabsf(a));
+        abuf[c][j] = a;
+      }
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(TEMPTY_BAR(0), 0));
+#pragma unroll
+    for (int c = 0; c < NH; ++c) {
+      const int col0 = n0 + 32 * (c0 + c);
+      uint32_t q4[4];
+      const uint32_t sfc =
+          nvfp4_block16(abuf[c], p.fp4_scale, q4) | (nvfp4_block16(abuf[c] + 16, p.fp4_scale, q4 + 2) << 8);
+      if (row < p.M && col0 < p.N)
+        *reinterpret_cast<uint16_t*>(p.out_sf + sf_offset(row, col0 / 16, p.out_sf_kc)) = (uint16_t)sfc;
+      const uint32_t oslot = out_base + (c & 1) * C::OUTSET;
+      if (lane == 0) ptx::bulk_wait_read<1>();  // the group that last used this set is done reading
+      __syncwarp();
+      ptx::st_shared_v4(oslot + 16 * lane, q4[0], q4[1], q4[2], q4[3]);   // 32 rows of 16 bytes
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (col0 < p.N && r0 < p.M) ptx::tma_store_2d_hint(&tmOut, col0 / 2, r0, oslot, pol);
+        ptx::bulk_commit();
+      }
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -754,55 +804,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const uint32_t tacc = tmem_base + ((uint32_t)(32 * q) << 16) + acc * C::UN;
       float rowacc = 0.f;
 
-      // NVFP4 SwiGLU with its one accumulator: the tile's SwiGLU outputs (4 chunks of 32 per
-      // thread, read 16 columns at a time) are formed from TMEM first and TMEM is handed back
-      // before they are quantised and stored, so that the next tile's MMAs run under that work.
-      constexpr bool EARLY = C::FP4 && C::DUAL && C::OUT_DT == DT_E2M1;
-      if constexpr (EARLY) {
-        float abuf[C::NCHUNK][32];
-        const float sc = ts * rs;
-#pragma unroll
-        for (int c = 0; c < 2 * C::NCHUNK; ++c) {
-          uint32_t v[16], u[16];
-          ptx::tmem_ld16(tacc + 16 * c, v);
-          ptx::tmem_ld16(tacc + C::UN / 2 + 16 * c, u);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float G = __uint_as_float(v[j]) * sc, U = __uint_as_float(u[j]) * sc;
-            const float a = silu_f(G) * U;
-            amax_local = fmaxf(amax_local, fabsf(a));
-            abuf[c / 2][16 * (c % 2) + j] = a;
-          }
-        }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          if constexpr (C::CG == 2)
-            ptx::mbar_arrive_cluster(ptx::mapa(TEMPTY_BAR(acc), 0));
-          else
-            ptx::mbar_arrive(TEMPTY_BAR(acc));
-        }
-#pragma unroll
-        for (int c = 0; c < C::NCHUNK; ++c) {
-          const int col0 = n0 + 32 * c;
-          uint32_t q4[4];
-          const uint32_t sfc =
-              nvfp4_block16(abuf[c], p.fp4_scale, q4) | (nvfp4_block16(abuf[c] + 16, p.fp4_scale, q4 + 2) << 8);
-          if (row_ok && col0 < p.N)
-            *reinterpret_cast<uint16_t*>(p.out_sf + sf_offset(row, col0 / 16, p.out_sf_kc)) = (uint16_t)sfc;
-          const uint32_t oslot = out_base + (c & 1) * C::OUTSET;
-          if (lane == 0) ptx::bulk_wait_read<1>();  // the group that last used this set is done reading
-          __syncwarp();
-          ptx::st_shared_v4(oslot + 16 * lane, q4[0], q4[1], q4[2], q4[3]);   // 32 rows of 16 bytes
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            if (col0 < p.N && r0 < p.M) ptx::tma_store_2d_hint(&tmOut, col0 / 2, r0, oslot, stream_pol);
-            ptx::bulk_commit();
-          }
-        }
-      }
+      // NVFP4 SwiGLU output: this warp forms the first half of the tile (the scale warp of the
+      // same TMEM lane quarter, the second half)
+      constexpr bool EARLY = C::EARLY;
+      if constexpr (EARLY) early_half(tacc, 0, n0, r0, ts * rs, out_base, stream_pol, amax_local);
 
 #pragma unroll 1
       for (int c = 0; c < (EARLY ? 0 : C::NCHUNK); ++c) {
@@ -1147,31 +1152,83 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = cluster_id; ok && tile < total_tiles; tile += n_clusters) {
-        int mb_, nb_, kb0, kb1;
-        work_coords(tile, p, mb_, nb_, kb0, kb1, num_kb);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          ok = __all_sync(0xffffffffu, bwait(SFULL_BAR(stage), phase, watch, SITE_SCALES_FULL));
-          if (!ok) break;
-          // atom row `lane` of a scale atom holds rows lane + 32 i (i = 0..3), 4 scales each
-          const uint32_t ssf = sm_stage + stage * C::STAGE_BYTES + A_STAGE_BYTES + C::B_STAGE_BYTES + 16 * lane;
-          const uint32_t tcol = tmem_base + ((32u * q) << 16) + C::ACC * C::UN + stage * C::SF_COLS;
-#pragma unroll
-          for (int k = 0; k < KSTEPS; ++k)
-            ptx::tmem_st_x1(tcol + 4 * k + q, ptx::ld_shared_u32(ssf + 512 * k + 4 * q));
-#pragma unroll
-          for (int k = 0; k < KSTEPS; ++k)
-            ptx::tmem_st_x8(tcol + 4 * KSTEPS + 8 * k, ptx::ld_shared_v4(ssf + C::SF_A_BYTES + 512 * k),
-                            ptx::ld_shared_v4(ssf + C::SF_A_BYTES + KSTEPS * 512 + 512 * k));
-          ptx::tmem_st_wait();
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(SREADY_BAR(stage), 0));
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+      // cursor over this CTA's k-blocks, in the MMA's order, whose scales go to TMEM next
+      int s_tile = cluster_id, s_kb = 0, s_kb1 = 0;
+      auto s_enter = [&]() {
+        if (s_tile < total_tiles) {
+          int mb_, nb_;
+          work_coords(s_tile, p, mb_, nb_, s_kb, s_kb1, num_kb);
         }
+      };
+      s_enter();
+      int staged = 0;   // k-blocks whose scales are in TMEM
+      auto stage_scales = [&]() {
+        if (!__all_sync(0xffffffffu, bwait(SFULL_BAR(stage), phase, watch, SITE_SCALES_FULL))) return false;
+        // atom row `lane` of a scale atom holds rows lane + 32 i (i = 0..3), 4 scales each
+        const uint32_t ssf = sm_stage + stage * C::STAGE_BYTES + A_STAGE_BYTES + C::B_STAGE_BYTES + 16 * lane;
+        const uint32_t tcol = tmem_base + ((32u * q) << 16) + C::ACC * C::UN + stage * C::SF_COLS;
+#pragma unroll
+        for (int k = 0; k < KSTEPS; ++k)
+          ptx::tmem_st_x1(tcol + 4 * k + q, ptx::ld_shared_u32(ssf + 512 * k + 4 * q));
+#pragma unroll
+        for (int k = 0; k < KSTEPS; ++k)
+          ptx::tmem_st_x8(tcol + 4 * KSTEPS + 8 * k, ptx::ld_shared_v4(ssf + C::SF_A_BYTES + 512 * k),
+                          ptx::ld_shared_v4(ssf + C::SF_A_BYTES + KSTEPS * 512 + 512 * k));
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(SREADY_BAR(stage), 0));
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++s_kb == s_kb1) {
+          s_tile += n_clusters;
+          s_enter();
+        }
+        ++staged;
+        return true;
+      };
+      if constexpr (!C::EARLY) {
+        while (ok && s_tile < total_tiles) ok = stage_scales();
+      } else {
+        // Also the second half of each tile's NVFP4 SwiGLU output.  Before waiting for a tile's
+        // accumulator, the scales of the tile and of the next tile's first stages (no more than
+        // the ring holds, which the producer loads while this accumulator is busy) go to TMEM,
+        // so that the next tile's MMAs start as soon as both halves have handed TMEM back.
+        const uint32_t out_base = sm_epi + (NUM_EPI_WARPS + (warp - 2 - NUM_EPI_WARPS)) * C::EPI_WARP_BYTES;
+        const uint64_t stream_pol = ptx::make_policy_evict_first();
+        float amax_local = 0.f;
+        int through = 0;   // k-blocks of the tiles up to this one
+        int t = 0;
+        for (int tile = cluster_id; ok && tile < total_tiles; tile += n_clusters, ++t) {
+          int mb, nb, kb0, kb1;
+          work_coords(tile, p, mb, nb, kb0, kb1, num_kb);
+          through += kb1 - kb0;
+          int ahead = 0;
+          if (tile + n_clusters < total_tiles) {
+            int mb2, nb2, k0, k1;
+            work_coords(tile + n_clusters, p, mb2, nb2, k0, k1, num_kb);
+            ahead = min(C::STAGES, k1 - k0);
+          }
+          while (ok && staged < through + ahead) ok = stage_scales();
+          if (!ok) break;
+          const int r0 = mb * C::PAIR_ROWS + (int)rank * BM + 32 * (int)q;
+          const int row = r0 + lane;
+          const float rs = ((p.flags & F_ROWSCALE) && row < p.M) ? __ldg(p.row_scale + row) : 1.f;
+          ok = __all_sync(0xffffffffu, bwait(TFULL_BAR(0), (uint32_t)(t & 1), watch, SITE_EPI_TMEM_FULL));
+          if (!ok) break;
+          ptx::tc_fence_after();
+          early_half(tmem_base + ((32u * q) << 16), C::NCHUNK / 2, nb * C::BN_OUT, r0, p.tensor_scale * rs, out_base,
+                     stream_pol, amax_local);
+        }
+        if (p.flags & F_AMAX) {
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1)
+            amax_local = fmaxf(amax_local, __shfl_xor_sync(0xffffffffu, amax_local, off));
+          if (lane == 0 && amax_local > 0.f) atomicMax(p.amax, __float_as_uint(amax_local));
+        }
+        if (lane == 0) ptx::bulk_wait<0>();   // every TMA store of this warp has completed
       }
     }
     __syncwarp();
