@@ -24,7 +24,10 @@ def _fails(fn, *args):
 
 
 def test_dropped_eps_is_caught(monkeypatch):
-    _plant(monkeypatch, "rms_scale", lambda h, eps: 1.0 / np.sqrt(np.mean(np.asarray(h, float) ** 2, axis=1)))
+    def no_eps(h, eps):
+        with np.errstate(divide="ignore"):   # a zero row divides by zero: that is the planted mistake
+            return 1.0 / np.sqrt(np.mean(np.asarray(h, float) ** 2, axis=1))
+    _plant(monkeypatch, "rms_scale", no_eps)
     assert _fails(pins.test_rms_eps_only_row) or _fails(pins.test_rms_constant_row)
 
 
