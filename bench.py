@@ -947,11 +947,23 @@ def other_workloads(torch, C, S, args, stream):
     roof = max(flop / (peak4 * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
     ms_q = _time(torch, quant_x, stream, steps)
     byt_q = 2 * M * H8 + M * H8 // 2 + sfb(M, H8)
+    # the chain's two GEMMs launched on their own through the public GEMM call, with its arguments
+    gate_up = lambda: C.coda_gemm_epilogue(X4, W4, [C.OP_TENSOR_SCALE, C.OP_ROW_SCALE, C.OP_SWIGLU, C.OP_AMAX], a4,
+                                           row_scale=r4, tensor_scale=X4.s * W4.s, amax=am4, stream=stream)
+    down = lambda: C.coda_gemm_epilogue(a4, Wd4, [C.OP_TENSOR_SCALE, C.OP_ADD_SIDE, C.OP_ROW_SUMSQ_PARTIAL], Y4,
+                                        residual=h4, tensor_scale=a4.s * Wd4.s, row_partials=P4, stream=stream)
+    per_gemm = {}
+    for name, fn, fl in (("gate_up_swiglu_nvfp4_out", gate_up, 2 * M * 2 * F8 * H8),
+                         ("down_residual", down, 2 * M * H8 * F8)):
+        g_ms = _time(torch, fn, stream, steps)
+        per_gemm[name] = {"ms": g_ms, "tflops": fl / (g_ms * 1e-3) / 1e12,
+                          "frac_of_peak": fl / (g_ms * 1e-3) / 1e12 / peak4}
     out["mlp_nvfp4_N4"] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "roofline_ms": roof,
                            "roofline_frac": roof / ms, "tokens_per_s": M / (ms * 1e-3), "launches": 3,
                            "peak_tflops": peak4, "vs_fp8_chain": out["mlp_fp8_C4"]["ms"] / ms,
                            "quantize_x_ms": ms_q, "quantize_x_gbs": byt_q / (ms_q * 1e-3) / 1e9,
                            "quantize_x_frac_of_hbm": byt_q / (ms_q * 1e-3) / 1e9 / pk["hbm"],
+                           "per_gemm": per_gemm,
                            "note": "row RMS, gate/up GEMM + r + SwiGLU + NVFP4 quantisation of a (codes, block "
                                    "scales, amax), down GEMM + residual + partials; X quantised beforehand "
                                    "(quantize_x_ms, the pass a previous layer's epilogue would fold in)"}
