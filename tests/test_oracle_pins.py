@@ -126,6 +126,18 @@ def test_deferred_r_equals_naive():
 
 
 # --------------------------------------------------------------------------- SwiGLU
+def test_sigmoid_closed_forms_and_symmetry():
+    assert O.sigmoid(0.0) == 0.5
+    np.testing.assert_allclose(O.sigmoid(math.log(3.0)), 0.75, rtol=1e-15)     # 1 / (1 + 1/3)
+    x = np.linspace(-30.0, 30.0, 121)
+    np.testing.assert_allclose(O.sigmoid(x) + O.sigmoid(-x), 1.0, rtol=0, atol=1e-15)
+    # the derivative is sigma (1 - sigma): central differences, whose rounding error is at most
+    # eps / h = 2.2e-11 and whose truncation error is below h^2 / 6 * max |sigma'''| < 2e-12
+    h = 1e-5
+    np.testing.assert_allclose((O.sigmoid(x + h) - O.sigmoid(x - h)) / (2 * h),
+                               O.sigmoid(x) * (1 - O.sigmoid(x)), rtol=1e-6, atol=5e-11)
+
+
 def test_silu_closed_forms():
     assert O.silu(0.0) == 0.0
     np.testing.assert_allclose(O.silu(40.0), 40.0, rtol=1e-15)
