@@ -76,6 +76,12 @@ def test_dropped_residual_grad_is_caught(monkeypatch):
     assert _fails(pins.test_backward_matches_finite_differences)
 
 
+def test_sigmoid_sign_flip_is_caught(monkeypatch):
+    _plant(monkeypatch, "sigmoid", lambda x: 1.0 / (1.0 + np.exp(np.asarray(x, float))))
+    assert _fails(pins.test_sigmoid_closed_forms_and_symmetry)
+    assert _fails(pins.test_silu_closed_forms)
+
+
 def test_swapped_gate_up_is_caught(monkeypatch):
     _plant(monkeypatch, "swiglu", lambda G, U: O.silu(U) * np.asarray(G, float))
     assert _fails(pins.test_swiglu_gate_and_up_roles)
