@@ -245,3 +245,40 @@ def test_nvfp4_scales_repeated_across_rows_is_caught(monkeypatch):
 
     _plant(monkeypatch, "nvfp4_dequantize", bad)
     assert _fails(fp4pins.test_block_scaled_gemm_is_the_sum_of_per_block_products)
+
+
+def test_fold_gain_divided_is_caught(monkeypatch):
+    _plant(monkeypatch, "fold_gain", lambda W, g: np.asarray(W, float) / np.asarray(g, float)[None, :])
+    assert _fails(pins.test_fold_gain_equals_scaling_input)
+
+
+def test_silu_grad_missing_term_is_caught(monkeypatch):
+    _plant(monkeypatch, "silu_grad", lambda x: O.sigmoid(x))   # drops the x sigma (1 - sigma) term
+    assert _fails(pins.test_silu_grad_finite_difference)
+
+
+def test_logsumexp_without_the_max_shift_is_caught(monkeypatch):
+    def unshifted(z):
+        with np.errstate(over="ignore"):   # exp(1000) overflows: that is the planted mistake
+            return np.log(np.sum(np.exp(np.asarray(z, float)), axis=1))
+    _plant(monkeypatch, "logsumexp", unshifted)
+    assert _fails(pins.test_logsumexp_matches_scipy_and_closed_forms)
+
+
+def test_rms_from_partials_over_the_tile_count_is_caught(monkeypatch):
+    # mean over the number of partials instead of over d
+    _plant(monkeypatch, "rms_scale_from_partials",
+           lambda P, d, eps: 1.0 / np.sqrt(np.sum(np.asarray(P, float), axis=0) / np.asarray(P).shape[0] + eps))
+    assert _fails(pins.test_partials_sum_to_row_sumsq, 256)
+
+
+def test_xent_partials_dropping_the_ragged_tile_is_caught(monkeypatch):
+    def full_tiles_only(z, bn):
+        z = np.asarray(z, float)
+        n = z.shape[1] // bn                # the last, partial tile is lost
+        blocks = [z[:, t * bn:(t + 1) * bn] for t in range(n)]
+        m = np.stack([b.max(axis=1) for b in blocks])
+        s = np.stack([np.exp(b - mb[:, None]).sum(axis=1) for b, mb in zip(blocks, m)])
+        return m, s
+    _plant(monkeypatch, "xent_partials", full_tiles_only)
+    assert _fails(pins.test_xent_partials_combine_to_logsumexp)
