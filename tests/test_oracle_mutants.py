@@ -282,3 +282,9 @@ def test_xent_partials_dropping_the_ragged_tile_is_caught(monkeypatch):
         return m, s
     _plant(monkeypatch, "xent_partials", full_tiles_only)
     assert _fails(pins.test_xent_partials_combine_to_logsumexp)
+
+
+def test_rope_frequency_without_the_factor_two_is_caught(monkeypatch):
+    # theta_p = base^(-p / head_dim) instead of base^(-2p / head_dim)
+    _plant(monkeypatch, "rope_inv_freq", lambda head_dim, base: float(base) ** (-np.arange(head_dim // 2) / head_dim))
+    assert _fails(pins.test_rope_closed_form_first_pair)
