@@ -288,3 +288,17 @@ def test_rope_frequency_without_the_factor_two_is_caught(monkeypatch):
     # theta_p = base^(-p / head_dim) instead of base^(-2p / head_dim)
     _plant(monkeypatch, "rope_inv_freq", lambda head_dim, base: float(base) ** (-np.arange(head_dim // 2) / head_dim))
     assert _fails(pins.test_rope_closed_form_first_pair)
+
+
+@pytest.mark.parametrize("dropped", ["s_x", "s_wd", "s_a"])
+def test_mlp_fp8_dropped_tensor_scale_is_caught(monkeypatch, dropped):
+    orig = O.mlp_fp8
+
+    def mutant(h, Xq, s_x, Wq, s_w, Wdq, s_wd, s_a, eps, bn):
+        res = orig(h, Xq, 1.0 if dropped == "s_x" else s_x, Wq, s_w, Wdq, 1.0 if dropped == "s_wd" else s_wd,
+                   s_a, eps, bn)
+        if dropped == "s_a":   # a quantised at s_a but dequantised without it
+            res = dict(res, Y=(res["Y"] - np.asarray(h, float)) / s_a + np.asarray(h, float))
+        return res
+    _plant(monkeypatch, "mlp_fp8", mutant)
+    assert _fails(pins.test_mlp_fp8_power_of_two_scales_are_exact)

@@ -339,6 +339,28 @@ def test_mlp_fp8_unit_scales_reduce_to_block_pieces():
     assert res["amax"] == np.max(np.abs(a))
 
 
+def test_mlp_fp8_power_of_two_scales_are_exact():
+    # Scaling laws fixed by the arithmetic, exact for powers of two in e4m3's normal range:
+    # s_x and s_w enter only as their product; doubling s_wd doubles Y - h; doubling s_a leaves
+    # Y unchanged (e4m3(a / 2 s_a) 2 s_a = e4m3(a / s_a) s_a while a / s_a stays normal).
+    # Data built to stay there: |h| = 1 (r = 1 / sqrt(1 + eps)), X's codes all 1 and W's codes in
+    # [1, 4] with 32 per row, so G and U lie in [1, 4] and a / s_a in [5.8, 126].
+    rng = np.random.default_rng(19)
+    h = rng.choice([-1.0, 1.0], size=(6, 32))
+    Xq = np.ones((6, 32))
+    Wq = rng.choice([1.0, 1.5, 2.0, 2.5, 3.0, 3.5, 4.0], size=(16, 32))
+    Wdq = O.e4m3_round(rng.normal(size=(32, 8)) * 4)
+    run = lambda s_x, s_w, s_wd, s_a: O.mlp_fp8(h, Xq, s_x, Wq, s_w, Wdq, s_wd, s_a, 1e-6, 16)
+    base = run(0.25, 0.125, 0.0625, 2.0 ** -3)
+    a_over = np.abs(base["a"]) / 2.0 ** -3
+    assert np.all((a_over > 2.0 ** -5) & (a_over < 224)), "test data left the normal range"
+    np.testing.assert_array_equal(run(0.5, 0.0625, 0.0625, 2.0 ** -3)["Y"], base["Y"])
+    np.testing.assert_allclose(run(0.25, 0.125, 0.125, 2.0 ** -3)["Y"] - h, 2 * (base["Y"] - h), rtol=1e-13)
+    np.testing.assert_allclose(run(0.25, 0.125, 0.0625, 2.0 ** -2)["Y"], base["Y"], rtol=1e-15)
+    assert not np.allclose(run(0.5, 0.125, 0.0625, 2.0 ** -3)["a"], base["a"])   # s_x does act
+    assert not np.allclose(run(0.25, 0.125, 0.0625, 0.3)["Y"], base["Y"])        # s_a does act
+
+
 # ------------------------------------------------------------------ fp8 MLP backward
 def _mlp_loss(h, W, W_d, dY, eps):
     """The gain-free MLP forward in exact arithmetic, written out here independently of the
