@@ -302,3 +302,17 @@ def test_mlp_fp8_dropped_tensor_scale_is_caught(monkeypatch, dropped):
         return res
     _plant(monkeypatch, "mlp_fp8", mutant)
     assert _fails(pins.test_mlp_fp8_power_of_two_scales_are_exact)
+
+
+@pytest.mark.parametrize("dropped", ["s_x", "s_wd", "s_a"])
+def test_mlp_nvfp4_dropped_tensor_scale_is_caught(monkeypatch, dropped):
+    orig = O.mlp_nvfp4
+
+    def mutant(h, Xq, Xsf, s_x, Wq, Wsf, s_w, Wdq, Wdsf, s_wd, s_a, eps, bn):
+        res = orig(h, Xq, Xsf, 1.0 if dropped == "s_x" else s_x, Wq, Wsf, s_w, Wdq, Wdsf,
+                   1.0 if dropped == "s_wd" else s_wd, s_a, eps, bn)
+        if dropped == "s_a":   # a quantised at s_a but dequantised without it
+            res = dict(res, Y=(res["Y"] - np.asarray(h, float)) / s_a + np.asarray(h, float))
+        return res
+    _plant(monkeypatch, "mlp_nvfp4", mutant)
+    assert _fails(fp4pins.test_mlp_nvfp4_power_of_two_scales_are_exact)

@@ -157,3 +157,28 @@ def test_mlp_nvfp4_unit_scales_reduce_to_block_pieces():
     err = np.abs(s_a * np.repeat(asf, 16, axis=1) * aq - a)
     bmax = np.repeat(np.max(np.abs(a).reshape(M, F // 16, 16), axis=2), 16, axis=1)
     assert np.all(err <= bmax / 6 * (1 + 1 / 16) + 1e-12)
+
+
+def test_mlp_nvfp4_power_of_two_scales_are_exact():
+    # Scaling laws fixed by the arithmetic, exact for powers of two while block scales stay
+    # normal e4m3 numbers: s_x and s_w enter only as their product; doubling s_wd doubles Y - h;
+    # doubling s_a halves a's block scales and leaves its codes and Y unchanged.
+    rng = np.random.default_rng(26)
+    M, H, F = 6, 64, 32
+    h = rng.normal(size=(M, H))
+    Xq, Xsf = O.nvfp4_quantize(h, 2.0 ** -6)
+    Wq, Wsf = O.nvfp4_quantize(rng.normal(size=(2 * F, H)), 2.0 ** -7)
+    Wdq, Wdsf = O.nvfp4_quantize(rng.normal(size=(H, F)), 2.0 ** -7)
+    run = lambda s_x, s_w, s_wd, s_a: O.mlp_nvfp4(h, Xq, Xsf, s_x, Wq, Wsf, s_w, Wdq, Wdsf, s_wd, s_a, 1e-6, 16)
+    a = run(2.0 ** -6, 2.0 ** -7, 2.0 ** -7, 1.0)["a"]
+    s_a = 2.0 ** np.round(np.log2(np.max(np.abs(a)) / (6 * 64)))      # block scales near 64 and below
+    base = run(2.0 ** -6, 2.0 ** -7, 2.0 ** -7, s_a)
+    twice = run(2.0 ** -6, 2.0 ** -7, 2.0 ** -7, 2 * s_a)
+    nz = base["asf"] > 0
+    assert np.all(base["asf"][nz] >= 2.0 ** -5), "test data left the normal e4m3 range"
+    np.testing.assert_array_equal(run(2.0 ** -5, 2.0 ** -8, 2.0 ** -7, s_a)["Y"], base["Y"])
+    np.testing.assert_allclose(run(2.0 ** -6, 2.0 ** -7, 2.0 ** -6, s_a)["Y"] - h, 2 * (base["Y"] - h), rtol=1e-13)
+    np.testing.assert_array_equal(twice["aq"], base["aq"])
+    np.testing.assert_array_equal(twice["asf"], base["asf"] / 2)
+    np.testing.assert_array_equal(twice["Y"], base["Y"])
+    assert not np.allclose(run(2.0 ** -5, 2.0 ** -7, 2.0 ** -7, s_a)["a"], base["a"])   # s_x does act
