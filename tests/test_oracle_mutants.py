@@ -317,3 +317,13 @@ def test_mlp_nvfp4_dropped_tensor_scale_is_caught(monkeypatch, dropped):
         return res
     _plant(monkeypatch, "mlp_nvfp4", mutant)
     assert _fails(fp4pins.test_mlp_nvfp4_power_of_two_scales_are_exact)
+
+
+def test_qkv_rope_positions_without_the_sequence_wrap_are_caught(monkeypatch):
+    # positions taken as the row index of the whole batch instead of the index within a sequence
+    def mutant(h, g, W_qkv, eps, seq_len, n_rot_cols, head_dim, base):
+        Z = O.linear(O.rmsnorm(h, g, eps), W_qkv)
+        return dict(r=O.rms_scale(h, eps), Z=Z,
+                    out=O.rope_rotate(Z, np.arange(Z.shape[0]), n_rot_cols, head_dim, base))
+    _plant(monkeypatch, "qkv_rope", mutant)
+    assert _fails(pins.test_qkv_rope_chain_is_norm_then_gemm_then_rotate)
