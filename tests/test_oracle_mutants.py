@@ -327,3 +327,19 @@ def test_qkv_rope_positions_without_the_sequence_wrap_are_caught(monkeypatch):
                     out=O.rope_rotate(Z, np.arange(Z.shape[0]), n_rot_cols, head_dim, base))
     _plant(monkeypatch, "qkv_rope", mutant)
     assert _fails(pins.test_qkv_rope_chain_is_norm_then_gemm_then_rotate)
+
+
+def test_deferred_r_on_the_gate_half_only_is_caught(monkeypatch):
+    def mutant(O_, R, W_o, g, W_gu, W_d, eps, bn):
+        h = O.linear(O_, W_o) + np.asarray(R, float)
+        P = O.partial_sumsq(h, bn)
+        r = O.rms_scale_from_partials(P, h.shape[1], eps)
+        Z = O.linear(h, O.fold_gain(W_gu, g))
+        F = Z.shape[1] // 2
+        Z[:, :F] *= r[:, None]             # r left off the up half
+        G, U = Z[:, :F], Z[:, F:]
+        a = O.swiglu(G, U)
+        Y = O.linear(a, W_d) + h
+        return dict(h=h, P=P, r=r, Z=Z, G=G, U=U, a=a, Y=Y)
+    _plant(monkeypatch, "block_forward_deferred", mutant)
+    assert _fails(pins.test_deferred_r_equals_naive)
