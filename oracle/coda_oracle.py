@@ -54,12 +54,13 @@ Readings of points the pages leave open (the plainest reading consistent with th
      pages name FP4 only as a faster matmul format).  Each row of an operand is cut into
      blocks of 16 consecutive K elements.  A block carries one unsigned e4m3 scale sf, the
      tensor carries one fp32 scale s, and an element carries an e2m1 code q (values 0, 0.5,
-     1, 1.5, 2, 3, 4, 6 and their negatives); its value is s * sf * q.  Quantising a block:
-     sf = e4m3(amax / (6 s)), then q = e2m1(x * (1 / (sf s))) (zero when sf is zero), both
-     rounded to nearest-even with saturation.  amax / (6 s), sf s, its reciprocal and the
-     product with x are each rounded once in fp32, the precision the kernels decide the codes
-     in (the reciprocal, as for e4m3 in reading 8), so that equal fp32 inputs give equal codes.  s is chosen by the caller: amax / (6 * 448) of the tensor for operands
-     known up front, and a delayed scale (as s_a above) for the SwiGLU output.
+     1, 1.5, 2, 3, 4, 6 and their negatives); its value is s * sf * q.  Quantising a block is
+     the plain definition, in float64: sf = e4m3(amax / (6 s)), then q = e2m1(x / (sf s))
+     (zero when sf is zero), both rounded to nearest-even with saturation.  A quantiser that
+     takes these steps in fp32 may round the other way where a value lies within an fp32
+     rounding of a midpoint; the tests accept exactly those codes.  s is chosen by the
+     caller: amax / (6 * 448) of the tensor for operands known up front, and a delayed scale
+     (as s_a above) for the SwiGLU output.
 Every function here is pinned by a test (closed form, invariant, library special case
 or brute force); none is "parity unpinned".
 """
@@ -273,21 +274,17 @@ def nvfp4_quantize(x, s):
     """NVFP4 quantisation of x [R, K] (K a multiple of 16) with the tensor scale s (reading 9).
 
     Returns (q, sf): q [R, K] e2m1 values and sf [R, K / 16] e4m3 block scales (float64), so
-    that the dequantised tensor is s * sf (repeated over each block) * q.  x is taken in fp32
-    first; amax / (6 s), d = sf * s, 1 / d and x * (1 / d) are fp32 operations, each rounded
-    once."""
-    x32 = np.asarray(x, dtype=np.float32)
-    R, K = x32.shape
+    that the dequantised tensor is s * sf (repeated over each block) * q.  Every step is the
+    float64 definition: sf = e4m3(amax / (6 s)), q = e2m1(x / (sf s)), q = 0 where sf = 0."""
+    x = _f64(x)
+    R, K = x.shape
     assert K % NVFP4_BLOCK == 0
-    s32 = np.float32(s)
-    xb = x32.reshape(R, K // NVFP4_BLOCK, NVFP4_BLOCK)
+    xb = x.reshape(R, K // NVFP4_BLOCK, NVFP4_BLOCK)
     amax = np.max(np.abs(xb), axis=2)
-    u = amax / (np.float32(E2M1_MAX) * s32)                     # fp32 product, fp32 quotient
-    sf = e4m3_round(u.astype(F64))
-    d = (sf.astype(np.float32) * s32)[:, :, None]                # exact e4m3 value times s, in fp32
-    rd = np.where(d > 0, np.float32(1) / np.where(d > 0, d, np.float32(1)), np.float32(0)).astype(np.float32)
-    y = xb * rd                                                  # fp32 product
-    q = e2m1_round(y.astype(F64)).reshape(R, K)
+    sf = e4m3_round(amax / (E2M1_MAX * F64(s)))
+    d = (sf * F64(s))[:, :, None]
+    y = np.where(d > 0, xb / np.where(d > 0, d, 1.0), 0.0)
+    q = e2m1_round(y).reshape(R, K)
     return q, sf
 
 

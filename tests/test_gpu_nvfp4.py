@@ -1,7 +1,8 @@
 """GPU parity of the NVFP4 path against the fp64 oracle, through the C ABI (oracle reading 9:
 e2m1 codes, e4m3 block scales per 16 K elements, fp32 tensor scales):
 
-* the quantiser, bit-exact in codes and block scales;
+* the quantiser: codes and block scales within the rounding window of the oracle's plain
+  float64 definition, almost all equal to it;
 * the block-scaled GEMM (plain store), on operands the oracle quantised, at ragged sizes;
 * the gate/up GEMM with r, SwiGLU and a bf16 or NVFP4 output (codes checked against the
   oracle's rounding window, block scales and amax);
@@ -41,8 +42,36 @@ def _scale_of(x):
 
 
 # ------------------------------------------------------------------------- quantiser
+def _nvfp4_window(got_q, got_sf, x, s, rel):
+    """NVFP4 codes and block scales are rounding decisions the GPU takes in fp32; the oracle
+    takes them in float64 on the plain definition.  Each block scale must lie between the e4m3
+    roundings of amax / (6 s) moved by `rel` either way, and each code between the e2m1
+    roundings of x / (sf s) moved by `rel` either way, sf being the GPU's own block scale (so a
+    block whose scale rounded the other way is still checked, against that scale).  Only values
+    within `rel` of a rounding midpoint may therefore differ from the oracle.  Returns the
+    fractions of block scales and of codes equal to the oracle's own rounding."""
+    R, K = x.shape
+    q, sf = O.nvfp4_quantize(x, s)
+    amax_b = np.max(np.abs(x).reshape(R, K // 16, 16), axis=2)
+    u = amax_b / (6.0 * s)
+    lo, hi = O.e4m3_round(u * (1 - rel)), O.e4m3_round(u * (1 + rel))
+    bad_sf = ~((got_sf >= lo) & (got_sf <= hi))
+    assert not bad_sf.any(), f"{int(bad_sf.sum())} block scales outside the rounding window"
+    d = s * np.repeat(got_sf, 16, axis=1)
+    y = np.where(d > 0, x / np.where(d > 0, d, 1.0), 0.0)
+    slack = rel * np.abs(y)
+    bad_q = ~((got_q >= O.e2m1_round(y - slack)) & (got_q <= O.e2m1_round(y + slack)))
+    assert not bad_q.any(), f"{int(bad_q.sum())} codes outside the rounding window"
+    return float(np.mean(got_sf == sf)), float(np.mean(got_q == q))
+
+
+# an fp32 quotient, product and reciprocal each round once (2^-24 relative): 1e-6 covers
+# the quantiser's few roundings with room to spare
+QUANT_REL = 1e-6
+
+
 @pytest.mark.parametrize("R,K", [(300, 512), (256, 320), (128, 192)])
-def test_quantize_nvfp4_bit_exact(C, R, K):
+def test_quantize_nvfp4_codes_in_rounding_window(C, R, K):
     X = _bf16((R, K), 31 + R)
     X[0, :16] = 0.0                                   # an all-zero block: scale 0, codes 0
     X[1, 5] = 1e4                                     # one large value: its block saturates nothing
@@ -54,10 +83,13 @@ def test_quantize_nvfp4_bit_exact(C, R, K):
     C.coda_quantize_nvfp4(dev(X), Q, amax=amax)
     torch.cuda.synchronize()
     fresh_status()
-    q, sf = O.nvfp4_quantize(x, s)
-    np.testing.assert_array_equal(L.unpack_codes(Q.codes.cpu().numpy()), O.e2m1_encode(q))
+    got_q = O.e2m1_decode(L.unpack_codes(Q.codes.cpu().numpy()))
     buf = Q.scales.cpu().numpy()
-    np.testing.assert_array_equal(L.from_atoms(buf, R, K), O.e4m3_encode(sf))
+    got_sf = O.e4m3_decode(L.from_atoms(buf, R, K))
+    same_sf, same_q = _nvfp4_window(got_q, got_sf, x, s, QUANT_REL)
+    print(f"nvfp4 quantiser {R}x{K}: block scales equal to the oracle's {same_sf:.6f}, codes {same_q:.6f}")
+    assert same_sf >= 0.999 and same_q >= 0.999
+    assert np.all(got_sf[0, :1] == 0) and np.all(got_q[0, :16] == 0)
     used = np.zeros(buf.size, dtype=bool)
     used[L.atom_offsets(R, K)] = True
     assert not buf[~used].any(), "scales of padding rows are not zero"
@@ -142,18 +174,10 @@ def _check_nvfp4_output(out, a, s_a, M, F, rel=1e-4):
     rounding, and the dequantised tensor must be within half an e2m1 step of a."""
     got_q = O.e2m1_decode(L.unpack_codes(out.codes.cpu().numpy()))
     got_sf = O.e4m3_decode(L.from_atoms(out.scales.cpu().numpy(), M, F))
-    q, sf = O.nvfp4_quantize(a, s_a)
+    same_sf, same_q = _nvfp4_window(got_q, got_sf, a, s_a, rel)
+    print(f"nvfp4 output {M}x{F}: block scales equal to the oracle's {same_sf:.6f}, codes {same_q:.6f}")
+    assert same_sf >= 0.999 and same_q >= 0.999
     amax_b = np.max(np.abs(a).reshape(M, F // 16, 16), axis=2)
-    u = amax_b / (6 * s_a)
-    lo, hi = O.e4m3_round(u * (1 - rel)), O.e4m3_round(u * (1 + rel))
-    assert np.all((got_sf >= lo) & (got_sf <= hi)), "block scale outside the rounding window"
-    assert np.mean(got_sf == sf) >= 0.999
-    same = np.repeat(got_sf == sf, 16, axis=1)     # codes are compared where the scales agree
-    y = a / (s_a * np.repeat(np.where(sf > 0, sf, 1), 16, axis=1))
-    slack = rel * np.abs(y) + 1e-6
-    ok = (got_q >= O.e2m1_round(y - slack)) & (got_q <= O.e2m1_round(y + slack))
-    assert np.all(ok[same]), f"{int((~ok & same).sum())} codes outside the rounding window"
-    assert np.mean((got_q == q)[same]) >= 0.999
     deq = L.nvfp4_values(out, M, F)
     bmax = np.repeat(amax_b, 16, axis=1)
     assert np.all(np.abs(deq - a) <= bmax / 6 * (1 + 1 / 16) + rel * bmax + 1e-30)

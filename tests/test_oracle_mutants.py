@@ -223,13 +223,13 @@ def test_nvfp4_block_of_32_is_caught(monkeypatch):
 def test_nvfp4_scale_from_e4m3_range_is_caught(monkeypatch):
     # block scale amax / 448 (the e4m3 range) instead of amax / 6 (the e2m1 range)
     def bad(x, s):
-        x32 = np.asarray(x, dtype=np.float32)
-        R, K = x32.shape
-        xb = x32.reshape(R, K // 16, 16)
-        sf = O.e4m3_round((np.max(np.abs(xb), axis=2) / (np.float32(448) * np.float32(s))).astype(float))
-        d = (sf.astype(np.float32) * np.float32(s))[:, :, None]
+        x = np.asarray(x, dtype=float)
+        R, K = x.shape
+        xb = x.reshape(R, K // 16, 16)
+        sf = O.e4m3_round(np.max(np.abs(xb), axis=2) / (448.0 * s))
+        d = (sf * s)[:, :, None]
         y = np.where(d > 0, xb / np.where(d > 0, d, 1), 0)
-        return O.e2m1_round(y.astype(float)).reshape(R, K), sf
+        return O.e2m1_round(y).reshape(R, K), sf
 
     _plant(monkeypatch, "nvfp4_quantize", bad)
     assert _fails(fp4pins.test_nvfp4_exactly_representable_blocks_round_trip)

@@ -182,3 +182,32 @@ def test_mlp_nvfp4_power_of_two_scales_are_exact():
     np.testing.assert_array_equal(twice["asf"], base["asf"] / 2)
     np.testing.assert_array_equal(twice["Y"], base["Y"])
     assert not np.allclose(run(2.0 ** -5, 2.0 ** -7, 2.0 ** -7, s_a)["a"], base["a"])   # s_x does act
+
+
+def test_nvfp4_quantize_is_the_brute_force_nearest_definition():
+    # The plain float64 definition, by brute force over the two value tables: the block scale
+    # is the e4m3 value nearest to amax / (6 s) (torch's e4m3 decoding of all 256 bytes; ties to
+    # the even code, saturating at 448), and each code is the e2m1 value nearest to x / (sf s).
+    import torch
+    tab = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()[:127]
+    codes = np.arange(127)
+
+    def nearest_e4m3(u):
+        d = np.abs(np.minimum(u, 448.0) - tab)
+        best = np.flatnonzero(d == d.min())
+        return tab[best[0] if len(best) == 1 else [c for c in codes[best] if c % 2 == 0][0]]
+
+    rng = np.random.default_rng(27)
+    R, K = 5, 96
+    x = rng.normal(size=(R, K)) * np.exp(rng.normal(size=(R, 1)) * 2)
+    x[0, :16] = 0.0
+    s = float(np.float32(np.max(np.abs(x)) / (6 * 448) * 0.37))     # some blocks saturate at 448
+    q, sf = O.nvfp4_quantize(x, s)
+    for i in range(R):
+        for b in range(K // 16):
+            blk = x[i, 16 * b:16 * b + 16]
+            want_sf = nearest_e4m3(np.max(np.abs(blk)) / (6.0 * s))
+            assert sf[i, b] == want_sf, (i, b)
+            for j, v in enumerate(blk):
+                want = _nearest_e2m1(v / (want_sf * s)) if want_sf > 0 else 0.0
+                assert q[i, 16 * b + j] == want, (i, b, j)
