@@ -268,10 +268,9 @@ CODA_API int coda_block_forward(const coda_block_fwd* io, void* stream);
 /* coda_block_forward_noalloc — the same chain for callers that cannot allocate device memory.
  * The pages describe no such call; it exists for deployment, not for the method.
  * Some callers cannot call cudaMalloc at all: a custom operator inside a host runtime that
- * owns the whole device memory pool and hands its operators only their inputs and outputs;
- * a deployment with a fixed memory budget that forbids allocation after start-up; code that
- * runs while a stream capture is in progress, where allocating is illegal.  Such callers
- * cannot provide the chain's scratch (`workspace`).
+ * owns the whole device memory pool and hands its operators only their inputs and outputs,
+ * or a deployment with a fixed memory budget that forbids allocation after start-up.  Such
+ * callers cannot provide the chain's scratch (`workspace`).
  *   - The caller still owns and passes every input and output (O, R, the weights, h, r, a,
  *     Y and the optional Z and Y_partials); `io->workspace` must be NULL.
  *   - The partial sums of squares that G1 writes and the row reduce reads live instead in
@@ -280,13 +279,16 @@ CODA_API int coda_block_forward(const coda_block_fwd* io, void* stream);
  *   - Limit: ceil(H / 256) * M <= CODA_NOALLOC_MAX_PARTIALS (M <= 131072 tokens at
  *     H = 2048).  Larger problems, or a non-NULL workspace, return CODA_ERR_SHAPE and
  *     launch nothing.
- *   - Set-up: the first call on each device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any stream capture.
+ *   - Set-up: the first call on each device (in each CUDA context of that device) looks up
+ *     the array's device address, with that device current, and caches it; make that first
+ *     call before any stream capture.  After a device reset the next call sees a new
+ *     context and looks the address up again.
  *   - Sharing: all calls on a device use the same array, which keeps the last call's
  *     contents.  Nothing in it needs clearing (each call writes every partial it reads
  *     before reading it), but calls that overlap on the GPU (unordered streams) race on it.
  *   - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
- * Results equal those of coda_block_forward with a caller workspace. */
+ * It issues the same kernels, in the same order, as coda_block_forward with a caller
+ * workspace, so its results equal that call's bit for bit. */
 #define CODA_NOALLOC_MAX_PARTIALS (1 << 20)
 CODA_API int coda_block_forward_noalloc(const coda_block_fwd* io, void* stream);
 

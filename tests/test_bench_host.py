@@ -91,3 +91,27 @@ def test_peaks_fall_back_without_the_measured_file(tmp_path, monkeypatch):
                                                  '"bf16_tflops_sustained": 1733.0}')
     p = bench.peaks()
     assert p["source"] == "measured" and p["bf16_sus"] == 1733.0 and p["hbm"] == 6676.8
+
+
+def test_tensor_peak_is_burst_for_short_regions_and_sustained_for_long_ones():
+    pk = {"bf16": 1904.0, "bf16_sus": 1709.5, "hbm": 6776.3, "source": "measured"}
+    peak, kind = bench.tensor_peak(pk, 0.02)             # 20 steps of about 1 ms
+    assert peak == 1904.0 and kind.startswith("bf16 burst")
+    peak, kind = bench.tensor_peak(pk, bench.SUSTAINED_REGION_S + 0.5)
+    assert peak == 1709.5 and kind.startswith("bf16 sustained")
+
+
+def test_lib_peak_takes_the_higher_measured_rate_or_the_fallback():
+    assert bench.lib_peak({"burst_tflops": 3400.0, "sustained_tflops": 3350.0}, 1.0) == 3400.0
+    assert bench.lib_peak({"burst_tflops": 4900.0, "sustained_tflops": 7000.0}, 1.0) == 7000.0
+    assert bench.lib_peak({"error": "no e4m3 GEMM"}, 3808.0) == 3808.0
+
+
+def test_reference_rows_take_the_whole_batch_when_the_run_fits_the_budget():
+    # 3860 tokens/s: a whole 16384-row step takes 4.2 s; 25 steps fit 240 s, 1020 do not
+    assert bench.reference_rows(3860.0, 20, 5) == bench.M_TOK
+    rows = bench.reference_rows(3860.0, 1000, 20)
+    assert rows % 64 == 0 and 64 <= rows < bench.M_TOK
+    assert rows / 3860.0 * 1020 <= bench.REFERENCE_BUDGET_S
+    assert bench.reference_rows(1.0, 1000, 20) == 64     # never below one 64-row slice
+

@@ -4,7 +4,14 @@ RoPE, fp8 MLP) against the fp64 oracle, through the C ABI.
 Reduced sizes compare every output element; the full 16384-token sizes (the launch
 configuration the bench times) compare sampled token rows (rows 0-255 plus 256 random
 rows: forward rows are independent, so the oracle computes exactly those rows) and, for
-weight gradients, sampled columns over all rows."""
+weight gradients, sampled columns over all rows.
+
+Tensors that are products of two bf16-stored GEMM results (a, e and the weight gradients
+dW_d, dW_gu built from them) get two checks: against the oracle's plain chain (normwise,
+and element-wise against the bf16-storage model), and element by element at 2e-2 against
+the oracle given the chain's own stored inputs of that step (exact inputs: the u or h the
+gate/up GEMM read, r, the saved Z, a, e, dh).  The second holds each kernel to the bar
+wherever the chain stands, the first bounds how far bf16 storage moves the chain."""
 import numpy as np
 import pytest
 import torch
@@ -72,6 +79,7 @@ def _run_block_forward(C, inp, train=True, gain="broadcast"):
     if gain == "fold":
         Wf = torch.empty_like(W_gu)
         C.coda_fold_gain(W_gu, g, Wf)
+        out["Wf"] = Wf
         C.coda_block_forward(O_, R, W_o, Wf, W_d, inp["eps"], out["h"], out["r"], out["a"], out["Y"], ws,
                              Z=out["Z"], Y_partials=out["Yp"])
     else:
@@ -81,6 +89,19 @@ def _run_block_forward(C, inp, train=True, gain="broadcast"):
     torch.cuda.synchronize()
     fresh_status()
     return out, None
+
+
+def _a_exact_inputs(out, inp, rows):
+    """a on `rows` from the inputs the gate/up GEMM read in this chain: the stored bf16 u = h g
+    with the unfolded W_gu (gain broadcast), or the stored h with the folded bf16 W_gu', and
+    the chain's fp32 r:  Z = r (x W^T),  a = silu(G) U  (fp64)."""
+    if "Wf" in out:
+        x, W = f64(out["h"])[rows], f64(out["Wf"])
+    else:
+        x, W = f64(out["u"])[rows], f64(inp["W_gu"])
+    Z = f64(out["r"])[rows][:, None] * O.linear(x, W)
+    F = Z.shape[1] // 2
+    return O.swiglu(Z[:, :F], Z[:, F:])
 
 
 def _oracle_forward_rows(inp, rows):
@@ -135,6 +156,7 @@ def _check_block_forward(C, M, H, F, gain):
     for k in ("h", "r", "Y"):
         assert_close(f64(out[k]), ref[k], TOL_BF16, k)
     assert_product_close(f64(out["a"]), ref["a"], sim["a"], "a")
+    assert_close(f64(out["a"]), _a_exact_inputs(out, inp, np.arange(M)), TOL_BF16, "a (exact inputs)")
     assert_close(f64(out["Z"]), ref["Z"], TOL_BF16, "Z")
     assert_close(f64(out["Yp"]), O.partial_sumsq(ref["Y"], 256), TOL_BF16, "Y partials")
     if gain == "broadcast":
@@ -152,6 +174,7 @@ def test_block_forward_full_size_sampled_rows(C):
     for k in ("h", "r", "Y"):
         assert_close(f64(out[k])[rows], ref[k], TOL_BF16, k)
     assert_product_close(f64(out["a"])[rows], ref["a"], sim["a"], "a")
+    assert_close(f64(out["a"])[rows], _a_exact_inputs(out, inp, rows), TOL_BF16, "a (exact inputs)")
 
 
 # --------------------------------------------------------------------- block backward
@@ -169,6 +192,37 @@ def _run_block_backward(C, inp, fwd_out):
     torch.cuda.synchronize()
     fresh_status()
     return o
+
+
+def _e_exact_inputs(fwd, inp, rows):
+    """e on `rows` from the saved bf16 Z = [G | U], the chain's r and dY (fp64):
+    dA = dY W_d,  e = r [dA U silu'(G) | dA silu(G)]."""
+    Z, r = f64(fwd["Z"])[rows], f64(fwd["r"])[rows]
+    dA = f64(inp["dY"])[rows] @ f64(inp["W_d"])
+    F = Z.shape[1] // 2
+    G, U = Z[:, :F], Z[:, F:]
+    return r[:, None] * np.hstack([dA * U * O.silu_grad(G), dA * O.silu(G)])
+
+
+def _check_backward_exact_inputs(inp, fwd, got, rows, fcols, hcols):
+    """Each backward output against the oracle given the chain's own stored tensors: e on
+    `rows`; dW_d[:, fcols] = dY^T a; dW_gu on the gate and up rows fcols, F + fcols as
+    g (e^T h); dW_o[:, hcols] = dh^T O; dg[hcols] = sum_i h (e W_gu)[:, hcols]."""
+    F = f64(inp["W_d"]).shape[1]
+    assert_close(f64(got["e"])[rows], _e_exact_inputs(fwd, inp, rows), TOL_BF16, "e (exact inputs)")
+    dY, Ox, g = f64(inp["dY"]), f64(inp["O"]), f64(inp["g"])
+    h, a = f64(fwd["h"]), f64(fwd["a"])
+    assert_close(f64(got["dW_d"])[:, fcols], dY.T @ a[:, fcols], TOL_BF16, "dW_d[:, cols] (exact inputs)")
+    e_t = got["e"].cpu()
+    ecols = np.concatenate([fcols, F + fcols])
+    ref_dWgu = g[None, :] * (f64(e_t[:, torch.from_numpy(ecols)]).T @ h)
+    assert_close(f64(got["dW_gu"])[ecols], ref_dWgu, TOL_BF16, "dW_gu[cols] (exact inputs)")
+    assert_close(f64(got["dW_o"])[:, hcols], f64(got["dh"]).T @ Ox[:, hcols], TOL_BF16, "dW_o[:, cols] (exact inputs)")
+    Wc = f64(inp["W_gu"])[:, hcols]
+    dg = np.zeros(len(hcols))
+    for i0 in range(0, h.shape[0], 2048):                       # t = e W_gu on the sampled columns
+        dg += np.sum(h[i0:i0 + 2048, hcols] * (f64(e_t[i0:i0 + 2048]) @ Wc), axis=0)
+    assert_close(f64(got["dg"])[hcols], dg, TOL_BF16, "dg[cols] (exact inputs)")
 
 
 def test_block_backward_zero_output_gradient(C):
@@ -202,6 +256,7 @@ def test_block_backward_small(C, M, H, F):
         assert_close(f64(got[k]), ref[k], TOL_BF16, k)
     for k in ("dW_gu", "dW_d"):
         assert_product_close(f64(got[k]), ref[k], sb[k], k)
+    _check_backward_exact_inputs(inp, fwd, got, np.arange(M), np.arange(F), np.arange(H))
 
 
 @pytest.mark.slow
@@ -239,6 +294,9 @@ def test_block_backward_full_size_sampled(C):
     sim_dWgu = x["g"][None, :] * (SIM.bf(rs[:, None] * dA * Us * O.silu_grad(Gs)).T @ hs)
     assert_product_close(f64(got["dW_d"])[:, cols], ref_dWd, sim_dWd, "dW_d[:, cols]")
     assert_product_close(f64(got["dW_gu"])[cols], ref_dWgu, sim_dWgu, "dW_gu[cols]")
+    # every output, dW_o and dg included, against the oracle given the chain's stored tensors
+    hcols = np.sort(np.random.default_rng(6).choice(H, size=64, replace=False))
+    _check_backward_exact_inputs(inp, fwd, got, rows, cols, hcols)
 
 
 # --------------------------------------------------------------------- QKV + RoPE

@@ -1,12 +1,14 @@
 """coda_block_forward_noalloc: the block forward chain for callers that cannot allocate
-device memory (an operator inside a runtime that owns the whole device memory pool, a
-deployment that forbids allocation after start-up, code running during a stream capture).
-It takes no workspace; the chain's partial sums live in the library's static device array.
+device memory (an operator inside a runtime that owns the whole device memory pool, or a
+deployment that forbids allocation after start-up).  It takes no workspace; the chain's
+partial sums live in the library's static device array.
 
 Checked here, through the C ABI: two calls in a row (different sizes, so the second call
-reuses the array the first one left behind) give the same results as coda_block_forward
-with a caller-allocated workspace, within the parity tolerance of the other tests; and
-problems beyond the array's size are refused before anything is launched.
+reuses the array the first one left behind) give exactly the results of coda_block_forward
+with a caller-allocated workspace (the same kernels in the same order, so bit for bit; a
+stale or missing partial would change r and everything after it), and they also meet the
+parity tolerance of the other tests; problems beyond the array's size are refused before
+anything is launched.
 
 This file is collected last so that a run stopping at the first failure has already run
 every other test; it also passes on its own in a fresh process."""
@@ -70,6 +72,7 @@ def test_no_alloc_matches_workspace_entry_point_on_two_calls(C):
     fresh_status()
     for ref, got, (M, H, F, _) in zip(refs, gots, shapes):
         for k in ("h", "r", "a", "Y", "Yp"):
+            assert torch.equal(got[k], ref[k]), f"{k} differs from the workspace call (M={M}, H={H}, F={F})"
             assert_close(f64(got[k]), f64(ref[k]), TOL_BF16, f"{k} (M={M}, H={H}, F={F})")
 
 
