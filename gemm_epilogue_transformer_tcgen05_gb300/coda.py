@@ -166,7 +166,7 @@ def lib():
                                     c_void_p],
         "coda_row_rms": [P(CodaTensor), c_float, c_void_p, c_void_p],
         "coda_col_reduce": [c_void_p, c_int64, c_int64, c_int64, c_void_p, c_void_p],
-        "coda_fold_gain": [P(CodaTensor), c_void_p, P(CodaTensor), c_void_p],
+        "coda_fold_gain": [P(CodaTensor), c_void_p, c_float, P(CodaTensor), c_void_p],
         "coda_rope_table": [c_int32, c_int32, c_double, c_void_p, c_void_p, c_void_p],
         "coda_block_forward": [P(CodaBlockFwd), c_void_p],
         "coda_block_forward_noalloc": [P(CodaBlockFwd), c_void_p],
@@ -346,9 +346,10 @@ def coda_col_reduce(parts, out, stream=None):
     _check(st, "coda_col_reduce")
 
 
-def coda_fold_gain(W, g, W_out, stream=None):
+def coda_fold_gain(W, g, W_out, stream=None, out_scale=1.0):
     w, wo = desc(W), desc(W_out)
-    _check(lib().coda_fold_gain(ctypes.byref(w), _ptr(g), ctypes.byref(wo), _stream(stream)), "coda_fold_gain")
+    st = lib().coda_fold_gain(ctypes.byref(w), _ptr(g), float(out_scale), ctypes.byref(wo), _stream(stream))
+    _check(st, "coda_fold_gain")
 
 
 def coda_rope_table(seq_len, head_dim, base, cos_out, sin_out, stream=None):

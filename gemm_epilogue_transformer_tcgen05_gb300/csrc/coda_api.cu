@@ -685,20 +685,27 @@ int coda_col_reduce(const float* parts, int64_t nblocks, int64_t N, int64_t ld, 
   return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
 }
 
-int coda_fold_gain(const coda_tensor* W, const float* g, const coda_tensor* W_out, void* stream) {
+int coda_fold_gain(const coda_tensor* W, const float* g, float out_scale, const coda_tensor* W_out, void* stream) {
   int st;
   if ((st = check_tensor(W, false)) != CODA_OK) return st;
   if ((st = check_tensor(W_out, false)) != CODA_OK) return st;
   if (!g) return CODA_ERR_NULL;
   if (!aligned16(g)) return CODA_ERR_ALIGN;
-  if (W->dtype != W_out->dtype || (W->dtype != CODA_BF16 && W->dtype != CODA_F32)) return CODA_ERR_DTYPE;
-  const bool f32 = W->dtype == CODA_F32;
-  if (W->rows != W_out->rows || W->cols != W_out->cols || W->cols % (f32 ? 4 : 8) != 0) return CODA_ERR_SHAPE;
+  if (W->layout != CODA_ROW_MAJOR || W_out->layout != CODA_ROW_MAJOR) return CODA_ERR_SHAPE;
+  int kind;
+  if (W->dtype == CODA_F32 && W_out->dtype == CODA_F32) kind = FOLD_OUT_F32;
+  else if (W->dtype == CODA_BF16 && W_out->dtype == CODA_BF16) kind = FOLD_OUT_BF16;
+  else if (W->dtype == CODA_BF16 && W_out->dtype == CODA_E4M3) kind = FOLD_OUT_E4M3;
+  else return CODA_ERR_DTYPE;
+  if (!(out_scale > 0.0f) || !(out_scale < INFINITY)) return CODA_ERR_SHAPE;
+  if (kind == FOLD_OUT_E4M3 && W->ptr == W_out->ptr) return CODA_ERR_SHAPE;   // widths differ: no in place
+  const int vec = kind == FOLD_OUT_F32 ? 4 : kind == FOLD_OUT_E4M3 ? 16 : 8;
+  if (W->rows != W_out->rows || W->cols != W_out->cols || W->cols % vec != 0) return CODA_ERR_SHAPE;
   if (W->rows == 0 || W->cols == 0) return CODA_OK;
   DevState* dv;
   if ((st = ensure_device(&dv)) != CODA_OK) return st;
-  cudaError_t e = launch_fold_gain(W->ptr, W->rows, W->cols, W->ld, g, W_out->ptr, W_out->ld, f32,
-                                   static_cast<cudaStream_t>(stream), dv->sms);
+  cudaError_t e = launch_fold_gain(W->ptr, W->rows, W->cols, W->ld, g, 1.0f / out_scale, W_out->ptr, W_out->ld,
+                                   kind, static_cast<cudaStream_t>(stream), dv->sms);
   return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
 }
 

@@ -51,8 +51,9 @@ cudaError_t launch_row_rms(const void* X, int64_t M, int64_t d, int64_t ld, floa
                            int sms);
 cudaError_t launch_col_reduce(const float* parts, int64_t nblocks, int64_t N, int64_t ld, float* out,
                               cudaStream_t s);
-cudaError_t launch_fold_gain(const void* W, int64_t N, int64_t K, int64_t ld_in, const float* g, void* W_out,
-                             int64_t ld_out, bool f32, cudaStream_t s, int sms);
+enum FoldOut { FOLD_OUT_BF16 = 0, FOLD_OUT_F32 = 1, FOLD_OUT_E4M3 = 2 };
+cudaError_t launch_fold_gain(const void* W, int64_t N, int64_t K, int64_t ld_in, const float* g, float inv_scale,
+                             void* W_out, int64_t ld_out, int out_kind, cudaStream_t s, int sms);
 cudaError_t launch_rope_table(int seq_len, int head_dim, double base, float* cos_out, float* sin_out,
                               cudaStream_t s);
 cudaError_t launch_rms_gain(const void* X, int64_t M, int64_t d, int64_t ld, const float* g, float eps, float* r,

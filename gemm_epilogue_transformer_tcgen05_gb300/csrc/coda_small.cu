@@ -321,7 +321,8 @@ cudaError_t launch_col_reduce(const float* parts, int64_t nblocks, int64_t N, in
 // ---------------------------------------------------------------- gain fold
 // W'[n, k] = bf16(W[n, k] * g[k]); 8 elements (16 bytes) per thread per step, grid-stride.
 __global__ void fold_gain_kernel(const __nv_bfloat16* __restrict__ W, int64_t N, int64_t K, int64_t ld_in,
-                                 const float* __restrict__ g, __nv_bfloat16* __restrict__ Wo, int64_t ld_out) {
+                                 const float* __restrict__ g, float inv_scale, __nv_bfloat16* __restrict__ Wo,
+                                 int64_t ld_out) {
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
   const int64_t kv = K >> 3;
@@ -336,8 +337,8 @@ __global__ void fold_gain_kernel(const __nv_bfloat16* __restrict__ W, int64_t N,
     uint32_t o[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float lo = __uint_as_float(w[e] << 16) * gv[2 * e];
-      const float hi = __uint_as_float(w[e] & 0xFFFF0000u) * gv[2 * e + 1];
+      const float lo = __uint_as_float(w[e] << 16) * gv[2 * e] * inv_scale;
+      const float hi = __uint_as_float(w[e] & 0xFFFF0000u) * gv[2 * e + 1] * inv_scale;
       __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
       o[e] = *reinterpret_cast<uint32_t*>(&b);
     }
@@ -347,7 +348,8 @@ __global__ void fold_gain_kernel(const __nv_bfloat16* __restrict__ W, int64_t N,
 
 // fp32 weights: 4 elements (16 bytes) per thread per step.
 __global__ void fold_gain_f32_kernel(const float* __restrict__ W, int64_t N, int64_t K, int64_t ld_in,
-                                     const float* __restrict__ g, float* __restrict__ Wo, int64_t ld_out) {
+                                     const float* __restrict__ g, float inv_scale, float* __restrict__ Wo,
+                                     int64_t ld_out) {
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
   const int64_t kv = K >> 2;
@@ -356,23 +358,57 @@ __global__ void fold_gain_f32_kernel(const float* __restrict__ W, int64_t N, int
     const int64_t n = v / kv, k = (v - n * kv) << 2;
     const float4 w = __ldcs(reinterpret_cast<const float4*>(W + n * ld_in + k));
     const float4 gv = __ldg(reinterpret_cast<const float4*>(g + k));
-    __stcs(reinterpret_cast<float4*>(Wo + n * ld_out + k), make_float4(w.x * gv.x, w.y * gv.y, w.z * gv.z, w.w * gv.w));
+    __stcs(reinterpret_cast<float4*>(Wo + n * ld_out + k),
+           make_float4(w.x * gv.x * inv_scale, w.y * gv.y * inv_scale, w.z * gv.z * inv_scale,
+                       w.w * gv.w * inv_scale));
   }
 }
 
-cudaError_t launch_fold_gain(const void* W, int64_t N, int64_t K, int64_t ld_in, const float* g, void* W_out,
-                             int64_t ld_out, bool f32, cudaStream_t s, int sms) {
+// bf16 weights to e4m3 codes of W g / out_scale: 16 elements (32 bytes in, 16 bytes out) per
+// thread per step.
+__global__ void fold_gain_e4m3_kernel(const __nv_bfloat16* __restrict__ W, int64_t N, int64_t K, int64_t ld_in,
+                                      const float* __restrict__ g, float inv_scale, uint8_t* __restrict__ Wo,
+                                      int64_t ld_out) {
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+  const int64_t kv = K >> 4;
+  const int64_t total = N * kv;
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = v / kv, k = (v - n * kv) << 4;
+    const uint4 u0 = __ldcs(reinterpret_cast<const uint4*>(W + n * ld_in + k));
+    const uint4 u1 = __ldcs(reinterpret_cast<const uint4*>(W + n * ld_in + k + 8));
+    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float4 gv = __ldg(reinterpret_cast<const float4*>(g + k + 4 * e));
+      const float a0 = __uint_as_float(w[2 * e] << 16) * gv.x * inv_scale;
+      const float a1 = __uint_as_float(w[2 * e] & 0xFFFF0000u) * gv.y * inv_scale;
+      const float a2 = __uint_as_float(w[2 * e + 1] << 16) * gv.z * inv_scale;
+      const float a3 = __uint_as_float(w[2 * e + 1] & 0xFFFF0000u) * gv.w * inv_scale;
+      o[e] = (uint32_t)ptx::cvt_e4m3x2(a0, a1) | ((uint32_t)ptx::cvt_e4m3x2(a2, a3) << 16);
+    }
+    __stcs(reinterpret_cast<uint4*>(Wo + n * ld_out + k), make_uint4(o[0], o[1], o[2], o[3]));
+  }
+}
+
+cudaError_t launch_fold_gain(const void* W, int64_t N, int64_t K, int64_t ld_in, const float* g, float inv_scale,
+                             void* W_out, int64_t ld_out, int out_kind, cudaStream_t s, int sms) {
   const int threads = 256;
-  const int64_t need = (N * (K >> (f32 ? 2 : 3)) + threads - 1) / threads;
+  const int shift = out_kind == FOLD_OUT_F32 ? 2 : out_kind == FOLD_OUT_E4M3 ? 4 : 3;
+  const int64_t need = (N * (K >> shift) + threads - 1) / threads;
   const int64_t cap = (int64_t)sms * 8;
   const int64_t blocks = need < cap ? need : cap;
   if (blocks <= 0) return cudaSuccess;
-  if (f32)
+  if (out_kind == FOLD_OUT_F32)
     launch_k(fold_gain_f32_kernel, (unsigned)blocks, threads, s, static_cast<const float*>(W), N, K, ld_in, g,
-                                                               static_cast<float*>(W_out), ld_out);
+             inv_scale, static_cast<float*>(W_out), ld_out);
+  else if (out_kind == FOLD_OUT_E4M3)
+    launch_k(fold_gain_e4m3_kernel, (unsigned)blocks, threads, s, static_cast<const __nv_bfloat16*>(W), N, K, ld_in,
+             g, inv_scale, static_cast<uint8_t*>(W_out), ld_out);
   else
     launch_k(fold_gain_kernel, (unsigned)blocks, threads, s, static_cast<const __nv_bfloat16*>(W), N, K, ld_in, g,
-                                                           static_cast<__nv_bfloat16*>(W_out), ld_out);
+             inv_scale, static_cast<__nv_bfloat16*>(W_out), ld_out);
   return cudaGetLastError();
 }
 

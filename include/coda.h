@@ -182,7 +182,10 @@ typedef struct coda_aux_outputs {
   void* out_block_scales;       /* NVFP4 out: block scales of the codes (16-byte aligned) */
 } coda_aux_outputs;
 
-/* out = epilogue(prog, A . W^T).
+/* out = epilogue(prog, A . W^T): one GEMM whose fp32 tile stays on chip while the program runs
+ * [KuCoin, "El epílogo esconde un tesoro" (fixed mainloop, programmable epilogue before the
+ * single store); Ecosistema, "¿Qué es GEMM-epilogue…?" (C = alpha A B + beta C; scaling,
+ * activation, residual add, cast in the epilogue)].
  *   A    logical [M, K]: ROW_MAJOR (K contiguous) or COL_MAJOR (M contiguous).
  *   W    logical [N, K] (nn.Linear [out, in] layout when ROW_MAJOR); [2N, K] for SWIGLU.
  *   out  logical [M, N] ROW_MAJOR ([M, 2N] for SWIGLU_BWD).
@@ -206,10 +209,14 @@ enum coda_reduce_mode { CODA_REDUCE_RSQRT_MEAN = 0, CODA_REDUCE_SCALE_SUM = 1 };
 CODA_API int coda_rms_partial_reduce(const float* partials, int64_t ld, int32_t nparts, int64_t M, int64_t d, float eps,
                             int32_t mode, const float* rowscale, float* out, void* stream);
 
-/* Full-row RMS scale: r[i] = 1 / sqrt(mean_j X[i, j]^2 + eps) for X bf16 [M, d] ROW_MAJOR. */
+/* Full-row RMS scale: r[i] = 1 / sqrt(mean_j X[i, j]^2 + eps) for X bf16 [M, d] ROW_MAJOR
+ * [KuCoin, "El epílogo esconde un tesoro" (the light reduce that yields r), here over a stored
+ * activation that no GEMM epilogue produced].  r_out: fp32 [M], 16-byte aligned.  M = 0 is a
+ * no-op; d < 1 returns CODA_ERR_SHAPE. */
 CODA_API int coda_row_rms(const coda_tensor* X, float eps, float* r_out, void* stream);
 
-/* RMS scale and gain broadcast in one pass over X (bf16 [M, d] ROW_MAJOR):
+/* [KuCoin, "Cinco bloques…" (vector load: the RMSNorm weights broadcast)]
+ * RMS scale and gain broadcast in one pass over X (bf16 [M, d] ROW_MAJOR):
  *   r[i] = 1 / sqrt(mean_j X[i, j]^2 + eps),  u[i, j] = X[i, j] * g[j] (bf16 [M, d]).
  * The RMSNorm of a stored activation, split as the deferred-r chains use it. */
 CODA_API int coda_rms_gain(const coda_tensor* X, const float* g, float eps, float* r_out, const coda_tensor* u_out,
@@ -224,18 +231,39 @@ CODA_API int coda_xent_combine(const float* Pm, const float* Ps, int64_t ld, int
                                const float* target_logit, const int32_t* targets, int64_t V, float* lse, float* loss,
                                float* mean, void* stream);
 
-/* Column reduce: out[j] = sum_b parts[b*ld + j] over b in [0, nblocks) (fixed order). */
+/* Column reduce [KuCoin, "El epílogo esconde un tesoro" (the backward inherits the partial +
+ * light-reduce structure: here the gain gradient dg from per-slab column partials)]:
+ *   out[j] = sum_b parts[b*ld + j] over b in [0, nblocks) (fixed order, so deterministic).
+ * parts: fp32 [nblocks, ld] device, ld >= N; out: fp32 [N].  N = 0 or nblocks = 0 writes
+ * nothing / zeros respectively; negative sizes return CODA_ERR_SHAPE. */
 CODA_API int coda_col_reduce(const float* parts, int64_t nblocks, int64_t N, int64_t ld, float* out, void* stream);
 
-/* Gain fold W'[n, k] = W[n, k] * g[k] (bf16 -> bf16 or fp32 -> fp32, ROW_MAJOR [N, K]); the RMSNorm
- * gain moved onto the weight of the GEMM that follows the norm.  W_out may alias W. */
-CODA_API int coda_fold_gain(const coda_tensor* W, const float* g, const coda_tensor* W_out, void* stream);
+/* Gain fold [KuCoin, "Cinco bloques…" (vector load of the RMSNorm weights) and "El epílogo
+ * esconde un tesoro" (the normalisation's per-column factor moved onto the next GEMM)]:
+ *   W'[n, k] = W[n, k] * g[k] * (1 / out_scale)
+ * The RMSNorm gain moved onto the weight of the GEMM that follows the norm, optionally
+ * requantised for an FP8 GEMM.  W and W_out are ROW_MAJOR [N, K]:
+ *   - bf16 -> bf16 (K a multiple of 8) or fp32 -> fp32 (K a multiple of 4): out_scale = 1 gives
+ *     the plain fold; W_out may alias W.
+ *   - bf16 -> e4m3 (K a multiple of 16): W_out receives the e4m3 codes of W g / out_scale
+ *     (round to nearest even, saturating to +-448), so that out_scale * code is the folded
+ *     weight; out_scale is its per-tensor scale (e.g. max_nk |W g| / 448).  No aliasing.
+ * The product is taken in fp32 (W g, then times the fp32 reciprocal of out_scale), one rounding
+ * at the store.  g: fp32 [K] device, 16-byte aligned (CODA_ERR_ALIGN).  out_scale must be
+ * finite and > 0.  Other dtype pairs: CODA_ERR_DTYPE; mismatched shapes, K not a multiple of
+ * the vector width, a column-major tensor or an aliased e4m3 output: CODA_ERR_SHAPE. */
+CODA_API int coda_fold_gain(const coda_tensor* W, const float* g, float out_scale, const coda_tensor* W_out,
+                            void* stream);
 
-/* RoPE table: cos/sin[pos, p] = cos/sin(pos * base^(-2p / head_dim)), fp32
+/* [KuCoin, "Cinco bloques…" (RoPE as a pairwise transform)]
+ * RoPE table: cos/sin[pos, p] = cos/sin(pos * base^(-2p / head_dim)), fp32
  * [seq_len, head_dim / 2], angles evaluated in fp64 on the device. */
 CODA_API int coda_rope_table(int32_t seq_len, int32_t head_dim, double base, float* cos_out, float* sin_out, void* stream);
 
 /* ------------------------------------------------------------ block chains
+ * [KuCoin, "El epílogo esconde un tesoro" (GEMM -> residual -> RMSNorm -> GEMM with partial
+ * RMS, a light reduce and r deferred past the second GEMM) and "Resultados del experimento"
+ * (LLaMA-style blocks, 16K-token batches)]
  * LLaMA-style block tail, hidden H, FFN width F, M tokens, bf16, weights [out, in]:
  *   h = O W_o^T + R;  r = rms(h);  [G | U] = r ((h * g) W_gu^T);  a = silu(G) U;  Y = a W_d^T + h
  * (the RMSNorm y = r h g followed by the gate/up GEMM, with r deferred past the GEMM).
@@ -292,7 +320,9 @@ CODA_API int coda_block_forward(const coda_block_fwd* io, void* stream);
 #define CODA_NOALLOC_MAX_PARTIALS (1 << 20)
 CODA_API int coda_block_forward_noalloc(const coda_block_fwd* io, void* stream);
 
-/* Backward of coda_block_forward (plain-chain gradients in fused form):
+/* [KuCoin, "El epílogo esconde un tesoro" (the backward inherits the same structure: GEMMs
+ * whose epilogues apply the SwiGLU and RMSNorm backward and emit partials)]
+ * Backward of coda_block_forward (plain-chain gradients in fused form):
  *   e = r [dA U silu'(G) | dA silu(G)] with dA = dY W_d;  s_i = sum e . Z;  c = r s / H
  *   t = e W_gu;  dh = g t - c h + dY (= dR);  dg = sum_rows h t;  dO = dh W_o
  *   dW_d = dY^T a;  dW_gu[n, k] = g_k (e^T h)[n, k];  dW_o = dh^T O
@@ -323,7 +353,9 @@ typedef struct coda_block_bwd {
 } coda_block_bwd;
 CODA_API int coda_block_backward(const coda_block_bwd* io, void* stream);
 
-/* QKV projection with the deferred input-RMSNorm scale and RoPE on Q and K:
+/* [KuCoin, "El epílogo esconde un tesoro" (r deferred past the GEMM) and "Cinco bloques…"
+ * (RoPE as a pairwise transform in the epilogue)]
+ * QKV projection with the deferred input-RMSNorm scale and RoPE on Q and K:
  *   QKV = rope(r (h W_qkv'^T)), pos = row mod seq_len, r = rms(h) computed here. */
 typedef struct coda_qkv_rope_io {
   int64_t M, H, N;           /* N = (n_q + 2 n_kv) * head_dim */
@@ -337,7 +369,8 @@ typedef struct coda_qkv_rope_io {
 } coda_qkv_rope_io;
 CODA_API int coda_qkv_rope(const coda_qkv_rope_io* io, void* stream);
 
-/* Backward of coda_qkv_rope for an upstream gradient dout of its output (the attention
+/* [KuCoin, "El epílogo esconde un tesoro" (the backward inherits the structure)]
+ * Backward of coda_qkv_rope for an upstream gradient dout of its output (the attention
  * backward's dQ, dK, dV), in fused form:
  *   e = r R(-phi) dout   (rotation transposed on the first rope_ncols columns; coda_rope_backward)
  *   c = r s / H with s = r sum_n dout_n out_n (= sum_n e_n Z_n: rotations keep inner products)
@@ -363,14 +396,17 @@ typedef struct coda_qkv_rope_bwd_io {
 } coda_qkv_rope_bwd_io;
 CODA_API int coda_qkv_rope_backward(const coda_qkv_rope_bwd_io* io, void* stream);
 
-/* The row-wise RoPE-backward pass on its own: e = r R(-phi) dout (bf16 [M, N]) and
+/* [KuCoin, "Cinco bloques…" (RoPE, a pairwise transform; its gradient rotates back)]
+ * The row-wise RoPE-backward pass on its own: e = r R(-phi) dout (bf16 [M, N]) and
  * c[i] = r_i^2 sum_n dout_in out_in / H.  The cos/sin tables are those of coda_rope_table,
  * 16-byte aligned (CODA_ERR_ALIGN otherwise); head_dim a multiple of 8. */
 CODA_API int coda_rope_backward(const coda_tensor* dout, const coda_tensor* out, const float* r, const float* rope_cos,
                                 const float* rope_sin, int32_t seq_len, int32_t head_dim, int32_t rope_ncols,
                                 int64_t H, const coda_tensor* e_out, float* c_out, void* stream);
 
-/* FP8 (e4m3, per-tensor fp32 scales) MLP with deferred r:
+/* [KuCoin, "El «impuesto a la pereza»…" (FP8 makes the matmul faster, so the epilogue work
+ * around it weighs more) and "El epílogo esconde un tesoro" (deferred r)]
+ * FP8 (e4m3, per-tensor fp32 scales) MLP with deferred r:
  *   Z = r s_x s_w (X_q W_q^T);  a = silu(Z_gate) Z_up;  a_q = e4m3(a / s_a);  amax = max|a|
  *   Y = s_a s_wd (a_q W_dq^T) + h;  Y_partials = partial sums of squares of Y. */
 typedef struct coda_mlp_fp8_io {
@@ -427,17 +463,22 @@ typedef struct coda_mlp_fp8_bwd_io {
 } coda_mlp_fp8_bwd_io;
 CODA_API int coda_mlp_fp8_backward(const coda_mlp_fp8_bwd_io* io, void* stream);
 
-/* e4m3 quantisation of a bf16 tensor X (ROW_MAJOR [M, N], N a multiple of 16) into Q
+/* [KuCoin, "El «impuesto a la pereza»…" (FP8 operands for the matmul)]
+ * e4m3 quantisation of a bf16 tensor X (ROW_MAJOR [M, N], N a multiple of 16) into Q
  * (e4m3 ROW_MAJOR [M, N]): Q = e4m3(X * (1 / scale)), round to nearest even, saturating
  * to +-448, 1 / scale taken in fp32; amax (optional) receives the atomic max of |X| (the
  * caller zeroes it).  A bandwidth-bound pass: 3 bytes moved per element. */
 CODA_API int coda_quantize_e4m3(const coda_tensor* X, float scale, const coda_tensor* Q, float* amax, void* stream);
 
-/* NVFP4 quantisation of a bf16 tensor X (ROW_MAJOR [R, K], K a multiple of 64) with tensor
+/* [KuCoin, "El «impuesto a la pereza»…" (FP4 operands for the matmul; NVFP4 is the 4-bit
+ * block-scaled format of these tensor cores)]
+ * NVFP4 quantisation of a bf16 tensor X (ROW_MAJOR [R, K], K a multiple of 64) with tensor
  * scale s > 0: for each block of 16 consecutive elements of a row,
- *   sf = e4m3(amax_block / (6 s)),  q = e2m1(x * (1 / (sf s)))   (q = 0 where sf = 0),
- * each product, quotient and reciprocal rounded once in fp32 (the reciprocal, as the e4m3
- * quantiser multiplies by 1 / scale), both conversions round-to-nearest-even and saturating.
+ *   sf = e4m3(amax_block / (6 s)),  q = e2m1(x / (sf s))   (q = 0 where sf = 0),
+ * both conversions round-to-nearest-even and saturating.  The kernel takes these steps in
+ * fp32, as x * (1 / (sf s)) with each product, quotient and reciprocal rounded once, so a
+ * value within an fp32 rounding of a rounding midpoint may round the other way than in exact
+ * arithmetic.
  * Q (CODA_NVFP4 [R, K]) receives the codes, block_scales the e4m3 scale bytes, amax (optional,
  * zeroed by the caller) the atomic max of |X|.  The SwiGLU epilogue of an NVFP4 GEMM decides
  * its output's codes the same way.
@@ -451,10 +492,13 @@ CODA_API int coda_quantize_e4m3(const coda_tensor* X, float scale, const coda_te
 CODA_API int coda_quantize_nvfp4(const coda_tensor* X, float s, const coda_tensor* Q, void* block_scales,
                                  float* amax, void* stream);
 
-/* Bytes of the block scales of an NVFP4 tensor [R, K]: ceil(R / 128) * (K / 64) * 512. */
+/* Bytes of the block scales of an NVFP4 tensor [R, K]: ceil(R / 128) * (K / 64) * 512 (the
+ * layout at coda_quantize_nvfp4; no counterpart on the pages).  Needs no device. */
 CODA_API size_t coda_nvfp4_scale_bytes(int64_t R, int64_t K);
 
-/* NVFP4 MLP with deferred r, the FP8 MLP above with every GEMM operand in NVFP4:
+/* [KuCoin, "El «impuesto a la pereza»…" (FP4 makes the matmul faster) and "El epílogo esconde
+ * un tesoro" (deferred r; quantisation as an epilogue cast)]
+ * NVFP4 MLP with deferred r, the FP8 MLP above with every GEMM operand in NVFP4:
  *   Z = r s_x s_w (X W^T);  a = silu(Z_gate) Z_up;  (a_q, a_sf) = nvfp4(a, s_a);  amax = max|a|
  *   Y = s_a s_wd (a W_d^T) + h;  Y_partials = partial sums of squares of Y
  * X, W, W_d, a are (codes, block scales); s_a is the caller's delayed scale of a (e.g. the
@@ -525,8 +569,10 @@ typedef struct coda_lm_head_xent_bwd_io {
 } coda_lm_head_xent_bwd_io;
 CODA_API int coda_lm_head_xent_backward(const coda_lm_head_xent_bwd_io* io, void* stream);
 
-/* Bytes of fp32 scratch a chain needs (caller allocates).  The third size is F for the
- * block chains and V for the cross-entropy chains. */
+/* Bytes of fp32 scratch a chain needs (caller allocates): the partial buffers of the
+ * partial + light-reduce pattern [KuCoin, "El epílogo esconde un tesoro"].  The third size
+ * is F for the block chains and V for the cross-entropy chains.  Returns 0 for an unknown
+ * `which` or negative sizes.  Allocates nothing and needs no device. */
 enum coda_workspace_kind {
   CODA_WS_BLOCK_FWD = 0,
   CODA_WS_BLOCK_BWD = 1,
@@ -537,6 +583,8 @@ enum coda_workspace_kind {
 CODA_API size_t coda_workspace_size(int32_t which, int64_t M, int64_t H, int64_t F);
 
 /* ------------------------------------------------------------------ device status
+ * The pages describe no failure detection; this is the library's own: every kernel wait is
+ * bounded in time and a wait that runs out records where, instead of hanging.
  * Synchronises `stream`, then reads and clears the current device's status word.
  * *site receives 0 or the site code of the first kernel wait that ran out of time
  * (1 producer / empty stage, 2 MMA / free accumulator, 3 MMA / full stage,
@@ -545,22 +593,27 @@ CODA_API size_t coda_workspace_size(int32_t which, int64_t M, int64_t H, int64_t
  * CODA_ERR_DEVICE_TIMEOUT, or CODA_ERR_LAUNCH if the stream itself reports an error. */
 CODA_API int coda_get_device_status(void* stream, int32_t* site);
 
-/* Per-wait time limit of every kernel wait (default 2000 ms, or CODA_WATCHDOG_MS). */
+/* Per-wait time limit of every kernel wait (default 2000 ms, or CODA_WATCHDOG_MS); the
+ * library's own failure detection (no counterpart on the pages).  0 returns CODA_ERR_SHAPE. */
 CODA_API int coda_set_watchdog_ms(uint32_t ms);
 
-/* Launch overlap (default on; CODA_LAUNCH_OVERLAP=0 in the environment turns it off): every
+/* No counterpart on the pages (a launch property of this library).
+ * Launch overlap (default on; CODA_LAUNCH_OVERLAP=0 in the environment turns it off): every
  * kernel of the library is launched with a programmatic dependency on the previous kernel of
  * the stream, signals at entry and waits for that kernel's completion before its first global
  * memory access, so stream order is kept while the launch itself overlaps the previous kernel's
  * tail.  enable = 0 gives plain stream serialisation.  Other values: CODA_ERR_SHAPE. */
 CODA_API int coda_set_launch_overlap(int32_t enable);
 
-/* Test hook for the watchdog: when set, the next coda_gemm_epilogue call makes its
+/* No counterpart on the pages (tests the library's own failure detection).
+ * Test hook for the watchdog: when set, the next coda_gemm_epilogue call makes its
  * producer drop one k-block, so the MMA wait runs out of time and the kernel returns
  * through the abort path.  Cleared after one call. */
 CODA_API int coda_inject_dropped_stage(int32_t enable);
 
-/* Number of SMs of the current device and the library's build tag. */
+/* No counterpart on the pages (utilities).  Number of SMs of the current device
+ * (CODA_ERR_NO_DEVICE without an sm_103 device), the message of a status code, and the
+ * library's build tag. */
 CODA_API int coda_device_sm_count(int32_t* sms);
 CODA_API const char* coda_status_string(int status);
 CODA_API const char* coda_version(void);

@@ -104,7 +104,17 @@ def test_other_entry_points_validate(L):
     assert L.coda_col_reduce(None, 1, 1, 1, None, None) == C.ERR_NULL
     assert L.coda_rope_table(0, 64, 1e4, ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), None) == C.ERR_SHAPE
     W = _t(FAKE, C.BF16, 16, 12, 12)
-    assert L.coda_fold_gain(ctypes.byref(W), ctypes.c_void_p(FAKE), ctypes.byref(W), None) == C.ERR_ALIGN
+    assert L.coda_fold_gain(ctypes.byref(W), ctypes.c_void_p(FAKE), 1.0, ctypes.byref(W), None) == C.ERR_ALIGN
+    Wb = _t(FAKE, C.BF16, 16, 32, 32)
+    g = ctypes.c_void_p(FAKE + 0x4000)
+    fold = lambda w, s, wo: L.coda_fold_gain(ctypes.byref(w), g, s, ctypes.byref(wo), None)
+    assert fold(Wb, 0.0, Wb) == C.ERR_SHAPE                                        # out_scale must be > 0
+    assert fold(Wb, float("inf"), Wb) == C.ERR_SHAPE
+    assert fold(Wb, 1.0, _t(FAKE + 0x8000, C.F32, 16, 32, 32)) == C.ERR_DTYPE       # bf16 -> fp32
+    assert fold(Wb, 1.0, _t(FAKE, C.E4M3, 16, 32, 32)) == C.ERR_SHAPE              # e4m3 out in place
+    assert fold(_t(FAKE, C.BF16, 16, 24, 32), 1.0, _t(FAKE + 0x8000, C.E4M3, 16, 24, 32)) == C.ERR_SHAPE  # K % 16
+    assert fold(Wb, 1.0, _t(FAKE + 0x8000, C.E4M3, 16, 16, 32)) == C.ERR_SHAPE    # shapes differ
+    assert L.coda_fold_gain(None, g, 1.0, ctypes.byref(Wb), None) == C.ERR_NULL
     assert L.coda_block_forward(None, None) == C.ERR_NULL
     assert L.coda_block_backward(None, None) == C.ERR_NULL
     assert L.coda_qkv_rope(None, None) == C.ERR_NULL

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle as O
-from tests.gpu_helpers import TOL_BF16, assert_close, f64, fresh_status, seeded
+from tests.gpu_helpers import TOL_BF16, assert_close, assert_e4m3_codes, f64, fresh_status, seeded
 
 pytestmark = pytest.mark.gpu
 
@@ -150,6 +150,40 @@ def test_fold_gain_in_place(C, dtype):
         np.testing.assert_array_equal(W.cpu().numpy(), ref.astype(np.float32))
     else:
         assert np.all(np.abs(f64(W) - ref) <= np.abs(ref) * (2.0 ** -8 + U32) * (1 + 1e-12)), "in-place bf16 fold"
+
+
+@pytest.mark.parametrize("N,K,pad", [(300, 512, 0), (129, 1008, 16)])
+def test_fold_gain_e4m3_out_scale(C, N, K, pad):
+    """The fold with an FP8 requant: codes of W g / out_scale.  A code is a rounding decision the
+    kernel takes in fp32 (W g rounded once, then times the rounded reciprocal: within 3 fp32
+    roundings), so each must lie in the e4m3 rounding window of the fp64 value within 1e-6
+    relative and almost all must equal its rounding; values beyond 448 saturate."""
+    W = _padded(N, K, pad, 83, dtype=BF, std=0.05)
+    g = seeded((K,), 84, std=0.1, mean=1.0).cuda()
+    ref = O.fold_gain(f64(W), f64(g))
+    out_scale = float(np.float32(np.max(np.abs(ref)) / 448.0 * 0.8))   # the largest few saturate
+    Q = torch.full((N, K), 0xEE, dtype=torch.uint8, device="cuda")
+    C.coda_fold_gain(W, g, Q, out_scale=out_scale)
+    torch.cuda.synchronize()
+    fresh_status()
+    assert_e4m3_codes(Q.cpu().numpy(), ref / out_scale, "W g / out_scale codes", rel=1e-6)
+    assert np.any(np.abs(O.e4m3_decode(Q.cpu().numpy())) == 448.0), "no value reached the saturation"
+
+
+def test_fold_gain_out_scale_divides_bf16_and_fp32(C):
+    N, K = 256, 512
+    g = seeded((K,), 86, std=0.1, mean=1.0).cuda()
+    for dtype in (torch.float32, BF):
+        W = seeded((N, K), 85, std=0.05, dtype=dtype).cuda()
+        out = torch.empty((N, K), dtype=dtype, device="cuda")
+        C.coda_fold_gain(W, g, out, out_scale=0.25)      # a power of two: the reciprocal is exact
+        torch.cuda.synchronize()
+        ref = O.fold_gain(f64(W), f64(g)) / 0.25
+        if dtype == torch.float32:
+            np.testing.assert_array_equal(out.cpu().numpy(), ref.astype(np.float32))
+        else:
+            assert np.all(np.abs(f64(out) - ref) <= np.abs(ref) * (2.0 ** -8 + U32) * (1 + 1e-12))
+    fresh_status()
 
 
 # ------------------------------------------------------------------------- sm count
