@@ -73,6 +73,9 @@ def parse():
     p.add_argument("--nvfp4-pass", action="store_true",
                    help="run only the NVFP4 MLP (H 4096, F 14336): quantise X, then the chain twice (a short "
                         "program for a per-kernel capture)")
+    p.add_argument("--row-rms-pass", action="store_true",
+                   help="run only the full-row RMS of a [16384, 8192] bf16 tensor, five times (a short program for "
+                        "a per-kernel DRAM-bytes capture of the bandwidth-bound reduce)")
     p.add_argument("--tokens", type=int, default=M_TOK, help="token count of --traffic-pass / --nvfp4-pass")
     p.add_argument("--compile-compare", action="store_true",
                    help="also time torch.compile of the unfused comparators (compiles on first use)")
@@ -387,6 +390,25 @@ def nvfp4_pass(args):
     print(json.dumps({"nvfp4_pass": {"tokens": M, "hidden": H, "ffn": F,
                                      "order": "quantise W_gu, W_d, X; chain x2 (row RMS, gate/up GEMM, down GEMM)",
                                      "Y_rms": float(Y.float().pow(2).mean().sqrt())}}), flush=True)
+
+
+def row_rms_pass(args):
+    """The full-row RMS (coda_row_rms) of a [16384, 8192] bf16 tensor (268 MB read, 64 KB
+    written) five times back to back, with nothing else on the device."""
+    import torch
+
+    from gemm_epilogue_transformer_tcgen05_gb300 import coda as C
+
+    C.lib()
+    X = torch.randn((M_TOK, 8192), device="cuda", generator=torch.Generator(device="cuda").manual_seed(5))
+    X = X.to(torch.bfloat16)
+    r = torch.empty((M_TOK,), device="cuda")
+    for _ in range(5):
+        C.coda_row_rms(X, EPS, r)
+    torch.cuda.synchronize()
+    print(json.dumps({"row_rms_pass": {"rows": M_TOK, "cols": 8192, "launches": 5,
+                                       "bytes_per_launch": 2 * M_TOK * 8192 + 4 * M_TOK,
+                                       "r_mean": float(r.mean())}}), flush=True)
 
 
 def run_coda(args, world, rank, local):
@@ -1223,9 +1245,14 @@ def main():
     if args.impl == "reference":
         run_reference(args, world, rank)
         return
-    if args.traffic_pass or args.nvfp4_pass:
+    if args.traffic_pass or args.nvfp4_pass or args.row_rms_pass:
         if rank == 0:
-            traffic_pass(args) if args.traffic_pass else nvfp4_pass(args)
+            if args.traffic_pass:
+                traffic_pass(args)
+            elif args.nvfp4_pass:
+                nvfp4_pass(args)
+            else:
+                row_rms_pass(args)
         return
     run_coda(args, world, rank, local)
 
