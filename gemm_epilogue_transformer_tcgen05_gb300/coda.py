@@ -511,7 +511,10 @@ def coda_set_watchdog_ms(ms):
 
 
 def coda_inject_dropped_stage(enable=True):
-    _check(lib().coda_inject_dropped_stage(1 if enable else 0), "coda_inject_dropped_stage")
+    """enable: False / 0 off, True / 1 every producer drops its first k-block, 2 only the
+    second CTA of each pair, 3 only the pair's leader."""
+    mode = int(enable) if not isinstance(enable, bool) else (1 if enable else 0)
+    _check(lib().coda_inject_dropped_stage(mode), "coda_inject_dropped_stage")
 
 
 def coda_device_sm_count():

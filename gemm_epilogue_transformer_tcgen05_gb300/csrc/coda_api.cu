@@ -284,7 +284,8 @@ int coda_set_watchdog_ms(uint32_t ms) {
 }
 
 int coda_inject_dropped_stage(int32_t enable) {
-  g_inject_once = enable ? 1 : 0;
+  if (enable < 0 || enable > 3) return CODA_ERR_SHAPE;
+  g_inject_once = enable;
   return CODA_OK;
 }
 
@@ -569,7 +570,12 @@ static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const 
             (has(CODA_OP_ROW_SCALE) ? F_ROWSCALE : 0) | (has(CODA_OP_COL_DOT_PARTIAL) ? F_COLPART : 0) |
             (epi == EPI_RMSBWD && !sd.aux_in2 ? F_NO_SIDE1 : 0);
   if (ab_ready && g_launch_overlap) p.flags |= F_AB_READY;
-  if (g_inject_once.exchange(0)) p.flags |= F_INJECT_SKIP;
+  switch (g_inject_once.exchange(0)) {
+    case 1: p.flags |= F_INJECT_SKIP; break;
+    case 2: p.flags |= F_INJECT_RANK1; break;
+    case 3: p.flags |= F_INJECT_RANK0; break;
+    default: break;
+  }
   p.up_offset = (int)N;
   p.tensor_scale = has(CODA_OP_TENSOR_SCALE) ? sd.tensor_scale : 1.0f;
   p.out_scale = (out->dtype == CODA_E4M3 || epi == EPI_XENT_BWD) ? sd.out_scale : 1.0f;

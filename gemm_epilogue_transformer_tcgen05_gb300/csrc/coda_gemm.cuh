@@ -101,6 +101,8 @@ enum : int {
   F_COLPART = 64,   // write column partials (EPI_RMSBWD)
   F_AB_READY = 128, // A and B are not written by the previous kernel of the stream
   F_INJECT_SKIP = 1 << 30,  // test hook: the producer drops its first k-block
+  F_INJECT_RANK0 = 1 << 29, // test hook: only the pair's leader drops it
+  F_INJECT_RANK1 = 1 << 28, // test hook: only the pair's second CTA drops it
 };
 
 // Device status word: 0 = fine; otherwise the site of the first wait that timed out.
@@ -199,7 +201,7 @@ struct GemmCfg {
   static constexpr int OUT_WARPS = NUM_EPI_WARPS + (EARLY ? SF_WARPS : 0);   // warps storing output
   static constexpr int EPI_BYTES = OUT_WARPS * EPI_WARP_BYTES;
   static constexpr int THREADS = NUM_THREADS + 32 * SF_WARPS;
-  static constexpr int BAR_BYTES = FP4 ? 384 : 320;
+  static constexpr int BAR_BYTES = FP4 ? 384 : 320;   // barriers, then 12 bytes of flags (see the kernel)
   static constexpr int STAGES_FIT = (MAX_SMEM - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
   static constexpr int MAX_STAGES = FP4 ? 8 : 6;
   static constexpr int STAGES = STAGES_FIT > MAX_STAGES ? MAX_STAGES : STAGES_FIT;
@@ -216,7 +218,7 @@ struct GemmCfg {
   // barriers: full and empty per stage, 2 + 2 accumulator, side loads, done; NVFP4 adds per
   // stage the scales-landed (this CTA) and scales-in-TMEM (leader) barriers
   static constexpr int NBAR = 2 * STAGES + 5 + NSS * NUM_EPI_WARPS + (FP4 ? 2 * STAGES : 0);
-  static_assert(8 * NBAR + 8 <= BAR_BYTES, "barrier area");
+  static_assert(8 * NBAR + 12 <= BAR_BYTES, "barrier area");
   static_assert(!(A_MN || B_MN) || KIND != KIND_TF32, "MN-major operands are bf16 or e4m3");
   // MN-major operands: a 128-byte swizzle row holds MN_ATOM elements of M (or N); one atom is
   // BK rows of K; a 128-row tile is BM / MN_ATOM atoms; one MMA consumes UMMA_K rows of K
@@ -439,6 +441,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   uint8_t* misc = smem_raw + (sm_bar - raw) + 8 * NBAR;
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+  // CTA pairs: the second CTA's producer leaves its k-block count here, in the leader, for the
+  // leader's drain at exit (bit 31: it dropped its first k-block, the test hook)
+  volatile uint32_t* peer_iters = reinterpret_cast<volatile uint32_t*>(misc + 8);
 
 #define FULL_BAR(s) (sm_bar + 8u * (s))
 #define EMPTY_BAR(s) (sm_bar + 8u * (C::STAGES + (s)))
@@ -474,6 +479,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       }
     }
     *abort_flag = 0;
+    *peer_iters = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -508,6 +514,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
   const Watch watch{abort_flag, p.status, p.timeout_ns};
   const int total_tiles = p.m_tiles * p.n_tiles * p.k_splits;   // work items
+  // Producer (warp 0, lane 0): k-blocks it went through (issued, or dropped by the test hook)
+  // and whether it dropped the first one.  Its copies of k-block i land on FULL_BAR(i %
+  // STAGES) in phase i / STAGES; at exit these counts tell which phases may still be open.
+  int prod_iters = 0;
+  bool prod_skip0 = false;
   const int num_kb = (p.K + C::BK - 1) / C::BK;
 
   // NVFP4 SwiGLU output with its one accumulator: a quarter's epilogue warp and scale warp split
@@ -562,8 +573,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued_any = 0, issued_par = 0;
-      bool skip = (p.flags & F_INJECT_SKIP) != 0;
+      bool skip = (p.flags & F_INJECT_SKIP) || ((p.flags & F_INJECT_RANK0) && rank == 0) ||
+                  ((p.flags & F_INJECT_RANK1) && rank == 1);
+      prod_skip0 = skip;
       bool ok = true;
       const uint64_t keep = ptx::make_policy_evict_last();   // B: reused by every M-tile of a group
       const uint64_t normal = ptx::make_policy_evict_normal();
@@ -631,18 +643,27 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                       sfb_bar, keep);
               }
             }
-            issued_any |= 1u << stage;
-            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           }
+          ++prod_iters;
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      if (!ok && C::CG == 1) {  // let loads already in flight land before the CTA exits
-        for (int s = 0; s < C::STAGES; ++s)
-          if (issued_any & (1u << s)) drain_wait(FULL_BAR(s), (issued_par >> s) & 1u);
+      // Let this CTA's copies still in flight land before it exits (at once when every phase
+      // has completed, the normal case).  A k-block older than the last STAGES was consumed by
+      // the MMA, so its phase is complete.  A pair's operand copies complete on the leader's
+      // barriers, which only the leader can poll: the leader drains them for both CTAs at exit.
+      for (int i = max(0, prod_iters - C::STAGES); i < prod_iters; ++i) {
+        if (prod_skip0 && i == 0) continue;
+        if constexpr (C::CG == 1) drain_wait(FULL_BAR(i % C::STAGES), (uint32_t)(i / C::STAGES) & 1u);
+        if constexpr (C::FP4) drain_wait(SFULL_BAR(i % C::STAGES), (uint32_t)(i / C::STAGES) & 1u);
+      }
+      if constexpr (C::CG == 2) {
+        if (rank != 0)
+          ptx::st_cluster_u32(ptx::mapa(ptx::smem_u32(const_cast<uint32_t*>(peer_iters)), 0),
+                              (uint32_t)prod_iters | (prod_skip0 ? 0x80000000u : 0u));
       }
     }
     __syncwarp();
@@ -1234,11 +1255,32 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     __syncwarp();
   }
 
-  if (C::CG == 2 && *abort_flag) {
-    // aborted: a pair's loads complete on the leader's barriers, which the peer cannot poll,
-    // so give copies still in flight a fixed 200 us to land before the pair exits
-    const uint64_t t0 = ptx::globaltimer();
-    while (ptx::globaltimer() - t0 < 200000ull) {
+  if constexpr (C::CG == 2) {
+    // Both CTAs' operand copies of a k-block complete on the leader's full barrier, in one
+    // phase that the leader arms (arrive + expect_tx of both CTAs' bytes).  After an abort
+    // the two producers may have gone through different numbers of k-blocks, leaving phases
+    // that can never complete on their own: armed by the leader with bytes the second CTA
+    // never sent, or receiving the second CTA's bytes without being armed.  Once every role
+    // of both CTAs has stopped (this barrier; it also makes the second CTA's count visible),
+    // the leader completes those phases for the missing side and waits, bounded, until every
+    // copy has landed.  Only then does the pair meet at the final barrier below, after which
+    // either CTA may exit.
+    ptx::tc_fence_before();
+    ptx::cluster_sync();
+    if (warp == 0 && lane == 0 && leader) {
+      const uint32_t w = *peer_iters;
+      const int n_l = prod_iters, n_p = (int)(w & 0x7FFFFFFFu);
+      const bool skip_l = prod_skip0, skip_p = (w >> 31) != 0;
+      constexpr uint32_t PEER_BYTES = A_STAGE_BYTES + C::B_STAGE_BYTES;
+      for (int i = max(0, min(n_l, n_p) - C::STAGES); i < max(n_l, n_p); ++i) {
+        const bool by_l = i < n_l && !(skip_l && i == 0);
+        const bool by_p = i < n_p && !(skip_p && i == 0);
+        if (!by_l && !by_p) continue;
+        const uint32_t fb = FULL_BAR(i % C::STAGES);
+        if (by_l && !by_p) ptx::mbar_complete_tx(fb, PEER_BYTES);       // bytes that will never come
+        if (!by_l && by_p) ptx::mbar_arrive_expect_tx(fb, PEER_BYTES);  // arm it for the bytes that do
+        drain_wait(fb, (uint32_t)(i / C::STAGES) & 1u);
+      }
     }
   }
   ptx::tc_fence_before();

@@ -32,6 +32,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Lowers the current phase's pending transaction count by `bytes` without a copy (used only
+// after an abort, for bytes that were expected but will never be sent).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
 // True once the phase with the given parity has completed (try_wait may suspend the
 // thread for a short, hardware-defined time before answering false).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -158,6 +163,10 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
 // cluster scope would add a cluster-wide fence (about half a microsecond) to every arrival.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// 32-bit store to shared memory given by its cluster address (possibly in the peer CTA).
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 // Cluster-wide barrier (every thread of every CTA of the cluster).
 __device__ __forceinline__ void cluster_sync() {

@@ -606,9 +606,12 @@ CODA_API int coda_set_watchdog_ms(uint32_t ms);
 CODA_API int coda_set_launch_overlap(int32_t enable);
 
 /* No counterpart on the pages (tests the library's own failure detection).
- * Test hook for the watchdog: when set, the next coda_gemm_epilogue call makes its
- * producer drop one k-block, so the MMA wait runs out of time and the kernel returns
- * through the abort path.  Cleared after one call. */
+ * Test hook for the watchdog: the next coda_gemm_epilogue call drops its first k-block, so
+ * the MMA wait runs out of time and the kernel returns through the abort path.  Cleared after
+ * one call.  enable: 0 off; 1 every producer drops it; for the CTA-pair GEMMs (every bf16,
+ * e4m3 and NVFP4 program) 2 only the second CTA of each pair drops it (the leader has armed
+ * that phase for bytes that never come) and 3 only the leader does (the second CTA's bytes
+ * land on a phase nobody armed).  Other values: CODA_ERR_SHAPE. */
 CODA_API int coda_inject_dropped_stage(int32_t enable);
 
 /* No counterpart on the pages (utilities).  Number of SMs of the current device

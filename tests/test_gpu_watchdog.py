@@ -1,10 +1,11 @@
 """Failure detection on the GPU without a fault: a wait that runs out.
 
-The test hook makes the producer of the next GEMM launch drop one k-block, so the MMA
-thread waits for a stage that never fills.  The bounded wait gives up after the watchdog
-limit (200 ms here), the kernel leaves through its abort path (drains its copies, frees
-TMEM, returns) and the host reads CODA_ERR_DEVICE_TIMEOUT with the site of the wait.
-Nothing traps.  The context must still be usable afterwards: the next GEMM is exact."""
+The test hook makes the producer of the next GEMM launch drop one k-block (in both CTAs of
+a pair, or in one of them only), so the MMA thread waits for a stage that never fills.  The
+bounded wait gives up after the watchdog limit (200 ms here), the kernel leaves through its
+abort path (drains its copies, frees TMEM, returns) and the host reads
+CODA_ERR_DEVICE_TIMEOUT with the site of the wait.  Nothing traps.  The context must still
+be usable afterwards: the next GEMM is exact."""
 import pytest
 import torch
 
@@ -46,6 +47,42 @@ def test_dropped_stage_times_out_and_context_survives(C):
     st3, _ = C.coda_get_device_status()
     assert st3 == C.OK
     assert_close(f64(out2), O.linear(f64(A), f64(W)), TOL_BF16, "GEMM after a timed-out launch")
+
+
+@pytest.mark.parametrize("mode,what", [(2, "second CTA only"), (3, "leader only")])
+def test_one_side_of_a_pair_drops_a_stage(C, mode, what):
+    """A CTA pair whose two producers disagree: with mode 2 the leader arms the k-block's phase
+    for both CTAs' bytes and the second CTA never sends its own; with mode 3 the second CTA's
+    bytes land on a phase the leader never armed.  Either way the MMA wait runs out, and at
+    exit the leader completes that phase for the missing side and waits for every copy to land
+    before the pair leaves.  The next launch is exact; so is one with several waves of tiles."""
+    M, N, K = 512, 1024, 1024
+    A = dev(seeded((M, K), 68, dtype=BF))
+    W = dev(seeded((N, K), 69, std=0.05, dtype=BF))
+    out = torch.zeros((M, N), dtype=BF, device="cuda")
+    C.coda_set_watchdog_ms(200)
+    C.coda_inject_dropped_stage(mode)
+    C.coda_gemm_epilogue(A, W, [], out)
+    st, site = C.coda_get_device_status()
+    assert st == C.ERR_DEVICE_TIMEOUT, (what, st)
+    assert site in (1, 2, 3, 4, 5, 6, 7), site
+    C.coda_set_watchdog_ms(2000)
+    out2 = torch.empty((M, N), dtype=BF, device="cuda")
+    C.coda_gemm_epilogue(A, W, [], out2)
+    assert C.coda_get_device_status()[0] == C.OK
+    assert_close(f64(out2), O.linear(f64(A), f64(W)), TOL_BF16, f"GEMM after a timed-out launch ({what})")
+    M2, N2 = 4096, 4096                                  # 256 tiles over the resident pairs
+    A2 = dev(seeded((M2, K), 70, dtype=BF))
+    W2 = dev(seeded((N2, K), 71, std=0.05, dtype=BF))
+    out3 = torch.empty((M2, N2), dtype=BF, device="cuda")
+    C.coda_gemm_epilogue(A2, W2, [], out3)
+    assert C.coda_get_device_status()[0] == C.OK
+    assert_close(f64(out3), O.linear(f64(A2), f64(W2)), TOL_BF16, "a multi-wave GEMM afterwards")
+
+
+def test_inject_mode_out_of_range_is_refused(C):
+    with pytest.raises(C.CodaError):
+        C.coda_inject_dropped_stage(4)
 
 
 @pytest.mark.parametrize("program", ["residual", "swiglu_backward"])
