@@ -61,6 +61,16 @@ Readings of points the pages leave open (the plainest reading consistent with th
      rounding of a midpoint; the tests accept exactly those codes.  s is chosen by the
      caller: amax / (6 * 448) of the tensor for operands known up front, and a delayed scale
      (as s_a above) for the SwiGLU output.
+ 10. NVFP4 backward of the MLP: the block-scaled tensor cores take both operands blocked along
+     the GEMM's own K, so every backward GEMM quantises its two operands along its K.  dY is
+     quantised along its rows for dA = dY W_d (K = H) and along its columns for dW_d = dY^T a
+     (K = tokens); W_d and W_gu are quantised transposed (blocks along F and 2F); e along its
+     rows for t = e W_gu (K = 2F) and along its columns for dW = e^T x (K = tokens); a is
+     recomputed from the saved Z (a = silu(G) U) and x is the bf16 activation h, both quantised
+     along the token axis for the weight gradients.  Scales: s_dy and s_e are the caller's
+     delayed scales (as reading 8), s_a the forward's, the others amax / (6 * 448) of their
+     tensor.  The row sum behind c uses e before quantisation (the SwiGLU-backward epilogue
+     forms it there), and the residual gradient and the combine use dY and h as stored.
 Every function here is pinned by a test (closed form, invariant, library special case
 or brute force); none is "parity unpinned".
 """
@@ -294,6 +304,18 @@ def nvfp4_dequantize(q, sf, s):
     return F64(s) * np.repeat(sf, NVFP4_BLOCK, axis=1) * q
 
 
+def nvfp4_round_rows(x, s):
+    """x [R, K] quantised along its rows (blocks of 16 consecutive columns) and dequantised."""
+    q, sf = nvfp4_quantize(x, s)
+    return nvfp4_dequantize(q, sf, s)
+
+
+def nvfp4_round_cols(x, s):
+    """x [R, K] quantised along its columns (blocks of 16 consecutive rows) and dequantised:
+    the row quantisation of the transpose, transposed back."""
+    return nvfp4_round_rows(_f64(x).T, s).T
+
+
 def mlp_nvfp4(h, Xq, Xsf, s_x, Wq, Wsf, s_w, Wdq, Wdsf, s_wd, s_a, eps, bn):
     """The FP8 MLP above with NVFP4 operands (reading 9).  x, W (the effective gate/up weight)
     and W_d are given as (codes, block scales, tensor scale); r comes from the bf16 h.
@@ -481,6 +503,33 @@ def mlp_fp8_backward(h, Xq_val, s_x, Wq_val, s_w, Wdq_val, s_wd, Z, aq_val, s_a,
     return dict(dYq_val=dYq_val, amax_dy=float(np.max(np.abs(dY))), dA=dA, e=e, eq_val=eq_val,
                 amax_e=float(np.max(np.abs(e))), e_hat=e_hat, s=s, c=c, t=t, dh=dh, dW_d=dYd.T @ a,
                 dW=e_hat.T @ x)
+
+
+def mlp_nvfp4_backward(h, W_gu, W_d, Z, r, dY, s_dy, s_e, s_a, s_x, s_wt, s_wdt, quant=True):
+    """Backward of the MLP with NVFP4 GEMM operands (reading 10).  h, W_gu (the effective
+    gate/up weight, [2F, H]), W_d ([H, F]) and dY are the bf16 tensors; Z = [G | U] and r are
+    saved by the forward.  Rr / Rc quantise along rows / columns (identity when quant is False):
+      dA = Rr(dY, s_dy) Rr(W_d^T, s_wdt)^T;  e = r [dA U silu'(G) | dA silu(G)]
+      s_i = sum_k e_ik Z_ik;  c = r s / H
+      t = Rr(e, s_e) Rr(W_gu^T, s_wt)^T;  dh = t - c h + dY
+      dW_d = Rc(dY, s_dy)^T Rc(silu(G) U, s_a);  dW = Rc(e, s_e)^T Rc(h, s_x)"""
+    h, W_gu, W_d, Z, r, dY = (_f64(v) for v in (h, W_gu, W_d, Z, r, dY))
+    Rr = nvfp4_round_rows if quant else (lambda x, s: _f64(x))
+    Rc = nvfp4_round_cols if quant else (lambda x, s: _f64(x))
+    H = h.shape[1]
+    F = Z.shape[1] // 2
+    G, U = Z[:, :F], Z[:, F:]
+    dA = Rr(dY, s_dy) @ Rr(W_d.T, s_wdt).T
+    e = r[:, None] * np.hstack([dA * U * silu_grad(G), dA * silu(G)])
+    s = np.sum(e * Z, axis=1)
+    c = r * s / H
+    t = Rr(e, s_e) @ Rr(W_gu.T, s_wt).T
+    dh = t - c[:, None] * h + dY
+    a = swiglu(G, U)
+    dW_d = Rc(dY, s_dy).T @ Rc(a, s_a)
+    dW = Rc(e, s_e).T @ Rc(h, s_x)
+    return dict(dA=dA, e=e, amax_e=float(np.max(np.abs(e))), amax_dy=float(np.max(np.abs(dY))), s=s, c=c, t=t,
+                dh=dh, a=a, dW_d=dW_d, dW=dW)
 
 
 # ---------------------------------------------------------------------------------------

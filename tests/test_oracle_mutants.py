@@ -343,3 +343,36 @@ def test_deferred_r_on_the_gate_half_only_is_caught(monkeypatch):
         return dict(h=h, P=P, r=r, Z=Z, G=G, U=U, a=a, Y=Y)
     _plant(monkeypatch, "block_forward_deferred", mutant)
     assert _fails(pins.test_deferred_r_equals_naive)
+
+
+def _nvfp4_bwd_variant(transform):
+    """A copy of the oracle's NVFP4 MLP backward with one planted change applied by `transform`
+    to the source of the function."""
+    import inspect
+    src = inspect.getsource(OC.mlp_nvfp4_backward)
+    mutated = transform(src)
+    assert mutated != src
+    ns = dict(OC.__dict__)
+    exec(mutated, ns)
+    return ns["mlp_nvfp4_backward"]
+
+
+def test_nvfp4_bwd_dy_quantised_along_the_wrong_axis_is_caught(monkeypatch):
+    import tests.test_oracle_nvfp4_bwd as bwd
+    bad = _nvfp4_bwd_variant(lambda s: s.replace("dW_d = Rc(dY, s_dy).T", "dW_d = Rr(dY, s_dy).T"))
+    _plant(monkeypatch, "mlp_nvfp4_backward", bad)
+    assert _fails(bwd.test_quantised_gradients_match_brute_force_blocks_along_each_contraction)
+
+
+def test_nvfp4_bwd_e_quantised_along_the_wrong_axis_is_caught(monkeypatch):
+    import tests.test_oracle_nvfp4_bwd as bwd
+    bad = _nvfp4_bwd_variant(lambda s: s.replace("dW = Rc(e, s_e).T", "dW = Rr(e, s_e).T"))
+    _plant(monkeypatch, "mlp_nvfp4_backward", bad)
+    assert _fails(bwd.test_quantised_gradients_match_brute_force_blocks_along_each_contraction)
+
+
+def test_nvfp4_bwd_dropped_rmsnorm_term_is_caught(monkeypatch):
+    import tests.test_oracle_nvfp4_bwd as bwd
+    bad = _nvfp4_bwd_variant(lambda s: s.replace("dh = t - c[:, None] * h + dY", "dh = t + dY"))
+    _plant(monkeypatch, "mlp_nvfp4_backward", bad)
+    assert _fails(bwd.test_unquantised_gradients_are_the_finite_differences)
