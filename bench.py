@@ -1037,6 +1037,8 @@ def other_workloads(torch, C, S, args, stream):
                                    "(quantize_x_ms, the pass a previous layer's epilogue would fold in)"}
     del h4, X4, W4, Wd4, Y4, P4, a4
     torch.cuda.empty_cache()
+    # N4: the NVFP4 MLP backward (each GEMM's operands quantised along its own K)
+    out["mlp_nvfp4_backward_N4"] = nvfp4_backward_workload(torch, C, S, steps, peak4, pk)
     # N3: the block forward at the 7B and 70B LLaMA-3 hidden sizes, beside torch eager
     for name, Hs, Fs in (("block_forward_7B_H4096_F14336", 4096, 14336), ("block_forward_70B_H8192_F28672", 8192,
                                                                            28672)):
@@ -1089,6 +1091,53 @@ def other_workloads(torch, C, S, args, stream):
     del hl, gl, Wv, tg, ul, el, dhl, dWv, wsb, wsx
     torch.cuda.empty_cache()
     return out
+
+
+def nvfp4_backward_workload(torch, C, S, steps, peak4, pk, M=M_TOK, H=4096, F=14336):
+    """Device time of the NVFP4 MLP backward at the LLaMA-3-8B MLP shape: 11 launches (dY
+    quantised along rows and columns, the dA GEMM with the SwiGLU-backward epilogue, the row
+    reduce, e along rows and columns, silu(G) U and h along columns, the dW_d, dh and dW GEMMs).
+    The weights' transposed quantisation is weight preparation, outside the timing."""
+    t = S.nvfp4_mlp_bwd_inputs(M, H, F, seed=0, device="cuda")
+    sc = lambda x: float(x.abs().max()) / (6 * 448)
+    W_guT, W_dT = C.Nvfp4.empty(H, 2 * F, sc(t["W_gu"])), C.Nvfp4.empty(F, H, sc(t["W_d"]))
+    C.coda_quantize_nvfp4_t(t["W_gu"], W_guT)
+    C.coda_quantize_nvfp4_t(t["W_d"], W_dT)
+    nv = lambda R, K: C.Nvfp4.empty(R, K)
+    bufs = dict(dY_r=nv(M, H), dY_c=nv(H, M), e=torch.empty((M, 2 * F), dtype=torch.bfloat16, device="cuda"),
+                e_r=nv(M, 2 * F), e_c=nv(2 * F, M), a_c=nv(F, M), x_c=nv(H, M),
+                amax_dy=torch.empty((1,), device="cuda"), amax_e=torch.empty((1,), device="cuda"),
+                c=torch.empty((M,), device="cuda"), dh=torch.empty((M, H), dtype=torch.bfloat16, device="cuda"),
+                dW_d=torch.empty((H, F), device="cuda"), dW=torch.empty((2 * F, H), device="cuda"))
+    ws = torch.empty((C.coda_workspace_size(C.WS_MLP_NVFP4_BWD, M, H, F) // 4,), device="cuda")
+    G, U = t["Z"][:, :F].float(), t["Z"][:, F:].float()
+    s_a = float((torch.nn.functional.silu(G) * U).abs().max()) / (6 * 448)
+    del G, U
+    s_dy, s_x = sc(t["dY"]), sc(t["h"])
+    s_e = [1.0]
+    b = bufs
+    run = lambda: C.coda_mlp_nvfp4_backward(t["h"], W_guT, W_dT, t["Z"], t["r"], t["dY"], s_x, s_a, s_dy, s_e[0],
+                                            b["dY_r"], b["dY_c"], b["e"], b["e_r"], b["e_c"], b["a_c"], b["x_c"],
+                                            b["amax_dy"], b["amax_e"], b["c"], b["dh"], b["dW_d"], b["dW"], ws)
+    run()
+    torch.cuda.synchronize()
+    s_e[0] = float(b["amax_e"].item()) / (6 * 448)      # delayed scaling from the previous pass
+    ms = _time(torch, run, torch.cuda.current_stream(), steps)
+    flop = 12 * M * H * F                                # dA, dW_d: 2MHF each; dh, dW: 4MHF each
+    n4 = lambda R, K: R * K // 2 + R * K // 16           # NVFP4 codes + block scales
+    byt = (2 * M * H + 2 * n4(M, H)) + (n4(M, H) + n4(F, H) + 2 * 2 * M * F + 2 * 2 * M * F + 4 * M) + \
+        (2 * 2 * M * F + 2 * n4(M, 2 * F)) + (2 * 2 * M * F + n4(F, M)) + (2 * M * H + n4(H, M)) + \
+        (n4(H, M) + n4(F, M) + 4 * H * F) + (n4(M, 2 * F) + n4(H, 2 * F) + 2 * 3 * M * H + 4 * M) + \
+        (n4(2 * F, M) + n4(H, M) + 4 * 2 * F * H)
+    roof = max(flop / (peak4 * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
+    res = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "roofline_ms": roof, "roofline_frac": roof / ms,
+           "tokens_per_s": M / (ms * 1e-3), "launches": 11, "peak_tflops": peak4, "bytes": byt,
+           "note": "quantise dY (rows, columns), dA GEMM + SwiGLU-bwd (bf16 e), row reduce, quantise e (rows, "
+                   "columns), silu(G) U and h (columns), dW_d, dh GEMM + RMSNorm-bwd combine, dW; NVFP4 operands "
+                   "blocked along each GEMM's K"}
+    del t, bufs, ws
+    torch.cuda.empty_cache()
+    return res
 
 
 def compiled_time(torch, fn, stream, steps, ms_coda):

@@ -124,6 +124,21 @@ def nvfp4_mlp_inputs(M, H, F, seed=0, w_std=0.015, device="cpu"):
     return dict(h=h, W_gu=W_gu, W_d=W_d, eps=1e-6)
 
 
+def nvfp4_mlp_bwd_inputs(M, H, F, seed=0, w_std=0.015, device="cpu"):
+    """Tensors of the NVFP4 MLP backward in bf16: h ~ N(0, 1), weights ~ N(0, 0.015^2), a saved
+    Z = [G | U] ~ N(0, 1), a row scale r ~ 1 + N(0, 0.1^2) (fp32) and an output gradient
+    dY ~ N(0, 1); the drawing order is h, W_gu, W_d, Z, r, dY."""
+    gen = torch.Generator(device=device).manual_seed(seed)
+    bf = torch.bfloat16
+    h = torch.randn((M, H), generator=gen, device=device).to(bf)
+    W_gu = (torch.randn((2 * F, H), generator=gen, device=device) * w_std).to(bf)
+    W_d = (torch.randn((H, F), generator=gen, device=device) * w_std).to(bf)
+    Z = torch.randn((M, 2 * F), generator=gen, device=device).to(bf)
+    r = 1.0 + 0.1 * torch.randn((M,), generator=gen, device=device)
+    dY = torch.randn((M, H), generator=gen, device=device).to(bf)
+    return dict(h=h, W_gu=W_gu, W_d=W_d, Z=Z, r=r, dY=dY)
+
+
 def lm_head_inputs(M, H, V, seed=0, w_std=0.02, dtype=torch.bfloat16):
     gen = torch.Generator().manual_seed(seed)
     return dict(

@@ -29,7 +29,7 @@ OP_TENSOR_SCALE, OP_ROW_SCALE, OP_COL_SCALE, OP_ADD_SIDE, OP_SWIGLU, OP_ROPE = 1
 OP_SWIGLU_BWD, OP_RMSBWD_COMBINE, OP_ROW_SUMSQ_PARTIAL, OP_ROW_DOT_PARTIAL = 7, 8, 9, 10
 OP_COL_DOT_PARTIAL, OP_AMAX, OP_STORE_AUX, OP_STORE_COL_SCALED, OP_XENT_PARTIAL, OP_XENT_BWD = 11, 12, 13, 14, 15, 16
 REDUCE_RSQRT_MEAN, REDUCE_SCALE_SUM = 0, 1
-WS_BLOCK_FWD, WS_BLOCK_BWD, WS_XENT_FWD, WS_XENT_BWD, WS_MLP_FP8_BWD = 0, 1, 2, 3, 4
+WS_BLOCK_FWD, WS_BLOCK_BWD, WS_XENT_FWD, WS_XENT_BWD, WS_MLP_FP8_BWD, WS_MLP_NVFP4_BWD = 0, 1, 2, 3, 4, 5
 MAX_OPS = 8
 
 EXPORTED = [
@@ -39,7 +39,8 @@ EXPORTED = [
     "coda_device_sm_count", "coda_status_string", "coda_version", "coda_block_forward_noalloc", "coda_rms_gain",
     "coda_xent_combine", "coda_lm_head_xent_forward", "coda_lm_head_xent_backward", "coda_rope_backward",
     "coda_qkv_rope_backward", "coda_mlp_fp8_backward", "coda_quantize_e4m3", "coda_set_launch_overlap",
-    "coda_quantize_nvfp4", "coda_nvfp4_scale_bytes", "coda_mlp_nvfp4",
+    "coda_quantize_nvfp4", "coda_nvfp4_scale_bytes", "coda_mlp_nvfp4", "coda_quantize_nvfp4_t",
+    "coda_mlp_nvfp4_backward",
 ]
 NOALLOC_MAX_PARTIALS = 1 << 20
 
@@ -113,6 +114,14 @@ class CodaMlpNvfp4(Structure):
                 ("X_sf", c_void_p), ("W_q", c_void_p), ("W_sf", c_void_p), ("W_dq", c_void_p), ("W_dsf", c_void_p),
                 ("r", c_void_p), ("a_q", c_void_p), ("a_sf", c_void_p), ("amax", c_void_p), ("Y", c_void_p),
                 ("Y_partials", c_void_p)]
+
+
+class CodaMlpNvfp4Bwd(Structure):
+    _fields_ = [("M", c_int64), ("H", c_int64), ("F", c_int64), ("s_x", c_float), ("s_wt", c_float),
+                ("s_wdt", c_float), ("s_a", c_float), ("s_dy", c_float), ("s_e", c_float)] + \
+               [(n, c_void_p) for n in ("h", "W_guT", "W_guT_sf", "W_dT", "W_dT_sf", "Z", "r", "dY", "dY_r", "dY_r_sf",
+                                        "dY_c", "dY_c_sf", "e", "e_r", "e_r_sf", "e_c", "e_c_sf", "a_c", "a_c_sf",
+                                        "x_c", "x_c_sf", "amax_dy", "amax_e", "c", "dh", "dW_d", "dW", "workspace")]
 
 
 class CodaMlpFp8Bwd(Structure):
@@ -190,6 +199,8 @@ def lib():
         "coda_qkv_rope_backward": [P(CodaQkvRopeBwd), c_void_p],
         "coda_quantize_nvfp4": [P(CodaTensor), c_float, P(CodaTensor), c_void_p, c_void_p, c_void_p],
         "coda_mlp_nvfp4": [P(CodaMlpNvfp4), c_void_p],
+        "coda_quantize_nvfp4_t": [P(CodaTensor), c_int32, c_float, P(CodaTensor), c_void_p, c_void_p, c_void_p],
+        "coda_mlp_nvfp4_backward": [P(CodaMlpNvfp4Bwd), c_void_p],
     }
     for name, args in sigs.items():
         fn = getattr(L, name)
@@ -476,6 +487,33 @@ def coda_quantize_nvfp4(X, Q, amax=None, stream=None):
     x, q = desc(X), desc_nvfp4(Q.codes)
     _check(lib().coda_quantize_nvfp4(ctypes.byref(x), Q.s, ctypes.byref(q), _ptr(Q.scales), _ptr(amax),
                                      _stream(stream)), "coda_quantize_nvfp4")
+
+
+QT_PLAIN, QT_SWIGLU = 0, 1
+
+
+def coda_mlp_nvfp4_backward(h, W_guT, W_dT, Z, r, dY, s_x, s_a, s_dy, s_e, dY_r, dY_c, e, e_r, e_c, a_c, x_c, amax_dy,
+                            amax_e, c, dh, dW_d, dW, workspace, stream=None):
+    """Backward of the NVFP4 MLP.  W_guT, W_dT are the transposed weight quantisations (Nvfp4
+    [H, 2F] and [F, H], their .s the tensor scales); dY_r, dY_c, e_r, e_c, a_c, x_c are Nvfp4
+    outputs whose .s is ignored (the scales s_dy, s_e, s_a, s_x apply)."""
+    M, H = h.shape
+    F = Z.shape[1] // 2
+    io = CodaMlpNvfp4Bwd(M, H, F, s_x, W_guT.s, W_dT.s, s_a, s_dy, s_e, _ptr(h), _ptr(W_guT.codes),
+                         _ptr(W_guT.scales), _ptr(W_dT.codes), _ptr(W_dT.scales), _ptr(Z), _ptr(r), _ptr(dY),
+                         _ptr(dY_r.codes), _ptr(dY_r.scales), _ptr(dY_c.codes), _ptr(dY_c.scales), _ptr(e),
+                         _ptr(e_r.codes), _ptr(e_r.scales), _ptr(e_c.codes), _ptr(e_c.scales), _ptr(a_c.codes),
+                         _ptr(a_c.scales), _ptr(x_c.codes), _ptr(x_c.scales), _ptr(amax_dy), _ptr(amax_e), _ptr(c),
+                         _ptr(dh), _ptr(dW_d), _ptr(dW), _ptr(workspace))
+    _check(lib().coda_mlp_nvfp4_backward(ctypes.byref(io), _stream(stream)), "coda_mlp_nvfp4_backward")
+
+
+def coda_quantize_nvfp4_t(X, Q, mode=QT_PLAIN, amax=None, stream=None):
+    """Q (an Nvfp4 [C, R], tensor scale Q.s) = NVFP4 quantisation of the bf16 X [R, C] along its
+    columns, i.e. of X^T; with mode QT_SWIGLU, X is [G | U] ([R, 2C]) and silu(G) U is quantised."""
+    x, q = desc(X), desc_nvfp4(Q.codes)
+    _check(lib().coda_quantize_nvfp4_t(ctypes.byref(x), int(mode), Q.s, ctypes.byref(q), _ptr(Q.scales), _ptr(amax),
+                                       _stream(stream)), "coda_quantize_nvfp4_t")
 
 
 def coda_mlp_nvfp4(h, X, W, Wd, eps, r, a, amax, Y, Y_partials, stream=None):

@@ -130,16 +130,19 @@ int encode_2d(CUtensorMap* m, int dtype, const void* ptr, int64_t inner, int64_t
 }
 
 // 3-D map of a ROW_MAJOR [rows, 2 * half] tensor whose two column halves (gate, up) are copied
-// together: dims {half, rows, 2} (strides: a row, then a half), box {32, 32, 2}, i.e. the two
-// 32 x 32 blocks of the halves one after the other, each swizzled like a 2-D 32 x 32 box.
-int encode_pair(CUtensorMap* m, int dtype, const void* ptr, int64_t half, int64_t rows, int64_t ld) {
+// together: dims {half, rows, 2} (strides: a row, then a half), box {box_in, 32, 2}, i.e. the
+// two 32-row blocks of the halves one after the other, each swizzled like a 2-D box.
+int encode_pair(CUtensorMap* m, int dtype, const void* ptr, int64_t half, int64_t rows, int64_t ld,
+                uint32_t box_in = 32) {
   const int es = esize(dtype);
-  const uint32_t row_bytes = 32u * (uint32_t)es;
-  CUtensorMapSwizzle sw = row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  const uint32_t row_bytes = box_in * (uint32_t)es;
+  CUtensorMapSwizzle sw = row_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                          : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                            : CU_TENSOR_MAP_SWIZZLE_32B;
   CUtensorMapDataType t = dtype == CODA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   cuuint64_t dims[3] = {(cuuint64_t)(half > 0 ? half : 1), (cuuint64_t)(rows > 0 ? rows : 1), 2};
   cuuint64_t strides[2] = {(cuuint64_t)(ld * es), (cuuint64_t)(half * es)};
-  cuuint32_t box[3] = {32, 32, 2};
+  cuuint32_t box[3] = {box_in, 32, 2};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, t, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -483,10 +486,10 @@ static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const 
   }
   if (out->dtype == CODA_NVFP4) {
     if ((st = encode_2d(&L.tmOut, CODA_E4M3, out->ptr, N / 2, M, out->ld / 2, 16, 32)) != CODA_OK) return st;
-  } else if (epi == EPI_SWIGLU_BWD) {
-    if ((st = encode_pair(&L.tmOut, out->dtype, out->ptr, N, M, out->ld)) != CODA_OK) return st;   // e: both halves
-  } else if (epi != EPI_XENT &&
-             (st = encode_2d(&L.tmOut, out->dtype, out->ptr, out->cols, M, out->ld, 32, 32)) != CODA_OK) {
+  } else if (epi == EPI_SWIGLU_BWD) {   // e: both halves, ow chunks of 32 columns per store
+    if ((st = encode_pair(&L.tmOut, out->dtype, out->ptr, N, M, out->ld, 32u * var->ow)) != CODA_OK) return st;
+  } else if (epi != EPI_XENT && (st = encode_2d(&L.tmOut, out->dtype, out->ptr, out->cols, M, out->ld,
+                                                32u * var->ow, 32)) != CODA_OK) {
     return st;
   }
   if (epi == EPI_RESID) {
@@ -504,11 +507,11 @@ static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const 
     }
   }
   if (want_aux && epi == EPI_SWIGLU) {
-    const coda_tensor* z = ax.store_aux;   // saved Z = [G | U]: both halves of a chunk in one copy
-    if ((st = encode_pair(&L.tmAux, z->dtype, z->ptr, N, M, z->ld)) != CODA_OK) return st;
+    const coda_tensor* z = ax.store_aux;   // saved Z = [G | U]: both halves of a store group in one copy
+    if ((st = encode_pair(&L.tmAux, z->dtype, z->ptr, N, M, z->ld, 32u * var->ow)) != CODA_OK) return st;
   } else if (want_aux) {
     const coda_tensor* z = ax.store_aux;
-    if ((st = encode_2d(&L.tmAux, z->dtype, z->ptr, z->cols, M, z->ld, 32, 32)) != CODA_OK) return st;
+    if ((st = encode_2d(&L.tmAux, z->dtype, z->ptr, z->cols, M, z->ld, 32u * var->ow, 32)) != CODA_OK) return st;
   }
 
   GemmParams& p = L.p;
@@ -680,6 +683,28 @@ int coda_quantize_nvfp4(const coda_tensor* X, float s, const coda_tensor* Q, voi
   return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
 }
 
+int coda_quantize_nvfp4_t(const coda_tensor* X, int32_t mode, float s, const coda_tensor* Q, void* block_scales,
+                          float* amax, void* stream) {
+  int st;
+  if ((st = check_tensor(X, false)) != CODA_OK) return st;
+  if ((st = check_tensor(Q, false)) != CODA_OK) return st;
+  if (X->dtype != CODA_BF16 || Q->dtype != CODA_NVFP4) return CODA_ERR_DTYPE;
+  if (mode != CODA_QT_PLAIN && mode != CODA_QT_SWIGLU) return CODA_ERR_SHAPE;
+  const int64_t R = X->rows, C = mode == CODA_QT_SWIGLU ? X->cols / 2 : X->cols;
+  if (mode == CODA_QT_SWIGLU && X->cols % 2 != 0) return CODA_ERR_SHAPE;
+  if (Q->rows != C || Q->cols != R || R % 64 != 0 || C % 128 != 0) return CODA_ERR_SHAPE;
+  if (!(s > 0.f) || !(s < INFINITY)) return CODA_ERR_SHAPE;
+  if (R == 0 || C == 0) return CODA_OK;
+  if (!block_scales) return CODA_ERR_NULL;
+  if (!aligned16(block_scales)) return CODA_ERR_ALIGN;
+  DevState* dv;
+  if ((st = ensure_device(&dv)) != CODA_OK) return st;
+  cudaError_t e = launch_quantize_nvfp4_t(X->ptr, R, C, X->ld, mode == CODA_QT_SWIGLU, s, Q->ptr, Q->ld / 2,
+                                          static_cast<uint8_t*>(block_scales), amax,
+                                          static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
+}
+
 int coda_col_reduce(const float* parts, int64_t nblocks, int64_t N, int64_t ld, float* out, void* stream) {
   if (!parts || !out) return CODA_ERR_NULL;
   if (nblocks < 0 || N < 0 || ld < N) return CODA_ERR_SHAPE;
@@ -762,7 +787,8 @@ size_t coda_workspace_size(int32_t which, int64_t M, int64_t H, int64_t F) {
   if (which == CODA_WS_BLOCK_BWD || which == CODA_WS_XENT_BWD)
     return ((size_t)((F + 255) / 256) * (size_t)M + (size_t)((M + 31) / 32) * (size_t)H) * sizeof(float);
   if (which == CODA_WS_XENT_FWD) return (size_t)(2 * ((F + 255) / 256) + 1) * (size_t)M * sizeof(float);
-  if (which == CODA_WS_MLP_FP8_BWD) return (size_t)((F + 255) / 256) * (size_t)M * sizeof(float);
+  if (which == CODA_WS_MLP_FP8_BWD || which == CODA_WS_MLP_NVFP4_BWD)
+    return (size_t)((F + 255) / 256) * (size_t)M * sizeof(float);
   return 0;
 }
 
@@ -1281,6 +1307,106 @@ int coda_mlp_fp8_backward(const coda_mlp_fp8_bwd_io* io, void* stream) {
     coda_side_inputs sd{};
     sd.tensor_scale = io->s_e * io->s_x;
     if ((st = gemm_epilogue_impl(&A, &W, &pg, &sd, &out, nullptr, stream, true)) != CODA_OK) return st;
+  }
+  return CODA_OK;
+}
+
+int coda_mlp_nvfp4_backward(const coda_mlp_nvfp4_bwd_io* io, void* stream) {
+  if (!io) return CODA_ERR_NULL;
+  const int64_t M = io->M, H = io->H, F = io->F;
+  if (M < 0 || M % 256 != 0 || H < 256 || F < 256 || H % 256 != 0 || F % 256 != 0) return CODA_ERR_SHAPE;
+  const float scales[6] = {io->s_x, io->s_wt, io->s_wdt, io->s_a, io->s_dy, io->s_e};
+  for (float v : scales)
+    if (!(v > 0.f) || !(v < INFINITY)) return CODA_ERR_SHAPE;
+  if (!io->W_guT || !io->W_guT_sf || !io->W_dT || !io->W_dT_sf || !io->amax_dy || !io->amax_e || !io->dW_d || !io->dW)
+    return CODA_ERR_NULL;
+  if (M > 0 && (!io->h || !io->Z || !io->r || !io->dY || !io->dY_r || !io->dY_r_sf || !io->dY_c || !io->dY_c_sf ||
+                !io->e || !io->e_r || !io->e_r_sf || !io->e_c || !io->e_c_sf || !io->a_c || !io->a_c_sf ||
+                !io->x_c || !io->x_c_sf || !io->c || !io->dh || !io->workspace))
+    return CODA_ERR_NULL;
+  if (M > 0 && !aligned16(io->workspace)) return CODA_ERR_ALIGN;
+  int st;
+  DevState* dv;
+  if ((st = ensure_device(&dv)) != CODA_OK) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(io->amax_dy, 0, sizeof(float), cs) != cudaSuccess ||
+      cudaMemsetAsync(io->amax_e, 0, sizeof(float), cs) != cudaSuccess)
+    return CODA_ERR_LAUNCH;
+  if (M == 0) {   // sums over an empty batch: zero weight gradients
+    if (cudaMemsetAsync(io->dW_d, 0, (size_t)H * F * sizeof(float), cs) != cudaSuccess ||
+        cudaMemsetAsync(io->dW, 0, (size_t)2 * F * H * sizeof(float), cs) != cudaSuccess)
+      return CODA_ERR_LAUNCH;
+    return CODA_OK;
+  }
+  // dY along its rows (for dA, K = H) and along its columns (for dW_d, K = tokens)
+  coda_tensor dY = mk(io->dY, CODA_BF16, M, H, H);
+  coda_tensor dYr = mk(io->dY_r, CODA_NVFP4, M, H, H), dYc = mk(io->dY_c, CODA_NVFP4, H, M, M);
+  if ((st = coda_quantize_nvfp4(&dY, io->s_dy, &dYr, io->dY_r_sf, io->amax_dy, stream)) != CODA_OK) return st;
+  if ((st = coda_quantize_nvfp4_t(&dY, CODA_QT_PLAIN, io->s_dy, &dYc, io->dY_c_sf, nullptr, stream)) != CODA_OK)
+    return st;
+  float* spart = io->workspace;   // [ceil(F / 256), M] row partials of sum e . Z
+  coda_tensor e = mk(io->e, CODA_BF16, M, 2 * F, 2 * F);
+  coda_tensor Z = mk(io->Z, CODA_BF16, M, 2 * F, 2 * F);
+  {
+    // dA = s_dy s_wdt (dY_r W_dT^T); SwiGLU backward with r; e in bf16, row partials of e . Z
+    coda_tensor W = mk(io->W_dT, CODA_NVFP4, F, H, H);
+    coda_epilogue_program pg = prog_of({CODA_OP_TENSOR_SCALE, CODA_OP_SWIGLU_BWD, CODA_OP_ROW_SCALE,
+                                        CODA_OP_ROW_DOT_PARTIAL});
+    coda_side_inputs sd{};
+    sd.tensor_scale = io->s_dy * io->s_wdt;
+    sd.row_scale = io->r;
+    sd.aux_in = &Z;
+    sd.a_block_scales = io->dY_r_sf;
+    sd.w_block_scales = io->W_dT_sf;
+    coda_aux_outputs ax{};
+    ax.row_partials = spart;
+    ax.row_partials_ld = M;
+    if ((st = gemm_epilogue_impl(&dYr, &W, &pg, &sd, &e, &ax, stream, true)) != CODA_OK) return st;
+  }
+  if ((st = coda_rms_partial_reduce(spart, M, (int32_t)((F + 255) / 256), M, H, 0.f, CODA_REDUCE_SCALE_SUM, io->r,
+                                    io->c, stream)) != CODA_OK)
+    return st;
+  // e along its rows (for t = e W_gu, K = 2F) and along its columns (for dW, K = tokens); a
+  // from the saved Z and h, along their columns (for dW_d and dW)
+  coda_tensor er = mk(io->e_r, CODA_NVFP4, M, 2 * F, 2 * F), ec = mk(io->e_c, CODA_NVFP4, 2 * F, M, M);
+  coda_tensor ac = mk(io->a_c, CODA_NVFP4, F, M, M), xc = mk(io->x_c, CODA_NVFP4, H, M, M);
+  coda_tensor h = mk(io->h, CODA_BF16, M, H, H);
+  if ((st = coda_quantize_nvfp4(&e, io->s_e, &er, io->e_r_sf, io->amax_e, stream)) != CODA_OK) return st;
+  if ((st = coda_quantize_nvfp4_t(&e, CODA_QT_PLAIN, io->s_e, &ec, io->e_c_sf, nullptr, stream)) != CODA_OK) return st;
+  if ((st = coda_quantize_nvfp4_t(&Z, CODA_QT_SWIGLU, io->s_a, &ac, io->a_c_sf, nullptr, stream)) != CODA_OK) return st;
+  if ((st = coda_quantize_nvfp4_t(&h, CODA_QT_PLAIN, io->s_x, &xc, io->x_c_sf, nullptr, stream)) != CODA_OK) return st;
+  {
+    // dW_d = s_dy s_a (dY_c a_c^T), contracting over the tokens
+    coda_tensor out = mk(io->dW_d, CODA_F32, H, F, F);
+    coda_epilogue_program pg = prog_of({CODA_OP_TENSOR_SCALE});
+    coda_side_inputs sd{};
+    sd.tensor_scale = io->s_dy * io->s_a;
+    sd.a_block_scales = io->dY_c_sf;
+    sd.w_block_scales = io->a_c_sf;
+    if ((st = gemm_epilogue_impl(&dYc, &ac, &pg, &sd, &out, nullptr, stream, true)) != CODA_OK) return st;
+  }
+  {
+    // dh = s_e s_wt (e_r W_guT^T) - c h + dY
+    coda_tensor W = mk(io->W_guT, CODA_NVFP4, H, 2 * F, 2 * F), out = mk(io->dh, CODA_BF16, M, H, H);
+    coda_epilogue_program pg = prog_of({CODA_OP_TENSOR_SCALE, CODA_OP_RMSBWD_COMBINE});
+    coda_side_inputs sd{};
+    sd.tensor_scale = io->s_e * io->s_wt;
+    sd.row_coef = io->c;
+    sd.aux_in = &h;
+    sd.aux_in2 = &dY;
+    sd.a_block_scales = io->e_r_sf;
+    sd.w_block_scales = io->W_guT_sf;
+    if ((st = gemm_epilogue_impl(&er, &W, &pg, &sd, &out, nullptr, stream, true)) != CODA_OK) return st;
+  }
+  {
+    // dW = s_e s_x (e_c x_c^T), contracting over the tokens
+    coda_tensor out = mk(io->dW, CODA_F32, 2 * F, H, H);
+    coda_epilogue_program pg = prog_of({CODA_OP_TENSOR_SCALE});
+    coda_side_inputs sd{};
+    sd.tensor_scale = io->s_e * io->s_x;
+    sd.a_block_scales = io->e_c_sf;
+    sd.w_block_scales = io->x_c_sf;
+    if ((st = gemm_epilogue_impl(&ec, &xc, &pg, &sd, &out, nullptr, stream, true)) != CODA_OK) return st;
   }
   return CODA_OK;
 }

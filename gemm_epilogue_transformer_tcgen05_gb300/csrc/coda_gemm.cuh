@@ -148,6 +148,11 @@ struct GemmParams {
   unsigned long long timeout_ns;
 };
 
+// Pipeline stages that fit in `free_bytes` of shared memory, at most `max_stages`.
+__host__ __device__ constexpr int fit_stages(int free_bytes, int stage_bytes, int max_stages) {
+  return free_bytes / stage_bytes > max_stages ? max_stages : free_bytes / stage_bytes;
+}
+
 // CG = CTAs per MMA: 1, or 2 for a CTA pair (cluster of two) issuing cta_group::2 MMAs of
 // 256 x 256: each CTA holds 128 rows of A and 128 rows (N) of B per stage and receives its
 // 128 accumulator rows in its own TMEM.
@@ -190,21 +195,47 @@ struct GemmCfg {
   static constexpr bool PAIR_OUT = EPI == EPI_SWIGLU_BWD;
   static constexpr bool PAIR_AUX = EPI == EPI_SWIGLU && AUX;
   // side inputs are prefetched NSS chunks ahead (one staging set per chunk in flight); the
-  // SwiGLU backward, with two side inputs and two outputs per chunk, goes deeper
-  static constexpr int NSS = EPI == EPI_SWIGLU_BWD ? 4 : 2;
+  // SwiGLU backward, with two side inputs and two outputs per chunk, goes deeper, except with
+  // NVFP4 operands, whose larger stages leave the shared memory for two
+  static constexpr int NSS = (EPI == EPI_SWIGLU_BWD && KIND != KIND_NVFP4) ? 4 : 2;
   static_assert(NCHUNK % NSS == 0, "a chunk and the next tile's chunk NCHUNK later share a ring slot");
-  static constexpr int EPI_WARP_BYTES = NSS * NS * SSLOT + 2 * OUTSET;
   // NVFP4: four scale warps write the block scales into TMEM (see the kernel)
   static constexpr int SF_WARPS = FP4 ? 4 : 0;
   // NVFP4 SwiGLU with NVFP4 output: the scale warps also form half of each tile's output
   static constexpr bool EARLY = FP4 && DUAL && OUT_DT == DT_E2M1;
   static constexpr int OUT_WARPS = NUM_EPI_WARPS + (EARLY ? SF_WARPS : 0);   // warps storing output
-  static constexpr int EPI_BYTES = OUT_WARPS * EPI_WARP_BYTES;
   static constexpr int THREADS = NUM_THREADS + 32 * SF_WARPS;
   static constexpr int BAR_BYTES = FP4 ? 384 : 320;   // barriers, then 12 bytes of flags (see the kernel)
-  static constexpr int STAGES_FIT = (MAX_SMEM - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
   static constexpr int MAX_STAGES = FP4 ? 8 : 6;
-  static constexpr int STAGES = STAGES_FIT > MAX_STAGES ? MAX_STAGES : STAGES_FIT;
+  // Wide stores: OW chunks of 32 columns leave in one TMA store (a staging row of up to 128
+  // bytes), so that a warp issues fewer bulk-tensor operations per tile; the number of small
+  // TMA operations, not their bytes, is what competes with the mainloop's loads.  OSETS
+  // staging sets of OW chunks are double-buffered when the shared memory allows it without
+  // costing a pipeline stage, else one set is reused once its previous store has been read.
+  static constexpr int OW_MAX = (OUT_DT == DT_E2M1 || NO == 0 || OUT_DT == DT_F32)
+                                    ? 1
+                                    : (NX > 0 ? 2 : 128 / (32 * dt_bytes(OUT_DT)));
+  static constexpr int SIDE_BYTES = NSS * NS * SSLOT;
+  static constexpr int SMEM_FREE = MAX_SMEM - 1024 - BAR_BYTES;   // for the stages and the epilogue
+  static constexpr int S_NARROW =
+      fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + 2 * OUTSET), STAGE_BYTES, MAX_STAGES);   // one chunk per store
+  static constexpr int OW =
+      (OW_MAX > 1 && NCHUNK % OW_MAX == 0 &&
+       fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + OW_MAX * OUTSET), STAGE_BYTES, MAX_STAGES) >= S_NARROW)
+          ? OW_MAX
+          : (OW_MAX > 1 && NCHUNK % 2 == 0 ? 2 : 1);
+  static constexpr int OSETS =
+      (OW == 1 ||
+       fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + 2 * OW * OUTSET), STAGE_BYTES, MAX_STAGES) >= S_NARROW)
+          ? 2
+          : 1;
+  static constexpr int OUTSET_W = OW * OUTSET;               // one staging set: OW chunks of each output
+  static constexpr int RB_OUT = OW * 32 * dt_bytes(OUT_DT);  // staging row bytes of the main output
+  static constexpr int RB_X = OW * 64;                       // ... of the bf16 aux output
+  static_assert(OW == 1 || (RB_OUT <= 128 && (NX == 0 || RB_X <= 128) && NCHUNK % OW == 0), "wide store rows");
+  static constexpr int EPI_WARP_BYTES = SIDE_BYTES + OSETS * OUTSET_W;
+  static constexpr int EPI_BYTES = OUT_WARPS * EPI_WARP_BYTES;
+  static constexpr int STAGES = fit_stages(SMEM_FREE - EPI_BYTES, STAGE_BYTES, MAX_STAGES);
   // TMEM: two accumulators of UN columns, then (NVFP4) each stage's block scales, 4 columns
   // per atom
   static constexpr int SF_COLS = (SF_A_BYTES + SF_B_BYTES) / 128;
@@ -300,11 +331,16 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // chunk j of row i sits at chunk j ^ ((i * RB / 128) & (RB / 16 - 1)), which is the TMA
 // 32/64/128-byte swizzle for that row width.  Thread i touches row i only; the XOR spreads
 // 8 consecutive rows over all 32 banks.
+// The same for staging rows of RB bytes (32 <= RB <= 128, a wide store's block): 16-byte unit
+// u of row i sits at u ^ ((i * RB / 128) & (RB / 16 - 1)).
+template <int RB>
+__device__ __forceinline__ uint32_t swz_rb(uint32_t slot, int row, int u) {
+  constexpr int MASK = RB / 16 - 1;
+  return slot + row * RB + ((u ^ ((row * RB >> 7) & MASK)) << 4);
+}
 template <int DT>
 __device__ __forceinline__ uint32_t swz(uint32_t slot, int row, int j) {
-  constexpr int RB = 32 * dt_bytes(DT);
-  constexpr int MASK = RB / 16 - 1;
-  return slot + row * RB + ((j ^ ((row * RB >> 7) & MASK)) << 4);
+  return swz_rb<32 * dt_bytes(DT)>(slot, row, j);
 }
 
 template <int DT>
@@ -338,17 +374,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 __device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
-template <int DT>
-__device__ __forceinline__ void slot_write(uint32_t slot, int row, const float (&x)[32]) {
+// Writes the 32 values of a chunk into row `row` of a staging block whose rows are RB bytes,
+// starting at 16-byte unit u0 of the row (a wide block holds several chunks side by side).
+template <int DT, int RB = 32 * dt_bytes(DT)>
+__device__ __forceinline__ void slot_write(uint32_t slot, int row, const float (&x)[32], int u0 = 0) {
   if constexpr (DT == DT_BF16) {
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      ptx::st_shared_v4(swz<DT>(slot, row, j), pack_bf16(x[8 * j], x[8 * j + 1]), pack_bf16(x[8 * j + 2], x[8 * j + 3]),
-                        pack_bf16(x[8 * j + 4], x[8 * j + 5]), pack_bf16(x[8 * j + 6], x[8 * j + 7]));
+      ptx::st_shared_v4(swz_rb<RB>(slot, row, u0 + j), pack_bf16(x[8 * j], x[8 * j + 1]),
+                        pack_bf16(x[8 * j + 2], x[8 * j + 3]), pack_bf16(x[8 * j + 4], x[8 * j + 5]),
+                        pack_bf16(x[8 * j + 6], x[8 * j + 7]));
   } else if constexpr (DT == DT_F32) {
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      ptx::st_shared_v4(swz<DT>(slot, row, j), __float_as_uint(x[4 * j]), __float_as_uint(x[4 * j + 1]),
+      ptx::st_shared_v4(swz_rb<RB>(slot, row, u0 + j), __float_as_uint(x[4 * j]), __float_as_uint(x[4 * j + 1]),
                         __float_as_uint(x[4 * j + 2]), __float_as_uint(x[4 * j + 3]));
   } else {
 #pragma unroll
@@ -359,19 +398,21 @@ __device__ __forceinline__ void slot_write(uint32_t slot, int row, const float (
         const int e = 16 * j + 4 * k;
         w[k] = (uint32_t)ptx::cvt_e4m3x2(x[e], x[e + 1]) | ((uint32_t)ptx::cvt_e4m3x2(x[e + 2], x[e + 3]) << 16);
       }
-      ptx::st_shared_v4(swz<DT>(slot, row, j), w[0], w[1], w[2], w[3]);
+      ptx::st_shared_v4(swz_rb<RB>(slot, row, u0 + j), w[0], w[1], w[2], w[3]);
     }
   }
 }
 
-// An e4m3 staging block from codes already packed in pairs (q[i] holds elements 2i, 2i+1).
-__device__ __forceinline__ void slot_write_codes(uint32_t slot, int row, const uint16_t (&q)[16]) {
+// An e4m3 chunk from codes already packed in pairs (q[i] holds elements 2i, 2i+1), into a
+// staging block with rows of RB bytes from unit u0 on.
+template <int RB = 32>
+__device__ __forceinline__ void slot_write_codes(uint32_t slot, int row, const uint16_t (&q)[16], int u0 = 0) {
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     uint32_t w[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) w[k] = (uint32_t)q[8 * j + 2 * k] | ((uint32_t)q[8 * j + 2 * k + 1] << 16);
-    ptx::st_shared_v4(swz<DT_E4M3>(slot, row, j), w[0], w[1], w[2], w[3]);
+    ptx::st_shared_v4(swz_rb<RB>(slot, row, u0 + j), w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -1086,47 +1127,52 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
 
         // ---------------------------------------------------------------- stage + store
+        // OW chunks form one store group: their blocks sit side by side in wide staging rows
+        // and leave in one TMA store per output after the group's last chunk.
         if constexpr (C::NO == 0) continue;
-        const bool store = col0 < p.N && r0 < p.M;
-        const uint32_t oslot = out_base + (c & 1) * C::OUTSET;
-        if (lane == 0) ptx::bulk_wait_read<1>();  // the group that last used this set is done reading
-        __syncwarp();
-        if constexpr (FP4_OUT) {
-          ptx::st_shared_v4(oslot + 16 * lane, q4[0], q4[1], q4[2], q4[3]);   // 32 rows of 16 bytes
-        } else if constexpr (CODES) {
-          slot_write_codes(oslot, lane, qg);
-          slot_write_codes(oslot + C::OSLOT, lane, qu);
-        } else {
-          slot_write<C::OUT_DT>(oslot, lane, x);
-          if constexpr (C::NO > 1) slot_write<C::OUT_DT>(oslot + C::OSLOT, lane, o1);
+        constexpr int OW = C::OW;
+        constexpr int OBLK = OW * C::OSLOT;             // one output block of a staging set
+        constexpr int XBLK = OW * C::XSLOT;             // one aux block
+        constexpr int UO = 2 * dt_bytes(C::OUT_DT);     // 16-byte units of a chunk's output row
+        const int h = c % OW;                           // the chunk's place in its group
+        const uint32_t oset = out_base + ((c / OW) % C::OSETS) * C::OUTSET_W;
+        if (h == 0) {
+          if (lane == 0) ptx::bulk_wait_read<C::OSETS - 1>();  // the group that last used this set is read
+          __syncwarp();
         }
-        if constexpr (C::NX > 0) slot_write<DT_BF16>(oslot + C::NO * C::OSLOT, lane, zg);
-        if constexpr (C::NX > 1) slot_write<DT_BF16>(oslot + C::NO * C::OSLOT + C::XSLOT, lane, zu);
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (store) {
-            if constexpr (C::PAIR_OUT) {
-              ptx::tma_store_3d_hint(&tmOut, col0, r0, 0, oslot, stream_pol);   // e's gate and up blocks
-            } else {
-              if (C::EPI == EPI_STORE && C::OUT_DT == DT_F32 && p.k_splits > 1)
-                ptx::tma_reduce_add_2d_hint(&tmOut, col0, r0, oslot, stream_pol);   // split-K partial
-              else
-                ptx::tma_store_2d_hint(&tmOut, FP4_OUT ? col0 / 2 : col0, r0, oslot, stream_pol);
-              if constexpr (C::EPI == EPI_SWIGLU_BWD)
-                ptx::tma_store_2d_hint(&tmOut, p.up_offset + col0, r0, oslot + C::OSLOT, stream_pol);
+        if constexpr (FP4_OUT) {
+          ptx::st_shared_v4(oset + 16 * lane, q4[0], q4[1], q4[2], q4[3]);   // 32 rows of 16 bytes (OW = 1)
+        } else if constexpr (CODES) {
+          slot_write_codes<C::RB_OUT>(oset, lane, qg, h * UO);
+          slot_write_codes<C::RB_OUT>(oset + OBLK, lane, qu, h * UO);
+        } else {
+          slot_write<C::OUT_DT, C::RB_OUT>(oset, lane, x, h * UO);
+          if constexpr (C::NO > 1) slot_write<C::OUT_DT, C::RB_OUT>(oset + OBLK, lane, o1, h * UO);
+        }
+        if constexpr (C::NX > 0) slot_write<DT_BF16, C::RB_X>(oset + C::NO * OBLK, lane, zg, h * 4);
+        if constexpr (C::NX > 1) slot_write<DT_BF16, C::RB_X>(oset + C::NO * OBLK + XBLK, lane, zu, h * 4);
+        if (h == OW - 1) {
+          const int gcol = col0 - 32 * (OW - 1);        // first column of the group
+          const bool store = gcol < p.N && r0 < p.M;
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (store) {
+              if constexpr (C::PAIR_OUT) {
+                ptx::tma_store_3d_hint(&tmOut, gcol, r0, 0, oset, stream_pol);   // e's gate and up blocks
+              } else if (C::EPI == EPI_STORE && C::OUT_DT == DT_F32 && p.k_splits > 1) {
+                ptx::tma_reduce_add_2d_hint(&tmOut, gcol, r0, oset, stream_pol);   // split-K partial
+              } else {
+                ptx::tma_store_2d_hint(&tmOut, FP4_OUT ? gcol / 2 : gcol, r0, oset, stream_pol);
+              }
+              if constexpr (C::PAIR_AUX) {
+                ptx::tma_store_3d_hint(&tmAux, gcol, r0, 0, oset + C::NO * OBLK, stream_pol);   // Z's G and U
+              } else if constexpr (C::NX > 0) {
+                ptx::tma_store_2d_hint(&tmAux, gcol, r0, oset + C::NO * OBLK, stream_pol);
+              }
             }
-            if constexpr (C::PAIR_AUX) {
-              ptx::tma_store_3d_hint(&tmAux, col0, r0, 0, oslot + C::NO * C::OSLOT, stream_pol);   // Z's G and U
-            } else {
-              if constexpr (C::NX > 0)
-                ptx::tma_store_2d_hint(&tmAux, col0, r0, oslot + C::NO * C::OSLOT, stream_pol);
-              if constexpr (C::NX > 1)
-                ptx::tma_store_2d_hint(&tmAux, p.up_offset + col0, r0, oslot + C::NO * C::OSLOT + C::XSLOT,
-                                       stream_pol);
-            }
+            ptx::bulk_commit();
           }
-          ptx::bulk_commit();
         }
       }
       if (!ok) break;

@@ -24,6 +24,7 @@ struct VariantEntry {
   int bn_out;      // output columns per tile
   int b_box;       // B rows per TMA copy
   int bk;          // K elements per pipeline stage
+  int ow;          // chunks of 32 output columns per TMA store (box width of the output maps)
 };
 
 // Tables defined by the instantiation units.
@@ -65,6 +66,8 @@ cudaError_t launch_quantize_e4m3(const void* X, int64_t M, int64_t N, int64_t ld
                                  int64_t ldq, float* amax, cudaStream_t s, int sms);
 cudaError_t launch_quantize_nvfp4(const void* X, int64_t R, int64_t K, int64_t ldx, float s, void* Q, int64_t ldq_bytes,
                                   uint8_t* sf, float* amax, cudaStream_t st, int sms);
+cudaError_t launch_quantize_nvfp4_t(const void* X, int64_t R, int64_t C, int64_t ldx, bool swiglu, float s, void* Q,
+                                    int64_t ldq_bytes, uint8_t* sf, float* amax, cudaStream_t st);
 cudaError_t launch_xent_reduce(const float* Pm, const float* Ps, int64_t ld, int nparts, int64_t M, const float* T,
                                const int* targets, int64_t V, float* lse, float* loss, float* mean, cudaStream_t s);
 
@@ -73,7 +76,7 @@ cudaError_t launch_xent_reduce(const float* Pm, const float* Ps, int64_t ld, int
 namespace coda {
 template <class C>
 constexpr VariantEntry make_variant(VariantKey k) {
-  return {k, &launch_gemm<C>, C::SMEM_BYTES, C::STAGES, C::CG, C::UN, C::BN_OUT, C::B_BOX, C::BK};
+  return {k, &launch_gemm<C>, C::SMEM_BYTES, C::STAGES, C::CG, C::UN, C::BN_OUT, C::B_BOX, C::BK, C::OW};
 }
 }  // namespace coda
 #define CODA_VARIANT(KIND, EPI, AMN, BMN, OUT, SIDE, AUX) \

@@ -525,6 +525,88 @@ cudaError_t launch_quantize_nvfp4(const void* X, int64_t R, int64_t K, int64_t l
   return cudaGetLastError();
 }
 
+// Transposed NVFP4 quantiser: X [R, C] bf16 is quantised along its columns, into Q = X^T
+// ([C, R] codes, blocks of 16 consecutive rows of X), the operand layout of a GEMM that
+// contracts over R (a weight gradient contracts over the tokens).  With `swiglu`, X is the
+// saved [G | U] ([R, 2C]) and the quantised value is silu(G) U.  A CTA stages a tile of 64 rows
+// x 64 columns in shared memory with 16-byte coalesced loads; thread (column c, row block b)
+// then quantises rows 16 b .. 16 b + 15 of column c: 8 bytes of codes (32 bytes per column
+// and tile, contiguous) and one block-scale byte.
+constexpr int QT_ROWS = 64, QT_COLS = 64;
+__global__ void __launch_bounds__(256) quantize_nvfp4_t_kernel(const __nv_bfloat16* __restrict__ X, int64_t R,
+                                                               int64_t C, int64_t ldx, int swiglu, float s,
+                                                               uint8_t* __restrict__ Q, int64_t ldq,
+                                                               uint8_t* __restrict__ sf,
+                                                               unsigned int* __restrict__ amax) {
+  __shared__ float tile[QT_ROWS][QT_COLS + 1];
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+  const int64_t col_tiles = (C + QT_COLS - 1) / QT_COLS;
+  const int64_t r0 = (int64_t)(blockIdx.x / col_tiles) * QT_ROWS;
+  const int64_t c0 = (int64_t)(blockIdx.x % col_tiles) * QT_COLS;
+  const int t = threadIdx.x;
+  // load: 64 rows x 8 units of 8 bf16 (16 bytes); thread t takes row t / 8 (+ 32), unit t % 8
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int row = t / 8 + 32 * pass, u = t % 8;
+    const int64_t gr = r0 + row, gc = c0 + 8 * u;
+    float v[8];
+    if (gr < R && gc < C) {   // C is a multiple of 8, so a unit is in range or not at all
+      const uint4 a = __ldcs(reinterpret_cast<const uint4*>(X + gr * ldx + gc));
+      const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        v[2 * k] = __uint_as_float(w[k] << 16);
+        v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+      }
+      if (swiglu) {
+        const uint4 b = __ldcs(reinterpret_cast<const uint4*>(X + gr * ldx + C + gc));
+        const uint32_t wu[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          v[2 * k] = silu_f(v[2 * k]) * __uint_as_float(wu[k] << 16);
+          v[2 * k + 1] = silu_f(v[2 * k + 1]) * __uint_as_float(wu[k] & 0xFFFF0000u);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tile[row][8 * u + k] = v[k];
+  }
+  __syncthreads();
+  // quantise: thread t -> column t / 4, row block t % 4
+  const int c = t / 4, b = t % 4;
+  const int64_t gc = c0 + c;
+  float x[16], m = 0.f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    x[k] = tile[16 * b + k][c];
+    m = fmaxf(m, fabsf(x[k]));
+  }
+  if (gc < C && r0 + 16 * b < R) {
+    uint32_t q[2];
+    const uint32_t code = nvfp4_block16(x, s, q);
+    *reinterpret_cast<uint2*>(Q + gc * ldq + (r0 + 16 * b) / 2) = make_uint2(q[0], q[1]);
+    sf[sf_offset(gc, (r0 + 16 * b) / 16, R / 64)] = (uint8_t)code;
+  }
+  if (amax) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((t & 31) == 0 && m > 0.f) atomicMax(amax, __float_as_uint(m));
+  }
+}
+
+cudaError_t launch_quantize_nvfp4_t(const void* X, int64_t R, int64_t C, int64_t ldx, bool swiglu, float s, void* Q,
+                                    int64_t ldq_bytes, uint8_t* sf, float* amax, cudaStream_t st) {
+  const int64_t tiles = ((R + QT_ROWS - 1) / QT_ROWS) * ((C + QT_COLS - 1) / QT_COLS);
+  if (tiles <= 0) return cudaSuccess;
+  launch_k(quantize_nvfp4_t_kernel, (unsigned)tiles, 256, st, reinterpret_cast<const __nv_bfloat16*>(X), R, C, ldx,
+           swiglu ? 1 : 0, s, reinterpret_cast<uint8_t*>(Q), ldq_bytes, sf, reinterpret_cast<unsigned int*>(amax));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_rope_table(int seq_len, int head_dim, double base, float* cos_out, float* sin_out,
                               cudaStream_t s) {
   const int half = head_dim / 2;

@@ -492,6 +492,21 @@ CODA_API int coda_quantize_e4m3(const coda_tensor* X, float scale, const coda_te
 CODA_API int coda_quantize_nvfp4(const coda_tensor* X, float s, const coda_tensor* Q, void* block_scales,
                                  float* amax, void* stream);
 
+/* [KuCoin, "El «impuesto a la pereza»…" (FP4 operands) and "El epílogo esconde un tesoro" (the
+ * backward inherits the structure: a weight gradient contracts over the tokens)]
+ * Transposed NVFP4 quantisation: X (bf16 ROW_MAJOR [R, C]) quantised along its columns into
+ * Q = X^T (CODA_NVFP4 [C, R]): for each column c and each block of 16 consecutive rows,
+ *   sf = e4m3(amax_block / (6 s)),  Q[c, r] = e2m1(X[r, c] / (sf s))   (fp32 decisions, as at
+ * coda_quantize_nvfp4), block scales in the layout described there for the tensor [C, R].  It
+ * is the K-major operand of a GEMM that contracts over R, as the block-scaled tensor cores
+ * need.  mode CODA_QT_SWIGLU: X is a saved [G | U] ([R, 2C]) and the value quantised is
+ * silu(G) U, formed in fp32.  R must be a multiple of 64 and C of 128 (CODA_ERR_SHAPE);
+ * amax (optional, zeroed by the caller) receives the atomic max of the quantised values' |x|.
+ * A bandwidth-bound pass: 2 (or 4) bytes read and 9 / 16 written per element. */
+enum coda_qt_mode { CODA_QT_PLAIN = 0, CODA_QT_SWIGLU = 1 };
+CODA_API int coda_quantize_nvfp4_t(const coda_tensor* X, int32_t mode, float s, const coda_tensor* Q,
+                                   void* block_scales, float* amax, void* stream);
+
 /* Bytes of the block scales of an NVFP4 tensor [R, K]: ceil(R / 128) * (K / 64) * 512 (the
  * layout at coda_quantize_nvfp4; no counterpart on the pages).  Needs no device. */
 CODA_API size_t coda_nvfp4_scale_bytes(int64_t R, int64_t K);
@@ -522,6 +537,61 @@ typedef struct coda_mlp_nvfp4_io {
   float* Y_partials;         /* out [H/256, M] fp32 */
 } coda_mlp_nvfp4_io;
 CODA_API int coda_mlp_nvfp4(const coda_mlp_nvfp4_io* io, void* stream);
+
+/* [KuCoin, "El epílogo esconde un tesoro" (the backward inherits the structure) and "El
+ * «impuesto a la pereza»…" (FP4 operands for the matmul)]
+ * Backward of the NVFP4 MLP for an output gradient dY, every GEMM on NVFP4 operands.  The
+ * block-scaled tensor cores take both operands blocked along the GEMM's K, so each operand is
+ * quantised along the K of the GEMM that reads it:
+ *   dY_r = nvfp4 of dY along its rows, dY_c along its columns (tensor scale s_dy)
+ *   dA = s_dy s_wdt (dY_r W_dT^T);  e = r [dA U silu'(G) | dA silu(G)] (bf16, from the saved Z)
+ *   s_i = sum_k e_ik Z_ik;  c = r s / H
+ *   e_r, e_c = e along its rows / columns (s_e);  a_c = silu(G) U along its columns (s_a);
+ *   x_c = h along its columns (s_x)
+ *   dh = s_e s_wt (e_r W_guT^T) - c h + dY
+ *   dW_d = s_dy s_a (dY_c a_c^T)  [H, F];  dW = s_e s_x (e_c x_c^T)  [2F, H]   (fp32)
+ * W_guT ([H, 2F]) and W_dT ([F, H]) are the gate/up and down weights quantised transposed,
+ * along 2F and H (coda_quantize_nvfp4_t of W_gu and W_d; once per weight update), with tensor
+ * scales s_wt and s_wdt.  s_dy and s_e are the caller's delayed scales (e.g. amax_dy / 2688
+ * and amax_e / 2688 of an earlier step), s_a the forward's, s_x that of h.  The caller owns
+ * every intermediate; the NVFP4 ones are (codes, block scales) pairs of the sizes given by
+ * their shapes (coda_nvfp4_scale_bytes).  M must be a multiple of 256 (the weight gradients
+ * contract over the tokens), H and F multiples of 256: CODA_ERR_SHAPE otherwise.  Eleven
+ * launches: two quantisations of dY, the dA GEMM with the SwiGLU-backward epilogue, the row
+ * reduce, four quantisations, the dW_d, dh and dW GEMMs. */
+typedef struct coda_mlp_nvfp4_bwd_io {
+  int64_t M, H, F;
+  float s_x, s_wt, s_wdt, s_a, s_dy, s_e;
+  const void* h;             /* [M, H] bf16 */
+  const void* W_guT;         /* NVFP4 [H, 2F] codes */
+  const void* W_guT_sf;      /* its block scales */
+  const void* W_dT;          /* NVFP4 [F, H] codes */
+  const void* W_dT_sf;
+  const void* Z;             /* [M, 2F] bf16: saved [G | U] */
+  const float* r;            /* [M] */
+  const void* dY;            /* [M, H] bf16 */
+  void* dY_r;                /* out NVFP4 [M, H] codes, and scales */
+  void* dY_r_sf;
+  void* dY_c;                /* out NVFP4 [H, M] */
+  void* dY_c_sf;
+  void* e;                   /* out [M, 2F] bf16 */
+  void* e_r;                 /* out NVFP4 [M, 2F] */
+  void* e_r_sf;
+  void* e_c;                 /* out NVFP4 [2F, M] */
+  void* e_c_sf;
+  void* a_c;                 /* out NVFP4 [F, M] */
+  void* a_c_sf;
+  void* x_c;                 /* out NVFP4 [H, M] */
+  void* x_c_sf;
+  float* amax_dy;            /* out: max |dY| (zeroed by this call on the stream) */
+  float* amax_e;             /* out: max |e| (likewise) */
+  float* c;                  /* out [M] */
+  void* dh;                  /* out [M, H] bf16 */
+  float* dW_d;               /* out [H, F] fp32 */
+  float* dW;                 /* out [2F, H] fp32 */
+  float* workspace;          /* coda_workspace_size(CODA_WS_MLP_NVFP4_BWD, M, H, F) bytes */
+} coda_mlp_nvfp4_bwd_io;
+CODA_API int coda_mlp_nvfp4_backward(const coda_mlp_nvfp4_bwd_io* io, void* stream);
 
 /* ------------------------------------------------------------ LM head + cross-entropy
  * Final RMSNorm, LM head and mean cross-entropy, with the logits never stored
@@ -578,7 +648,8 @@ enum coda_workspace_kind {
   CODA_WS_BLOCK_BWD = 1,
   CODA_WS_XENT_FWD = 2,
   CODA_WS_XENT_BWD = 3,
-  CODA_WS_MLP_FP8_BWD = 4
+  CODA_WS_MLP_FP8_BWD = 4,
+  CODA_WS_MLP_NVFP4_BWD = 5
 };
 CODA_API size_t coda_workspace_size(int32_t which, int64_t M, int64_t H, int64_t F);
 

@@ -66,3 +66,32 @@ def assert_product_close(got, ref, sim, what, factor=1.5):
     bound = max(TOL_BF16, factor * el_sim)
     assert el <= bound, f"{what}: element-wise err {el:.3e} > {bound:.3e} (bf16-storage model {el_sim:.3e})"
     return el, el_sim
+
+
+def nvfp4_window(got_q, got_sf, x, s, rel):
+    """NVFP4 codes and block scales are rounding decisions the GPU takes in fp32; the oracle
+    takes them in float64 on the plain definition.  Each block scale must lie between the e4m3
+    roundings of amax / (6 s) moved by `rel` either way, and each code between the e2m1
+    roundings of x / (sf s) moved by `rel` either way, sf being the GPU's own block scale (so a
+    block whose scale rounded the other way is still checked, against that scale).  Where that
+    window holds a single value (the value is not within `rel` of a rounding midpoint) the
+    GPU's decision must therefore equal the oracle's; only the ambiguous ones may differ.
+    Returns the fractions of block scales and of codes equal to the oracle's rounding, and the
+    fraction of codes whose window is ambiguous."""
+    R, K = x.shape
+    q, sf = O.nvfp4_quantize(x, s)
+    amax_b = np.max(np.abs(x).reshape(R, K // 16, 16), axis=2)
+    u = amax_b / (6.0 * s)
+    lo, hi = O.e4m3_round(u * (1 - rel)), O.e4m3_round(u * (1 + rel))
+    bad_sf = ~((got_sf >= lo) & (got_sf <= hi))
+    assert not bad_sf.any(), f"{int(bad_sf.sum())} block scales outside the rounding window"
+    d = s * np.repeat(got_sf, 16, axis=1)
+    y = np.where(d > 0, x / np.where(d > 0, d, 1.0), 0.0)
+    slack = rel * np.abs(y)
+    qlo, qhi = O.e2m1_round(y - slack), O.e2m1_round(y + slack)
+    bad_q = ~((got_q >= qlo) & (got_q <= qhi))
+    assert not bad_q.any(), f"{int(bad_q.sum())} codes outside the rounding window"
+    same_scale = np.repeat(got_sf == sf, 16, axis=1)
+    clear = (qlo == qhi) & same_scale
+    assert np.all((got_q == q)[clear]), "a code away from every rounding midpoint differs from the oracle's"
+    return float(np.mean(got_sf == sf)), float(np.mean(got_q == q)), float(np.mean(qlo != qhi))

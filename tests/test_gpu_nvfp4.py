@@ -17,7 +17,7 @@ import torch
 
 import oracle as O
 from tests import nvfp4_layout as L
-from tests.gpu_helpers import TOL_BF16, TOL_FP8, assert_close, dev, f64, fresh_status
+from tests.gpu_helpers import TOL_BF16, TOL_FP8, assert_close, dev, f64, fresh_status, nvfp4_window
 
 pytestmark = pytest.mark.gpu
 BF = torch.bfloat16
@@ -42,35 +42,6 @@ def _scale_of(x):
 
 
 # ------------------------------------------------------------------------- quantiser
-def _nvfp4_window(got_q, got_sf, x, s, rel):
-    """NVFP4 codes and block scales are rounding decisions the GPU takes in fp32; the oracle
-    takes them in float64 on the plain definition.  Each block scale must lie between the e4m3
-    roundings of amax / (6 s) moved by `rel` either way, and each code between the e2m1
-    roundings of x / (sf s) moved by `rel` either way, sf being the GPU's own block scale (so a
-    block whose scale rounded the other way is still checked, against that scale).  Where that
-    window holds a single value (the value is not within `rel` of a rounding midpoint) the
-    GPU's decision must therefore equal the oracle's; only the ambiguous ones may differ.
-    Returns the fractions of block scales and of codes equal to the oracle's rounding, and the
-    fraction of codes whose window is ambiguous."""
-    R, K = x.shape
-    q, sf = O.nvfp4_quantize(x, s)
-    amax_b = np.max(np.abs(x).reshape(R, K // 16, 16), axis=2)
-    u = amax_b / (6.0 * s)
-    lo, hi = O.e4m3_round(u * (1 - rel)), O.e4m3_round(u * (1 + rel))
-    bad_sf = ~((got_sf >= lo) & (got_sf <= hi))
-    assert not bad_sf.any(), f"{int(bad_sf.sum())} block scales outside the rounding window"
-    d = s * np.repeat(got_sf, 16, axis=1)
-    y = np.where(d > 0, x / np.where(d > 0, d, 1.0), 0.0)
-    slack = rel * np.abs(y)
-    qlo, qhi = O.e2m1_round(y - slack), O.e2m1_round(y + slack)
-    bad_q = ~((got_q >= qlo) & (got_q <= qhi))
-    assert not bad_q.any(), f"{int(bad_q.sum())} codes outside the rounding window"
-    same_scale = np.repeat(got_sf == sf, 16, axis=1)
-    clear = (qlo == qhi) & same_scale
-    assert np.all((got_q == q)[clear]), "a code away from every rounding midpoint differs from the oracle's"
-    return float(np.mean(got_sf == sf)), float(np.mean(got_q == q)), float(np.mean(qlo != qhi))
-
-
 # an fp32 quotient, product and reciprocal each round once (2^-24 relative): 1e-6 covers
 # the quantiser's few roundings with room to spare
 QUANT_REL = 1e-6
@@ -92,7 +63,7 @@ def test_quantize_nvfp4_codes_in_rounding_window(C, R, K):
     got_q = O.e2m1_decode(L.unpack_codes(Q.codes.cpu().numpy()))
     buf = Q.scales.cpu().numpy()
     got_sf = O.e4m3_decode(L.from_atoms(buf, R, K))
-    same_sf, same_q, ambiguous = _nvfp4_window(got_q, got_sf, x, s, QUANT_REL)
+    same_sf, same_q, ambiguous = nvfp4_window(got_q, got_sf, x, s, QUANT_REL)
     print(f"nvfp4 quantiser {R}x{K}: block scales equal to the oracle's {same_sf:.6f}, codes {same_q:.6f} "
           f"(within fp32 reach of a midpoint: {ambiguous:.6f})")
     # bf16 values over e4m3 block scales often land on an e2m1 midpoint up to the rounding of
@@ -183,7 +154,7 @@ def _check_nvfp4_output(out, a, s_a, M, F, rel=1e-4):
     rounding, and the dequantised tensor must be within half an e2m1 step of a."""
     got_q = O.e2m1_decode(L.unpack_codes(out.codes.cpu().numpy()))
     got_sf = O.e4m3_decode(L.from_atoms(out.scales.cpu().numpy(), M, F))
-    same_sf, same_q, ambiguous = _nvfp4_window(got_q, got_sf, a, s_a, rel)
+    same_sf, same_q, ambiguous = nvfp4_window(got_q, got_sf, a, s_a, rel)
     print(f"nvfp4 output {M}x{F}: block scales equal to the oracle's {same_sf:.6f}, codes {same_q:.6f} "
           f"(within {rel:g} of a midpoint: {ambiguous:.6f})")
     assert same_sf >= 0.999 and same_q >= 0.999 and ambiguous <= 0.01

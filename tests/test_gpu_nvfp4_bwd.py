@@ -1,0 +1,226 @@
+"""GPU parity of the NVFP4 MLP backward against the fp64 oracle, through the C ABI (oracle
+reading 10: every backward GEMM takes its two operands quantised along its own K):
+
+* the transposed quantiser (a tensor quantised along its columns, and silu(G) U of a saved
+  [G | U] quantised the same way): codes and block scales within the rounding window of the
+  oracle's plain definition;
+* the block-scaled SwiGLU-backward and RMSNorm-backward GEMMs on operands the oracle
+  quantised;
+* the whole backward chain, small (every element) and at the LLaMA-3-8B MLP shape (16384
+  tokens, sampled rows and columns, with the chain's own stored tensors as exact inputs).
+
+Source: [KuCoin] "CODA: new research optimizes Transformer training with GEMM-epilogue
+programming", sections "El epílogo esconde un tesoro" (the backward inherits the structure)
+and "El impuesto a la pereza" (FP4 operands for the matmul)."""
+import numpy as np
+import pytest
+import torch
+
+import coda_synth as S
+import oracle as O
+from tests import nvfp4_layout as L
+from tests.gpu_helpers import TOL_BF16, TOL_FP8, assert_close, dev, f64, fresh_status, nvfp4_window
+
+pytestmark = pytest.mark.gpu
+BF = torch.bfloat16
+QUANT_REL = 1e-6
+
+
+@pytest.fixture(scope="module")
+def C():
+    from gemm_epilogue_transformer_tcgen05_gb300 import coda
+    coda.lib()
+    coda.coda_set_watchdog_ms(2000)
+    return coda
+
+
+def _scale_of(x):
+    return float(np.float32(np.max(np.abs(x)) / (6 * 448)))
+
+
+def _check_codes(Q, x, rel, what, min_same=0.995):
+    """Q (device Nvfp4 [R, K]) against the oracle's quantisation of x [R, K] with Q.s."""
+    R, K = x.shape
+    got_q = O.e2m1_decode(L.unpack_codes(Q.codes.cpu().numpy()))
+    got_sf = O.e4m3_decode(L.from_atoms(Q.scales.cpu().numpy(), R, K))
+    same_sf, same_q, amb = nvfp4_window(got_q, got_sf, x, Q.s, rel)
+    print(f"{what}: block scales equal to the oracle's {same_sf:.6f}, codes {same_q:.6f}, ambiguous {amb:.6f}")
+    assert same_sf >= 0.999 and same_q >= min_same and amb <= 0.01, what
+
+
+# ------------------------------------------------------------------- transposed quantiser
+@pytest.mark.parametrize("R,Cc", [(256, 384), (320, 128)])
+def test_quantize_nvfp4_t_plain(C, R, Cc):
+    g = torch.Generator().manual_seed(R + Cc)
+    X = (torch.randn((R, Cc), generator=g) * 2.0).to(BF)
+    X[:16, 0] = 0.0                                      # an all-zero column block: scale 0
+    x = f64(X)
+    Q = C.Nvfp4.empty(Cc, R, _scale_of(x))
+    amax = torch.zeros((1,), device="cuda")
+    C.coda_quantize_nvfp4_t(dev(X), Q, amax=amax)
+    torch.cuda.synchronize()
+    fresh_status()
+    _check_codes(Q, x.T, QUANT_REL, f"transposed quantiser {R}x{Cc}")
+    assert float(amax.item()) == float(np.max(np.abs(x)))
+
+
+def test_quantize_nvfp4_t_swiglu_of_saved_z(C):
+    R, F = 256, 256
+    g = torch.Generator().manual_seed(7)
+    Z = (torch.randn((R, 2 * F), generator=g) * 1.5).to(BF)
+    z = f64(Z)
+    a = O.swiglu(z[:, :F], z[:, F:])
+    Q = C.Nvfp4.empty(F, R, _scale_of(a))
+    C.coda_quantize_nvfp4_t(dev(Z), Q, mode=C.QT_SWIGLU)
+    torch.cuda.synchronize()
+    fresh_status()
+    # silu(G) U is formed in fp32 with the fast exponential: a few ulp of relative error
+    _check_codes(Q, a.T, 1e-5, "transposed quantiser of silu(G) U")
+
+
+# ------------------------------------------------------------------ block-scaled GEMMs
+def test_nvfp4_swiglu_backward_gemm(C):
+    M, H, F = 512, 512, 384
+    t = S.nvfp4_mlp_bwd_inputs(M, H, F, seed=3)
+    dy, wd, z, r = f64(t["dY"]), f64(t["W_d"]), f64(t["Z"]), t["r"].numpy().astype(np.float64)
+    A, qa, sfa = L.oracle_nvfp4(dy, _scale_of(dy))
+    B, qb, sfb = L.oracle_nvfp4(wd.T.copy(), _scale_of(wd))            # W_d^T [F, H]
+    e = torch.empty((M, 2 * F), dtype=BF, device="cuda")
+    Sp = torch.empty(((F + 255) // 256, M), device="cuda")
+    C.coda_gemm_epilogue(A, B, [C.OP_TENSOR_SCALE, C.OP_SWIGLU_BWD, C.OP_ROW_SCALE, C.OP_ROW_DOT_PARTIAL], e,
+                         aux_in=dev(t["Z"]), row_scale=dev(t["r"]), row_partials=Sp, tensor_scale=A.s * B.s)
+    torch.cuda.synchronize()
+    fresh_status()
+    dA = O.linear(O.nvfp4_dequantize(qa, sfa, A.s), O.nvfp4_dequantize(qb, sfb, B.s))
+    G, U = z[:, :F], z[:, F:]
+    ref = r[:, None] * np.hstack([dA * U * O.silu_grad(G), dA * O.silu(G)])
+    assert_close(f64(e), ref, TOL_BF16, "e")
+    ge = f64(e)
+    part = np.stack([np.sum((ge * z)[:, np.r_[b * 256:min(F, b * 256 + 256), F + b * 256:F + min(F, b * 256 + 256)]],
+                            axis=1) for b in range((F + 255) // 256)])
+    assert_close(f64(Sp), part, 1e-4, "row partials of the stored e . Z")
+
+
+def test_nvfp4_rmsnorm_backward_gemm(C):
+    M, H, F = 256, 512, 256
+    t = S.nvfp4_mlp_bwd_inputs(M, H, F, seed=4)
+    g = torch.Generator().manual_seed(5)
+    e = (torch.randn((M, 2 * F), generator=g) * 0.01).to(BF)
+    c = (torch.randn((M,), generator=g) * 0.1).float()
+    ex, w = f64(e), f64(t["W_gu"])
+    A, qa, sfa = L.oracle_nvfp4(ex, _scale_of(ex))
+    B, qb, sfb = L.oracle_nvfp4(w.T.copy(), _scale_of(w))                # W_gu^T [H, 2F]
+    dh = torch.empty((M, H), dtype=BF, device="cuda")
+    C.coda_gemm_epilogue(A, B, [C.OP_TENSOR_SCALE, C.OP_RMSBWD_COMBINE], dh, row_coef=dev(c), aux_in=dev(t["h"]),
+                         aux_in2=dev(t["dY"]), tensor_scale=A.s * B.s)
+    torch.cuda.synchronize()
+    fresh_status()
+    tt = O.linear(O.nvfp4_dequantize(qa, sfa, A.s), O.nvfp4_dequantize(qb, sfb, B.s))
+    ref = tt - c.numpy().astype(np.float64)[:, None] * f64(t["h"]) + f64(t["dY"])
+    assert_close(f64(dh), ref, TOL_BF16, "dh")
+
+
+# ------------------------------------------------------------------------- the chain
+def _weights(C, t):
+    wg, wd = t["W_gu"], t["W_d"]
+    H = wg.shape[1]
+    F = wd.shape[1]
+    W_guT = C.Nvfp4.empty(H, 2 * F, _scale_of(f64(wg)))
+    W_dT = C.Nvfp4.empty(F, H, _scale_of(f64(wd)))
+    C.coda_quantize_nvfp4_t(dev(wg), W_guT)
+    C.coda_quantize_nvfp4_t(dev(wd), W_dT)
+    return W_guT, W_dT
+
+
+def _run(C, t, W_guT, W_dT, s_dy, s_e, s_a, s_x):
+    M, H = t["h"].shape
+    F = t["W_d"].shape[1]
+    nv = lambda R, K: C.Nvfp4.empty(R, K)
+    o = dict(dY_r=nv(M, H), dY_c=nv(H, M), e=torch.empty((M, 2 * F), dtype=BF, device="cuda"), e_r=nv(M, 2 * F),
+             e_c=nv(2 * F, M), a_c=nv(F, M), x_c=nv(H, M), amax_dy=torch.empty((1,), device="cuda"),
+             amax_e=torch.empty((1,), device="cuda"), c=torch.empty((M,), device="cuda"),
+             dh=torch.empty((M, H), dtype=BF, device="cuda"), dW_d=torch.empty((H, F), device="cuda"),
+             dW=torch.empty((2 * F, H), device="cuda"))
+    ws = torch.empty((C.coda_workspace_size(C.WS_MLP_NVFP4_BWD, M, H, F) // 4,), device="cuda")
+    C.coda_mlp_nvfp4_backward(dev(t["h"]), W_guT, W_dT, dev(t["Z"]), dev(t["r"]), dev(t["dY"]), s_x, s_a, s_dy, s_e,
+                              o["dY_r"], o["dY_c"], o["e"], o["e_r"], o["e_c"], o["a_c"], o["x_c"], o["amax_dy"],
+                              o["amax_e"], o["c"], o["dh"], o["dW_d"], o["dW"], ws)
+    torch.cuda.synchronize()
+    fresh_status()
+    for k, s in (("dY_r", s_dy), ("dY_c", s_dy), ("e_r", s_e), ("e_c", s_e), ("a_c", s_a), ("x_c", s_x)):
+        o[k].s = s
+    return o
+
+
+def _scales(t):
+    z = f64(t["Z"])
+    F = z.shape[1] // 2
+    s_a = _scale_of(O.swiglu(z[:, :F], z[:, F:]))
+    return _scale_of(f64(t["dY"])), s_a, _scale_of(f64(t["h"]))
+
+
+def test_mlp_nvfp4_backward_small(C):
+    M, H, F = 512, 512, 768
+    t = S.nvfp4_mlp_bwd_inputs(M, H, F, seed=11)
+    W_guT, W_dT = _weights(C, t)
+    s_dy, s_a, s_x = _scales(t)
+    args = (f64(t["h"]), f64(t["W_gu"]), f64(t["W_d"]), f64(t["Z"]), t["r"].numpy().astype(np.float64),
+            f64(t["dY"]))
+    pre = O.mlp_nvfp4_backward(*args, s_dy, 1.0, s_a, s_x, W_guT.s, W_dT.s)
+    s_e = _scale_of(pre["e"])                                            # delayed scale of e
+    ref = O.mlp_nvfp4_backward(*args, s_dy, s_e, s_a, s_x, W_guT.s, W_dT.s)
+    o = _run(C, t, W_guT, W_dT, s_dy, s_e, s_a, s_x)
+    assert_close(f64(o["e"]), ref["e"], TOL_BF16, "e")
+    assert_close(f64(o["c"]), ref["c"], TOL_BF16, "c")
+    assert_close(f64(o["dh"]), ref["dh"], TOL_FP8, "dh")
+    assert_close(f64(o["dW_d"]), ref["dW_d"], TOL_FP8, "dW_d")
+    assert_close(f64(o["dW"]), ref["dW"], TOL_FP8, "dW")
+    assert float(o["amax_dy"].item()) == ref["amax_dy"]
+    assert abs(float(o["amax_e"].item()) - ref["amax_e"]) <= 1e-2 * ref["amax_e"]
+    # each quantised operand against the oracle's quantisation of the tensor it was made from
+    z = f64(t["Z"])
+    _check_codes(o["dY_r"], f64(t["dY"]), QUANT_REL, "dY along rows")
+    _check_codes(o["dY_c"], f64(t["dY"]).T, QUANT_REL, "dY along columns")
+    _check_codes(o["e_r"], f64(o["e"]), QUANT_REL, "e along rows")
+    _check_codes(o["e_c"], f64(o["e"]).T, QUANT_REL, "e along columns")
+    _check_codes(o["a_c"], O.swiglu(z[:, :F], z[:, F:]).T, 1e-5, "silu(G) U along columns")
+    _check_codes(o["x_c"], f64(t["h"]).T, QUANT_REL, "h along columns")
+
+
+@pytest.mark.slow
+def test_mlp_nvfp4_backward_llama8b_shape_sampled(C):
+    """M = 16384 tokens, H = 4096, F = 14336.  Row-local outputs on 96 sampled rows from the
+    oracle; the weight gradients on 32 sampled columns over all rows, from the chain's stored
+    bf16 e (exact inputs: the oracle quantises it and h, dY, silu(G) U along the tokens itself)."""
+    M, H, F = 16384, 4096, 14336
+    t = S.nvfp4_mlp_bwd_inputs(M, H, F, seed=21, device="cuda")
+    W_guT, W_dT = _weights(C, t)
+    z = f64(t["Z"])
+    s_dy, s_x = _scale_of(f64(t["dY"])), _scale_of(f64(t["h"]))
+    G, U = z[:, :F], z[:, F:]
+    a = O.swiglu(G, U)
+    s_a = _scale_of(a)
+    o = _run(C, t, W_guT, W_dT, s_dy, 1.0, s_a, s_x)                    # a first step for the delayed s_e
+    amax_e = float(o["amax_e"].item())
+    s_e = amax_e / (6 * 448)
+    del o
+    o = _run(C, t, W_guT, W_dT, s_dy, s_e, s_a, s_x)
+    assert float(o["amax_e"].item()) == amax_e                          # e does not depend on s_e
+    rows = np.concatenate([np.arange(32), np.random.default_rng(8).choice(np.arange(32, M), 64, replace=False)])
+    hx, dy, r = f64(t["h"]), f64(t["dY"]), t["r"].cpu().numpy().astype(np.float64)
+    Wgu, Wd = f64(t["W_gu"]), f64(t["W_d"])
+    dA = O.nvfp4_round_rows(dy[rows], s_dy) @ O.nvfp4_round_rows(Wd.T, W_dT.s).T
+    e_ref = r[rows, None] * np.hstack([dA * U[rows] * O.silu_grad(G[rows]), dA * O.silu(G[rows])])
+    e_gpu = f64(o["e"])
+    assert_close(e_gpu[rows], e_ref, TOL_BF16, "e (sampled rows)")
+    c_ref = r[rows] * np.sum(e_ref * z[rows], axis=1) / H
+    assert_close(f64(o["c"])[rows], c_ref, TOL_BF16, "c (sampled rows)")
+    tt = O.nvfp4_round_rows(e_gpu[rows], s_e) @ O.nvfp4_round_rows(Wgu.T, W_guT.s).T
+    dh_ref = tt - f64(o["c"])[rows, None] * hx[rows] + dy[rows]
+    assert_close(f64(o["dh"])[rows], dh_ref, TOL_FP8, "dh (sampled rows, the chain's e and c)")
+    cols = np.sort(np.random.default_rng(9).choice(F, 32, replace=False))
+    dYc = O.nvfp4_round_cols(dy, s_dy)
+    assert_close(f64(o["dW_d"])[:, cols], dYc.T @ O.nvfp4_round_cols(a[:, cols], s_a), TOL_FP8, "dW_d[:, cols]")
+    ecols = np.concatenate([cols, F + cols])
+    assert_close(f64(o["dW"])[ecols], O.nvfp4_round_cols(e_gpu[:, ecols], s_e).T @ O.nvfp4_round_cols(hx, s_x),
+                 TOL_FP8, "dW[cols] (the chain's e)")
