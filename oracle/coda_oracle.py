@@ -505,17 +505,20 @@ def mlp_fp8_backward(h, Xq_val, s_x, Wq_val, s_w, Wdq_val, s_wd, Z, aq_val, s_a,
                 dW=e_hat.T @ x)
 
 
-def mlp_nvfp4_backward(h, W_gu, W_d, Z, r, dY, s_dy, s_e, s_a, s_x, s_wt, s_wdt, quant=True):
+def mlp_nvfp4_backward(h, W_gu, W_d, Z, r, dY, s_dy, s_e, s_a, s_x, s_wt, s_wdt, quant=True, round_rows=None,
+                       round_cols=None):
     """Backward of the MLP with NVFP4 GEMM operands (reading 10).  h, W_gu (the effective
     gate/up weight, [2F, H]), W_d ([H, F]) and dY are the bf16 tensors; Z = [G | U] and r are
-    saved by the forward.  Rr / Rc quantise along rows / columns (identity when quant is False):
+    saved by the forward.  Rr / Rc quantise along rows / columns: nvfp4_round_rows / _cols, or
+    the caller's round_rows / round_cols (a test that takes the rounding decisions in another
+    precision), or the identity when quant is False:
       dA = Rr(dY, s_dy) Rr(W_d^T, s_wdt)^T;  e = r [dA U silu'(G) | dA silu(G)]
       s_i = sum_k e_ik Z_ik;  c = r s / H
       t = Rr(e, s_e) Rr(W_gu^T, s_wt)^T;  dh = t - c h + dY
       dW_d = Rc(dY, s_dy)^T Rc(silu(G) U, s_a);  dW = Rc(e, s_e)^T Rc(h, s_x)"""
     h, W_gu, W_d, Z, r, dY = (_f64(v) for v in (h, W_gu, W_d, Z, r, dY))
-    Rr = nvfp4_round_rows if quant else (lambda x, s: _f64(x))
-    Rc = nvfp4_round_cols if quant else (lambda x, s: _f64(x))
+    Rr = (round_rows or nvfp4_round_rows) if quant else (lambda x, s: _f64(x))
+    Rc = (round_cols or nvfp4_round_cols) if quant else (lambda x, s: _f64(x))
     H = h.shape[1]
     F = Z.shape[1] // 2
     G, U = Z[:, :F], Z[:, F:]
