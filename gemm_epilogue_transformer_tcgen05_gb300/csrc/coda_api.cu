@@ -573,6 +573,15 @@ static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const 
             (has(CODA_OP_ROW_SCALE) ? F_ROWSCALE : 0) | (has(CODA_OP_COL_DOT_PARTIAL) ? F_COLPART : 0) |
             (epi == EPI_RMSBWD && !sd.aux_in2 ? F_NO_SIDE1 : 0);
   if (ab_ready && g_launch_overlap) p.flags |= F_AB_READY;
+  // One group holds every N-tile, so each A row-block is read only by the CTA groups of one
+  // wave, while all of B is reused by every wave.  With a long K, a wave streams more A than
+  // L2 keeps beside B, and A at normal priority pushed B out (G3 of the block forward, K = 8192:
+  // B re-read every wave, 537 MB read for 369 MB of compulsory reads).  There A is streamed
+  // with evict_first (411 MB).  With K = 2048 the same policy measured slower, so it is kept
+  // to long K, and to a B that L2 can hold (at most 48 MB).
+  if (p.group_n == p.n_tiles && (K + var->bk - 1) / var->bk >= 128 &&
+      n_tiles * (int64_t)var->un * row_bytes(W->dtype, K) <= ((int64_t)48 << 20))
+    p.flags |= F_A_STREAM;
   switch (g_inject_once.exchange(0)) {
     case 1: p.flags |= F_INJECT_SKIP; break;
     case 2: p.flags |= F_INJECT_RANK1; break;

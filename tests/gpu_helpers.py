@@ -76,8 +76,8 @@ def nvfp4_window(got_q, got_sf, x, s, rel):
     block whose scale rounded the other way is still checked, against that scale).  Where that
     window holds a single value (the value is not within `rel` of a rounding midpoint) the
     GPU's decision must therefore equal the oracle's; only the ambiguous ones may differ.
-    Returns the fractions of block scales and of codes equal to the oracle's rounding, and the
-    fraction of codes whose window is ambiguous."""
+    Returns the fractions of block scales and of codes equal to the oracle's rounding, the
+    fraction of codes whose window is ambiguous, and the same for the block scales."""
     R, K = x.shape
     q, sf = O.nvfp4_quantize(x, s)
     amax_b = np.max(np.abs(x).reshape(R, K // 16, 16), axis=2)
@@ -94,4 +94,5 @@ def nvfp4_window(got_q, got_sf, x, s, rel):
     same_scale = np.repeat(got_sf == sf, 16, axis=1)
     clear = (qlo == qhi) & same_scale
     assert np.all((got_q == q)[clear]), "a code away from every rounding midpoint differs from the oracle's"
-    return float(np.mean(got_sf == sf)), float(np.mean(got_q == q)), float(np.mean(qlo != qhi))
+    return (float(np.mean(got_sf == sf)), float(np.mean(got_q == q)), float(np.mean(qlo != qhi)),
+            float(np.mean(lo != hi)))

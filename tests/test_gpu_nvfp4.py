@@ -63,7 +63,7 @@ def test_quantize_nvfp4_codes_in_rounding_window(C, R, K):
     got_q = O.e2m1_decode(L.unpack_codes(Q.codes.cpu().numpy()))
     buf = Q.scales.cpu().numpy()
     got_sf = O.e4m3_decode(L.from_atoms(buf, R, K))
-    same_sf, same_q, ambiguous = nvfp4_window(got_q, got_sf, x, s, QUANT_REL)
+    same_sf, same_q, ambiguous, _ = nvfp4_window(got_q, got_sf, x, s, QUANT_REL)
     print(f"nvfp4 quantiser {R}x{K}: block scales equal to the oracle's {same_sf:.6f}, codes {same_q:.6f} "
           f"(within fp32 reach of a midpoint: {ambiguous:.6f})")
     # bf16 values over e4m3 block scales often land on an e2m1 midpoint up to the rounding of
@@ -154,7 +154,7 @@ def _check_nvfp4_output(out, a, s_a, M, F, rel=1e-4):
     rounding, and the dequantised tensor must be within half an e2m1 step of a."""
     got_q = O.e2m1_decode(L.unpack_codes(out.codes.cpu().numpy()))
     got_sf = O.e4m3_decode(L.from_atoms(out.scales.cpu().numpy(), M, F))
-    same_sf, same_q, ambiguous = nvfp4_window(got_q, got_sf, a, s_a, rel)
+    same_sf, same_q, ambiguous, _ = nvfp4_window(got_q, got_sf, a, s_a, rel)
     print(f"nvfp4 output {M}x{F}: block scales equal to the oracle's {same_sf:.6f}, codes {same_q:.6f} "
           f"(within {rel:g} of a midpoint: {ambiguous:.6f})")
     assert same_sf >= 0.999 and same_q >= 0.999 and ambiguous <= 0.01

@@ -38,14 +38,18 @@ def _scale_of(x):
     return float(np.float32(np.max(np.abs(x)) / (6 * 448)))
 
 
-def _check_codes(Q, x, rel, what, min_same=0.995):
+def _check_codes(Q, x, rel, what):
     """Q (device Nvfp4 [R, K]) against the oracle's quantisation of x [R, K] with Q.s."""
     R, K = x.shape
     got_q = O.e2m1_decode(L.unpack_codes(Q.codes.cpu().numpy()))
     got_sf = O.e4m3_decode(L.from_atoms(Q.scales.cpu().numpy(), R, K))
-    same_sf, same_q, amb = nvfp4_window(got_q, got_sf, x, Q.s, rel)
-    print(f"{what}: block scales equal to the oracle's {same_sf:.6f}, codes {same_q:.6f}, ambiguous {amb:.6f}")
-    assert same_sf >= 0.999 and same_q >= min_same and amb <= 0.01, what
+    same_sf, same_q, amb, amb_sf = nvfp4_window(got_q, got_sf, x, Q.s, rel)
+    print(f"{what}: block scales equal to the oracle's {same_sf:.6f} (ambiguous {amb_sf:.6f}), codes {same_q:.6f} "
+          f"(ambiguous {amb:.6f})")
+    # with bf16 data and a scale amax / 2688 both decisions often tie exactly in exact arithmetic
+    # (up to the fp32 rounding of s); the window check above lets only those go either way
+    # (a block whose scale went the other way has all its codes on that scale)
+    assert same_sf >= 1 - amb_sf - 1e-3 and same_q >= 1 - amb - (1 - same_sf) - 1e-3 and amb <= 0.01, what
 
 
 # ------------------------------------------------------------------- transposed quantiser
