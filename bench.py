@@ -73,6 +73,9 @@ def parse():
     p.add_argument("--nvfp4-pass", action="store_true",
                    help="run only the NVFP4 MLP (H 4096, F 14336): quantise X, then the chain twice (a short "
                         "program for a per-kernel capture)")
+    p.add_argument("--nvfp4-bwd-pass", action="store_true",
+                   help="run only the NVFP4 MLP backward (H 4096, F 14336) twice, after its weight preparation "
+                        "(a short program for a per-kernel capture)")
     p.add_argument("--row-rms-pass", action="store_true",
                    help="run only the full-row RMS of a [16384, 8192] bf16 tensor, five times (a short program for "
                         "a per-kernel DRAM-bytes capture of the bandwidth-bound reduce)")
@@ -1294,12 +1297,23 @@ def main():
     if args.impl == "reference":
         run_reference(args, world, rank)
         return
-    if args.traffic_pass or args.nvfp4_pass or args.row_rms_pass:
+    if args.traffic_pass or args.nvfp4_pass or args.row_rms_pass or args.nvfp4_bwd_pass:
         if rank == 0:
             if args.traffic_pass:
                 traffic_pass(args)
             elif args.nvfp4_pass:
                 nvfp4_pass(args)
+            elif args.nvfp4_bwd_pass:
+                import torch
+
+                import coda_synth as S
+                from gemm_epilogue_transformer_tcgen05_gb300 import coda as C
+                C.lib()
+                res = nvfp4_backward_workload(torch, C, S, 1, 1.0, peaks(), M=args.tokens)
+                print(json.dumps({"nvfp4_bwd_pass": {"tokens": args.tokens, "hidden": 4096, "ffn": 14336,
+                                                     "order": "weight prep (2 launches), backward x2 (warm-up "
+                                                              "with s_e = 1), then 3 warm-up + 1 timed",
+                                                     "ms": res["ms"]}}), flush=True)
             else:
                 row_rms_pass(args)
         return
