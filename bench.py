@@ -1097,9 +1097,10 @@ def other_workloads(torch, C, S, args, stream):
 
 
 def nvfp4_backward_workload(torch, C, S, steps, peak4, pk, M=M_TOK, H=4096, F=14336):
-    """Device time of the NVFP4 MLP backward at the LLaMA-3-8B MLP shape: 11 launches (dY
-    quantised along rows and columns, the dA GEMM with the SwiGLU-backward epilogue, the row
-    reduce, e along rows and columns, silu(G) U and h along columns, the dW_d, dh and dW GEMMs).
+    """Device time of the NVFP4 MLP backward at the LLaMA-3-8B MLP shape: 9 launches (dY
+    quantised along rows and columns in one pass, the dA GEMM with the SwiGLU-backward epilogue,
+    the row reduce, e along rows and columns in one pass, silu(G) U and h along columns, the
+    dW_d, dh and dW GEMMs).
     The weights' transposed quantisation is weight preparation, outside the timing."""
     t = S.nvfp4_mlp_bwd_inputs(M, H, F, seed=0, device="cuda")
     sc = lambda x: float(x.abs().max()) / (6 * 448)
@@ -1134,10 +1135,10 @@ def nvfp4_backward_workload(torch, C, S, steps, peak4, pk, M=M_TOK, H=4096, F=14
         (n4(2 * F, M) + n4(H, M) + 4 * 2 * F * H)
     roof = max(flop / (peak4 * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
     res = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "roofline_ms": roof, "roofline_frac": roof / ms,
-           "tokens_per_s": M / (ms * 1e-3), "launches": 11, "peak_tflops": peak4, "bytes": byt,
-           "note": "quantise dY (rows, columns), dA GEMM + SwiGLU-bwd (bf16 e), row reduce, quantise e (rows, "
-                   "columns), silu(G) U and h (columns), dW_d, dh GEMM + RMSNorm-bwd combine, dW; NVFP4 operands "
-                   "blocked along each GEMM's K"}
+           "tokens_per_s": M / (ms * 1e-3), "launches": 9, "peak_tflops": peak4, "bytes": byt,
+           "note": "quantise dY (rows and columns, one pass), dA GEMM + SwiGLU-bwd (bf16 e), row reduce, quantise e "
+                   "(rows and columns, one pass), silu(G) U and h (columns), dW_d, dh GEMM + RMSNorm-bwd combine, dW; "
+                   "NVFP4 operands blocked along each GEMM's K"}
     del t, bufs, ws
     torch.cuda.empty_cache()
     return res
@@ -1311,7 +1312,7 @@ def main():
                 C.lib()
                 res = nvfp4_backward_workload(torch, C, S, 1, 1.0, peaks(), M=args.tokens)
                 print(json.dumps({"nvfp4_bwd_pass": {"tokens": args.tokens, "hidden": 4096, "ffn": 14336,
-                                                     "order": "weight prep (2 launches), backward x2 (warm-up "
+                                                     "order": "weight prep (2 launches), backward (warm-up "
                                                               "with s_e = 1), then 3 warm-up + 1 timed",
                                                      "ms": res["ms"]}}), flush=True)
             else:

@@ -199,7 +199,8 @@ def lib():
         "coda_qkv_rope_backward": [P(CodaQkvRopeBwd), c_void_p],
         "coda_quantize_nvfp4": [P(CodaTensor), c_float, P(CodaTensor), c_void_p, c_void_p, c_void_p],
         "coda_mlp_nvfp4": [P(CodaMlpNvfp4), c_void_p],
-        "coda_quantize_nvfp4_t": [P(CodaTensor), c_int32, c_float, P(CodaTensor), c_void_p, c_void_p, c_void_p],
+        "coda_quantize_nvfp4_t": [P(CodaTensor), c_int32, c_float, P(CodaTensor), c_void_p, P(CodaTensor), c_void_p,
+                                  c_void_p, c_void_p],
         "coda_mlp_nvfp4_backward": [P(CodaMlpNvfp4Bwd), c_void_p],
     }
     for name, args in sigs.items():
@@ -508,11 +509,14 @@ def coda_mlp_nvfp4_backward(h, W_guT, W_dT, Z, r, dY, s_x, s_a, s_dy, s_e, dY_r,
     _check(lib().coda_mlp_nvfp4_backward(ctypes.byref(io), _stream(stream)), "coda_mlp_nvfp4_backward")
 
 
-def coda_quantize_nvfp4_t(X, Q, mode=QT_PLAIN, amax=None, stream=None):
+def coda_quantize_nvfp4_t(X, Q, mode=QT_PLAIN, amax=None, stream=None, Q_rows=None):
     """Q (an Nvfp4 [C, R], tensor scale Q.s) = NVFP4 quantisation of the bf16 X [R, C] along its
-    columns, i.e. of X^T; with mode QT_SWIGLU, X is [G | U] ([R, 2C]) and silu(G) U is quantised."""
+    columns, i.e. of X^T; with mode QT_SWIGLU, X is [G | U] ([R, 2C]) and silu(G) U is quantised.
+    Q_rows (an Nvfp4 [R, C]) also receives the quantisation along the rows, with the scale Q.s."""
     x, q = desc(X), desc_nvfp4(Q.codes)
-    _check(lib().coda_quantize_nvfp4_t(ctypes.byref(x), int(mode), Q.s, ctypes.byref(q), _ptr(Q.scales), _ptr(amax),
+    qr = ctypes.byref(desc_nvfp4(Q_rows.codes)) if Q_rows is not None else None
+    _check(lib().coda_quantize_nvfp4_t(ctypes.byref(x), int(mode), Q.s, ctypes.byref(q), _ptr(Q.scales), qr,
+                                       _ptr(Q_rows.scales) if Q_rows is not None else None, _ptr(amax),
                                        _stream(stream)), "coda_quantize_nvfp4_t")
 
 

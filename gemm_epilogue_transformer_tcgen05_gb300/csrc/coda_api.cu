@@ -693,7 +693,7 @@ int coda_quantize_nvfp4(const coda_tensor* X, float s, const coda_tensor* Q, voi
 }
 
 int coda_quantize_nvfp4_t(const coda_tensor* X, int32_t mode, float s, const coda_tensor* Q, void* block_scales,
-                          float* amax, void* stream) {
+                          const coda_tensor* Q_rows, void* row_block_scales, float* amax, void* stream) {
   int st;
   if ((st = check_tensor(X, false)) != CODA_OK) return st;
   if ((st = check_tensor(Q, false)) != CODA_OK) return st;
@@ -703,13 +703,19 @@ int coda_quantize_nvfp4_t(const coda_tensor* X, int32_t mode, float s, const cod
   if (mode == CODA_QT_SWIGLU && X->cols % 2 != 0) return CODA_ERR_SHAPE;
   if (Q->rows != C || Q->cols != R || R % 64 != 0 || C % 128 != 0) return CODA_ERR_SHAPE;
   if (!(s > 0.f) || !(s < INFINITY)) return CODA_ERR_SHAPE;
+  if (Q_rows) {
+    if ((st = check_tensor(Q_rows, false)) != CODA_OK) return st;
+    if (Q_rows->dtype != CODA_NVFP4) return CODA_ERR_DTYPE;
+    if (Q_rows->rows != R || Q_rows->cols != C || R % 128 != 0) return CODA_ERR_SHAPE;
+  }
   if (R == 0 || C == 0) return CODA_OK;
-  if (!block_scales) return CODA_ERR_NULL;
-  if (!aligned16(block_scales)) return CODA_ERR_ALIGN;
+  if (!block_scales || (Q_rows && !row_block_scales)) return CODA_ERR_NULL;
+  if (!aligned16(block_scales) || (Q_rows && !aligned16(row_block_scales))) return CODA_ERR_ALIGN;
   DevState* dv;
   if ((st = ensure_device(&dv)) != CODA_OK) return st;
   cudaError_t e = launch_quantize_nvfp4_t(X->ptr, R, C, X->ld, mode == CODA_QT_SWIGLU, s, Q->ptr, Q->ld / 2,
-                                          static_cast<uint8_t*>(block_scales), amax,
+                                          static_cast<uint8_t*>(block_scales), Q_rows ? Q_rows->ptr : nullptr,
+                                          Q_rows ? Q_rows->ld / 2 : 0, static_cast<uint8_t*>(row_block_scales), amax,
                                           static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
 }
@@ -796,8 +802,8 @@ size_t coda_workspace_size(int32_t which, int64_t M, int64_t H, int64_t F) {
   if (which == CODA_WS_BLOCK_BWD || which == CODA_WS_XENT_BWD)
     return ((size_t)((F + 255) / 256) * (size_t)M + (size_t)((M + 31) / 32) * (size_t)H) * sizeof(float);
   if (which == CODA_WS_XENT_FWD) return (size_t)(2 * ((F + 255) / 256) + 1) * (size_t)M * sizeof(float);
-  if (which == CODA_WS_MLP_FP8_BWD || which == CODA_WS_MLP_NVFP4_BWD)
-    return (size_t)((F + 255) / 256) * (size_t)M * sizeof(float);
+  if (which == CODA_WS_MLP_FP8_BWD) return (size_t)((F + 255) / 256) * (size_t)M * sizeof(float);
+  if (which == CODA_WS_MLP_NVFP4_BWD) return (size_t)((F + 127) / 128) * (size_t)M * sizeof(float);
   return 0;
 }
 
@@ -1350,10 +1356,10 @@ int coda_mlp_nvfp4_backward(const coda_mlp_nvfp4_bwd_io* io, void* stream) {
   // dY along its rows (for dA, K = H) and along its columns (for dW_d, K = tokens)
   coda_tensor dY = mk(io->dY, CODA_BF16, M, H, H);
   coda_tensor dYr = mk(io->dY_r, CODA_NVFP4, M, H, H), dYc = mk(io->dY_c, CODA_NVFP4, H, M, M);
-  if ((st = coda_quantize_nvfp4(&dY, io->s_dy, &dYr, io->dY_r_sf, io->amax_dy, stream)) != CODA_OK) return st;
-  if ((st = coda_quantize_nvfp4_t(&dY, CODA_QT_PLAIN, io->s_dy, &dYc, io->dY_c_sf, nullptr, stream)) != CODA_OK)
+  if ((st = coda_quantize_nvfp4_t(&dY, CODA_QT_PLAIN, io->s_dy, &dYc, io->dY_c_sf, &dYr, io->dY_r_sf, io->amax_dy,
+                                   stream)) != CODA_OK)
     return st;
-  float* spart = io->workspace;   // [ceil(F / 256), M] row partials of sum e . Z
+  float* spart = io->workspace;   // [ceil(F / 128), M] row partials of sum e . Z (one per 128-column tile)
   coda_tensor e = mk(io->e, CODA_BF16, M, 2 * F, 2 * F);
   coda_tensor Z = mk(io->Z, CODA_BF16, M, 2 * F, 2 * F);
   {
@@ -1372,7 +1378,7 @@ int coda_mlp_nvfp4_backward(const coda_mlp_nvfp4_bwd_io* io, void* stream) {
     ax.row_partials_ld = M;
     if ((st = gemm_epilogue_impl(&dYr, &W, &pg, &sd, &e, &ax, stream, true)) != CODA_OK) return st;
   }
-  if ((st = coda_rms_partial_reduce(spart, M, (int32_t)((F + 255) / 256), M, H, 0.f, CODA_REDUCE_SCALE_SUM, io->r,
+  if ((st = coda_rms_partial_reduce(spart, M, (int32_t)((F + 127) / 128), M, H, 0.f, CODA_REDUCE_SCALE_SUM, io->r,
                                     io->c, stream)) != CODA_OK)
     return st;
   // e along its rows (for t = e W_gu, K = 2F) and along its columns (for dW, K = tokens); a
@@ -1380,10 +1386,15 @@ int coda_mlp_nvfp4_backward(const coda_mlp_nvfp4_bwd_io* io, void* stream) {
   coda_tensor er = mk(io->e_r, CODA_NVFP4, M, 2 * F, 2 * F), ec = mk(io->e_c, CODA_NVFP4, 2 * F, M, M);
   coda_tensor ac = mk(io->a_c, CODA_NVFP4, F, M, M), xc = mk(io->x_c, CODA_NVFP4, H, M, M);
   coda_tensor h = mk(io->h, CODA_BF16, M, H, H);
-  if ((st = coda_quantize_nvfp4(&e, io->s_e, &er, io->e_r_sf, io->amax_e, stream)) != CODA_OK) return st;
-  if ((st = coda_quantize_nvfp4_t(&e, CODA_QT_PLAIN, io->s_e, &ec, io->e_c_sf, nullptr, stream)) != CODA_OK) return st;
-  if ((st = coda_quantize_nvfp4_t(&Z, CODA_QT_SWIGLU, io->s_a, &ac, io->a_c_sf, nullptr, stream)) != CODA_OK) return st;
-  if ((st = coda_quantize_nvfp4_t(&h, CODA_QT_PLAIN, io->s_x, &xc, io->x_c_sf, nullptr, stream)) != CODA_OK) return st;
+  if ((st = coda_quantize_nvfp4_t(&e, CODA_QT_PLAIN, io->s_e, &ec, io->e_c_sf, &er, io->e_r_sf, io->amax_e,
+                                   stream)) != CODA_OK)
+    return st;
+  if ((st = coda_quantize_nvfp4_t(&Z, CODA_QT_SWIGLU, io->s_a, &ac, io->a_c_sf, nullptr, nullptr, nullptr, stream)) !=
+      CODA_OK)
+    return st;
+  if ((st = coda_quantize_nvfp4_t(&h, CODA_QT_PLAIN, io->s_x, &xc, io->x_c_sf, nullptr, nullptr, nullptr, stream)) !=
+      CODA_OK)
+    return st;
   {
     // dW_d = s_dy s_a (dY_c a_c^T), contracting over the tokens
     coda_tensor out = mk(io->dW_d, CODA_F32, H, F, F);

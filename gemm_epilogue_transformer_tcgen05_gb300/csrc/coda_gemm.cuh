@@ -198,7 +198,7 @@ struct GemmCfg {
   // side inputs are prefetched NSS chunks ahead (one staging set per chunk in flight); the
   // SwiGLU backward, with two side inputs and two outputs per chunk, goes deeper, except with
   // NVFP4 operands, whose larger stages leave the shared memory for two
-  static constexpr int NSS = (EPI == EPI_SWIGLU_BWD && KIND != KIND_NVFP4) ? 4 : 2;
+  static constexpr int NSS = (EPI == EPI_SWIGLU_BWD && (KIND != KIND_NVFP4 || UN == 128)) ? 4 : 2;
   static_assert(NCHUNK % NSS == 0, "a chunk and the next tile's chunk NCHUNK later share a ring slot");
   // NVFP4: four scale warps write the block scales into TMEM (see the kernel)
   static constexpr int SF_WARPS = FP4 ? 4 : 0;
@@ -236,10 +236,13 @@ struct GemmCfg {
   // TMEM: two accumulators of UN columns, then (NVFP4) each stage's block scales, 4 columns
   // per atom
   static constexpr int SF_COLS = (SF_A_BYTES + SF_B_BYTES) / 128;
-  static constexpr int ACC = FP4 ? 1 : 2;   // accumulators in TMEM
+  static constexpr int ACC = (FP4 && UN == 256) ? 1 : 2;   // accumulators in TMEM
   static_assert(ACC * UN + STAGES * SF_COLS <= TMEM_COLS, "TMEM columns");
   static_assert(UN % 128 == 0 && UN <= UMMA_N && B_ROWS % B_BOX == 0, "MMA N");
-  static_assert(!FP4 || (!A_MN && !B_MN && !AUX && UN == 256 && CG == 2), "NVFP4: K-major operands, CTA pairs, MMA N 256");
+  static_assert(!FP4 || (!A_MN && !B_MN && !AUX && (UN == 256 || UN == 128) && CG == 2),
+                "NVFP4: K-major operands, CTA pairs, MMA N 256 or 128");
+  // a SwiGLU tile's B rows come from two places (gate and up), one 128-row scale atom each
+  static_assert(!(FP4 && DUAL) || UN == 256, "NVFP4 SwiGLU: MMA N 256");
   static_assert(OUT_DT != DT_E2M1 || (FP4 && EPI == EPI_SWIGLU), "e2m1 output: NVFP4 SwiGLU");
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(STAGES >= 2, "shared memory budget");
@@ -1236,9 +1239,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         for (int k = 0; k < KSTEPS; ++k)
           ptx::tmem_st_x1(tcol + 4 * k + q, ptx::ld_shared_u32(ssf + 512 * k + 4 * q));
 #pragma unroll
-        for (int k = 0; k < KSTEPS; ++k)
-          ptx::tmem_st_x8(tcol + 4 * KSTEPS + 8 * k, ptx::ld_shared_v4(ssf + C::SF_A_BYTES + 512 * k),
-                          ptx::ld_shared_v4(ssf + C::SF_A_BYTES + KSTEPS * 512 + 512 * k));
+        for (int k = 0; k < KSTEPS; ++k) {
+          if constexpr (C::UN == 256)
+            ptx::tmem_st_x8(tcol + 4 * KSTEPS + 8 * k, ptx::ld_shared_v4(ssf + C::SF_A_BYTES + 512 * k),
+                            ptx::ld_shared_v4(ssf + C::SF_A_BYTES + KSTEPS * 512 + 512 * k));
+          else   // MMA N 128: one atom of B rows, 4 columns per MMA
+            ptx::tmem_st_x4(tcol + 4 * KSTEPS + 4 * k, ptx::ld_shared_v4(ssf + C::SF_A_BYTES + 512 * k));
+        }
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();

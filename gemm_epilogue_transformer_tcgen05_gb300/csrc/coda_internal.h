@@ -67,7 +67,8 @@ cudaError_t launch_quantize_e4m3(const void* X, int64_t M, int64_t N, int64_t ld
 cudaError_t launch_quantize_nvfp4(const void* X, int64_t R, int64_t K, int64_t ldx, float s, void* Q, int64_t ldq_bytes,
                                   uint8_t* sf, float* amax, cudaStream_t st, int sms);
 cudaError_t launch_quantize_nvfp4_t(const void* X, int64_t R, int64_t C, int64_t ldx, bool swiglu, float s, void* Q,
-                                    int64_t ldq_bytes, uint8_t* sf, float* amax, cudaStream_t st);
+                                    int64_t ldq_bytes, uint8_t* sf, void* Qr, int64_t ldqr_bytes, uint8_t* sfr,
+                                    float* amax, cudaStream_t st);
 cudaError_t launch_xent_reduce(const float* Pm, const float* Ps, int64_t ld, int nparts, int64_t M, const float* T,
                                const int* targets, int64_t V, float* lse, float* loss, float* mean, cudaStream_t s);
 
@@ -81,7 +82,8 @@ constexpr VariantEntry make_variant(VariantKey k) {
 }  // namespace coda
 #define CODA_VARIANT(KIND, EPI, AMN, BMN, OUT, SIDE, AUX) \
   make_variant<GemmCfg<KIND, EPI, AMN, BMN, OUT, SIDE, AUX>>(VariantKey{KIND, EPI, AMN, BMN, OUT, SIDE, AUX})
-// NVFP4 variants: CTA pairs with MMA N = 256 and one accumulator
-#define CODA_VARIANT_FP4(EPI, OUT)                                                        \
-  make_variant<GemmCfg<KIND_NVFP4, EPI, false, false, OUT, DT_BF16, false, 2, 256>>( \
+// NVFP4 variants: CTA pairs with MMA N = 256 and one accumulator, or MMA N = 128 and two
+#define CODA_VARIANT_FP4_N(EPI, OUT, UN_)                                                 \
+  make_variant<GemmCfg<KIND_NVFP4, EPI, false, false, OUT, DT_BF16, false, 2, UN_>>( \
       VariantKey{KIND_NVFP4, EPI, false, false, OUT, DT_BF16, false})
+#define CODA_VARIANT_FP4(EPI, OUT) CODA_VARIANT_FP4_N(EPI, OUT, 256)

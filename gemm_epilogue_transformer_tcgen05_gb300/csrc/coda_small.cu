@@ -527,69 +527,101 @@ cudaError_t launch_quantize_nvfp4(const void* X, int64_t R, int64_t K, int64_t l
 
 // Transposed NVFP4 quantiser: X [R, C] bf16 is quantised along its columns, into Q = X^T
 // ([C, R] codes, blocks of 16 consecutive rows of X), the operand layout of a GEMM that
-// contracts over R (a weight gradient contracts over the tokens).  With `swiglu`, X is the
-// saved [G | U] ([R, 2C]) and the quantised value is silu(G) U.  A CTA stages a tile of 64 rows
-// x 64 columns in shared memory with 16-byte coalesced loads; thread (column c, row block b)
-// then quantises rows 16 b .. 16 b + 15 of column c: 8 bytes of codes (32 bytes per column
-// and tile, contiguous) and one block-scale byte.
-constexpr int QT_ROWS = 64, QT_COLS = 64;
+// contracts over R (a weight gradient contracts over the tokens).  With SWIGLU, X is the saved
+// [G | U] ([R, 2C]) and the quantised value is silu(G) U.  With ROWS, the same pass also writes
+// X quantised along its rows (Qr [R, C], blocks of 16 consecutive columns), so that a tensor
+// needed both ways is read once.  A CTA stages a tile of 64 rows x 128 columns in shared
+// memory, every 16-byte load of the tile issued before the first is used; then thread pairs
+// (column c, row block b) quantise rows 16 b .. 16 b + 15 of column c: 8 bytes of codes (32
+// bytes per column and tile, contiguous) and one block-scale byte; and (row, column block) the
+// same along the rows.
+constexpr int QT_ROWS = 64, QT_COLS = 128;
+template <bool SWIGLU, bool ROWS>
 __global__ void __launch_bounds__(256) quantize_nvfp4_t_kernel(const __nv_bfloat16* __restrict__ X, int64_t R,
-                                                               int64_t C, int64_t ldx, int swiglu, float s,
+                                                               int64_t C, int64_t ldx, float s,
                                                                uint8_t* __restrict__ Q, int64_t ldq,
-                                                               uint8_t* __restrict__ sf,
+                                                               uint8_t* __restrict__ sf, uint8_t* __restrict__ Qr,
+                                                               int64_t ldqr, uint8_t* __restrict__ sfr,
                                                                unsigned int* __restrict__ amax) {
-  __shared__ float tile[QT_ROWS][QT_COLS + 1];
+  extern __shared__ float tile[];   // [QT_ROWS][QT_COLS + 1]
+  constexpr int TS = QT_COLS + 1;
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
   const int64_t col_tiles = (C + QT_COLS - 1) / QT_COLS;
   const int64_t r0 = (int64_t)(blockIdx.x / col_tiles) * QT_ROWS;
   const int64_t c0 = (int64_t)(blockIdx.x % col_tiles) * QT_COLS;
   const int t = threadIdx.x;
-  // load: 64 rows x 8 units of 8 bf16 (16 bytes); thread t takes row t / 8 (+ 32), unit t % 8
+  // load: 64 rows x 16 units of 8 bf16 (16 bytes); thread t takes unit t % 16 of rows
+  // t / 16 + 16 p, p = 0..3 (and the matching units of U)
+  constexpr int NP = QT_ROWS * QT_COLS / 8 / 256;
+  uint4 a[NP], b[SWIGLU ? NP : 1];
+  const int u = t % 16;
 #pragma unroll
-  for (int pass = 0; pass < 2; ++pass) {
-    const int row = t / 8 + 32 * pass, u = t % 8;
-    const int64_t gr = r0 + row, gc = c0 + 8 * u;
+  for (int p = 0; p < NP; ++p) {
+    const int64_t gr = r0 + t / 16 + 16 * p, gc = c0 + 8 * u;
+    const bool in = gr < R && gc < C;   // C is a multiple of 8: a unit is in range or not at all
+    a[p] = in ? __ldcs(reinterpret_cast<const uint4*>(X + gr * ldx + gc)) : make_uint4(0, 0, 0, 0);
+    if constexpr (SWIGLU)
+      b[p] = in ? __ldcs(reinterpret_cast<const uint4*>(X + gr * ldx + C + gc)) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    const uint32_t w[4] = {a[p].x, a[p].y, a[p].z, a[p].w};
     float v[8];
-    if (gr < R && gc < C) {   // C is a multiple of 8, so a unit is in range or not at all
-      const uint4 a = __ldcs(reinterpret_cast<const uint4*>(X + gr * ldx + gc));
-      const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[2 * k] = __uint_as_float(w[k] << 16);
+      v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+    if constexpr (SWIGLU) {
+      const uint32_t wu[4] = {b[p].x, b[p].y, b[p].z, b[p].w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        v[2 * k] = __uint_as_float(w[k] << 16);
-        v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+        v[2 * k] = silu_f(v[2 * k]) * __uint_as_float(wu[k] << 16);
+        v[2 * k + 1] = silu_f(v[2 * k + 1]) * __uint_as_float(wu[k] & 0xFFFF0000u);
       }
-      if (swiglu) {
-        const uint4 b = __ldcs(reinterpret_cast<const uint4*>(X + gr * ldx + C + gc));
-        const uint32_t wu[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          v[2 * k] = silu_f(v[2 * k]) * __uint_as_float(wu[k] << 16);
-          v[2 * k + 1] = silu_f(v[2 * k + 1]) * __uint_as_float(wu[k] & 0xFFFF0000u);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = 0.f;
     }
+    float* dst = tile + (t / 16 + 16 * p) * TS + 8 * u;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) tile[row][8 * u + k] = v[k];
+    for (int k = 0; k < 8; ++k) dst[k] = v[k];
   }
   __syncthreads();
-  // quantise: thread t -> column t / 4, row block t % 4
-  const int c = t / 4, b = t % 4;
-  const int64_t gc = c0 + c;
-  float x[16], m = 0.f;
+  float m = 0.f;
+  // along the columns: pair t + 256 h -> column (t + 256 h) / 4, row block t % 4
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    x[k] = tile[16 * b + k][c];
-    m = fmaxf(m, fabsf(x[k]));
+  for (int h = 0; h < QT_COLS * 4 / 256; ++h) {
+    const int c = (t + 256 * h) / 4, blk = t % 4;
+    const int64_t gc = c0 + c;
+    float x[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      x[k] = tile[(16 * blk + k) * TS + c];
+      m = fmaxf(m, fabsf(x[k]));
+    }
+    if (gc < C && r0 + 16 * blk < R) {
+      uint32_t q[2];
+      const uint32_t code = nvfp4_block16(x, s, q);
+      *reinterpret_cast<uint2*>(Q + gc * ldq + (r0 + 16 * blk) / 2) = make_uint2(q[0], q[1]);
+      sf[sf_offset(gc, (r0 + 16 * blk) / 16, R / 64)] = (uint8_t)code;
+    }
   }
-  if (gc < C && r0 + 16 * b < R) {
-    uint32_t q[2];
-    const uint32_t code = nvfp4_block16(x, s, q);
-    *reinterpret_cast<uint2*>(Q + gc * ldq + (r0 + 16 * b) / 2) = make_uint2(q[0], q[1]);
-    sf[sf_offset(gc, (r0 + 16 * b) / 16, R / 64)] = (uint8_t)code;
+  if constexpr (ROWS) {
+    // along the rows: thread t, pass h -> row t / 4, column block 4 h + t % 4 (four threads
+    // write one 32-byte sector of a row)
+#pragma unroll
+    for (int h = 0; h < QT_ROWS * (QT_COLS / 16) / 256; ++h) {
+      const int r = t / 4, blk = 4 * h + t % 4;
+      const int64_t gr = r0 + r, gc = c0 + 16 * blk;
+      float x[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) x[k] = tile[r * TS + 16 * blk + k];
+      if (gr < R && gc < C) {
+        uint32_t q[2];
+        const uint32_t code = nvfp4_block16(x, s, q);
+        *reinterpret_cast<uint2*>(Qr + gr * ldqr + gc / 2) = make_uint2(q[0], q[1]);
+        sfr[sf_offset(gr, gc / 16, C / 64)] = (uint8_t)code;
+      }
+    }
   }
   if (amax) {
 #pragma unroll
@@ -599,12 +631,32 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_t_kernel(const __nv_bfloat
 }
 
 cudaError_t launch_quantize_nvfp4_t(const void* X, int64_t R, int64_t C, int64_t ldx, bool swiglu, float s, void* Q,
-                                    int64_t ldq_bytes, uint8_t* sf, float* amax, cudaStream_t st) {
+                                    int64_t ldq_bytes, uint8_t* sf, void* Qr, int64_t ldqr_bytes, uint8_t* sfr,
+                                    float* amax, cudaStream_t st) {
   const int64_t tiles = ((R + QT_ROWS - 1) / QT_ROWS) * ((C + QT_COLS - 1) / QT_COLS);
   if (tiles <= 0) return cudaSuccess;
-  launch_k(quantize_nvfp4_t_kernel, (unsigned)tiles, 256, st, reinterpret_cast<const __nv_bfloat16*>(X), R, C, ldx,
-           swiglu ? 1 : 0, s, reinterpret_cast<uint8_t*>(Q), ldq_bytes, sf, reinterpret_cast<unsigned int*>(amax));
-  return cudaGetLastError();
+  const size_t smem = sizeof(float) * QT_ROWS * (QT_COLS + 1);
+  auto go = [&](auto kernel) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)tiles, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = at;
+    cfg.numAttrs = g_launch_overlap ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, reinterpret_cast<const __nv_bfloat16*>(X), R, C, ldx, s,
+                              reinterpret_cast<uint8_t*>(Q), ldq_bytes, sf, reinterpret_cast<uint8_t*>(Qr), ldqr_bytes,
+                              sfr, reinterpret_cast<unsigned int*>(amax));
+  };
+  cudaError_t e;
+  if (swiglu)
+    e = Qr ? go(quantize_nvfp4_t_kernel<true, true>) : go(quantize_nvfp4_t_kernel<true, false>);
+  else
+    e = Qr ? go(quantize_nvfp4_t_kernel<false, true>) : go(quantize_nvfp4_t_kernel<false, false>);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_rope_table(int seq_len, int head_dim, double base, float* cos_out, float* sin_out,

@@ -500,12 +500,16 @@ CODA_API int coda_quantize_nvfp4(const coda_tensor* X, float s, const coda_tenso
  * coda_quantize_nvfp4), block scales in the layout described there for the tensor [C, R].  It
  * is the K-major operand of a GEMM that contracts over R, as the block-scaled tensor cores
  * need.  mode CODA_QT_SWIGLU: X is a saved [G | U] ([R, 2C]) and the value quantised is
- * silu(G) U, formed in fp32.  R must be a multiple of 64 and C of 128 (CODA_ERR_SHAPE);
- * amax (optional, zeroed by the caller) receives the atomic max of the quantised values' |x|.
- * A bandwidth-bound pass: 2 (or 4) bytes read and 9 / 16 written per element. */
+ * silu(G) U, formed in fp32.  With Q_rows (optional, CODA_NVFP4 [R, C], R a multiple of 128)
+ * and its row_block_scales, the same pass also writes the value quantised along its rows (as
+ * coda_quantize_nvfp4 would, same s), for a tensor that two GEMMs read along different K.
+ * R must be a multiple of 64 and C of 128 (CODA_ERR_SHAPE); amax (optional, zeroed by the
+ * caller) receives the atomic max of the quantised values' |x|.  A bandwidth-bound pass: 2 (or
+ * 4) bytes read and 9 / 16 (twice that with Q_rows) written per element. */
 enum coda_qt_mode { CODA_QT_PLAIN = 0, CODA_QT_SWIGLU = 1 };
 CODA_API int coda_quantize_nvfp4_t(const coda_tensor* X, int32_t mode, float s, const coda_tensor* Q,
-                                   void* block_scales, float* amax, void* stream);
+                                   void* block_scales, const coda_tensor* Q_rows, void* row_block_scales,
+                                   float* amax, void* stream);
 
 /* Bytes of the block scales of an NVFP4 tensor [R, K]: ceil(R / 128) * (K / 64) * 512 (the
  * layout at coda_quantize_nvfp4; no counterpart on the pages).  Needs no device. */
@@ -556,9 +560,10 @@ CODA_API int coda_mlp_nvfp4(const coda_mlp_nvfp4_io* io, void* stream);
  * and amax_e / 2688 of an earlier step), s_a the forward's, s_x that of h.  The caller owns
  * every intermediate; the NVFP4 ones are (codes, block scales) pairs of the sizes given by
  * their shapes (coda_nvfp4_scale_bytes).  M must be a multiple of 256 (the weight gradients
- * contract over the tokens), H and F multiples of 256: CODA_ERR_SHAPE otherwise.  Eleven
- * launches: two quantisations of dY, the dA GEMM with the SwiGLU-backward epilogue, the row
- * reduce, four quantisations, the dW_d, dh and dW GEMMs. */
+ * contract over the tokens), H and F multiples of 256: CODA_ERR_SHAPE otherwise.  Nine
+ * launches: dY quantised both ways in one pass, the dA GEMM with the SwiGLU-backward epilogue,
+ * the row reduce, e quantised both ways in one pass, silu(G) U and h along their columns, the
+ * dW_d, dh and dW GEMMs. */
 typedef struct coda_mlp_nvfp4_bwd_io {
   int64_t M, H, F;
   float s_x, s_wt, s_wdt, s_a, s_dy, s_e;

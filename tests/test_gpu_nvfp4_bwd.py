@@ -68,6 +68,29 @@ def test_quantize_nvfp4_t_plain(C, R, Cc):
     assert float(amax.item()) == float(np.max(np.abs(x)))
 
 
+def test_quantize_nvfp4_t_both_ways_in_one_pass(C):
+    """With a row output the same pass also quantises X along its rows: both outputs against the
+    oracle's quantisation of X^T and of X, and amax over the tensor."""
+    R, Cc = 384, 256
+    g = torch.Generator().manual_seed(17)
+    X = (torch.randn((R, Cc), generator=g) * 0.7).to(BF)
+    x = f64(X)
+    s = _scale_of(x) * 1.37                             # a delayed scale: no value sits at the top
+    Qc, Qr = C.Nvfp4.empty(Cc, R, s), C.Nvfp4.empty(R, Cc, s)
+    Qr.scales.fill_(0xEE)
+    amax = torch.zeros((1,), device="cuda")
+    C.coda_quantize_nvfp4_t(dev(X), Qc, amax=amax, Q_rows=Qr)
+    torch.cuda.synchronize()
+    fresh_status()
+    _check_codes(Qc, x.T, QUANT_REL, "both ways: along columns")
+    _check_codes(Qr, x, QUANT_REL, "both ways: along rows")
+    assert float(amax.item()) == float(np.max(np.abs(x)))
+    buf = Qr.scales.cpu().numpy()
+    used = np.zeros(buf.size, dtype=bool)
+    used[L.atom_offsets(R, Cc)] = True
+    assert not buf[~used].any()                         # every byte of the row scales written or zero
+
+
 def test_quantize_nvfp4_t_swiglu_of_saved_z(C):
     R, F = 256, 256
     g = torch.Generator().manual_seed(7)
@@ -83,14 +106,14 @@ def test_quantize_nvfp4_t_swiglu_of_saved_z(C):
 
 
 # ------------------------------------------------------------------ block-scaled GEMMs
-def test_nvfp4_swiglu_backward_gemm(C):
-    M, H, F = 512, 512, 384
+@pytest.mark.parametrize("M,H,F", [(512, 512, 384), (4096, 512, 1024)])   # the second: more tiles than CTA pairs
+def test_nvfp4_swiglu_backward_gemm(C, M, H, F):
     t = S.nvfp4_mlp_bwd_inputs(M, H, F, seed=3)
     dy, wd, z, r = f64(t["dY"]), f64(t["W_d"]), f64(t["Z"]), t["r"].numpy().astype(np.float64)
     A, qa, sfa = L.oracle_nvfp4(dy, _scale_of(dy))
     B, qb, sfb = L.oracle_nvfp4(wd.T.copy(), _scale_of(wd))            # W_d^T [F, H]
     e = torch.empty((M, 2 * F), dtype=BF, device="cuda")
-    Sp = torch.empty(((F + 255) // 256, M), device="cuda")
+    Sp = torch.empty(((F + 127) // 128, M), device="cuda")
     C.coda_gemm_epilogue(A, B, [C.OP_TENSOR_SCALE, C.OP_SWIGLU_BWD, C.OP_ROW_SCALE, C.OP_ROW_DOT_PARTIAL], e,
                          aux_in=dev(t["Z"]), row_scale=dev(t["r"]), row_partials=Sp, tensor_scale=A.s * B.s)
     torch.cuda.synchronize()
@@ -100,8 +123,9 @@ def test_nvfp4_swiglu_backward_gemm(C):
     ref = r[:, None] * np.hstack([dA * U * O.silu_grad(G), dA * O.silu(G)])
     assert_close(f64(e), ref, TOL_BF16, "e")
     ge = f64(e)
-    part = np.stack([np.sum((ge * z)[:, np.r_[b * 256:min(F, b * 256 + 256), F + b * 256:F + min(F, b * 256 + 256)]],
-                            axis=1) for b in range((F + 255) // 256)])
+    bn = 128   # output columns of dA per tile (MMA N 128)
+    part = np.stack([np.sum((ge * z)[:, np.r_[b * bn:min(F, b * bn + bn), F + b * bn:F + min(F, b * bn + bn)]],
+                            axis=1) for b in range((F + bn - 1) // bn)])
     assert_close(f64(Sp), part, 1e-4, "row partials of the stored e . Z")
 
 
