@@ -716,7 +716,7 @@ int coda_quantize_nvfp4_t(const coda_tensor* X, int32_t mode, float s, const cod
   cudaError_t e = launch_quantize_nvfp4_t(X->ptr, R, C, X->ld, mode == CODA_QT_SWIGLU, s, Q->ptr, Q->ld / 2,
                                           static_cast<uint8_t*>(block_scales), Q_rows ? Q_rows->ptr : nullptr,
                                           Q_rows ? Q_rows->ld / 2 : 0, static_cast<uint8_t*>(row_block_scales), amax,
-                                          static_cast<cudaStream_t>(stream));
+                                          static_cast<cudaStream_t>(stream), dv->sms);
   return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
 }
 

@@ -68,7 +68,7 @@ cudaError_t launch_quantize_nvfp4(const void* X, int64_t R, int64_t K, int64_t l
                                   uint8_t* sf, float* amax, cudaStream_t st, int sms);
 cudaError_t launch_quantize_nvfp4_t(const void* X, int64_t R, int64_t C, int64_t ldx, bool swiglu, float s, void* Q,
                                     int64_t ldq_bytes, uint8_t* sf, void* Qr, int64_t ldqr_bytes, uint8_t* sfr,
-                                    float* amax, cudaStream_t st);
+                                    float* amax, cudaStream_t st, int sms);
 cudaError_t launch_xent_reduce(const float* Pm, const float* Ps, int64_t ld, int nparts, int64_t M, const float* T,
                                const int* targets, int64_t V, float* lse, float* loss, float* mean, cudaStream_t s);
 

@@ -11,6 +11,8 @@
 //   * e4m3 and NVFP4 quantisers.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "coda_internal.h"
 
 namespace coda {
@@ -530,12 +532,33 @@ cudaError_t launch_quantize_nvfp4(const void* X, int64_t R, int64_t K, int64_t l
 // contracts over R (a weight gradient contracts over the tokens).  With SWIGLU, X is the saved
 // [G | U] ([R, 2C]) and the quantised value is silu(G) U.  With ROWS, the same pass also writes
 // X quantised along its rows (Qr [R, C], blocks of 16 consecutive columns), so that a tensor
-// needed both ways is read once.  A CTA stages a tile of 64 rows x 128 columns in shared
-// memory, every 16-byte load of the tile issued before the first is used; then thread pairs
-// (column c, row block b) quantise rows 16 b .. 16 b + 15 of column c: 8 bytes of codes (32
-// bytes per column and tile, contiguous) and one block-scale byte; and (row, column block) the
-// same along the rows.
+// needed both ways is read once.
+// Persistent CTAs walk tiles of 64 rows x 128 columns.  A tile's 16-byte loads (8 consecutive
+// values of a row per thread) are issued into registers while the previous tile is quantised.
+//   - Along the rows the values never leave the registers: the two threads holding a block of
+//     16 exchange their maxima with one shuffle, and each writes its 8 codes (4 bytes).
+//   - Along the columns the tile is staged in shared memory (as bf16, or fp32 for silu(G) U)
+//     and each warp reads 32 consecutive columns of a 16-row block, conflict-free; a thread
+//     quantises one column's block (8 bytes of codes, one block-scale byte).
 constexpr int QT_ROWS = 64, QT_COLS = 128;
+
+// NVFP4 codes of 8 values x with tensor scale s, given the amax of their block of 16: the
+// decisions of nvfp4_block16, taken on this thread's half of the block.  Returns the 8 codes
+// (element j in nibble j) and the block scale's e4m3 byte in *code.
+__device__ __forceinline__ uint32_t nvfp4_half_block(const float* x, float amax, float s, uint32_t* code) {
+  const float u = __fdiv_rn(amax, __fmul_rn(6.0f, s));
+  const uint16_t code2 = ptx::cvt_e4m3x2(u, 0.0f);
+  float sfv, zero;
+  ptx::e4m3x2_to_f32(code2, sfv, zero);
+  const float d = __fmul_rn(sfv, s);
+  const float rd = d > 0.f ? __frcp_rn(d) : 0.f;
+  float y[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) y[j] = __fmul_rn(x[j], rd);
+  *code = code2 & 0xFFu;
+  return ptx::cvt_e2m1x8(y);
+}
+
 template <bool SWIGLU, bool ROWS>
 __global__ void __launch_bounds__(256) quantize_nvfp4_t_kernel(const __nv_bfloat16* __restrict__ X, int64_t R,
                                                                int64_t C, int64_t ldx, float s,
@@ -543,105 +566,121 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_t_kernel(const __nv_bfloat
                                                                uint8_t* __restrict__ sf, uint8_t* __restrict__ Qr,
                                                                int64_t ldqr, uint8_t* __restrict__ sfr,
                                                                unsigned int* __restrict__ amax) {
-  extern __shared__ float tile[];   // [QT_ROWS][QT_COLS + 1]
-  constexpr int TS = QT_COLS + 1;
+  using T = typename std::conditional<SWIGLU, float, __nv_bfloat16>::type;
+  extern __shared__ __align__(16) uint8_t qt_smem[];
+  T* tile = reinterpret_cast<T*>(qt_smem);   // [QT_ROWS][QT_COLS]
+  constexpr int NP = QT_ROWS * QT_COLS / 8 / 256;   // 16-byte units of X per thread and tile
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
   const int64_t col_tiles = (C + QT_COLS - 1) / QT_COLS;
-  const int64_t r0 = (int64_t)(blockIdx.x / col_tiles) * QT_ROWS;
-  const int64_t c0 = (int64_t)(blockIdx.x % col_tiles) * QT_COLS;
-  const int t = threadIdx.x;
-  // load: 64 rows x 16 units of 8 bf16 (16 bytes); thread t takes unit t % 16 of rows
-  // t / 16 + 16 p, p = 0..3 (and the matching units of U)
-  constexpr int NP = QT_ROWS * QT_COLS / 8 / 256;
+  const int64_t tiles = ((R + QT_ROWS - 1) / QT_ROWS) * col_tiles;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, u = t % 16;
+  float m = 0.f;
   uint4 a[NP], b[SWIGLU ? NP : 1];
-  const int u = t % 16;
+  auto issue = [&](int64_t tl) {
+    const int64_t r0 = (tl / col_tiles) * QT_ROWS, c0 = (tl % col_tiles) * QT_COLS;
 #pragma unroll
-  for (int p = 0; p < NP; ++p) {
-    const int64_t gr = r0 + t / 16 + 16 * p, gc = c0 + 8 * u;
-    const bool in = gr < R && gc < C;   // C is a multiple of 8: a unit is in range or not at all
-    a[p] = in ? __ldcs(reinterpret_cast<const uint4*>(X + gr * ldx + gc)) : make_uint4(0, 0, 0, 0);
-    if constexpr (SWIGLU)
-      b[p] = in ? __ldcs(reinterpret_cast<const uint4*>(X + gr * ldx + C + gc)) : make_uint4(0, 0, 0, 0);
-  }
-#pragma unroll
-  for (int p = 0; p < NP; ++p) {
-    const uint32_t w[4] = {a[p].x, a[p].y, a[p].z, a[p].w};
-    float v[8];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      v[2 * k] = __uint_as_float(w[k] << 16);
-      v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    for (int p = 0; p < NP; ++p) {
+      const int64_t gr = r0 + t / 16 + 16 * p, gc = c0 + 8 * u;
+      const bool in = gr < R && gc < C;   // C is a multiple of 8: a unit is in range or not at all
+      a[p] = in ? __ldcs(reinterpret_cast<const uint4*>(X + gr * ldx + gc)) : make_uint4(0, 0, 0, 0);
+      if constexpr (SWIGLU)
+        b[p] = in ? __ldcs(reinterpret_cast<const uint4*>(X + gr * ldx + C + gc)) : make_uint4(0, 0, 0, 0);
     }
-    if constexpr (SWIGLU) {
-      const uint32_t wu[4] = {b[p].x, b[p].y, b[p].z, b[p].w};
+  };
+  int64_t tl = blockIdx.x;
+  if (tl < tiles) issue(tl);
+  for (; tl < tiles; tl += gridDim.x) {
+    const int64_t r0 = (tl / col_tiles) * QT_ROWS, c0 = (tl % col_tiles) * QT_COLS;
+    __syncthreads();   // the previous tile's reads of the shared tile are done
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      const int row = t / 16 + 16 * p;
+      const uint32_t w[4] = {a[p].x, a[p].y, a[p].z, a[p].w};
+      float v[8];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        v[2 * k] = silu_f(v[2 * k]) * __uint_as_float(wu[k] << 16);
-        v[2 * k + 1] = silu_f(v[2 * k + 1]) * __uint_as_float(wu[k] & 0xFFFF0000u);
+        v[2 * k] = __uint_as_float(w[k] << 16);
+        v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+      }
+      if constexpr (SWIGLU) {
+        const uint32_t wu[4] = {b[p].x, b[p].y, b[p].z, b[p].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          v[2 * k] = silu_f(v[2 * k]) * __uint_as_float(wu[k] << 16);
+          v[2 * k + 1] = silu_f(v[2 * k + 1]) * __uint_as_float(wu[k] & 0xFFFF0000u);
+        }
+        float4* dst = reinterpret_cast<float4*>(tile + row * QT_COLS + 8 * u);
+        dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+        dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+      } else {
+        *reinterpret_cast<uint4*>(tile + row * QT_COLS + 8 * u) = a[p];
+      }
+      float m8 = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m8 = fmaxf(m8, fabsf(v[k]));
+      m = fmaxf(m, m8);
+      if constexpr (ROWS) {   // along the rows, from the registers: threads t, t ^ 1 hold a block
+        const float m16 = fmaxf(m8, __shfl_xor_sync(0xffffffffu, m8, 1));
+        const int64_t gr = r0 + row, gc = c0 + 8 * u;
+        uint32_t code;
+        const uint32_t q = nvfp4_half_block(v, m16, s, &code);
+        if (gr < R && gc < C) {
+          *reinterpret_cast<uint32_t*>(Qr + gr * ldqr + gc / 2) = q;
+          if ((u & 1) == 0) sfr[sf_offset(gr, gc / 16, C / 64)] = (uint8_t)code;
+        }
       }
     }
-    float* dst = tile + (t / 16 + 16 * p) * TS + 8 * u;
+    __syncthreads();
+    const int64_t nx = tl + gridDim.x;   // the next tile's loads fly while this one is quantised
+    if (nx < tiles) issue(nx);
+    // along the columns: warp w takes (column group, row block) pairs 2 w and 2 w + 1; lane =
+    // column within the group of 32
 #pragma unroll
-    for (int k = 0; k < 8; ++k) dst[k] = v[k];
-  }
-  __syncthreads();
-  float m = 0.f;
-  // along the columns: pair t + 256 h -> column (t + 256 h) / 4, row block t % 4
-#pragma unroll
-  for (int h = 0; h < QT_COLS * 4 / 256; ++h) {
-    const int c = (t + 256 * h) / 4, blk = t % 4;
-    const int64_t gc = c0 + c;
-    float x[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      x[k] = tile[(16 * blk + k) * TS + c];
-      m = fmaxf(m, fabsf(x[k]));
-    }
-    if (gc < C && r0 + 16 * blk < R) {
-      uint32_t q[2];
-      const uint32_t code = nvfp4_block16(x, s, q);
-      *reinterpret_cast<uint2*>(Q + gc * ldq + (r0 + 16 * blk) / 2) = make_uint2(q[0], q[1]);
-      sf[sf_offset(gc, (r0 + 16 * blk) / 16, R / 64)] = (uint8_t)code;
-    }
-  }
-  if constexpr (ROWS) {
-    // along the rows: thread t, pass h -> row t / 4, column block 4 h + t % 4 (four threads
-    // write one 32-byte sector of a row)
-#pragma unroll
-    for (int h = 0; h < QT_ROWS * (QT_COLS / 16) / 256; ++h) {
-      const int r = t / 4, blk = 4 * h + t % 4;
-      const int64_t gr = r0 + r, gc = c0 + 16 * blk;
+    for (int h = 0; h < 2; ++h) {
+      const int pr = 2 * warp + h, cg = pr % 4, blk = pr / 4;
+      const int c = 32 * cg + lane;
+      const int64_t gc = c0 + c;
       float x[16];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) x[k] = tile[r * TS + 16 * blk + k];
-      if (gr < R && gc < C) {
+      for (int k = 0; k < 16; ++k) {
+        if constexpr (SWIGLU) x[k] = tile[(16 * blk + k) * QT_COLS + c];
+        else x[k] = __bfloat162float(tile[(16 * blk + k) * QT_COLS + c]);
+      }
+      if (gc < C && r0 + 16 * blk < R) {
         uint32_t q[2];
         const uint32_t code = nvfp4_block16(x, s, q);
-        *reinterpret_cast<uint2*>(Qr + gr * ldqr + gc / 2) = make_uint2(q[0], q[1]);
-        sfr[sf_offset(gr, gc / 16, C / 64)] = (uint8_t)code;
+        *reinterpret_cast<uint2*>(Q + gc * ldq + (r0 + 16 * blk) / 2) = make_uint2(q[0], q[1]);
+        sf[sf_offset(gc, (r0 + 16 * blk) / 16, R / 64)] = (uint8_t)code;
       }
     }
   }
   if (amax) {
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if ((t & 31) == 0 && m > 0.f) atomicMax(amax, __float_as_uint(m));
+    if (lane == 0 && m > 0.f) atomicMax(amax, __float_as_uint(m));
   }
 }
 
 cudaError_t launch_quantize_nvfp4_t(const void* X, int64_t R, int64_t C, int64_t ldx, bool swiglu, float s, void* Q,
                                     int64_t ldq_bytes, uint8_t* sf, void* Qr, int64_t ldqr_bytes, uint8_t* sfr,
-                                    float* amax, cudaStream_t st) {
+                                    float* amax, cudaStream_t st, int sms) {
   const int64_t tiles = ((R + QT_ROWS - 1) / QT_ROWS) * ((C + QT_COLS - 1) / QT_COLS);
   if (tiles <= 0) return cudaSuccess;
-  const size_t smem = sizeof(float) * QT_ROWS * (QT_COLS + 1);
+  const size_t smem = (swiglu ? sizeof(float) : sizeof(__nv_bfloat16)) * QT_ROWS * QT_COLS;
   auto go = [&](auto kernel) {
+    // persistent: as many CTAs as fit on every SM at once
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, smem) != cudaSuccess || per_sm < 1) {
+      cudaGetLastError();
+      per_sm = 1;
+    }
+    const int64_t grid = tiles < (int64_t)sms * per_sm ? tiles : (int64_t)sms * per_sm;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3((unsigned)tiles, 1, 1);
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
