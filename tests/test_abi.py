@@ -204,3 +204,41 @@ def test_nvfp4_entry_points_validate(L):
     assert L.coda_mlp_nvfp4(ctypes.byref(io), None) == C.ERR_NULL
     io.W_dsf, io.M = f, 0
     assert L.coda_mlp_nvfp4(ctypes.byref(io), None) == C.OK                                   # empty batch: no-op
+
+
+def test_nvfp4_backward_entry_points_validate(L):
+    f = ctypes.c_void_p(FAKE)
+    qt = L.coda_quantize_nvfp4_t
+    X = _t(FAKE, C.BF16, 256, 384, 384)
+    Qc = _t(FAKE, C.NVFP4, 384, 256, 256)          # X^T
+    Qr = _t(FAKE, C.NVFP4, 256, 384, 384)
+    assert qt(None, 0, 1.0, ctypes.byref(Qc), f, None, None, None, None) == C.ERR_NULL
+    assert qt(ctypes.byref(X), 0, 1.0, ctypes.byref(Qc), None, None, None, None, None) == C.ERR_NULL  # scales missing
+    assert qt(ctypes.byref(X), 2, 1.0, ctypes.byref(Qc), f, None, None, None, None) == C.ERR_SHAPE    # mode
+    assert qt(ctypes.byref(X), 0, 0.0, ctypes.byref(Qc), f, None, None, None, None) == C.ERR_SHAPE    # s > 0
+    assert qt(ctypes.byref(X), 0, 1.0, ctypes.byref(Qr), f, None, None, None, None) == C.ERR_SHAPE    # not X^T
+    assert qt(ctypes.byref(X), 1, 1.0, ctypes.byref(Qc), f, None, None, None, None) == C.ERR_SHAPE    # SwiGLU: C = 192
+    assert qt(ctypes.byref(X), 0, 1.0, ctypes.byref(Qc), ctypes.c_void_p(FAKE + 8), None, None, None,
+              None) == C.ERR_ALIGN
+    assert qt(ctypes.byref(X), 0, 1.0, ctypes.byref(Qc), f, ctypes.byref(Qc), f, None, None) == C.ERR_SHAPE  # rows: [R, C]
+    assert qt(ctypes.byref(X), 0, 1.0, ctypes.byref(Qc), f, ctypes.byref(Qr), None, None, None) == C.ERR_NULL
+    X2 = _t(FAKE, C.BF16, 320, 384, 384)           # R % 128 != 0: no row output
+    assert qt(ctypes.byref(X2), 0, 1.0, ctypes.byref(_t(FAKE, C.NVFP4, 384, 320, 320)), f,
+              ctypes.byref(_t(FAKE, C.NVFP4, 320, 384, 384)), f, None, None) == C.ERR_SHAPE
+    assert qt(ctypes.byref(_t(FAKE, C.BF16, 200, 384, 384)), 0, 1.0, ctypes.byref(_t(FAKE, C.NVFP4, 384, 200, 256)),
+              f, None, None, None, None) == C.ERR_SHAPE                                   # R % 64
+    # the chain
+    assert L.coda_mlp_nvfp4_backward(None, None) == C.ERR_NULL
+    names = [n for n, _ in C.CodaMlpNvfp4Bwd._fields_[9:]]
+    io = C.CodaMlpNvfp4Bwd(256, 512, 512, 1.0, 1.0, 1.0, 1.0, 1.0, 1.0, *([f] * len(names)))
+    io.M = 320
+    assert L.coda_mlp_nvfp4_backward(ctypes.byref(io), None) == C.ERR_SHAPE        # M % 256
+    io.M, io.F = 256, 384
+    assert L.coda_mlp_nvfp4_backward(ctypes.byref(io), None) == C.ERR_SHAPE        # F % 256
+    io.F, io.s_e = 512, 0.0
+    assert L.coda_mlp_nvfp4_backward(ctypes.byref(io), None) == C.ERR_SHAPE        # scales > 0
+    io.s_e, io.e_c = 1.0, None
+    assert L.coda_mlp_nvfp4_backward(ctypes.byref(io), None) == C.ERR_NULL
+    io.e_c, io.workspace = f, ctypes.c_void_p(FAKE + 4)
+    assert L.coda_mlp_nvfp4_backward(ctypes.byref(io), None) == C.ERR_ALIGN
+    assert C.coda_workspace_size(C.WS_MLP_NVFP4_BWD, 16384, 4096, 14336) == (14336 // 128) * 16384 * 4
