@@ -102,9 +102,17 @@ def peaks():
 SUSTAINED_REGION_S = 2.0
 
 
-def tensor_peak(pk, region_s):
+CAPPED_CLOCK_FRAC = 0.9   # a median SM clock below this share of the maximum: power-capped run
+
+
+def tensor_peak(pk, region_s, sm_mhz=None, sm_max_mhz=None):
     """(peak TFLOP/s, kind) of the bf16 tensor roofline for a timed region of region_s seconds:
-    the measured burst figure for a short region, the sustained one for a long region."""
+    the measured burst figure for a short region at full clocks; the sustained one (measured
+    under the power cap) for a long region, or wherever the SM clocks sampled during the region
+    show the cap (median below CAPPED_CLOCK_FRAC of the maximum)."""
+    if sm_mhz and sm_max_mhz and sm_mhz < CAPPED_CLOCK_FRAC * sm_max_mhz:
+        return pk["bf16_sus"], (f"bf16 sustained, of {pk['source']} (median SM clock {sm_mhz:.0f} of "
+                                f"{sm_max_mhz:.0f} MHz during the {region_s:.3f} s region: power-capped)")
     if region_s < SUSTAINED_REGION_S:
         return pk["bf16"], f"bf16 burst, of {pk['source']} (timed region {region_s:.3f} s < {SUSTAINED_REGION_S} s)"
     return pk["bf16_sus"], f"bf16 sustained, of {pk['source']} (timed region {region_s:.3f} s)"
@@ -636,7 +644,8 @@ def run_coda(args, world, rank, local):
     g2_tflops = FLOP["G2"] / (g2_ms * 1e-3) / 1e12
     traffic = recorded_traffic()
     clocks = sampler.summary() if sampler else None
-    peak, peak_kind = tensor_peak(pk, ms / 1e3)
+    peak, peak_kind = tensor_peak(pk, ms / 1e3, clocks.get("sm_mhz") if clocks else None,
+                                  clocks.get("sm_max_mhz") if clocks else None)
     chain_roof = lambda tf: max(CHAIN_FLOP / (tf * 1e12), CHAIN_BYTES / (pk["hbm"] * 1e9)) * 1e3
     chain_roof_ms = chain_roof(peak)
     line = {

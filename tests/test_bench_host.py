@@ -101,6 +101,16 @@ def test_tensor_peak_is_burst_for_short_regions_and_sustained_for_long_ones():
     assert peak == 1709.5 and kind.startswith("bf16 sustained")
 
 
+def test_tensor_peak_follows_the_sampled_clocks():
+    pk = {"bf16": 1904.0, "bf16_sus": 1709.5, "hbm": 6776.3, "source": "measured"}
+    peak, kind = bench.tensor_peak(pk, 1.1, sm_mhz=1604.5, sm_max_mhz=2070.0)   # capped under load
+    assert peak == 1709.5 and "power-capped" in kind
+    peak, kind = bench.tensor_peak(pk, 0.02, sm_mhz=2002.0, sm_max_mhz=2070.0)  # full clocks
+    assert peak == 1904.0 and kind.startswith("bf16 burst")
+    peak, kind = bench.tensor_peak(pk, 0.02, sm_mhz=None, sm_max_mhz=2070.0)    # no samples
+    assert peak == 1904.0
+
+
 def test_lib_peak_takes_the_higher_measured_rate_or_the_fallback():
     assert bench.lib_peak({"burst_tflops": 3400.0, "sustained_tflops": 3350.0}, 1.0) == 3400.0
     assert bench.lib_peak({"burst_tflops": 4900.0, "sustained_tflops": 7000.0}, 1.0) == 7000.0
