@@ -533,14 +533,20 @@ cudaError_t launch_quantize_nvfp4(const void* X, int64_t R, int64_t K, int64_t l
 // [G | U] ([R, 2C]) and the quantised value is silu(G) U.  With ROWS, the same pass also writes
 // X quantised along its rows (Qr [R, C], blocks of 16 consecutive columns), so that a tensor
 // needed both ways is read once.
-// Persistent CTAs walk tiles of 64 rows x 128 columns.  A tile's 16-byte loads (8 consecutive
-// values of a row per thread) are issued into registers while the previous tile is quantised.
+// Persistent CTAs walk tiles of 128 rows x 128 columns: the block scales of a tile are then
+// whole 512-byte atoms in both directions (128 rows of the destination by four blocks of 16
+// along its K).  Every output of a tile is staged in shared memory and leaves in 16-byte
+// stores: each destination row's codes as 64 contiguous bytes, the scales as two contiguous
+// atoms.  (Single-byte scale stores straight from the quantising threads cost more than the
+// whole read.)
+//   - A tile's 16-byte loads (8 consecutive values of a row per thread, 8 per thread) are
+//     issued into registers while the previous tile is quantised.
 //   - Along the rows the values never leave the registers: the two threads holding a block of
-//     16 exchange their maxima with one shuffle, and each writes its 8 codes (4 bytes).
-//   - Along the columns the tile is staged in shared memory (as bf16, or fp32 for silu(G) U)
-//     and each warp reads 32 consecutive columns of a 16-row block, conflict-free; a thread
-//     quantises one column's block (8 bytes of codes, one block-scale byte).
-constexpr int QT_ROWS = 64, QT_COLS = 128;   // 128-row tiles measured no faster (524 against 502 us for e)
+//     16 exchange their maxima with one shuffle, and each stages its 8 codes (4 bytes).
+//   - Along the columns the tile is staged in shared memory (as bf16, or fp32 for silu(G) U);
+//     a warp reads 32 consecutive columns of a row, conflict-free, and a thread quantises four
+//     16-row blocks of one column.
+constexpr int QT_ROWS = 128, QT_COLS = 128;
 
 // NVFP4 codes of 8 values x with tensor scale s, given the amax of their block of 16: the
 // decisions of nvfp4_block16, taken on this thread's half of the block.  Returns the 8 codes
@@ -560,19 +566,23 @@ __device__ __forceinline__ uint32_t nvfp4_half_block(const float* x, float amax,
 }
 
 template <bool SWIGLU, bool ROWS>
-__global__ void __launch_bounds__(256) quantize_nvfp4_t_kernel(const __nv_bfloat16* __restrict__ X, int64_t R,
-                                                               int64_t C, int64_t ldx, float s,
-                                                               uint8_t* __restrict__ Q, int64_t ldq,
-                                                               uint8_t* __restrict__ sf, uint8_t* __restrict__ Qr,
-                                                               int64_t ldqr, uint8_t* __restrict__ sfr,
-                                                               unsigned int* __restrict__ amax) {
+__global__ void __launch_bounds__(256, SWIGLU ? 2 : 3) quantize_nvfp4_t_kernel(const __nv_bfloat16* __restrict__ X, int64_t R,
+                                                                  int64_t C, int64_t ldx, float s,
+                                                                  uint8_t* __restrict__ Q, int64_t ldq,
+                                                                  uint8_t* __restrict__ sf, uint8_t* __restrict__ Qr,
+                                                                  int64_t ldqr, uint8_t* __restrict__ sfr,
+                                                                  unsigned int* __restrict__ amax) {
   using T = typename std::conditional<SWIGLU, float, __nv_bfloat16>::type;
   extern __shared__ __align__(16) uint8_t qt_smem[];
-  T* tile = reinterpret_cast<T*>(qt_smem);   // [QT_ROWS][QT_COLS]
+  T* tile = reinterpret_cast<T*>(qt_smem);                              // [QT_ROWS][QT_COLS]
+  uint8_t* colq = qt_smem + sizeof(T) * QT_ROWS * QT_COLS;               // [QT_COLS][64 B]: Q's rows
+  uint8_t* colsf = colq + QT_COLS * QT_ROWS / 2;                         // two atoms of Q's scales
+  uint8_t* rowq = colsf + 1024;                                          // [QT_ROWS][64 B]: Qr's rows
+  uint8_t* rowsf = rowq + QT_ROWS * QT_COLS / 2;                         // two atoms of Qr's scales
   constexpr int NP = QT_ROWS * QT_COLS / 8 / 256;   // 16-byte units of X per thread and tile
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
-  const int64_t col_tiles = (C + QT_COLS - 1) / QT_COLS;
+  const int64_t col_tiles = C / QT_COLS;   // C is a multiple of 128
   const int64_t tiles = ((R + QT_ROWS - 1) / QT_ROWS) * col_tiles;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5, u = t % 16;
   float m = 0.f;
@@ -582,7 +592,7 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_t_kernel(const __nv_bfloat
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
       const int64_t gr = r0 + t / 16 + 16 * p, gc = c0 + 8 * u;
-      const bool in = gr < R && gc < C;   // C is a multiple of 8: a unit is in range or not at all
+      const bool in = gr < R;   // rows past R (R is a multiple of 64) read as zeros
       a[p] = in ? __ldcs(reinterpret_cast<const uint4*>(X + gr * ldx + gc)) : make_uint4(0, 0, 0, 0);
       if constexpr (SWIGLU)
         b[p] = in ? __ldcs(reinterpret_cast<const uint4*>(X + gr * ldx + C + gc)) : make_uint4(0, 0, 0, 0);
@@ -592,7 +602,7 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_t_kernel(const __nv_bfloat
   if (tl < tiles) issue(tl);
   for (; tl < tiles; tl += gridDim.x) {
     const int64_t r0 = (tl / col_tiles) * QT_ROWS, c0 = (tl % col_tiles) * QT_COLS;
-    __syncthreads();   // the previous tile's reads of the shared tile are done
+    __syncthreads();   // the previous tile's shared tile and staged outputs are no longer read
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
       const int row = t / 16 + 16 * p;
@@ -622,37 +632,59 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_t_kernel(const __nv_bfloat
       m = fmaxf(m, m8);
       if constexpr (ROWS) {   // along the rows, from the registers: threads t, t ^ 1 hold a block
         const float m16 = fmaxf(m8, __shfl_xor_sync(0xffffffffu, m8, 1));
-        const int64_t gr = r0 + row, gc = c0 + 8 * u;
         uint32_t code;
         const uint32_t q = nvfp4_half_block(v, m16, s, &code);
-        if (gr < R && gc < C) {
-          *reinterpret_cast<uint32_t*>(Qr + gr * ldqr + gc / 2) = q;
-          if ((u & 1) == 0) sfr[sf_offset(gr, gc / 16, C / 64)] = (uint8_t)code;
+        *reinterpret_cast<uint32_t*>(rowq + row * 64 + 4 * u) = q;
+        if ((u & 1) == 0) {
+          const int kb = u >> 1;   // block of 16 along the row, 0..7
+          rowsf[(kb >> 2) * 512 + 16 * (row % 32) + 4 * (row / 32) + (kb & 3)] = (uint8_t)code;
         }
       }
     }
     __syncthreads();
     const int64_t nx = tl + gridDim.x;   // the next tile's loads fly while this one is quantised
     if (nx < tiles) issue(nx);
-    // along the columns: warp w takes (column group, row block) pairs w + 8 h; lane = column
-    // within the group of 32
+    {   // along the columns: warp w takes the 32 columns 32 (w % 4) + lane, 16-row blocks 4 (w / 4) + i
+      const int c = 32 * (warp & 3) + lane;
 #pragma unroll
-    for (int h = 0; h < QT_ROWS / 16 * QT_COLS / 32 / 8; ++h) {
-      const int pr = warp + 8 * h, cg = pr % 4, blk = pr / 4;
-      const int c = 32 * cg + lane;
-      const int64_t gc = c0 + c;
-      float x[16];
+      for (int i = 0; i < 4; ++i) {
+        const int blk = 4 * (warp >> 2) + i;
+        float x[16];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        if constexpr (SWIGLU) x[k] = tile[(16 * blk + k) * QT_COLS + c];
-        else x[k] = __bfloat162float(tile[(16 * blk + k) * QT_COLS + c]);
-      }
-      if (gc < C && r0 + 16 * blk < R) {
+        for (int k = 0; k < 16; ++k) {
+          if constexpr (SWIGLU) x[k] = tile[(16 * blk + k) * QT_COLS + c];
+          else x[k] = __bfloat162float(tile[(16 * blk + k) * QT_COLS + c]);
+        }
         uint32_t q[2];
-        const uint32_t code = nvfp4_block16(x, s, q);
-        *reinterpret_cast<uint2*>(Q + gc * ldq + (r0 + 16 * blk) / 2) = make_uint2(q[0], q[1]);
-        sf[sf_offset(gc, (r0 + 16 * blk) / 16, R / 64)] = (uint8_t)code;
+        const uint32_t code = nvfp4_block16(x, s, q);   // blocks past R are staged, never stored
+        // 16-byte unit blk / 2 of row c, its place XOR-swizzled by bits 1-2 of c so that a
+        // warp's stores spread over the banks
+        const int js = (blk >> 1) ^ ((c >> 1) & 3);
+        *reinterpret_cast<uint2*>(colq + c * 64 + 16 * js + 8 * (blk & 1)) = make_uint2(q[0], q[1]);
+        colsf[(blk >> 2) * 512 + 16 * (c % 32) + 4 * (c / 32) + (blk & 3)] = (uint8_t)code;
       }
+    }
+    __syncthreads();
+    // the staged outputs, in 16-byte stores: 4 units per destination row, 32 per atom
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i = t + 256 * k, c = i >> 2, j = i & 3;
+      if (r0 + 32 * j < R)
+        __stcs(reinterpret_cast<uint4*>(Q + (c0 + c) * ldq + r0 / 2 + 16 * j),
+               *reinterpret_cast<const uint4*>(colq + c * 64 + 16 * (j ^ ((c >> 1) & 3))));
+      if constexpr (ROWS)   // R is a multiple of 128 here
+        __stcs(reinterpret_cast<uint4*>(Qr + (r0 + c) * ldqr + c0 / 2 + 16 * j),
+               *reinterpret_cast<const uint4*>(rowq + c * 64 + 16 * j));
+    }
+    if (t < 64) {
+      const int at = t >> 5, off = 16 * (t & 31);
+      if (r0 + 64 * at < R)
+        __stcs(reinterpret_cast<uint4*>(sf + ((c0 / 128) * (R / 64) + r0 / 64 + at) * 512 + off),
+               *reinterpret_cast<const uint4*>(colsf + at * 512 + off));
+    } else if (ROWS && t < 128) {
+      const int at = (t - 64) >> 5, off = 16 * (t & 31);
+      __stcs(reinterpret_cast<uint4*>(sfr + ((r0 / 128) * (C / 64) + c0 / 64 + at) * 512 + off),
+             *reinterpret_cast<const uint4*>(rowsf + at * 512 + off));
     }
   }
   if (amax) {
@@ -667,7 +699,9 @@ cudaError_t launch_quantize_nvfp4_t(const void* X, int64_t R, int64_t C, int64_t
                                     float* amax, cudaStream_t st, int sms) {
   const int64_t tiles = ((R + QT_ROWS - 1) / QT_ROWS) * ((C + QT_COLS - 1) / QT_COLS);
   if (tiles <= 0) return cudaSuccess;
-  const size_t smem = (swiglu ? sizeof(float) : sizeof(__nv_bfloat16)) * QT_ROWS * QT_COLS;
+  // the tile, then the staged outputs: Q's codes and scales, Qr's codes and scales
+  const size_t smem = (swiglu ? sizeof(float) : sizeof(__nv_bfloat16)) * QT_ROWS * QT_COLS +
+                      (QT_ROWS * QT_COLS / 2 + 1024) * (Qr ? 2 : 1);
   auto go = [&](auto kernel) {
     if (smem > 48 * 1024) {   // the fp32 tile of silu(G) U: above the default dynamic limit
       const cudaError_t ae = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
