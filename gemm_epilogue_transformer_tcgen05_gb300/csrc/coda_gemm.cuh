@@ -860,6 +860,25 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       float xmax = -INFINITY, xsum = 0.f, xtgt = 0.f;   // online softmax state of this row's tile
       const float ts = p.tensor_scale;
 
+      // RoPE: the rotation table entries of a chunk (16 pairs of this row's position) are
+      // loaded a chunk ahead, the first chunk's before the accumulator is waited for
+      constexpr bool ROPE = C::EPI == EPI_ROPE;
+      float4 rcv[ROPE ? 4 : 1], rsv[ROPE ? 4 : 1];
+      auto rope_fetch = [&](int c) {
+        if constexpr (ROPE) {
+          const int col = n0 + 32 * c;
+          if (col < p.rope_ncols) {
+            const int pos = row % p.rope_seq_len;
+            const size_t base = (size_t)pos * (p.rope_head_dim >> 1) + ((col % p.rope_head_dim) >> 1);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              rcv[j] = __ldg(reinterpret_cast<const float4*>(p.rope_cos + base) + j);
+              rsv[j] = __ldg(reinterpret_cast<const float4*>(p.rope_sin + base) + j);
+            }
+          }
+        }
+      };
+      rope_fetch(0);
       ok = bwait(TFULL_BAR(acc), aph, watch, SITE_EPI_TMEM_FULL);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -1017,14 +1036,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[j] *= sc;
           if (col0 < p.rope_ncols) {
-            const int pos = row % p.rope_seq_len;
-            const int half = p.rope_head_dim >> 1;
-            const int pb = (col0 % p.rope_head_dim) >> 1;
-            const float4* c4 = reinterpret_cast<const float4*>(p.rope_cos + (size_t)pos * half + pb);
-            const float4* s4 = reinterpret_cast<const float4*>(p.rope_sin + (size_t)pos * half + pb);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const float4 cv = __ldg(c4 + j), sv = __ldg(s4 + j);
+              const float4 cv = rcv[j], sv = rsv[j];
               const float cs[4] = {cv.x, cv.y, cv.z, cv.w};
               const float sn[4] = {sv.x, sv.y, sv.z, sv.w};
 #pragma unroll
@@ -1036,6 +1050,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               }
             }
           }
+          if (c + 1 < C::NCHUNK) rope_fetch(c + 1);
         } else if constexpr (C::EPI == EPI_SWIGLU_BWD) {
           const float sc = ts * rs;
           if constexpr (C::OUT_DT == DT_E4M3) {
