@@ -73,13 +73,17 @@ def parse():
     p.add_argument("--nvfp4-pass", action="store_true",
                    help="run only the NVFP4 MLP (H 4096, F 14336): quantise X, then the chain twice (a short "
                         "program for a per-kernel capture)")
+    p.add_argument("--fp8-pass", action="store_true",
+                   help="run only the FP8 MLP (H 4096, F 14336): the chain once for the delayed s_a, then twice "
+                        "(a short program for a per-kernel capture)")
     p.add_argument("--nvfp4-bwd-pass", action="store_true",
                    help="run only the NVFP4 MLP backward (H 4096, F 14336) twice, after its weight preparation "
                         "(a short program for a per-kernel capture)")
     p.add_argument("--row-rms-pass", action="store_true",
                    help="run only the full-row RMS of a [16384, 8192] bf16 tensor, five times (a short program for "
                         "a per-kernel DRAM-bytes capture of the bandwidth-bound reduce)")
-    p.add_argument("--tokens", type=int, default=M_TOK, help="token count of --traffic-pass / --nvfp4-pass")
+    p.add_argument("--tokens", type=int, default=M_TOK,
+                   help="token count of --traffic-pass / --nvfp4-pass / --fp8-pass / --nvfp4-bwd-pass")
     p.add_argument("--compile-compare", action="store_true",
                    help="also time torch.compile of the unfused comparators (compiles on first use)")
     return p.parse_args()
@@ -401,6 +405,38 @@ def nvfp4_pass(args):
     print(json.dumps({"nvfp4_pass": {"tokens": M, "hidden": H, "ffn": F,
                                      "order": "quantise W_gu, W_d, X; chain x2 (row RMS, gate/up GEMM, down GEMM)",
                                      "Y_rms": float(Y.float().pow(2).mean().sqrt())}}), flush=True)
+
+
+def fp8_pass(args):
+    """The FP8 MLP at the LLaMA-3-8B width (row RMS, gate/up e4m3 GEMM + r + SwiGLU + e4m3
+    requantisation + amax, down e4m3 GEMM + residual + partials): once to take the delayed s_a
+    from its amax, then twice, nothing else on the device."""
+    import torch
+
+    import coda_synth as S
+    from gemm_epilogue_transformer_tcgen05_gb300 import coda as C
+
+    C.lib()
+    M, H, F = args.tokens, 4096, 14336
+    fi = S.fp8_mlp_inputs(M, H, F, seed=0)
+    h, X, W, Wd = (fi[k].to("cuda").contiguous() for k in ("h", "Xq", "Wq", "Wdq"))
+    r, amax = torch.empty((M,), device="cuda"), torch.empty((1,), device="cuda")
+    aq = torch.empty((M, F), dtype=torch.uint8, device="cuda")
+    Y = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    P = torch.empty((H // 256, M), device="cuda")
+    s_a = 1.0
+    for i in range(3):
+        C.coda_mlp_fp8(h, X, W, Wd, fi["s_x"], fi["s_w"], fi["s_wd"], s_a, EPS, r, aq, amax, Y, P)
+        if i == 0:
+            torch.cuda.synchronize()
+            s_a = float(amax.item()) / 448.0
+    torch.cuda.synchronize()
+    st, site = C.coda_get_device_status()
+    if st != C.OK:
+        raise RuntimeError(f"device status {st} (site {site})")
+    print(json.dumps({"fp8_pass": {"tokens": M, "hidden": H, "ffn": F,
+                                   "order": "chain x3 (row RMS, gate/up GEMM, down GEMM); the first sets s_a",
+                                   "Y_rms": float(Y.float().pow(2).mean().sqrt())}}), flush=True)
 
 
 def row_rms_pass(args):
@@ -1307,12 +1343,14 @@ def main():
     if args.impl == "reference":
         run_reference(args, world, rank)
         return
-    if args.traffic_pass or args.nvfp4_pass or args.row_rms_pass or args.nvfp4_bwd_pass:
+    if args.traffic_pass or args.nvfp4_pass or args.row_rms_pass or args.nvfp4_bwd_pass or args.fp8_pass:
         if rank == 0:
             if args.traffic_pass:
                 traffic_pass(args)
             elif args.nvfp4_pass:
                 nvfp4_pass(args)
+            elif args.fp8_pass:
+                fp8_pass(args)
             elif args.nvfp4_bwd_pass:
                 import torch
 
