@@ -152,3 +152,41 @@ def test_dropped_stage_in_a_block_scaled_nvfp4_gemm(C):
     assert st2 == C.OK
     ref = O.linear(O.nvfp4_dequantize(qa, sfa, A.s), O.nvfp4_dequantize(qb, sfb, B.s))
     assert_close(f64(out2), ref, 1e-3, "NVFP4 GEMM after a timed-out launch")
+
+
+def test_dropped_stage_in_the_nvfp4_swiglu_output_gemm(C):
+    """The NVFP4 SwiGLU with NVFP4 output, whose scale warps also form half of every tile and
+    stage the next tile's block scales between their output chunks: a dropped stage (operands
+    and scales) ends the launch through the abort path, and the next launch's codes, block
+    scales and amax are bit-identical to a launch made before the fault."""
+    import numpy as np
+    from tests import nvfp4_layout as L
+    M, H, F = 4096, 1024, 1024                            # 128 tiles: more than the CTA pairs
+    g = torch.Generator().manual_seed(72)
+    xh = f64((torch.randn((M, H), generator=g)).to(BF))
+    xw = f64((torch.randn((2 * F, H), generator=g) * 0.03).to(BF))
+    sc = lambda x: float(np.float32(np.max(np.abs(x)) / (6 * 448)))
+    X, _, _ = L.oracle_nvfp4(xh, sc(xh))
+    W, _, _ = L.oracle_nvfp4(xw, sc(xw))
+    r = dev(seeded((M,), 73, std=0.1, mean=1.0))
+
+    def run():
+        out = C.Nvfp4.empty(M, F, 0.01)
+        amax = torch.zeros((1,), device="cuda")
+        C.coda_gemm_epilogue(X, W, [C.OP_TENSOR_SCALE, C.OP_ROW_SCALE, C.OP_SWIGLU, C.OP_AMAX], out,
+                             row_scale=r, tensor_scale=X.s * W.s, amax=amax)
+        return out, amax
+
+    ref, ref_amax = run()
+    assert C.coda_get_device_status()[0] == C.OK
+    C.coda_set_watchdog_ms(200)
+    C.coda_inject_dropped_stage(True)
+    run()
+    st, site = C.coda_get_device_status()
+    assert st == C.ERR_DEVICE_TIMEOUT, st
+    assert site in (1, 2, 3, 4, 5, 6, 7), site
+    C.coda_set_watchdog_ms(2000)
+    got, got_amax = run()
+    assert C.coda_get_device_status()[0] == C.OK
+    assert torch.equal(got.codes, ref.codes) and torch.equal(got.scales, ref.scales)
+    assert torch.equal(got_amax, ref_amax)
