@@ -579,7 +579,7 @@ static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const 
   // B re-read every wave, 537 MB read for 369 MB of compulsory reads).  There A is streamed
   // with evict_first (411 MB).  With K = 2048 the same policy measured slower, so it is kept
   // to long K, and to a B that L2 can hold (at most 48 MB).
-  if (p.group_n == p.n_tiles && (K + var->bk - 1) / var->bk >= 128 &&
+  if (p.group_n == p.n_tiles && (K + bk - 1) / bk >= 128 &&
       n_tiles * (int64_t)var->un * row_bytes(W->dtype, K) <= ((int64_t)48 << 20))
     p.flags |= F_A_STREAM;
   switch (g_inject_once.exchange(0)) {

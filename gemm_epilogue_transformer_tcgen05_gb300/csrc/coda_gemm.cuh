@@ -168,16 +168,14 @@ struct GemmCfg {
   static constexpr bool FP4 = KIND == KIND_NVFP4;
   static constexpr int B_ROWS = UN / CG;                       // B rows (N) held by this CTA
   static constexpr int B_BOX = B_ROWS < 128 ? B_ROWS : 128;    // rows per B copy
-  static constexpr int B_STAGE_BYTES = B_ROWS * BK_BYTES;
+  static constexpr int B_ROW_BYTES = B_ROWS * BK_BYTES;        // this CTA's B for one 128-byte row of K
   // NVFP4 block scales of a stage: one atom per MMA for this CTA's 128 rows of A, and one per
   // MMA and 128 rows of the tile's N for B (each CTA of a pair holds all of them)
   static constexpr int SF_A_BYTES = FP4 ? KSTEPS * 512 : 0;
   static constexpr int SF_B_BYTES = FP4 ? KSTEPS * 512 * (UN / 128) : 0;
-  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES + SF_A_BYTES + SF_B_BYTES;
+  static constexpr int SB1 = A_STAGE_BYTES + B_ROW_BYTES + SF_A_BYTES + SF_B_BYTES;   // a stage of one K row
   static constexpr int PAIR_ROWS = BM * CG;                    // output rows per tile
   static constexpr int OP_BYTES = KIND == KIND_TF32 ? 4 : KIND == KIND_BF16 ? 2 : 1;
-  static constexpr int BK = FP4 ? 2 * BK_BYTES : BK_BYTES / OP_BYTES;   // K elements per stage
-  static constexpr int K_COORD = FP4 ? BK_BYTES : BK;   // TMA K step per stage (NVFP4 maps count bytes)
   static constexpr bool DUAL = EPI == EPI_SWIGLU;
   static constexpr int BN_OUT = DUAL ? UN / 2 : UN;  // output columns per tile
   static constexpr int NCHUNK = BN_OUT / 32;
@@ -218,6 +216,29 @@ struct GemmCfg {
                                     : (NX > 0 ? 2 : 128 / (32 * dt_bytes(OUT_DT)));
   static constexpr int SIDE_BYTES = NSS * NS * SSLOT;
   static constexpr int SMEM_FREE = MAX_SMEM - 1024 - BAR_BYTES;   // for the stages and the epilogue
+  // Pipeline stages of sb bytes that fit beside the epilogue's staging (with the store width
+  // chosen below for that stage size).
+  static constexpr int stages_with(int sb) {
+    const int narrow = fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + 2 * OUTSET), sb, MAX_STAGES);
+    int ow = 1;
+    for (int w = 4; w >= 2; w /= 2) {
+      if (ow == 1 && w <= OW_MAX && NCHUNK % w == 0 &&
+          fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + 2 * w * OUTSET), sb, MAX_STAGES) >= narrow)
+        ow = w;
+    }
+    return fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + 2 * ow * OUTSET), sb, MAX_STAGES);
+  }
+  // K-major bf16 and e4m3 operands take two 128-byte rows of K per stage (64 KB stages) where
+  // three such stages fit: the same bytes in flight as six stages of one row, with half the
+  // barrier round trips and copies per byte (measured: the gate/up GEMM of the block forward
+  // 5.6% faster, the down GEMM 4.6%; with two stages, G1 13% slower, so it keeps one row).
+  static constexpr bool KROWS2_OK = !FP4 && !A_MN && !B_MN && KIND != KIND_TF32;
+  static constexpr int KROWS = (KROWS2_OK && stages_with(2 * SB1) >= 3) ? 2 : 1;
+  static constexpr int A_BYTES = A_STAGE_BYTES * KROWS;          // this CTA's A in a stage
+  static constexpr int B_STAGE_BYTES = B_ROW_BYTES * KROWS;
+  static constexpr int STAGE_BYTES = KROWS * SB1;
+  static constexpr int BK = FP4 ? 2 * BK_BYTES : KROWS * BK_BYTES / OP_BYTES;   // K elements per stage
+  static constexpr int K_COORD = FP4 ? BK_BYTES : BK;   // TMA K step per stage (NVFP4 maps count bytes)
   static constexpr int S_NARROW =
       fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + 2 * OUTSET), STAGE_BYTES, MAX_STAGES);   // one chunk per store
   static constexpr bool fits_ow(int ow) {
@@ -646,10 +667,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           } else {
             const uint32_t fb = FULL_BAR(stage);
             const uint32_t sa = sm_stage + stage * C::STAGE_BYTES;
-            const uint32_t sb = sa + A_STAGE_BYTES;
+            const uint32_t sb = sa + C::A_BYTES;
             const int k0 = kb * C::K_COORD;
             // the leader's full barrier counts the operand bytes of both CTAs of a pair
-            if (leader) ptx::mbar_arrive_expect_tx(fb, C::CG * (A_STAGE_BYTES + C::B_STAGE_BYTES));
+            if (leader) ptx::mbar_arrive_expect_tx(fb, C::CG * (C::A_BYTES + C::B_STAGE_BYTES));
             auto load = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1, uint64_t pol) {
               if constexpr (C::CG == 2)
                 ptx::tma_load_2d_pair(dst, m, c0, c1, ptx::mapa(fb, 0), pol);
@@ -660,8 +681,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
               for (int j = 0; j < BM / C::MN_ATOM; ++j)
                 load(sa + C::MN_ATOM_BYTES * j, &tmA, m0 + C::MN_ATOM * j, k0, normal);
-            } else {
-              load(sa, &tmA, k0, m0, normal);
+            } else {   // KROWS rows of K, each its own 128-byte-swizzled block of 128 rows
+#pragma unroll
+              for (int a = 0; a < C::KROWS; ++a)
+                load(sa + a * A_STAGE_BYTES, &tmA, k0 + a * (BK_BYTES / C::OP_BYTES), m0, normal);
             }
             // B: this CTA's B_ROWS rows of the tile's UN (SwiGLU: UN / 2 gate rows, then up rows)
             if constexpr (C::B_MN) {
@@ -676,7 +699,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const int off = ((int)rank * (C::B_ROWS / C::B_BOX) + h) * C::B_BOX;   // row offset in the tile
                 const int row = C::DUAL ? (off < HALF ? nb * HALF + off : p.up_offset + nb * HALF + off - HALF)
                                         : nb * C::UN + off;
-                load(sb + C::B_BOX * BK_BYTES * h, &tmB, k0, row, keep);
+#pragma unroll
+                for (int a = 0; a < C::KROWS; ++a)
+                  load(sb + a * C::B_ROW_BYTES + C::B_BOX * BK_BYTES * h, &tmB, k0 + a * (BK_BYTES / C::OP_BYTES), row,
+                       keep);
               }
             }
             if constexpr (C::FP4) {
@@ -745,7 +771,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
           ptx::tc_fence_after();
           const uint32_t sa = sm_stage + stage * C::STAGE_BYTES;
-          const uint32_t sb = sa + A_STAGE_BYTES;
+          const uint32_t sb = sa + C::A_BYTES;
           if constexpr (C::FP4) {
             // the scale warps of both CTAs have written this stage's block scales into TMEM
             // (A: 4 columns per MMA; B: 4 per MMA and 128 rows of N)
@@ -766,11 +792,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
           } else {
 #pragma unroll
-            for (int k = 0; k < KSTEPS; ++k) {
+            for (int k = 0; k < KSTEPS * C::KROWS; ++k) {
+              const int kr = k / KSTEPS, ks = k % KSTEPS;   // row of K in the stage, 32-byte step in it
               const uint64_t ad = C::A_MN ? smem_desc(sa + k * C::UMMA_K * 128, C::MN_ATOM_BYTES, 1024)
-                                          : smem_desc(sa + k * 32, 16, 1024);
+                                          : smem_desc(sa + kr * A_STAGE_BYTES + ks * 32, 16, 1024);
               const uint64_t bd = C::B_MN ? smem_desc(sb + k * C::UMMA_K * 128, C::MN_ATOM_BYTES, 1024)
-                                          : smem_desc(sb + k * 32, 16, 1024);
+                                          : smem_desc(sb + kr * C::B_ROW_BYTES + ks * 32, 16, 1024);
               ptx::umma<C::KIND, C::CG>(d_tmem, ad, bd, C::IDESC, (kb != kb0 || k != 0) ? 1u : 0u);
             }
           }
@@ -1259,7 +1286,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       auto stage_scales = [&]() {
         if (!__all_sync(0xffffffffu, bwait(SFULL_BAR(stage), phase, watch, SITE_SCALES_FULL))) return false;
         // atom row `lane` of a scale atom holds rows lane + 32 i (i = 0..3), 4 scales each
-        const uint32_t ssf = sm_stage + stage * C::STAGE_BYTES + A_STAGE_BYTES + C::B_STAGE_BYTES + 16 * lane;
+        const uint32_t ssf = sm_stage + stage * C::STAGE_BYTES + C::A_BYTES + C::B_STAGE_BYTES + 16 * lane;
         const uint32_t tcol = tmem_base + ((32u * q) << 16) + C::ACC * C::UN + stage * C::SF_COLS;
 #pragma unroll
         for (int k = 0; k < KSTEPS; ++k)
@@ -1356,7 +1383,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const uint32_t w = *peer_iters;
       const int n_l = prod_iters, n_p = (int)(w & 0x7FFFFFFFu);
       const bool skip_l = prod_skip0, skip_p = (w >> 31) != 0;
-      constexpr uint32_t PEER_BYTES = A_STAGE_BYTES + C::B_STAGE_BYTES;
+      constexpr uint32_t PEER_BYTES = C::A_BYTES + C::B_STAGE_BYTES;
       for (int i = max(0, min(n_l, n_p) - C::STAGES); i < max(n_l, n_p); ++i) {
         const bool by_l = i < n_l && !(skip_l && i == 0);
         const bool by_p = i < n_p && !(skip_p && i == 0);
