@@ -467,14 +467,14 @@ static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const 
   if (fp4)
     st = encode_2d(&L.tmA, CODA_E4M3, A->ptr, K / 2, M, A->ld / 2, 128, 128);
   else if (a_mn)
-    st = encode_2d(&L.tmA, A->dtype, A->ptr, M, K, A->ld, mn_atom, bk);
+    st = encode_2d(&L.tmA, A->dtype, A->ptr, M, K, A->ld, mn_atom, (uint32_t)var->bk);   // one stage's K rows
   else
     st = encode_2d(&L.tmA, A->dtype, A->ptr, K, M, A->ld, bk, 128);
   if (st != CODA_OK) return st;
   if (fp4)
     st = encode_2d(&L.tmB, CODA_E4M3, W->ptr, K / 2, W->rows, W->ld / 2, 128, (uint32_t)var->b_box);
   else if (b_mn)
-    st = encode_2d(&L.tmB, W->dtype, W->ptr, W->rows, K, W->ld, mn_atom, bk);
+    st = encode_2d(&L.tmB, W->dtype, W->ptr, W->rows, K, W->ld, mn_atom, (uint32_t)var->bk);
   else
     st = encode_2d(&L.tmB, W->dtype, W->ptr, K, W->rows, W->ld, bk, (uint32_t)var->b_box);
   if (st != CODA_OK) return st;
@@ -547,8 +547,9 @@ static int gemm_epilogue_impl(const coda_tensor* A, const coda_tensor* W, const 
     // and the reduce-adds cost more than the idle groups otherwise
     const double eff1 = (double)tiles / (double)(((tiles + groups - 1) / groups) * groups);
     if (epi == EPI_STORE && out->dtype == CODA_F32 && eff1 < 0.75) {
+      const int64_t k_rows = (K + bk - 1) / bk;   // 128-byte rows of K: each slice keeps at least 32
       for (int sk = 1; sk <= 8; ++sk) {
-        if (sk > 1 && num_kb / sk < 32) break;
+        if (sk > 1 && k_rows / sk < 32) break;
         const int64_t work = tiles * sk;
         const double eff = (double)work / (double)(((work + groups - 1) / groups) * groups);
         const double score = eff - 0.02 * (sk - 1);
