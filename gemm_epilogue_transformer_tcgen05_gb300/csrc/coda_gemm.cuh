@@ -218,15 +218,15 @@ struct GemmCfg {
   static constexpr int SMEM_FREE = MAX_SMEM - 1024 - BAR_BYTES;   // for the stages and the epilogue
   // Pipeline stages of sb bytes that fit beside the epilogue's staging (with the store width
   // chosen below for that stage size).
-  static constexpr int stages_with(int sb) {
-    const int narrow = fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + 2 * OUTSET), sb, MAX_STAGES);
+  static constexpr int stages_with(int sb, int osets = 2) {
+    const int narrow = fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + osets * OUTSET), sb, MAX_STAGES);
     int ow = 1;
     for (int w = 4; w >= 2; w /= 2) {
       if (ow == 1 && w <= OW_MAX && NCHUNK % w == 0 &&
-          fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + 2 * w * OUTSET), sb, MAX_STAGES) >= narrow)
+          fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + osets * w * OUTSET), sb, MAX_STAGES) >= narrow)
         ow = w;
     }
-    return fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + 2 * ow * OUTSET), sb, MAX_STAGES);
+    return fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + osets * ow * OUTSET), sb, MAX_STAGES);
   }
   // bf16 and e4m3 operands take two K rows per stage (64 KB stages) where three such stages
   // fit: the same bytes in flight as six stages of one row, with half the barrier round trips
@@ -235,20 +235,24 @@ struct GemmCfg {
   // forward 5.6% faster, the down GEMM 4.6%, the block backward 2.3%; with two stages, G1 13%
   // slower, so it keeps one row.
   static constexpr bool KROWS2_OK = !FP4 && KIND != KIND_TF32;
-  static constexpr int KROWS = (KROWS2_OK && stages_with(2 * SB1) >= 3) ? 2 : 1;
+  // A program whose double-buffered output staging leaves room for only two such stages (G1,
+  // with its second output) stages its outputs through one set instead, waiting for each
+  // store to leave shared memory before the next (G1: 98.9 -> 95.9 us against one K row).
+  static constexpr int KROWS = (KROWS2_OK && (stages_with(2 * SB1) >= 3 || stages_with(2 * SB1, 1) >= 3)) ? 2 : 1;
+  static constexpr int OSETS = (KROWS == 2 && stages_with(2 * SB1) < 3) ? 1 : 2;   // output staging sets
+  static_assert(!EARLY || OSETS == 2, "the NVFP4 SwiGLU output alternates two staging sets");
   static constexpr int A_BYTES = A_STAGE_BYTES * KROWS;          // this CTA's A in a stage
   static constexpr int B_STAGE_BYTES = B_ROW_BYTES * KROWS;
   static constexpr int STAGE_BYTES = KROWS * SB1;
   static constexpr int BK = FP4 ? 2 * BK_BYTES : KROWS * BK_BYTES / OP_BYTES;   // K elements per stage
   static constexpr int K_COORD = FP4 ? BK_BYTES : BK;   // TMA K step per stage (NVFP4 maps count bytes)
   static constexpr int S_NARROW =
-      fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + 2 * OUTSET), STAGE_BYTES, MAX_STAGES);   // one chunk per store
+      fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + OSETS * OUTSET), STAGE_BYTES, MAX_STAGES);   // one chunk per store
   static constexpr bool fits_ow(int ow) {
     return ow <= OW_MAX && NCHUNK % ow == 0 &&
-           fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + 2 * ow * OUTSET), STAGE_BYTES, MAX_STAGES) >= S_NARROW;
+           fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + OSETS * ow * OUTSET), STAGE_BYTES, MAX_STAGES) >= S_NARROW;
   }
   static constexpr int OW = fits_ow(4) ? 4 : fits_ow(2) ? 2 : 1;
-  static constexpr int OSETS = 2;
   static constexpr int OUTSET_W = OW * OUTSET;               // one staging set: OW chunks of each output
   static constexpr int RB_OUT = OW * 32 * dt_bytes(OUT_DT);  // staging row bytes of the main output
   static constexpr int RB_X = OW * 64;                       // ... of the bf16 aux output
