@@ -196,8 +196,9 @@ struct GemmCfg {
   // side inputs are prefetched NSS chunks ahead (one staging set per chunk in flight); the
   // SwiGLU backward, with two side inputs and two outputs per chunk, goes deeper, except with
   // NVFP4 operands, whose larger stages leave the shared memory for two
-  static constexpr int NSS = (EPI == EPI_SWIGLU_BWD && (KIND != KIND_NVFP4 || UN == 128)) ? 4 : 2;
-  static_assert(NCHUNK % NSS == 0, "a chunk and the next tile's chunk NCHUNK later share a ring slot");
+  static constexpr int NSS0 = (EPI == EPI_SWIGLU_BWD && (KIND != KIND_NVFP4 || UN == 128)) ? 4 : 2;
+  // (NSS itself is chosen below, with the pipeline stages: one chunk ahead where that is what
+  // buys three two-row stages)
   // NVFP4: four scale warps write the block scales into TMEM (see the kernel)
   static constexpr int SF_WARPS = FP4 ? 4 : 0;
   // NVFP4 SwiGLU with NVFP4 output: the scale warps also form half of each tile's output
@@ -214,19 +215,19 @@ struct GemmCfg {
   static constexpr int OW_MAX = (OUT_DT == DT_E2M1 || NO == 0 || OUT_DT == DT_F32)
                                     ? 1
                                     : (NX > 0 ? 2 : 128 / (32 * dt_bytes(OUT_DT)));
-  static constexpr int SIDE_BYTES = NSS * NS * SSLOT;
   static constexpr int SMEM_FREE = MAX_SMEM - 1024 - BAR_BYTES;   // for the stages and the epilogue
   // Pipeline stages of sb bytes that fit beside the epilogue's staging (with the store width
   // chosen below for that stage size).
-  static constexpr int stages_with(int sb, int osets = 2) {
-    const int narrow = fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + osets * OUTSET), sb, MAX_STAGES);
+  static constexpr int stages_with(int sb, int osets = 2, int nss = NSS0) {
+    const int side = nss * NS * SSLOT;
+    const int narrow = fit_stages(SMEM_FREE - OUT_WARPS * (side + osets * OUTSET), sb, MAX_STAGES);
     int ow = 1;
     for (int w = 4; w >= 2; w /= 2) {
       if (ow == 1 && w <= OW_MAX && NCHUNK % w == 0 &&
-          fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + osets * w * OUTSET), sb, MAX_STAGES) >= narrow)
+          fit_stages(SMEM_FREE - OUT_WARPS * (side + osets * w * OUTSET), sb, MAX_STAGES) >= narrow)
         ow = w;
     }
-    return fit_stages(SMEM_FREE - OUT_WARPS * (SIDE_BYTES + osets * ow * OUTSET), sb, MAX_STAGES);
+    return fit_stages(SMEM_FREE - OUT_WARPS * (side + osets * ow * OUTSET), sb, MAX_STAGES);
   }
   // bf16 and e4m3 operands take two K rows per stage (64 KB stages) where three such stages
   // fit: the same bytes in flight as six stages of one row, with half the barrier round trips
@@ -235,11 +236,18 @@ struct GemmCfg {
   // forward 5.6% faster, the down GEMM 4.6%, the block backward 2.3%; with two stages, G1 13%
   // slower, so it keeps one row.
   static constexpr bool KROWS2_OK = !FP4 && KIND != KIND_TF32;
-  // A program whose double-buffered output staging leaves room for only two such stages (G1,
-  // with its second output) stages its outputs through one set instead, waiting for each
-  // store to leave shared memory before the next (G1: 98.9 -> 95.9 us against one K row).
-  static constexpr int KROWS = (KROWS2_OK && (stages_with(2 * SB1) >= 3 || stages_with(2 * SB1, 1) >= 3)) ? 2 : 1;
-  static constexpr int OSETS = (KROWS == 2 && stages_with(2 * SB1) < 3) ? 1 : 2;   // output staging sets
+  // A program whose epilogue staging leaves room for only two such stages gives up first the
+  // second output staging set (waiting for each store to leave shared memory before the next:
+  // G1, with its second output, 98.9 -> 95.9 us), then the side-input prefetch depth (one chunk
+  // ahead: the SwiGLU and RMSNorm backward GEMMs, the block backward 2.117 -> 2.060 ms).  The
+  // three-stage two-row pipeline is worth more to them than the deeper epilogue buffers.
+  static constexpr int CFG = !KROWS2_OK ? 0 : stages_with(2 * SB1) >= 3 ? 1 : stages_with(2 * SB1, 1) >= 3 ? 2
+                             : (NS > 0 && stages_with(2 * SB1, 1, 1) >= 3) ? 3 : 0;
+  static constexpr int KROWS = CFG > 0 ? 2 : 1;
+  static constexpr int OSETS = CFG >= 2 ? 1 : 2;   // output staging sets
+  static constexpr int NSS = CFG == 3 ? 1 : NSS0;
+  static_assert(NCHUNK % NSS == 0, "a chunk and the next tile's chunk NCHUNK later share a ring slot");
+  static constexpr int SIDE_BYTES = NSS * NS * SSLOT;
   static_assert(!EARLY || OSETS == 2, "the NVFP4 SwiGLU output alternates two staging sets");
   static constexpr int A_BYTES = A_STAGE_BYTES * KROWS;          // this CTA's A in a stage
   static constexpr int B_STAGE_BYTES = B_ROW_BYTES * KROWS;
