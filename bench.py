@@ -911,12 +911,17 @@ def other_workloads(torch, C, S, args, stream):
     fold()
     fwd_fold = lambda: C.coda_block_forward(d["O"], d["R"], d["W_o"], Wf, d["W_d"], EPS, h, r, a, Y, wsf,
                                             stream=stream)
+    fwd_bc = lambda: C.coda_block_forward(d["O"], d["R"], d["W_o"], d["W_gu"], d["W_d"], EPS, h, r, a, Y, wsf,
+                                          g=d["g"], u=u, stream=stream)
+    ms_bc = _time(torch, fwd_bc, stream, steps)        # the headline chain, timed again beside it
     ms_ff = _time(torch, fwd_fold, stream, steps)
     ms_fold = _time(torch, fold, stream, steps)
     out["block_forward_folded_gain"] = {"ms": ms_ff, "tokens_per_s": M / (ms_ff * 1e-3), "fold_ms": ms_fold,
-                                        "plus_fold_ms": ms_ff + ms_fold,
+                                        "plus_fold_ms": ms_ff + ms_fold, "broadcast_ms_same_section": ms_bc,
                                         "note": "C1 with W_gu' = W_gu diag(g) folded beforehand (timed on its own): "
-                                                "G1 stores h only, G2 reads h; the headline broadcasts g instead"}
+                                                "G1 stores h only, G2 reads h; the headline broadcasts g instead "
+                                                "(broadcast_ms_same_section: the headline chain timed just before, "
+                                                "under the same clocks)"}
     del Wf
     del d, h, u, r, a, Y, Z, e, dh, dO, dW_o, dW_gu, dW_d, dg, c, wsb, wsf
     torch.cuda.empty_cache()
