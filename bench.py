@@ -671,6 +671,7 @@ def run_coda(args, world, rank, local):
     compare = None
     if not args.no_compare and rank == 0:
         compare = unfused_compare(torch, d, {"h": h, "r": r, "a": a, "Y": Y}, inp, stream, args)
+        compare["backward"] = backward_compare(torch, C, S, stream)
 
     if rank != 0:
         if dist is not None:
@@ -1340,6 +1341,48 @@ def unfused_compare(torch, d, fused, inp, stream, args):
             "max_rel_err_unfused_torch_vs_oracle": errs["Y"]["unfused_torch"],
             "max_rel_err_vs_oracle": errs, "error_rows": 256,
             "error_metric": "max_i |x_i - ref_i| / max(|ref_i|, rms(ref)) against the fp64 oracle's plain chain"}
+
+
+def backward_compare(torch, C, S, stream):
+    """The block backward's row outputs (dh = dR, dO, and e) against the fp64 oracle on 256
+    sampled rows: the fused chain (training-mode forward, then coda_block_backward) and torch
+    autograd through the unfused bf16 chain.  The weight gradients sum over every row; the
+    tests check them (on exact inputs at full size)."""
+    import numpy as np
+
+    import oracle as O
+    M, H, F = M_TOK, HID, FFN
+    BF = torch.bfloat16
+    inp = S.block_inputs(M, H, F, seed=0, with_grad=True)
+    d = {k: inp[k].to("cuda").contiguous() for k in ("O", "R", "W_o", "W_gu", "W_d", "g", "dY")}
+    h, u, a, Y = (torch.empty((M, n), dtype=BF, device="cuda") for n in (H, H, F, H))
+    r = torch.empty((M,), device="cuda")
+    Z = torch.empty((M, 2 * F), dtype=BF, device="cuda")
+    wsf = torch.empty((C.coda_workspace_size(C.WS_BLOCK_FWD, M, H, F) // 4,), device="cuda")
+    C.coda_block_forward(d["O"], d["R"], d["W_o"], d["W_gu"], d["W_d"], EPS, h, r, a, Y, wsf, Z=Z, g=d["g"], u=u,
+                         stream=stream)
+    e = torch.empty((M, 2 * F), dtype=BF, device="cuda")
+    dh, dO = torch.empty((M, H), dtype=BF, device="cuda"), torch.empty((M, H), dtype=BF, device="cuda")
+    dW_o, dW_gu, dW_d = (torch.empty(s, device="cuda") for s in ((H, H), (2 * F, H), (H, F)))
+    dg, c = torch.empty((H,), device="cuda"), torch.empty((M,), device="cuda")
+    wsb = torch.empty((C.coda_workspace_size(C.WS_BLOCK_BWD, M, H, F) // 4,), device="cuda")
+    C.coda_block_backward(d["O"], d["W_o"], d["W_gu"], d["W_d"], d["g"], h, r, Z, a, d["dY"], e, dh, dO, dW_o,
+                          dW_gu, dW_d, dg, c, wsb, stream=stream)
+    torch.cuda.synchronize()
+    leaf = {k: d[k].clone().requires_grad_(k in ("O", "R")) for k in ("O", "R", "W_o", "W_gu", "W_d", "g")}
+    unfused_chain(torch, leaf, F).backward(d["dY"])
+    torch.cuda.synchronize()
+    rows = np.sort(np.random.default_rng(1).choice(M, size=256, replace=False))
+    x = {k: inp[k].to(torch.float64).numpy() for k in ("O", "R", "W_o", "W_gu", "W_d", "g", "dY")}
+    f = O.block_forward(x["O"][rows], x["R"][rows], x["W_o"], x["g"], x["W_gu"], x["W_d"], EPS)
+    b = O.block_backward_fused(f, x["O"][rows], x["W_o"], x["g"], x["W_gu"], x["W_d"], x["dY"][rows])
+    rows_t = torch.from_numpy(rows).cuda()
+    pick = lambda t: t.detach().index_select(0, rows_t).double().cpu().numpy()
+    errs = {"dh": {"fused": O.max_rel_err(pick(dh), b["dh"]), "unfused_torch": O.max_rel_err(pick(leaf["R"].grad), b["dh"])},
+            "dO": {"fused": O.max_rel_err(pick(dO), b["dO"]), "unfused_torch": O.max_rel_err(pick(leaf["O"].grad), b["dO"])},
+            "e": {"fused": O.max_rel_err(pick(e), b["e"])}}
+    return {"max_rel_err_vs_oracle": errs, "error_rows": 256,
+            "note": "row outputs of the block backward; e = r [dG | dU] exists in the fused chain only"}
 
 
 def main():
