@@ -308,9 +308,8 @@ CODA_API int coda_block_forward(const coda_block_fwd* io, void* stream);
  *     H = 2048).  Larger problems, or a non-NULL workspace, return CODA_ERR_SHAPE and
  *     launch nothing.
  *   - Set-up: the first call on each device (in each CUDA context of that device) looks up
- *     the array's device address, with that device current, and caches it; make that first
- *     call before any stream capture.  After a device reset the next call sees a new
- *     context and looks the address up again.
+ *     the array's device address, with that device current, and caches it.  After a device
+ *     reset the next call sees a new context and looks the address up again.
  *   - Sharing: all calls on a device use the same array, which keeps the last call's
  *     contents.  Nothing in it needs clearing (each call writes every partial it reads
  *     before reading it), but calls that overlap on the GPU (unordered streams) race on it.
