@@ -548,26 +548,38 @@ cudaError_t launch_quantize_nvfp4(const void* X, int64_t R, int64_t K, int64_t l
 //     16-row blocks of one column.
 constexpr int QT_ROWS = 128, QT_COLS = 128;
 
-// NVFP4 codes of 8 values x with tensor scale s, given the amax of their block of 16: the
-// decisions of nvfp4_block16, taken on this thread's half of the block.  Returns the 8 codes
-// (element j in nibble j) and the block scale's e4m3 byte in *code.
-__device__ __forceinline__ uint32_t nvfp4_half_block(const float* x, float amax, float s, uint32_t* code) {
-  const float u = __fdiv_rn(amax, __fmul_rn(6.0f, s));
-  const uint16_t code2 = ptx::cvt_e4m3x2(u, 0.0f);
+// The transposed pass's own NVFP4 decisions, cheaper than nvfp4_block16's (the pass issues
+// about 20 instructions per element and is bound by instruction issue, not by DRAM):
+//   sf = e4m3(amax * inv6s), inv6s = 1 / (6 s) rounded once on the host, and
+//   q = e2m1(x * rcp(sf s)) with the hardware's approximate reciprocal (at most one ulp from
+// 1 / (sf s)).  Both stay within a few fp32 roundings of the exact quotients, so a decision
+// can differ from exact arithmetic only for a value that close to a rounding midpoint.
+__device__ __forceinline__ float qt_rcp(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+// e4m3 block scale of a block with maximum magnitude amax (its byte in *code), and the
+// multiplier that takes the block's values to e2m1 code units (0 for a zero scale)
+__device__ __forceinline__ float qt_scale(float amax, float inv6s, float s, uint32_t* code) {
+  const uint16_t code2 = ptx::cvt_e4m3x2(amax * inv6s, 0.0f);
   float sfv, zero;
   ptx::e4m3x2_to_f32(code2, sfv, zero);
-  const float d = __fmul_rn(sfv, s);
-  const float rd = d > 0.f ? __frcp_rn(d) : 0.f;
+  *code = code2 & 0xFFu;
+  const float d = sfv * s;
+  return d > 0.f ? qt_rcp(d) : 0.f;
+}
+// codes of 8 values times the multiplier rd (element j in nibble j)
+__device__ __forceinline__ uint32_t qt_codes8(const float* x, float rd) {
   float y[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) y[j] = __fmul_rn(x[j], rd);
-  *code = code2 & 0xFFu;
+  for (int j = 0; j < 8; ++j) y[j] = x[j] * rd;
   return ptx::cvt_e2m1x8(y);
 }
 
 template <bool SWIGLU, bool ROWS>
 __global__ void __launch_bounds__(256, SWIGLU ? 2 : 3) quantize_nvfp4_t_kernel(const __nv_bfloat16* __restrict__ X, int64_t R,
-                                                                  int64_t C, int64_t ldx, float s,
+                                                                  int64_t C, int64_t ldx, float s, float inv6s,
                                                                   uint8_t* __restrict__ Q, int64_t ldq,
                                                                   uint8_t* __restrict__ sf, uint8_t* __restrict__ Qr,
                                                                   int64_t ldqr, uint8_t* __restrict__ sfr,
@@ -633,8 +645,8 @@ __global__ void __launch_bounds__(256, SWIGLU ? 2 : 3) quantize_nvfp4_t_kernel(c
       if constexpr (ROWS) {   // along the rows, from the registers: threads t, t ^ 1 hold a block
         const float m16 = fmaxf(m8, __shfl_xor_sync(0xffffffffu, m8, 1));
         uint32_t code;
-        const uint32_t q = nvfp4_half_block(v, m16, s, &code);
-        *reinterpret_cast<uint32_t*>(rowq + row * 64 + 4 * u) = q;
+        const float rd = qt_scale(m16, inv6s, s, &code);
+        *reinterpret_cast<uint32_t*>(rowq + row * 64 + 4 * u) = qt_codes8(v, rd);
         if ((u & 1) == 0) {
           const int kb = u >> 1;   // block of 16 along the row, 0..7
           rowsf[(kb >> 2) * 512 + 16 * (row % 32) + 4 * (row / 32) + (kb & 3)] = (uint8_t)code;
@@ -644,24 +656,59 @@ __global__ void __launch_bounds__(256, SWIGLU ? 2 : 3) quantize_nvfp4_t_kernel(c
     __syncthreads();
     const int64_t nx = tl + gridDim.x;   // the next tile's loads fly while this one is quantised
     if (nx < tiles) issue(nx);
-    {   // along the columns: warp w takes the 32 columns 32 (w % 4) + lane, 16-row blocks 4 (w / 4) + i
-      const int c = 32 * (warp & 3) + lane;
+    {   // along the columns: warp w takes the column pairs (2 cp, 2 cp + 1), cp = 32 (w % 2) +
+        // lane (a warp's loads cover 128 or 256 contiguous bytes of a row, conflict-free), and
+        // the two 16-row blocks 2 j, 2 j + 1, j = w / 2: 32 rows of each of its two columns
+      const int cp = 32 * (warp & 1) + lane, j = warp >> 1;
+      uint32_t q[2][4], code[2][2];   // [column h][...]: codes of blocks 2 j, 2 j + 1; their scales
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int blk = 4 * (warp >> 2) + i;
-        float x[16];
+      for (int i = 0; i < 2; ++i) {   // block 2 j + i: 16 rows of both columns
+        if constexpr (SWIGLU) {
+          float x[2][16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          if constexpr (SWIGLU) x[k] = tile[(16 * blk + k) * QT_COLS + c];
-          else x[k] = __bfloat162float(tile[(16 * blk + k) * QT_COLS + c]);
+          for (int k = 0; k < 16; ++k) {
+            const float2 v2 = *reinterpret_cast<const float2*>(tile + (32 * j + 16 * i + k) * QT_COLS + 2 * cp);
+            x[0][k] = v2.x;
+            x[1][k] = v2.y;
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float am = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) am = fmaxf(am, fabsf(x[h][k]));
+            const float rd = qt_scale(am, inv6s, s, &code[h][i]);
+            q[h][2 * i] = qt_codes8(x[h], rd);
+            q[h][2 * i + 1] = qt_codes8(x[h] + 8, rd);
+          }
+        } else {   // the two columns' bf16 values stay packed until each is quantised
+          uint32_t w2[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            w2[k] = *reinterpret_cast<const uint32_t*>(tile + (32 * j + 16 * i + k) * QT_COLS + 2 * cp);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float x[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) x[k] = __uint_as_float(h ? (w2[k] & 0xFFFF0000u) : (w2[k] << 16));
+            float am = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) am = fmaxf(am, fabsf(x[k]));
+            const float rd = qt_scale(am, inv6s, s, &code[h][i]);
+            q[h][2 * i] = qt_codes8(x, rd);
+            q[h][2 * i + 1] = qt_codes8(x + 8, rd);
+          }
         }
-        uint32_t q[2];
-        const uint32_t code = nvfp4_block16(x, s, q);   // blocks past R are staged, never stored
-        // 16-byte unit blk / 2 of row c, its place XOR-swizzled by bits 1-2 of c so that a
-        // warp's stores spread over the banks
-        const int js = (blk >> 1) ^ ((c >> 1) & 3);
-        *reinterpret_cast<uint2*>(colq + c * 64 + 16 * js + 8 * (blk & 1)) = make_uint2(q[0], q[1]);
-        colsf[(blk >> 2) * 512 + 16 * (c % 32) + 4 * (c / 32) + (blk & 3)] = (uint8_t)code;
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {   // column c = 2 cp + h
+        const int c = 2 * cp + h;
+        // blocks 2 j, 2 j + 1 of column c form 16-byte unit j of row c, its place XOR-swizzled
+        // by bits 1-2 of c (blocks past R are staged, never stored)
+        *reinterpret_cast<uint4*>(colq + c * 64 + 16 * (j ^ ((c >> 1) & 3))) =
+            make_uint4(q[h][0], q[h][1], q[h][2], q[h][3]);
+        // their scales: bytes 2 (j % 2) and 2 (j % 2) + 1 of row c's group in atom j / 2
+        *reinterpret_cast<uint16_t*>(colsf + (j >> 1) * 512 + 16 * (c % 32) + 4 * (c / 32) + 2 * (j & 1)) =
+            (uint16_t)(code[h][0] | (code[h][1] << 8));
       }
     }
     __syncthreads();
@@ -724,7 +771,8 @@ cudaError_t launch_quantize_nvfp4_t(const void* X, int64_t R, int64_t C, int64_t
     cfg.stream = st;
     cfg.attrs = at;
     cfg.numAttrs = g_launch_overlap ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kernel, reinterpret_cast<const __nv_bfloat16*>(X), R, C, ldx, s,
+    const float inv6s = (float)(1.0 / (6.0 * (double)s));
+    return cudaLaunchKernelEx(&cfg, kernel, reinterpret_cast<const __nv_bfloat16*>(X), R, C, ldx, s, inv6s,
                               reinterpret_cast<uint8_t*>(Q), ldq_bytes, sf, reinterpret_cast<uint8_t*>(Qr), ldqr_bytes,
                               sfr, reinterpret_cast<unsigned int*>(amax));
   };

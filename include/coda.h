@@ -495,8 +495,12 @@ CODA_API int coda_quantize_nvfp4(const coda_tensor* X, float s, const coda_tenso
  * backward inherits the structure: a weight gradient contracts over the tokens)]
  * Transposed NVFP4 quantisation: X (bf16 ROW_MAJOR [R, C]) quantised along its columns into
  * Q = X^T (CODA_NVFP4 [C, R]): for each column c and each block of 16 consecutive rows,
- *   sf = e4m3(amax_block / (6 s)),  Q[c, r] = e2m1(X[r, c] / (sf s))   (fp32 decisions, as at
- * coda_quantize_nvfp4), block scales in the layout described there for the tensor [C, R].  It
+ *   sf = e4m3(amax_block / (6 s)),  Q[c, r] = e2m1(X[r, c] / (sf s)),
+ * block scales in the layout described there for the tensor [C, R].  The decisions are taken
+ * in fp32 as amax_block * (1 / (6 s)) (the reciprocal rounded once) and X[r, c] times the
+ * hardware's approximate reciprocal of sf s (at most one ulp off), so a value within a few
+ * fp32 roundings of a rounding midpoint (an exact tie included) may round the other way than
+ * in exact arithmetic.  It
  * is the K-major operand of a GEMM that contracts over R, as the block-scaled tensor cores
  * need.  mode CODA_QT_SWIGLU: X is a saved [G | U] ([R, 2C]) and the value quantised is
  * silu(G) U, formed in fp32.  With Q_rows (optional, CODA_NVFP4 [R, C], R a multiple of 128)
