@@ -644,7 +644,9 @@ int coda_rms_partial_reduce(const float* partials, int64_t ld, int32_t nparts, i
   return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
 }
 
-int coda_row_rms(const coda_tensor* X, float eps, float* r_out, void* stream) {
+// coda_row_rms, also setting *zero (optional) to 0: the chains' amax reset, folded into the
+// chain's first kernel so that no memset interrupts the launch overlap
+static int row_rms_impl(const coda_tensor* X, float eps, float* r_out, void* stream, float* zero) {
   int st;
   if ((st = check_tensor(X, false)) != CODA_OK) return st;
   if (!r_out) return CODA_ERR_NULL;
@@ -654,8 +656,12 @@ int coda_row_rms(const coda_tensor* X, float eps, float* r_out, void* stream) {
   DevState* dv;
   if ((st = ensure_device(&dv)) != CODA_OK) return st;
   cudaError_t e = launch_row_rms(X->ptr, X->rows, X->cols, X->ld, eps, r_out, static_cast<cudaStream_t>(stream),
-                                 dv->sms);
+                                 dv->sms, zero);
   return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
+}
+
+int coda_row_rms(const coda_tensor* X, float eps, float* r_out, void* stream) {
+  return row_rms_impl(X, eps, r_out, stream, nullptr);
 }
 
 int coda_quantize_e4m3(const coda_tensor* X, float scale, const coda_tensor* Q, float* amax, void* stream) {
@@ -1166,9 +1172,7 @@ int coda_mlp_fp8(const coda_mlp_fp8_io* io, void* stream) {
   if (M == 0) return CODA_OK;
   int st;
   coda_tensor h = mk(io->h, CODA_BF16, M, H, H);
-  if (cudaMemsetAsync(io->amax, 0, sizeof(float), static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return CODA_ERR_LAUNCH;
-  if ((st = coda_row_rms(&h, io->eps, io->r, stream)) != CODA_OK) return st;
+  if ((st = row_rms_impl(&h, io->eps, io->r, stream, io->amax)) != CODA_OK) return st;   // also amax = 0
   {
     coda_tensor A = mk(io->X_q, CODA_E4M3, M, H, H), W = mk(io->W_q, CODA_E4M3, 2 * F, H, H);
     coda_tensor out = mk(io->a_q, CODA_E4M3, M, F, F);
@@ -1211,9 +1215,7 @@ int coda_mlp_nvfp4(const coda_mlp_nvfp4_io* io, void* stream) {
   if (M == 0) return CODA_OK;
   int st;
   coda_tensor h = mk(io->h, CODA_BF16, M, H, H);
-  if (cudaMemsetAsync(io->amax, 0, sizeof(float), static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return CODA_ERR_LAUNCH;
-  if ((st = coda_row_rms(&h, io->eps, io->r, stream)) != CODA_OK) return st;
+  if ((st = row_rms_impl(&h, io->eps, io->r, stream, io->amax)) != CODA_OK) return st;   // also amax = 0
   {
     coda_tensor A = mk(io->X_q, CODA_NVFP4, M, H, H), W = mk(io->W_q, CODA_NVFP4, 2 * F, H, H);
     coda_tensor out = mk(io->a_q, CODA_NVFP4, M, F, F);

@@ -71,9 +71,12 @@ cudaError_t launch_partial_reduce(const float* partials, int64_t ld, int nparts,
 // ---------------------------------------------------------------- full-row RMS
 // One warp per row, 16-byte loads (8 bf16 per lane), four loads in flight per lane.
 __global__ void row_rms_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, int64_t d, int64_t ld, float eps,
-                               float* __restrict__ r) {
+                               float* __restrict__ r, float* __restrict__ zero) {
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
+  // a chain's amax accumulator, reset here rather than by a separate memset: the next kernel
+  // of the stream reads it only after this one has completed
+  if (zero && blockIdx.x == 0 && threadIdx.x == 0) *zero = 0.f;
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= M) return;
@@ -111,12 +114,12 @@ __global__ void row_rms_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, i
 }
 
 cudaError_t launch_row_rms(const void* X, int64_t M, int64_t d, int64_t ld, float eps, float* r, cudaStream_t s,
-                           int sms) {
+                           int sms, float* zero) {
   (void)sms;
   const int rows_per_block = 8;
   const int64_t blocks = (M + rows_per_block - 1) / rows_per_block;
   launch_k(row_rms_kernel, (unsigned)blocks, 32 * rows_per_block, s, static_cast<const __nv_bfloat16*>(X), M, d, ld,
-                                                                   eps, r);
+                                                                   eps, r, zero);
   return cudaGetLastError();
 }
 
