@@ -547,12 +547,12 @@ cudaError_t launch_quantize_nvfp4(const void* X, int64_t R, int64_t K, int64_t l
 //   - Along the rows the values never leave the registers: the two threads holding a block of
 //     16 exchange their maxima with one shuffle, and each stages its 8 codes (4 bytes).
 //   - Along the columns the tile is staged in shared memory (as bf16, or fp32 for silu(G) U);
-//     a warp reads 32 consecutive columns of a row, conflict-free, and a thread quantises four
-//     16-row blocks of one column.
+//     a warp reads 64 consecutive columns of a row, two per thread in one 4- or 8-byte load,
+//     conflict-free, and a thread quantises two 16-row blocks of each of its two columns.
 constexpr int QT_ROWS = 128, QT_COLS = 128;
 
-// The transposed pass's own NVFP4 decisions, cheaper than nvfp4_block16's (the pass issues
-// about 20 instructions per element and is bound by instruction issue, not by DRAM):
+// The transposed pass's own NVFP4 decisions, cheaper than nvfp4_block16's (the pass is bound
+// by instruction issue, not by DRAM, so every instruction per element counts):
 //   sf = e4m3(amax * inv6s), inv6s = 1 / (6 s) rounded once on the host, and
 //   q = e2m1(x * rcp(sf s)) with the hardware's approximate reciprocal (at most one ulp from
 // 1 / (sf s)).  Both stay within a few fp32 roundings of the exact quotients, so a decision
