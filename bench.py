@@ -675,6 +675,11 @@ def run_coda(args, world, rank, local):
         compare = unfused_compare(torch, d, {"h": h, "r": r, "a": a, "Y": Y}, inp, stream, args)
         compare["backward"] = backward_compare(torch, C, S, stream)
 
+    # ---- the library e4m3 / NVFP4 peaks, once nothing is left to time (their sustained loops
+    # leave the GPU at its power cap for a while)
+    if others is not None:
+        finish_lib_peaks(torch, others, peaks())
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -844,6 +849,32 @@ def fp4_peak(torch, fp8_sustained, seconds=2.0):
                 "how": "library NVFP4 GEMM unavailable here: 3x the measured e4m3 sustained peak (nominal ratio)"}
 
 
+def finish_lib_peaks(torch, out, pk):
+    """The library e4m3 and NVFP4 GEMM rates (the denominators of those chains' rooflines),
+    measured once every workload has been timed, and the rooflines that wait for them."""
+    deferred = out.pop("_deferred", [])
+    try:
+        out["fp8_peak"] = fp8_peak(torch)
+    except Exception as ex:                       # a torch without e4m3 GEMMs: keep the nominal ratio
+        out["fp8_peak"] = {"error": f"{type(ex).__name__}: {ex}"[:200]}
+    if "sustained_tflops" in out["fp8_peak"]:
+        peak8 = lib_peak(out["fp8_peak"], 2 * pk["bf16"])
+        note8 = "e4m3 library GEMM measured after every workload, the higher of burst and sustained"
+    else:
+        peak8 = 2 * pk["bf16"]
+        note8 = "fp8 peak taken as 2x the measured bf16 burst peak (nominal ratio)"
+    out["fp4_peak"] = fp4_peak(torch, peak8)
+    peak4 = lib_peak(out["fp4_peak"], out["fp4_peak"].get("sustained_tflops_nominal_ratio"))
+    for v in out.get("mlp_nvfp4_N4", {}).get("per_gemm", {}).values():
+        v["frac_of_peak"] = v["tflops"] / peak4
+    for kind, entry, fl, by in deferred:
+        peak = peak8 if kind == "fp8" else peak4
+        roof = max(fl / (peak * 1e12), by / (pk["hbm"] * 1e9)) * 1e3
+        entry.update({"roofline_ms": roof, "roofline_frac": roof / entry["ms"], "peak_tflops": peak})
+        if kind == "fp8":
+            entry["peak_note"] = note8
+
+
 def other_workloads(torch, C, S, args, stream):
     """Device time of the other chains at their full sizes (16384 tokens): the block backward
     (C2), QKV + RoPE (C3), the fp8 and NVFP4 MLPs (C4, N4), the hidden-size sweep (N3) and the
@@ -855,11 +886,11 @@ def other_workloads(torch, C, S, args, stream):
     pk = peaks()
     steps = max(5, min(args.steps, 50))
     out = {}
-    # measured e4m3 peak (library GEMM), the denominator of the fp8 chain below
-    try:
-        out["fp8_peak"] = fp8_peak(torch)
-    except Exception as ex:                       # a torch without e4m3 GEMMs: keep the nominal ratio
-        out["fp8_peak"] = {"error": f"{type(ex).__name__}: {ex}"[:200]}
+    # The e4m3 and NVFP4 rooflines are held to the library GEMMs' measured rates, taken at the
+    # end of this section: their seconds-long sustained loops leave the GPU at its power cap for
+    # a while, which would slow whatever were timed right after them.  Until then each entry
+    # keeps its FLOP and byte counts here.
+    deferred = []   # (dtype, entry, flop, bytes)
     # the light row reduce in its full-row form, where bandwidth can be seen: r of a
     # [16384, 8192] bf16 tensor (268 MB read), back to back
     Xr = torch.randn((M_TOK, 8192), device="cuda", generator=torch.Generator(device="cuda").manual_seed(5)).to(BF)
@@ -994,17 +1025,9 @@ def other_workloads(torch, C, S, args, stream):
     ms = _time(torch, run8, stream, steps)
     flop = 2 * M * 2 * F8 * H8 + 2 * M * H8 * F8
     byt = (M * H8 + 2 * F8 * H8 + M * F8) + (M * F8 + H8 * F8) + 2 * (M * H8 * 3) + 4 * M * (H8 // 256 + 1)
-    if "sustained_tflops" in out["fp8_peak"]:
-        peak8 = lib_peak(out["fp8_peak"], 2 * pk["bf16"])
-        note = "fp8 peak: e4m3 library GEMM measured above, the higher of burst and sustained"
-    else:
-        peak8 = 2 * pk["bf16"]
-        note = "fp8 peak taken as 2x the measured bf16 burst peak (nominal ratio)"
-    roof = max(flop / (peak8 * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
-    out["mlp_fp8_C4"] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "roofline_ms": roof,
-                         "roofline_frac": roof / ms, "tokens_per_s": M / (ms * 1e-3), "launches": 3,
-                         "peak_tflops": peak8, "peak_note": note,
-                         "frac_of_2x_bf16": flop / (ms * 1e-3) / 1e12 / (2 * pk["bf16"])}
+    out["mlp_fp8_C4"] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "tokens_per_s": M / (ms * 1e-3),
+                         "launches": 3, "frac_of_2x_bf16": flop / (ms * 1e-3) / 1e12 / (2 * pk["bf16"])}
+    deferred.append(("fp8", out["mlp_fp8_C4"], flop, byt))
     # N4: its backward on e4m3 operands, after a training-mode forward that saves Z = [G | U]
     Z8 = torch.empty((M, 2 * F8), dtype=BF, device="cuda")
     fwd8 = lambda: C.coda_mlp_fp8(h8, X8, W8, Wd8, fi["s_x"], fi["s_w"], fi["s_wd"], s_a, EPS, r8, aq, am, Y8, P8,
@@ -1031,18 +1054,15 @@ def other_workloads(torch, C, S, args, stream):
     flop = 12 * M * H8 * F8                            # dA, dW_d: 2MHF each; dh, dW: 4MHF each
     byt = 3 * M * H8 + (M * H8 + H8 * F8 + 4 * M * F8 + 2 * M * F8) + (M * H8 + M * F8 + 4 * H8 * F8) + \
         (2 * M * F8 + 2 * F8 * H8 + 6 * M * H8) + (2 * M * F8 + M * H8 + 8 * F8 * H8)
-    roof = max(flop / (peak8 * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
-    out["mlp_fp8_backward_N4"] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "roofline_ms": roof,
-                                  "roofline_frac": roof / ms, "tokens_per_s": M / (ms * 1e-3), "launches": 6,
-                                  "train_forward_ms": ms_fz, "peak_tflops": peak8,
+    out["mlp_fp8_backward_N4"] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "tokens_per_s": M / (ms * 1e-3),
+                                  "launches": 6, "train_forward_ms": ms_fz,
                                   "note": "quantise dY, dA GEMM + SwiGLU-bwd (e4m3 e), row reduce, dW_d, "
                                           "dh GEMM + RMSNorm-bwd combine, dW; e4m3 operands, MN-major where "
                                           "transposed"}
+    deferred.append(("fp8", out["mlp_fp8_backward_N4"], flop, byt))
     del h8, X8, W8, Wd8, aq, Y8, P8, Z8, dY8, dYq8, eq8, dh8, dWd8, dW8, ws8
     torch.cuda.empty_cache()
     # N4: the same MLP with NVFP4 operands (e2m1 codes, e4m3 block scales per 16 K elements)
-    out["fp4_peak"] = fp4_peak(torch, peak8)
-    peak4 = lib_peak(out["fp4_peak"], out["fp4_peak"].get("sustained_tflops_nominal_ratio"))
     ni = S.nvfp4_mlp_inputs(M, H8, F8, seed=0, device="cuda")
     h4 = ni["h"]
     amax4 = lambda t: float(t.abs().max()) / (6 * 448)
@@ -1068,7 +1088,6 @@ def other_workloads(torch, C, S, args, stream):
     sfb = lambda R, K: (R * K) // 16                    # block-scale bytes
     byt = (M * H8 // 2 + sfb(M, H8) + F8 * H8 + sfb(2 * F8, H8) + M * F8 // 2 + sfb(M, F8)) + \
         (M * F8 // 2 + sfb(M, F8) + H8 * F8 // 2 + sfb(H8, F8)) + 2 * (M * H8 * 3) + 4 * M * (H8 // 256 + 1)
-    roof = max(flop / (peak4 * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
     ms_q = _time(torch, quant_x, stream, steps)
     byt_q = 2 * M * H8 + M * H8 // 2 + sfb(M, H8)
     # the chain's two GEMMs launched on their own through the public GEMM call, with its arguments
@@ -1080,21 +1099,23 @@ def other_workloads(torch, C, S, args, stream):
     for name, fn, fl in (("gate_up_swiglu_nvfp4_out", gate_up, 2 * M * 2 * F8 * H8),
                          ("down_residual", down, 2 * M * H8 * F8)):
         g_ms = _time(torch, fn, stream, steps)
-        per_gemm[name] = {"ms": g_ms, "tflops": fl / (g_ms * 1e-3) / 1e12,
-                          "frac_of_peak": fl / (g_ms * 1e-3) / 1e12 / peak4}
-    out["mlp_nvfp4_N4"] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "roofline_ms": roof,
-                           "roofline_frac": roof / ms, "tokens_per_s": M / (ms * 1e-3), "launches": 3,
-                           "peak_tflops": peak4, "vs_fp8_chain": out["mlp_fp8_C4"]["ms"] / ms,
-                           "quantize_x_ms": ms_q, "quantize_x_gbs": byt_q / (ms_q * 1e-3) / 1e9,
-                           "quantize_x_frac_of_hbm": byt_q / (ms_q * 1e-3) / 1e9 / pk["hbm"],
-                           "per_gemm": per_gemm,
-                           "note": "row RMS, gate/up GEMM + r + SwiGLU + NVFP4 quantisation of a (codes, block "
-                                   "scales, amax), down GEMM + residual + partials; X quantised beforehand "
-                                   "(quantize_x_ms, the pass a previous layer's epilogue would fold in)"}
+        per_gemm[name] = {"ms": g_ms, "tflops": fl / (g_ms * 1e-3) / 1e12}
+    nv4 = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "tokens_per_s": M / (ms * 1e-3), "launches": 3,
+           "vs_fp8_chain": out["mlp_fp8_C4"]["ms"] / ms,
+           "quantize_x_ms": ms_q, "quantize_x_gbs": byt_q / (ms_q * 1e-3) / 1e9,
+           "quantize_x_frac_of_hbm": byt_q / (ms_q * 1e-3) / 1e9 / pk["hbm"],
+           "per_gemm": per_gemm,
+           "note": "row RMS, gate/up GEMM + r + SwiGLU + NVFP4 quantisation of a (codes, block scales, amax), "
+                   "down GEMM + residual + partials; X quantised beforehand (quantize_x_ms, the pass a previous "
+                   "layer's epilogue would fold in)"}
     del h4, X4, W4, Wd4, Y4, P4, a4
     torch.cuda.empty_cache()
     # N4: the NVFP4 MLP backward (each GEMM's operands quantised along its own K)
-    out["mlp_nvfp4_backward_N4"] = nvfp4_backward_workload(torch, C, S, steps, peak4, pk)
+    nvb = nvfp4_backward_workload(torch, C, S, steps, pk)
+    out["mlp_nvfp4_N4"] = nv4
+    out["mlp_nvfp4_backward_N4"] = nvb
+    deferred.append(("fp4", nv4, flop, byt))
+    deferred.append(("fp4", nvb, nvb.pop("flop"), nvb["bytes"]))
     # N3: the block forward at the 7B and 70B LLaMA-3 hidden sizes, beside torch eager
     for name, Hs, Fs in (("block_forward_7B_H4096_F14336", 4096, 14336), ("block_forward_70B_H8192_F28672", 8192,
                                                                            28672)):
@@ -1146,10 +1167,11 @@ def other_workloads(torch, C, S, args, stream):
                      "tokens_per_s": M / (ms * 1e-3), "launches": nl, "vocab": V}
     del hl, gl, Wv, tg, ul, el, dhl, dWv, wsb, wsx
     torch.cuda.empty_cache()
+    out["_deferred"] = deferred   # finished by finish_lib_peaks once nothing else is left to time
     return out
 
 
-def nvfp4_backward_workload(torch, C, S, steps, peak4, pk, M=M_TOK, H=4096, F=14336):
+def nvfp4_backward_workload(torch, C, S, steps, pk, M=M_TOK, H=4096, F=14336, peak4=None):
     """Device time of the NVFP4 MLP backward at the LLaMA-3-8B MLP shape: 9 launches (dY
     quantised along rows and columns in one pass, the dA GEMM with the SwiGLU-backward epilogue,
     the row reduce, e along rows and columns in one pass, silu(G) U and h along columns, the
@@ -1186,12 +1208,14 @@ def nvfp4_backward_workload(torch, C, S, steps, peak4, pk, M=M_TOK, H=4096, F=14
         (2 * 2 * M * F + 2 * n4(M, 2 * F)) + (2 * 2 * M * F + n4(F, M)) + (2 * M * H + n4(H, M)) + \
         (n4(H, M) + n4(F, M) + 4 * H * F) + (n4(M, 2 * F) + n4(H, 2 * F) + 2 * 3 * M * H + 4 * M) + \
         (n4(2 * F, M) + n4(H, M) + 4 * 2 * F * H)
-    roof = max(flop / (peak4 * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
-    res = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "roofline_ms": roof, "roofline_frac": roof / ms,
-           "tokens_per_s": M / (ms * 1e-3), "launches": 9, "peak_tflops": peak4, "bytes": byt,
+    res = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "tokens_per_s": M / (ms * 1e-3), "launches": 9,
+           "bytes": byt, "flop": flop,
            "note": "quantise dY (rows and columns, one pass), dA GEMM + SwiGLU-bwd (bf16 e), row reduce, quantise e "
                    "(rows and columns, one pass), silu(G) U and h (columns), dW_d, dh GEMM + RMSNorm-bwd combine, dW; "
                    "NVFP4 operands blocked along each GEMM's K"}
+    if peak4:
+        roof = max(flop / (peak4 * 1e12), byt / (pk["hbm"] * 1e9)) * 1e3
+        res.update({"roofline_ms": roof, "roofline_frac": roof / ms, "peak_tflops": peak4})
     del t, bufs, ws
     torch.cuda.empty_cache()
     return res
@@ -1407,7 +1431,7 @@ def main():
                 import coda_synth as S
                 from gemm_epilogue_transformer_tcgen05_gb300 import coda as C
                 C.lib()
-                res = nvfp4_backward_workload(torch, C, S, 1, 1.0, peaks(), M=args.tokens)
+                res = nvfp4_backward_workload(torch, C, S, 1, peaks(), M=args.tokens)
                 print(json.dumps({"nvfp4_bwd_pass": {"tokens": args.tokens, "hidden": 4096, "ffn": 14336,
                                                      "order": "weight prep (2 launches), backward (warm-up "
                                                               "with s_e = 1), then 3 warm-up + 1 timed",
