@@ -46,7 +46,7 @@ namespace coda {
 // ----------------------------------------------------------------------- constants
 constexpr int BM = 128;                               // tile rows = TMEM lanes
 constexpr int UMMA_N = 256;                           // MMA N = B tile rows
-constexpr int BK_BYTES = 128;                         // K bytes per stage (one 128B swizzle row)
+constexpr int BK_BYTES = 128;                         // K bytes per 128B swizzle row (a stage holds one or two)
 constexpr int KSTEPS = 4;                             // MMAs per stage, 32 bytes of K each
 constexpr int A_STAGE_BYTES = BM * BK_BYTES;          // 16 KB: this CTA's 128 rows of A
 constexpr int TMEM_COLS = 2 * UMMA_N;                 // two fp32 accumulators
