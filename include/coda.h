@@ -223,8 +223,10 @@ CODA_API int coda_rms_gain(const coda_tensor* X, const float* g, float eps, floa
                            void* stream);
 
 /* The light reduce of the cross-entropy partials [KuCoin, "Cinco bloques…": block
- * log-sum-exp and the max / sum-exp state]: per row, in tile order,
- *   lse[i] = m + log(sum_t Ps[t, i] exp(Pm[t, i] - m)),  m = max_t Pm[t, i];
+ * log-sum-exp and the max / sum-exp state]: per row,
+ *   lse[i] = m + log(sum_t Ps[t, i] exp(Pm[t, i] - m)),  m = max_t Pm[t, i]
+ * (the tiles folded into eight running (max, scaled sum) states, tile t into state t % 8,
+ * which are then merged in order: the result does not depend on the launch);
  *   loss[i] = lse[i] - target_logit[i]  (NaN when targets[i] is outside [0, V));
  *   *mean = sum_i loss[i] / M (fixed-order reduction; mean may be NULL). */
 CODA_API int coda_xent_combine(const float* Pm, const float* Ps, int64_t ld, int32_t nparts, int64_t M,
