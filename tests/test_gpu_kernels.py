@@ -303,6 +303,60 @@ def test_partial_reduce_and_row_rms(C):
     assert_close(f64(r2), ref, 1e-5, "partial reduce")
 
 
+@pytest.mark.parametrize("nparts", [1, 3, 8, 37, 501])
+def test_partial_reduce_many_parts(C, nparts):
+    """The reduce splits a row's parts over eight warps and merges them in a fixed order: every
+    part count (fewer than the warps, not a multiple of them, the LM head's 501) against the
+    plain sums, with a ragged number of rows, in both modes, and bit-identical run to run."""
+    M, d = 1000, 2048
+    g = np.random.default_rng(nparts)
+    Pn = g.uniform(0.0, 4.0, size=(nparts, M))
+    P = torch.tensor(Pn, dtype=torch.float32, device="cuda")
+    r1, r2 = torch.empty((M,), device="cuda"), torch.empty((M,), device="cuda")
+    C.coda_rms_partial_reduce(P, M, d, 1e-6, r1)
+    C.coda_rms_partial_reduce(P, M, d, 1e-6, r2)
+    rs = torch.tensor(g.uniform(0.5, 1.5, size=M), dtype=torch.float32, device="cuda")
+    c = torch.empty((M,), device="cuda")
+    C.coda_rms_partial_reduce(P, M, d, 0.0, c, mode=C.REDUCE_SCALE_SUM, rowscale=rs)
+    torch.cuda.synchronize()
+    fresh_status()
+    assert torch.equal(r1, r2), "not reproducible"
+    tot = np.sum(f64(P), axis=0)
+    assert_close(f64(r1), 1.0 / np.sqrt(tot / d + 1e-6), 1e-5, f"r from {nparts} parts")
+    assert_close(f64(c), f64(rs) * tot / d, 1e-5, f"c = r s / d from {nparts} parts")
+
+
+@pytest.mark.parametrize("nparts", [4, 37, 501])
+def test_xent_combine_many_tiles(C, nparts):
+    """The cross-entropy combine folds the tile states into eight running (max, scaled sum)
+    pairs and merges them in order: against the oracle's combine for several tile counts, a
+    ragged number of rows, a tile state with no column (max -inf, sum 0) that must be ignored,
+    and bit-identical run to run."""
+    M, V = 1000, 256 * nparts
+    g = np.random.default_rng(100 + nparts)
+    m = g.normal(0.0, 3.0, size=(nparts, M))
+    s = g.uniform(1.0, 256.0, size=(nparts, M))
+    if nparts > 1:
+        m[nparts // 2, :7] = -np.inf   # rows 0..6: one tile without columns
+        s[nparts // 2, :7] = 0.0
+    Pm = torch.tensor(m, dtype=torch.float32, device="cuda")
+    Ps = torch.tensor(s, dtype=torch.float32, device="cuda")
+    T = torch.tensor(g.normal(size=M), dtype=torch.float32, device="cuda")
+    tg = torch.tensor(g.integers(0, V, size=M), dtype=torch.int32, device="cuda")
+    outs = []
+    for _ in range(2):
+        lse, loss, mean = (torch.empty((n,), device="cuda") for n in (M, M, 1))
+        C.coda_xent_combine(Pm, Ps, T, tg, V, lse, loss, mean)
+        outs.append((lse, loss, mean))
+    torch.cuda.synchronize()
+    fresh_status()
+    assert all(torch.equal(a, b) for a, b in zip(outs[0], outs[1])), "not reproducible"
+    keep = np.isfinite(m)
+    ref = O.xent_combine(np.where(keep, m, -1e300), np.where(keep, s, 0.0))
+    assert_close(f64(outs[0][0]), ref, 1e-6, f"lse from {nparts} tiles")
+    assert_close(f64(outs[0][1]), ref - f64(T), 1e-5, "loss")
+
+
 def test_fold_gain(C):
     N, K = 300, 512
     W = seeded((N, K), 44, std=0.05, dtype=BF)
