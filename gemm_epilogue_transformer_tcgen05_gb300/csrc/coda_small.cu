@@ -35,16 +35,38 @@ cudaError_t launch_k(void (*kernel)(KArgs...), unsigned grid, unsigned block, cu
 }
 
 // ---------------------------------------------------------------- partial reduce
-// Partials stored [nparts, M], so a warp's load of 32 consecutive rows is coalesced.  A CTA
-// takes 32 rows (one per lane) and splits the parts over its 8 warps: warp w adds parts w,
-// w + 8, ... in that order (four loads in flight); the warps' sums are then added as
-// ((w0 + w4) + (w1 + w5)) + ((w2 + w6) + (w3 + w7)), a fixed order (for 8 parts, that of
-// four interleaved running sums).  (One thread per row over all parts ran at 1.3 TB/s for
-// 501 parts: 64 CTAs for 16384 rows.)
+// Partials stored [nparts, M], so a warp's load of 32 consecutive rows is coalesced.
+// Few parts (the chains' own, e.g. 8 for a 2048-wide layer): one thread per row, four running
+// sums (part t into sum t % 4) added as (s0 + s1) + (s2 + s3).  The kernel uses no shared
+// memory, so the next GEMM's CTA (all but a few KB of an SM's shared memory) can start beside
+// it (the block forward ran 0.2% slower with the shared-merge kernel below in its place).
+// Many parts (the LM head's 501): a CTA takes 32 rows and splits the parts over its 8 warps,
+// warp w adding parts w, w + 8, ... in order (four loads in flight), and the warps' sums are
+// added as ((w0 + w4) + (w1 + w5)) + ((w2 + w6) + (w3 + w7)).  One thread per row over all
+// parts ran at 1.3 TB/s there (64 CTAs for 16384 rows).
+__device__ __forceinline__ float reduce_finish(float tot, int mode, float inv_d, float eps, float rs) {
+  return mode == 0 ? rsqrtf(fmaf(tot, inv_d, eps)) : rs * (tot * inv_d);
+}
+__global__ void partial_reduce_kernel(const float* __restrict__ P, int64_t ld, int nparts, int64_t M, float inv_d,
+                                      float eps, int mode, const float* __restrict__ rowscale,
+                                      float* __restrict__ out) {
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= M) return;
+  float s4[4] = {0.f, 0.f, 0.f, 0.f};
+  int t = 0;
+  for (; t + 4 <= nparts; t += 4) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) s4[k] += __ldg(P + (int64_t)(t + k) * ld + i);
+  }
+  for (; t < nparts; ++t) s4[0] += __ldg(P + (int64_t)t * ld + i);
+  out[i] = reduce_finish((s4[0] + s4[1]) + (s4[2] + s4[3]), mode, inv_d, eps, mode ? __ldg(rowscale + i) : 0.f);
+}
 constexpr int PR_WARPS = 8;
 __global__ void __launch_bounds__(32 * PR_WARPS)
-    partial_reduce_kernel(const float* __restrict__ P, int64_t ld, int nparts, int64_t M, float inv_d, float eps,
-                          int mode, const float* __restrict__ rowscale, float* __restrict__ out) {
+    partial_reduce_split_kernel(const float* __restrict__ P, int64_t ld, int nparts, int64_t M, float inv_d,
+                                float eps, int mode, const float* __restrict__ rowscale, float* __restrict__ out) {
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
   __shared__ float st[PR_WARPS][32];
@@ -67,17 +89,20 @@ __global__ void __launch_bounds__(32 * PR_WARPS)
   if (w == 0 && i < M) {
     const float tot = ((st[0][lane] + st[4][lane]) + (st[1][lane] + st[5][lane])) +
                       ((st[2][lane] + st[6][lane]) + (st[3][lane] + st[7][lane]));
-    if (mode == 0)
-      out[i] = rsqrtf(fmaf(tot, inv_d, eps));
-    else
-      out[i] = __ldg(rowscale + i) * (tot * inv_d);
+    out[i] = reduce_finish(tot, mode, inv_d, eps, mode ? __ldg(rowscale + i) : 0.f);
   }
 }
 
 cudaError_t launch_partial_reduce(const float* partials, int64_t ld, int nparts, int64_t M, float inv_d, float eps,
                                   int mode, const float* rowscale, float* out, cudaStream_t s) {
-  launch_k(partial_reduce_kernel, (unsigned)((M + 31) / 32), 32 * PR_WARPS, s, partials, ld, nparts, M, inv_d, eps, mode,
-           rowscale, out);
+  if (nparts <= 16) {
+    const int threads = 256;
+    launch_k(partial_reduce_kernel, (unsigned)((M + threads - 1) / threads), threads, s, partials, ld, nparts, M, inv_d,
+             eps, mode, rowscale, out);
+  } else {
+    launch_k(partial_reduce_split_kernel, (unsigned)((M + 31) / 32), 32 * PR_WARPS, s, partials, ld, nparts, M, inv_d,
+             eps, mode, rowscale, out);
+  }
   return cudaGetLastError();
 }
 

@@ -203,8 +203,9 @@ CODA_API int coda_gemm_epilogue(const coda_tensor* A, const coda_tensor* W, cons
 
 /* The light row reduce [KuCoin, "El epílogo esconde un tesoro"].
  *   partials: fp32 [nparts, ld] (part t of row i at partials[t*ld + i]), summed in a fixed
- *   order (part t into running sum t % 8, in t order; then ((0 + 4) + (1 + 5)) + ((2 + 6) + (3 + 7))),
- *   so the result does not depend on the launch.
+ *   order, so the result does not depend on the launch: up to 16 parts, part t into running sum
+ *   t % 4 and then (0 + 1) + (2 + 3); above, part t into running sum t % 8 and then
+ *   ((0 + 4) + (1 + 5)) + ((2 + 6) + (3 + 7)).
  *   mode CODA_REDUCE_RSQRT_MEAN: out[i] = 1 / sqrt(sum_t P[t, i] / d + eps)   (r)
  *   mode CODA_REDUCE_SCALE_SUM:  out[i] = rowscale[i] * sum_t P[t, i] / d     (c = r s / d) */
 enum coda_reduce_mode { CODA_REDUCE_RSQRT_MEAN = 0, CODA_REDUCE_SCALE_SUM = 1 };
