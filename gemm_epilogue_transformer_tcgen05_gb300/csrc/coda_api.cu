@@ -646,7 +646,8 @@ int coda_rms_partial_reduce(const float* partials, int64_t ld, int32_t nparts, i
 
 // coda_row_rms, also setting *zero (optional) to 0: the chains' amax reset, folded into the
 // chain's first kernel so that no memset interrupts the launch overlap
-static int row_rms_impl(const coda_tensor* X, float eps, float* r_out, void* stream, float* zero) {
+static int row_rms_impl(const coda_tensor* X, float eps, float* r_out, void* stream, float* zero,
+                        bool beside = false) {
   int st;
   if ((st = check_tensor(X, false)) != CODA_OK) return st;
   if (!r_out) return CODA_ERR_NULL;
@@ -656,7 +657,7 @@ static int row_rms_impl(const coda_tensor* X, float eps, float* r_out, void* str
   DevState* dv;
   if ((st = ensure_device(&dv)) != CODA_OK) return st;
   cudaError_t e = launch_row_rms(X->ptr, X->rows, X->cols, X->ld, eps, r_out, static_cast<cudaStream_t>(stream),
-                                 dv->sms, zero);
+                                 dv->sms, zero, beside);
   return e == cudaSuccess ? CODA_OK : CODA_ERR_LAUNCH;
 }
 
@@ -1149,7 +1150,8 @@ int coda_qkv_rope(const coda_qkv_rope_io* io, void* stream) {
   if (M == 0) return CODA_OK;
   int st;
   coda_tensor h = mk(io->h, CODA_BF16, M, H, H);
-  if ((st = coda_row_rms(&h, io->eps, io->r, stream)) != CODA_OK) return st;
+  // the QKV GEMM reads r only in its epilogue and its CTAs fit beside the pass
+  if ((st = row_rms_impl(&h, io->eps, io->r, stream, nullptr, true)) != CODA_OK) return st;
   coda_tensor W = mk(io->W_qkv, CODA_BF16, N, H, H), out = mk(io->out, CODA_BF16, M, N, N);
   coda_epilogue_program pg = prog_of({CODA_OP_ROW_SCALE, CODA_OP_ROPE});
   coda_side_inputs sd{};
@@ -1172,7 +1174,8 @@ int coda_mlp_fp8(const coda_mlp_fp8_io* io, void* stream) {
   if (M == 0) return CODA_OK;
   int st;
   coda_tensor h = mk(io->h, CODA_BF16, M, H, H);
-  if ((st = row_rms_impl(&h, io->eps, io->r, stream, io->amax)) != CODA_OK) return st;   // also amax = 0
+  // also amax = 0; the e4m3 gate/up GEMM reads r only in its epilogue and fits beside the pass
+  if ((st = row_rms_impl(&h, io->eps, io->r, stream, io->amax, true)) != CODA_OK) return st;
   {
     coda_tensor A = mk(io->X_q, CODA_E4M3, M, H, H), W = mk(io->W_q, CODA_E4M3, 2 * F, H, H);
     coda_tensor out = mk(io->a_q, CODA_E4M3, M, F, F);
@@ -1215,7 +1218,9 @@ int coda_mlp_nvfp4(const coda_mlp_nvfp4_io* io, void* stream) {
   if (M == 0) return CODA_OK;
   int st;
   coda_tensor h = mk(io->h, CODA_BF16, M, H, H);
-  if ((st = row_rms_impl(&h, io->eps, io->r, stream, io->amax)) != CODA_OK) return st;   // also amax = 0
+  // also amax = 0; the many-CTA pass: the NVFP4 GEMM (ten warps of 168 registers) cannot sit
+  // beside a resident one
+  if ((st = row_rms_impl(&h, io->eps, io->r, stream, io->amax)) != CODA_OK) return st;
   {
     coda_tensor A = mk(io->X_q, CODA_NVFP4, M, H, H), W = mk(io->W_q, CODA_NVFP4, 2 * F, H, H);
     coda_tensor out = mk(io->a_q, CODA_NVFP4, M, F, F);

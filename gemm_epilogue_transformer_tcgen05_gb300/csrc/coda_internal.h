@@ -46,12 +46,13 @@ const VariantEntry* find_variant(const VariantKey& k);
 extern std::atomic<int> g_launch_overlap;
 
 // Small bandwidth-bound kernels (coda_small.cu).  Arguments are validated by the caller.
-// launch_row_rms: `zero` (optional) is a float the kernel sets to 0 before its dependants run.
+// launch_row_rms: `zero` (optional) is a float the kernel sets to 0 before its dependants run;
+// `beside`: one CTA per SM, leaving room for the next GEMM's CTA (a chain whose GEMM reads r
+// only in its epilogue); otherwise the many-CTA pass.
 cudaError_t launch_partial_reduce(const float* partials, int64_t ld, int nparts, int64_t M, float inv_d, float eps,
                                   int mode, const float* rowscale, float* out, cudaStream_t s);
 cudaError_t launch_row_rms(const void* X, int64_t M, int64_t d, int64_t ld, float eps, float* r, cudaStream_t s,
-                           int sms,
-                           float* zero = nullptr);
+                           int sms, float* zero = nullptr, bool beside = false);
 cudaError_t launch_col_reduce(const float* parts, int64_t nblocks, int64_t N, int64_t ld, float* out,
                               cudaStream_t s);
 enum FoldOut { FOLD_OUT_BF16 = 0, FOLD_OUT_F32 = 1, FOLD_OUT_E4M3 = 2 };

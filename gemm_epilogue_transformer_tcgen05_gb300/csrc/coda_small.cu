@@ -107,7 +107,59 @@ cudaError_t launch_partial_reduce(const float* partials, int64_t ld, int nparts,
 }
 
 // ---------------------------------------------------------------- full-row RMS
-// One warp per row, 16-byte loads (8 bf16 per lane), four loads in flight per lane.
+// Sum of squares of R rows of bf16 (nvec 16-byte chunks each, 8 values a chunk) across one
+// warp, in the order both row-RMS kernels share, so they give the same bits: lane l takes
+// chunks l + 32 j; in the main loop chunk v + 32 k goes into running sum k (four loads in
+// flight a row), in the tail into sum 0; then (s0 + s1) + (s2 + s3) and the lanes by xor
+// shuffles.  The R rows' loads are issued together.
+template <int R>
+__device__ __forceinline__ void rows_sumsq(const uint4* const (&src)[R], int64_t nvec, int lane, float (&out)[R]) {
+  float acc[R][4];
+#pragma unroll
+  for (int j = 0; j < R; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+  int64_t v = lane;
+  for (; v + 96 < nvec; v += 128) {
+    uint4 u[R][4];
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) u[j][k] = __ldcs(src[j] + v + 32 * k);
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t w[4] = {u[j][k].x, u[j][k].y, u[j][k].z, u[j][k].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
+          acc[j][k] = fmaf(lo, lo, fmaf(hi, hi, acc[j][k]));
+        }
+      }
+  }
+  for (; v < nvec; v += 32) {
+    uint4 u[R];
+#pragma unroll
+    for (int j = 0; j < R; ++j) u[j] = __ldcs(src[j] + v);
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const uint32_t w[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
+        acc[j][0] = fmaf(lo, lo, fmaf(hi, hi, acc[j][0]));
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    float s = (acc[j][0] + acc[j][1]) + (acc[j][2] + acc[j][3]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    out[j] = s;
+  }
+}
+
+// One warp per row, many CTAs: the fastest pass on its own.
 __global__ void row_rms_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, int64_t d, int64_t ld, float eps,
                                float* __restrict__ r, float* __restrict__ zero) {
   ptx::griddep_wait();
@@ -118,46 +170,60 @@ __global__ void row_rms_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, i
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= M) return;
-  const uint4* src = reinterpret_cast<const uint4*>(X + row * ld);
-  const int64_t nvec = d >> 3;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  int64_t v = lane;
-  for (; v + 96 < nvec; v += 128) {
-    uint4 u[4];
+  const uint4* const src[1] = {reinterpret_cast<const uint4*>(X + row * ld)};
+  float s[1];
+  rows_sumsq<1>(src, d >> 3, lane, s);
+  if (lane == 0) r[row] = rsqrtf(fmaf(s[0], 1.0f / (float)d, eps));
+}
+
+// One CTA of 8 warps per SM, a warp taking 4 rows at a time (16 loads in flight a lane), at most
+// 128 registers a thread: the GEMM that follows in a chain (6 warps of up to 128 registers, up
+// to 226 KB of shared memory) fits on the SM beside it, so a GEMM that reads r only in its
+// epilogue runs its first mainloop under this pass.  On its own the pass is slower than the
+// many-CTA kernel (16384 x 8192: 55 against 37 us; each warp's groups are serial DRAM round
+// trips, and prefetching the next group into L2 did not help), so only the chains use it.
+constexpr int RR_WARPS = 8, RR_ROWS = 4;
+__global__ void __launch_bounds__(32 * RR_WARPS, 2)
+    row_rms_beside_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, int64_t d, int64_t ld, float eps,
+                          float* __restrict__ r, float* __restrict__ zero) {
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+  if (zero && blockIdx.x == 0 && threadIdx.x == 0) *zero = 0.f;
+  const int lane = threadIdx.x & 31;
+  const int64_t step = (int64_t)gridDim.x * RR_WARPS;
+  for (int64_t grp = (int64_t)blockIdx.x * RR_WARPS + (threadIdx.x >> 5); grp * RR_ROWS < M; grp += step) {
+    const int64_t row0 = grp * RR_ROWS;
+    const uint4* src[RR_ROWS];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) u[k] = __ldcs(src + v + 32 * k);
+    for (int j = 0; j < RR_ROWS; ++j)   // rows past M re-read row0 (always in range) and are not stored
+      src[j] = reinterpret_cast<const uint4*>(X + (row0 + j < M ? row0 + j : row0) * ld);
+    float s[RR_ROWS];
+    rows_sumsq<RR_ROWS>(src, d >> 3, lane, s);
+    if (lane == 0) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t w[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
-        acc[k] = fmaf(lo, lo, fmaf(hi, hi, acc[k]));
-      }
+      for (int j = 0; j < RR_ROWS; ++j)
+        if (row0 + j < M) r[row0 + j] = rsqrtf(fmaf(s[j], 1.0f / (float)d, eps));
     }
   }
-  for (; v < nvec; v += 32) {
-    const uint4 u = __ldcs(src + v);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
-      acc[0] = fmaf(lo, lo, fmaf(hi, hi, acc[0]));
-    }
-  }
-  float s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (lane == 0) r[row] = rsqrtf(fmaf(s, 1.0f / (float)d, eps));
 }
 
 cudaError_t launch_row_rms(const void* X, int64_t M, int64_t d, int64_t ld, float eps, float* r, cudaStream_t s,
-                           int sms, float* zero) {
-  (void)sms;
-  const int rows_per_block = 8;
-  const int64_t blocks = (M + rows_per_block - 1) / rows_per_block;
-  launch_k(row_rms_kernel, (unsigned)blocks, 32 * rows_per_block, s, static_cast<const __nv_bfloat16*>(X), M, d, ld,
-                                                                   eps, r, zero);
+                           int sms, float* zero, bool beside) {
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(X);
+  if (beside) {
+    // the carve-out the GEMM beside it needs; set once (a function-local static is initialised once)
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        row_rms_beside_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+    if (attr != cudaSuccess) return attr;
+    const int64_t groups = (M + RR_ROWS - 1) / RR_ROWS;
+    const int64_t need = (groups + RR_WARPS - 1) / RR_WARPS;
+    const unsigned grid = (unsigned)(need < sms ? need : sms);
+    launch_k(row_rms_beside_kernel, grid, 32 * RR_WARPS, s, x, M, d, ld, eps, r, zero);
+  } else {
+    const int rows_per_block = 8;
+    const int64_t blocks = (M + rows_per_block - 1) / rows_per_block;
+    launch_k(row_rms_kernel, (unsigned)blocks, 32 * rows_per_block, s, x, M, d, ld, eps, r, zero);
+  }
   return cudaGetLastError();
 }
 
