@@ -350,6 +350,31 @@ def test_qkv_rope_full_size_sampled_rows(C):
     assert_close(f64(out)[rows], ref, TOL_BF16, "qkv rows")
 
 
+@pytest.mark.parametrize("M", [1, 7, 1000, 1001, 16384])
+def test_chain_row_rms_bitwise_equal_to_row_rms(C, M):
+    """The QKV + RoPE chain and the FP8 MLP open with a one-CTA-per-SM row RMS that shares the
+    standalone pass's summation order: r must be the same bits as coda_row_rms gives for the
+    same h, for row counts below one warp's group of 4 rows, ragged, and full size (every
+    SM's CTA taking several groups)."""
+    H, hd = 2048, 64
+    inp = S.qkv_inputs(M, H, 8 * hd, seed=5)
+    _, r_chain = _run_qkv(C, inp, 128, hd, 6 * hd)
+    r_plain = torch.empty((M,), device="cuda")
+    C.coda_row_rms(dev(inp["h"]), inp["eps"], r_plain)
+    torch.cuda.synchronize()
+    fresh_status()
+    assert torch.equal(r_chain, r_plain)
+    if M < 1000:
+        return   # the FP8 chain at the larger row counts (ragged and not) only
+    fi = S.fp8_mlp_inputs(M, 512, 384, seed=5)
+    r8 = _run_fp8(C, fi, 1.0)[0]
+    r8_plain = torch.empty((M,), device="cuda")
+    C.coda_row_rms(dev(fi["h"]), fi["eps"], r8_plain)
+    torch.cuda.synchronize()
+    fresh_status()
+    assert torch.equal(r8, r8_plain)
+
+
 # --------------------------------------------------------------------- FP8 MLP
 def _run_fp8(C, inp, s_a):
     h, Xq, Wq, Wdq = dev(inp["h"]), dev(inp["Xq"]), dev(inp["Wq"]), dev(inp["Wdq"])
