@@ -432,16 +432,19 @@ __global__ void col_reduce_kernel(const float* __restrict__ parts, int64_t nbloc
   __shared__ float red[32][33];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int64_t j = (int64_t)blockIdx.x * 32 + tx;
-  float s0 = 0.f, s1 = 0.f;
+  // thread (ty, tx) sums rows ty, ty + 32, ... of column j: row ty + 32 i into running sum i % 8
+  // (eight loads in flight), the rows left over into sum 0, then ((0 + 1) + (2 + 3)) + ((4 + 5) +
+  // (6 + 7)); the 32 threads of a column are added in ty order
+  float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (j < N) {
     int64_t b = ty;
-    for (; b + 32 < nblocks; b += 64) {
-      s0 += __ldg(parts + b * ld + j);
-      s1 += __ldg(parts + (b + 32) * ld + j);
+    for (; b + 7 * 32 < nblocks; b += 8 * 32) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) s[k] += __ldg(parts + (b + 32 * k) * ld + j);
     }
-    if (b < nblocks) s0 += __ldg(parts + b * ld + j);
+    for (; b < nblocks; b += 32) s[0] += __ldg(parts + b * ld + j);
   }
-  red[ty][tx] = s0 + s1;
+  red[ty][tx] = ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
   __syncthreads();
   if (ty == 0 && j < N) {
     float t = 0.f;

@@ -238,7 +238,10 @@ CODA_API int coda_xent_combine(const float* Pm, const float* Ps, int64_t ld, int
 
 /* Column reduce [KuCoin, "El epílogo esconde un tesoro" (the backward inherits the partial +
  * light-reduce structure: here the gain gradient dg from per-slab column partials)]:
- *   out[j] = sum_b parts[b*ld + j] over b in [0, nblocks) (fixed order, so deterministic).
+ *   out[j] = sum_b parts[b*ld + j] over b in [0, nblocks) (fixed order, so deterministic:
+ *   b into running sum (b mod 32, (b / 32) mod 8) up to the last whole 256-row sweep, the rest
+ *   into sum (b mod 32, 0); each group of 8 as ((0 + 1) + (2 + 3)) + ((4 + 5) + (6 + 7)), then
+ *   the 32 groups in order).
  * parts: fp32 [nblocks, ld] device, ld >= N; out: fp32 [N].  N = 0 or nblocks = 0 writes
  * nothing / zeros respectively; negative sizes return CODA_ERR_SHAPE. */
 CODA_API int coda_col_reduce(const float* parts, int64_t nblocks, int64_t N, int64_t ld, float* out, void* stream);
